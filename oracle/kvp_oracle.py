@@ -1,0 +1,352 @@
+"""Oracle for pruned-KV decode: a plain, slow, obviously correct CPU reference.
+
+TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the
+benchmark's CPU-baseline leg may import this module. The library's GPU path
+never calls it and shares no code with it.
+
+Everything here is float64 numpy (bf16 inputs are widened exactly). The
+method is taken step by step from these pages:
+
+[DMS]     "Nvidia의 새로운 기술, 정확도 손실 없이 LLM 추론 비용을 8배 절감"
+          (euno.news rendering of a VentureBeat article on Dynamic Memory
+          Sparsification).
+[KVzap]   "NVIDIA가 AI 메모리 압축 신기술 KVzap 오픈소스 공개!" (max5.ai summary
+          of a MarkTechPost article).
+[DeInfer] gist.science summary of arXiv 2604.17709 (DeInfer), section
+          "2. 제안 방법 → 나. 페이지드 KV 캐시 및 CUDA Graph 통합".
+
+Steps and where they come from:
+
+1. score   [KVzap, 핵심 내용 정리 → "KVzap의 구조", "실제 적용"]: a surrogate
+           maps each token's hidden state to one score per KV head; either a
+           single linear layer or a 2-layer MLP.
+2. mask    [KVzap, "실제 적용"]: low-scoring entries are removed, the most
+           recent 128 tokens are always kept.
+           [DMS, "지연 삭제 (Delayed Eviction)"]: a token flagged for eviction
+           stays for a delay window, then is removed.
+3. compact [DeInfer, 나. → 준비 단계 / 그래프 재생 단계]: scan the logical
+           blocks, produce a remapping index list, copy the kept rows into a
+           compact buffer with fixed addresses (16-token pages here).
+4. attend  [DMS, "DMS 작동 방식" step 5 and "메모리의 미래"]: standard
+           attention over what is kept (single-query decode, GQA).
+
+Readings where the pages are silent (each is listed with its reason in the
+repository's design notes): scores are raw surrogate outputs compared to a
+per-(batch, kv-head) threshold tau, kept iff score >= tau; the window is the
+last ``window`` positions counted from ``now`` inclusive; an entry flagged at
+step f with delay d is present up to step f+d-1 and gone at f+d; GQA uses
+contiguous query-head groups; softmax scale is 1/sqrt(head_dim); an empty kept
+set gives a zero output; the MLP activation is the exact (erf) GELU and its
+hidden activations stay in full precision.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.special import erf
+
+NEVER = 2**31 - 1     # expire value of an entry that is kept forever
+PAGE = 16             # rows per page of the compacted cache
+WINDOW = 128          # [KVzap, "실제 적용"]: the most recent 128 tokens are always kept
+
+
+class CapacityError(RuntimeError):
+    """The compacted cache does not fit the page budget the caller gave."""
+
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64, exactly."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# 1. Scoring  [KVzap, 핵심 내용 정리 → "KVzap의 구조", "실제 적용"]
+# ---------------------------------------------------------------------------
+
+def score_linear(x_bits: np.ndarray, w: np.ndarray, bias: np.ndarray | None = None) -> np.ndarray:
+    """KVzap-Linear: s[t, h] = sum_k x[t, k] * W[h, k] + b[h].
+
+    x_bits: bf16 bits [n_tok, D]; w: float [H, D] (one row per KV head, the
+    layout of a linear layer's weight); bias: [H] or None. Returns float64
+    [n_tok, H].
+    """
+    x = widen_bf16(x_bits)
+    s = x @ np.asarray(w, dtype=np.float64).T
+    if bias is not None:
+        s = s + np.asarray(bias, dtype=np.float64)[None, :]
+    return s
+
+
+def gelu(u: np.ndarray) -> np.ndarray:
+    """Exact GELU: u * Phi(u) = u/2 * (1 + erf(u / sqrt 2))."""
+    return 0.5 * u * (1.0 + erf(u / math.sqrt(2.0)))
+
+
+def score_mlp(x_bits, w1_bits, w2_bits, b1=None, b2=None) -> np.ndarray:
+    """KVzap-MLP: s = GELU(x W1^T + b1) W2^T + b2, hidden kept in float64.
+
+    x_bits [n_tok, D], w1_bits [hidden, D], w2_bits [H, hidden], all bf16 bits.
+    """
+    x = widen_bf16(x_bits)
+    u = x @ widen_bf16(w1_bits).T
+    if b1 is not None:
+        u = u + np.asarray(b1, dtype=np.float64)[None, :]
+    z = gelu(u)
+    s = z @ widen_bf16(w2_bits).T
+    if b2 is not None:
+        s = s + np.asarray(b2, dtype=np.float64)[None, :]
+    return s
+
+
+# ---------------------------------------------------------------------------
+# 2. Masking  [KVzap, "실제 적용"]  [DMS, "지연 삭제 (Delayed Eviction)"]
+#
+# Each entry gets an "expire" step: the first decode step at which it is no
+# longer in the cache. At step `now` an entry is present iff now < expire.
+# ---------------------------------------------------------------------------
+
+def expire_kvzap(score, tau, pos, window: int = WINDOW):
+    """KVzap rule: an entry whose score is at least tau is kept for good;
+    otherwise it survives only while it is one of the last `window` positions,
+    i.e. while now < pos + window. NaN scores are treated as low."""
+    score = np.asarray(score)
+    pos = np.asarray(pos, dtype=np.int64)
+    keep_forever = score >= tau
+    return np.where(keep_forever, NEVER, pos + window).astype(np.int64)
+
+
+def expire_dms(flag_step, pos, delay: int, window: int = WINDOW):
+    """DMS rule with delayed eviction: an entry never flagged (flag_step < 0)
+    is kept; one flagged at step f is gone at step f + delay, but not before it
+    leaves the recent window (pos + window)."""
+    f = np.asarray(flag_step, dtype=np.int64)
+    pos = np.asarray(pos, dtype=np.int64)
+    return np.where(f < 0, NEVER, np.maximum(f + delay, pos + window)).astype(np.int64)
+
+
+def present(expire, now: int):
+    return np.asarray(now) < np.asarray(expire)
+
+
+def mask(expire_bht: np.ndarray, now: int):
+    """From expire [B, H, T] -> (keep bool [B,H,T], keep_bits uint32 [B,H,ceil(T/32)],
+    count int [B,H]). Bit i of word w stands for position 32*w + i."""
+    keep = present(expire_bht, now)
+    B, H, T = keep.shape
+    nw = (T + 31) // 32
+    bits = np.zeros((B, H, nw), dtype=np.uint64)
+    for i in range(32):
+        col = keep[:, :, i::32]
+        bits[:, :, : col.shape[2]] |= col.astype(np.uint64) << np.uint64(i)
+    return keep, bits.astype(np.uint32), keep.sum(axis=2).astype(np.int64)
+
+
+def mask_kvzap(scores_bth, tau_bh, now: int, window: int = WINDOW, pos0: int = 0):
+    """Scores laid out [B, T, H] (token-major, as the scorer emits them)."""
+    s = np.asarray(scores_bth)
+    B, T, H = s.shape
+    pos = pos0 + np.arange(T)
+    exp = expire_kvzap(s.transpose(0, 2, 1), np.asarray(tau_bh)[:, :, None], pos[None, None, :], window)
+    return (exp,) + mask(exp, now)
+
+
+def mask_dms(flag_step_bht, now: int, delay: int, window: int = WINDOW, pos0: int = 0):
+    f = np.asarray(flag_step_bht)
+    B, H, T = f.shape
+    pos = pos0 + np.arange(T)
+    exp = expire_dms(f, pos[None, None, :], delay, window)
+    return (exp,) + mask(exp, now)
+
+
+def threshold_at_quantile(scores_bth: np.ndarray, q: float) -> np.ndarray:
+    """Per-(b, h) threshold: the lower order statistic at index floor(q*(T-1))
+    of that head's T scores, rounded to float32 (the threshold is a float32
+    input of the masking step). A harness choice, not part of the method."""
+    s = np.sort(np.asarray(scores_bth, dtype=np.float64), axis=1)
+    T = s.shape[1]
+    return s[:, int(math.floor(q * (T - 1))), :].astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# 3. Compaction  [DeInfer, 나. 페이지드 KV 캐시 및 CUDA Graph 통합]
+#
+# Preparation: list the kept rows of every (b, h) in ascending position (the
+# remapping index list). Copy: gather those rows into 16-row pages of a
+# compact pool. Pages are handed out in (b-major, h-minor) order, each (b, h)
+# getting ceil((count + reserve) / 16) contiguous pages; `reserve` free slots
+# per (b, h) take later appends without moving anything.
+# ---------------------------------------------------------------------------
+
+class PagedCache:
+    """The compacted cache: pools [n_pages, 16, d] (bf16 bits), expire_pool
+    [n_pages, 16], page_table [B, H, max_pages] (-1 = unused), remap
+    [B, H, max_pages*16] (source position of slot j, -1 = unused), count [B, H]."""
+
+    def __init__(self, batch, n_kv_heads, head_dim, n_pages_cap, max_pages):
+        self.k_pool = np.zeros((n_pages_cap, PAGE, head_dim), dtype=np.uint16)
+        self.v_pool = np.zeros((n_pages_cap, PAGE, head_dim), dtype=np.uint16)
+        self.expire_pool = np.zeros((n_pages_cap, PAGE), dtype=np.int64)
+        self.page_table = np.full((batch, n_kv_heads, max_pages), -1, dtype=np.int64)
+        self.remap = np.full((batch, n_kv_heads, max_pages * PAGE), -1, dtype=np.int64)
+        self.count = np.zeros((batch, n_kv_heads), dtype=np.int64)
+        self.pages_used = 0
+
+    def slot_rows(self, b, h, slots):
+        """(page, row) of slots j of (b, h)."""
+        slots = np.asarray(slots, dtype=np.int64)
+        return self.page_table[b, h, slots // PAGE], slots % PAGE
+
+
+def _pages_for(n: int, reserve: int) -> int:
+    return (n + reserve + PAGE - 1) // PAGE
+
+
+def _fill(out: PagedCache, b, h, k_rows, v_rows, expire, positions, reserve):
+    n = len(positions)
+    npg = _pages_for(n, reserve)
+    if npg > out.page_table.shape[2] or out.pages_used + npg > out.k_pool.shape[0]:
+        raise CapacityError(f"(b={b}, h={h}) needs {npg} pages")
+    base = out.pages_used
+    out.page_table[b, h, :npg] = base + np.arange(npg)
+    j = np.arange(n)
+    out.k_pool[base + j // PAGE, j % PAGE] = k_rows
+    out.v_pool[base + j // PAGE, j % PAGE] = v_rows
+    out.expire_pool[base + j // PAGE, j % PAGE] = expire
+    out.remap[b, h, :n] = positions
+    out.count[b, h] = n
+    out.pages_used += npg
+
+
+def compact_dense(k_bits, v_bits, expire_bht, now, reserve, n_pages_cap, max_pages) -> PagedCache:
+    """Dense K/V [B, T, H, d] + expire [B, H, T] -> PagedCache of the entries
+    present at step `now`."""
+    B, T, H, d = k_bits.shape
+    out = PagedCache(B, H, d, n_pages_cap, max_pages)
+    for b in range(B):
+        for h in range(H):
+            pos = np.nonzero(present(expire_bht[b, h], now))[0]
+            _fill(out, b, h, k_bits[b, pos, h], v_bits[b, pos, h], expire_bht[b, h, pos], pos, reserve)
+    return out
+
+
+def compact_paged(src: PagedCache, now, reserve, n_pages_cap, max_pages) -> PagedCache:
+    """Re-compaction of an existing paged cache: keep the slots present at
+    `now`, in slot order, into a fresh set of pages."""
+    B, H, _ = src.page_table.shape
+    d = src.k_pool.shape[2]
+    out = PagedCache(B, H, d, n_pages_cap, max_pages)
+    for b in range(B):
+        for h in range(H):
+            slots = np.arange(src.count[b, h])
+            pg, row = src.slot_rows(b, h, slots)
+            e = src.expire_pool[pg, row]
+            sel = present(e, now)
+            pg, row = pg[sel], row[sel]
+            _fill(out, b, h, src.k_pool[pg, row], src.v_pool[pg, row], e[sel],
+                  src.remap[b, h, slots[sel]], reserve)
+    return out
+
+
+def append(cache: PagedCache, k_new_bits, v_new_bits, pos: int, expire_new):
+    """Decode step: the new token's k/v [B, H, d] go into slot count[b, h] of
+    its own (b, h) pages, with its expire step; raises if the reserve is used
+    up."""
+    B, H = cache.count.shape
+    for b in range(B):
+        for h in range(H):
+            j = int(cache.count[b, h])
+            p = j // PAGE
+            if p >= cache.page_table.shape[2] or cache.page_table[b, h, p] < 0:
+                raise CapacityError(f"(b={b}, h={h}) has no free slot")
+            page = cache.page_table[b, h, p]
+            cache.k_pool[page, j % PAGE] = k_new_bits[b, h]
+            cache.v_pool[page, j % PAGE] = v_new_bits[b, h]
+            cache.expire_pool[page, j % PAGE] = expire_new[b, h]
+            cache.remap[b, h, j] = pos
+            cache.count[b, h] = j + 1
+
+
+# ---------------------------------------------------------------------------
+# 4. Attention over the kept entries  [DMS, "DMS 작동 방식" step 5]
+# ---------------------------------------------------------------------------
+
+def _softmax_attend(q, K, V, scale):
+    """One query q [d] over rows K, V [n, d] (float64). Two-pass softmax."""
+    if K.shape[0] == 0:
+        return np.zeros(q.shape[0])
+    logits = (K @ q) * scale
+    m = logits.max()
+    w = np.exp(logits - m)
+    return (w @ V) / w.sum()
+
+
+def decode_attention(q_bits, cache: PagedCache, now: int, scale: float | None = None) -> np.ndarray:
+    """o[b, j] = softmax_i(q[b, j] . k_i * scale) v_i over the slots i of
+    (b, h = j // g) present at `now`; g = Hq / H. Returns float32 [B, Hq, d]."""
+    B, Hq, d = q_bits.shape
+    H = cache.count.shape[1]
+    g = Hq // H
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    q = widen_bf16(q_bits)
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        for h in range(H):
+            slots = np.arange(cache.count[b, h])
+            pg, row = cache.slot_rows(b, h, slots)
+            sel = present(cache.expire_pool[pg, row], now)
+            K = widen_bf16(cache.k_pool[pg[sel], row[sel]])
+            V = widen_bf16(cache.v_pool[pg[sel], row[sel]])
+            for j in range(h * g, (h + 1) * g):
+                out[b, j] = _softmax_attend(q[b, j], K, V, scale)
+    return out.astype(np.float32)
+
+
+def dense_attention(q_bits, k_bits, v_bits, now: int, scale=None, lo=None):
+    """Brute force over the dense cache [B, T, H, d]: every position in
+    [lo, now] (lo = 0 by default). No pages, no masks."""
+    B, Hq, d = q_bits.shape
+    H = k_bits.shape[2]
+    g = Hq // H
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    lo = 0 if lo is None else max(0, lo)
+    q = widen_bf16(q_bits)
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        for j in range(Hq):
+            h = j // g
+            out[b, j] = _softmax_attend(q[b, j], widen_bf16(k_bits[b, lo:now + 1, h]),
+                                        widen_bf16(v_bits[b, lo:now + 1, h]), scale)
+    return out.astype(np.float32)
+
+
+def window_attention(q_bits, k_bits, v_bits, now: int, window: int = WINDOW, scale=None):
+    """Sliding-window attention over the last `window` positions ending at now
+    ([DMS, "문제 완화를 위한 이전 시도" table, first row])."""
+    return dense_attention(q_bits, k_bits, v_bits, now, scale, lo=now - window + 1)
+
+
+# ---------------------------------------------------------------------------
+# Closed forms the pages quote
+# ---------------------------------------------------------------------------
+
+def kv_cache_bytes(n_layers: int, d_model: int, n_tokens: int, elem_bytes: int = 2) -> int:
+    """K and V, one d_model-wide row each per token per layer
+    ([KVzap, 이게 뭔데? / 핵심 내용 정리: Llama1-65B at 128k tokens])."""
+    return 2 * n_layers * d_model * n_tokens * elem_bytes
+
+
+def linear_projection_macs(d_model, n_q_heads, n_kv_heads, head_dim, ffn_hidden, gated=True) -> int:
+    """Per-token multiply-adds of a decoder layer's linear projections
+    (Q, K, V, O and the feed-forward block)."""
+    qo = 2 * d_model * n_q_heads * head_dim
+    kv = 2 * d_model * n_kv_heads * head_dim
+    ffn = (3 if gated else 2) * d_model * ffn_hidden
+    return qo + kv + ffn
+
+
+def scorer_macs(d_model, n_kv_heads, hidden=None) -> int:
+    """Per-token multiply-adds of the KVzap surrogate ([KVzap, "메모리 및 계산 효율"])."""
+    if hidden is None:
+        return d_model * n_kv_heads
+    return d_model * hidden + hidden * n_kv_heads

@@ -1,0 +1,417 @@
+"""Pins for the oracle: each check ties an oracle function to something other
+than itself (the pages' printed figures, hand-worked rule timelines, textbook
+values, closed forms, invariants, library routines, brute force). CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.stats import norm
+
+import kvp_synth as syn
+import oracle as orc
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def _exp_list(v):
+    return [orc.NEVER if e == "never" else e for e in v]
+
+
+def _bits(a):
+    return syn.f32_to_bf16_bits(np.asarray(a, dtype=np.float32))
+
+
+# --------------------------------------------------------------------------- score
+
+def test_widen_bf16_exact():
+    vals = np.array([0.0, 1.0, -2.5, 0.1015625, 3.0e38, -1.0e-38], dtype=np.float32)
+    b = _bits(vals)
+    back = orc.widen_bf16(b)
+    # bf16 keeps the top 16 bits of float32: exact for these, rounded otherwise
+    np.testing.assert_array_equal(back[:4], [0.0, 1.0, -2.5, 0.1015625])
+    assert orc.widen_bf16(np.array([0x3F80], np.uint16))[0] == 1.0
+    assert orc.widen_bf16(np.array([0xC000], np.uint16))[0] == -2.0
+
+
+def test_score_linear_unit_columns_pick_inputs():
+    # W[h] = e_{k_h}: head h must read exactly column k_h of x (catches a transposed W)
+    rng = np.random.default_rng(1)
+    n, D, H = 37, 48, 5
+    x = _bits(rng.standard_normal((n, D)))
+    ks = [3, 0, 47, 11, 11]
+    W = np.zeros((H, D), np.float32)
+    for h, k in enumerate(ks):
+        W[h, k] = 1.0
+    s = orc.score_linear(x, W)
+    xf = orc.widen_bf16(x)
+    for h, k in enumerate(ks):
+        np.testing.assert_array_equal(s[:, h], xf[:, k])
+
+
+def test_score_linear_bias_and_full_sum():
+    D, H = 64, 3
+    x = _bits(np.ones((4, D)))
+    W = np.tile(np.arange(D, dtype=np.float32), (H, 1)) * np.array([[1], [2], [-1]], np.float32)
+    s = orc.score_linear(x, W, bias=np.array([0.5, 0.0, -3.0]))
+    closed = D * (D - 1) / 2  # sum of 0..D-1: every term of the dot product counts
+    np.testing.assert_array_equal(s, np.tile([closed + 0.5, 2 * closed, -closed - 3.0], (4, 1)))
+    s0 = orc.score_linear(x, np.zeros((H, D), np.float32), bias=np.array([1.0, 2.0, 3.0]))
+    np.testing.assert_array_equal(s0, np.tile([1.0, 2.0, 3.0], (4, 1)))
+
+
+def test_gelu_matches_textbook_phi():
+    g = _gold("gelu_phi.json")
+    for p in g["points"]:
+        assert orc.gelu(np.array(p["u"])) == pytest.approx(p["u"] * p["phi"], abs=1e-15)
+    u = np.linspace(-8, 8, 1001)
+    np.testing.assert_allclose(orc.gelu(u), u * norm.cdf(u), rtol=0, atol=1e-14)
+    big = np.array([30.0, -30.0])
+    np.testing.assert_allclose(orc.gelu(big), [30.0, 0.0], atol=1e-12)
+
+
+def test_score_mlp_selection_weights():
+    # W1 row j reads x[:, k_j] scaled by c_j; W2 row h picks hidden unit j_h.
+    # Then s[:, h] = GELU(c_{j_h} x[:, k_{j_h}] + b1) + b2 exactly, checked with Phi.
+    rng = np.random.default_rng(2)
+    n, D, hid, H = 19, 32, 24, 3
+    x = _bits(rng.standard_normal((n, D)))
+    W1 = np.zeros((hid, D), np.float32)
+    ks = rng.integers(0, D, hid)
+    cs = np.array([0.5, 1.0, 2.0, -1.0] * (hid // 4), np.float32)
+    W1[np.arange(hid), ks] = cs
+    W2 = np.zeros((H, hid), np.float32)
+    js = [5, 0, 23]
+    for h, j in enumerate(js):
+        W2[h, j] = 1.0
+    b1 = np.linspace(-0.5, 0.5, hid)
+    b2 = np.array([0.25, 0.0, -1.0])
+    s = orc.score_mlp(x, _bits(W1), _bits(W2), b1=b1, b2=b2)
+    xf = orc.widen_bf16(x)
+    for h, j in enumerate(js):
+        u = cs[j] * xf[:, ks[j]] + b1[j]
+        np.testing.assert_allclose(s[:, h], u * norm.cdf(u) + b2[h], rtol=0, atol=1e-13)
+
+
+def test_score_mlp_sums_hidden_units():
+    # all hidden units equal: s = hidden * GELU(u) (catches a dropped hidden term)
+    D, hid = 16, 40
+    x = _bits(np.full((2, D), 0.25))
+    W1 = _bits(np.full((hid, D), 0.125))
+    W2 = _bits(np.ones((1, hid)))
+    s = orc.score_mlp(x, W1, W2)
+    u = D * 0.25 * 0.125
+    assert s[0, 0] == pytest.approx(hid * u * norm.cdf(u), abs=1e-13)
+
+
+# --------------------------------------------------------------------------- mask
+
+def test_kvzap_rule_worked_example():
+    g = _gold("mask_rules.json")["kvzap"]
+    s = np.array([np.nan if v == "nan" else v for v in g["scores"]], dtype=np.float32)
+    T = len(s)
+    exp, keep, bits, count = orc.mask_kvzap(s[None, :, None], np.array([[g["tau"]]], np.float32),
+                                            g["now"], window=g["window"])
+    assert list(exp[0, 0]) == _exp_list(g["expire"])
+    assert list(np.nonzero(keep[0, 0])[0]) == g["present"]
+    assert count[0, 0] == g["count"]
+    assert T == 10
+    e = _gold("mask_rules.json")["kvzap_early"]
+    _, keep, _, count = orc.mask_kvzap(np.array(e["scores"], np.float32)[None, :, None],
+                                       np.array([[e["tau"]]], np.float32), e["now"], window=e["window"])
+    assert list(np.nonzero(keep[0, 0])[0]) == e["present"] and count[0, 0] == e["count"]
+
+
+def test_dms_rule_worked_timeline():
+    g = _gold("mask_rules.json")["dms"]
+    f = np.array(g["flag_step"])[None, None, :]
+    T = f.shape[2]
+    for now_s, want in g["timeline"].items():
+        now = int(now_s)
+        exp, keep, _, _ = orc.mask_dms(f, now, delay=g["delay"], window=g["window"])
+        assert list(exp[0, 0]) == _exp_list(g["expire"])
+        have = [p for p in range(T) if p <= now and keep[0, 0, p]]
+        assert have == want, (now, have, want)
+
+
+@pytest.mark.parametrize("delay", [1, 129, 256, 300])
+def test_dms_delay_present_until_f_plus_d_minus_1(delay):
+    # flagged at its own step f (= position): present at f+d-1, gone at f+d when the
+    # delay outlasts the window; otherwise the window decides (gone at f+window)
+    W = 128
+    f = np.array([7, 500, 1000])
+    exp = orc.expire_dms(f, f, delay, W)
+    for fi, e in zip(f, exp):
+        gone = fi + max(delay, W)
+        assert e == gone
+        assert orc.present(e, gone - 1) and not orc.present(e, gone)
+    assert orc.expire_dms(np.array([-1]), np.array([3]), delay, W)[0] == orc.NEVER
+
+
+def test_mask_keep_all_and_window_only():
+    rng = np.random.default_rng(3)
+    B, T, H = 2, 700, 3
+    s = rng.standard_normal((B, T, H)).astype(np.float32)
+    now = T - 1
+    _, keep, bits, count = orc.mask_kvzap(s, np.full((B, H), -np.inf, np.float32), now)
+    assert (count == T).all() and keep.all()
+    _, keep, bits, count = orc.mask_kvzap(np.full((B, T, H), -np.inf, np.float32),
+                                          np.zeros((B, H), np.float32), now)
+    assert (count == 128).all()
+    assert keep[:, :, T - 128:].all() and not keep[:, :, : T - 128].any()
+    # fewer than 128 cached tokens: everything is in the window
+    _, _, _, count = orc.mask_kvzap(np.full((1, 50, 1), -np.inf, np.float32), np.zeros((1, 1), np.float32), 49)
+    assert count[0, 0] == 50
+
+
+def test_mask_monotone_in_tau_and_popcount():
+    rng = np.random.default_rng(4)
+    B, T, H = 2, 333, 4
+    s = rng.standard_normal((B, T, H)).astype(np.float32)
+    prev = None
+    for tau in [-3.0, -1.0, 0.0, 0.5, 2.0, 9.0]:
+        _, keep, bits, count = orc.mask_kvzap(s, np.full((B, H), tau, np.float32), T - 1)
+        pop = np.vectorize(lambda w: bin(int(w)).count("1"))(bits).sum(axis=2)
+        np.testing.assert_array_equal(pop, count)
+        # bit i of word w is position 32w+i
+        for p in [0, 31, 32, 100, T - 1]:
+            np.testing.assert_array_equal((bits[:, :, p // 32] >> (p % 32)) & 1, keep[:, :, p])
+        if prev is not None:
+            assert (count <= prev).all()
+        prev = count
+
+
+def test_threshold_quantile_prunes_expected_share():
+    rng = np.random.default_rng(5)
+    B, T, H = 1, 512, 2
+    s = rng.standard_normal((B, T, H))
+    for q in [0.5, 0.75]:
+        tau = orc.threshold_at_quantile(s, q)
+        above = (s.astype(np.float32) >= tau[:, None, :]).sum(axis=1)
+        # distinct scores: exactly T - floor(q (T-1)) are at or above the order statistic
+        assert (above == T - math.floor(q * (T - 1))).all()
+
+
+def test_dms_bernoulli_keep_rate():
+    # 8x compression: evict bit ~ Bernoulli(7/8) -> outside the delay band ~1/8 kept
+    B, H, T = 4, 8, 4096
+    ev = syn.bernoulli(0, syn.S_FLAG, (B, H, T), 7 / 8)
+    f = np.where(ev, np.arange(T)[None, None, :], -1)
+    now = T - 1
+    _, keep, _, count = orc.mask_dms(f, now, delay=256)
+    old = keep[:, :, : T - 256]
+    n = old.size
+    rate = old.mean()
+    assert abs(rate - 1 / 8) < 5 * math.sqrt(n * (1 / 8) * (7 / 8)) / n
+    assert keep[:, :, T - 256:].all()  # within the delay: everything still present
+
+
+# --------------------------------------------------------------------------- compact
+
+def _toy(B=2, T=300, H=3, d=16, seed=0):
+    k = syn.normal_bf16(seed, 5, (B, T, H, d))
+    v = syn.normal_bf16(seed, 6, (B, T, H, d))
+    return k, v
+
+
+def test_compact_rows_remap_pages():
+    B, T, H, d = 2, 300, 3, 16
+    k, v = _toy(B, T, H, d)
+    rng = np.random.default_rng(6)
+    s = rng.standard_normal((B, T, H)).astype(np.float32)
+    tau = np.full((B, H), 0.3, np.float32)
+    now = T - 1
+    exp, keep, _, count = orc.mask_kvzap(s, tau, now)
+    reserve = 5
+    maxp = (T + reserve + 15) // 16
+    c = orc.compact_dense(k, v, exp, now, reserve, n_pages_cap=B * H * maxp, max_pages=maxp)
+    base = 0
+    for b in range(B):
+        for h in range(H):
+            n = int(count[b, h])
+            assert c.count[b, h] == n
+            r = c.remap[b, h, :n]
+            assert (np.diff(r) > 0).all() and (c.remap[b, h, n:] == -1).all()
+            np.testing.assert_array_equal(r, np.nonzero(keep[b, h])[0])
+            npg = (n + reserve + 15) // 16
+            np.testing.assert_array_equal(c.page_table[b, h, :npg], base + np.arange(npg))
+            assert (c.page_table[b, h, npg:] == -1).all()
+            for j in [0, n // 2, n - 1]:
+                pg, row = c.page_table[b, h, j // 16], j % 16
+                np.testing.assert_array_equal(c.k_pool[pg, row], k[b, r[j], h])
+                np.testing.assert_array_equal(c.v_pool[pg, row], v[b, r[j], h])
+                assert c.expire_pool[pg, row] == exp[b, h, r[j]]
+            # unused rows of the last pages are zero, expire 0 (never present)
+            for j in range(n, npg * 16):
+                pg, row = c.page_table[b, h, j // 16], j % 16
+                assert c.expire_pool[pg, row] == 0 and not c.k_pool[pg, row].any()
+            base += npg
+    assert c.pages_used == base
+
+
+def test_compact_keep_all_is_identity():
+    B, T, H, d = 1, 64, 2, 8
+    k, v = _toy(B, T, H, d)
+    exp = np.full((B, H, T), orc.NEVER)
+    c = orc.compact_dense(k, v, exp, T - 1, 0, n_pages_cap=8, max_pages=4)
+    for h in range(H):
+        np.testing.assert_array_equal(c.remap[h * 0, h, :T], np.arange(T))
+        rows = c.k_pool[c.page_table[0, h, :4]].reshape(T, d)
+        np.testing.assert_array_equal(rows, k[0, :, h])
+
+
+def test_compact_capacity_error():
+    k, v = _toy(1, 64, 1, 8)
+    exp = np.full((1, 1, 64), orc.NEVER)
+    with pytest.raises(orc.CapacityError):
+        orc.compact_dense(k, v, exp, 63, 0, n_pages_cap=3, max_pages=8)
+    with pytest.raises(orc.CapacityError):
+        orc.compact_dense(k, v, exp, 63, 1, n_pages_cap=10, max_pages=4)
+
+
+def test_paged_recompaction_equals_dense_on_same_set():
+    # prefill compaction at step 60, then appends of positions 61..120, then a
+    # paged re-compaction at 120 == one dense compaction of positions 0..120 at 120
+    B, T, H, d = 2, 121, 2, 16
+    k, v = _toy(B, T, H, d)
+    pos = np.arange(T)[None, None, :]
+    f = np.where(syn.bernoulli(1, 8, (B, H, T), 0.875), pos, -1)
+    exp = orc.expire_dms(f, pos, delay=40, window=16)
+    c1 = orc.compact_dense(k[:, :61], v[:, :61], exp[:, :, :61], 60, reserve=64, n_pages_cap=200, max_pages=20)
+    for t in range(61, T):
+        orc.append(c1, k[:, t], v[:, t], t, exp[:, :, t])
+    c2 = orc.compact_paged(c1, T - 1, reserve=3, n_pages_cap=200, max_pages=20)
+    ref = orc.compact_dense(k, v, exp, T - 1, reserve=3, n_pages_cap=200, max_pages=20)
+    for name in ["k_pool", "v_pool", "expire_pool", "page_table", "remap", "count", "pages_used"]:
+        np.testing.assert_array_equal(getattr(c2, name), getattr(ref, name), err_msg=name)
+
+
+def test_append_fills_reserved_slots():
+    B, T, H, d = 1, 40, 2, 8
+    k, v = _toy(B, T, H, d)
+    exp = np.full((B, H, T), orc.NEVER)
+    exp[0, 1, :10] = 5
+    c = orc.compact_dense(k, v, exp, T - 1, reserve=2, n_pages_cap=20, max_pages=4)
+    kn = syn.normal_bf16(3, 1, (B, H, d))
+    vn = syn.normal_bf16(3, 2, (B, H, d))
+    orc.append(c, kn, vn, T, np.array([[orc.NEVER, 77]]))
+    assert list(c.count[0]) == [41, 31]
+    pg, row = c.slot_rows(0, 1, [30])
+    np.testing.assert_array_equal(c.k_pool[pg[0], row[0]], kn[0, 1])
+    assert c.expire_pool[pg[0], row[0]] == 77 and c.remap[0, 1, 30] == T
+    orc.append(c, kn, vn, T + 1, np.full((1, 2), orc.NEVER))
+    with pytest.raises(orc.CapacityError):  # head 0: 40 + 2 reserve = 42 = 3 pages -> 48 slots
+        for i in range(10):
+            orc.append(c, kn, vn, T + 2 + i, np.full((1, 2), orc.NEVER))
+
+
+# --------------------------------------------------------------------------- attention
+
+def _sdpa_ref(q_bits, k_bits, v_bits, allowed, scale=None):
+    """torch's scaled_dot_product_attention in float64 with a boolean mask over
+    the dense cache [B, T, H, d]; an independent library routine."""
+    q = torch.from_numpy(orc.widen_bf16(q_bits))          # [B, Hq, d]
+    K = torch.from_numpy(orc.widen_bf16(k_bits))          # [B, T, H, d]
+    V = torch.from_numpy(orc.widen_bf16(v_bits))
+    B, Hq, d = q.shape
+    H = K.shape[2]
+    g = Hq // H
+    K = K.permute(0, 2, 1, 3).repeat_interleave(g, dim=1)  # [B, Hq, T, d]
+    V = V.permute(0, 2, 1, 3).repeat_interleave(g, dim=1)
+    m = torch.from_numpy(np.asarray(allowed)).repeat_interleave(g, dim=1)[:, :, None, :]  # [B,Hq,1,T]
+    o = torch.nn.functional.scaled_dot_product_attention(q[:, :, None, :], K, V, attn_mask=m, scale=scale)
+    return o[:, :, 0, :].numpy()
+
+
+def test_dense_attention_matches_library_sdpa():
+    B, T, H, Hq, d = 2, 90, 2, 6, 32
+    k, v = _toy(B, T, H, d)
+    q = syn.normal_bf16(0, 7, (B, Hq, d))
+    now = T - 1
+    o = orc.dense_attention(q, k, v, now)
+    ref = _sdpa_ref(q, k, v, np.ones((B, H, T), bool))
+    np.testing.assert_allclose(o, ref, rtol=1e-6, atol=1e-7)
+    ow = orc.window_attention(q, k, v, now, window=20)
+    allowed = np.zeros((B, H, T), bool)
+    allowed[:, :, T - 20:] = True
+    np.testing.assert_allclose(ow, _sdpa_ref(q, k, v, allowed), rtol=1e-6, atol=1e-7)
+
+
+def test_decode_attention_equals_masked_sdpa():
+    # paged pruned attention == library attention over the dense cache with the
+    # rule's presence mask (catches any page/slot/remap/GQA indexing slip)
+    B, T, H, Hq, d = 2, 333, 2, 8, 64
+    k, v = _toy(B, T, H, d)
+    q = syn.normal_bf16(0, 7, (B, Hq, d))
+    rng = np.random.default_rng(8)
+    s = rng.standard_normal((B, T, H)).astype(np.float32)
+    now = T - 1
+    exp, keep, _, _ = orc.mask_kvzap(s, np.full((B, H), 0.6, np.float32), now)
+    c = orc.compact_dense(k, v, exp, now, 7, n_pages_cap=100, max_pages=30)
+    o = orc.decode_attention(q, c, now)
+    np.testing.assert_allclose(o, _sdpa_ref(q, k, v, keep), rtol=1e-6, atol=1e-7)
+
+
+def test_decode_attention_special_cases():
+    B, T, H, Hq, d = 1, 400, 2, 4, 64
+    k, v = _toy(B, T, H, d)
+    q = syn.normal_bf16(0, 7, (B, Hq, d))
+    now = T - 1
+    cap = dict(n_pages_cap=100, max_pages=30)
+    # keep-all threshold -> dense attention
+    exp, *_ = orc.mask_kvzap(np.zeros((B, T, H), np.float32), np.full((B, H), -np.inf, np.float32), now)
+    c = orc.compact_dense(k, v, exp, now, 0, **cap)
+    np.testing.assert_allclose(orc.decode_attention(q, c, now), orc.dense_attention(q, k, v, now), rtol=1e-6, atol=1e-7)
+    # score -inf everywhere -> last-128 sliding window attention
+    exp, *_ = orc.mask_kvzap(np.full((B, T, H), -np.inf, np.float32), np.zeros((B, H), np.float32), now)
+    c = orc.compact_dense(k, v, exp, now, 0, **cap)
+    np.testing.assert_allclose(orc.decode_attention(q, c, now), orc.window_attention(q, k, v, now), rtol=1e-6, atol=1e-7)
+    # q = 0 -> mean of the kept V rows (closed form)
+    q0 = np.zeros_like(q)
+    o = orc.decode_attention(q0, c, now)
+    vm = orc.widen_bf16(v[0, T - 128:, :, :]).mean(axis=0)  # [H, d]
+    np.testing.assert_allclose(o[0], np.repeat(vm, Hq // H, axis=0), rtol=1e-6, atol=1e-7)
+
+
+def test_decode_attention_dominant_key_and_empty():
+    d = 16
+    k = np.zeros((1, 8, 1, d), np.uint16)
+    v = syn.normal_bf16(0, 6, (1, 8, 1, d))
+    kf = np.zeros((1, 8, 1, d), np.float32)
+    kf[0, 5, 0, 0] = 256.0  # logit 256*q0*scale = 60 above the others
+    k = _bits(kf)
+    q = _bits(np.concatenate([[60 * 4.0 / 256.0], np.zeros(d - 1)]).reshape(1, 1, d))
+    exp = np.full((1, 1, 8), orc.NEVER)
+    c = orc.compact_dense(k, v, exp, 7, 0, n_pages_cap=2, max_pages=2)
+    o = orc.decode_attention(q, c, 7)
+    np.testing.assert_allclose(o[0, 0], orc.widen_bf16(v[0, 5, 0]), rtol=0, atol=1e-20 + 1e-24)
+    # nothing present -> zero output
+    exp0 = np.zeros((1, 1, 8), np.int64)
+    c0 = orc.compact_dense(k, v, exp0, 7, 0, n_pages_cap=2, max_pages=2)
+    assert c0.count[0, 0] == 0 and (orc.decode_attention(q, c0, 7) == 0).all()
+
+
+# --------------------------------------------------------------------------- closed forms
+
+def test_kv_cache_size_matches_page():
+    g = _gold("kv_cache_size.json")
+    nb = orc.kv_cache_bytes(g["n_layers"], g["d_model"], g["n_tokens"], g["elem_bytes"])
+    # 335.54e9 bytes: the page prints the integer part of the decimal-GB figure
+    assert 0 <= nb / 1e9 - g["printed_total_gb"] < g["printed_precision_gb"]
+
+
+def test_scorer_overhead_matches_page():
+    g = _gold("scorer_overhead.json")
+    m = g["model"]
+    proj = orc.linear_projection_macs(m["d_model"], m["n_q_heads"], m["n_kv_heads"], m["head_dim"], m["ffn_hidden"])
+    lin = 100.0 * orc.scorer_macs(m["d_model"], m["n_kv_heads"]) / proj
+    mlp = 100.0 * orc.scorer_macs(m["d_model"], m["n_kv_heads"], g["mlp_hidden_reading"]) / proj
+    assert round(lin, g["linear_printed_digits"]) == g["linear_percent"]
+    assert round(mlp, g["mlp_printed_digits"]) == g["mlp_percent"]
