@@ -1,0 +1,254 @@
+/*
+ * kvp.h - C ABI of libkvp, KV-cache pruning at decode time on one GB300
+ * (sm_103a).
+ *
+ * The path, step by step, and the pages that define it:
+ *
+ *   kvp_score        "NVIDIA가 AI 메모리 압축 신기술 KVzap 오픈소스 공개!" (KVzap
+ *                    summary), 핵심 내용 정리 -> "KVzap의 구조", "실제 적용": a
+ *                    small surrogate (one linear layer, or a 2-layer MLP) maps
+ *                    each token's hidden state to one score per KV head.
+ *   kvp_mask         same page, "실제 적용": low-scoring entries are removed,
+ *                    the most recent 128 tokens are always kept; and
+ *                    "Nvidia의 새로운 기술, 정확도 손실 없이 LLM 추론 비용을 8배
+ *                    절감" (DMS article), "지연 삭제 (Delayed Eviction)": a token
+ *                    flagged for eviction stays for a delay window first.
+ *   kvp_compact      DeInfer summary (gist.science, arXiv 2604.17709), "나.
+ *                    페이지드 KV 캐시 및 CUDA Graph 통합": a preparation pass
+ *                    builds a remapping index list, a copy pass gathers the
+ *                    kept rows into a compact buffer with fixed addresses.
+ *   kvp_append       the decode-time side of the same rules: the new token is
+ *                    scored once and written into a reserved slot.
+ *   kvp_decode_attn  DMS article, "DMS 작동 방식" step 5: standard attention
+ *                    over what is kept; here split-KV single-query GQA decode.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named in a comment as "device" are CUDA device addresses
+ *     (any allocator; torch tensors work). The library never allocates,
+ *     frees or keeps a device buffer: the caller owns every buffer,
+ *     including workspace (size from the matching *_workspace_bytes call).
+ *   - Every call is asynchronous and ordered on `stream` (a cudaStream_t,
+ *     NULL = legacy default stream). Nothing synchronises the host.
+ *   - Host-side argument checks return a status at once and launch nothing.
+ *   - Errors found on the device (page budget exhausted, a bounded wait that
+ *     gave up) are recorded in `status`, a device int32 the caller zeroes:
+ *     kernels only ever replace a 0 there with a nonzero kvp_status code, so
+ *     it holds the first error. Outputs of a call that recorded an error are
+ *     unspecified. `status` may be NULL where a call cannot fail on device.
+ *   - bf16 means IEEE-754 binary32 truncated to its top 16 bits (the
+ *     `__nv_bfloat16` / torch.bfloat16 format). Rows are 16-byte aligned.
+ *   - Positions count tokens from 0; `now` is the position of the token being
+ *     decoded, whose own K/V is already in the cache.
+ */
+#ifndef KVP_H
+#define KVP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVP_API __attribute__((visibility("default")))
+#else
+#define KVP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvp_status {
+  KVP_OK = 0,
+  KVP_ERR_INVALID = 1,      /* null pointer, negative size, inconsistent shapes */
+  KVP_ERR_ALIGN = 2,        /* a pointer or stride breaks the 16-byte rule */
+  KVP_ERR_CAPACITY = 3,     /* page pool, page table or reserve too small (device) */
+  KVP_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  KVP_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (device) */
+  KVP_ERR_UNSUPPORTED = 6,  /* shape outside what the kernels handle */
+  KVP_ERR_WORKSPACE = 7,    /* workspace pointer NULL or smaller than required */
+  KVP_ERR_BOUNDS = 8        /* a page id or count read on the device is out of range (device);
+                               the access is skipped, never performed */
+} kvp_status;
+
+enum { KVP_SCORER_LINEAR = 0, KVP_SCORER_MLP = 1 };
+enum { KVP_MASK_KVZAP = 0, KVP_MASK_DMS = 1 };
+
+#define KVP_PAGE_TOKENS 16            /* rows per page of the compacted cache */
+#define KVP_WINDOW_DEFAULT 128        /* KVzap: the last 128 tokens are always kept */
+#define KVP_EXPIRE_NEVER 2147483647   /* expire value of an entry kept for good */
+
+/* Human-readable name of a status code (static string). */
+KVP_API const char* kvp_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+KVP_API int kvp_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* kvp_score - KVzap surrogate scores (KVzap summary, "KVzap의 구조",
+ * "실제 적용").
+ *
+ *   LINEAR: scores[t, h] = sum_k x[t, k] * w[h, k] + b[h]
+ *   MLP:    scores[t, h] = sum_j GELU(sum_k x[t, k] * w[j, k] + b[j]) * w2[h, j] + b2[h]
+ *           with the exact (erf) GELU and the hidden activations in fp32.
+ *
+ * n_tok      rows of x (any >= 0; 0 is a no-op)
+ * d_model    D, a multiple of 8, <= 65536
+ * n_kv_heads H, 1..64
+ * hidden     MLP hidden width, a multiple of 256 (ignored for LINEAR)
+ * x          device bf16 [n_tok, D], row stride ld_x elements (multiple of 8,
+ *            >= D), base 16-byte aligned
+ * w          LINEAR: device fp32 [H, D] (a linear layer's weight layout)
+ *            MLP:    device bf16 W1 [hidden, D]
+ * b          LINEAR: device fp32 [H] or NULL;  MLP: device fp32 b1 [hidden] or NULL
+ * w2         MLP: device bf16 [H, hidden];  LINEAR: must be NULL
+ * b2         MLP: device fp32 [H] or NULL;  LINEAR: must be NULL
+ * scores     device fp32 [n_tok, H] (output, token-major)
+ * workspace  device, >= kvp_score_workspace_bytes(...) bytes, 256-byte aligned
+ *
+ * The dense contraction runs on the tcgen05 tensor cores: LINEAR splits the
+ * fp32 weight into two bf16 halves (hi + lo) so that the products keep ~16
+ * mantissa bits of w; accumulation is fp32 throughout.
+ */
+KVP_API size_t kvp_score_workspace_bytes(int scorer, int64_t n_tok, int d_model, int n_kv_heads, int hidden);
+KVP_API kvp_status kvp_score(int scorer, int64_t n_tok, int d_model, int n_kv_heads, int hidden,
+                     const void* x, int64_t ld_x, const void* w, const float* b,
+                     const void* w2, const float* b2, float* scores,
+                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* kvp_mask - keep/evict decision per (batch, kv head, position) (KVzap
+ * summary "실제 적용"; DMS article "지연 삭제").
+ *
+ * Each entry gets expire = the first step at which it is no longer cached:
+ *   KVZAP: expire = (score >= tau[b,h]) ? KVP_EXPIRE_NEVER : pos + window
+ *          (NaN scores count as low)
+ *   DMS:   expire = (flag_step < 0) ? KVP_EXPIRE_NEVER
+ *                                   : max(flag_step + delay, pos + window)
+ * and is present at step `now` iff now < expire. pos = pos0 + index.
+ *
+ * mode       KVP_MASK_KVZAP or KVP_MASK_DMS
+ * scores     KVZAP: device fp32 [B, n_pos, H] (kvp_score output with
+ *            n_tok = B*n_pos);  DMS: NULL
+ * tau        KVZAP: device fp32 [B, H];  DMS: NULL
+ * flag_step  DMS: device int32 [B, H, n_pos], -1 = never flagged; KVZAP: NULL
+ * window     >= 0 (KVP_WINDOW_DEFAULT = 128);  delay >= 0 (DMS)
+ * expire     device int32 [B, H, n_pos] (output, required)
+ * keep_bits  device uint32 [B, H, ceil(n_pos/32)] (output or NULL); bit i of
+ *            word w is position index 32*w + i; bits past n_pos are 0
+ * count      device int32 [B, H] (output or NULL): present entries
+ */
+KVP_API kvp_status kvp_mask(int mode, int batch, int n_kv_heads, int n_pos, int pos0,
+                    const float* scores, const float* tau, const int32_t* flag_step,
+                    int window, int delay, int now,
+                    int32_t* expire, uint32_t* keep_bits, int32_t* count, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* kvp_compact - gather the entries present at `now` into 16-row pages
+ * (DeInfer summary, "나. 페이지드 KV 캐시 및 CUDA Graph 통합": remapping index
+ * list, then a copy into a compact fixed-address buffer).
+ *
+ * For every (b, h), in b-major then h-minor order, the present positions are
+ * taken in ascending order; (b, h) receives n = ceil((count + reserve) / 16)
+ * consecutive pages starting right after the previous (b, h)'s pages. Slot j
+ * of (b, h) is row j % 16 of page page_table[b, h, j / 16].
+ *
+ * Source (dense): k_src, v_src device bf16, element (b, t, h, e) at
+ *   b*stride_b + t*stride_t + h*stride_h + e (strides in elements, multiples
+ *   of 8; e contiguous), t in [0, n_pos).
+ * expire     device int32 [B, H, n_pos] (kvp_mask output)
+ * reserve    free slots kept after the survivors of each (b, h) for kvp_append
+ * Outputs (all device):
+ *   k_pool, v_pool   bf16 [n_pages_cap, 16, head_dim]; rows past count in a
+ *                    (b, h)'s last page are zero
+ *   expire_pool      int32 [n_pages_cap, 16]; the entry's expire, 0 in unused rows
+ *   page_table       int32 [B, H, max_pages]; page ids, -1 past the (b, h)'s pages
+ *   remap            int32 [B, H, max_pages*16]; source position of slot j, -1
+ *                    past count
+ *   count            int32 [B, H]
+ * A budget overflow records KVP_ERR_CAPACITY in `status` (required).
+ * head_dim is 64 or 128.
+ */
+KVP_API size_t kvp_compact_workspace_bytes(int batch, int n_kv_heads, int n_pos);
+KVP_API kvp_status kvp_compact(int batch, int n_kv_heads, int head_dim, int n_pos,
+                       const void* k_src, const void* v_src,
+                       int64_t stride_b, int64_t stride_t, int64_t stride_h,
+                       const int32_t* expire, int now, int reserve,
+                       void* k_pool, void* v_pool, int32_t* expire_pool, int n_pages_cap,
+                       int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                       void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* kvp_compact_paged - the same compaction with a paged cache (as written by
+ * kvp_compact / kvp_append) as the source: slots j < src_count[b, h] whose
+ * expire_pool entry is present at `now` are kept, in slot order, and carry
+ * their remap position and expire value over. Source and destination must
+ * not overlap (use two pools and swap them). A source page id outside
+ * [0, src_n_pages_cap) records KVP_ERR_BOUNDS and its slots count as absent.
+ */
+KVP_API size_t kvp_compact_paged_workspace_bytes(int batch, int n_kv_heads, int src_max_pages);
+KVP_API kvp_status kvp_compact_paged(int batch, int n_kv_heads, int head_dim,
+                             const void* src_k_pool, const void* src_v_pool,
+                             const int32_t* src_expire_pool, int src_n_pages_cap,
+                             const int32_t* src_page_table,
+                             int src_max_pages, const int32_t* src_remap, const int32_t* src_count,
+                             int now, int reserve,
+                             void* k_pool, void* v_pool, int32_t* expire_pool, int n_pages_cap,
+                             int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                             void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* kvp_append - decode step: write the new token (position `pos`) of every
+ * (b, h) into slot count[b, h], with its expire value from the same rules as
+ * kvp_mask (KVZAP: score[b, h] vs tau[b, h]; DMS: flag_step[b, h]), then
+ * increment count. A (b, h) with no free slot left records
+ * KVP_ERR_CAPACITY in `status` (required) and is left unchanged.
+ *
+ * k_new, v_new  device bf16 [B, H, head_dim]
+ * score, tau    KVZAP: device fp32 [B, H] each;  DMS: NULL
+ * flag_step     DMS: device int32 [B, H];  KVZAP: NULL
+ * pools (n_pages_cap pages), page_table, remap, count: as written by
+ *               kvp_compact; a page id outside [0, n_pages_cap) records
+ *               KVP_ERR_BOUNDS and nothing is written for that (b, h).
+ */
+KVP_API kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_dim, int pos,
+                      const void* k_new, const void* v_new,
+                      const float* score, const float* tau, const int32_t* flag_step,
+                      int window, int delay,
+                      void* k_pool, void* v_pool, int32_t* expire_pool, int n_pages_cap,
+                      const int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                      int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* kvp_decode_attn - single-query attention over the kept entries (DMS
+ * article, "DMS 작동 방식" step 5: standard attention kernels on the pruned
+ * cache).
+ *
+ *   out[b, j] = sum_i softmax_i(scale * q[b, j] . k_i) v_i
+ *
+ * over the slots i < count[b, h] of kv head h = j / (Hq / H) whose expire is
+ * greater than `now`. An empty set gives a zero row.
+ *
+ * q          device bf16 [B, Hq, head_dim];  Hq a multiple of H, Hq/H in {1,2,4,8}
+ * pools (n_pages_cap pages), expire_pool, page_table (width max_pages), count:
+ *            as kvp_compact writes them. count is clamped to max_pages*16; a
+ *            page id outside [0, n_pages_cap) records KVP_ERR_BOUNDS in
+ *            `status` (may be NULL) and that page counts as empty.
+ * scale      > 0, or 0 for 1/sqrt(head_dim)
+ * out        device fp32 [B, Hq, head_dim]
+ * pages_per_split  pages one CTA reads (0 = 16); the work is split along the
+ *            pages and the partial softmax states are merged in fp32.
+ * workspace  device, >= kvp_decode_attn_workspace_bytes(...)
+ */
+KVP_API size_t kvp_decode_attn_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                       int max_pages, int pages_per_split);
+KVP_API kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                           const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* expire_pool, int n_pages_cap,
+                           const int32_t* page_table, int max_pages,
+                           const int32_t* count, int now, float scale, float* out,
+                           int pages_per_split, void* workspace, size_t workspace_bytes,
+                           int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVP_H */

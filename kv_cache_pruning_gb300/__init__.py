@@ -1,0 +1,321 @@
+"""Python binding of libkvp (KV-cache pruning at decode time, sm_103a).
+
+Each function here has the name of the C entry point it calls (see
+include/kvp.h) and only marshals arguments: torch tensors are checked for
+dtype, device and contiguity, their device pointers and sizes are passed on,
+and a non-OK status raises KvpError. Every step of the path runs in the
+library's CUDA kernels; there is no other implementation to fall back on, so
+importing this package fails loudly when libkvp.so has not been built.
+
+PyTorch is used for device memory and streams only: calls are enqueued on
+torch's current CUDA stream unless a stream is passed.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvp.so")
+
+KVP_OK = 0
+KVP_ERR_INVALID = 1
+KVP_ERR_ALIGN = 2
+KVP_ERR_CAPACITY = 3
+KVP_ERR_CUDA = 4
+KVP_ERR_TIMEOUT = 5
+KVP_ERR_UNSUPPORTED = 6
+KVP_ERR_WORKSPACE = 7
+KVP_ERR_BOUNDS = 8
+
+KVP_SCORER_LINEAR = 0
+KVP_SCORER_MLP = 1
+KVP_MASK_KVZAP = 0
+KVP_MASK_DMS = 1
+PAGE = 16
+WINDOW = 128
+EXPIRE_NEVER = 2**31 - 1
+
+
+class KvpError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn}: {status_string(code)} (status {code})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libkvp.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    return ctypes.CDLL(LIB_PATH)
+
+
+_lib = _load()
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_int64
+_S = ctypes.c_size_t
+_F = ctypes.c_float
+
+_SIGS = {
+    "kvp_status_string": (ctypes.c_char_p, [_I]),
+    "kvp_version": (_I, []),
+    "kvp_score_workspace_bytes": (_S, [_I, _L, _I, _I, _I]),
+    "kvp_score": (_I, [_I, _L, _I, _I, _I, _P, _L, _P, _P, _P, _P, _P, _P, _S, _P, _P]),
+    "kvp_mask": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "kvp_compact_workspace_bytes": (_S, [_I, _I, _I]),
+    "kvp_compact": (_I, [_I, _I, _I, _I, _P, _P, _L, _L, _L, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
+                         _P, _S, _P, _P]),
+    "kvp_compact_paged_workspace_bytes": (_S, [_I, _I, _I]),
+    "kvp_compact_paged": (_I, [_I, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I,
+                               _P, _P, _P, _S, _P, _P]),
+    "kvp_append": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
+                        _P, _P]),
+    "kvp_decode_attn_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
+    "kvp_decode_attn": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _I, _P, _S, _P, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def library():
+    """The loaded ctypes handle of libkvp.so."""
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return _lib.kvp_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return _lib.kvp_version()
+
+
+# --------------------------------------------------------------------------- marshalling helpers
+
+def _ptr(t, dtype=None, name="tensor", optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, code: int):
+    if code != KVP_OK:
+        raise KvpError(fn, code)
+
+
+def _ws(nbytes: int, device, workspace=None):
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+# --------------------------------------------------------------------------- score
+
+def kvp_score_workspace_bytes(scorer, n_tok, d_model, n_kv_heads, hidden=0) -> int:
+    return _lib.kvp_score_workspace_bytes(scorer, n_tok, d_model, n_kv_heads, hidden)
+
+
+def kvp_score(x, w, b=None, w2=None, b2=None, *, scorer=KVP_SCORER_LINEAR, out=None, workspace=None,
+              status=None, stream=None):
+    """scores[n_tok, H] from hidden states x[n_tok, D] (bf16).
+
+    LINEAR: w fp32 [H, D], b fp32 [H] or None.
+    MLP:    w bf16 W1 [hidden, D], b fp32 b1 [hidden] or None, w2 bf16 [H, hidden], b2 fp32 [H] or None.
+    """
+    if x.dim() != 2:
+        raise ValueError("x must be [n_tok, D]")
+    n_tok, D = x.shape
+    if x.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    if scorer == KVP_SCORER_LINEAR:
+        H, hidden = w.shape[0], 0
+        wp = _ptr(w, torch.float32, "w")
+    else:
+        hidden, H = w.shape[0], w2.shape[0]
+        wp = _ptr(w, torch.bfloat16, "w1")
+    if out is None:
+        out = torch.empty((n_tok, H), dtype=torch.float32, device=x.device)
+    need = kvp_score_workspace_bytes(scorer, n_tok, D, H, hidden)
+    ws = _ws(need, x.device, workspace)
+    code = _lib.kvp_score(scorer, n_tok, D, H, hidden, x.data_ptr(), x.stride(0), wp,
+                          _ptr(b, torch.float32, "b", True),
+                          _ptr(w2, torch.bfloat16, "w2", True), _ptr(b2, torch.float32, "b2", True),
+                          _ptr(out, torch.float32, "out"), ws.data_ptr(), ws.numel() * ws.element_size(),
+                          _ptr(status, torch.int32, "status", True), _stream(stream))
+    _check("kvp_score", code)
+    return out
+
+
+# --------------------------------------------------------------------------- mask
+
+def kvp_mask(*, mode, batch, n_kv_heads, n_pos, now, scores=None, tau=None, flag_step=None, window=WINDOW,
+             delay=0, pos0=0, expire=None, keep_bits=None, count=None, want_bits=True, stream=None):
+    """expire [B, H, n_pos] (+ keep_bits, count) from KVzap scores [B, n_pos, H] and tau [B, H], or from
+    DMS flag steps [B, H, n_pos]."""
+    dev = (scores if scores is not None else flag_step).device
+    if expire is None:
+        expire = torch.empty((batch, n_kv_heads, n_pos), dtype=torch.int32, device=dev)
+    if want_bits and keep_bits is None:
+        keep_bits = torch.empty((batch, n_kv_heads, (n_pos + 31) // 32), dtype=torch.int32, device=dev)
+    if count is None:
+        count = torch.empty((batch, n_kv_heads), dtype=torch.int32, device=dev)
+    code = _lib.kvp_mask(mode, batch, n_kv_heads, n_pos, pos0, _ptr(scores, torch.float32, "scores", True),
+                         _ptr(tau, torch.float32, "tau", True), _ptr(flag_step, torch.int32, "flag_step", True),
+                         window, delay, now, _ptr(expire, torch.int32, "expire"),
+                         _ptr(keep_bits, torch.int32, "keep_bits", True), _ptr(count, torch.int32, "count"),
+                         _stream(stream))
+    _check("kvp_mask", code)
+    return expire, keep_bits, count
+
+
+# --------------------------------------------------------------------------- paged cache
+
+@dataclass
+class PagedKV:
+    """Device buffers of one compacted cache (allocated with torch)."""
+    k_pool: torch.Tensor        # bf16 [n_pages_cap, 16, d]
+    v_pool: torch.Tensor        # bf16 [n_pages_cap, 16, d]
+    expire_pool: torch.Tensor   # int32 [n_pages_cap, 16]
+    page_table: torch.Tensor    # int32 [B, H, max_pages]
+    remap: torch.Tensor         # int32 [B, H, max_pages * 16]
+    count: torch.Tensor         # int32 [B, H]
+
+    @staticmethod
+    def allocate(batch, n_kv_heads, head_dim, n_pages_cap, max_pages, device="cuda"):
+        return PagedKV(
+            torch.zeros((n_pages_cap, PAGE, head_dim), dtype=torch.bfloat16, device=device),
+            torch.zeros((n_pages_cap, PAGE, head_dim), dtype=torch.bfloat16, device=device),
+            torch.zeros((n_pages_cap, PAGE), dtype=torch.int32, device=device),
+            torch.full((batch, n_kv_heads, max_pages), -1, dtype=torch.int32, device=device),
+            torch.full((batch, n_kv_heads, max_pages * PAGE), -1, dtype=torch.int32, device=device),
+            torch.zeros((batch, n_kv_heads), dtype=torch.int32, device=device),
+        )
+
+    @property
+    def n_pages_cap(self):
+        return self.k_pool.shape[0]
+
+    @property
+    def max_pages(self):
+        return self.page_table.shape[2]
+
+    @property
+    def head_dim(self):
+        return self.k_pool.shape[2]
+
+
+def kvp_compact_workspace_bytes(batch, n_kv_heads, n_pos) -> int:
+    return _lib.kvp_compact_workspace_bytes(batch, n_kv_heads, n_pos)
+
+
+def kvp_compact(k, v, expire, now, reserve, dst: PagedKV, *, status, workspace=None, stream=None):
+    """Dense K, V [B, T, H, d] (any strides with d contiguous) + expire [B, H, T] -> dst."""
+    B, T, H, d = k.shape
+    if k.stride() != v.stride() or k.stride(3) != 1:
+        raise ValueError("k and v need identical strides with the head_dim axis contiguous")
+    need = kvp_compact_workspace_bytes(B, H, T)
+    ws = _ws(need, k.device, workspace)
+    for t, nm in ((k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{nm} must be a CUDA bf16 tensor")
+    code = _lib.kvp_compact(B, H, d, T, k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), k.stride(2),
+                            _ptr(expire, torch.int32, "expire"), now, reserve,
+                            _ptr(dst.k_pool, torch.bfloat16), _ptr(dst.v_pool, torch.bfloat16),
+                            _ptr(dst.expire_pool, torch.int32), dst.n_pages_cap,
+                            _ptr(dst.page_table, torch.int32), dst.max_pages, _ptr(dst.remap, torch.int32),
+                            _ptr(dst.count, torch.int32), ws.data_ptr(), ws.numel() * ws.element_size(),
+                            _ptr(status, torch.int32, "status"), _stream(stream))
+    _check("kvp_compact", code)
+    return dst
+
+
+def kvp_compact_paged_workspace_bytes(batch, n_kv_heads, src_max_pages) -> int:
+    return _lib.kvp_compact_paged_workspace_bytes(batch, n_kv_heads, src_max_pages)
+
+
+def kvp_compact_paged(src: PagedKV, now, reserve, dst: PagedKV, *, status, workspace=None, stream=None):
+    B, H, _ = src.page_table.shape
+    need = kvp_compact_paged_workspace_bytes(B, H, src.max_pages)
+    ws = _ws(need, src.k_pool.device, workspace)
+    code = _lib.kvp_compact_paged(B, H, src.head_dim, _ptr(src.k_pool), _ptr(src.v_pool),
+                                  _ptr(src.expire_pool, torch.int32), src.n_pages_cap,
+                                  _ptr(src.page_table, torch.int32), src.max_pages, _ptr(src.remap, torch.int32),
+                                  _ptr(src.count, torch.int32), now, reserve, _ptr(dst.k_pool), _ptr(dst.v_pool),
+                                  _ptr(dst.expire_pool, torch.int32), dst.n_pages_cap,
+                                  _ptr(dst.page_table, torch.int32), dst.max_pages, _ptr(dst.remap, torch.int32),
+                                  _ptr(dst.count, torch.int32), ws.data_ptr(), ws.numel() * ws.element_size(),
+                                  _ptr(status, torch.int32, "status"), _stream(stream))
+    _check("kvp_compact_paged", code)
+    return dst
+
+
+# --------------------------------------------------------------------------- append
+
+def kvp_append(cache: PagedKV, k_new, v_new, pos, *, mode, score=None, tau=None, flag_step=None,
+               window=WINDOW, delay=0, status, stream=None):
+    """Writes the token at position `pos` (k_new, v_new [B, H, d]) into every (b, h)'s next slot."""
+    B, H, d = k_new.shape
+    code = _lib.kvp_append(mode, B, H, d, pos, _ptr(k_new, torch.bfloat16, "k_new"),
+                           _ptr(v_new, torch.bfloat16, "v_new"), _ptr(score, torch.float32, "score", True),
+                           _ptr(tau, torch.float32, "tau", True), _ptr(flag_step, torch.int32, "flag_step", True),
+                           window, delay, _ptr(cache.k_pool), _ptr(cache.v_pool),
+                           _ptr(cache.expire_pool, torch.int32), cache.n_pages_cap,
+                           _ptr(cache.page_table, torch.int32), cache.max_pages, _ptr(cache.remap, torch.int32),
+                           _ptr(cache.count, torch.int32), _ptr(status, torch.int32, "status"), _stream(stream))
+    _check("kvp_append", code)
+
+
+# --------------------------------------------------------------------------- attention
+
+def kvp_decode_attn_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, max_pages, pages_per_split=0) -> int:
+    return _lib.kvp_decode_attn_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, max_pages,
+                                                pages_per_split)
+
+
+def kvp_decode_attn(q, cache: PagedKV, now, *, scale=0.0, out=None, pages_per_split=0, workspace=None,
+                    status=None, stream=None):
+    """out[B, Hq, d] fp32 = attention of q [B, Hq, d] (bf16) over the slots of `cache` present at `now`."""
+    B, Hq, d = q.shape
+    H = cache.count.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    need = kvp_decode_attn_workspace_bytes(B, Hq, H, d, cache.max_pages, pages_per_split)
+    ws = _ws(need, q.device, workspace)
+    code = _lib.kvp_decode_attn(B, Hq, H, d, _ptr(q, torch.bfloat16, "q"), _ptr(cache.k_pool),
+                                _ptr(cache.v_pool), _ptr(cache.expire_pool, torch.int32), cache.n_pages_cap,
+                                _ptr(cache.page_table, torch.int32), cache.max_pages,
+                                _ptr(cache.count, torch.int32), now, float(scale), _ptr(out, torch.float32, "out"),
+                                pages_per_split, ws.data_ptr(), ws.numel() * ws.element_size(),
+                                _ptr(status, torch.int32, "status", True), _stream(stream))
+    _check("kvp_decode_attn", code)
+    return out
+
+
+__all__ = [n for n in dir() if n.startswith(("kvp_", "KVP_", "PagedKV", "KvpError"))] + [
+    "status_string", "version", "library", "PAGE", "WINDOW", "EXPIRE_NEVER"]

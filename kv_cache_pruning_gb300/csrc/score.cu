@@ -1,0 +1,431 @@
+// kvp_score: KVzap surrogate scores on the tcgen05 tensor cores.
+//
+// KVzap summary ("NVIDIA가 AI 메모리 압축 신기술 KVzap 오픈소스 공개!"),
+// 핵심 내용 정리 -> "KVzap의 구조": one linear layer, or a 2-layer MLP, maps a
+// token's hidden state to a score per KV head; "실제 적용": every cache entry is
+// scored during inference.
+//
+// One persistent warp-specialised kernel serves both scorers:
+//   warp 0      TMA producer: 128x64 tiles of x and BNx64 tiles of the weight
+//               (both K-major, 128-byte swizzle) into a STAGES-deep ring
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128xBNx16, fp32
+//               accumulators double-buffered in tensor memory
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, then
+//               LINEAR: s_h = acc[2h] + acc[2h+1] + b_h (weight rows interleave
+//                       the bf16 high and low halves of the fp32 weight)
+//               MLP:    GELU(acc + b1) dotted with W2 over this 256-wide hidden
+//                       chunk -> per-chunk partial scores
+// A small reduction kernel then sums the MLP chunk partials in a fixed order.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kvp_common.cuh"
+
+namespace kvp {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr int kMlpBN = 256;
+constexpr int kMlpMaxH = 16;
+
+template <int BN>
+struct ScoreCfg {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = BN <= 32 ? 8 : (BN <= 128 ? 6 : 4);
+  static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kEpiBytes = (BN == kMlpBN) ? (kMlpBN * kMlpMaxH * 4 + kMlpBN * 4) : 0;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kEpiBytes;
+  static_assert(kBBytes % 1024 == 0, "B tile must keep 1024-byte alignment");
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+struct ScoreParams {
+  int n_tok;
+  int n_heads;
+  int hidden;
+  int m_tiles;
+  int n_tiles;
+  int k_blocks;
+  const float* bias;        // LINEAR: b[H]; MLP: b1[hidden]; may be null
+  const uint16_t* w2;       // MLP: bf16 [H, hidden]
+  float* out;               // LINEAR: scores [n_tok, H]; MLP: partials [n_tiles, n_tok, H]
+  int32_t* status;
+};
+
+enum { kEpiLinear = 0, kEpiMlp = 1 };
+
+KVP_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const ScoreParams p) {
+  using C = ScoreCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* w2s = reinterpret_cast<float*>(tiles + C::kStages * C::kStageBytes + C::kBarBytes);
+  float* b1s = w2s + kMlpBN * kMlpMaxH;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_tiles_total = p.m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const uint64_t pol_x = policy_evict_first();  // hidden states stream through once
+      const uint64_t pol_w = policy_evict_last();   // weights are re-read by every tile
+      uint32_t stage = 0, phase = 0;
+      for (int t = blockIdx.x; t < n_tiles_total && !*abort_flag; t += gridDim.x) {
+        const int mt = t / p.n_tiles, nt = t - mt * p.n_tiles;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+            record_error(p.status, KVP_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* a = tiles + stage * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          tma_load_2d_hint(a, &tmA, kb * kBK, mt * kBM, &full[stage], pol_x);
+          tma_load_2d_hint(a + C::kABytes, &tmB, kb * kBK, nt * BN, &full[stage], pol_w);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      for (int t = blockIdx.x; t < n_tiles_total && !*abort_flag; t += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
+          record_error(p.status, KVP_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+            record_error(p.status, KVP_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(tiles + stage * C::kStageBytes);
+          const uint64_t adesc = sw128_kmajor_desc(a_addr);
+          const uint64_t bdesc = sw128_kmajor_desc(a_addr + C::kABytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);  // frees this smem stage once the MMAs have read it
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        umma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;
+    const int etid = threadIdx.x - 64;
+    uint32_t acc = 0, acc_phase = 0;
+    int cur_nt = -1;
+    for (int t = blockIdx.x; t < n_tiles_total; t += gridDim.x) {
+      const int mt = t / p.n_tiles, nt = t - mt * p.n_tiles;
+      if constexpr (EPI == kEpiMlp) {
+        if (nt != cur_nt) {  // stage this hidden chunk's W2 columns and b1 as fp32
+          named_bar_sync(1, 128);
+          const int H = p.n_heads;
+          for (int i = etid; i < kMlpBN * H; i += 128) {
+            const int c = i / H, h = i - c * H;
+            const uint32_t w = p.w2[static_cast<size_t>(h) * p.hidden + nt * kMlpBN + c];
+            w2s[c * H + h] = __uint_as_float(w << 16);
+          }
+          for (int c = etid; c < kMlpBN; c += 128) b1s[c] = p.bias ? p.bias[nt * kMlpBN + c] : 0.f;
+          named_bar_sync(1, 128);
+          cur_nt = nt;
+        }
+      }
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) {
+        record_error(p.status, KVP_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      const int grow = mt * kBM + row;
+      if constexpr (EPI == kEpiLinear) {
+        float v[BN];
+#pragma unroll
+        for (int c = 0; c < BN; c += 16) tmem_ld16(taddr + c, *reinterpret_cast<float(*)[16]>(&v[c]));
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        if (grow < p.n_tok) {
+          const int H = p.n_heads;
+          float* o = p.out + static_cast<size_t>(grow) * H;
+#pragma unroll
+          for (int h = 0; h < BN / 2; ++h) {
+            if (h < H) o[h] = v[2 * h] + v[2 * h + 1] + (p.bias ? __ldg(p.bias + h) : 0.f);
+          }
+        }
+      } else {
+        const int H = p.n_heads;
+        float part[kMlpMaxH];
+#pragma unroll
+        for (int h = 0; h < kMlpMaxH; ++h) part[h] = 0.f;
+#pragma unroll 1
+        for (int cc = 0; cc < kMlpBN; cc += 32) {
+          float v[32];
+          tmem_ld32(taddr + cc, v);
+          if (cc == kMlpBN - 32) {
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float u = v[j] + b1s[cc + j];
+            const float z = 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));
+            const float* wr = w2s + (cc + j) * H;
+#pragma unroll
+            for (int h = 0; h < kMlpMaxH; ++h)
+              if (h < H) part[h] = fmaf(z, wr[h], part[h]);
+          }
+        }
+        if (grow < p.n_tok) {
+          float* o = p.out + (static_cast<size_t>(nt) * p.n_tok + grow) * H;
+#pragma unroll
+          for (int h = 0; h < kMlpMaxH; ++h)
+            if (h < H) o[h] = part[h];
+        }
+      }
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// W [H, D] fp32 -> Wt [n_rows, D] bf16 with row 2h = bf16(W[h]) and row 2h+1 =
+// bf16(W[h] - bf16(W[h])); rows >= 2H are zero.
+__global__ void split_weight_kernel(const float* __restrict__ w, int H, int D, int n_rows,
+                                    __nv_bfloat16* __restrict__ wt) {
+  const size_t n = static_cast<size_t>(n_rows) * D;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / D);
+    const int k = static_cast<int>(i - static_cast<size_t>(r) * D);
+    const int h = r >> 1;
+    __nv_bfloat16 out = __float2bfloat16_rn(0.f);
+    if (h < H) {
+      const float x = w[static_cast<size_t>(h) * D + k];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+      out = (r & 1) ? __float2bfloat16_rn(x - __bfloat162float(hi)) : hi;
+    }
+    wt[i] = out;
+  }
+}
+
+// scores[t, h] = sum_c part[c, t, h] + b2[h], chunks summed in order.
+__global__ void mlp_reduce_kernel(const float* __restrict__ part, int n_chunks, int64_t n, int H,
+                                  const float* __restrict__ b2, float* __restrict__ scores) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float s = b2 ? b2[i % H] : 0.f;
+    for (int c = 0; c < n_chunks; ++c) s += part[c * n + i];
+    scores[i] = s;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// K-major bf16 matrix [rows, cols] with row stride ld elements, boxes of
+// box_rows x 64 columns, 128-byte swizzle, zero fill outside the matrix.
+bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int linear_bn(int H) {
+  const int rows = 2 * H;
+  return rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+template <int BN, int EPI>
+kvp_status launch_score(const CUtensorMap& ta, const CUtensorMap& tb, const ScoreParams& p, cudaStream_t st) {
+  using C = ScoreCfg<BN>;
+  auto kern = score_tc_kernel<BN, EPI>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+    return KVP_ERR_CUDA;
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int nsm = sm_count();
+  if (nsm <= 0) return KVP_ERR_CUDA;
+  const int grid = tiles < nsm ? tiles : nsm;
+  kern<<<grid, kThreads, C::kSmem, st>>>(ta, tb, p);
+  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace kvp
+
+using namespace kvp;
+
+extern "C" size_t kvp_score_workspace_bytes(int scorer, int64_t n_tok, int d_model, int n_kv_heads, int hidden) {
+  if (n_tok < 0 || d_model <= 0 || n_kv_heads <= 0) return 0;
+  if (scorer == KVP_SCORER_LINEAR) {
+    return static_cast<size_t>(linear_bn(n_kv_heads)) * d_model * 2;
+  }
+  if (scorer == KVP_SCORER_MLP) {
+    if (hidden <= 0) return 0;
+    return static_cast<size_t>(hidden / kMlpBN) * n_tok * n_kv_heads * sizeof(float);
+  }
+  return 0;
+}
+
+extern "C" kvp_status kvp_score(int scorer, int64_t n_tok, int d_model, int n_kv_heads, int hidden, const void* x,
+                                int64_t ld_x, const void* w, const float* b, const void* w2, const float* b2,
+                                float* scores, void* workspace, size_t workspace_bytes, int32_t* status,
+                                void* stream) {
+  if (scorer != KVP_SCORER_LINEAR && scorer != KVP_SCORER_MLP) return KVP_ERR_INVALID;
+  if (n_tok < 0 || d_model <= 0 || n_kv_heads <= 0) return KVP_ERR_INVALID;
+  if (n_tok == 0) return KVP_OK;
+  if (x == nullptr || w == nullptr || scores == nullptr) return KVP_ERR_INVALID;
+  if (ld_x < d_model) return KVP_ERR_INVALID;
+  if (d_model % 8 != 0 || d_model > 65536 || n_kv_heads > 64) return KVP_ERR_UNSUPPORTED;
+  if (ld_x % 8 != 0 || !aligned16(x)) return KVP_ERR_ALIGN;
+  if (n_tok > (int64_t(1) << 31) - 1) return KVP_ERR_UNSUPPORTED;
+  const size_t need = kvp_score_workspace_bytes(scorer, n_tok, d_model, n_kv_heads, hidden);
+  if (workspace == nullptr || workspace_bytes < need) return KVP_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVP_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  ScoreParams p{};
+  p.n_tok = static_cast<int>(n_tok);
+  p.n_heads = n_kv_heads;
+  p.m_tiles = static_cast<int>((n_tok + kBM - 1) / kBM);
+  p.k_blocks = (d_model + kBK - 1) / kBK;
+  p.status = status;
+
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, x, n_tok, d_model, ld_x, kBM)) return KVP_ERR_CUDA;
+
+  if (scorer == KVP_SCORER_LINEAR) {
+    if (w2 != nullptr || b2 != nullptr) return KVP_ERR_INVALID;
+    const int bn = linear_bn(n_kv_heads);
+    auto* wt = static_cast<__nv_bfloat16*>(workspace);
+    const size_t nel = static_cast<size_t>(bn) * d_model;
+    const int blocks = static_cast<int>((nel + 255) / 256 < 4096 ? (nel + 255) / 256 : 4096);
+    split_weight_kernel<<<blocks, 256, 0, st>>>(static_cast<const float*>(w), n_kv_heads, d_model, bn, wt);
+    if (cudaGetLastError() != cudaSuccess) return KVP_ERR_CUDA;
+    if (!make_tmap(&tb, wt, bn, d_model, d_model, bn)) return KVP_ERR_CUDA;
+    p.n_tiles = 1;
+    p.bias = b;
+    p.out = scores;
+    switch (bn) {
+      case 16: return launch_score<16, kEpiLinear>(ta, tb, p, st);
+      case 32: return launch_score<32, kEpiLinear>(ta, tb, p, st);
+      case 64: return launch_score<64, kEpiLinear>(ta, tb, p, st);
+      default: return launch_score<128, kEpiLinear>(ta, tb, p, st);
+    }
+  }
+
+  // MLP
+  if (w2 == nullptr) return KVP_ERR_INVALID;
+  if (hidden <= 0 || hidden % kMlpBN != 0 || n_kv_heads > kMlpMaxH) return KVP_ERR_UNSUPPORTED;
+  if (!aligned16(w)) return KVP_ERR_ALIGN;
+  if (!make_tmap(&tb, w, hidden, d_model, d_model, kMlpBN)) return KVP_ERR_CUDA;
+  float* part = static_cast<float*>(workspace);
+  p.n_tiles = hidden / kMlpBN;
+  p.hidden = hidden;
+  p.bias = b;
+  p.w2 = static_cast<const uint16_t*>(w2);
+  p.out = part;
+  kvp_status s = launch_score<kMlpBN, kEpiMlp>(ta, tb, p, st);
+  if (s != KVP_OK) return s;
+  const int64_t n = n_tok * n_kv_heads;
+  const int blocks = static_cast<int>((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
+  mlp_reduce_kernel<<<blocks, 256, 0, st>>>(part, p.n_tiles, n, n_kv_heads, b2, scores);
+  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}

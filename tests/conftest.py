@@ -11,3 +11,22 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: full-size workload, minutes")
+
+
+def _cuda_ok():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+@pytest.fixture(scope="session")
+def kvp():
+    """The package, built for sm_103a; GPU tests only."""
+    if not _cuda_ok():
+        pytest.skip("no CUDA device")
+    from kv_cache_pruning_gb300 import _build
+    _build.build()
+    import kv_cache_pruning_gb300 as pkg
+    return pkg

@@ -1,0 +1,85 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every entry
+point include/kvp.h declares, and rejects bad arguments on the host (no call
+here reaches a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "kvp.h")) as f:
+        text = f.read()
+    return re.findall(r"^KVP_API[^;(]*?\b(kvp_\w+)\s*\(", text, flags=re.M | re.S)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cache_pruning_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_path():
+    names = set(_declared())
+    for n in ["kvp_score", "kvp_mask", "kvp_compact", "kvp_compact_paged", "kvp_append", "kvp_decode_attn",
+              "kvp_score_workspace_bytes", "kvp_compact_workspace_bytes", "kvp_decode_attn_workspace_bytes",
+              "kvp_status_string", "kvp_version"]:
+        assert n in names, n
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in kvp.h but not exported"
+
+
+def test_status_strings_and_version(lib):
+    lib.kvp_status_string.restype = ctypes.c_char_p
+    assert lib.kvp_status_string(0) == b"ok"
+    assert b"aligned" in lib.kvp_status_string(2)
+    assert lib.kvp_status_string(99) == b"unknown status"
+    assert lib.kvp_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    lib.kvp_score_workspace_bytes.restype = ctypes.c_size_t
+    lib.kvp_score_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    # LINEAR: bf16 hi/lo weight rows, padded to 16 rows for 8 heads
+    assert lib.kvp_score_workspace_bytes(0, 131072, 4096, 8, 0) == 16 * 4096 * 2
+    # MLP: one fp32 partial per 256-wide hidden chunk, token and head
+    assert lib.kvp_score_workspace_bytes(1, 1000, 4096, 8, 1024) == 4 * 1000 * 8 * 4
+    lib.kvp_decode_attn_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.kvp_decode_attn_workspace_bytes(2, 8, 2, 128, 100, 16) == 2 * 8 * 7 * 130 * 4
+
+
+def test_host_validation_without_gpu(lib):
+    import kv_cache_pruning_gb300 as k
+    L = k.library()
+    # null x -> invalid; unsupported head count; unaligned x
+    assert L.kvp_score(0, 10, 64, 2, 0, None, 64, None, None, None, None, None, None, 0, None, None) == k.KVP_ERR_INVALID
+    assert L.kvp_score(0, 10, 64, 65, 0, 16, 64, 16, None, None, None, 16, 16, 1 << 20, None, None) == k.KVP_ERR_UNSUPPORTED
+    assert L.kvp_score(0, 10, 64, 2, 0, 18, 64, 16, None, None, None, 16, 16, 1 << 20, None, None) == k.KVP_ERR_ALIGN
+    assert L.kvp_score(0, 10, 64, 2, 0, 16, 64, 16, None, None, None, 16, 16, 8, None, None) == k.KVP_ERR_WORKSPACE
+    # mask: both inputs given / unknown mode
+    assert L.kvp_mask(0, 1, 1, 8, 0, 16, 16, 16, 128, 0, 7, 16, None, None, None) == k.KVP_ERR_INVALID
+    assert L.kvp_mask(5, 1, 1, 8, 0, 16, 16, None, 128, 0, 7, 16, None, None, None) == k.KVP_ERR_INVALID
+    # attention: head ratio not in {1,2,4,8}, bad head_dim
+    assert L.kvp_decode_attn(1, 6, 2, 128, 16, 16, 16, 16, 1, 16, 1, 16, 0, 0.0, 16, 0, 16, 1 << 20, None,
+                             None) == k.KVP_ERR_UNSUPPORTED
+    assert L.kvp_decode_attn(1, 4, 2, 96, 16, 16, 16, 16, 1, 16, 1, 16, 0, 0.0, 16, 0, 16, 1 << 20, None,
+                             None) == k.KVP_ERR_UNSUPPORTED
+    # compaction: status word is required
+    assert L.kvp_compact(1, 1, 128, 16, 16, 16, 0, 0, 0, 16, 15, 0, 16, 16, 16, 1, 16, 1, 16, 16, 16, 1 << 20,
+                         None, None) == k.KVP_ERR_INVALID
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    import kv_cache_pruning_gb300 as k
+    monkeypatch.setattr(k, "LIB_PATH", os.path.join(ROOT, "no_such_libkvp.so"))
+    with pytest.raises(ImportError):
+        k._load()

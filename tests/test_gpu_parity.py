@@ -1,0 +1,391 @@
+"""GPU path vs the oracle, element by element, on the same seeded inputs.
+
+Bars: masks, expire values, page tables, remap lists and pools bit-exact;
+scores within 1e-3 relative (to max(|s|, ||x_t * w_h||_2)); attention within
+max-abs 2e-2, mean-abs 2e-3 and 1e-2 relative per head."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kvp_synth as syn
+import oracle as orc
+from helpers import check_attention, check_scores, dev_bf16, dev_f32, dev_i32, host_bits, status_word
+
+pytestmark = pytest.mark.gpu
+
+
+def _linear_scale(x_bits, w):
+    """||x_t * w_h||_2 per (t, h): the size of the dot product's terms."""
+    x = orc.widen_bf16(x_bits)
+    return np.sqrt((x * x) @ (np.asarray(w, np.float64) ** 2).T)
+
+
+# --------------------------------------------------------------------------- score
+
+@pytest.mark.parametrize("n_tok,D,H,bias", [
+    (512, 256, 2, False),     # tiny workload shape, one layer
+    (1000, 4096, 8, True),    # Llama-3-8B width, 8 tiles with a ragged tail
+    (300, 512, 64, False),    # 64 heads (widest weight tile), ragged
+    (129, 1032, 5, True),     # d_model not a multiple of 64, odd head count
+    (1, 64, 1, False),        # single token, single head
+])
+def test_score_linear(kvp, n_tok, D, H, bias):
+    x, w = syn.linear_inputs(0, n_tok, D, H)
+    b = syn.normal_f32(0, 77, (H,)) if bias else None
+    ref = orc.score_linear(x, w, b)
+    st = status_word()
+    s = kvp.kvp_score(dev_bf16(x), dev_f32(w), dev_f32(b) if bias else None, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    check_scores(s.cpu().numpy(), ref, _linear_scale(x, w))
+
+
+def test_score_linear_strided_rows(kvp):
+    n_tok, D, H = 200, 512, 8
+    x, w = syn.linear_inputs(1, n_tok, D + 64, H)
+    xs = dev_bf16(x)[:, :D]  # row stride D + 64
+    s = kvp.kvp_score(xs, dev_f32(w[:, :D].copy()))
+    torch.cuda.synchronize()
+    check_scores(s.cpu().numpy(), orc.score_linear(x[:, :D], w[:, :D]), _linear_scale(x[:, :D], w[:, :D]))
+
+
+@pytest.mark.parametrize("n_tok,D,hidden,H,bias", [
+    (300, 512, 512, 8, True),
+    (128, 256, 1024, 8, False),
+    (77, 320, 256, 3, True),
+])
+def test_score_mlp(kvp, n_tok, D, hidden, H, bias):
+    x, w1, w2 = syn.mlp_inputs(0, n_tok, D, hidden, H)
+    b1 = syn.normal_f32(0, 78, (hidden,), std=0.1) if bias else None
+    b2 = syn.normal_f32(0, 79, (H,)) if bias else None
+    ref = orc.score_mlp(x, w1, w2, b1, b2)
+    st = status_word()
+    s = kvp.kvp_score(dev_bf16(x), dev_bf16(w1), dev_f32(b1) if bias else None, dev_bf16(w2),
+                      dev_f32(b2) if bias else None, scorer=kvp.KVP_SCORER_MLP, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    # natural error scale: the 2-norm of the hidden terms z_j * w2[h, j]
+    u = orc.widen_bf16(x) @ orc.widen_bf16(w1).T + (0 if b1 is None else b1[None, :])
+    z = orc.gelu(u)
+    scale = np.sqrt((z * z) @ (orc.widen_bf16(w2) ** 2).T)
+    check_scores(s.cpu().numpy(), ref, scale)
+
+
+# --------------------------------------------------------------------------- mask
+
+@pytest.mark.parametrize("B,T,H,window", [(1, 512, 2, 128), (3, 1000, 5, 128), (2, 33, 3, 7), (1, 4096, 8, 0)])
+def test_mask_kvzap_bit_exact(kvp, B, T, H, window):
+    s = syn.normal_f32(2, 11, (B, T, H))
+    s[0, 5, 0] = np.nan
+    tau = syn.normal_f32(2, 12, (B, H), std=0.5)
+    tau[0, 0] = -np.inf
+    now = T - 1
+    exp_r, keep_r, bits_r, cnt_r = orc.mask_kvzap(s, tau, now, window=window)
+    exp, bits, cnt = kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=now,
+                                  scores=dev_f32(s), tau=dev_f32(tau), window=window)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(exp.cpu().numpy(), exp_r)
+    np.testing.assert_array_equal(bits.cpu().numpy().view(np.uint32), bits_r)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), cnt_r)
+
+
+@pytest.mark.parametrize("delay,now", [(256, 4095), (40, 3000), (0, 4095)])
+def test_mask_dms_bit_exact(kvp, delay, now):
+    B, H, T = 4, 8, 4096
+    ev = syn.bernoulli(0, syn.S_FLAG, (B, H, T), 7 / 8)
+    f = np.where(ev, np.arange(T)[None, None, :], -1).astype(np.int32)
+    exp_r, keep_r, bits_r, cnt_r = orc.mask_dms(f, now, delay)
+    exp, bits, cnt = kvp.kvp_mask(mode=kvp.KVP_MASK_DMS, batch=B, n_kv_heads=H, n_pos=T, now=now,
+                                  flag_step=dev_i32(f), delay=delay)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(exp.cpu().numpy(), exp_r)
+    np.testing.assert_array_equal(bits.cpu().numpy().view(np.uint32), bits_r)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), cnt_r)
+
+
+# --------------------------------------------------------------------------- compact
+
+def _compare_cache(gpu, ref: orc.PagedCache):
+    np.testing.assert_array_equal(gpu.count.cpu().numpy(), ref.count, err_msg="count")
+    np.testing.assert_array_equal(gpu.page_table.cpu().numpy(), ref.page_table, err_msg="page_table")
+    np.testing.assert_array_equal(gpu.remap.cpu().numpy(), ref.remap, err_msg="remap")
+    used = ref.pages_used
+    np.testing.assert_array_equal(gpu.expire_pool.cpu().numpy()[:used], ref.expire_pool[:used], err_msg="expire")
+    np.testing.assert_array_equal(host_bits(gpu.k_pool)[:used], ref.k_pool[:used], err_msg="k_pool")
+    np.testing.assert_array_equal(host_bits(gpu.v_pool)[:used], ref.v_pool[:used], err_msg="v_pool")
+
+
+def _kvzap_case(B, T, H, d, seed=3, tau_std=0.7):
+    k, v = syn.kv_inputs(seed, B, T, H, d)
+    s = syn.normal_f32(seed, 21, (B, T, H))
+    tau = syn.normal_f32(seed, 22, (B, H), std=tau_std)
+    exp, keep, bits, cnt = orc.mask_kvzap(s, tau, T - 1)
+    return k, v, exp.astype(np.int32), cnt
+
+
+@pytest.mark.parametrize("B,T,H,d,reserve", [
+    (1, 512, 2, 64, 0),
+    (2, 3000, 3, 128, 5),      # 3 chunks, ragged
+    (4, 1030, 8, 128, 64),
+    (2, 17, 2, 64, 16),        # tiny ragged, reserve a full page
+])
+def test_compact_dense_bit_exact(kvp, B, T, H, d, reserve):
+    k, v, exp, cnt = _kvzap_case(B, T, H, d)
+    max_pages = (T + reserve + 15) // 16
+    cap = B * H * max_pages
+    ref = orc.compact_dense(k, v, exp, T - 1, reserve, cap, max_pages)
+    st = status_word()
+    dst = kvp.PagedKV.allocate(B, H, d, cap, max_pages)
+    kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp), T - 1, reserve, dst, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_cache(dst, ref)
+    # rows past count in a (b, h)'s last page are zero, expire 0
+    ep = dst.expire_pool.cpu().numpy()
+    assert (ep[ref.pages_used:] == 0).all()
+
+
+def test_compact_strided_source(kvp):
+    # K/V as a [B, H, T, d] tensor viewed as [B, T, H, d]
+    B, T, H, d = 2, 700, 4, 128
+    k, v, exp, cnt = _kvzap_case(B, T, H, d, seed=5)
+    kt = dev_bf16(np.ascontiguousarray(k.transpose(0, 2, 1, 3))).permute(0, 2, 1, 3)
+    vt = dev_bf16(np.ascontiguousarray(v.transpose(0, 2, 1, 3))).permute(0, 2, 1, 3)
+    max_pages = (T + 15) // 16
+    ref = orc.compact_dense(k, v, exp, T - 1, 0, B * H * max_pages, max_pages)
+    st = status_word()
+    dst = kvp.PagedKV.allocate(B, H, d, B * H * max_pages, max_pages)
+    kvp.kvp_compact(kt, vt, dev_i32(exp), T - 1, 0, dst, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_cache(dst, ref)
+
+
+def test_compact_keep_all_and_keep_none(kvp):
+    B, T, H, d = 1, 300, 2, 64
+    k, v = syn.kv_inputs(6, B, T, H, d)
+    for exp in [np.full((B, H, T), orc.NEVER, np.int32), np.zeros((B, H, T), np.int32)]:
+        ref = orc.compact_dense(k, v, exp, T - 1, 3, 64, 32)
+        st = status_word()
+        dst = kvp.PagedKV.allocate(B, H, d, 64, 32)
+        kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp), T - 1, 3, dst, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        _compare_cache(dst, ref)
+
+
+def test_compact_capacity_status(kvp):
+    B, T, H, d = 1, 256, 2, 64
+    k, v = syn.kv_inputs(6, B, T, H, d)
+    exp = dev_i32(np.full((B, H, T), orc.NEVER, np.int32))
+    st = status_word()
+    dst = kvp.PagedKV.allocate(B, H, d, 20, 32)  # needs 32 pages in all
+    kvp.kvp_compact(dev_bf16(k), dev_bf16(v), exp, T - 1, 0, dst, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == kvp.KVP_ERR_CAPACITY
+    st.zero_()
+    dst = kvp.PagedKV.allocate(B, H, d, 64, 15)  # a (b, h) needs 16 > max_pages
+    kvp.kvp_compact(dev_bf16(k), dev_bf16(v), exp, T - 1, 0, dst, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == kvp.KVP_ERR_CAPACITY
+
+
+def _dms_stream(B, T, H, d, delay, window, seed):
+    k, v = syn.kv_inputs(seed, B, T, H, d)
+    pos = np.arange(T)[None, None, :]
+    f = np.where(syn.bernoulli(seed, 8, (B, H, T), 0.875), pos, -1).astype(np.int32)
+    exp = orc.expire_dms(f, pos, delay, window).astype(np.int32)
+    return k, v, f, exp
+
+
+def test_append_then_paged_recompaction(kvp):
+    """Prefill compaction, appends of the next tokens, then a paged re-compaction:
+    bit-exact against the oracle at every stage."""
+    B, T0, steps, H, d = 3, 700, 90, 4, 128
+    delay, window, reserve = 60, 32, 96
+    T = T0 + steps
+    k, v, f, exp = _dms_stream(B, T, H, d, delay, window, seed=9)
+    max_pages = (T + reserve + 15) // 16
+    cap = B * H * max_pages
+    now0 = T0 - 1
+    ref = orc.compact_dense(k[:, :T0], v[:, :T0], exp[:, :, :T0], now0, reserve, cap, max_pages)
+    st = status_word()
+    c = kvp.PagedKV.allocate(B, H, d, cap, max_pages)
+    kvp.kvp_compact(dev_bf16(k[:, :T0].copy()), dev_bf16(v[:, :T0].copy()), dev_i32(exp[:, :, :T0].copy()), now0,
+                    reserve, c, status=st)
+    kd, vd, fd = dev_bf16(k), dev_bf16(v), dev_i32(f)
+    for t in range(T0, T):
+        orc.append(ref, k[:, t], v[:, t], t, exp[:, :, t])
+        kvp.kvp_append(c, kd[:, t].contiguous(), vd[:, t].contiguous(), t, mode=kvp.KVP_MASK_DMS,
+                       flag_step=fd[:, :, t].contiguous(), delay=delay, window=window, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_cache(c, ref)
+    now = T - 1
+    ref2 = orc.compact_paged(ref, now, 16, cap, max_pages)
+    c2 = kvp.PagedKV.allocate(B, H, d, cap, max_pages)
+    kvp.kvp_compact_paged(c, now, 16, c2, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_cache(c2, ref2)
+
+
+def test_append_kvzap_and_reserve_exhausted(kvp):
+    B, T, H, d = 2, 100, 2, 64
+    k, v = syn.kv_inputs(4, B, T + 40, H, d)
+    exp = np.full((B, H, T), orc.NEVER, np.int32)
+    reserve = 12  # 100 + 12 = 112 slots = 7 pages exactly
+    max_pages = 8
+    ref = orc.compact_dense(k[:, :T], v[:, :T], exp, T - 1, reserve, 64, max_pages)
+    st = status_word()
+    c = kvp.PagedKV.allocate(B, H, d, 64, max_pages)
+    kvp.kvp_compact(dev_bf16(k[:, :T].copy()), dev_bf16(v[:, :T].copy()), dev_i32(exp), T - 1, reserve, c, status=st)
+    score = syn.normal_f32(4, 30, (12, B, H))
+    tau = np.zeros((B, H), np.float32)
+    for i in range(12):
+        t = T + i
+        orc.append(ref, k[:, t], v[:, t], t, orc.expire_kvzap(score[i], tau, t, 128))
+        kvp.kvp_append(c, dev_bf16(k[:, t].copy()), dev_bf16(v[:, t].copy()), t, mode=kvp.KVP_MASK_KVZAP,
+                       score=dev_f32(score[i]), tau=dev_f32(tau), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_cache(c, ref)
+    kvp.kvp_append(c, dev_bf16(k[:, T].copy()), dev_bf16(v[:, T].copy()), T + 12, mode=kvp.KVP_MASK_KVZAP,
+                   score=dev_f32(score[0]), tau=dev_f32(tau), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == kvp.KVP_ERR_CAPACITY
+    np.testing.assert_array_equal(c.count.cpu().numpy(), ref.count)  # unchanged
+
+
+# --------------------------------------------------------------------------- attention
+
+def _attn_case(kvp, B, T, H, G, d, tau_std=0.7, seed=3, reserve=0, pps=0, peaked=False):
+    k, v, exp, cnt = _kvzap_case(B, T, H, d, seed=seed, tau_std=tau_std)
+    q = syn.q_inputs(seed, B, H * G, d)
+    if peaked:  # q x 8 and 16 planted keys equal to q: a sharp softmax
+        qf = orc.widen_bf16(q) * 8.0
+        q = syn.f32_to_bf16_bits(qf.astype(np.float32))
+        k = k.copy()
+        for i in range(16):
+            t = (i * 97 + 11) % T
+            exp[:, :, t] = orc.NEVER
+            k[:, t, :, :] = syn.f32_to_bf16_bits((qf[:, ::G, :] / 8.0).astype(np.float32))
+    max_pages = (T + reserve + 15) // 16
+    cap = B * H * max_pages
+    now = T - 1
+    ref_c = orc.compact_dense(k, v, exp, now, reserve, cap, max_pages)
+    ref = orc.decode_attention(q, ref_c, now)
+    st = status_word()
+    c = kvp.PagedKV.allocate(B, H, d, cap, max_pages)
+    kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp), now, reserve, c, status=st)
+    out = kvp.kvp_decode_attn(dev_bf16(q), c, now, pages_per_split=pps, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return out.cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("B,T,H,G,d,pps", [
+    (1, 512, 2, 2, 64, 0),       # tiny workload shape
+    (2, 2000, 8, 4, 128, 0),     # Llama-3-8B GQA 4, several splits
+    (2, 2000, 8, 4, 128, 3),     # odd split size
+    (1, 3000, 4, 1, 128, 5),     # MHA
+    (2, 1500, 2, 8, 128, 0),     # GQA 8
+    (3, 777, 3, 2, 64, 1),       # one page per split
+    (1, 900, 2, 8, 64, 7),
+    (1, 1200, 4, 4, 64, 2),
+])
+def test_decode_attn(kvp, B, T, H, G, d, pps):
+    o, ref = _attn_case(kvp, B, T, H, G, d, pps=pps)
+    check_attention(o, ref)
+
+
+@pytest.mark.parametrize("G,d", [(4, 128), (1, 128), (8, 64)])
+def test_decode_attn_peaked(kvp, G, d):
+    o, ref = _attn_case(kvp, 2, 1500, 2, G, d, peaked=True)
+    check_attention(o, ref)
+
+
+def test_decode_attn_split_independent(kvp):
+    outs = [_attn_case(kvp, 1, 2500, 2, 4, 128, pps=p)[0] for p in (1, 4, 16, 200)]
+    for o in outs[1:]:
+        np.testing.assert_allclose(o, outs[0], rtol=0, atol=1e-5)
+
+
+def test_decode_attn_keep_all_is_dense_and_window(kvp):
+    B, T, H, G, d = 1, 1100, 2, 4, 128
+    k, v = syn.kv_inputs(8, B, T, H, d)
+    q = syn.q_inputs(8, B, H * G, d)
+    now = T - 1
+    mp = (T + 15) // 16
+    for exp, ref in [(np.full((B, H, T), orc.NEVER, np.int32), orc.dense_attention(q, k, v, now)),
+                     (orc.mask_kvzap(np.full((B, T, H), -np.inf, np.float32), np.zeros((B, H), np.float32),
+                                     now)[0].astype(np.int32), orc.window_attention(q, k, v, now))]:
+        c = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp)
+        st = status_word()
+        kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp), now, 0, c, status=st)
+        o = kvp.kvp_decode_attn(dev_bf16(q), c, now, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        check_attention(o.cpu().numpy(), ref)
+
+
+def test_decode_attn_empty_heads_and_expired_slots(kvp):
+    # window 0 and tau +inf for head 0: nothing kept -> zero rows; later `now`
+    # turns slots of head 1 absent without re-compaction (masked in attention)
+    B, T, H, G, d = 1, 400, 2, 2, 64
+    k, v = syn.kv_inputs(10, B, T, H, d)
+    q = syn.q_inputs(10, B, H * G, d)
+    s = syn.normal_f32(10, 21, (B, T, H))
+    tau = np.array([[np.inf, 0.5]], np.float32)
+    exp = orc.mask_kvzap(s, tau, T - 1, window=0)[0].astype(np.int32)
+    exp[0, 1, ::3] = T + 5   # these leave the cache at step T+5
+    mp = (T + 15) // 16
+    for now in (T - 1, T + 5):
+        ref = orc.decode_attention(q, orc.compact_dense(k, v, exp, T - 1, 0, B * H * mp, mp), now)
+        c = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp)
+        st = status_word()
+        kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp), T - 1, 0, c, status=st)
+        o = kvp.kvp_decode_attn(dev_bf16(q), c, now, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        on = o.cpu().numpy()
+        assert (on[0, :G] == 0).all()
+        check_attention(on, ref)
+
+
+# --------------------------------------------------------------------------- chained path
+
+def test_chain_score_mask_compact_attend_tiny(kvp):
+    """The tiny workload end to end on the GPU: scores from the scorer, the
+    per-head median threshold from the oracle's scores, then mask, compaction and
+    attention; near-threshold entries (|s - tau| <= 1e-3) are excluded from the
+    mask comparison and the downstream steps take the oracle's keep set."""
+    cfg = syn.WORKLOADS["tiny"]
+    B, T, H, G, d, D = 1, cfg["n_pos"], cfg["n_kv_heads"], 2, cfg["head_dim"], cfg["d_model"]
+    x, w = syn.linear_inputs(0, B * T, D, H)
+    k, v = syn.kv_inputs(0, B, T, H, d)
+    q = syn.q_inputs(0, B, H * G, d)
+    s_ref = orc.score_linear(x, w).reshape(B, T, H)
+    tau = orc.threshold_at_quantile(s_ref, 0.5)
+    s_gpu = kvp.kvp_score(dev_bf16(x), dev_f32(w))
+    exp_g, _, cnt_g = kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=T - 1,
+                                   scores=s_gpu, tau=dev_f32(tau))
+    torch.cuda.synchronize()
+    exp_r = orc.mask_kvzap(s_ref, tau, T - 1)[0]
+    near = np.abs(s_ref - tau[:, None, :]).transpose(0, 2, 1) <= 1e-3
+    assert near.sum() <= 4
+    np.testing.assert_array_equal(exp_g.cpu().numpy()[~near], exp_r[~near])
+    kept = (T - 1 < exp_r).sum(axis=2)
+    assert np.all(np.abs(kept / T - 0.627) < 0.05)  # ~37% pruned: median minus the window's share
+    mp = (T + 15) // 16
+    ref_c = orc.compact_dense(k, v, exp_r.astype(np.int32), T - 1, 0, B * H * mp, mp)
+    c = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp)
+    st = status_word()
+    kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp_r), T - 1, 0, c, status=st)
+    o = kvp.kvp_decode_attn(dev_bf16(q), c, T - 1, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_cache(c, ref_c)
+    check_attention(o.cpu().numpy(), orc.decode_attention(q, ref_c, T - 1))
