@@ -26,7 +26,7 @@ def kvp():
     """The package, built for sm_103a; GPU tests only."""
     if not _cuda_ok():
         pytest.skip("no CUDA device")
-    from kv_cache_pruning_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import kv_cache_pruning_gb300 as pkg
     return pkg

@@ -18,8 +18,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    from kv_cache_pruning_gb300 import _build
-    path = _build.build()
+    import __graft_entry__
+    path = __graft_entry__._builder().build()
     return ctypes.CDLL(path)
 
 
