@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Benchmark of the pruned-KV decode path on GB300.
+
+One step = the whole path over one batch: KVzap-Linear scores of every cached
+token (tcgen05), keep/evict mask, compaction of the survivors into 16-token
+pages, split-KV decode attention of the batch's query tokens. Workload: a
+Llama-3-8B-shaped layer (d_model 4096, 32 query / 8 KV heads, head_dim 128,
+batch 16, 8192 cached tokens, threshold at each head's 75th-percentile score,
+last 128 tokens always kept). Metric: decode tokens/s (batch / step time).
+
+Arms:
+  default            the CUDA path through the C ABI (device-resident inputs),
+                     plus an end-to-end leg with pinned host inputs copied in
+                     and the output copied back inside the timed region, plus
+                     the oracle timed on a bounded sample (cpu_baseline)
+  --impl reference   the oracle (float64 CPU reference) on host cores, on a
+                     bounded sample per step
+Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no data-path
+collective); rank 0 prints the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+if "--impl" in sys.argv and "reference" in sys.argv or "--cpu-baseline-only" in sys.argv:
+    # the oracle is timed single-threaded: every library below runs on one core
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "pruned-KV decode tokens/s at 1 GB300; effective HBM GB/s vs ~8 TB/s peak"
+UNIT = "tokens/s"
+WORKLOAD = dict(name="llama3_8b_layer", d_model=4096, n_q_heads=32, n_kv_heads=8, head_dim=128, batch=16,
+                n_pos=8192, prune_q=0.75, window=128)
+
+
+def config_desc(w=WORKLOAD):
+    return {
+        "workload": (f"{w['name']}: one layer, d_model {w['d_model']}, {w['n_q_heads']} q / {w['n_kv_heads']} kv "
+                     f"heads, head_dim {w['head_dim']}, batch {w['batch']}, context {w['n_pos']}, KVzap-Linear "
+                     f"scorer, threshold at each head's {int(w['prune_q'] * 100)}th-percentile score, last "
+                     f"{w['window']} tokens kept; step = score + mask + compact + decode attention"),
+        "global_batch": w["batch"],
+        "seq_len": w["n_pos"],
+        "parallelism": "replicas: each rank decodes its own batch",
+        "l2": "inputs larger than L2 (hidden states 1.07 GB, dense K/V 1.07 GB per step); no flush",
+    }
+
+
+# --------------------------------------------------------------------------- oracle sample (CPU)
+
+class OracleSample:
+    """One sequence of the workload drawn once on the host; run(rows) times the
+    oracle over the last `rows` cached positions of it (score, mask,
+    compaction, attention of the sequence's query heads) and returns (seconds,
+    sequences-equivalent = rows / n_pos)."""
+
+    def __init__(self, seed: int = 0, w=WORKLOAD):
+        import kvp_synth as syn
+        self.w = w
+        D, H, d, T = w["d_model"], w["n_kv_heads"], w["head_dim"], w["n_pos"]
+        G = w["n_q_heads"] // H
+        self.x, self.W = syn.linear_inputs(seed, T, D, H)
+        self.k, self.v = syn.kv_inputs(seed, 1, T, H, d)
+        self.q = syn.q_inputs(seed, 1, H * G, d)
+        self.tau = np.zeros((1, H), np.float32)  # the oracle's work does not depend on tau's value
+
+    def run(self, rows: int):
+        import oracle as orc
+        w = self.w
+        H, T = w["n_kv_heads"], w["n_pos"]
+        now, pos0 = T - 1, T - rows
+        t0 = time.perf_counter()
+        s = orc.score_linear(self.x[pos0:], self.W).reshape(1, rows, H)
+        exp = orc.mask_kvzap(s, self.tau, now, window=w["window"], pos0=pos0)[0]
+        mp = (rows + 15) // 16
+        c = orc.compact_dense(self.k[:, pos0:], self.v[:, pos0:], exp, now, 0, H * mp, mp)
+        orc.decode_attention(self.q, c, now)
+        return time.perf_counter() - t0, rows / T
+
+
+def run_cpu_baseline(budget_s: float):
+    """About `budget_s` seconds of oracle work, single-threaded."""
+    T = WORKLOAD["n_pos"]
+    sample = OracleSample()
+    t1, _ = sample.run(T)
+    total_t, total_seq, runs = t1, 1.0, 1
+    while total_t < budget_s and runs < 1000:
+        t, sq = sample.run(T)
+        total_t += t
+        total_seq += sq
+        runs += 1
+    return {"value": total_seq / total_t, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{runs} full sequences of the workload (one sequence's 8192 cached positions, drawn once "
+                      f"and re-run): float64 score, mask, compaction and attention of its query heads, one thread",
+            "seconds": total_t}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    T = WORKLOAD["n_pos"]
+    budget = 120.0
+    sample = OracleSample()
+    t1, _ = sample.run(T)
+    rows = int(max(64, min(T, budget / max(1, args.steps + args.warmup) / (t1 / T))))
+    for _ in range(args.warmup):
+        sample.run(rows)
+    total_t, total_seq = 0.0, 0.0
+    for _ in range(args.steps):
+        t, sq = sample.run(rows)
+        total_t += t
+        total_seq += sq
+    value = total_seq / total_t
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": config_desc(), "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"per step the last {rows} cached positions of one sequence ({rows / T:.4f} of "
+                                   f"a sequence's decode step): score, mask, compaction, attention in float64"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kvp_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9 and p[0].isdigit() and int(p[0]) == self.index:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def run_gpu(args, rank: int, world: int):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import kv_cache_pruning_gb300 as kvp
+
+    w = dict(WORKLOAD)
+    if args.batch:
+        w["batch"] = args.batch
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    B, T, H, Hq, d, D = w["batch"], w["n_pos"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"], w["d_model"]
+    n_tok = B * T
+    now = T - 1
+
+    # ---- seeded synthetic inputs, resident in HBM
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 * args.seed + rank)
+    x = torch.randn(n_tok, D, generator=g, device=dev).to(torch.bfloat16)
+    W = torch.randn(H, D, generator=g, device=dev) / math.sqrt(D)
+    K = torch.randn(B, T, H, d, generator=g, device=dev).to(torch.bfloat16)
+    V = torch.randn(B, T, H, d, generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn(B, Hq, d, generator=g, device=dev).to(torch.bfloat16)
+
+    # ---- buffers, sized once (keep-all capacity), reused by every step
+    max_pages = (T + 15) // 16
+    n_pages_cap = B * H * max_pages
+    cache = kvp.PagedKV.allocate(B, H, d, n_pages_cap, max_pages, device=dev)
+    scores = torch.empty(n_tok, H, dtype=torch.float32, device=dev)
+    expire = torch.empty(B, H, T, dtype=torch.int32, device=dev)
+    bits = torch.empty(B, H, (T + 31) // 32, dtype=torch.int32, device=dev)
+    count = torch.empty(B, H, dtype=torch.int32, device=dev)
+    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_s = torch.empty(kvp.kvp_score_workspace_bytes(0, n_tok, D, H), dtype=torch.uint8, device=dev)
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
+    ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+
+    # ---- threshold per (b, h): the 75th-percentile score (harness set-up, untimed)
+    kvp.kvp_score(x, W, out=scores, workspace=ws_s, status=status)
+    kth = int(math.floor(w["prune_q"] * (T - 1))) + 1
+    tau = torch.kthvalue(scores.view(B, T, H), kth, dim=1).values.contiguous()
+
+    stream = torch.cuda.current_stream(dev)
+    N_EV = 5  # event slots per step: before score, mask, compact, attention, after
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        kvp.kvp_score(x, W, out=scores, workspace=ws_s, status=status)
+        if evs is not None:
+            evs[1].record(stream)
+        kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=now, scores=scores, tau=tau,
+                     window=w["window"], expire=expire, keep_bits=bits, count=count)
+        if evs is not None:
+            evs[2].record(stream)
+        kvp.kvp_compact(K, V, expire, now, 0, cache, status=status, workspace=ws_c)
+        if evs is not None:
+            evs[3].record(stream)
+        kvp.kvp_decode_attn(q, cache, now, out=out, workspace=ws_a, status=status)
+        if evs is not None:
+            evs[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert status.item() == 0, kvp.status_string(status.item())
+    kept = int(count.sum().item())
+    surv_pages = int(((count + 15) // 16).sum().item())
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(N_EV)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        if dist:
+            tdist.barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            tdist.barrier()
+    clocks = clk.summary()
+    assert status.item() == 0, kvp.status_string(status.item())
+    total_ms = t_start.elapsed_time(t_end)
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(N_EV - 1)] for i in range(args.steps)])
+    k_ms = per.mean(axis=0)  # score, mask, compact, attention (per launch, ms)
+
+    # ---- algorithmic bytes (what the method must move)
+    x_b = n_tok * D * 2
+    score_b = x_b + H * D * 4 + n_tok * H * 4
+    mask_b = n_tok * H * 4 + B * H * 4 + B * H * T * 4 + B * H * ((T + 31) // 32) * 4 + B * H * 4
+    row_b = d * 2
+    compact_b = 2 * B * H * T * 4 + 2 * kept * 2 * row_b + kept * 4 + B * H * max_pages * 16 * 4 \
+        + B * H * max_pages * 4
+    attn_b = surv_pages * 16 * (2 * row_b + 4) + B * Hq * d * 2 + B * Hq * d * 4
+    step_b = score_b + mask_b + compact_b + attn_b
+    hbm, _, peak_kind = measured_peaks()
+    names = ["score", "mask", "compact", "decode_attn"]
+    kb = [score_b, mask_b, compact_b, attn_b]
+    kernels = {n: {"ms": float(k_ms[i]), "bytes": int(kb[i]), "GB_s": kb[i] / (k_ms[i] * 1e-3) / 1e9,
+                   "frac_of_hbm": kb[i] / (k_ms[i] * 1e-3) / 1e9 / hbm} for i, n in enumerate(names)}
+    dom = int(np.argmax(k_ms))
+    roofline = {"bound": "hbm", "kernel": names[dom], "achieved": kb[dom] / (k_ms[dom] * 1e-3) / 1e9,
+                "peak": hbm, "unit": "GB/s", "frac": kb[dom] / (k_ms[dom] * 1e-3) / 1e9 / hbm,
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                "traffic": args.traffic}
+    value = B * world / (ms_step * 1e-3)
+
+    # ---- end to end: pinned host inputs in, result out, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        Kh, Vh, qh = K.cpu().pin_memory(), V.cpu().pin_memory(), q.cpu().pin_memory()
+        Wh, tauh = W.cpu().pin_memory(), tau.cpu().pin_memory()
+        outh = torch.empty_like(out, device="cpu").pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (xh, Kh, Vh, qh, Wh, tauh))
+        d2h = outh.numel() * outh.element_size()
+
+        def e2e_step():
+            for dst, src in ((x, xh), (K, Kh), (V, Vh), (q, qh), (W, Wh), (tau, tauh)):
+                dst.copy_(src, non_blocking=True)
+            step()
+            outh.copy_(out, non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, args.e2e_steps))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist:
+            tdist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / n_e2e
+        if dist:
+            tt = torch.tensor([e_ms], device=dev)
+            tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": B * world / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms, "steps": n_e2e}
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-only",
+                            "--cpu-budget", str(args.cpu_budget)], capture_output=True, text=True, cwd=ROOT)
+        try:
+            cpu = json.loads(r.stdout.strip().splitlines()[-1])
+        except Exception:
+            cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch RNG, N(0,1) hidden states and K/V)",
+        "config": config_desc(w), "e2e": e2e, "gpu_launches": 8 * args.steps, "roofline": roofline,
+        "kernels": kernels, "effective_step_GB_s": step_b / (ms_step * 1e-3) / 1e9,
+        "kept_fraction": kept / (B * H * T), "clocks": clocks, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvp", choices=["kvp", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs only)")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-baseline-only", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture of this kernel")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.cpu_baseline_only:
+        print(json.dumps(run_cpu_baseline(args.cpu_budget)), flush=True)
+        return
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if world > 1 and args.impl != "reference":
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_gpu(args, rank, world)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

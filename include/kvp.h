@@ -226,26 +226,34 @@ KVP_API kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_dim,
  * over the slots i < count[b, h] of kv head h = j / (Hq / H) whose expire is
  * greater than `now`. An empty set gives a zero row.
  *
- * q          device bf16 [B, Hq, head_dim];  Hq a multiple of H, Hq/H in {1,2,4,8}
+ * The pages of all (b, h) are split evenly over the warps of a persistent
+ * grid (split-KV along pages, whatever the per-head survivor counts); partial
+ * softmax states of a (b, h) that spans several warps are merged in fp32 by
+ * the last of them to finish.
+ *
+ * q          device bf16 [B, Hq, head_dim];  Hq a multiple of H, Hq/H in {1,2,4,8},
+ *            B*H <= 4096
  * pools (n_pages_cap pages), expire_pool, page_table (width max_pages), count:
  *            as kvp_compact writes them. count is clamped to max_pages*16; a
  *            page id outside [0, n_pages_cap) records KVP_ERR_BOUNDS in
  *            `status` (may be NULL) and that page counts as empty.
  * scale      > 0, or 0 for 1/sqrt(head_dim)
- * out        device fp32 [B, Hq, head_dim]
- * pages_per_split  pages one CTA reads (0 = 16); the work is split along the
- *            pages and the partial softmax states are merged in fp32.
- * workspace  device, >= kvp_decode_attn_workspace_bytes(...)
+ * out        device fp32 [B, Hq, head_dim], 16-byte aligned
+ * grid_limit 0 = the default grid (one CTA per SM); > 0 caps the number of
+ *            CTAs (so the same inputs can be split differently)
+ * workspace  device, >= kvp_decode_attn_workspace_bytes(...), 16-byte aligned;
+ *            holds the partial states and per-(b, h) arrival counters (the
+ *            call clears the counters itself). Calls that share a workspace
+ *            must not overlap on the GPU.
  */
-KVP_API size_t kvp_decode_attn_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
-                                       int max_pages, int pages_per_split);
+KVP_API size_t kvp_decode_attn_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim);
 KVP_API kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, int head_dim,
-                           const void* q, const void* k_pool, const void* v_pool,
-                           const int32_t* expire_pool, int n_pages_cap,
-                           const int32_t* page_table, int max_pages,
-                           const int32_t* count, int now, float scale, float* out,
-                           int pages_per_split, void* workspace, size_t workspace_bytes,
-                           int32_t* status, void* stream);
+                                   const void* q, const void* k_pool, const void* v_pool,
+                                   const int32_t* expire_pool, int n_pages_cap,
+                                   const int32_t* page_table, int max_pages,
+                                   const int32_t* count, int now, float scale, float* out,
+                                   int grid_limit, void* workspace, size_t workspace_bytes,
+                                   int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

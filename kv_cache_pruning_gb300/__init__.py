@@ -74,7 +74,7 @@ _SIGS = {
                                _P, _P, _P, _S, _P, _P]),
     "kvp_append": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
                         _P, _P]),
-    "kvp_decode_attn_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
+    "kvp_decode_attn_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "kvp_decode_attn": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _I, _P, _S, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -293,25 +293,24 @@ def kvp_append(cache: PagedKV, k_new, v_new, pos, *, mode, score=None, tau=None,
 
 # --------------------------------------------------------------------------- attention
 
-def kvp_decode_attn_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, max_pages, pages_per_split=0) -> int:
-    return _lib.kvp_decode_attn_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, max_pages,
-                                                pages_per_split)
+def kvp_decode_attn_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim) -> int:
+    return _lib.kvp_decode_attn_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim)
 
 
-def kvp_decode_attn(q, cache: PagedKV, now, *, scale=0.0, out=None, pages_per_split=0, workspace=None,
+def kvp_decode_attn(q, cache: PagedKV, now, *, scale=0.0, out=None, grid_limit=0, workspace=None,
                     status=None, stream=None):
     """out[B, Hq, d] fp32 = attention of q [B, Hq, d] (bf16) over the slots of `cache` present at `now`."""
     B, Hq, d = q.shape
     H = cache.count.shape[1]
     if out is None:
         out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
-    need = kvp_decode_attn_workspace_bytes(B, Hq, H, d, cache.max_pages, pages_per_split)
+    need = kvp_decode_attn_workspace_bytes(B, Hq, H, d)
     ws = _ws(need, q.device, workspace)
     code = _lib.kvp_decode_attn(B, Hq, H, d, _ptr(q, torch.bfloat16, "q"), _ptr(cache.k_pool),
                                 _ptr(cache.v_pool), _ptr(cache.expire_pool, torch.int32), cache.n_pages_cap,
                                 _ptr(cache.page_table, torch.int32), cache.max_pages,
                                 _ptr(cache.count, torch.int32), now, float(scale), _ptr(out, torch.float32, "out"),
-                                pages_per_split, ws.data_ptr(), ws.numel() * ws.element_size(),
+                                grid_limit, ws.data_ptr(), ws.numel() * ws.element_size(),
                                 _ptr(status, torch.int32, "status", True), _stream(stream))
     _check("kvp_decode_attn", code)
     return out

@@ -1,28 +1,34 @@
-// kvp_decode_attn: split-KV single-query GQA attention over the compacted
-// pages (DMS article, "DMS 작동 방식" step 5: standard attention over the kept
-// cache).
+// kvp_decode_attn: single-query GQA attention over the compacted pages (DMS
+// article, "DMS 작동 방식" step 5: standard attention over the kept cache).
 //
-// Grid (split, kv head, batch); each CTA reads up to `pps` pages of one
-// (b, h). Its 4 warps take every 4th page; each warp owns a ring of NST
-// stages that its lane 0 fills with 1-D bulk copies (K page, V page, the
-// page's 16 expire values) completing on an mbarrier.
+// Persistent, page-balanced split-KV decode. All pages of all (b, h) form one
+// global list (b-major, h-minor, page order); every warp of the grid takes one
+// contiguous slice of it, so every warp streams the same number of pages
+// (+-1) whatever the per-head survivor counts are. A warp's lane 0 keeps
+// NST pages in flight with 1-D bulk copies (K page, V page, the page's 16
+// expire values) completing on per-stage mbarriers; all lanes compute.
 //
-// Lane layout per warp: LPR = D/8 lanes cover one row (8 bf16 = 16 bytes
-// each), RPS = 32/LPR rows are processed per step, RS = 16/RPS steps per page.
-// q . k partial sums of all G heads and RS steps are reduced across the LPR
-// lanes with a transposing butterfly (each exchange halves the values a lane
-// holds), then masked (slot < count and now < expire), and an fp32 online
-// softmax in base 2 (q is pre-scaled by scale*log2 e) updates the running
-// max, sum and the G x 8 output accumulators of the lane. The 4 warps' states
-// are merged in shared memory, one partial (acc, m, l) per (b, q head, split)
-// goes to the workspace, and a second kernel merges the splits.
+// Per page (LPR = D/8 lanes cover a row, 16 bytes each; RPS = 32/LPR rows per
+// step; RS = 16/RPS steps): q.k partial sums of the G query heads of the kv
+// head are reduced across the row's lanes with a transposing butterfly, masked
+// (slot < count and now < expire), and an fp32 base-2 online softmax updates
+// the running max, sum and G x 8 accumulators of each lane.
+//
+// When a warp's slice ends a (b, h) segment it either owns the whole (b, h)
+// (writes the output) or writes its partial (acc, m, l) to the workspace and
+// bumps the (b, h)'s counter; the warp that brings the counter to the number
+// of pieces merges them (log-sum-exp in fp32) and resets the counter. Nothing
+// ever waits on another warp.
 #include "kvp_common.cuh"
 
 namespace kvp {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kNst = 3;
+constexpr int kWarps = 8;       // warps per CTA
+constexpr int kNst = 3;         // pages in flight per warp
+constexpr int kMaxBH = 4096;    // (b, h) pairs whose page prefix fits in shared memory
+constexpr int kMaxCtas = 512;   // grid bound used to size the workspace
+constexpr int kThreads = kWarps * 32;
 
 template <int D, int G>
 struct AttnCfg {
@@ -35,14 +41,15 @@ struct AttnCfg {
   static constexpr int GL = LPR / G;
   static constexpr int PAGE_BYTES = kPage * D * 2;
   static constexpr int STAGE_BYTES = 2 * PAGE_BYTES + kPage * 4;
-  static constexpr int STAGES_BYTES = kWarps * kNst * STAGE_BYTES;
+  static constexpr int RING_BYTES = kWarps * kNst * STAGE_BYTES;
   static constexpr int PS_FLOATS = RPS * G * RS;  // per warp
   static constexpr int PS_BYTES = kWarps * PS_FLOATS * 4;
   static constexpr int BAR_BYTES = kWarps * kNst * 8;
-  static constexpr int MERGE_BYTES = kWarps * G * (D + 2) * 4;
-  static constexpr int SMEM = STAGES_BYTES + PS_BYTES + BAR_BYTES + MERGE_BYTES;
+  static constexpr int PREF_BYTES = (kMaxBH + 1) * 4;
+  static constexpr int SMEM = RING_BYTES + PS_BYTES + BAR_BYTES + PREF_BYTES;
   static_assert(G <= LPR, "group larger than lanes per row");
   static_assert(STAGE_BYTES % 16 == 0 && PS_BYTES % 16 == 0, "16-byte layout");
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct AttnParams {
@@ -52,10 +59,12 @@ struct AttnParams {
   const int32_t* expire_pool;
   const int32_t* page_table;
   const int32_t* count;
-  int H, Hq, max_pages, n_pages_cap, now, pps, n_splits;
+  int B, H, Hq, max_pages, n_pages_cap, now;
   float qscale;
-  float* part_acc;  // [B, Hq, n_splits, D]
-  float* part_ml;   // [B, Hq, n_splits, 2]
+  float* out;        // [B, Hq, D]
+  float* part_acc;   // [slots, G, D]
+  float* part_ml;    // [slots, G, 2]
+  int32_t* pieces;   // [B*H] arrival counters, zero at entry and exit
   int32_t* status;
 };
 
@@ -90,44 +99,110 @@ KVP_DEV void unpack8(const uint4& w, float (&f)[8]) {
   f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
 }
 
+KVP_DEV int clamp_count(const int32_t* count, int bh, int max_pages) {
+  return min(max(count[bh], 0), max_pages * kPage);
+}
+
+// Warp whose page slice holds global page g, for nw non-empty slices of np pages.
+KVP_DEV int warp_of(int g, int np, int nw) {
+  return static_cast<int>(((static_cast<int64_t>(g) + 1) * nw - 1) / np);
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnParams p) {
   using C = AttnCfg<D, G>;
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int bh = b * p.H + h;
-  const int cnt = min(max(p.count[bh], 0), p.max_pages * kPage);
-  const int npages = (cnt + kPage - 1) / kPage;
-  const int pg0 = split * p.pps;
-  if (pg0 >= npages) return;  // whole CTA: nothing of this (b, h) falls in this split
-  const int pg1 = min(npages, pg0 + p.pps);
-
   extern __shared__ __align__(128) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = p.B * p.H;
   uint8_t* ring = smem + warp * kNst * C::STAGE_BYTES;
-  float* p_s = reinterpret_cast<float*>(smem + C::STAGES_BYTES) + warp * C::PS_FLOATS;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES_BYTES + C::PS_BYTES) + warp * kNst;
-  float* merge = reinterpret_cast<float*>(smem + C::STAGES_BYTES + C::PS_BYTES + C::BAR_BYTES);
+  float* p_s = reinterpret_cast<float*>(smem + C::RING_BYTES) + warp * C::PS_FLOATS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES + C::PS_BYTES) + warp * kNst;
+  int* pref = reinterpret_cast<int*>(smem + C::RING_BYTES + C::PS_BYTES + C::BAR_BYTES);
 
-  const int rowsel = lane / C::LPR;
-  const int s = lane % C::LPR;
-
-  float qf[G][8];
+  // ---- page prefix over (b, h), identical in every CTA
+  {
+    __shared__ int wsum[kWarps];
+    __shared__ int carry;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < BH; base += kThreads) {
+      const int bh = base + tid;
+      const int np = bh < BH ? (clamp_count(p.count, bh, p.max_pages) + kPage - 1) / kPage : 0;
+      int incl = np;
 #pragma unroll
-  for (int i = 0; i < G; ++i) {
-    const uint4 w =
-        __ldg(reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(b) * p.Hq + h * G + i) * D) + s);
-    unpack8(w, qf[i]);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) qf[i][e] *= p.qscale;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      int before = carry;
+      for (int w = 0; w < warp; ++w) before += wsum[w];
+      if (bh < BH) pref[bh] = before + incl - np;
+      __syncthreads();
+      if (tid == 0) {
+        int t = 0;
+        for (int w = 0; w < kWarps; ++w) t += wsum[w];
+        carry += t;
+      }
+      __syncthreads();
+    }
+    if (tid == 0) pref[BH] = carry;
+    __syncthreads();
   }
+  const int NP = pref[BH];
 
-  const int first = pg0 + warp;
-  const int nk = first < pg1 ? (pg1 - first + kWarps - 1) / kWarps : 0;
-  const int32_t* ptab = p.page_table + static_cast<int64_t>(bh) * p.max_pages;
+  // ---- (b, h) without pages: zero output rows
+  for (int bh = blockIdx.x; bh < BH; bh += gridDim.x) {
+    if (pref[bh + 1] == pref[bh]) {
+      for (int i = tid; i < G * D; i += kThreads) p.out[static_cast<size_t>(bh) * G * D + i] = 0.f;
+    }
+  }
+  if (NP == 0) return;
 
-  auto issue = [&](int k) {
+  // ---- this warp's slice of the global page list
+  const int nw_all = gridDim.x * kWarps;
+  const int NW = min(nw_all, NP);  // every one of the first NW slices is non-empty
+  const int gw = blockIdx.x * kWarps + warp;
+  if (gw >= NW) return;
+  const int r0 = static_cast<int>(static_cast<int64_t>(gw) * NP / NW);
+  const int r1 = static_cast<int>((static_cast<int64_t>(gw) + 1) * NP / NW);
+  const int n_my = r1 - r0;
+
+  // first (b, h) of the slice: the one whose page range holds page r0
+  int lo = 0, hi = BH - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= r0) lo = mid; else hi = mid - 1;
+  }
+  int cbh = lo;  // consumer cursor
+  while (pref[cbh + 1] <= r0) ++cbh;
+
+  // Page ids of the slice, 32 per register: lane j of block b holds the id of
+  // slice page 32*b + j. Block b+1 is loaded when issuing enters block b, so
+  // every id is in a register about 32 pages before lane 0 needs it.
+  auto load_ids = [&](int blk) {
+    const int kk = blk * 32 + lane;
+    if (kk >= n_my) return -1;
+    const int g = r0 + kk;
+    int a = 0, b = BH - 1;
+    while (a < b) {
+      const int mid = (a + b + 1) >> 1;
+      if (pref[mid] <= g) a = mid; else b = mid - 1;
+    }
+    return static_cast<int>(p.page_table[static_cast<int64_t>(a) * p.max_pages + (g - pref[a])]);
+  };
+  int ids0 = load_ids(0), ids1 = load_ids(1);
+  auto page_id = [&](int k) {  // all lanes call this
+    const int blk = k >> 5;
+    const int v = __shfl_sync(0xffffffffu, (blk & 1) ? ids1 : ids0, k & 31);
+    if ((k & 31) == 0 && k > 0) {  // block blk - 1 is done: its register takes block blk + 1
+      if (blk & 1) ids0 = load_ids(blk + 1); else ids1 = load_ids(blk + 1);
+    }
+    return v;
+  };
+  auto issue = [&](int k, int64_t phys) {  // lane 0
     const int st = k % kNst;
-    const int64_t phys = ptab[first + k * kWarps];
     uint8_t* dst = ring + st * C::STAGE_BYTES;
     if (phys < 0 || phys >= p.n_pages_cap) {
       // inconsistent page table: no copy; the stage reads as an empty page
@@ -142,13 +217,52 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(const AttnParam
     bulk_g2s(dst + C::PAGE_BYTES, p.v_pool + phys * kPage * D, C::PAGE_BYTES, &bars[st]);
     bulk_g2s(dst + 2 * C::PAGE_BYTES, p.expire_pool + phys * kPage, kPage * 4, &bars[st]);
   };
-
   if (lane == 0) {
     for (int st = 0; st < kNst; ++st) mbar_init(&bars[st], 1);
     fence_mbar_init();
-    for (int k = 0; k < nk && k < kNst; ++k) issue(k);
   }
   __syncwarp();
+  for (int k = 0; k < n_my && k < kNst; ++k) {
+    const int pid = page_id(k);
+    if (lane == 0) issue(k, pid);
+  }
+  __syncwarp();
+
+  const int rowsel = lane / C::LPR;
+  const int s = lane % C::LPR;
+  const int idx_base = (C::V >= C::LPR) ? s * C::VL : s / C::DUP;
+  const int my_head = idx_base / C::RS;
+
+  auto load_q = [&](int bh, uint4 (&raw)[G]) {
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+      raw[i] = __ldg(reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(bh) * G + i) * D) + s);
+  };
+  auto next_bh = [&](int bh) {  // next (b, h) that has pages
+    int n = bh + 1;
+    while (n < BH && pref[n + 1] == pref[n]) ++n;
+    return n;
+  };
+
+  float qf[G][8];
+  uint4 qn[G];
+  {
+    uint4 qc[G];
+    load_q(cbh, qc);
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      unpack8(qc[i], qf[i]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qf[i][e] *= p.qscale;
+    }
+  }
+  int seg_end = min(pref[cbh + 1], r1);
+  int cnt = clamp_count(p.count, cbh, p.max_pages);
+  int cnt_next = 0;
+  if (seg_end < r1) {
+    load_q(next_bh(cbh), qn);
+    cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
+  }
 
   float m_run[G], l_run[G], acc[G][8];
 #pragma unroll
@@ -159,23 +273,21 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(const AttnParam
     for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
   }
 
-  const int idx_base = (C::V >= C::LPR) ? s * C::VL : s / C::DUP;
-  const int my_head = idx_base / C::RS;
-
-  for (int k = 0; k < nk; ++k) {
+  for (int k = 0; k < n_my; ++k) {
+    const int g = r0 + k;
     const int st = k % kNst;
     const bool ok = mbar_wait(&bars[st], static_cast<uint32_t>((k / kNst) & 1), nullptr, p.status);
     if (!__all_sync(0xffffffffu, ok)) {
       if (lane == 0) record_error(p.status, KVP_ERR_TIMEOUT);
-      break;
+      return;  // outputs of this call are unspecified after a timeout
     }
     const uint8_t* stage = ring + st * C::STAGE_BYTES;
     const uint16_t* Ks = reinterpret_cast<const uint16_t*>(stage);
     const uint16_t* Vs = reinterpret_cast<const uint16_t*>(stage + C::PAGE_BYTES);
     const int32_t* Es = reinterpret_cast<const int32_t*>(stage + 2 * C::PAGE_BYTES);
-    const int page = first + k * kWarps;
+    const int slot0 = (g - pref[cbh]) * kPage;
 
-    // ---- logits: partial dot products, then reduce across the row's lanes
+    // ---- logits
     float part[C::V];
 #pragma unroll
     for (int t = 0; t < C::RS; ++t) {
@@ -196,9 +308,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(const AttnParam
     float mloc = -INFINITY;
 #pragma unroll
     for (int u = 0; u < C::VL; ++u) {
-      const int idx = idx_base + u;
-      const int r = (idx % C::RS) * C::RPS + rowsel;
-      const bool valid = (page * kPage + r < cnt) && (p.now < Es[r]);
+      const int r = ((idx_base + u) % C::RS) * C::RPS + rowsel;
+      const bool valid = (slot0 + r < cnt) && (p.now < Es[r]);
       x[u] = valid ? part[u] : -INFINITY;
       mloc = fmaxf(mloc, x[u]);
     }
@@ -226,7 +337,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(const AttnParam
     }
     __syncwarp();
 
-    // ---- rescale and accumulate P . V for this lane's rows and columns
+    // ---- rescale, accumulate P . V
 #pragma unroll
     for (int i = 0; i < G; ++i) {
       l_run[i] *= alpha[i];
@@ -247,172 +358,238 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(const AttnParam
       }
     }
     __syncwarp();
-    if (lane == 0 && k + kNst < nk) {
-      fence_proxy_async();
-      issue(k + kNst);
+    if (k + kNst < n_my) {
+      const int pid = page_id(k + kNst);
+      if (lane == 0) {
+        fence_proxy_async();
+        issue(k + kNst, pid);
+      }
     }
-  }
 
-  // ---- combine the RPS row groups of the warp
+    // ---- end of a (b, h) segment of this slice
+    if (g + 1 == seg_end) {
+      // the running state is reset after this segment: combine the row groups in place
+      float (&lt)[G] = l_run;
+      float (&at)[G][8] = acc;
 #pragma unroll
-  for (int o = C::LPR; o < 32; o <<= 1) {
+      for (int o = C::LPR; o < 32; o <<= 1) {
 #pragma unroll
-    for (int i = 0; i < G; ++i) {
-      l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], o);
+        for (int i = 0; i < G; ++i) {
+          lt[i] += __shfl_xor_sync(0xffffffffu, lt[i], o);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[i][e] += __shfl_xor_sync(0xffffffffu, acc[i][e], o);
-    }
-  }
-  if (rowsel == 0) {
+          for (int e = 0; e < 8; ++e) at[i][e] += __shfl_xor_sync(0xffffffffu, at[i][e], o);
+        }
+      }
+      const bool whole = pref[cbh] >= r0 && pref[cbh + 1] <= r1;
+      if (whole) {
+        if (rowsel == 0) {
 #pragma unroll
-    for (int i = 0; i < G; ++i) {
-      float* mrow = merge + (warp * G + i) * (D + 2);
+          for (int i = 0; i < G; ++i) {
+            float4* o = reinterpret_cast<float4*>(p.out + (static_cast<size_t>(cbh) * G + i) * D + 8 * s);
+            const float inv = lt[i] > 0.f ? 1.f / lt[i] : 0.f;
+            o[0] = make_float4(at[i][0] * inv, at[i][1] * inv, at[i][2] * inv, at[i][3] * inv);
+            o[1] = make_float4(at[i][4] * inv, at[i][5] * inv, at[i][6] * inv, at[i][7] * inv);
+          }
+        }
+      } else {
+        const int w_first = warp_of(pref[cbh], NP, NW);
+        const int w_last = warp_of(pref[cbh + 1] - 1, NP, NW);
+        const size_t slot = static_cast<size_t>(gw) + cbh;
+        if (rowsel == 0) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mrow[8 * s + e] = acc[i][e];
-      if (s == 0) {
-        mrow[D] = m_run[i];
-        mrow[D + 1] = l_run[i];
+          for (int i = 0; i < G; ++i) {
+            float4* o = reinterpret_cast<float4*>(p.part_acc + (slot * G + i) * D + 8 * s);
+            o[0] = make_float4(at[i][0], at[i][1], at[i][2], at[i][3]);
+            o[1] = make_float4(at[i][4], at[i][5], at[i][6], at[i][7]);
+          }
+        }
+        if (lane < G) {
+          float mm = m_run[0], ll = lt[0];
+#pragma unroll
+          for (int i = 1; i < G; ++i)
+            if (lane == i) {
+              mm = m_run[i];
+              ll = lt[i];
+            }
+          p.part_ml[(slot * G + lane) * 2] = mm;
+          p.part_ml[(slot * G + lane) * 2 + 1] = ll;
+        }
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&p.pieces[cbh], 1) == (w_last - w_first);
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          // every piece of this (b, h) is written: merge them (lanes across
+          // pieces for the max and the sum, across columns for the values)
+          __threadfence();
+          const int npc = w_last - w_first + 1;
+          const size_t s0 = static_cast<size_t>(w_first) + cbh;
+          for (int i = 0; i < G; ++i) {
+            float M = -1e30f;
+            for (int c0 = 0; c0 < npc; c0 += 32)
+              if (c0 + lane < npc) M = fmaxf(M, __ldcg(p.part_ml + ((s0 + c0 + lane) * G + i) * 2));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            float L = 0.f;
+            for (int c0 = 0; c0 < npc; c0 += 32)
+              if (c0 + lane < npc) {
+                const float* ml = p.part_ml + ((s0 + c0 + lane) * G + i) * 2;
+                L = fmaf(exp2f(__ldcg(ml) - M), __ldcg(ml + 1), L);
+              }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            float A[D / 32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) A[c] = 0.f;
+#pragma unroll 4
+            for (int pc = 0; pc < npc; ++pc) {
+              const size_t sl = (s0 + pc) * G + i;
+              const float w = exp2f(__ldcg(p.part_ml + sl * 2) - M);
+#pragma unroll
+              for (int c = 0; c < D / 32; ++c) A[c] = fmaf(w, __ldcg(p.part_acc + sl * D + lane + 32 * c), A[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) p.out[(static_cast<size_t>(cbh) * G + i) * D + lane + 32 * c] = A[c] * inv;
+          }
+          if (lane == 0) p.pieces[cbh] = 0;
+        }
+      }
+      // next segment
+      if (g + 1 < r1) {
+        cbh = next_bh(cbh);
+        seg_end = min(pref[cbh + 1], r1);
+        cnt = cnt_next;
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          unpack8(qn[i], qf[i]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) qf[i][e] *= p.qscale;
+        }
+        if (seg_end < r1) {
+          load_q(next_bh(cbh), qn);
+          cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
+        }
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          m_run[i] = -1e30f;
+          l_run[i] = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+        }
       }
     }
   }
-  __syncthreads();
-
-  // ---- merge the warps into this split's partial
-  for (int idx = threadIdx.x; idx < G * D; idx += kWarps * 32) {
-    const int i = idx / D, e = idx - i * D;
-    float M = -1e30f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, merge[(w * G + i) * (D + 2) + D]);
-    float L = 0.f, A = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float* mrow = merge + (w * G + i) * (D + 2);
-      const float sc = exp2f(mrow[D] - M);
-      L = fmaf(sc, mrow[D + 1], L);
-      A = fmaf(sc, mrow[e], A);
-    }
-    const size_t o = (static_cast<size_t>(b) * p.Hq + h * G + i) * p.n_splits + split;
-    p.part_acc[o * D + e] = A;
-    if (e == 0) {
-      p.part_ml[o * 2] = M;
-      p.part_ml[o * 2 + 1] = L;
-    }
-  }
 }
 
-// out[b, j] = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s over the splits
-// that hold pages of (b, h = j / G); zero when nothing is present.
-__global__ void attn_merge_kernel(int H, int Hq, int G, int D, int pps, int n_splits, int max_pages,
-                                  const int32_t* __restrict__ count,
-                                  const float* __restrict__ part_acc, const float* __restrict__ part_ml,
-                                  float* __restrict__ out) {
-  const int j = blockIdx.x, b = blockIdx.y;
-  const int h = j / G;
-  const int cnt = min(max(count[b * H + h], 0), max_pages * kPage);
-  const int npages = (cnt + kPage - 1) / kPage;
-  const int ns = min(n_splits, (npages + pps - 1) / pps);
-  const size_t base = (static_cast<size_t>(b) * Hq + j) * n_splits;
-  float M = -1e30f;
-  for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, part_ml[(base + sp) * 2]);
-  for (int e = threadIdx.x; e < D; e += blockDim.x) {
-    float L = 0.f, A = 0.f;
-    for (int sp = 0; sp < ns; ++sp) {
-      const float sc = exp2f(part_ml[(base + sp) * 2] - M);
-      L = fmaf(sc, part_ml[(base + sp) * 2 + 1], L);
-      A = fmaf(sc, part_acc[(base + sp) * D + e], A);
-    }
-    out[(static_cast<size_t>(b) * Hq + j) * D + e] = L > 0.f ? A / L : 0.f;
-  }
+// Grid of the persistent kernel on this process's device: one CTA per SM
+// times the CTAs an SM holds, computed once (with the shared-memory opt-in).
+template <int D, int G>
+int attn_grid() {
+  static const int grid = [] {
+    using C = AttnCfg<D, G>;
+    auto kern = attn_decode_kernel<D, G>;
+    int dev = 0, nsm = 0, occ = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess ||
+        cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, C::SMEM) != cudaSuccess || occ <= 0)
+      return 0;
+    return nsm * occ < kMaxCtas ? nsm * occ : kMaxCtas;
+  }();
+  return grid;
 }
 
 template <int D, int G>
-kvp_status launch_attn(const AttnParams& p, int B, cudaStream_t st) {
+kvp_status launch_attn(const AttnParams& p, int grid_limit, cudaStream_t st) {
   using C = AttnCfg<D, G>;
-  auto kern = attn_split_kernel<D, G>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-    return KVP_ERR_CUDA;
-  kern<<<dim3(p.n_splits, p.H, B), kWarps * 32, C::SMEM, st>>>(p);
+  int grid = attn_grid<D, G>();
+  if (grid <= 0) return KVP_ERR_CUDA;
+  if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
+  attn_decode_kernel<D, G><<<grid, kThreads, C::SMEM, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
 template <int D>
-kvp_status dispatch_g(const AttnParams& p, int B, int G, cudaStream_t st) {
+kvp_status dispatch_g(const AttnParams& p, int G, int grid_limit, cudaStream_t st) {
   switch (G) {
-    case 1: return launch_attn<D, 1>(p, B, st);
-    case 2: return launch_attn<D, 2>(p, B, st);
-    case 4: return launch_attn<D, 4>(p, B, st);
-    case 8: return launch_attn<D, 8>(p, B, st);
+    case 1: return launch_attn<D, 1>(p, grid_limit, st);
+    case 2: return launch_attn<D, 2>(p, grid_limit, st);
+    case 4: return launch_attn<D, 4>(p, grid_limit, st);
+    case 8: return launch_attn<D, 8>(p, grid_limit, st);
     default: return KVP_ERR_UNSUPPORTED;
   }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-int pps_or_default(int pps) { return pps > 0 ? pps : 16; }
+
+// workspace: arrival counters [BH] (rounded to 16 bytes), then part_ml
+// [slots, G, 2], then part_acc [slots, G, D]; slots = warps of the largest
+// grid + BH (a slice's piece of (b, h) goes to slot warp + b*H + h).
+size_t ws_counter_bytes(int BH) { return (static_cast<size_t>(BH) * 4 + 15) / 16 * 16; }
+size_t ws_slots(int BH) { return static_cast<size_t>(kMaxCtas) * kWarps + BH; }
 
 }  // namespace
 }  // namespace kvp
 
 using namespace kvp;
 
-extern "C" size_t kvp_decode_attn_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
-                                                  int max_pages, int pages_per_split) {
-  if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || max_pages < 0) return 0;
-  const int pps = pps_or_default(pages_per_split);
-  const size_t ns = max_pages > 0 ? (max_pages + pps - 1) / pps : 1;
-  return static_cast<size_t>(batch) * n_q_heads * ns * (head_dim + 2) * sizeof(float);
+extern "C" size_t kvp_decode_attn_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim) {
+  if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || n_q_heads % n_kv_heads) return 0;
+  const int BH = batch * n_kv_heads;
+  const int G = n_q_heads / n_kv_heads;
+  const size_t slots = ws_slots(BH);
+  return ws_counter_bytes(BH) + slots * G * 2 * sizeof(float) + slots * G * head_dim * sizeof(float);
 }
 
 extern "C" kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q,
                                       const void* k_pool, const void* v_pool, const int32_t* expire_pool,
                                       int n_pages_cap, const int32_t* page_table, int max_pages,
-                                      const int32_t* count, int now, float scale, float* out, int pages_per_split,
+                                      const int32_t* count, int now, float scale, float* out, int grid_limit,
                                       void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
-  if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_pages < 0 || pages_per_split < 0 || n_pages_cap < 0)
+  if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_pages < 0 || grid_limit < 0 || n_pages_cap < 0)
     return KVP_ERR_INVALID;
-  if (static_cast<int64_t>(max_pages) * kPage > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
   if (n_q_heads % n_kv_heads != 0) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(max_pages) * kPage > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
   const int G = n_q_heads / n_kv_heads;
   if (head_dim != 64 && head_dim != 128) return KVP_ERR_UNSUPPORTED;
   if (G != 1 && G != 2 && G != 4 && G != 8) return KVP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(batch) * n_kv_heads > kMaxBH) return KVP_ERR_UNSUPPORTED;
   if (!(scale >= 0.f)) return KVP_ERR_INVALID;
   if (q == nullptr || k_pool == nullptr || v_pool == nullptr || expire_pool == nullptr || page_table == nullptr ||
       count == nullptr || out == nullptr)
     return KVP_ERR_INVALID;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(expire_pool)) return KVP_ERR_ALIGN;
-  const size_t need =
-      kvp_decode_attn_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, max_pages, pages_per_split);
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(expire_pool) || !aligned16(out))
+    return KVP_ERR_ALIGN;
+  const size_t need = kvp_decode_attn_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim);
   if (workspace == nullptr || workspace_bytes < need) return KVP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return KVP_ERR_ALIGN;
-  if (static_cast<int64_t>(batch) * n_kv_heads > 65535 * 65535LL || n_kv_heads > 65535 || batch > 65535)
-    return KVP_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int pps = pps_or_default(pages_per_split);
-  const int ns = max_pages > 0 ? (max_pages + pps - 1) / pps : 1;
+  const int BH = batch * n_kv_heads;
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(head_dim));
-  float* part_acc = static_cast<float*>(workspace);
-  float* part_ml = part_acc + static_cast<size_t>(batch) * n_q_heads * ns * head_dim;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* pieces = reinterpret_cast<int32_t*>(ws);
+  float* part_ml = reinterpret_cast<float*>(ws + ws_counter_bytes(BH));
+  float* part_acc = part_ml + ws_slots(BH) * G * 2;
+  if (cudaMemsetAsync(pieces, 0, static_cast<size_t>(BH) * 4, st) != cudaSuccess) return KVP_ERR_CUDA;
   AttnParams p{static_cast<const uint16_t*>(q),
                static_cast<const uint16_t*>(k_pool),
                static_cast<const uint16_t*>(v_pool),
                expire_pool,
                page_table,
                count,
+               batch,
                n_kv_heads,
                n_q_heads,
                max_pages,
                n_pages_cap,
                now,
-               pps,
-               ns,
                sc * 1.4426950408889634f,
+               out,
                part_acc,
                part_ml,
+               pieces,
                status};
-  if (max_pages > 0) {
-    const kvp_status s = head_dim == 128 ? dispatch_g<128>(p, batch, G, st) : dispatch_g<64>(p, batch, G, st);
-    if (s != KVP_OK) return s;
-  }
-  attn_merge_kernel<<<dim3(n_q_heads, batch), head_dim, 0, st>>>(n_kv_heads, n_q_heads, G, head_dim, pps, ns, max_pages, count,
-                                                                 part_acc, part_ml, out);
-  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+  return head_dim == 128 ? dispatch_g<128>(p, G, grid_limit, st) : dispatch_g<64>(p, G, grid_limit, st);
 }

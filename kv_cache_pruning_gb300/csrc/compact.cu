@@ -7,18 +7,20 @@
 // and is present at step `now` iff now < expire.
 //
 // Compaction (DeInfer summary, "나. 페이지드 KV 캐시 및 CUDA Graph 통합"):
-// a preparation pass counts the present entries of each 1024-entry chunk of
-// every (b, h) (warp ballots), a single-CTA scan turns the counts into the
-// remapping offsets and the page base of every (b, h), and a copy pass
-// re-derives each entry's slot from a block-wide prefix sum of ballots and
-// moves its K and V rows with 16-byte vector loads and stores.
+// a preparation pass counts the present entries of each 128-entry segment of
+// every (b, h) (one warp per segment, ballots), a single-CTA scan turns the
+// counts into the remapping offsets and the page base of every (b, h), and a
+// copy pass (again one warp per segment, no block-level synchronisation)
+// re-derives each entry's slot from its segment offset plus a ballot prefix
+// and moves its K and V rows with 16-byte vector loads and stores, 8 rows'
+// loads in flight per lane before their stores.
 #include "kvp_common.cuh"
 
 namespace kvp {
 namespace {
 
-constexpr int kChunk = 1024;        // entries per counting / copying CTA
-constexpr int kCopyThreads = 256;   // 8 warps; 256 entries per round
+constexpr int kSeg = 128;           // entries per warp segment
+constexpr int kWarpsPerCta = 4;     // segments per CTA in the count and copy passes
 
 KVP_DEV int32_t expire_kvzap(float s, float tau, int pos, int window) {
   return (s >= tau) ? kNever : pos + window;  // NaN compares false: treated as low
@@ -70,8 +72,10 @@ __global__ void __launch_bounds__(1024) mask_kernel(int mode, int H, int n_pos, 
 }
 
 // ------------------------------------------------------------------ sources
-// Dense source: entry t of (b, h) is row (b, t, h) of K/V, present iff
-// now < expire[b, h, t].
+// A source yields, for entry t of one (b, h): its expire value, the index of
+// its K/V row (row address = base + row * stride elements) and its position.
+//
+// Dense source: entry t is row (b, t, h) of K/V, present iff now < expire[b, h, t].
 struct DenseSrc {
   const uint16_t* k;
   const uint16_t* v;
@@ -79,16 +83,23 @@ struct DenseSrc {
   const int32_t* expire;  // [B, H, n]
   int H;
   int n;                  // entries per (b, h)
-  KVP_DEV int length(int) const { return n; }
-  KVP_DEV int32_t expire_of(int bh, int t) const { return expire[static_cast<int64_t>(bh) * n + t]; }
-  KVP_DEV int position_of(int, int t) const { return t; }
-  KVP_DEV const uint16_t* k_row(int bh, int t) const {
+  struct View {
+    const uint16_t* kb;
+    const uint16_t* vb;
+    int64_t stride;
+    const int32_t* exp;
+    int n;
+    KVP_DEV int length() const { return n; }
+    KVP_DEV int32_t expire_row(int t, int64_t& row) const {
+      row = t;
+      return exp[t];
+    }
+    KVP_DEV int position_of(int t) const { return t; }
+  };
+  KVP_DEV View view(int bh) const {
     const int b = bh / H, h = bh - b * H;
-    return k + b * sb + t * st + h * sh;
-  }
-  KVP_DEV const uint16_t* v_row(int bh, int t) const {
-    const int b = bh / H, h = bh - b * H;
-    return v + b * sb + t * st + h * sh;
+    const int64_t off = b * sb + h * sh;
+    return View{k + off, v + off, st, expire + static_cast<int64_t>(bh) * n, n};
   }
 };
 
@@ -106,64 +117,75 @@ struct PagedSrc {
   int n_pages_cap;
   int d;
   int32_t* status;
-  KVP_DEV int length(int bh) const { return min(max(count[bh], 0), max_pages * kPage); }
-  KVP_DEV int64_t row_index(int bh, int j) const {
-    const int pg = page_table[static_cast<int64_t>(bh) * max_pages + (j >> 4)];
-    if (pg < 0 || pg >= n_pages_cap) return -1;
-    return static_cast<int64_t>(pg) * kPage + (j & 15);
-  }
-  KVP_DEV int32_t expire_of(int bh, int j) const {
-    const int64_t r = row_index(bh, j);
-    if (r < 0) {
-      record_error(status, KVP_ERR_BOUNDS);
-      return 0;
+  struct View {
+    const uint16_t* kb;
+    const uint16_t* vb;
+    int64_t stride;
+    const int32_t* expire_pool;
+    const int32_t* ptab;
+    const int32_t* remap;
+    int n, n_pages_cap;
+    int32_t* status;
+    KVP_DEV int length() const { return n; }
+    KVP_DEV int32_t expire_row(int j, int64_t& row) const {
+      const int pg = ptab[j >> 4];
+      if (pg < 0 || pg >= n_pages_cap) {
+        record_error(status, KVP_ERR_BOUNDS);
+        row = -1;
+        return 0;
+      }
+      row = static_cast<int64_t>(pg) * kPage + (j & 15);
+      return expire_pool[row];
     }
-    return expire_pool[r];
+    KVP_DEV int position_of(int j) const { return remap[j]; }
+  };
+  KVP_DEV View view(int bh) const {
+    const int n = min(max(count[bh], 0), max_pages * kPage);
+    return View{k, v, d, expire_pool, page_table + static_cast<int64_t>(bh) * max_pages,
+                remap + static_cast<int64_t>(bh) * max_pages * kPage, n, n_pages_cap, status};
   }
-  KVP_DEV int position_of(int bh, int j) const {
-    return remap[static_cast<int64_t>(bh) * max_pages * kPage + j];
-  }
-  KVP_DEV const uint16_t* k_row(int bh, int j) const { return k + row_index(bh, j) * d; }
-  KVP_DEV const uint16_t* v_row(int bh, int j) const { return v + row_index(bh, j) * d; }
 };
 
-// Workspace layout (int32): chunk counts [BH*NC], chunk offsets [BH*NC],
+// Workspace layout (int32): segment counts [BH*NS], segment offsets [BH*NS],
 // page base [BH], flag [1] (1 = budget ok).
 struct CompactWs {
-  int32_t* chunk_cnt;
-  int32_t* chunk_off;
+  int32_t* seg_cnt;
+  int32_t* seg_off;
   int32_t* base;
   int32_t* ok;
 };
-size_t compact_ws_bytes(int BH, int NC) { return (static_cast<size_t>(2) * BH * NC + BH + 1) * sizeof(int32_t); }
-CompactWs carve(void* ws, int BH, int NC) {
+size_t compact_ws_bytes(int BH, int NS) { return (static_cast<size_t>(2) * BH * NS + BH + 1) * sizeof(int32_t); }
+CompactWs carve(void* ws, int BH, int NS) {
   int32_t* p = static_cast<int32_t*>(ws);
-  return CompactWs{p, p + static_cast<size_t>(BH) * NC, p + static_cast<size_t>(2) * BH * NC,
-                   p + static_cast<size_t>(2) * BH * NC + BH};
+  const size_t n = static_cast<size_t>(BH) * NS;
+  return CompactWs{p, p + n, p + 2 * n, p + 2 * n + BH};
 }
+int n_segments(int n) { return n > 0 ? (n + kSeg - 1) / kSeg : 1; }
 
-// Preparation, part 1: present entries per chunk.
+// Preparation, part 1: present entries per segment (one warp each).
 template <class Src>
-__global__ void __launch_bounds__(256) count_kernel(Src src, int now, int NC, int32_t* __restrict__ chunk_cnt) {
-  const int bh = blockIdx.y, c = blockIdx.x;
-  const int n = src.length(bh);
-  const int lo = c * kChunk;
+__global__ void __launch_bounds__(kWarpsPerCta * 32) count_kernel(Src src, int now, int NS,
+                                                                   int32_t* __restrict__ seg_cnt) {
+  const int bh = blockIdx.y;
+  const int sg = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (sg >= NS) return;
+  const auto sv = src.view(bh);
+  const int lo = sg * kSeg, hi = min(lo + kSeg, sv.length());
   int kept = 0;
-  for (int t = lo + threadIdx.x; t < lo + kChunk && t < n; t += blockDim.x) kept += (now < src.expire_of(bh, t));
-  kept = __reduce_add_sync(0xffffffffu, kept);
-  __shared__ int sums[8];
-  if ((threadIdx.x & 31) == 0) sums[threadIdx.x >> 5] = kept;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int total = 0;
-    for (int w = 0; w < 8; ++w) total += sums[w];
-    chunk_cnt[static_cast<int64_t>(bh) * NC + c] = total;
+  for (int t = lo + lane; t < hi; t += 32) {
+    int64_t row;
+    const int32_t e = sv.expire_row(t, row);
+    kept += (row >= 0 && now < e);
   }
+  kept = __reduce_add_sync(0xffffffffu, kept);
+  if (lane == 0) seg_cnt[static_cast<int64_t>(bh) * NS + sg] = kept;
 }
 
-// Preparation, part 2 (one CTA): per-(b, h) counts, chunk offsets, page bases
-// in (b-major, h-minor) order, budget checks.
-__global__ void __launch_bounds__(1024) scan_kernel(int BH, int NC, int reserve, int max_pages, int n_pages_cap,
+// Preparation, part 2 (one CTA): per-(b, h) counts and segment offsets (one
+// warp per (b, h) at a time), then page bases in (b-major, h-minor) order and
+// the budget checks.
+__global__ void __launch_bounds__(1024) scan_kernel(int BH, int NS, int reserve, int max_pages, int n_pages_cap,
                                                     CompactWs ws, int32_t* __restrict__ count,
                                                     int32_t* __restrict__ status) {
   __shared__ int warp_tot[32];
@@ -174,21 +196,30 @@ __global__ void __launch_bounds__(1024) scan_kernel(int BH, int NC, int reserve,
     carry_s = 0;
     bad_s = 0;
   }
+  for (int bh = warp; bh < BH; bh += 32) {
+    int run = 0;
+    for (int s0 = 0; s0 < NS; s0 += 32) {
+      const int sg = s0 + lane;
+      const int c = sg < NS ? ws.seg_cnt[static_cast<int64_t>(bh) * NS + sg] : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (sg < NS) ws.seg_off[static_cast<int64_t>(bh) * NS + sg] = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) count[bh] = run;
+  }
   __syncthreads();
   for (int b0 = 0; b0 < BH; b0 += 1024) {
     const int bh = b0 + tid;
     int pages = 0;
     if (bh < BH) {
-      int cnt = 0;
-      for (int c = 0; c < NC; ++c) {
-        ws.chunk_off[static_cast<int64_t>(bh) * NC + c] = cnt;
-        cnt += ws.chunk_cnt[static_cast<int64_t>(bh) * NC + c];
-      }
-      count[bh] = cnt;
-      pages = (cnt + reserve + kPage - 1) / kPage;
+      pages = (count[bh] + reserve + kPage - 1) / kPage;
       if (pages > max_pages) atomicExch(&bad_s, 1);
     }
-    // block-wide exclusive scan of pages
     int incl = pages;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -221,38 +252,50 @@ __global__ void __launch_bounds__(1024) scan_kernel(int BH, int NC, int reserve,
   }
 }
 
-// Copy pass: one CTA per (chunk, b*H + h).
+// Copy pass: one warp per 128-entry segment of one (b, h); grid
+// (ceil(NS / 4), B*H). The warp first lists the segment's present entries
+// (source row indices, in order) in shared memory and writes their expire and
+// remap entries, then moves their K and V rows, kLoads passes of loads in
+// flight before the matching stores.
 template <int D, class Src>
-__global__ void __launch_bounds__(kCopyThreads) scatter_kernel(Src src, int now, int NC, int reserve, int max_pages,
-                                                               CompactWs ws, const int32_t* __restrict__ count,
-                                                               uint16_t* __restrict__ k_pool,
-                                                               uint16_t* __restrict__ v_pool,
-                                                               int32_t* __restrict__ expire_pool,
-                                                               int32_t* __restrict__ page_table,
-                                                               int32_t* __restrict__ remap) {
+__global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int now, int NS, int reserve,
+                                                                     int max_pages, CompactWs ws,
+                                                                     const int32_t* __restrict__ count,
+                                                                     uint16_t* __restrict__ k_pool,
+                                                                     uint16_t* __restrict__ v_pool,
+                                                                     int32_t* __restrict__ expire_pool,
+                                                                     int32_t* __restrict__ page_table,
+                                                                     int32_t* __restrict__ remap) {
   constexpr int VPR = D / 8;            // 16-byte vectors per row
-  constexpr int EPP = 32 / (2 * VPR);   // entries copied per warp pass (K and V rows)
+  constexpr int EPP = 32 / (2 * VPR);   // entries per warp pass (a K and a V row each)
+  constexpr int kLoads = 8;             // passes whose loads are issued before their stores
+  __shared__ int64_t lst_all[kWarpsPerCta][kSeg];
   if (ws.ok[0] == 0) return;
-  const int bh = blockIdx.y, c = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = src.length(bh);
+  const int bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const int sg = blockIdx.x * kWarpsPerCta + warp;
+  const int lane = threadIdx.x & 31;
+  if (sg >= NS) return;
+  int64_t* lst = lst_all[warp];
+  const auto sv = src.view(bh);
+  const int n = sv.length();
   const int cnt = count[bh];
   const int base = ws.base[bh];
   const int pages = (cnt + reserve + kPage - 1) / kPage;
   const int64_t cap = static_cast<int64_t>(max_pages) * kPage;
+  int32_t* remap_bh = remap + bh * cap;
 
-  // page table row and remap tail, split across this (b, h)'s chunk CTAs
+  // this segment's share of the page-table row, the remap tail and the
+  // zeroing of unused rows in the (b, h)'s last pages
   {
-    const int seg = (max_pages + NC - 1) / NC;
-    for (int p = c * seg + threadIdx.x; p < min(max_pages, (c + 1) * seg); p += blockDim.x)
+    const int seg = (max_pages + NS - 1) / NS;
+    for (int p = sg * seg + lane; p < min(max_pages, (sg + 1) * seg); p += 32)
       page_table[static_cast<int64_t>(bh) * max_pages + p] = p < pages ? base + p : -1;
-    const int64_t rseg = (cap + NC - 1) / NC;
-    for (int64_t j = c * rseg + threadIdx.x; j < min(cap, (c + 1) * rseg); j += blockDim.x)
-      if (j >= cnt) remap[bh * cap + j] = -1;
-  }
-  // zero the unused rows of this (b, h)'s pages
-  if (c == 0) {
-    for (int j = cnt + warp; j < pages * kPage; j += kCopyThreads / 32) {
+    const int64_t rseg = (cap + NS - 1) / NS;
+    const int64_t rlo = sg * rseg > cnt ? sg * rseg : static_cast<int64_t>(cnt);
+    for (int64_t j = rlo + lane; j < min(cap, (sg + 1) * rseg); j += 32) remap_bh[j] = -1;
+    const int zseg = (pages * kPage - cnt + NS - 1) / NS;
+    for (int j = cnt + sg * zseg; j < min(pages * kPage, cnt + (sg + 1) * zseg); ++j) {
       const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
       if (lane < VPR) {
         reinterpret_cast<uint4*>(k_pool + row * D)[lane] = make_uint4(0, 0, 0, 0);
@@ -262,71 +305,51 @@ __global__ void __launch_bounds__(kCopyThreads) scatter_kernel(Src src, int now,
     }
   }
 
-  __shared__ int warp_cnt[kCopyThreads / 32];
-  int running = ws.chunk_off[static_cast<int64_t>(bh) * NC + c];
-  const int lo = c * kChunk, hi = min(lo + kChunk, n);
-  for (int r0 = lo; r0 < hi; r0 += kCopyThreads) {
-    const int t = r0 + threadIdx.x;
+  // list the present entries; write their expire and remap entries
+  const int slot0 = ws.seg_off[static_cast<int64_t>(bh) * NS + sg];
+  const int lo = sg * kSeg, hi = min(lo + kSeg, n);
+  int nk = 0;
+  for (int r0 = lo; r0 < hi; r0 += 32) {
+    const int t = r0 + lane;
+    int64_t row = -1;
     int32_t e = 0;
-    bool keep = false;
-    if (t < hi) {
-      e = src.expire_of(bh, t);
-      keep = now < e;
-    }
+    if (t < hi) e = sv.expire_row(t, row);
+    const bool keep = (t < hi) && (row >= 0) && (now < e);
     const unsigned bal = __ballot_sync(0xffffffffu, keep);
-    if (lane == 0) warp_cnt[warp] = __popc(bal);
-    __syncthreads();
-    int woff = 0, rtot = 0;
-#pragma unroll
-    for (int w = 0; w < kCopyThreads / 32; ++w) {
-      const int x = warp_cnt[w];
-      woff += (w < warp) ? x : 0;
-      rtot += x;
-    }
-    __syncthreads();
-    const int slot0 = running + woff;  // slot of this warp's first kept entry
     if (keep) {
-      const int j = slot0 + __popc(bal & ((1u << lane) - 1u));
-      const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
-      expire_pool[row] = e;
-      remap[bh * cap + j] = src.position_of(bh, t);
+      const int i = nk + __popc(bal & ((1u << lane) - 1u));
+      const int j = slot0 + i;
+      lst[i] = row;
+      expire_pool[static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15)] = e;
+      remap_bh[j] = sv.position_of(t);
     }
-    // move the K and V rows: EPP entries per pass, one 16-byte vector per
-    // lane; up to kBatch passes are loaded before any is stored
-    constexpr int kBatch = 8;
-    const int sub = lane / (2 * VPR);
-    const int vec = lane % (2 * VPR);
-    const bool is_v = vec >= VPR;
-    const int vi = is_v ? vec - VPR : vec;
-    unsigned m = bal;
-    int done = 0;
-    while (m) {
-      uint4 val[kBatch];
-      int js[kBatch];
+    nk += __popc(bal);
+  }
+  __syncwarp();
+
+  // move the rows
+  const int sub = lane / (2 * VPR);
+  const int vec = lane % (2 * VPR);
+  const bool is_v = vec >= VPR;
+  const int vi = is_v ? vec - VPR : vec;
+  const uint16_t* sbase = is_v ? sv.vb : sv.kb;
+  uint16_t* dbase = is_v ? v_pool : k_pool;
+  for (int i0 = 0; i0 < nk; i0 += kLoads * EPP) {
+    uint4 val[kLoads];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        unsigned mm = m;
-        for (int q = 0; q < sub; ++q) mm &= mm - 1u;  // the sub-th remaining entry
-        js[u] = -1;
-        if (mm) {
-          const int ts = r0 + warp * 32 + (__ffs(mm) - 1);
-          const uint16_t* srow = is_v ? src.v_row(bh, ts) : src.k_row(bh, ts);
-          val[u] = __ldg(reinterpret_cast<const uint4*>(srow) + vi);
-          js[u] = slot0 + done + sub;
-        }
+    for (int u = 0; u < kLoads; ++u) {
+      const int i = i0 + u * EPP + sub;
+      if (i < nk) val[u] = __ldg(reinterpret_cast<const uint4*>(sbase + lst[i] * sv.stride) + vi);
+    }
 #pragma unroll
-        for (int q = 0; q < EPP; ++q) m &= (m ? m - 1u : 0u);
-        done += EPP;
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        if (js[u] >= 0) {
-          const int64_t row = static_cast<int64_t>(base + (js[u] >> 4)) * kPage + (js[u] & 15);
-          reinterpret_cast<uint4*>((is_v ? v_pool : k_pool) + row * D)[vi] = val[u];
-        }
+    for (int u = 0; u < kLoads; ++u) {
+      const int i = i0 + u * EPP + sub;
+      if (i < nk) {
+        const int j = slot0 + i;
+        const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
+        reinterpret_cast<uint4*>(dbase + row * D)[vi] = val[u];
       }
     }
-    running += rtot;
   }
 }
 
@@ -379,21 +402,21 @@ __global__ void __launch_bounds__(256) append_kernel(int mode, int BH, int pos, 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 template <class Src>
-kvp_status run_compact(const Src& src, int BH, int NC, int head_dim, int now, int reserve, void* k_pool,
+kvp_status run_compact(const Src& src, int BH, int NS, int head_dim, int now, int reserve, void* k_pool,
                        void* v_pool, int32_t* expire_pool, int n_pages_cap, int32_t* page_table, int max_pages,
                        int32_t* remap, int32_t* count, void* workspace, int32_t* status, cudaStream_t st) {
-  CompactWs ws = carve(workspace, BH, NC);
-  const dim3 grid(NC, BH);
-  count_kernel<Src><<<grid, 256, 0, st>>>(src, now, NC, ws.chunk_cnt);
-  scan_kernel<<<1, 1024, 0, st>>>(BH, NC, reserve, max_pages, n_pages_cap, ws, count, status);
+  CompactWs ws = carve(workspace, BH, NS);
+  const dim3 grid((NS + kWarpsPerCta - 1) / kWarpsPerCta, BH);
+  count_kernel<Src><<<grid, kWarpsPerCta * 32, 0, st>>>(src, now, NS, ws.seg_cnt);
+  scan_kernel<<<1, 1024, 0, st>>>(BH, NS, reserve, max_pages, n_pages_cap, ws, count, status);
   auto* kp = static_cast<uint16_t*>(k_pool);
   auto* vp = static_cast<uint16_t*>(v_pool);
   if (head_dim == 128)
-    scatter_kernel<128, Src><<<grid, kCopyThreads, 0, st>>>(src, now, NC, reserve, max_pages, ws, count, kp, vp,
-                                                            expire_pool, page_table, remap);
+    scatter_kernel<128, Src><<<grid, kWarpsPerCta * 32, 0, st>>>(src, now, NS, reserve, max_pages, ws, count, kp,
+                                                                  vp, expire_pool, page_table, remap);
   else
-    scatter_kernel<64, Src><<<grid, kCopyThreads, 0, st>>>(src, now, NC, reserve, max_pages, ws, count, kp, vp,
-                                                           expire_pool, page_table, remap);
+    scatter_kernel<64, Src><<<grid, kWarpsPerCta * 32, 0, st>>>(src, now, NS, reserve, max_pages, ws, count, kp,
+                                                                 vp, expire_pool, page_table, remap);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
@@ -432,8 +455,7 @@ extern "C" kvp_status kvp_mask(int mode, int batch, int n_kv_heads, int n_pos, i
 
 extern "C" size_t kvp_compact_workspace_bytes(int batch, int n_kv_heads, int n_pos) {
   if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0) return 0;
-  const int NC = n_pos > 0 ? (n_pos + kChunk - 1) / kChunk : 1;
-  return compact_ws_bytes(batch * n_kv_heads, NC);
+  return compact_ws_bytes(batch * n_kv_heads, n_segments(n_pos));
 }
 
 extern "C" size_t kvp_compact_paged_workspace_bytes(int batch, int n_kv_heads, int src_max_pages) {
@@ -469,10 +491,10 @@ extern "C" kvp_status kvp_compact(int batch, int n_kv_heads, int head_dim, int n
   if (stride_b < 0 || stride_t < 0 || stride_h < 0) return KVP_ERR_INVALID;
   if (workspace == nullptr || workspace_bytes < kvp_compact_workspace_bytes(batch, n_kv_heads, n_pos))
     return KVP_ERR_WORKSPACE;
-  const int NC = n_pos > 0 ? (n_pos + kChunk - 1) / kChunk : 1;
+  const int NS = n_segments(n_pos);
   DenseSrc src{static_cast<const uint16_t*>(k_src), static_cast<const uint16_t*>(v_src), stride_b, stride_t,
                stride_h, expire, n_kv_heads, n_pos};
-  return run_compact(src, batch * n_kv_heads, NC, head_dim, now, reserve, k_pool, v_pool, expire_pool, n_pages_cap,
+  return run_compact(src, batch * n_kv_heads, NS, head_dim, now, reserve, k_pool, v_pool, expire_pool, n_pages_cap,
                      page_table, max_pages, remap, count, workspace, status, static_cast<cudaStream_t>(stream));
 }
 
@@ -498,8 +520,7 @@ extern "C" kvp_status kvp_compact_paged(int batch, int n_kv_heads, int head_dim,
   if (workspace == nullptr ||
       workspace_bytes < kvp_compact_paged_workspace_bytes(batch, n_kv_heads, src_max_pages))
     return KVP_ERR_WORKSPACE;
-  const int n_slots = src_max_pages * kPage;
-  const int NC = n_slots > 0 ? (n_slots + kChunk - 1) / kChunk : 1;
+  const int NS = n_segments(src_max_pages * kPage);
   PagedSrc src{static_cast<const uint16_t*>(src_k_pool),
                static_cast<const uint16_t*>(src_v_pool),
                src_expire_pool,
@@ -510,7 +531,7 @@ extern "C" kvp_status kvp_compact_paged(int batch, int n_kv_heads, int head_dim,
                src_n_pages_cap,
                head_dim,
                status};
-  return run_compact(src, batch * n_kv_heads, NC, head_dim, now, reserve, k_pool, v_pool, expire_pool, n_pages_cap,
+  return run_compact(src, batch * n_kv_heads, NS, head_dim, now, reserve, k_pool, v_pool, expire_pool, n_pages_cap,
                      page_table, max_pages, remap, count, workspace, status, static_cast<cudaStream_t>(stream));
 }
 

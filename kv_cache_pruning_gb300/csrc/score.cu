@@ -331,17 +331,28 @@ int sm_count() {
   return n;
 }
 
+// Per-instance launch set-up, done once per process: the shared-memory
+// opt-in and the SM count of the device.
+template <int BN, int EPI>
+int score_grid_cap() {
+  static const int nsm = [] {
+    using C = ScoreCfg<BN>;
+    if (cudaFuncSetAttribute(score_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+        cudaSuccess)
+      return 0;
+    return sm_count();
+  }();
+  return nsm;
+}
+
 template <int BN, int EPI>
 kvp_status launch_score(const CUtensorMap& ta, const CUtensorMap& tb, const ScoreParams& p, cudaStream_t st) {
   using C = ScoreCfg<BN>;
-  auto kern = score_tc_kernel<BN, EPI>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
-    return KVP_ERR_CUDA;
-  const int tiles = p.m_tiles * p.n_tiles;
-  const int nsm = sm_count();
+  const int nsm = score_grid_cap<BN, EPI>();
   if (nsm <= 0) return KVP_ERR_CUDA;
+  const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < nsm ? tiles : nsm;
-  kern<<<grid, kThreads, C::kSmem, st>>>(ta, tb, p);
+  score_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmem, st>>>(ta, tb, p);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 

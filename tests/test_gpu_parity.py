@@ -280,7 +280,7 @@ def _attn_case(kvp, B, T, H, G, d, tau_std=0.7, seed=3, reserve=0, pps=0, peaked
     st = status_word()
     c = kvp.PagedKV.allocate(B, H, d, cap, max_pages)
     kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp), now, reserve, c, status=st)
-    out = kvp.kvp_decode_attn(dev_bf16(q), c, now, pages_per_split=pps, status=st)
+    out = kvp.kvp_decode_attn(dev_bf16(q), c, now, grid_limit=pps, status=st)
     torch.cuda.synchronize()
     assert st.item() == 0
     return out.cpu().numpy(), ref
@@ -288,13 +288,14 @@ def _attn_case(kvp, B, T, H, G, d, tau_std=0.7, seed=3, reserve=0, pps=0, peaked
 
 @pytest.mark.parametrize("B,T,H,G,d,pps", [
     (1, 512, 2, 2, 64, 0),       # tiny workload shape
-    (2, 2000, 8, 4, 128, 0),     # Llama-3-8B GQA 4, several splits
-    (2, 2000, 8, 4, 128, 3),     # odd split size
+    (2, 2000, 8, 4, 128, 0),     # Llama-3-8B GQA 4: more warps than pages, one piece per slice
+    (2, 2000, 8, 4, 128, 3),     # 3 CTAs: slices span several (b, h)
     (1, 3000, 4, 1, 128, 5),     # MHA
     (2, 1500, 2, 8, 128, 0),     # GQA 8
-    (3, 777, 3, 2, 64, 1),       # one page per split
+    (3, 777, 3, 2, 64, 1),       # one CTA: 8 slices
     (1, 900, 2, 8, 64, 7),
     (1, 1200, 4, 4, 64, 2),
+    (7, 3333, 5, 4, 128, 2),     # ragged everything, slices cross (b, h) boundaries
 ])
 def test_decode_attn(kvp, B, T, H, G, d, pps):
     o, ref = _attn_case(kvp, B, T, H, G, d, pps=pps)
@@ -308,7 +309,7 @@ def test_decode_attn_peaked(kvp, G, d):
 
 
 def test_decode_attn_split_independent(kvp):
-    outs = [_attn_case(kvp, 1, 2500, 2, 4, 128, pps=p)[0] for p in (1, 4, 16, 200)]
+    outs = [_attn_case(kvp, 1, 2500, 2, 4, 128, pps=p)[0] for p in (1, 2, 5, 0)]
     for o in outs[1:]:
         np.testing.assert_allclose(o, outs[0], rtol=0, atol=1e-5)
 
