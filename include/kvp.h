@@ -176,6 +176,38 @@ KVP_API kvp_status kvp_compact(int batch, int n_kv_heads, int head_dim, int n_po
                        int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
+/* kvp_compact_noalloc - kvp_compact for callers that cannot allocate device
+ * memory. No page describes this entry point; it is a convenience of this
+ * library. Some hosts hand a library only the tensors of the operation and no
+ * way to get more GPU memory: a runtime that owns every device allocation
+ * through its own pool, or a plugin interface with no workspace hook, or a
+ * latency-critical loop where cudaMalloc (which can synchronise the device)
+ * is not allowed. This variant takes the same arguments as kvp_compact minus
+ * the workspace and allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library call. Its scratch is a fixed array of
+ * KVP_COMPACT_NOALLOC_SCRATCH_BYTES (1 MiB) in the library's device memory,
+ * which every GPU that loads the library keeps until the process exits.
+ *
+ * Limits and rules:
+ *   - kvp_compact_workspace_bytes(batch, n_kv_heads, n_pos) must not exceed
+ *     KVP_COMPACT_NOALLOC_SCRATCH_BYTES, else KVP_ERR_WORKSPACE and nothing
+ *     is launched (2*B*H*ceil(n_pos/128) + B*H + 1 words of 4 bytes, e.g.
+ *     B*H = 128 at 8192 positions needs 66 KB).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the one array per device and it keeps the last call's
+ *     contents; calls that overlap on the GPU (other streams, other host
+ *     threads) race on it. Nothing in it needs clearing between calls.
+ */
+#define KVP_COMPACT_NOALLOC_SCRATCH_BYTES (1u << 20)
+KVP_API kvp_status kvp_compact_noalloc(int batch, int n_kv_heads, int head_dim, int n_pos,
+                                       const void* k_src, const void* v_src,
+                                       int64_t stride_b, int64_t stride_t, int64_t stride_h,
+                                       const int32_t* expire, int now, int reserve,
+                                       void* k_pool, void* v_pool, int32_t* expire_pool, int n_pages_cap,
+                                       int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                                       int32_t* status, void* stream);
+
 /* kvp_compact_paged - the same compaction with a paged cache (as written by
  * kvp_compact / kvp_append) as the source: slots j < src_count[b, h] whose
  * expire_pool entry is present at `now` are kept, in slot order, and carry

@@ -14,6 +14,8 @@
 // re-derives each entry's slot from its segment offset plus a ballot prefix
 // and moves its K and V rows with 16-byte vector loads and stores, 8 rows'
 // loads in flight per lane before their stores.
+#include <mutex>
+
 #include "kvp_common.cuh"
 
 namespace kvp {
@@ -571,4 +573,45 @@ extern "C" kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_d
                                               expire_pool, n_pages_cap, page_table, max_pages, remap, count,
                                               status);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ no-allocation variant
+// Scratch of kvp_compact_noalloc: a fixed array in device memory, present on
+// every GPU that loads this library until the process exits. Host code only
+// sees a stand-in symbol for it; its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static __device__ __align__(256) int32_t g_compact_scratch[KVP_COMPACT_NOALLOC_SCRATCH_BYTES / sizeof(int32_t)];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" kvp_status kvp_compact_noalloc(int batch, int n_kv_heads, int head_dim, int n_pos, const void* k_src,
+                                          const void* v_src, int64_t stride_b, int64_t stride_t, int64_t stride_h,
+                                          const int32_t* expire, int now, int reserve, void* k_pool, void* v_pool,
+                                          int32_t* expire_pool, int n_pages_cap, int32_t* page_table, int max_pages,
+                                          int32_t* remap, int32_t* count, int32_t* status, void* stream) {
+  if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0) return KVP_ERR_INVALID;
+  const size_t need = kvp_compact_workspace_bytes(batch, n_kv_heads, n_pos);
+  if (need > KVP_COMPACT_NOALLOC_SCRATCH_BYTES) return KVP_ERR_WORKSPACE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return KVP_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_compact_scratch) != cudaSuccess || addr == nullptr) return KVP_ERR_CUDA;
+      g_scratch_addr[dev] = addr;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  // every word of the scratch that the compaction reads is written earlier in
+  // the same call, so nothing needs clearing between calls
+  return kvp_compact(batch, n_kv_heads, head_dim, n_pos, k_src, v_src, stride_b, stride_t, stride_h, expire, now,
+                     reserve, k_pool, v_pool, expire_pool, n_pages_cap, page_table, max_pages, remap, count, scratch,
+                     KVP_COMPACT_NOALLOC_SCRATCH_BYTES, status, stream);
 }
