@@ -45,6 +45,12 @@ WORKLOAD = dict(name="llama3_8b_layer", d_model=4096, n_q_heads=32, n_kv_heads=8
                 n_pos=8192, prune_q=0.75, window=128)
 
 
+# DRAM read + write bytes per row of hidden states of the tcgen05 scorer
+# (KVzap-Linear, d_model 4096, 8 heads), from an ncu capture of that kernel on
+# 32,768 rows: 272.03 MB / 32,768 rows. Valid while the scorer kernel is unchanged.
+SCORE_DRAM_BYTES_PER_ROW = 272.03e6 / 32768
+
+
 def config_desc(w=WORKLOAD):
     return {
         "workload": (f"{w['name']}: one layer, d_model {w['d_model']}, {w['n_q_heads']} q / {w['n_kv_heads']} kv "
@@ -191,6 +197,24 @@ class ClockSampler:
                 if any(r[3].replace(".", "").isdigit() for r in rows) else None}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of every rank's x (the job is as slow as its slowest rank);
+    x itself when no process group is running."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(batch_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Decode tokens/s of the whole job: every rank decodes its own batch of
+    one token per sequence per step."""
+    return batch_per_rank * world / (ms_per_step * 1e-3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -288,11 +312,7 @@ def run_gpu(args, rank: int, world: int):
             tdist.barrier()
     clocks = clk.summary()
     assert status.item() == 0, kvp.status_string(status.item())
-    total_ms = t_start.elapsed_time(t_end)
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     ms_step = total_ms / args.steps
     per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(N_EV - 1)] for i in range(args.steps)])
     k_ms = per.mean(axis=0)  # score, mask, compact, attention (per launch, ms)
@@ -312,11 +332,14 @@ def run_gpu(args, rank: int, world: int):
     kernels = {n: {"ms": float(k_ms[i]), "bytes": int(kb[i]), "GB_s": kb[i] / (k_ms[i] * 1e-3) / 1e9,
                    "frac_of_hbm": kb[i] / (k_ms[i] * 1e-3) / 1e9 / hbm} for i, n in enumerate(names)}
     dom = int(np.argmax(k_ms))
+    traffic = args.traffic
+    if traffic is None and names[dom] == "score":
+        traffic = SCORE_DRAM_BYTES_PER_ROW * n_tok
     roofline = {"bound": "hbm", "kernel": names[dom], "achieved": kb[dom] / (k_ms[dom] * 1e-3) / 1e9,
                 "peak": hbm, "unit": "GB/s", "frac": kb[dom] / (k_ms[dom] * 1e-3) / 1e9 / hbm,
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
-                "traffic": args.traffic}
-    value = B * world / (ms_step * 1e-3)
+                "traffic": traffic}
+    value = weak_scaling_value(B, world, ms_step)
 
     # ---- end to end: pinned host inputs in, result out, inside the timed region
     e2e = None
@@ -346,12 +369,8 @@ def run_gpu(args, rank: int, world: int):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1) / n_e2e
-        if dist:
-            tt = torch.tensor([e_ms], device=dev)
-            tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-            e_ms = float(tt.item())
-        e2e = {"value": B * world / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
+        e2e = {"value": weak_scaling_value(B, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms, "steps": n_e2e}
 
     if rank != 0:
@@ -389,7 +408,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--cpu-baseline-only", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="DRAM bytes per launch of the dominant kernel from an ncu capture of this kernel")
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture of this kernel "
+                         "(default: the scorer's measured bytes per row times the rows of one launch)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
