@@ -28,6 +28,7 @@ constexpr int kWarps = 8;       // warps per CTA
 constexpr int kNst = 3;         // pages in flight per warp
 constexpr int kMaxBH = 4096;    // (b, h) pairs whose page prefix fits in shared memory
 constexpr int kMaxCtas = 512;   // grid bound used to size the workspace
+constexpr int kMinPages = 8;    // fewest pages a warp's slice gets when there are enough
 constexpr int kThreads = kWarps * 32;
 
 template <int D, int G>
@@ -99,6 +100,23 @@ KVP_DEV void unpack8(const uint4& w, float (&f)[8]) {
   f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
 }
 
+// d += a * b on two fp32 lanes at once: the packed f32x2 FMA of sm_100 and later.
+KVP_DEV void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%0, %1};\n\t"
+      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// A logit may exceed the running max by this much (base 2) before the running
+// state is rescaled: p then stays below 2^8, far inside fp32 range, and most
+// pages skip the cross-lane max reduction altogether.
+constexpr float kLazyRescale = 8.0f;
+
 KVP_DEV int clamp_count(const int32_t* count, int bh, int max_pages) {
   return min(max(count[bh], 0), max_pages * kPage);
 }
@@ -161,9 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   if (NP == 0) return;
 
   // ---- this warp's slice of the global page list
+  // slices of at least kMinPages pages (fewer pieces to merge on small
+  // problems); every one of the first NW slices is non-empty
   const int nw_all = gridDim.x * kWarps;
-  const int NW = min(nw_all, NP);  // every one of the first NW slices is non-empty
-  const int gw = blockIdx.x * kWarps + warp;
+  const int NW = max(1, min(nw_all, NP / kMinPages));
+  const int gw = warp * gridDim.x + blockIdx.x;  // slices go round-robin over the CTAs (all SMs busy)
   if (gw >= NW) return;
   const int r0 = static_cast<int>(static_cast<int64_t>(gw) * NP / NW);
   const int r1 = static_cast<int>((static_cast<int64_t>(gw) + 1) * NP / NW);
@@ -287,49 +307,80 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
     const int32_t* Es = reinterpret_cast<const int32_t*>(stage + 2 * C::PAGE_BYTES);
     const int slot0 = (g - pref[cbh]) * kPage;
 
+    // this lane's share of the page goes to registers and the stage is handed
+    // straight back to the copy engine: every stage of the ring stays in
+    // flight while the warp computes
+    uint4 kr[C::RS], vr[C::RS];
+    int32_t er[C::VL];
+#pragma unroll
+    for (int t = 0; t < C::RS; ++t) {
+      kr[t] = reinterpret_cast<const uint4*>(Ks + (t * C::RPS + rowsel) * D)[s];
+      vr[t] = reinterpret_cast<const uint4*>(Vs + (t * C::RPS + rowsel) * D)[s];
+    }
+#pragma unroll
+    for (int u = 0; u < C::VL; ++u) er[u] = Es[((idx_base + u) % C::RS) * C::RPS + rowsel];
+    __syncwarp();
+    if (k + kNst < n_my) {
+      const int pid = page_id(k + kNst);
+      if (lane == 0) {
+        fence_proxy_async();
+        issue(k + kNst, pid);
+      }
+    }
+
     // ---- logits
     float part[C::V];
 #pragma unroll
     for (int t = 0; t < C::RS; ++t) {
-      const int r = t * C::RPS + rowsel;
       float kf[8];
-      unpack8(reinterpret_cast<const uint4*>(Ks + r * D)[s], kf);
+      unpack8(kr[t], kf);
 #pragma unroll
       for (int i = 0; i < G; ++i) {
-        float a = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) a = fmaf(qf[i][e], kf[e], a);
-        part[i * C::RS + t] = a;
+        for (int e = 0; e < 8; e += 2) fma2(a0, a1, qf[i][e], qf[i][e + 1], kf[e], kf[e + 1]);
+        part[i * C::RS + t] = a0 + a1;
       }
     }
     TransposeReduce<C::V, C::LPR / 2>::run(part, lane);
 
-    float x[C::VL];
-    float mloc = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < C::VL; ++u) {
-      const int r = ((idx_base + u) % C::RS) * C::RPS + rowsel;
-      const bool valid = (slot0 + r < cnt) && (p.now < Es[r]);
-      x[u] = valid ? part[u] : -INFINITY;
-      mloc = fmaxf(mloc, x[u]);
-    }
-#pragma unroll
-    for (int o = 1; o < C::GL; o <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-#pragma unroll
-    for (int o = C::LPR; o < 32; o <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-
-    float alpha[G];
-#pragma unroll
-    for (int i = 0; i < G; ++i) {
-      const float mi = __shfl_sync(0xffffffffu, mloc, i * C::GL);
-      const float mnew = fmaxf(m_run[i], mi);
-      alpha[i] = exp2f(m_run[i] - mnew);
-      m_run[i] = mnew;
-    }
     float mh = m_run[0];
 #pragma unroll
     for (int i = 1; i < G; ++i)
       if (my_head == i) mh = m_run[i];
+    float x[C::VL];
+    bool grow = false;
+#pragma unroll
+    for (int u = 0; u < C::VL; ++u) {
+      const int r = ((idx_base + u) % C::RS) * C::RPS + rowsel;
+      const bool valid = (slot0 + r < cnt) && (p.now < er[u]);
+      x[u] = valid ? part[u] : -INFINITY;
+      grow |= x[u] > mh + kLazyRescale;
+    }
+    if (__any_sync(0xffffffffu, grow)) {
+      // a logit outgrew the running max: exact page max per head, rescale
+      float mloc = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < C::VL; ++u) mloc = fmaxf(mloc, x[u]);
+#pragma unroll
+      for (int o = 1; o < C::GL; o <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+#pragma unroll
+      for (int o = C::LPR; o < 32; o <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const float mi = __shfl_sync(0xffffffffu, mloc, i * C::GL);
+        const float mnew = fmaxf(m_run[i], mi);
+        const float alpha = exp2f(m_run[i] - mnew);
+        m_run[i] = mnew;
+        l_run[i] *= alpha;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[i][e] *= alpha;
+      }
+      mh = m_run[0];
+#pragma unroll
+      for (int i = 1; i < G; ++i)
+        if (my_head == i) mh = m_run[i];
+    }
 #pragma unroll
     for (int u = 0; u < C::VL; ++u) {
       const float pv = exp2f(x[u] - mh);
@@ -337,32 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
     }
     __syncwarp();
 
-    // ---- rescale, accumulate P . V
-#pragma unroll
-    for (int i = 0; i < G; ++i) {
-      l_run[i] *= alpha[i];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[i][e] *= alpha[i];
-    }
+    // ---- accumulate P . V
 #pragma unroll
     for (int t = 0; t < C::RS; ++t) {
-      const int r = t * C::RPS + rowsel;
       float vf[8];
-      unpack8(reinterpret_cast<const uint4*>(Vs + r * D)[s], vf);
+      unpack8(vr[t], vf);
 #pragma unroll
       for (int i = 0; i < G; ++i) {
         const float pr = p_s[rowsel * G * C::RS + i * C::RS + t];
         l_run[i] += pr;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(pr, vf[e], acc[i][e]);
-      }
-    }
-    __syncwarp();
-    if (k + kNst < n_my) {
-      const int pid = page_id(k + kNst);
-      if (lane == 0) {
-        fence_proxy_async();
-        issue(k + kNst, pid);
+        for (int e = 0; e < 8; e += 2) fma2(acc[i][e], acc[i][e + 1], pr, pr, vf[e], vf[e + 1]);
       }
     }
 
@@ -420,38 +456,50 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
         if (lane == 0) last = atomicAdd(&p.pieces[cbh], 1) == (w_last - w_first);
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
-          // every piece of this (b, h) is written: merge them (lanes across
-          // pieces for the max and the sum, across columns for the values)
+          // every piece of this (b, h) is written: merge them, all heads at
+          // once (lanes across pieces for the maxima, across columns for the
+          // sums; the pieces' loads are independent, so they overlap)
           __threadfence();
           const int npc = w_last - w_first + 1;
           const size_t s0 = static_cast<size_t>(w_first) + cbh;
+          float M[G];
+#pragma unroll
+          for (int i = 0; i < G; ++i) M[i] = -1e30f;
+          for (int pc = lane; pc < npc; pc += 32) {
+            const float* ml = p.part_ml + (s0 + pc) * G * 2;
+#pragma unroll
+            for (int i = 0; i < G; ++i) M[i] = fmaxf(M[i], __ldcg(ml + 2 * i));
+          }
+#pragma unroll
           for (int i = 0; i < G; ++i) {
-            float M = -1e30f;
-            for (int c0 = 0; c0 < npc; c0 += 32)
-              if (c0 + lane < npc) M = fmaxf(M, __ldcg(p.part_ml + ((s0 + c0 + lane) * G + i) * 2));
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            float L = 0.f;
-            for (int c0 = 0; c0 < npc; c0 += 32)
-              if (c0 + lane < npc) {
-                const float* ml = p.part_ml + ((s0 + c0 + lane) * G + i) * 2;
-                L = fmaf(exp2f(__ldcg(ml) - M), __ldcg(ml + 1), L);
-              }
+            for (int o = 16; o > 0; o >>= 1) M[i] = fmaxf(M[i], __shfl_xor_sync(0xffffffffu, M[i], o));
+          }
+          float L[G], A[G][D / 32];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            float A[D / 32];
+          for (int i = 0; i < G; ++i) {
+            L[i] = 0.f;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) A[c] = 0.f;
+            for (int c = 0; c < D / 32; ++c) A[i][c] = 0.f;
+          }
 #pragma unroll 4
-            for (int pc = 0; pc < npc; ++pc) {
-              const size_t sl = (s0 + pc) * G + i;
-              const float w = exp2f(__ldcg(p.part_ml + sl * 2) - M);
+          for (int pc = 0; pc < npc; ++pc) {
+            const float* ml = p.part_ml + (s0 + pc) * G * 2;
+            const float* ac = p.part_acc + (s0 + pc) * G * D + lane;
 #pragma unroll
-              for (int c = 0; c < D / 32; ++c) A[c] = fmaf(w, __ldcg(p.part_acc + sl * D + lane + 32 * c), A[c]);
+            for (int i = 0; i < G; ++i) {
+              const float w = exp2f(__ldcg(ml + 2 * i) - M[i]);
+              L[i] = fmaf(w, __ldcg(ml + 2 * i + 1), L[i]);
+#pragma unroll
+              for (int c = 0; c < D / 32; ++c) A[i][c] = fmaf(w, __ldcg(ac + i * D + 32 * c), A[i][c]);
             }
+          }
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) p.out[(static_cast<size_t>(cbh) * G + i) * D + lane + 32 * c] = A[c] * inv;
+          for (int i = 0; i < G; ++i) {
+            const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c)
+              p.out[(static_cast<size_t>(cbh) * G + i) * D + lane + 32 * c] = A[i][c] * inv;
           }
           if (lane == 0) p.pieces[cbh] = 0;
         }

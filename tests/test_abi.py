@@ -54,7 +54,7 @@ def test_workspace_sizes(lib):
     # MLP: one fp32 partial per 256-wide hidden chunk, token and head
     assert lib.kvp_score_workspace_bytes(1, 1000, 4096, 8, 1024) == 4 * 1000 * 8 * 4
     lib.kvp_decode_attn_workspace_bytes.restype = ctypes.c_size_t
-    # counters (B*H, 16-byte rounded) + (4096 warp slots + B*H) * G * (d + 2) floats
+    # counters (B*H, 16-byte rounded) + (512 CTAs x 8 warps + B*H) * G * (d + 2) floats
     assert lib.kvp_decode_attn_workspace_bytes(2, 8, 2, 128) == 16 + (4096 + 4) * 4 * 130 * 4
 
 
