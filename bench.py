@@ -402,6 +402,10 @@ def main():
     ap.add_argument("--impl", default="kvp", choices=["kvp", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs only)")
+    ap.add_argument("--workload", default="llama3_8b_layer",
+                    choices=["llama3_8b_layer", "mlp_prefill", "dms_decode", "llama65b_mha"],
+                    help="llama3_8b_layer = the bench line; the others print measurement lines "
+                         "(see bench_workloads.py)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -425,6 +429,16 @@ def main():
         tdist.init_process_group("nccl")
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.workload != "llama3_8b_layer":
+        import torch
+        import __graft_entry__
+        import bench_workloads
+        __graft_entry__.build()
+        import kv_cache_pruning_gb300 as kvp
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+        torch.cuda.set_device(dev)
+        bench_workloads.run(args.workload, kvp, dev, measured_peaks())
         return
     run_gpu(args, rank, world)
     if world > 1:

@@ -1,0 +1,305 @@
+"""Measurement runs of the other synthetic workloads (bench.py --workload NAME).
+
+The default bench line is the Llama-3-8B-shaped layer; these runs measure the
+rest of the path on the shapes it is quoted for:
+
+  mlp_prefill    KVzap-MLP scoring of 4 x 32,768 prompt tokens (d_model 4096 ->
+                 1024 GELU -> 8 heads; tensor-bound), 80% pruned, compaction into
+                 16-token pages, then 64 decode steps (new token scored, appended,
+                 GQA attention over the survivors)
+  dms_decode     DMS delayed eviction, Qwen-3-8B-shaped attention: batch 64,
+                 4,096-token prompt, 1,024 decode steps, evict flag
+                 ~Bernoulli(7/8), eviction 256 steps after the flag, 128-token
+                 window, re-compaction every 64 steps into a second pool
+  llama65b_mha   8 MHA layers (64 heads, d_model 8192), batch 1, 131,072 cached
+                 tokens, KVzap-Linear with per-(layer, head) keep rates ~Beta(2,5),
+                 then 32 decode steps over all 8 layers
+
+Decode loops are captured once in a CUDA graph (the C-ABI calls only enqueue
+work on the current stream) and replayed for timing, so host launch overhead
+is not measured. Inputs are seeded torch draws on the device.
+"""
+from __future__ import annotations
+
+import json
+import math
+
+import torch
+
+
+def _ev():
+    return torch.cuda.Event(enable_timing=True)
+
+
+def _time(fn, reps=1):
+    torch.cuda.synchronize()
+    a, b = _ev(), _ev()
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def _graph(fn):
+    """Capture fn (after one eager warm-up) and return a replay callable."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g.replay
+
+
+def _randn_bf16(shape, gen, dev, std=1.0):
+    return (torch.randn(shape, generator=gen, device=dev, dtype=torch.bfloat16) * std).contiguous()
+
+
+def _tau_quantile(scores_bth, q):
+    """Per-(b, h) lower order statistic at index floor(q (T-1))."""
+    T = scores_bth.shape[1]
+    k = int(math.floor(q * (T - 1))) + 1
+    return torch.kthvalue(scores_bth, k, dim=1).values.contiguous()
+
+
+def mlp_prefill(kvp, dev, peaks, seed=0):
+    B, T, D, HID, H, Hq, d, steps, reserve = 4, 32768, 4096, 1024, 8, 32, 128, 64, 64
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    x = _randn_bf16((B * T, D), g, dev)
+    w1 = _randn_bf16((HID, D), g, dev, 1 / math.sqrt(D))
+    w2 = _randn_bf16((H, HID), g, dev, 1 / math.sqrt(HID))
+    K = _randn_bf16((B, T, H, d), g, dev)
+    V = _randn_bf16((B, T, H, d), g, dev)
+    xs = _randn_bf16((steps, B, D), g, dev)
+    ks = _randn_bf16((steps, B, H, d), g, dev)
+    vs = _randn_bf16((steps, B, H, d), g, dev)
+    qs = _randn_bf16((steps, B, Hq, d), g, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    MLP = kvp.KVP_SCORER_MLP
+    scores = torch.empty(B * T, H, dtype=torch.float32, device=dev)
+    ws = torch.empty(kvp.kvp_score_workspace_bytes(MLP, B * T, D, H, HID), dtype=torch.uint8, device=dev)
+
+    def score():
+        kvp.kvp_score(x, w1, None, w2, None, scorer=MLP, out=scores, workspace=ws, status=st)
+
+    for _ in range(3):
+        score()
+    ms_score = _time(score, reps=10)
+    flops = 2.0 * B * T * D * HID + 2.0 * B * T * HID * H
+    tau = _tau_quantile(scores.view(B, T, H), 0.8)
+    now = T - 1
+    expire, _, count = kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=now,
+                                    scores=scores, tau=tau)
+    mp = (T + reserve + 15) // 16
+    cache = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp, device=dev)
+
+    def prefill_rest():
+        kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=now, scores=scores, tau=tau,
+                     expire=expire, count=count, want_bits=False)
+        kvp.kvp_compact(K, V, expire, now, reserve, cache, status=st)
+
+    prefill_rest()
+    ms_mask_compact = _time(prefill_rest, reps=10)
+    kept = int(count.sum().item())
+    snapshot = [t.clone() for t in (cache.k_pool, cache.v_pool, cache.expire_pool, cache.page_table, cache.remap,
+                                    cache.count)]
+    s_new = torch.empty(B, H, dtype=torch.float32, device=dev)
+    ws_new = torch.empty(kvp.kvp_score_workspace_bytes(MLP, B, D, H, HID), dtype=torch.uint8, device=dev)
+    out = torch.empty(steps, B, Hq, d, dtype=torch.float32, device=dev)
+    ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+
+    def restore():
+        for dst, src in zip((cache.k_pool, cache.v_pool, cache.expire_pool, cache.page_table, cache.remap,
+                             cache.count), snapshot):
+            dst.copy_(src)
+
+    def decode():
+        for i in range(steps):
+            t = T + i
+            kvp.kvp_score(xs[i], w1, None, w2, None, scorer=MLP, out=s_new, workspace=ws_new, status=st)
+            kvp.kvp_append(cache, ks[i], vs[i], t, mode=kvp.KVP_MASK_KVZAP, score=s_new, tau=tau, status=st)
+            kvp.kvp_decode_attn(qs[i], cache, t, out=out[i], workspace=ws_a, status=st)
+
+    replay = _graph(lambda: (restore(), decode()))
+    ms_restore = _time(lambda: restore(), reps=3)
+    ms_decode = _time(replay, reps=3) - ms_restore
+    torch.cuda.synchronize()
+    assert st.item() == 0, kvp.status_string(st.item())
+    kv_pages = int(((cache.count + 15) // 16).sum().item())
+    attn_bytes = kv_pages * 16 * (2 * d * 2 + 4)
+    return {
+        "workload": "mlp_prefill: KVzap-MLP d_model 4096 -> 1024 (GELU) -> 8, batch 4 x 32768 prompt tokens, "
+                    "80% pruned, 128-token window, 64 decode steps (GQA 32/8, head_dim 128)",
+        "scorer_ms": ms_score, "scorer_tflops": flops / (ms_score * 1e-3) / 1e12,
+        "scorer_frac_of_bf16_peak": flops / (ms_score * 1e-3) / 1e12 / peaks[1],
+        "scored_tokens_per_s": B * T / (ms_score * 1e-3),
+        "mask_compact_ms": ms_mask_compact, "kept_fraction": kept / (B * H * T),
+        "decode_ms_per_step": ms_decode / steps, "decode_tokens_per_s": B * steps / (ms_decode * 1e-3),
+        "attn_bytes_last_step": attn_bytes, "peaks": {"hbm_gbs": peaks[0], "bf16_tflops": peaks[1]},
+    }
+
+
+def dms_decode(kvp, dev, peaks, seed=0, steps=1024):
+    B, T0, H, Hq, d, delay, W, every, reserve = 64, 4096, 8, 32, 128, 256, 128, 64, 64
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    K = _randn_bf16((B, T0, H, d), g, dev)
+    V = _randn_bf16((B, T0, H, d), g, dev)
+    pos = torch.arange(T0, device=dev, dtype=torch.int32)
+    f0 = torch.where(torch.rand((B, H, T0), generator=g, device=dev) < 7 / 8, pos, -1).to(torch.int32)
+    ks = _randn_bf16((steps, B, H, d), g, dev)
+    vs = _randn_bf16((steps, B, H, d), g, dev)
+    qs = _randn_bf16((steps, B, Hq, d), g, dev)
+    tpos = (T0 + torch.arange(steps, device=dev, dtype=torch.int32)).view(steps, 1, 1)
+    fs = torch.where(torch.rand((steps, B, H), generator=g, device=dev) < 7 / 8, tpos, -1).to(torch.int32)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    now0 = T0 - 1
+    expire, _, _ = kvp.kvp_mask(mode=kvp.KVP_MASK_DMS, batch=B, n_kv_heads=H, n_pos=T0, now=now0, flag_step=f0,
+                                delay=delay, window=W, want_bits=False)
+    mp = (T0 + steps + reserve + 15) // 16
+    cap = B * H * mp
+    pools = [kvp.PagedKV.allocate(B, H, d, cap, mp, device=dev) for _ in range(2)]
+    out = torch.empty(steps, B, Hq, d, dtype=torch.float32, device=dev)
+    ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T0), dtype=torch.uint8, device=dev)
+    ws_p = torch.empty(kvp.kvp_compact_paged_workspace_bytes(B, H, mp), dtype=torch.uint8, device=dev)
+    pages_read = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def prefill():
+        kvp.kvp_compact(K, V, expire, now0, reserve, pools[0], status=st, workspace=ws_c)
+
+    def decode(count_pages=False):
+        cur = 0
+        for i in range(steps):
+            t = T0 + i
+            if i > 0 and i % every == 0:
+                kvp.kvp_compact_paged(pools[cur], t, reserve, pools[1 - cur], status=st, workspace=ws_p)
+                cur = 1 - cur
+            c = pools[cur]
+            kvp.kvp_append(c, ks[i], vs[i], t, mode=kvp.KVP_MASK_DMS, flag_step=fs[i], delay=delay, window=W,
+                           status=st)
+            kvp.kvp_decode_attn(qs[i], c, t, out=out[i], workspace=ws_a, status=st)
+            if count_pages:
+                pages_read.add_(((c.count + 15) // 16).sum())
+
+    prefill()
+    decode(count_pages=True)  # eager pass: algorithmic bytes of the attention steps
+    torch.cuda.synchronize()
+    assert st.item() == 0, kvp.status_string(st.item())
+    total_pages = int(pages_read.item())
+    prefill()
+    replay = _graph(decode)
+    ms_pref = _time(prefill, reps=3)
+    ms = _time(lambda: (prefill(), replay()), reps=3) - ms_pref
+    torch.cuda.synchronize()
+    assert st.item() == 0, kvp.status_string(st.item())
+    attn_bytes = total_pages * 16 * (2 * d * 2 + 4)
+    return {
+        "workload": "dms_decode: batch 64, 32 q / 8 kv heads, head_dim 128, 4096-token prompt + 1024 steps, "
+                    "evict ~Bernoulli(7/8), delay 256, window 128, re-compaction every 64 steps",
+        "decode_ms_total": ms, "decode_ms_per_step": ms / steps, "decode_tokens_per_s": B * steps / (ms * 1e-3),
+        "attn_pages_read_total": total_pages, "attn_bytes_total": attn_bytes,
+        "effective_GB_s_attention_bytes_over_loop_time": attn_bytes / (ms * 1e-3) / 1e9,
+        "frac_of_hbm": attn_bytes / (ms * 1e-3) / 1e9 / peaks[0],
+        "dense_kv_bytes_last_step": B * H * (T0 + steps) * 2 * d * 2,
+    }
+
+
+def llama65b_mha(kvp, dev, peaks, seed=0, steps=32, n_layers=8):
+    B, T, D, H, d, reserve = 1, 131072, 8192, 64, 128, 32
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    layers = []
+    ms_score = ms_mc = 0.0
+    score_bytes = 0
+    scores = torch.empty(B * T, H, dtype=torch.float32, device=dev)
+    ws_s = torch.empty(kvp.kvp_score_workspace_bytes(0, B * T, D, H), dtype=torch.uint8, device=dev)
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
+    for layer in range(n_layers):
+        x = _randn_bf16((B * T, D), g, dev)
+        w = torch.randn((H, D), generator=g, device=dev) / math.sqrt(D)
+        K = _randn_bf16((B, T, H, d), g, dev)
+        V = _randn_bf16((B, T, H, d), g, dev)
+        kvp.kvp_score(x, w, out=scores, workspace=ws_s, status=st)
+        ms_score += _time(lambda: kvp.kvp_score(x, w, out=scores, workspace=ws_s, status=st), reps=3)
+        score_bytes += x.numel() * 2
+        # per-head keep rate r ~ Beta(2,5) (2nd smallest of 6 uniforms); tau at quantile 1 - r
+        r = torch.rand((H, 6), generator=g, device=dev).sort(dim=1).values[:, 1]
+        srt = scores.view(T, H).sort(dim=0).values
+        idx = torch.floor((1 - r) * (T - 1)).long()
+        tau = srt.gather(0, idx.view(1, H)).view(B, H).contiguous()
+        expire, _, count = kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=T - 1,
+                                        scores=scores, tau=tau, want_bits=False)
+        torch.cuda.synchronize()
+        pages = int(((count + reserve + 15) // 16).sum().item())
+        mp = (T + reserve + 15) // 16
+        cache = kvp.PagedKV.allocate(B, H, d, pages, mp, device=dev)
+
+        def mc():
+            kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=T - 1, scores=scores, tau=tau,
+                         expire=expire, count=count, want_bits=False)
+            kvp.kvp_compact(K, V, expire, T - 1, reserve, cache, status=st, workspace=ws_c)
+
+        mc()
+        ms_mc += _time(mc, reps=1)
+        layers.append(dict(w=w, tau=tau, cache=cache,
+                           snap=[t.clone() for t in (cache.expire_pool, cache.page_table, cache.remap, cache.count)]))
+        del x, K, V
+        torch.cuda.empty_cache()
+    xs = _randn_bf16((steps, n_layers, B, D), g, dev)
+    ks = _randn_bf16((steps, n_layers, B, H, d), g, dev)
+    vs = _randn_bf16((steps, n_layers, B, H, d), g, dev)
+    qs = _randn_bf16((steps, n_layers, B, H, d), g, dev)
+    out = torch.empty(B, H, d, dtype=torch.float32, device=dev)
+    s_new = torch.empty(B, H, dtype=torch.float32, device=dev)
+    ws_n = torch.empty(kvp.kvp_score_workspace_bytes(0, B, D, H), dtype=torch.uint8, device=dev)
+    ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, H, H, d), dtype=torch.uint8, device=dev)
+
+    def restore():
+        for L in layers:
+            c = L["cache"]
+            for dst, src in zip((c.expire_pool, c.page_table, c.remap, c.count), L["snap"]):
+                dst.copy_(src)
+
+    def decode():
+        for i in range(steps):
+            t = T + i
+            for li, L in enumerate(layers):
+                kvp.kvp_score(xs[i, li], L["w"], out=s_new, workspace=ws_n, status=st)
+                kvp.kvp_append(L["cache"], ks[i, li], vs[i, li], t, mode=kvp.KVP_MASK_KVZAP, score=s_new,
+                               tau=L["tau"], status=st)
+                kvp.kvp_decode_attn(qs[i, li], L["cache"], t, out=out, workspace=ws_a, status=st)
+
+    replay = _graph(lambda: (restore(), decode()))
+    ms_restore = _time(restore, reps=3)
+    ms = _time(replay, reps=3) - ms_restore
+    torch.cuda.synchronize()
+    assert st.item() == 0, kvp.status_string(st.item())
+    pages = sum(int(((L["cache"].count + 15) // 16).sum().item()) for L in layers)
+    kept = sum(int(L["cache"].count.sum().item()) for L in layers)
+    step_bytes = pages * 16 * (2 * d * 2 + 4)
+    return {
+        "workload": "llama65b_mha: 8 layers x (64 heads MHA, head_dim 128, d_model 8192), batch 1, 131072 cached "
+                    "tokens, KVzap-Linear, keep rate per (layer, head) ~Beta(2,5), 128-token window, 32 decode steps",
+        "prefill_score_ms_8_layers": ms_score, "prefill_score_GB_s": score_bytes / (ms_score * 1e-3) / 1e9,
+        "prefill_mask_compact_ms_8_layers": ms_mc,
+        "kept_fraction": kept / (n_layers * H * (T + steps)),
+        "decode_ms_per_step": ms / steps, "decode_tokens_per_s": B * steps / (ms * 1e-3),
+        "attn_bytes_last_step_8_layers": step_bytes,
+        "effective_GB_s_last_step_bytes": step_bytes / (ms / steps * 1e-3) / 1e9,
+        "frac_of_hbm": step_bytes / (ms / steps * 1e-3) / 1e9 / peaks[0],
+    }
+
+
+RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha}
+
+
+def run(name, kvp, dev, peaks):
+    res = RUNNERS[name](kvp, dev, peaks)
+    res["name"] = name
+    print(json.dumps(res), flush=True)
+    return res
