@@ -5,6 +5,9 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -59,18 +62,24 @@ KVP_DEV uint64_t globaltimer_ns() {
   return t;
 }
 // Waits for the phase of parity `parity` to complete. Gives up (returns
-// false) after kWaitLimitNs, as soon as *local_abort becomes nonzero, or as
-// soon as *status holds KVP_ERR_TIMEOUT (another CTA already gave up).
+// false) after about kWaitLimitNs, as soon as *local_abort becomes nonzero, or
+// once *status holds KVP_ERR_TIMEOUT (another CTA already gave up). The clock
+// and the status word are only consulted every 1024 probes, so a short wait
+// costs nothing but the barrier probes themselves.
 KVP_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* local_abort = nullptr,
                        const volatile int32_t* status = nullptr) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (local_abort != nullptr && *local_abort) return false;
-    if ((i & 63u) == 0) {
+    if ((i & 1023u) == 1023u) {
       if (status != nullptr && *status == KVP_ERR_TIMEOUT) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        return false;
+      }
     }
   }
 }
@@ -201,5 +210,35 @@ KVP_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // ---------------------------------------------------------------- bf16 helpers
 KVP_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 KVP_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------- host: TMA descriptors
+inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] (row stride ld elements) read in boxes of
+// box_rows x box_cols with the 128-byte swizzle; zero fill outside the matrix.
+inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows,
+                           int box_cols) {
+  auto fn = tmap_encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace kvp
