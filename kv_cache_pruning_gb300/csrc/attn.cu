@@ -456,50 +456,106 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
         if (lane == 0) last = atomicAdd(&p.pieces[cbh], 1) == (w_last - w_first);
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
-          // every piece of this (b, h) is written: merge them, all heads at
-          // once (lanes across pieces for the maxima, across columns for the
-          // sums; the pieces' loads are independent, so they overlap)
+          // every piece of this (b, h) is written: merge them. Lanes take
+          // pieces for the maxima and weights (one round of loads for up to
+          // 32 pieces); then lanes take float4 columns of all G heads and the
+          // pieces go by in batches of 8 whose loads are all in flight at once.
           __threadfence();
+          constexpr int F4 = G * D / 4;           // float4 of one piece's acc
+          constexpr int FPL = (F4 + 31) / 32;     // ... per lane
+          constexpr int JB = 16 / FPL < 8 ? (16 / FPL > 0 ? 16 / FPL : 1) : 8;  // pieces per batch of loads
           const int npc = w_last - w_first + 1;
           const size_t s0 = static_cast<size_t>(w_first) + cbh;
-          float M[G];
+          float M[G], mr[G], lr[G];
 #pragma unroll
           for (int i = 0; i < G; ++i) M[i] = -1e30f;
-          for (int pc = lane; pc < npc; pc += 32) {
-            const float* ml = p.part_ml + (s0 + pc) * G * 2;
+          for (int b0 = 0; b0 < npc; b0 += 32) {
+            const int pc = b0 + lane;
 #pragma unroll
-            for (int i = 0; i < G; ++i) M[i] = fmaxf(M[i], __ldcg(ml + 2 * i));
+            for (int i = 0; i < G; ++i) {
+              mr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2) : -1e30f;
+              lr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2 + 1) : 0.f;
+              M[i] = fmaxf(M[i], mr[i]);
+            }
           }
 #pragma unroll
           for (int i = 0; i < G; ++i) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) M[i] = fmaxf(M[i], __shfl_xor_sync(0xffffffffu, M[i], o));
           }
-          float L[G], A[G][D / 32];
+          float L[G];
+          float4 A[FPL];
 #pragma unroll
-          for (int i = 0; i < G; ++i) {
-            L[i] = 0.f;
+          for (int i = 0; i < G; ++i) L[i] = 0.f;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) A[i][c] = 0.f;
-          }
-#pragma unroll 4
-          for (int pc = 0; pc < npc; ++pc) {
-            const float* ml = p.part_ml + (s0 + pc) * G * 2;
-            const float* ac = p.part_acc + (s0 + pc) * G * D + lane;
+          for (int k = 0; k < FPL; ++k) A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int b0 = 0; b0 < npc; b0 += 32) {
+            const int pc = b0 + lane;
+            if (npc > 32) {  // the registers hold the last chunk of the first pass
+#pragma unroll
+              for (int i = 0; i < G; ++i) {
+                mr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2) : -1e30f;
+                lr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2 + 1) : 0.f;
+              }
+            }
+            float wr[G];
 #pragma unroll
             for (int i = 0; i < G; ++i) {
-              const float w = exp2f(__ldcg(ml + 2 * i) - M[i]);
-              L[i] = fmaf(w, __ldcg(ml + 2 * i + 1), L[i]);
+              wr[i] = pc < npc ? exp2f(mr[i] - M[i]) : 0.f;
+              L[i] = fmaf(wr[i], lr[i], L[i]);
+            }
+            const int nb = min(32, npc - b0);
+            for (int j0 = 0; j0 < nb; j0 += JB) {
+              float4 v[JB][FPL];
 #pragma unroll
-              for (int c = 0; c < D / 32; ++c) A[i][c] = fmaf(w, __ldcg(ac + i * D + 32 * c), A[i][c]);
+              for (int jj = 0; jj < JB; ++jj) {
+#pragma unroll
+                for (int k = 0; k < FPL; ++k) {
+                  const int f = lane + 32 * k;
+                  v[jj][k] = (j0 + jj < nb && f < F4)
+                                 ? __ldcg(reinterpret_cast<const float4*>(p.part_acc + (s0 + b0 + j0 + jj) * G * D) + f)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+              }
+#pragma unroll
+              for (int jj = 0; jj < JB; ++jj) {
+                const int src = (j0 + jj) & 31;  // the lane that holds this piece's weights
+#pragma unroll
+                for (int k = 0; k < FPL; ++k) {
+                  constexpr int kHeadF4 = D / 4;  // float4 per head row
+                  const int h0 = (32 * k) / kHeadF4 < G ? (32 * k) / kHeadF4 : G - 1;
+                  float w = __shfl_sync(0xffffffffu, wr[h0], src);
+                  if constexpr (kHeadF4 < 32) {  // lanes 16-31 are on the next head
+                    const int h1 = (32 * k + 16) / kHeadF4 < G ? (32 * k + 16) / kHeadF4 : G - 1;
+                    const float w1 = __shfl_sync(0xffffffffu, wr[h1], src);
+                    if (lane >= 16) w = w1;
+                  }
+                  A[k].x = fmaf(w, v[jj][k].x, A[k].x);
+                  A[k].y = fmaf(w, v[jj][k].y, A[k].y);
+                  A[k].z = fmaf(w, v[jj][k].z, A[k].z);
+                  A[k].w = fmaf(w, v[jj][k].w, A[k].w);
+                }
+              }
             }
           }
 #pragma unroll
           for (int i = 0; i < G; ++i) {
-            const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c)
-              p.out[(static_cast<size_t>(cbh) * G + i) * D + lane + 32 * c] = A[i][c] * inv;
+            for (int o = 16; o > 0; o >>= 1) L[i] += __shfl_xor_sync(0xffffffffu, L[i], o);
+          }
+#pragma unroll
+          for (int k = 0; k < FPL; ++k) {
+            const int f = lane + 32 * k;
+            if (f < F4) {
+              const int hd = f / (D / 4);
+              float Lh = L[0];
+#pragma unroll
+              for (int i = 1; i < G; ++i)
+                if (hd == i) Lh = L[i];
+              const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
+              reinterpret_cast<float4*>(p.out + static_cast<size_t>(cbh) * G * D)[f] =
+                  make_float4(A[k].x * inv, A[k].y * inv, A[k].z * inv, A[k].w * inv);
+            }
           }
           if (lane == 0) p.pieces[cbh] = 0;
         }
@@ -572,11 +628,13 @@ kvp_status dispatch_g(const AttnParams& p, int G, int grid_limit, cudaStream_t s
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// workspace: arrival counters [BH] (rounded to 16 bytes), then part_ml
-// [slots, G, 2], then part_acc [slots, G, D]; slots = warps of the largest
-// grid + BH (a slice's piece of (b, h) goes to slot warp + b*H + h).
-size_t ws_counter_bytes(int BH) { return (static_cast<size_t>(BH) * 4 + 15) / 16 * 16; }
+// workspace: arrival counters [BH], then part_ml [slots, G, 2], then
+// part_acc [slots, G, D], each region starting on 16 bytes; slots = warps of
+// the largest grid + BH (a slice's piece of (b, h) goes to slot warp + b*H + h).
+size_t round16(size_t n) { return (n + 15) / 16 * 16; }
+size_t ws_counter_bytes(int BH) { return round16(static_cast<size_t>(BH) * 4); }
 size_t ws_slots(int BH) { return static_cast<size_t>(kMaxCtas) * kWarps + BH; }
+size_t ws_ml_bytes(int BH, int G) { return round16(ws_slots(BH) * G * 2 * sizeof(float)); }
 
 }  // namespace
 }  // namespace kvp
@@ -587,8 +645,7 @@ extern "C" size_t kvp_decode_attn_workspace_bytes(int batch, int n_q_heads, int 
   if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || n_q_heads % n_kv_heads) return 0;
   const int BH = batch * n_kv_heads;
   const int G = n_q_heads / n_kv_heads;
-  const size_t slots = ws_slots(BH);
-  return ws_counter_bytes(BH) + slots * G * 2 * sizeof(float) + slots * G * head_dim * sizeof(float);
+  return ws_counter_bytes(BH) + ws_ml_bytes(BH, G) + ws_slots(BH) * G * head_dim * sizeof(float);
 }
 
 extern "C" kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q,
@@ -619,7 +676,7 @@ extern "C" kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* pieces = reinterpret_cast<int32_t*>(ws);
   float* part_ml = reinterpret_cast<float*>(ws + ws_counter_bytes(BH));
-  float* part_acc = part_ml + ws_slots(BH) * G * 2;
+  float* part_acc = reinterpret_cast<float*>(ws + ws_counter_bytes(BH) + ws_ml_bytes(BH, G));
   if (cudaMemsetAsync(pieces, 0, static_cast<size_t>(BH) * 4, st) != cudaSuccess) return KVP_ERR_CUDA;
   AttnParams p{static_cast<const uint16_t*>(q),
                static_cast<const uint16_t*>(k_pool),

@@ -296,6 +296,9 @@ def _attn_case(kvp, B, T, H, G, d, tau_std=0.7, seed=3, reserve=0, pps=0, peaked
     (1, 900, 2, 8, 64, 7),
     (1, 1200, 4, 4, 64, 2),
     (7, 3333, 5, 4, 128, 2),     # ragged everything, slices cross (b, h) boundaries
+    (1, 3000, 3, 1, 64, 0),      # odd B*H with G = 1: every workspace region stays 16-byte aligned
+    (3, 2200, 3, 1, 128, 0),
+    (1, 32768, 1, 4, 128, 0),    # one (b, h) over more than 32 slices: the merge goes in chunks of 32
 ])
 def test_decode_attn(kvp, B, T, H, G, d, pps):
     o, ref = _attn_case(kvp, B, T, H, G, d, pps=pps)
