@@ -32,6 +32,11 @@ KVP_DEV int32_t expire_dms(int flag, int pos, int delay, int window) {
 }
 
 // ------------------------------------------------------------------ mask
+// One CTA per (b, h). Each thread takes kMaskUnroll positions per round, all
+// of whose score (or flag) loads are issued before any is used, so a round
+// costs one memory latency rather than kMaskUnroll of them.
+constexpr int kMaskUnroll = 8;
+
 __global__ void __launch_bounds__(1024) mask_kernel(int mode, int H, int n_pos, int pos0,
                                                     const float* __restrict__ scores, const float* __restrict__ tau,
                                                     const int32_t* __restrict__ flag, int window, int delay, int now,
@@ -42,25 +47,42 @@ __global__ void __launch_bounds__(1024) mask_kernel(int mode, int H, int n_pos, 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float th = (mode == KVP_MASK_KVZAP) ? tau[bh] : 0.f;
   const int n_words = (n_pos + 31) >> 5;
+  const int step = blockDim.x;
   int kept = 0;
-  for (int t0 = 0; t0 < n_pos; t0 += blockDim.x) {
-    const int t = t0 + threadIdx.x;
-    bool keep = false;
-    if (t < n_pos) {
-      int32_t e;
-      if (mode == KVP_MASK_KVZAP) {
-        e = expire_kvzap(scores[(static_cast<int64_t>(b) * n_pos + t) * H + h], th, pos0 + t, window);
-      } else {
-        e = expire_dms(flag[static_cast<int64_t>(bh) * n_pos + t], pos0 + t, delay, window);
+  for (int t0 = 0; t0 < n_pos; t0 += step * kMaskUnroll) {
+    float sc[kMaskUnroll];
+    int32_t fl[kMaskUnroll];
+#pragma unroll
+    for (int u = 0; u < kMaskUnroll; ++u) {
+      const int t = t0 + u * step + threadIdx.x;
+      sc[u] = 0.f;
+      fl[u] = 0;
+      if (t < n_pos) {
+        if (mode == KVP_MASK_KVZAP) {
+          sc[u] = scores[(static_cast<int64_t>(b) * n_pos + t) * H + h];
+        } else {
+          fl[u] = flag[static_cast<int64_t>(bh) * n_pos + t];
+        }
       }
-      expire[static_cast<int64_t>(bh) * n_pos + t] = e;
-      keep = now < e;
     }
-    const unsigned bal = __ballot_sync(0xffffffffu, keep);
-    const int word = (t0 >> 5) + warp;
-    if (lane == 0 && word < n_words) {
-      if (keep_bits) keep_bits[static_cast<int64_t>(bh) * n_words + word] = bal;
-      kept += __popc(bal);
+#pragma unroll
+    for (int u = 0; u < kMaskUnroll; ++u) {
+      const int tb = t0 + u * step;  // first position of this sub-round
+      if (tb >= n_pos) break;        // uniform across the CTA
+      const int t = tb + threadIdx.x;
+      bool keep = false;
+      if (t < n_pos) {
+        const int32_t e = (mode == KVP_MASK_KVZAP) ? expire_kvzap(sc[u], th, pos0 + t, window)
+                                                   : expire_dms(fl[u], pos0 + t, delay, window);
+        expire[static_cast<int64_t>(bh) * n_pos + t] = e;
+        keep = now < e;
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      const int word = (tb >> 5) + warp;
+      if (lane == 0 && word < n_words) {
+        if (keep_bits) keep_bits[static_cast<int64_t>(bh) * n_words + word] = bal;
+        kept += __popc(bal);
+      }
     }
   }
   __shared__ int sums[32];
@@ -148,8 +170,9 @@ struct PagedSrc {
   }
 };
 
-// Workspace layout (int32): segment counts [BH*NS], segment offsets [BH*NS],
-// page base [BH], flag [1] (1 = budget ok).
+// Workspace layout (int32): segment counts [BH*NS], a second [BH*NS] block
+// kept for the layout's stability, page base [BH], flag [1] (1 = budget ok);
+// base and flag are used only above kFusedBH pairs.
 struct CompactWs {
   int32_t* seg_cnt;
   int32_t* seg_off;
@@ -164,10 +187,12 @@ CompactWs carve(void* ws, int BH, int NS) {
 }
 int n_segments(int n) { return n > 0 ? (n + kSeg - 1) / kSeg : 1; }
 
-// Preparation, part 1: present entries per segment (one warp each).
+// Preparation: present entries per segment (one warp each), summed into the
+// (b, h)'s count.
 template <class Src>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) count_kernel(Src src, int now, int NS,
-                                                                   int32_t* __restrict__ seg_cnt) {
+                                                                   int32_t* __restrict__ seg_cnt,
+                                                                   int32_t* __restrict__ count) {
   const int bh = blockIdx.y;
   const int sg = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -175,20 +200,29 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) count_kernel(Src src, int n
   const auto sv = src.view(bh);
   const int lo = sg * kSeg, hi = min(lo + kSeg, sv.length());
   int kept = 0;
-  for (int t = lo + lane; t < hi; t += 32) {
-    int64_t row;
-    const int32_t e = sv.expire_row(t, row);
-    kept += (row >= 0 && now < e);
+#pragma unroll
+  for (int u = 0; u < kSeg / 32; ++u) {  // independent loads, all in flight together
+    const int t = lo + u * 32 + lane;
+    if (t < hi) {
+      int64_t row;
+      const int32_t e = sv.expire_row(t, row);
+      kept += (row >= 0 && now < e);
+    }
   }
   kept = __reduce_add_sync(0xffffffffu, kept);
-  if (lane == 0) seg_cnt[static_cast<int64_t>(bh) * NS + sg] = kept;
+  if (lane == 0) {
+    seg_cnt[static_cast<int64_t>(bh) * NS + sg] = kept;
+    if (kept) atomicAdd(&count[bh], kept);  // count was zeroed before this kernel
+  }
 }
 
-// Preparation, part 2 (one CTA): per-(b, h) counts and segment offsets (one
-// warp per (b, h) at a time), then page bases in (b-major, h-minor) order and
-// the budget checks.
-__global__ void __launch_bounds__(1024) scan_kernel(int BH, int NS, int reserve, int max_pages, int n_pages_cap,
-                                                    CompactWs ws, int32_t* __restrict__ count,
+// Page bases for B*H above kFusedBH (one CTA): bases in (b-major, h-minor)
+// order and the budget checks. Up to kFusedBH pairs every copy-pass CTA
+// derives its own base and the checks from the counts instead.
+constexpr int kFusedBH = 1024;
+
+__global__ void __launch_bounds__(1024) base_kernel(int BH, int reserve, int max_pages, int n_pages_cap,
+                                                    CompactWs ws, const int32_t* __restrict__ count,
                                                     int32_t* __restrict__ status) {
   __shared__ int warp_tot[32];
   __shared__ int carry_s;
@@ -197,22 +231,6 @@ __global__ void __launch_bounds__(1024) scan_kernel(int BH, int NS, int reserve,
   if (tid == 0) {
     carry_s = 0;
     bad_s = 0;
-  }
-  for (int bh = warp; bh < BH; bh += 32) {
-    int run = 0;
-    for (int s0 = 0; s0 < NS; s0 += 32) {
-      const int sg = s0 + lane;
-      const int c = sg < NS ? ws.seg_cnt[static_cast<int64_t>(bh) * NS + sg] : 0;
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (sg < NS) ws.seg_off[static_cast<int64_t>(bh) * NS + sg] = run + incl - c;
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) count[bh] = run;
   }
   __syncthreads();
   for (int b0 = 0; b0 < BH; b0 += 1024) {
@@ -259,10 +277,12 @@ __global__ void __launch_bounds__(1024) scan_kernel(int BH, int NS, int reserve,
 // (source row indices, in order) in shared memory and writes their expire and
 // remap entries, then moves their K and V rows, kLoads passes of loads in
 // flight before the matching stores.
-template <int D, class Src>
-__global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int now, int NS, int reserve,
-                                                                     int max_pages, CompactWs ws,
+template <int D, class Src, bool kFused>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, 5) scatter_kernel(Src src, int now, int NS, int reserve,
+                                                                     int max_pages, int n_pages_cap, int BH,
+                                                                     CompactWs ws,
                                                                      const int32_t* __restrict__ count,
+                                                                     int32_t* __restrict__ status,
                                                                      uint16_t* __restrict__ k_pool,
                                                                      uint16_t* __restrict__ v_pool,
                                                                      int32_t* __restrict__ expire_pool,
@@ -270,19 +290,56 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
                                                                      int32_t* __restrict__ remap) {
   constexpr int VPR = D / 8;            // 16-byte vectors per row
   constexpr int EPP = 32 / (2 * VPR);   // entries per warp pass (a K and a V row each)
-  constexpr int kLoads = 8;             // passes whose loads are issued before their stores
+  constexpr int kLoads = 16;            // passes whose loads are issued before their stores
   __shared__ int64_t lst_all[kWarpsPerCta][kSeg];
-  if (ws.ok[0] == 0) return;
   const int bh = blockIdx.y;
   const int warp = threadIdx.x >> 5;
   const int sg = blockIdx.x * kWarpsPerCta + warp;
   const int lane = threadIdx.x & 31;
+  int base;
+  if constexpr (kFused) {
+    // this (b, h)'s first page and the budget, from the counts of all pairs
+    __shared__ int64_t red_s[3][kWarpsPerCta];
+    int64_t before = 0, total = 0, bad = 0;
+    for (int i = threadIdx.x; i < BH; i += kWarpsPerCta * 32) {
+      const int pg = (count[i] + reserve + kPage - 1) / kPage;
+      before += i < bh ? pg : 0;
+      total += pg;
+      bad |= pg > max_pages;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      total += __shfl_xor_sync(0xffffffffu, total, o);
+      bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    if (lane == 0) {
+      red_s[0][warp] = before;
+      red_s[1][warp] = total;
+      red_s[2][warp] = bad;
+    }
+    __syncthreads();
+    before = total = bad = 0;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerCta; ++w) {
+      before += red_s[0][w];
+      total += red_s[1][w];
+      bad |= red_s[2][w];
+    }
+    if (bad || total > n_pages_cap) {
+      if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) record_error(status, KVP_ERR_CAPACITY);
+      return;
+    }
+    base = static_cast<int>(before);
+  } else {
+    if (ws.ok[0] == 0) return;
+    base = ws.base[bh];
+  }
   if (sg >= NS) return;
   int64_t* lst = lst_all[warp];
   const auto sv = src.view(bh);
   const int n = sv.length();
   const int cnt = count[bh];
-  const int base = ws.base[bh];
   const int pages = (cnt + reserve + kPage - 1) / kPage;
   const int64_t cap = static_cast<int64_t>(max_pages) * kPage;
   int32_t* remap_bh = remap + bh * cap;
@@ -307,15 +364,30 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
     }
   }
 
-  // list the present entries; write their expire and remap entries
-  const int slot0 = ws.seg_off[static_cast<int64_t>(bh) * NS + sg];
+  // first slot of this segment: the present entries of the segments before it
+  int slot0 = 0;
+  for (int c0 = 0; c0 < sg; c0 += 32)
+    slot0 += c0 + lane < sg ? ws.seg_cnt[static_cast<int64_t>(bh) * NS + c0 + lane] : 0;
+  slot0 = __reduce_add_sync(0xffffffffu, slot0);
+
+  // list the present entries; write their expire and remap entries (the
+  // segment's expire values are all loaded before the first ballot)
   const int lo = sg * kSeg, hi = min(lo + kSeg, n);
+  int64_t rows[kSeg / 32];
+  int32_t exps[kSeg / 32];
+#pragma unroll
+  for (int u = 0; u < kSeg / 32; ++u) {
+    const int t = lo + u * 32 + lane;
+    rows[u] = -1;
+    exps[u] = 0;
+    if (t < hi) exps[u] = sv.expire_row(t, rows[u]);
+  }
   int nk = 0;
-  for (int r0 = lo; r0 < hi; r0 += 32) {
-    const int t = r0 + lane;
-    int64_t row = -1;
-    int32_t e = 0;
-    if (t < hi) e = sv.expire_row(t, row);
+#pragma unroll
+  for (int u = 0; u < kSeg / 32; ++u) {
+    const int t = lo + u * 32 + lane;
+    const int64_t row = rows[u];
+    const int32_t e = exps[u];
     const bool keep = (t < hi) && (row >= 0) && (now < e);
     const unsigned bal = __ballot_sync(0xffffffffu, keep);
     if (keep) {
@@ -409,16 +481,22 @@ kvp_status run_compact(const Src& src, int BH, int NS, int head_dim, int now, in
                        int32_t* remap, int32_t* count, void* workspace, int32_t* status, cudaStream_t st) {
   CompactWs ws = carve(workspace, BH, NS);
   const dim3 grid((NS + kWarpsPerCta - 1) / kWarpsPerCta, BH);
-  count_kernel<Src><<<grid, kWarpsPerCta * 32, 0, st>>>(src, now, NS, ws.seg_cnt);
-  scan_kernel<<<1, 1024, 0, st>>>(BH, NS, reserve, max_pages, n_pages_cap, ws, count, status);
+  if (cudaMemsetAsync(count, 0, static_cast<size_t>(BH) * sizeof(int32_t), st) != cudaSuccess) return KVP_ERR_CUDA;
+  count_kernel<Src><<<grid, kWarpsPerCta * 32, 0, st>>>(src, now, NS, ws.seg_cnt, count);
+  const bool fused = BH <= kFusedBH;
+  if (!fused) base_kernel<<<1, 1024, 0, st>>>(BH, reserve, max_pages, n_pages_cap, ws, count, status);
   auto* kp = static_cast<uint16_t*>(k_pool);
   auto* vp = static_cast<uint16_t*>(v_pool);
-  if (head_dim == 128)
-    scatter_kernel<128, Src><<<grid, kWarpsPerCta * 32, 0, st>>>(src, now, NS, reserve, max_pages, ws, count, kp,
-                                                                  vp, expire_pool, page_table, remap);
-  else
-    scatter_kernel<64, Src><<<grid, kWarpsPerCta * 32, 0, st>>>(src, now, NS, reserve, max_pages, ws, count, kp,
-                                                                 vp, expire_pool, page_table, remap);
+#define KVP_SCATTER(DIM, FUSED)                                                                                \
+  scatter_kernel<DIM, Src, FUSED><<<grid, kWarpsPerCta * 32, 0, st>>>(src, now, NS, reserve, max_pages,         \
+                                                                      n_pages_cap, BH, ws, count, status, kp, \
+                                                                      vp, expire_pool, page_table, remap)
+  if (head_dim == 128) {
+    if (fused) KVP_SCATTER(128, true); else KVP_SCATTER(128, false);
+  } else {
+    if (fused) KVP_SCATTER(64, true); else KVP_SCATTER(64, false);
+  }
+#undef KVP_SCATTER
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
