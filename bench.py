@@ -50,6 +50,11 @@ WORKLOAD = dict(name="llama3_8b_layer", d_model=4096, n_q_heads=32, n_kv_heads=8
 # 32,768 rows: 272.03 MB / 32,768 rows. Valid while the scorer kernel is unchanged.
 SCORE_DRAM_BYTES_PER_ROW = 272.03e6 / 32768
 
+# Kernels of this library launched per step at this workload's size (B*H <= 1024):
+# weight split + scorer, mask, segment count + copy pass, decode attention
+# (the compaction and attention calls also issue one memset each).
+KERNELS_PER_STEP = 6
+
 
 def config_desc(w=WORKLOAD):
     return {
@@ -297,7 +302,17 @@ def run_gpu(args, rank: int, world: int):
     dist = world > 1
     if dist:
         import torch.distributed as tdist
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(N_EV)] for _ in range(args.steps)]
+    # The step is captured once as a CUDA graph (its kernels and memsets as
+    # nodes) and replayed: no host launch work inside the timed region.
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert status.item() == 0, kvp.status_string(status.item())
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         if dist:
@@ -305,7 +320,10 @@ def run_gpu(args, rank: int, world: int):
         torch.cuda.synchronize()
         t_start.record(stream)
         for i in range(args.steps):
-            step(evs[i])
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
         t_end.record(stream)
         torch.cuda.synchronize()
         if dist:
@@ -314,7 +332,15 @@ def run_gpu(args, rank: int, world: int):
     assert status.item() == 0, kvp.status_string(status.item())
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     ms_step = total_ms / args.steps
-    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(N_EV - 1)] for i in range(args.steps)])
+
+    # ---- per-phase times: eager steps with an event between phases (a
+    # separate loop, so these events are not inside the timed region above)
+    n_break = max(3, min(args.steps, 50))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(N_EV)] for _ in range(n_break)]
+    for i in range(n_break):
+        step(evs[i])
+    torch.cuda.synchronize()
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(N_EV - 1)] for i in range(n_break)])
     k_ms = per.mean(axis=0)  # score, mask, compact, attention (per launch, ms)
 
     # ---- algorithmic bytes (what the method must move)
@@ -387,7 +413,8 @@ def run_gpu(args, rank: int, world: int):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch RNG, N(0,1) hidden states and K/V)",
-        "config": config_desc(w), "e2e": e2e, "gpu_launches": 8 * args.steps, "roofline": roofline,
+        "config": dict(config_desc(w), cuda_graph=graph is not None), "e2e": e2e,
+        "gpu_launches": KERNELS_PER_STEP * args.steps, "roofline": roofline,
         "kernels": kernels, "effective_step_GB_s": step_b / (ms_step * 1e-3) / 1e9,
         "kept_fraction": kept / (B * H * T), "clocks": clocks, "cpu_baseline": cpu,
     }
@@ -406,6 +433,7 @@ def main():
                     choices=["llama3_8b_layer", "mlp_prefill", "dms_decode", "llama65b_mha"],
                     help="llama3_8b_layer = the bench line; the others print measurement lines "
                          "(see bench_workloads.py)")
+    ap.add_argument("--eager", action="store_true", help="launch every step from the host (no CUDA graph)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -130,6 +130,7 @@ def _kvzap_case(B, T, H, d, seed=3, tau_std=0.7):
     (2, 3000, 3, 128, 5),      # 3 chunks, ragged
     (4, 1030, 8, 128, 64),
     (2, 17, 2, 64, 16),        # tiny ragged, reserve a full page
+    (131, 40, 8, 64, 3),       # more than 1024 (b, h): page bases from the separate base pass
 ])
 def test_compact_dense_bit_exact(kvp, B, T, H, d, reserve):
     k, v, exp, cnt = _kvzap_case(B, T, H, d)
@@ -187,6 +188,15 @@ def test_compact_capacity_status(kvp):
     assert st.item() == kvp.KVP_ERR_CAPACITY
     st.zero_()
     dst = kvp.PagedKV.allocate(B, H, d, 64, 15)  # a (b, h) needs 16 > max_pages
+    kvp.kvp_compact(dev_bf16(k), dev_bf16(v), exp, T - 1, 0, dst, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == kvp.KVP_ERR_CAPACITY
+    # the same check when more than 1024 (b, h) take the separate base pass
+    B, T, H = 130, 32, 8
+    k, v = syn.kv_inputs(6, B, T, H, d)
+    exp = dev_i32(np.full((B, H, T), orc.NEVER, np.int32))
+    st.zero_()
+    dst = kvp.PagedKV.allocate(B, H, d, 2000, 2)  # needs 2 * 1040 pages
     kvp.kvp_compact(dev_bf16(k), dev_bf16(v), exp, T - 1, 0, dst, status=st)
     torch.cuda.synchronize()
     assert st.item() == kvp.KVP_ERR_CAPACITY
