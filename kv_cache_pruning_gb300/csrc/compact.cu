@@ -187,32 +187,41 @@ CompactWs carve(void* ws, int BH, int NS) {
 }
 int n_segments(int n) { return n > 0 ? (n + kSeg - 1) / kSeg : 1; }
 
-// Preparation: present entries per segment (one warp each), summed into the
-// (b, h)'s count.
+// Preparation: present entries per segment (one warp each); the CTA's
+// segments (all of one (b, h)) are summed and added to the (b, h)'s count
+// with one atomic.
 template <class Src>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) count_kernel(Src src, int now, int NS,
                                                                    int32_t* __restrict__ seg_cnt,
                                                                    int32_t* __restrict__ count) {
+  __shared__ int cta_kept[kWarpsPerCta];
   const int bh = blockIdx.y;
-  const int sg = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int warp = threadIdx.x >> 5;
+  const int sg = blockIdx.x * kWarpsPerCta + warp;
   const int lane = threadIdx.x & 31;
-  if (sg >= NS) return;
-  const auto sv = src.view(bh);
-  const int lo = sg * kSeg, hi = min(lo + kSeg, sv.length());
   int kept = 0;
+  if (sg < NS) {
+    const auto sv = src.view(bh);
+    const int lo = sg * kSeg, hi = min(lo + kSeg, sv.length());
 #pragma unroll
-  for (int u = 0; u < kSeg / 32; ++u) {  // independent loads, all in flight together
-    const int t = lo + u * 32 + lane;
-    if (t < hi) {
-      int64_t row;
-      const int32_t e = sv.expire_row(t, row);
-      kept += (row >= 0 && now < e);
+    for (int u = 0; u < kSeg / 32; ++u) {  // independent loads, all in flight together
+      const int t = lo + u * 32 + lane;
+      if (t < hi) {
+        int64_t row;
+        const int32_t e = sv.expire_row(t, row);
+        kept += (row >= 0 && now < e);
+      }
     }
+    kept = __reduce_add_sync(0xffffffffu, kept);
+    if (lane == 0) seg_cnt[static_cast<int64_t>(bh) * NS + sg] = kept;
   }
-  kept = __reduce_add_sync(0xffffffffu, kept);
-  if (lane == 0) {
-    seg_cnt[static_cast<int64_t>(bh) * NS + sg] = kept;
-    if (kept) atomicAdd(&count[bh], kept);  // count was zeroed before this kernel
+  if (lane == 0) cta_kept[warp] = kept;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerCta; ++w) t += cta_kept[w];
+    if (t) atomicAdd(&count[bh], t);  // count was zeroed before this kernel
   }
 }
 
@@ -272,13 +281,33 @@ __global__ void __launch_bounds__(1024) base_kernel(int BH, int reserve, int max
   }
 }
 
+// 16-byte asynchronous global -> shared copy (no register staging).
+KVP_DEV void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+KVP_DEV void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Copy pass: one warp per 128-entry segment of one (b, h); grid
-// (ceil(NS / 4), B*H). The warp first lists the segment's present entries
-// (source row indices, in order) in shared memory and writes their expire and
-// remap entries, then moves their K and V rows, kLoads passes of loads in
-// flight before the matching stores.
+// (B*H, ceil(NS / 4)). The warp lists the segment's present entries (source
+// row indices, in order) in shared memory and writes their expire and remap
+// entries, then moves their K and V rows through a shared-memory stage of
+// kStage entries: every row of a batch is requested with 16-byte async
+// copies before the first one is stored, so a warp keeps up to
+// kStage * 2 * D * 2 bytes in flight without spending registers on them.
+// The segment's expire values, the counts of the segments before it and
+// (up to kFusedBH pairs) the counts of all pairs are requested together
+// before any of them is used.
+constexpr int kStage = 32;
+
+template <int D>
+constexpr int scatter_smem_bytes() {
+  return kWarpsPerCta * (kStage * 2 * D * 2 + kSeg * 8);
+}
+
 template <int D, class Src, bool kFused>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, 5) scatter_kernel(Src src, int now, int NS, int reserve,
+__global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int now, int NS, int reserve,
                                                                      int max_pages, int n_pages_cap, int BH,
                                                                      CompactWs ws,
                                                                      const int32_t* __restrict__ count,
@@ -288,14 +317,34 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 5) scatter_kernel(Src src, 
                                                                      int32_t* __restrict__ expire_pool,
                                                                      int32_t* __restrict__ page_table,
                                                                      int32_t* __restrict__ remap) {
-  constexpr int VPR = D / 8;            // 16-byte vectors per row
-  constexpr int EPP = 32 / (2 * VPR);   // entries per warp pass (a K and a V row each)
-  constexpr int kLoads = 16;            // passes whose loads are issued before their stores
-  __shared__ int64_t lst_all[kWarpsPerCta][kSeg];
-  const int bh = blockIdx.y;
+  constexpr int E16 = 2 * D * 2 / 16;   // 16-byte pieces per entry (K row then V row)
+  constexpr int EPI = 32 / E16;         // entries per warp instruction (1 for D = 128, 2 for D = 64)
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  const int bh = blockIdx.x;  // pairs vary fastest: CTAs resident together read the same positions of all heads
   const int warp = threadIdx.x >> 5;
-  const int sg = blockIdx.x * kWarpsPerCta + warp;
+  const int sg = blockIdx.y * kWarpsPerCta + warp;
   const int lane = threadIdx.x & 31;
+  uint4* stage = reinterpret_cast<uint4*>(sm_raw) + warp * kStage * E16;
+  int64_t* lst = reinterpret_cast<int64_t*>(sm_raw + kWarpsPerCta * kStage * E16 * 16) + warp * kSeg;
+  const bool live = sg < NS;
+
+  // ---- loads that do not depend on one another, all issued first
+  const auto sv = src.view(bh);
+  const int n = sv.length();
+  const int lo = sg * kSeg, hi = min(lo + kSeg, n);
+  int64_t rows[kSeg / 32];
+  int32_t exps[kSeg / 32];
+#pragma unroll
+  for (int u = 0; u < kSeg / 32; ++u) {
+    const int t = lo + u * 32 + lane;
+    rows[u] = -1;
+    exps[u] = 0;
+    if (live && t < hi) exps[u] = sv.expire_row(t, rows[u]);
+  }
+  int slot0 = 0;  // first slot of this segment: the present entries of the segments before it
+  if (live)
+    for (int c0 = 0; c0 < sg; c0 += 32)
+      slot0 += c0 + lane < sg ? ws.seg_cnt[static_cast<int64_t>(bh) * NS + c0 + lane] : 0;
   int base;
   if constexpr (kFused) {
     // this (b, h)'s first page and the budget, from the counts of all pairs
@@ -335,18 +384,17 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 5) scatter_kernel(Src src, 
     if (ws.ok[0] == 0) return;
     base = ws.base[bh];
   }
-  if (sg >= NS) return;
-  int64_t* lst = lst_all[warp];
-  const auto sv = src.view(bh);
-  const int n = sv.length();
+  if (!live) return;
+  slot0 = __reduce_add_sync(0xffffffffu, slot0);
   const int cnt = count[bh];
   const int pages = (cnt + reserve + kPage - 1) / kPage;
   const int64_t cap = static_cast<int64_t>(max_pages) * kPage;
   int32_t* remap_bh = remap + bh * cap;
 
-  // this segment's share of the page-table row, the remap tail and the
+  // ---- this segment's share of the page-table row, the remap tail and the
   // zeroing of unused rows in the (b, h)'s last pages
   {
+    constexpr int VPR = D / 8;
     const int seg = (max_pages + NS - 1) / NS;
     for (int p = sg * seg + lane; p < min(max_pages, (sg + 1) * seg); p += 32)
       page_table[static_cast<int64_t>(bh) * max_pages + p] = p < pages ? base + p : -1;
@@ -364,24 +412,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 5) scatter_kernel(Src src, 
     }
   }
 
-  // first slot of this segment: the present entries of the segments before it
-  int slot0 = 0;
-  for (int c0 = 0; c0 < sg; c0 += 32)
-    slot0 += c0 + lane < sg ? ws.seg_cnt[static_cast<int64_t>(bh) * NS + c0 + lane] : 0;
-  slot0 = __reduce_add_sync(0xffffffffu, slot0);
-
-  // list the present entries; write their expire and remap entries (the
-  // segment's expire values are all loaded before the first ballot)
-  const int lo = sg * kSeg, hi = min(lo + kSeg, n);
-  int64_t rows[kSeg / 32];
-  int32_t exps[kSeg / 32];
-#pragma unroll
-  for (int u = 0; u < kSeg / 32; ++u) {
-    const int t = lo + u * 32 + lane;
-    rows[u] = -1;
-    exps[u] = 0;
-    if (t < hi) exps[u] = sv.expire_row(t, rows[u]);
-  }
+  // ---- list the present entries; write their expire and remap entries
   int nk = 0;
 #pragma unroll
   for (int u = 0; u < kSeg / 32; ++u) {
@@ -401,29 +432,25 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 5) scatter_kernel(Src src, 
   }
   __syncwarp();
 
-  // move the rows
-  const int sub = lane / (2 * VPR);
-  const int vec = lane % (2 * VPR);
-  const bool is_v = vec >= VPR;
-  const int vi = is_v ? vec - VPR : vec;
+  // ---- move the rows through the stage
+  const int piece = lane % E16;          // 16-byte piece of an entry this lane moves
+  const int sub = lane / E16;            // entry of a warp instruction this lane serves
+  const bool is_v = piece >= E16 / 2;
+  const int vi = is_v ? piece - E16 / 2 : piece;
   const uint16_t* sbase = is_v ? sv.vb : sv.kb;
   uint16_t* dbase = is_v ? v_pool : k_pool;
-  for (int i0 = 0; i0 < nk; i0 += kLoads * EPP) {
-    uint4 val[kLoads];
-#pragma unroll
-    for (int u = 0; u < kLoads; ++u) {
-      const int i = i0 + u * EPP + sub;
-      if (i < nk) val[u] = __ldg(reinterpret_cast<const uint4*>(sbase + lst[i] * sv.stride) + vi);
+  for (int i0 = 0; i0 < nk; i0 += kStage) {
+    const int nb = min(kStage, nk - i0);
+    for (int i = sub; i < nb; i += EPI)
+      cp_async16(stage + i * E16 + piece, reinterpret_cast<const uint4*>(sbase + lst[i0 + i] * sv.stride) + vi);
+    cp_async_wait_all();
+    __syncwarp();
+    for (int i = sub; i < nb; i += EPI) {
+      const int j = slot0 + i0 + i;
+      const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
+      reinterpret_cast<uint4*>(dbase + row * D)[vi] = stage[i * E16 + piece];
     }
-#pragma unroll
-    for (int u = 0; u < kLoads; ++u) {
-      const int i = i0 + u * EPP + sub;
-      if (i < nk) {
-        const int j = slot0 + i;
-        const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
-        reinterpret_cast<uint4*>(dbase + row * D)[vi] = val[u];
-      }
-    }
+    __syncwarp();
   }
 }
 
@@ -481,16 +508,23 @@ kvp_status run_compact(const Src& src, int BH, int NS, int head_dim, int now, in
                        int32_t* remap, int32_t* count, void* workspace, int32_t* status, cudaStream_t st) {
   CompactWs ws = carve(workspace, BH, NS);
   const dim3 grid((NS + kWarpsPerCta - 1) / kWarpsPerCta, BH);
+  const dim3 grid_t(BH, (NS + kWarpsPerCta - 1) / kWarpsPerCta);
   if (cudaMemsetAsync(count, 0, static_cast<size_t>(BH) * sizeof(int32_t), st) != cudaSuccess) return KVP_ERR_CUDA;
   count_kernel<Src><<<grid, kWarpsPerCta * 32, 0, st>>>(src, now, NS, ws.seg_cnt, count);
   const bool fused = BH <= kFusedBH;
   if (!fused) base_kernel<<<1, 1024, 0, st>>>(BH, reserve, max_pages, n_pages_cap, ws, count, status);
   auto* kp = static_cast<uint16_t*>(k_pool);
   auto* vp = static_cast<uint16_t*>(v_pool);
-#define KVP_SCATTER(DIM, FUSED)                                                                                \
-  scatter_kernel<DIM, Src, FUSED><<<grid, kWarpsPerCta * 32, 0, st>>>(src, now, NS, reserve, max_pages,         \
-                                                                      n_pages_cap, BH, ws, count, status, kp, \
-                                                                      vp, expire_pool, page_table, remap)
+#define KVP_SCATTER(DIM, FUSED)                                                                              \
+  do {                                                                                                        \
+    static const bool attr_ok = cudaFuncSetAttribute(scatter_kernel<DIM, Src, FUSED>,                        \
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,            \
+                                                     scatter_smem_bytes<DIM>()) == cudaSuccess;               \
+    if (!attr_ok) return KVP_ERR_CUDA;                                                                        \
+    scatter_kernel<DIM, Src, FUSED><<<grid_t, kWarpsPerCta * 32, scatter_smem_bytes<DIM>(), st>>>(            \
+        src, now, NS, reserve, max_pages, n_pages_cap, BH, ws, count, status, kp, vp, expire_pool, page_table, \
+        remap);                                                                                               \
+  } while (0)
   if (head_dim == 128) {
     if (fused) KVP_SCATTER(128, true); else KVP_SCATTER(128, false);
   } else {
