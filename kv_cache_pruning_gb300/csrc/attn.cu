@@ -121,9 +121,20 @@ KVP_DEV int clamp_count(const int32_t* count, int bh, int max_pages) {
   return min(max(count[bh], 0), max_pages * kPage);
 }
 
-// Warp whose page slice holds global page g, for nw non-empty slices of np pages.
-KVP_DEV int warp_of(int g, int np, int nw) {
-  return static_cast<int>(((static_cast<int64_t>(g) + 1) * nw - 1) / np);
+// Slices are cut evenly in a cost coordinate rather than in pages: page g of
+// (b, h) number bh costs c(g) = 2g + kBoundaryCost * bh, i.e. every (b, h)
+// start counts as kBoundaryCost / 2 extra pages. A slice that holds a (b, h)
+// boundary stops its page stream to reduce and publish a partial state, so it
+// gets fewer pages and the warps finish closer together (measured on a GB300
+// at 16 x 8192 tokens: 3 extra pages per boundary, among 1.5 / 3 / 4.5 / 6,
+// took the kernel from 36.0 to 34.7 us). c is strictly increasing, so slices
+// are contiguous; a slice can be empty only between two (b, h) with empty ones
+// in between, never inside one.
+constexpr int kBoundaryCost = 6;
+
+// Slice holding page g of (b, h) bh, for nw slices and total cost c_end.
+KVP_DEV int slice_of(int g, int bh, int nw, int64_t c_end) {
+  return static_cast<int>((2 * static_cast<int64_t>(g) + static_cast<int64_t>(kBoundaryCost) * bh) * nw / c_end);
 }
 
 template <int D, int G>
@@ -185,8 +196,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   const int NW = max(1, min(nw_all, NP / kMinPages));
   const int gw = warp * gridDim.x + blockIdx.x;  // slices go round-robin over the CTAs (all SMs busy)
   if (gw >= NW) return;
-  const int r0 = static_cast<int>(static_cast<int64_t>(gw) * NP / NW);
-  const int r1 = static_cast<int>((static_cast<int64_t>(gw) + 1) * NP / NW);
+  int last_bh = 0;  // (b, h) of the last page
+  {
+    int a = 0, b = BH - 1;
+    while (a < b) {
+      const int mid = (a + b + 1) >> 1;
+      if (pref[mid] <= NP - 1) a = mid; else b = mid - 1;
+    }
+    last_bh = a;
+  }
+  const int64_t c_end = 2 * static_cast<int64_t>(NP - 1) + static_cast<int64_t>(kBoundaryCost) * last_bh + 1;
+  auto slice_start = [&](int w) {  // first page of slice w: the first page whose cost reaches ceil(w * c_end / NW)
+    const int64_t T = (static_cast<int64_t>(w) * c_end + NW - 1) / NW;
+    auto maxc = [&](int k) {
+      return 2 * static_cast<int64_t>(pref[k + 1] - 1) + static_cast<int64_t>(kBoundaryCost) * k;
+    };
+    if (maxc(BH - 1) < T) return NP;
+    int a = 0, b = BH - 1;
+    while (a < b) {
+      const int mid = (a + b) >> 1;
+      if (maxc(mid) >= T) b = mid; else a = mid + 1;
+    }
+    const int64_t g = (T - static_cast<int64_t>(kBoundaryCost) * a + 1) / 2;
+    return static_cast<int>(min(static_cast<int64_t>(NP), max(static_cast<int64_t>(pref[a]), g)));
+  };
+  const int r0 = slice_start(gw);
+  const int r1 = gw + 1 < NW ? slice_start(gw + 1) : NP;
+  if (r1 <= r0) return;  // an empty slice (between two (b, h) with empty ones in between)
   const int n_my = r1 - r0;
 
   // first (b, h) of the slice: the one whose page range holds page r0
@@ -428,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
           }
         }
       } else {
-        const int w_first = warp_of(pref[cbh], NP, NW);
-        const int w_last = warp_of(pref[cbh + 1] - 1, NP, NW);
+        const int w_first = slice_of(pref[cbh], cbh, NW, c_end);
+        const int w_last = slice_of(pref[cbh + 1] - 1, cbh, NW, c_end);
         const size_t slot = static_cast<size_t>(gw) + cbh;
         if (rowsel == 0) {
 #pragma unroll
