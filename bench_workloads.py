@@ -256,7 +256,6 @@ def llama65b_mha(kvp, dev, peaks, seed=0, steps=32, n_layers=8):
     qs = _randn_bf16((steps, n_layers, B, H, d), g, dev)
     out = torch.empty(B, H, d, dtype=torch.float32, device=dev)
     s_new = torch.empty(B, H, dtype=torch.float32, device=dev)
-    ws_n = torch.empty(kvp.kvp_score_workspace_bytes(0, B, D, H), dtype=torch.uint8, device=dev)
     ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, H, H, d), dtype=torch.uint8, device=dev)
 
     def restore():
@@ -265,11 +264,15 @@ def llama65b_mha(kvp, dev, peaks, seed=0, steps=32, n_layers=8):
             for dst, src in zip((c.expire_pool, c.page_table, c.remap, c.count), L["snap"]):
                 dst.copy_(src)
 
+    for L in layers:  # each layer's scorer weight in tensor-core form, once, like the weight itself
+        L["w_split"] = kvp.kvp_score_split_weight(L["w"])
+
     def decode():
         for i in range(steps):
             t = T + i
             for li, L in enumerate(layers):
-                kvp.kvp_score(xs[i, li], L["w"], out=s_new, workspace=ws_n, status=st)
+                kvp.kvp_score(xs[i, li], L["w_split"], scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H,
+                              out=s_new, status=st)
                 kvp.kvp_append(L["cache"], ks[i, li], vs[i, li], t, mode=kvp.KVP_MASK_KVZAP, score=s_new,
                                tau=L["tau"], status=st)
                 kvp.kvp_decode_attn(qs[i, li], L["cache"], t, out=out, workspace=ws_a, status=st)

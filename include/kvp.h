@@ -69,7 +69,7 @@ typedef enum kvp_status {
                                the access is skipped, never performed */
 } kvp_status;
 
-enum { KVP_SCORER_LINEAR = 0, KVP_SCORER_MLP = 1 };
+enum { KVP_SCORER_LINEAR = 0, KVP_SCORER_MLP = 1, KVP_SCORER_LINEAR_SPLIT = 2 };
 enum { KVP_MASK_KVZAP = 0, KVP_MASK_DMS = 1 };
 
 #define KVP_PAGE_TOKENS 16            /* rows per page of the compacted cache */
@@ -97,22 +97,40 @@ KVP_API int kvp_version(void);
  * x          device bf16 [n_tok, D], row stride ld_x elements (multiple of 8,
  *            >= D), base 16-byte aligned
  * w          LINEAR: device fp32 [H, D] (a linear layer's weight layout)
+ *            LINEAR_SPLIT: device bf16, the operand kvp_score_split_weight
+ *                    wrote for this (D, H), 16-byte aligned
  *            MLP:    device bf16 W1 [hidden, D]
  * b          LINEAR: device fp32 [H] or NULL;  MLP: device fp32 b1 [hidden] or NULL
  * w2         MLP: device bf16 [H, hidden];  LINEAR: must be NULL
  * b2         MLP: device fp32 [H] or NULL;  LINEAR: must be NULL
  * scores     device fp32 [n_tok, H] (output, token-major)
  * workspace  device, >= kvp_score_workspace_bytes(...) bytes, 256-byte aligned
+ *            (LINEAR_SPLIT needs none: NULL and 0 are accepted)
  *
  * The dense contraction runs on the tcgen05 tensor cores: LINEAR splits the
  * fp32 weight into two bf16 halves (hi + lo) so that the products keep ~16
- * mantissa bits of w; accumulation is fp32 throughout.
+ * mantissa bits of w; accumulation is fp32 throughout. LINEAR does that split
+ * on every call (one small kernel); a caller whose weight does not change
+ * between calls (a decode loop: the weight is the layer's) splits it once with
+ * kvp_score_split_weight and passes LINEAR_SPLIT; the scores are identical.
  */
 KVP_API size_t kvp_score_workspace_bytes(int scorer, int64_t n_tok, int d_model, int n_kv_heads, int hidden);
 KVP_API kvp_status kvp_score(int scorer, int64_t n_tok, int d_model, int n_kv_heads, int hidden,
                      const void* x, int64_t ld_x, const void* w, const float* b,
                      const void* w2, const float* b2, float* scores,
                      void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* kvp_score_split_weight - the KVzap-Linear weight in the form the scorer's
+ * tensor cores take (no page describes this step; it is how this library
+ * keeps fp32 weights on bf16 tensor cores): w_split is bf16
+ * [rows, D] with rows = kvp_score_split_weight_bytes / (2 D), row 2h =
+ * bf16(w[h]) (round to nearest even), row 2h+1 = bf16(w[h] - bf16(w[h])), and
+ * rows >= 2H zero. w device fp32 [H, D]; w_split device, >= the size below,
+ * 16-byte aligned. D a multiple of 8, H 1..64.
+ */
+KVP_API size_t kvp_score_split_weight_bytes(int d_model, int n_kv_heads);
+KVP_API kvp_status kvp_score_split_weight(int d_model, int n_kv_heads, const float* w, void* w_split,
+                                          size_t w_split_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* kvp_mask - keep/evict decision per (batch, kv head, position) (KVzap

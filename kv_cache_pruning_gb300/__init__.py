@@ -33,6 +33,7 @@ KVP_ERR_BOUNDS = 8
 
 KVP_SCORER_LINEAR = 0
 KVP_SCORER_MLP = 1
+KVP_SCORER_LINEAR_SPLIT = 2
 KVP_MASK_KVZAP = 0
 KVP_MASK_DMS = 1
 PAGE = 16
@@ -64,6 +65,8 @@ _SIGS = {
     "kvp_status_string": (ctypes.c_char_p, [_I]),
     "kvp_version": (_I, []),
     "kvp_score_workspace_bytes": (_S, [_I, _L, _I, _I, _I]),
+    "kvp_score_split_weight_bytes": (_S, [_I, _I]),
+    "kvp_score_split_weight": (_I, [_I, _I, _P, _P, _S, _P]),
     "kvp_score": (_I, [_I, _L, _I, _I, _I, _P, _L, _P, _P, _P, _P, _P, _P, _S, _P, _P]),
     "kvp_mask": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "kvp_compact_workspace_bytes": (_S, [_I, _I, _I]),
@@ -141,11 +144,29 @@ def kvp_score_workspace_bytes(scorer, n_tok, d_model, n_kv_heads, hidden=0) -> i
     return _lib.kvp_score_workspace_bytes(scorer, n_tok, d_model, n_kv_heads, hidden)
 
 
-def kvp_score(x, w, b=None, w2=None, b2=None, *, scorer=KVP_SCORER_LINEAR, out=None, workspace=None,
-              status=None, stream=None):
+def kvp_score_split_weight_bytes(d_model, n_kv_heads) -> int:
+    return _lib.kvp_score_split_weight_bytes(d_model, n_kv_heads)
+
+
+def kvp_score_split_weight(w, *, out=None, stream=None):
+    """The KVzap-Linear weight w fp32 [H, D] as the scorer's bf16 hi/lo operand (rows 2h, 2h+1), for
+    kvp_score(..., scorer=KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H)."""
+    H, D = w.shape
+    nbytes = kvp_score_split_weight_bytes(D, H)
+    if out is None:
+        out = torch.empty((nbytes // (2 * D), D), dtype=torch.bfloat16, device=w.device)
+    code = _lib.kvp_score_split_weight(D, H, _ptr(w, torch.float32, "w"), _ptr(out, torch.bfloat16, "out"),
+                                       out.numel() * out.element_size(), _stream(stream))
+    _check("kvp_score_split_weight", code)
+    return out
+
+
+def kvp_score(x, w, b=None, w2=None, b2=None, *, scorer=KVP_SCORER_LINEAR, n_kv_heads=None, out=None,
+              workspace=None, status=None, stream=None):
     """scores[n_tok, H] from hidden states x[n_tok, D] (bf16).
 
     LINEAR: w fp32 [H, D], b fp32 [H] or None.
+    LINEAR_SPLIT: w the bf16 operand from kvp_score_split_weight, n_kv_heads = H, b as for LINEAR.
     MLP:    w bf16 W1 [hidden, D], b fp32 b1 [hidden] or None, w2 bf16 [H, hidden], b2 fp32 [H] or None.
     """
     if x.dim() != 2:
@@ -156,6 +177,11 @@ def kvp_score(x, w, b=None, w2=None, b2=None, *, scorer=KVP_SCORER_LINEAR, out=N
     if scorer == KVP_SCORER_LINEAR:
         H, hidden = w.shape[0], 0
         wp = _ptr(w, torch.float32, "w")
+    elif scorer == KVP_SCORER_LINEAR_SPLIT:
+        if n_kv_heads is None:
+            raise ValueError("LINEAR_SPLIT needs n_kv_heads")
+        H, hidden = int(n_kv_heads), 0
+        wp = _ptr(w, torch.bfloat16, "w_split")
     else:
         hidden, H = w.shape[0], w2.shape[0]
         wp = _ptr(w, torch.bfloat16, "w1")

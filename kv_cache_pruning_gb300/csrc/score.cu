@@ -334,11 +334,31 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 using namespace kvp;
 
+extern "C" size_t kvp_score_split_weight_bytes(int d_model, int n_kv_heads) {
+  if (d_model <= 0 || n_kv_heads <= 0) return 0;
+  return static_cast<size_t>(linear_bn(n_kv_heads)) * d_model * 2;
+}
+
+extern "C" kvp_status kvp_score_split_weight(int d_model, int n_kv_heads, const float* w, void* w_split,
+                                             size_t w_split_bytes, void* stream) {
+  if (d_model <= 0 || n_kv_heads <= 0 || w == nullptr || w_split == nullptr) return KVP_ERR_INVALID;
+  if (d_model % 8 != 0 || d_model > 65536 || n_kv_heads > 64) return KVP_ERR_UNSUPPORTED;
+  if (w_split_bytes < kvp_score_split_weight_bytes(d_model, n_kv_heads)) return KVP_ERR_WORKSPACE;
+  if (!aligned16(w_split)) return KVP_ERR_ALIGN;
+  const int bn = linear_bn(n_kv_heads);
+  const size_t nel = static_cast<size_t>(bn) * d_model;
+  const int blocks = static_cast<int>((nel + 255) / 256 < 4096 ? (nel + 255) / 256 : 4096);
+  split_weight_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      w, n_kv_heads, d_model, bn, static_cast<__nv_bfloat16*>(w_split));
+  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
 extern "C" size_t kvp_score_workspace_bytes(int scorer, int64_t n_tok, int d_model, int n_kv_heads, int hidden) {
   if (n_tok < 0 || d_model <= 0 || n_kv_heads <= 0) return 0;
   if (scorer == KVP_SCORER_LINEAR) {
     return static_cast<size_t>(linear_bn(n_kv_heads)) * d_model * 2;
   }
+  if (scorer == KVP_SCORER_LINEAR_SPLIT) return 0;
   if (scorer == KVP_SCORER_MLP) {
     if (hidden <= 0) return 0;
     return static_cast<size_t>(hidden / kMlpBN) * n_tok * n_kv_heads * sizeof(float);
@@ -350,16 +370,19 @@ extern "C" kvp_status kvp_score(int scorer, int64_t n_tok, int d_model, int n_kv
                                 int64_t ld_x, const void* w, const float* b, const void* w2, const float* b2,
                                 float* scores, void* workspace, size_t workspace_bytes, int32_t* status,
                                 void* stream) {
-  if (scorer != KVP_SCORER_LINEAR && scorer != KVP_SCORER_MLP) return KVP_ERR_INVALID;
+  if (scorer != KVP_SCORER_LINEAR && scorer != KVP_SCORER_MLP && scorer != KVP_SCORER_LINEAR_SPLIT)
+    return KVP_ERR_INVALID;
   if (n_tok < 0 || d_model <= 0 || n_kv_heads <= 0) return KVP_ERR_INVALID;
   if (n_tok == 0) return KVP_OK;
   if (x == nullptr || w == nullptr || scores == nullptr) return KVP_ERR_INVALID;
   if (ld_x < d_model) return KVP_ERR_INVALID;
   if (d_model % 8 != 0 || d_model > 65536 || n_kv_heads > 64) return KVP_ERR_UNSUPPORTED;
   if (ld_x % 8 != 0 || !aligned16(x)) return KVP_ERR_ALIGN;
+  if (scorer != KVP_SCORER_MLP && (w2 != nullptr || b2 != nullptr)) return KVP_ERR_INVALID;
+  if (scorer == KVP_SCORER_LINEAR_SPLIT && !aligned16(w)) return KVP_ERR_ALIGN;
   if (n_tok > (int64_t(1) << 31) - 1) return KVP_ERR_UNSUPPORTED;
   const size_t need = kvp_score_workspace_bytes(scorer, n_tok, d_model, n_kv_heads, hidden);
-  if (workspace == nullptr || workspace_bytes < need) return KVP_ERR_WORKSPACE;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return KVP_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVP_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -373,14 +396,15 @@ extern "C" kvp_status kvp_score(int scorer, int64_t n_tok, int d_model, int n_kv
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, x, n_tok, d_model, ld_x, kBM)) return KVP_ERR_CUDA;
 
-  if (scorer == KVP_SCORER_LINEAR) {
-    if (w2 != nullptr || b2 != nullptr) return KVP_ERR_INVALID;
+  if (scorer == KVP_SCORER_LINEAR || scorer == KVP_SCORER_LINEAR_SPLIT) {
     const int bn = linear_bn(n_kv_heads);
-    auto* wt = static_cast<__nv_bfloat16*>(workspace);
-    const size_t nel = static_cast<size_t>(bn) * d_model;
-    const int blocks = static_cast<int>((nel + 255) / 256 < 4096 ? (nel + 255) / 256 : 4096);
-    split_weight_kernel<<<blocks, 256, 0, st>>>(static_cast<const float*>(w), n_kv_heads, d_model, bn, wt);
-    if (cudaGetLastError() != cudaSuccess) return KVP_ERR_CUDA;
+    const void* wt = w;
+    if (scorer == KVP_SCORER_LINEAR) {
+      const kvp_status s = kvp_score_split_weight(d_model, n_kv_heads, static_cast<const float*>(w), workspace,
+                                                  workspace_bytes, stream);
+      if (s != KVP_OK) return s;
+      wt = workspace;
+    }
     if (!make_tmap(&tb, wt, bn, d_model, d_model, bn)) return KVP_ERR_CUDA;
     p.n_tiles = 1;
     p.bias = b;

@@ -48,6 +48,10 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_sizes(lib):
     lib.kvp_score_workspace_bytes.restype = ctypes.c_size_t
+    lib.kvp_score_split_weight_bytes.restype = ctypes.c_size_t
+    assert lib.kvp_score_split_weight_bytes(4096, 8) == 16 * 4096 * 2   # 2H rows padded to 16
+    assert lib.kvp_score_split_weight_bytes(256, 20) == 64 * 256 * 2
+    assert lib.kvp_score_workspace_bytes(2, 1000, 4096, 8, 0) == 0      # LINEAR_SPLIT needs none
     lib.kvp_score_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     # LINEAR: bf16 hi/lo weight rows, padded to 16 rows for 8 heads
     assert lib.kvp_score_workspace_bytes(0, 131072, 4096, 8, 0) == 16 * 4096 * 2
@@ -66,6 +70,14 @@ def test_host_validation_without_gpu(lib):
     assert L.kvp_score(0, 10, 64, 65, 0, 16, 64, 16, None, None, None, 16, 16, 1 << 20, None, None) == k.KVP_ERR_UNSUPPORTED
     assert L.kvp_score(0, 10, 64, 2, 0, 18, 64, 16, None, None, None, 16, 16, 1 << 20, None, None) == k.KVP_ERR_ALIGN
     assert L.kvp_score(0, 10, 64, 2, 0, 16, 64, 16, None, None, None, 16, 16, 8, None, None) == k.KVP_ERR_WORKSPACE
+    # weight split: bad sizes, short output, unaligned output
+    assert L.kvp_score_split_weight(0, 8, 16, 16, 1 << 20, None) == k.KVP_ERR_INVALID
+    assert L.kvp_score_split_weight(4100, 8, 16, 16, 1 << 20, None) == k.KVP_ERR_UNSUPPORTED
+    assert L.kvp_score_split_weight(4096, 8, 16, 16, 16 * 4096 * 2 - 1, None) == k.KVP_ERR_WORKSPACE
+    assert L.kvp_score_split_weight(4096, 8, 16, 24, 1 << 20, None) == k.KVP_ERR_ALIGN
+    # scorer on a pre-split weight: unaligned weight, MLP-only arguments
+    assert L.kvp_score(2, 10, 64, 2, 0, 16, 64, 24, None, None, None, 16, None, 0, None, None) == k.KVP_ERR_ALIGN
+    assert L.kvp_score(2, 10, 64, 2, 0, 16, 64, 16, None, 16, None, 16, None, 0, None, None) == k.KVP_ERR_INVALID
     # mask: both inputs given / unknown mode
     assert L.kvp_mask(0, 1, 1, 8, 0, 16, 16, 16, 128, 0, 7, 16, None, None, None) == k.KVP_ERR_INVALID
     assert L.kvp_mask(5, 1, 1, 8, 0, 16, 16, None, 128, 0, 7, 16, None, None, None) == k.KVP_ERR_INVALID

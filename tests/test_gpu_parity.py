@@ -51,6 +51,34 @@ def test_score_linear_strided_rows(kvp):
     check_scores(s.cpu().numpy(), orc.score_linear(x[:, :D], w[:, :D]), _linear_scale(x[:, :D], w[:, :D]))
 
 
+def test_score_linear_split_weight(kvp):
+    # the pre-split operand: row 2h = bf16(w[h]) (round to nearest even), row
+    # 2h+1 = bf16(w[h] - bf16(w[h])), rows past 2H zero; scores from it are
+    # bit-identical to the LINEAR call and within the oracle tolerance
+    n_tok, D, H = 3000, 4096, 8
+    x, w = syn.linear_inputs(4, n_tok, D, H)
+    b = syn.normal_f32(4, 30, (H,))
+    wd = dev_f32(w)
+    ws = kvp.kvp_score_split_weight(wd)
+    torch.cuda.synchronize()
+    assert ws.shape == (16, D) and ws.dtype == torch.bfloat16
+    wt = torch.from_numpy(np.asarray(w, np.float32))
+    hi = wt.to(torch.bfloat16)
+    lo = (wt - hi.float()).to(torch.bfloat16)
+    got = ws.cpu()
+    assert torch.equal(got[0:2 * H:2].view(torch.int16), hi.view(torch.int16))
+    assert torch.equal(got[1:2 * H:2].view(torch.int16), lo.view(torch.int16))
+    assert not got[2 * H:].float().any()
+    xd = dev_bf16(x)
+    s_lin = kvp.kvp_score(xd, wd, dev_f32(b))
+    s_split = kvp.kvp_score(xd, ws, dev_f32(b), scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H)
+    torch.cuda.synchronize()
+    assert torch.equal(s_lin, s_split)
+    ref = orc.score_linear(x, w, b)
+    scale = np.sqrt(orc.widen_bf16(x) ** 2 @ (np.asarray(w, np.float64) ** 2).T)
+    check_scores(s_split.cpu().numpy(), ref, scale)
+
+
 @pytest.mark.parametrize("n_tok,D,hidden,H,bias", [
     (300, 512, 512, 8, True),
     (128, 256, 1024, 8, False),
