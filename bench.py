@@ -420,6 +420,7 @@ def run_gpu(args, rank: int, world: int):
         "config": dict(config_desc(w), cuda_graph=graph is not None), "e2e": e2e,
         "gpu_launches": KERNELS_PER_STEP * args.steps, "roofline": roofline,
         "kernels": kernels, "effective_step_GB_s": step_b / (ms_step * 1e-3) / 1e9,
+        "scored_tokens_per_s": n_tok / (k_ms[0] * 1e-3),
         "kept_fraction": kept / (B * H * T), "clocks": clocks, "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -434,7 +435,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs only)")
     ap.add_argument("--workload", default="llama3_8b_layer",
-                    choices=["llama3_8b_layer", "mlp_prefill", "dms_decode", "llama65b_mha"],
+                    choices=["llama3_8b_layer", "mlp_prefill", "dms_decode", "llama65b_mha", "prune_sweep"],
                     help="llama3_8b_layer = the bench line; the others print measurement lines "
                          "(see bench_workloads.py)")
     ap.add_argument("--eager", action="store_true", help="launch every step from the host (no CUDA graph)")

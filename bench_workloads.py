@@ -14,6 +14,9 @@ rest of the path on the shapes it is quoted for:
   llama65b_mha   8 MHA layers (64 heads, d_model 8192), batch 1, 131,072 cached
                  tokens, KVzap-Linear with per-(layer, head) keep rates ~Beta(2,5),
                  then 32 decode steps over all 8 layers
+  prune_sweep    decode attention on the Llama-3-8B-shaped cache at pruning
+                 levels 0 / 50 / 75 / 87.5 / 93.75 / 96.9 %: tokens/s against the
+                 inverse of the kept fraction
 
 Decode loops are captured once in a CUDA graph (the C-ABI calls only enqueue
 work on the current stream) and replayed for timing, so host launch overhead
@@ -298,7 +301,60 @@ def llama65b_mha(kvp, dev, peaks, seed=0, steps=32, n_layers=8):
     }
 
 
-RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha}
+def prune_sweep(kvp, dev, peaks, seed=0, calls=10, reps=5):
+    """Decode attention over the Llama-3-8B-shaped cache (batch 16, 8,192 cached
+    tokens, 32 q / 8 kv heads, head_dim 128) at several pruning levels: the
+    threshold at each head's q-quantile score, 128-token window, q = 0 keeps
+    everything. The kernel reads only surviving pages, so decode tokens/s should
+    rise as the inverse of the kept fraction while the kernel stays HBM-bound;
+    fixed per-call costs bend the curve at high pruning."""
+    B, T, H, Hq, d, W = 16, 8192, 8, 32, 128, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    K = _randn_bf16((B, T, H, d), g, dev)
+    V = _randn_bf16((B, T, H, d), g, dev)
+    q = _randn_bf16((B, Hq, d), g, dev)
+    s = torch.randn((B, T, H), generator=g, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    mp = (T + 15) // 16
+    cache = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp, device=dev)
+    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+    ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
+    points = []
+    for prune_q in (0.0, 0.5, 0.75, 0.875, 0.9375, 0.96875):
+        tau = (torch.full((B, H), -math.inf, device=dev) if prune_q == 0.0 else _tau_quantile(s, prune_q))
+        expire, _, _ = kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=T - 1,
+                                    scores=s.view(B * T, H), tau=tau, window=W, want_bits=False)
+        kvp.kvp_compact(K, V, expire, T - 1, 0, cache, status=st, workspace=ws_c)
+        torch.cuda.synchronize()
+        assert st.item() == 0, kvp.status_string(st.item())
+        kept = int(cache.count.sum().item())
+        pages = int(((cache.count + 15) // 16).sum().item())
+
+        def calls_fn():
+            for _ in range(calls):
+                kvp.kvp_decode_attn(q, cache, T - 1, out=out, workspace=ws_a, status=st)
+
+        replay = _graph(calls_fn)
+        ms = _time(replay, reps=reps) / calls
+        nbytes = pages * 16 * (2 * d * 2 + 4) + B * Hq * d * (2 + 4)
+        points.append({"prune_q": prune_q, "kept_fraction": kept / (B * H * T), "surviving_pages": pages,
+                       "decode_attn_us": ms * 1e3, "decode_tokens_per_s": B / (ms * 1e-3),
+                       "GB_s": nbytes / (ms * 1e-3) / 1e9, "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks[0]})
+    assert st.item() == 0, kvp.status_string(st.item())
+    base = points[0]
+    for p in points:
+        p["speedup_vs_keep_all"] = p["decode_tokens_per_s"] / base["decode_tokens_per_s"]
+        p["inverse_kept_ratio"] = base["kept_fraction"] / p["kept_fraction"]
+    return {"workload": "prune_sweep: decode attention, batch 16, 8192 cached tokens, 32 q / 8 kv heads, "
+                        "head_dim 128, threshold at each head's q-quantile score, 128-token window; "
+                        "each point = a CUDA graph of 10 calls",
+            "points": points}
+
+
+RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha,
+           "prune_sweep": prune_sweep}
 
 
 def run(name, kvp, dev, peaks):

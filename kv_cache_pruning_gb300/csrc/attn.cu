@@ -28,7 +28,12 @@ constexpr int kWarps = 8;       // warps per CTA
 constexpr int kNst = 3;         // pages in flight per warp
 constexpr int kMaxBH = 4096;    // (b, h) pairs whose page prefix fits in shared memory
 constexpr int kMaxCtas = 512;   // grid bound used to size the workspace
-constexpr int kMinPages = 8;    // fewest pages a warp's slice gets when there are enough
+// Fewest pages a warp's slice gets when there are not enough pages for every
+// warp of the grid: 8 when the average (b, h) has 64 pages or more (fewer
+// pieces to merge), else 4 (more warps streaming). Measured on a GB300: 4 x
+// 8192 tokens at 75 % pruned 20.7 us with 8 against 21.9 us with 4; 16 x 8192
+// at 93.75 % pruned 24.8 us with 8 against 20.7 us with 4.
+constexpr int kMinPagesLong = 8, kMinPagesShort = 4;
 constexpr int kThreads = kWarps * 32;
 
 template <int D, int G>
@@ -190,10 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   if (NP == 0) return;
 
   // ---- this warp's slice of the global page list
-  // slices of at least kMinPages pages (fewer pieces to merge on small
+  // slices of at least min_pages pages (fewer pieces to merge on small
   // problems); every one of the first NW slices is non-empty
   const int nw_all = gridDim.x * kWarps;
-  const int NW = max(1, min(nw_all, NP / kMinPages));
+  const int min_pages = NP >= 64 * BH ? kMinPagesLong : kMinPagesShort;
+  const int NW = max(1, min(nw_all, NP / min_pages));
   const int gw = warp * gridDim.x + blockIdx.x;  // slices go round-robin over the CTAs (all SMs busy)
   if (gw >= NW) return;
   int last_bh = 0;  // (b, h) of the last page
