@@ -103,7 +103,9 @@ def test_score_mlp(kvp, n_tok, D, hidden, H, bias):
 
 # --------------------------------------------------------------------------- mask
 
-@pytest.mark.parametrize("B,T,H,window", [(1, 512, 2, 128), (3, 1000, 5, 128), (2, 33, 3, 7), (1, 4096, 8, 0)])
+@pytest.mark.parametrize("B,T,H,window", [(1, 512, 2, 128), (3, 1000, 5, 128), (2, 33, 3, 7), (1, 4096, 8, 0),
+                                          (2, 700, 12, 128),   # two batches of heads per thread
+                                          (1, 300, 70, 128)])  # heads past the shared-memory counts
 def test_mask_kvzap_bit_exact(kvp, B, T, H, window):
     s = syn.normal_f32(2, 11, (B, T, H))
     s[0, 5, 0] = np.nan
