@@ -401,7 +401,8 @@ def run_gpu(args, rank: int, world: int):
         torch.cuda.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
         e2e = {"value": weak_scaling_value(B, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms, "steps": n_e2e}
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms, "steps": n_e2e,
+               "h2d_GB_s": h2d / (e_ms * 1e-3) / 1e9}
 
     if rank != 0:
         return
