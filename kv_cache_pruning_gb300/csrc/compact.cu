@@ -299,7 +299,10 @@ KVP_DEV void cp_async_wait_all() {
 // The segment's expire values, the counts of the segments before it and
 // (up to kFusedBH pairs) the counts of all pairs are requested together
 // before any of them is used.
-constexpr int kStage = 32;
+// Entries per warp batch: 20 (45 KB of stage per CTA, 5 CTAs and 20 warps per
+// SM) measured best on a GB300 at 16 x 8192 tokens, 26 % kept: 51.7 us against
+// 53.6 / 54.7 / 54.9 us for 16 / 24 / 32.
+constexpr int kStage = 20;
 
 template <int D>
 constexpr int scatter_smem_bytes() {
