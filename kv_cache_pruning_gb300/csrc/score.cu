@@ -10,11 +10,14 @@
 //               (both K-major, 128-byte swizzle) into a STAGES-deep ring
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128xBNx16, fp32
 //               accumulators double-buffered in tensor memory
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, then
-//               LINEAR: s_h = acc[2h] + acc[2h+1] + b_h (weight rows interleave
+//   epilogue    tcgen05.ld of the accumulator rows, then
+//               LINEAR (warps 2..5, one per TMEM lane quadrant):
+//                       s_h = acc[2h] + acc[2h+1] + b_h (weight rows interleave
 //                       the bf16 high and low halves of the fp32 weight)
-//               MLP:    GELU(acc + b1) dotted with W2 over this 256-wide hidden
-//                       chunk -> per-chunk partial scores
+//               MLP (warps 2..9, two per quadrant, each taking 128 of the 256
+//                       hidden columns): GELU(acc + b1) dotted with W2; the
+//                       upper half's partial scores are added to the lower
+//                       half's through shared memory -> per-chunk partials
 // A small reduction kernel then sums the MLP chunk partials in a fixed order.
 #include "kvp_common.cuh"
 
@@ -23,9 +26,16 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kThreads = 192;
 constexpr int kMlpBN = 256;
 constexpr int kMlpMaxH = 16;
+
+enum { kEpiLinear = 0, kEpiMlp = 1 };
+// TMA warp, MMA warp, then 4 epilogue warps (LINEAR) or 8 (MLP: its GELU and
+// W2 epilogue is the long pole, so two warps share each lane quadrant).
+template <int EPI>
+constexpr int epi_threads() { return EPI == kEpiMlp ? 256 : 128; }
+template <int EPI>
+constexpr int score_threads() { return 64 + epi_threads<EPI>(); }
 
 template <int BN>
 struct ScoreCfg {
@@ -35,7 +45,9 @@ struct ScoreCfg {
   static constexpr int kStages = BN <= 32 ? 8 : (BN <= 128 ? 6 : 4);
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int kBarBytes = 256;
-  static constexpr int kEpiBytes = (BN == kMlpBN) ? (kMlpBN * kMlpMaxH * 4 + kMlpBN * 4) : 0;
+  // MLP: W2 columns and b1 of the hidden chunk, then the upper half's partial
+  // scores [2 accumulator buffers][128 rows][kMlpMaxH]
+  static constexpr int kEpiBytes = (BN == kMlpBN) ? (kMlpBN * kMlpMaxH * 4 + kMlpBN * 4 + 2 * kBM * kMlpMaxH * 4) : 0;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kEpiBytes;
   static_assert(kBBytes % 1024 == 0, "B tile must keep 1024-byte alignment");
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -54,12 +66,23 @@ struct ScoreParams {
   int32_t* status;
 };
 
-enum { kEpiLinear = 0, kEpiMlp = 1 };
-
 KVP_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// Barrier over n threads that also ORs v across them (every one of the n must reach it).
+KVP_DEV bool named_bar_or(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(score_threads<EPI>(), 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const ScoreParams p) {
   using C = ScoreCfg<BN>;
@@ -74,6 +97,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* w2s = reinterpret_cast<float*>(tiles + C::kStages * C::kStageBytes + C::kBarBytes);
   float* b1s = w2s + kMlpBN * kMlpMaxH;
+  float* comb = b1s + kMlpBN;  // MLP: upper-half partial scores [2][kBM][kMlpMaxH]
+  constexpr int kEpi = epi_threads<EPI>();
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -85,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], kEpi);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -169,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int quad = warp & 3;          // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;   // MLP: which 128 of the 256 hidden columns (LINEAR: 0)
     const int row = quad * 32 + lane;
     const int etid = threadIdx.x - 64;
     uint32_t acc = 0, acc_phase = 0;
@@ -178,21 +204,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = t / p.n_tiles, nt = t - mt * p.n_tiles;
       if constexpr (EPI == kEpiMlp) {
         if (nt != cur_nt) {  // stage this hidden chunk's W2 columns and b1 as fp32
-          named_bar_sync(1, 128);
+          named_bar_sync(1, kEpi);
           const int H = p.n_heads;
-          for (int i = etid; i < kMlpBN * H; i += 128) {
+          for (int i = etid; i < kMlpBN * H; i += kEpi) {
             const int c = i / H, h = i - c * H;
             const uint32_t w = p.w2[static_cast<size_t>(h) * p.hidden + nt * kMlpBN + c];
             w2s[c * H + h] = __uint_as_float(w << 16);
           }
-          for (int c = etid; c < kMlpBN; c += 128) b1s[c] = p.bias ? p.bias[nt * kMlpBN + c] : 0.f;
-          named_bar_sync(1, 128);
+          for (int c = etid; c < kMlpBN; c += kEpi) b1s[c] = p.bias ? p.bias[nt * kMlpBN + c] : 0.f;
+          named_bar_sync(1, kEpi);
           cur_nt = nt;
         }
       }
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) {
-        record_error(p.status, KVP_ERR_TIMEOUT);
-        *abort_flag = 1;
+      const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
+      if (named_bar_or(3, kEpi, !ok)) {  // every epilogue thread leaves together
+        if (etid == 0) {
+          record_error(p.status, KVP_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
         break;
       }
       tc_fence_after();
@@ -217,11 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float part[kMlpMaxH];
 #pragma unroll
         for (int h = 0; h < kMlpMaxH; ++h) part[h] = 0.f;
+        constexpr int kCols = kMlpBN / 2;
 #pragma unroll 1
-        for (int cc = 0; cc < kMlpBN; cc += 32) {
+        for (int cc = half * kCols; cc < (half + 1) * kCols; cc += 32) {
           float v[32];
           tmem_ld32(taddr + cc, v);
-          if (cc == kMlpBN - 32) {
+          if (cc == (half + 1) * kCols - 32) {
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
           }
@@ -235,11 +265,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (h < H) part[h] = fmaf(z, wr[h], part[h]);
           }
         }
-        if (grow < p.n_tok) {
+        float* cb = comb + (acc * kBM + row) * kMlpMaxH;
+        if (half == 1) {
+#pragma unroll
+          for (int h = 0; h < kMlpMaxH; ++h) cb[h] = part[h];
+        }
+        named_bar_sync(2, kEpi);  // the buffer of this accumulator is next written two tiles on
+        if (half == 0 && grow < p.n_tok) {
           float* o = p.out + (static_cast<size_t>(nt) * p.n_tok + grow) * H;
 #pragma unroll
           for (int h = 0; h < kMlpMaxH; ++h)
-            if (h < H) o[h] = part[h];
+            if (h < H) o[h] = part[h] + cb[h];
         }
       }
       acc ^= 1u;
@@ -323,7 +359,7 @@ kvp_status launch_score(const CUtensorMap& ta, const CUtensorMap& tb, const Scor
   if (nsm <= 0) return KVP_ERR_CUDA;
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < nsm ? tiles : nsm;
-  score_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmem, st>>>(ta, tb, p);
+  score_tc_kernel<BN, EPI><<<grid, score_threads<EPI>(), C::kSmem, st>>>(ta, tb, p);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
