@@ -50,7 +50,7 @@ struct AttnCfg {
   static constexpr int RING_BYTES = kWarps * kNst * STAGE_BYTES;
   static constexpr int PS_FLOATS = RPS * G * RS;  // per warp
   static constexpr int PS_BYTES = kWarps * PS_FLOATS * 4;
-  static constexpr int BAR_BYTES = kWarps * kNst * 8;
+  static constexpr int BAR_BYTES = kWarps * (kNst + 1) * 8;  // per warp: ring stages, then its merge
   static constexpr int PREF_BYTES = (kMaxBH + 1) * 4;
   static constexpr int SMEM = RING_BYTES + PS_BYTES + BAR_BYTES + PREF_BYTES;
   static_assert(G <= LPR, "group larger than lanes per row");
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   const int BH = p.B * p.H;
   uint8_t* ring = smem + warp * kNst * C::STAGE_BYTES;
   float* p_s = reinterpret_cast<float*>(smem + C::RING_BYTES) + warp * C::PS_FLOATS;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES + C::PS_BYTES) + warp * kNst;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES + C::PS_BYTES) + warp * (kNst + 1);
   int* pref = reinterpret_cast<int*>(smem + C::RING_BYTES + C::PS_BYTES + C::BAR_BYTES);
 
   // ---- page prefix over (b, h), identical in every CTA
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
     bulk_g2s(dst + 2 * C::PAGE_BYTES, p.expire_pool + phys * kPage, kPage * 4, &bars[st]);
   };
   if (lane == 0) {
-    for (int st = 0; st < kNst; ++st) mbar_init(&bars[st], 1);
+    for (int st = 0; st <= kNst; ++st) mbar_init(&bars[st], 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
     for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
   }
 
+  uint32_t merge_par = 0;  // phase of this warp's merge barrier
   for (int k = 0; k < n_my; ++k) {
     const int g = r0 + k;
     const int st = k % kNst;
@@ -506,8 +507,87 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
           constexpr int F4 = G * D / 4;           // float4 of one piece's acc
           constexpr int FPL = (F4 + 31) / 32;     // ... per lane
           constexpr int JB = 16 / FPL < 8 ? (16 / FPL > 0 ? 16 / FPL : 1) : 8;  // pieces per batch of loads
+          constexpr int kAccB = G * D * 4, kMlB = G * 2 * 4;  // bytes of a piece's acc and (m, l)
+          constexpr int kStaged = (kNst * C::STAGE_BYTES - 32) / (kAccB + kMlB);  // pieces the idle ring holds
           const int npc = w_last - w_first + 1;
           const size_t s0 = static_cast<size_t>(w_first) + cbh;
+          if (g + 1 == r1 && npc <= kStaged) {
+            // End of the slice: this warp's ring is idle. The pieces sit in
+            // consecutive slots, so two bulk copies bring every acc and every
+            // (m, l) into it in one round trip.
+            float* sacc = reinterpret_cast<float*>(ring);
+            uint8_t* sml_raw = ring + static_cast<size_t>(npc) * kAccB;
+            const size_t ml0 = s0 * kMlB, ml_a = ml0 & ~size_t(15);
+            const size_t ml_b = (ml0 + static_cast<size_t>(npc) * kMlB + 15) & ~size_t(15);
+            const float* sml = reinterpret_cast<const float*>(sml_raw + (ml0 - ml_a));
+            if (lane == 0) {
+              fence_proxy_async();
+              mbar_arrive_expect_tx(&bars[kNst], static_cast<uint32_t>(npc * kAccB + (ml_b - ml_a)));
+              bulk_g2s(sacc, p.part_acc + s0 * G * D, static_cast<uint32_t>(npc * kAccB), &bars[kNst]);
+              bulk_g2s(sml_raw, reinterpret_cast<const uint8_t*>(p.part_ml) + ml_a, static_cast<uint32_t>(ml_b - ml_a),
+                       &bars[kNst]);
+            }
+            const bool okm = mbar_wait(&bars[kNst], merge_par, nullptr, p.status);
+            merge_par ^= 1u;
+            if (!__all_sync(0xffffffffu, okm)) {
+              if (lane == 0) record_error(p.status, KVP_ERR_TIMEOUT);
+              return;
+            }
+            float M[G], wr[G], L[G];
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+              const float m = lane < npc ? sml[lane * G * 2 + 2 * i] : -1e30f;
+              float mx = m;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+              M[i] = mx;
+              wr[i] = lane < npc ? exp2f(m - mx) : 0.f;
+              float l = wr[i] * (lane < npc ? sml[lane * G * 2 + 2 * i + 1] : 0.f);
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+              L[i] = l;
+            }
+            float4 A[FPL];
+#pragma unroll
+            for (int k2 = 0; k2 < FPL; ++k2) A[k2] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < npc; ++j) {
+#pragma unroll
+              for (int k2 = 0; k2 < FPL; ++k2) {
+                constexpr int kHeadF4 = D / 4;
+                const int h0 = (32 * k2) / kHeadF4 < G ? (32 * k2) / kHeadF4 : G - 1;
+                float w = __shfl_sync(0xffffffffu, wr[h0], j);
+                if constexpr (kHeadF4 < 32) {
+                  const int h1 = (32 * k2 + 16) / kHeadF4 < G ? (32 * k2 + 16) / kHeadF4 : G - 1;
+                  const float w1 = __shfl_sync(0xffffffffu, wr[h1], j);
+                  if (lane >= 16) w = w1;
+                }
+                const int f = lane + 32 * k2;
+                if (f < F4) {
+                  const float4 v = reinterpret_cast<const float4*>(sacc + static_cast<size_t>(j) * G * D)[f];
+                  A[k2].x = fmaf(w, v.x, A[k2].x);
+                  A[k2].y = fmaf(w, v.y, A[k2].y);
+                  A[k2].z = fmaf(w, v.z, A[k2].z);
+                  A[k2].w = fmaf(w, v.w, A[k2].w);
+                }
+              }
+            }
+#pragma unroll
+            for (int k2 = 0; k2 < FPL; ++k2) {
+              const int f = lane + 32 * k2;
+              if (f < F4) {
+                const int hd = f / (D / 4);
+                float Lh = L[0];
+#pragma unroll
+                for (int i = 1; i < G; ++i)
+                  if (hd == i) Lh = L[i];
+                const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
+                reinterpret_cast<float4*>(p.out + static_cast<size_t>(cbh) * G * D)[f] =
+                    make_float4(A[k2].x * inv, A[k2].y * inv, A[k2].z * inv, A[k2].w * inv);
+              }
+            }
+            if (lane == 0) p.pieces[cbh] = 0;
+            continue;  // the slice is done
+          }
           float M[G], mr[G], lr[G];
 #pragma unroll
           for (int i = 0; i < G; ++i) M[i] = -1e30f;
