@@ -122,6 +122,11 @@ KVP_DEV void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) 
 // pages skip the cross-lane max reduction altogether.
 constexpr float kLazyRescale = 8.0f;
 
+// Release/acquire fence at GPU scope: orders this thread's partial-state
+// stores before its arrival count, and the merger's loads after it sees the
+// final count (message passing needs no sequentially consistent fence).
+KVP_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 KVP_DEV int clamp_count(const int32_t* count, int bh, int max_pages) {
   return min(max(count[bh], 0), max_pages * kPage);
 }
@@ -493,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
           p.part_ml[(slot * G + lane) * 2] = mm;
           p.part_ml[(slot * G + lane) * 2 + 1] = ll;
         }
-        __threadfence();
+        fence_acq_rel_gpu();
         __syncwarp();
         int last = 0;
         if (lane == 0) last = atomicAdd(&p.pieces[cbh], 1) == (w_last - w_first);
@@ -503,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
           // pieces for the maxima and weights (one round of loads for up to
           // 32 pieces); then lanes take float4 columns of all G heads and the
           // pieces go by in batches of 8 whose loads are all in flight at once.
-          __threadfence();
+          fence_acq_rel_gpu();
           constexpr int F4 = G * D / 4;           // float4 of one piece's acc
           constexpr int FPL = (F4 + 31) / 32;     // ... per lane
           constexpr int JB = 16 / FPL < 8 ? (16 / FPL > 0 ? 16 / FPL : 1) : 8;  // pieces per batch of loads
