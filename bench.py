@@ -52,17 +52,20 @@ WORKLOAD = dict(name="llama3_8b_layer", d_model=4096, n_q_heads=32, n_kv_heads=8
 SCORE_DRAM_BYTES_PER_ROW = 272.084e6 / 32768
 
 # Kernels of this library launched per step at this workload's size (B*H <= 1024):
-# scorer (on the weight split once at set-up), mask, segment count + copy pass,
-# decode attention (the compaction and attention calls also issue one memset each).
-KERNELS_PER_STEP = 5
+# scorer (on the weight split once at set-up), segment count + copy pass of the
+# compaction with the mask fused in, decode attention; one more (the mask
+# kernel) with --mask separate. The compaction and attention calls also issue
+# one memset each.
+KERNELS_PER_STEP = {"fused": 4, "separate": 5}
 
 
-def config_desc(w=WORKLOAD):
+def config_desc(w=WORKLOAD, mask_mode=None):
     return {
         "workload": (f"{w['name']}: one layer, d_model {w['d_model']}, {w['n_q_heads']} q / {w['n_kv_heads']} kv "
                      f"heads, head_dim {w['head_dim']}, batch {w['batch']}, context {w['n_pos']}, KVzap-Linear "
                      f"scorer, threshold at each head's {int(w['prune_q'] * 100)}th-percentile score, last "
-                     f"{w['window']} tokens kept; step = score + mask + compact + decode attention"),
+                     f"{w['window']} tokens kept; step = score + mask + compact + decode attention"
+                     f"{ {'fused': ' (mask fused into the compaction)', 'separate': ' (mask as its own kernel)'}.get(mask_mode, '')}"),
         "global_batch": w["batch"],
         "seq_len": w["n_pos"],
         "parallelism": "replicas: each rank decodes its own batch",
@@ -272,35 +275,44 @@ def run_gpu(args, rank: int, world: int):
     # like the weight itself (set-up, untimed)
     Ws = kvp.kvp_score_split_weight(W)
 
-    # ---- threshold per (b, h): the 75th-percentile score (harness set-up, untimed)
+    # ---- threshold per (b, h): the 75th-percentile score, chosen on the device
+    # (harness set-up, untimed)
     kvp.kvp_score(x, W, out=scores, workspace=ws_s, status=status)
-    kth = int(math.floor(w["prune_q"] * (T - 1))) + 1
-    tau = torch.kthvalue(scores.view(B, T, H), kth, dim=1).values.contiguous()
+    tau = kvp.kvp_threshold(scores.view(B, T, H), w["prune_q"])
+    fused = args.mask == "fused"
 
     stream = torch.cuda.current_stream(dev)
-    N_EV = 5  # event slots per step: before score, mask, compact, attention, after
+    # event slots per step: before score, [mask,] compact, attention, after
+    names = ["score", "mask+compact", "decode_attn"] if fused else ["score", "mask", "compact", "decode_attn"]
+    N_EV = len(names) + 1
 
     def step(evs=None):
-        if evs is not None:
-            evs[0].record(stream)
+        e = iter(evs) if evs is not None else None
+        if e is not None:
+            next(e).record(stream)
         kvp.kvp_score(x, Ws, scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H, out=scores, status=status)
-        if evs is not None:
-            evs[1].record(stream)
-        kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=now, scores=scores, tau=tau,
-                     window=w["window"], expire=expire, keep_bits=bits, count=count)
-        if evs is not None:
-            evs[2].record(stream)
-        kvp.kvp_compact(K, V, expire, now, 0, cache, status=status, workspace=ws_c)
-        if evs is not None:
-            evs[3].record(stream)
+        if e is not None:
+            next(e).record(stream)
+        if fused:
+            kvp.kvp_compact_masked(K, V, now, 0, cache, mode=kvp.KVP_MASK_KVZAP, scores=scores, tau=tau,
+                                   window=w["window"], status=status, workspace=ws_c)
+        else:
+            kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=now, scores=scores, tau=tau,
+                         window=w["window"], expire=expire, keep_bits=bits, count=count)
+            if e is not None:
+                next(e).record(stream)
+            kvp.kvp_compact(K, V, expire, now, 0, cache, status=status, workspace=ws_c)
+        if e is not None:
+            next(e).record(stream)
         kvp.kvp_decode_attn(q, cache, now, out=out, workspace=ws_a, status=status)
-        if evs is not None:
-            evs[4].record(stream)
+        if e is not None:
+            next(e).record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert status.item() == 0, kvp.status_string(status.item())
+    count = cache.count
     kept = int(count.sum().item())
     surv_pages = int(((count + 15) // 16).sum().item())
 
@@ -346,7 +358,7 @@ def run_gpu(args, rank: int, world: int):
         step(evs[i])
     torch.cuda.synchronize()
     per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(N_EV - 1)] for i in range(n_break)])
-    k_ms = per.mean(axis=0)  # score, mask, compact, attention (per launch, ms)
+    k_ms = per.mean(axis=0)  # per phase of `names` (per launch, ms)
 
     # ---- algorithmic bytes (what the method must move)
     x_b = n_tok * D * 2
@@ -356,10 +368,11 @@ def run_gpu(args, rank: int, world: int):
     compact_b = 2 * B * H * T * 4 + 2 * kept * 2 * row_b + kept * 4 + B * H * max_pages * 16 * 4 \
         + B * H * max_pages * 4
     attn_b = surv_pages * 16 * (2 * row_b + 4) + B * Hq * d * 2 + B * Hq * d * 4
-    step_b = score_b + mask_b + compact_b + attn_b
+    # fused: the mask reads the scores and thresholds and writes nothing of its own
+    fused_b = n_tok * H * 4 + B * H * 4 + (compact_b - 2 * B * H * T * 4)
+    kb = [score_b, fused_b, attn_b] if fused else [score_b, mask_b, compact_b, attn_b]
+    step_b = sum(kb)
     hbm, _, peak_kind = measured_peaks()
-    names = ["score", "mask", "compact", "decode_attn"]
-    kb = [score_b, mask_b, compact_b, attn_b]
     kernels = {n: {"ms": float(k_ms[i]), "bytes": int(kb[i]), "GB_s": kb[i] / (k_ms[i] * 1e-3) / 1e9,
                    "frac_of_hbm": kb[i] / (k_ms[i] * 1e-3) / 1e9 / hbm} for i, n in enumerate(names)}
     dom = int(np.argmax(k_ms))
@@ -419,8 +432,8 @@ def run_gpu(args, rank: int, world: int):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch RNG, N(0,1) hidden states and K/V)",
-        "config": dict(config_desc(w), cuda_graph=graph is not None), "e2e": e2e,
-        "gpu_launches": KERNELS_PER_STEP * args.steps, "roofline": roofline,
+        "config": dict(config_desc(w, args.mask), cuda_graph=graph is not None), "e2e": e2e,
+        "gpu_launches": KERNELS_PER_STEP[args.mask] * args.steps, "roofline": roofline,
         "kernels": kernels, "effective_step_GB_s": step_b / (ms_step * 1e-3) / 1e9,
         "scored_tokens_per_s": n_tok / (k_ms[0] * 1e-3),
         "kept_fraction": kept / (B * H * T), "clocks": clocks, "cpu_baseline": cpu,
@@ -441,6 +454,9 @@ def main():
                     help="llama3_8b_layer = the bench line; the others print measurement lines "
                          "(see bench_workloads.py)")
     ap.add_argument("--eager", action="store_true", help="launch every step from the host (no CUDA graph)")
+    ap.add_argument("--mask", default="fused", choices=["fused", "separate"],
+                    help="fused: the mask is computed inside the compaction's passes (kvp_compact_masked); "
+                         "separate: kvp_mask writes expire, then kvp_compact reads it")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -60,11 +60,9 @@ def _randn_bf16(shape, gen, dev, std=1.0):
     return (torch.randn(shape, generator=gen, device=dev, dtype=torch.bfloat16) * std).contiguous()
 
 
-def _tau_quantile(scores_bth, q):
-    """Per-(b, h) lower order statistic at index floor(q (T-1))."""
-    T = scores_bth.shape[1]
-    k = int(math.floor(q * (T - 1))) + 1
-    return torch.kthvalue(scores_bth, k, dim=1).values.contiguous()
+def _tau_quantile(kvp, scores_bth, q):
+    """Per-(b, h) lower order statistic at index floor(q (T-1)), chosen on the device."""
+    return kvp.kvp_threshold(scores_bth.contiguous(), q)
 
 
 def mlp_prefill(kvp, dev, peaks, seed=0):
@@ -92,7 +90,7 @@ def mlp_prefill(kvp, dev, peaks, seed=0):
         score()
     ms_score = _time(score, reps=10)
     flops = 2.0 * B * T * D * HID + 2.0 * B * T * HID * H
-    tau = _tau_quantile(scores.view(B, T, H), 0.8)
+    tau = _tau_quantile(kvp, scores.view(B, T, H), 0.8)
     now = T - 1
     expire, _, count = kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=now,
                                     scores=scores, tau=tau)
@@ -323,7 +321,7 @@ def prune_sweep(kvp, dev, peaks, seed=0, calls=10, reps=5):
     ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
     points = []
     for prune_q in (0.0, 0.5, 0.75, 0.875, 0.9375, 0.96875):
-        tau = (torch.full((B, H), -math.inf, device=dev) if prune_q == 0.0 else _tau_quantile(s, prune_q))
+        tau = (torch.full((B, H), -math.inf, device=dev) if prune_q == 0.0 else _tau_quantile(kvp, s, prune_q))
         expire, _, _ = kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=T - 1,
                                     scores=s.view(B * T, H), tau=tau, window=W, want_bits=False)
         kvp.kvp_compact(K, V, expire, T - 1, 0, cache, status=st, workspace=ws_c)

@@ -159,6 +159,30 @@ KVP_API kvp_status kvp_mask(int mode, int batch, int n_kv_heads, int n_pos, int 
                     int window, int delay, int now,
                     int32_t* expire, uint32_t* keep_bits, int32_t* count, void* stream);
 
+/* kvp_threshold - each (b, h)'s KVzap threshold chosen on the device as an
+ * order statistic of its own scores. The KVzap summary ("실제 적용") removes
+ * low-scoring entries but leaves open how "low" is set; this entry point
+ * takes the plainest per-head reading, a quantile of the head's scores.
+ *
+ * tau[b, h] = the element of rank k = floor(q * (n_pos - 1)) (counted from 0,
+ * ascending) among scores[b, t, h], t in [0, n_pos); NaN ranks above +inf, so
+ * it is chosen only when fewer than n_pos - k scores are numbers. q = 0 gives
+ * the minimum, q = 1 the maximum, q = 0.5 at odd n_pos the median. Exact:
+ * the result is one of the inputs, bit for bit (-0.0 and +0.0 are one value).
+ *
+ * scores     device fp32 [B, n_pos, H] (kvp_score's output layout)
+ * q          in [0, 1], else KVP_ERR_INVALID
+ * tau        device fp32 [B, H] (output)
+ * workspace  device, kvp_threshold_workspace_bytes(batch, n_kv_heads) bytes
+ *            (1 KiB per (b, h) plus a little); zeroed by the call itself
+ * Limits: batch <= 65535 and n_pos * 32 below 2^31, else KVP_ERR_UNSUPPORTED.
+ * Radix select over the scores' order-preserving 32-bit keys: four passes of
+ * 8 bits, each one read of the scores (the later ones mostly from L2).
+ */
+KVP_API size_t kvp_threshold_workspace_bytes(int batch, int n_kv_heads);
+KVP_API kvp_status kvp_threshold(int batch, int n_kv_heads, int n_pos, const float* scores, double q,
+                                 float* tau, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* kvp_compact - gather the entries present at `now` into 16-row pages
  * (DeInfer summary, "나. 페이지드 KV 캐시 및 CUDA Graph 통합": remapping index
@@ -190,6 +214,36 @@ KVP_API kvp_status kvp_compact(int batch, int n_kv_heads, int head_dim, int n_po
                        const void* k_src, const void* v_src,
                        int64_t stride_b, int64_t stride_t, int64_t stride_h,
                        const int32_t* expire, int now, int reserve,
+                       void* k_pool, void* v_pool, int32_t* expire_pool, int n_pages_cap,
+                       int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                       void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* kvp_compact_masked - kvp_mask and kvp_compact in one pass, with no expire
+ * array in between (the mask is fused into the preparation and copy passes
+ * of the DeInfer summary's compaction, "나. 페이지드 KV 캐시 및 CUDA Graph
+ * 통합"; the keep rules are KVzap's "실제 적용" and the DMS article's "지연
+ * 삭제 (Delayed Eviction)").
+ *
+ * Every output is bit-identical to kvp_mask(mode, batch, n_kv_heads, n_pos,
+ * pos0 = 0, scores, tau, flag_step, window, delay, now, expire, ...) followed
+ * by kvp_compact(..., expire, now, reserve, ...) on the same K/V: entry t of
+ * the dense source is position t, its expire is derived from its score (or
+ * flag step) where it is needed, and expire_pool receives it for the kept
+ * entries. No dense expire, keep bits or per-position output is written.
+ *
+ * mode, scores, tau, flag_step, window, delay: as in kvp_mask (scores device
+ *   fp32 [B, n_pos, H] and tau [B, H] for KVP_MASK_KVZAP; flag_step device
+ *   int32 [B, H, n_pos] for KVP_MASK_DMS; the other mode's pointers NULL).
+ * Every other argument, output, workspace size
+ * (kvp_compact_workspace_bytes) and error is kvp_compact's.
+ * n_pos + window + delay must stay below KVP_EXPIRE_NEVER (else
+ * KVP_ERR_INVALID).
+ */
+KVP_API kvp_status kvp_compact_masked(int mode, int batch, int n_kv_heads, int head_dim, int n_pos,
+                       const void* k_src, const void* v_src,
+                       int64_t stride_b, int64_t stride_t, int64_t stride_h,
+                       const float* scores, const float* tau, const int32_t* flag_step,
+                       int window, int delay, int now, int reserve,
                        void* k_pool, void* v_pool, int32_t* expire_pool, int n_pages_cap,
                        int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream);

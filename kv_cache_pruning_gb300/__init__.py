@@ -69,9 +69,13 @@ _SIGS = {
     "kvp_score_split_weight": (_I, [_I, _I, _P, _P, _S, _P]),
     "kvp_score": (_I, [_I, _L, _I, _I, _I, _P, _L, _P, _P, _P, _P, _P, _P, _S, _P, _P]),
     "kvp_mask": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "kvp_threshold_workspace_bytes": (_S, [_I, _I]),
+    "kvp_threshold": (_I, [_I, _I, _I, _P, ctypes.c_double, _P, _P, _S, _P]),
     "kvp_compact_workspace_bytes": (_S, [_I, _I, _I]),
     "kvp_compact": (_I, [_I, _I, _I, _I, _P, _P, _L, _L, _L, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
                          _P, _S, _P, _P]),
+    "kvp_compact_masked": (_I, [_I, _I, _I, _I, _I, _P, _P, _L, _L, _L, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P,
+                                _I, _P, _I, _P, _P, _P, _S, _P, _P]),
     "kvp_compact_paged_workspace_bytes": (_S, [_I, _I, _I]),
     "kvp_compact_paged": (_I, [_I, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I,
                                _P, _P, _P, _S, _P, _P]),
@@ -256,6 +260,28 @@ class PagedKV:
         return self.k_pool.shape[2]
 
 
+def kvp_threshold_workspace_bytes(batch, n_kv_heads) -> int:
+    return _lib.kvp_threshold_workspace_bytes(batch, n_kv_heads)
+
+
+def kvp_threshold(scores, q, *, out=None, workspace=None, stream=None):
+    """Per-(b, h) threshold: the rank floor(q * (T - 1)) score of scores
+    [B, T, H] along T (NaN ranked last) -> tau fp32 [B, H]."""
+    if scores.dim() != 3:
+        raise ValueError("scores must be [B, T, H]")
+    B, T, H = scores.shape
+    dev = scores.device
+    tau = out if out is not None else torch.empty(B, H, dtype=torch.float32, device=dev)
+    if tau.numel() != B * H:
+        raise ValueError("out must hold B*H values")
+    ws = _ws(kvp_threshold_workspace_bytes(B, H), dev, workspace)
+    code = _lib.kvp_threshold(B, H, T, _ptr(scores, torch.float32, "scores"), float(q),
+                              _ptr(tau, torch.float32, "out"), ws.data_ptr(), ws.numel() * ws.element_size(),
+                              _stream(stream))
+    _check("kvp_threshold", code)
+    return tau
+
+
 def kvp_compact_workspace_bytes(batch, n_kv_heads, n_pos) -> int:
     return _lib.kvp_compact_workspace_bytes(batch, n_kv_heads, n_pos)
 
@@ -278,6 +304,38 @@ def kvp_compact(k, v, expire, now, reserve, dst: PagedKV, *, status, workspace=N
                             _ptr(dst.count, torch.int32), ws.data_ptr(), ws.numel() * ws.element_size(),
                             _ptr(status, torch.int32, "status"), _stream(stream))
     _check("kvp_compact", code)
+    return dst
+
+
+def kvp_compact_masked(k, v, now, reserve, dst: PagedKV, *, mode, scores=None, tau=None, flag_step=None,
+                       window=WINDOW, delay=0, status, workspace=None, stream=None):
+    """Dense K, V [B, T, H, d] with the mask applied on the fly: KVzap scores
+    [B*T, H] (or [B, T, H]) + tau [B, H], or DMS flag_step [B, H, T] -> dst.
+    Same result as kvp_mask (pos0 = 0) followed by kvp_compact."""
+    B, T, H, d = k.shape
+    if k.stride() != v.stride() or k.stride(3) != 1:
+        raise ValueError("k and v need identical strides with the head_dim axis contiguous")
+    for t, nm in ((k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{nm} must be a CUDA bf16 tensor")
+    if scores is not None and scores.numel() != B * T * H:
+        raise ValueError("scores must hold B*T*H values")
+    if flag_step is not None and flag_step.numel() != B * H * T:
+        raise ValueError("flag_step must hold B*H*T values")
+    if tau is not None and tau.numel() != B * H:
+        raise ValueError("tau must hold B*H values")
+    need = kvp_compact_workspace_bytes(B, H, T)
+    ws = _ws(need, k.device, workspace)
+    code = _lib.kvp_compact_masked(mode, B, H, d, T, k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1),
+                                   k.stride(2), _ptr(scores, torch.float32, "scores", True),
+                                   _ptr(tau, torch.float32, "tau", True),
+                                   _ptr(flag_step, torch.int32, "flag_step", True), window, delay, now, reserve,
+                                   _ptr(dst.k_pool, torch.bfloat16), _ptr(dst.v_pool, torch.bfloat16),
+                                   _ptr(dst.expire_pool, torch.int32), dst.n_pages_cap,
+                                   _ptr(dst.page_table, torch.int32), dst.max_pages, _ptr(dst.remap, torch.int32),
+                                   _ptr(dst.count, torch.int32), ws.data_ptr(), ws.numel() * ws.element_size(),
+                                   _ptr(status, torch.int32, "status"), _stream(stream))
+    _check("kvp_compact_masked", code)
     return dst
 
 

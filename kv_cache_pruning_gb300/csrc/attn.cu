@@ -122,10 +122,6 @@ KVP_DEV void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) 
 // pages skip the cross-lane max reduction altogether.
 constexpr float kLazyRescale = 8.0f;
 
-// Release/acquire fence at GPU scope: orders this thread's partial-state
-// stores before its arrival count, and the merger's loads after it sees the
-// final count (message passing needs no sequentially consistent fence).
-KVP_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 KVP_DEV int clamp_count(const int32_t* count, int bh, int max_pages) {
   return min(max(count[bh], 0), max_pages * kPage);

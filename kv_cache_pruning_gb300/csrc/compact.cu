@@ -1,4 +1,4 @@
-// kvp_mask, kvp_compact, kvp_compact_paged, kvp_append.
+// kvp_mask, kvp_compact, kvp_compact_masked, kvp_compact_paged, kvp_append.
 //
 // Rules (KVzap summary "실제 적용"; DMS article "지연 삭제 (Delayed Eviction)"):
 // an entry gets the first step at which it is gone,
@@ -124,6 +124,56 @@ struct DenseSrc {
     const int b = bh / H, h = bh - b * H;
     const int64_t off = b * sb + h * sh;
     return View{k + off, v + off, st, expire + static_cast<int64_t>(bh) * n, n};
+  }
+};
+
+// Masked dense source: the same rows as DenseSrc, but each entry's expire is
+// derived where it is needed from its score and the (b, h)'s threshold (KVzap)
+// or its flag step (DMS), with the mask kernel's rule and position t, so that
+// no [B, H, n] expire array is written or read.
+struct MaskedSrc {
+  const uint16_t* k;
+  const uint16_t* v;
+  int64_t sb, st, sh;
+  int mode;
+  const float* scores;     // KVzap: [B, n, H]
+  const float* tau;        // KVzap: [B, H]
+  const int32_t* flag;     // DMS: [B, H, n]
+  int window, delay;
+  int H;
+  int n;
+  struct View {
+    const uint16_t* kb;
+    const uint16_t* vb;
+    int64_t stride;
+    int mode;
+    const float* sc;       // this (b, h)'s scores, entry t at sc[t * H]
+    const int32_t* fl;     // this (b, h)'s flag steps, entry t at fl[t]
+    float th;
+    int H, window, delay, n;
+    KVP_DEV int length() const { return n; }
+    KVP_DEV int32_t expire_row(int t, int64_t& row) const {
+      row = t;
+      return mode == KVP_MASK_KVZAP ? expire_kvzap(sc[static_cast<int64_t>(t) * H], th, t, window)
+                                    : expire_dms(fl[t], t, delay, window);
+    }
+    KVP_DEV int position_of(int t) const { return t; }
+  };
+  KVP_DEV View view(int bh) const {
+    const int b = bh / H, h = bh - b * H;
+    const int64_t off = b * sb + h * sh;
+    const bool kvz = mode == KVP_MASK_KVZAP;
+    return View{k + off,
+                v + off,
+                st,
+                mode,
+                kvz ? scores + static_cast<int64_t>(b) * n * H + h : nullptr,
+                kvz ? nullptr : flag + static_cast<int64_t>(bh) * n,
+                kvz ? tau[bh] : 0.f,
+                H,
+                window,
+                delay,
+                n};
   }
 };
 
@@ -611,6 +661,48 @@ extern "C" kvp_status kvp_compact(int batch, int n_kv_heads, int head_dim, int n
   const int NS = n_segments(n_pos);
   DenseSrc src{static_cast<const uint16_t*>(k_src), static_cast<const uint16_t*>(v_src), stride_b, stride_t,
                stride_h, expire, n_kv_heads, n_pos};
+  return run_compact(src, batch * n_kv_heads, NS, head_dim, now, reserve, k_pool, v_pool, expire_pool, n_pages_cap,
+                     page_table, max_pages, remap, count, workspace, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvp_status kvp_compact_masked(int mode, int batch, int n_kv_heads, int head_dim, int n_pos,
+                                         const void* k_src, const void* v_src, int64_t stride_b, int64_t stride_t,
+                                         int64_t stride_h, const float* scores, const float* tau,
+                                         const int32_t* flag_step, int window, int delay, int now, int reserve,
+                                         void* k_pool, void* v_pool, int32_t* expire_pool, int n_pages_cap,
+                                         int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                                         void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+  if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0 || window < 0 || delay < 0) return KVP_ERR_INVALID;
+  if (mode == KVP_MASK_KVZAP) {
+    if (flag_step != nullptr || scores == nullptr || tau == nullptr) return KVP_ERR_INVALID;
+  } else if (mode == KVP_MASK_DMS) {
+    if (scores != nullptr || tau != nullptr || flag_step == nullptr) return KVP_ERR_INVALID;
+  } else {
+    return KVP_ERR_INVALID;
+  }
+  if (static_cast<int64_t>(n_pos) + window + delay >= kNever) return KVP_ERR_INVALID;
+  kvp_status s = check_dst(head_dim, reserve, k_pool, v_pool, expire_pool, n_pages_cap, page_table, max_pages,
+                           remap, count, status);
+  if (s != KVP_OK) return s;
+  if (n_pos > 0 && (k_src == nullptr || v_src == nullptr)) return KVP_ERR_INVALID;
+  if (!aligned16(k_src) || !aligned16(v_src) || stride_b % 8 || stride_t % 8 || stride_h % 8) return KVP_ERR_ALIGN;
+  if (stride_b < 0 || stride_t < 0 || stride_h < 0) return KVP_ERR_INVALID;
+  if (workspace == nullptr || workspace_bytes < kvp_compact_workspace_bytes(batch, n_kv_heads, n_pos))
+    return KVP_ERR_WORKSPACE;
+  const int NS = n_segments(n_pos);
+  MaskedSrc src{static_cast<const uint16_t*>(k_src),
+                static_cast<const uint16_t*>(v_src),
+                stride_b,
+                stride_t,
+                stride_h,
+                mode,
+                scores,
+                tau,
+                flag_step,
+                window,
+                delay,
+                n_kv_heads,
+                n_pos};
   return run_compact(src, batch * n_kv_heads, NS, head_dim, now, reserve, k_pool, v_pool, expire_pool, n_pages_cap,
                      page_table, max_pages, remap, count, workspace, status, static_cast<cudaStream_t>(stream));
 }

@@ -27,6 +27,12 @@ KVP_DEV void record_error(int32_t* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Release/acquire fence at GPU scope, for message passing between CTAs: a
+// writer orders its stores before its arrival on a counter, and the CTA that
+// sees the final count orders its loads after it (no sequentially consistent
+// fence is needed for that).
+KVP_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 KVP_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

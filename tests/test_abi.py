@@ -25,7 +25,7 @@ def lib():
 
 def test_header_declares_the_path():
     names = set(_declared())
-    for n in ["kvp_score", "kvp_mask", "kvp_compact", "kvp_compact_paged", "kvp_append", "kvp_decode_attn",
+    for n in ["kvp_score", "kvp_mask", "kvp_compact", "kvp_compact_masked", "kvp_compact_paged", "kvp_threshold", "kvp_append", "kvp_decode_attn",
               "kvp_score_workspace_bytes", "kvp_compact_workspace_bytes", "kvp_decode_attn_workspace_bytes",
               "kvp_status_string", "kvp_version"]:
         assert n in names, n
@@ -89,6 +89,50 @@ def test_host_validation_without_gpu(lib):
     # compaction: status word is required
     assert L.kvp_compact(1, 1, 128, 16, 16, 16, 0, 0, 0, 16, 15, 0, 16, 16, 16, 1, 16, 1, 16, 16, 16, 1 << 20,
                          None, None) == k.KVP_ERR_INVALID
+
+
+def test_compact_masked_host_checks():
+    """The fused mask + compaction entry point rejects bad arguments on the
+    host before any CUDA call."""
+    import kv_cache_pruning_gb300 as k
+    L = k.library()
+
+    def call(mode=0, hd=128, n_pos=16, kp=16, scores=16, tau=16, flag=None, window=128, delay=0, status=16):
+        return L.kvp_compact_masked(mode, 1, 1, hd, n_pos, kp, 16, 0, 0, 0, scores, tau, flag, window, delay, 15, 0,
+                                    16, 16, 16, 1, 16, 1, 16, 16, 16, 1 << 20, status, None)
+
+    assert call(flag=16) == k.KVP_ERR_INVALID                        # KVzap with a flag array too
+    assert call(tau=None) == k.KVP_ERR_INVALID                       # KVzap without a threshold
+    assert call(mode=1, flag=16) == k.KVP_ERR_INVALID                # DMS with scores too
+    assert call(mode=1, scores=None, tau=None) == k.KVP_ERR_INVALID  # DMS without flags
+    assert call(mode=7) == k.KVP_ERR_INVALID
+    assert call(window=-1) == k.KVP_ERR_INVALID
+    assert call(n_pos=2**31 - 200, window=128, delay=100) == k.KVP_ERR_INVALID  # expire would overflow
+    assert call(hd=96) == k.KVP_ERR_UNSUPPORTED
+    assert call(status=None) == k.KVP_ERR_INVALID
+    assert call(kp=8) == k.KVP_ERR_ALIGN
+
+
+def test_threshold_host_checks():
+    import kv_cache_pruning_gb300 as k
+    L = k.library()
+    # histogram 1 KiB per (b, h), prefix and rank, 4 pass counters per (b, head group of 32)
+    assert L.kvp_threshold_workspace_bytes(16, 8) == (128 * 256 + 2 * 128 + 4 * 16) * 4
+    assert L.kvp_threshold_workspace_bytes(1, 64) == (64 * 256 + 2 * 64 + 4 * 2) * 4
+    assert L.kvp_threshold_workspace_bytes(0, 8) == 0
+    ws = L.kvp_threshold_workspace_bytes(2, 3)
+
+    def call(B=2, H=3, n=100, scores=16, q=0.5, tau=16, wsp=16, wsb=ws):
+        return L.kvp_threshold(B, H, n, scores, q, tau, wsp, wsb, None)
+
+    for q in (-0.01, 1.01, float("nan")):
+        assert call(q=q) == k.KVP_ERR_INVALID
+    assert call(n=0) == k.KVP_ERR_INVALID
+    assert call(scores=None) == k.KVP_ERR_INVALID
+    assert call(tau=None) == k.KVP_ERR_INVALID
+    assert call(wsb=ws - 4) == k.KVP_ERR_WORKSPACE
+    assert call(wsp=None) == k.KVP_ERR_WORKSPACE
+    assert call(B=70000, wsb=1 << 40) == k.KVP_ERR_UNSUPPORTED
 
 
 def test_missing_library_fails_loudly(monkeypatch):

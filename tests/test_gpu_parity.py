@@ -135,6 +135,61 @@ def test_mask_dms_bit_exact(kvp, delay, now):
     np.testing.assert_array_equal(cnt.cpu().numpy(), cnt_r)
 
 
+# --------------------------------------------------------------------------- threshold
+
+def _check_tau(t_gpu, t_ref):
+    # bit-identical values (NaN == NaN; -0.0 and +0.0 are one value)
+    np.testing.assert_array_equal(t_gpu, t_ref)
+
+
+@pytest.mark.parametrize("B,T,H,q", [
+    (1, 512, 2, 0.5),
+    (16, 8192, 8, 0.75),       # a Llama-3-8B layer's scores
+    (3, 1000, 40, 0.3),        # two head groups, the second partial
+    (2, 1, 5, 0.9),            # one position
+    (4, 777, 3, 0.0),
+    (4, 777, 3, 1.0),
+    (1, 131072, 64, 0.6),      # the 65B-MHA layer: one b, 64 heads, long rows
+])
+def test_threshold_matches_oracle(kvp, B, T, H, q):
+    s = syn.normal_f32(4, 40, (B, T, H))
+    tau = kvp.kvp_threshold(dev_f32(s), q)
+    torch.cuda.synchronize()
+    _check_tau(tau.cpu().numpy(), orc.threshold_at_quantile(s, q))
+
+
+@pytest.mark.parametrize("H", [6, 8])   # one score per load; four heads per 16-byte load
+def test_threshold_ties_and_special_values(kvp, H):
+    B, T = 3, 2000
+    s = (np.round(syn.normal_f32(5, 41, (B, T, H)) * 2) / 2).astype(np.float32)   # heavy ties
+    s[0, :300, 0] = np.nan                  # NaN ranks last
+    s[0, 300:310, 0] = np.inf
+    s[1, :500, 1] = -np.inf
+    s[1, 500:900, 1] = -0.0
+    s[2, :, 2] = np.nan                     # all NaN
+    s[2, :, 3] = 1.5                        # all equal
+    s[2, ::2, 4] = -0.0                     # signed zeros mixed with +0.0 below
+    s[2, 1::2, 4] = 0.0
+    for q in [0.0, 0.05, 0.25, 0.5, 0.8, 0.86, 0.999, 1.0]:
+        tau = kvp.kvp_threshold(dev_f32(s), q)
+        torch.cuda.synchronize()
+        _check_tau(tau.cpu().numpy(), orc.threshold_at_quantile(s, q))
+
+
+def test_threshold_then_mask_prunes_the_quantile(kvp):
+    """Device threshold feeding the mask: per head, exactly T - k entries score
+    at or above it when the scores are distinct (k = floor(q (T - 1)))."""
+    B, T, H, q = 4, 4096, 8, 0.75
+    s = syn.normal_f32(6, 42, (B, T, H))
+    sd = dev_f32(s)
+    tau = kvp.kvp_threshold(sd, q)
+    exp, bits, cnt = kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=T - 1,
+                                  scores=sd.view(B * T, H), tau=tau, window=0)
+    torch.cuda.synchronize()
+    k = math.floor(q * (T - 1))
+    np.testing.assert_array_equal(cnt.cpu().numpy(), np.full((B, H), T - k))
+
+
 # --------------------------------------------------------------------------- compact
 
 def _compare_cache(gpu, ref: orc.PagedCache):
@@ -228,6 +283,81 @@ def test_compact_capacity_status(kvp):
     st.zero_()
     dst = kvp.PagedKV.allocate(B, H, d, 2000, 2)  # needs 2 * 1040 pages
     kvp.kvp_compact(dev_bf16(k), dev_bf16(v), exp, T - 1, 0, dst, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == kvp.KVP_ERR_CAPACITY
+
+
+# --------------------------------------------------------------------------- fused mask + compact
+
+@pytest.mark.parametrize("B,T,H,d,reserve,window,strided", [
+    (1, 512, 2, 64, 0, 128, False),
+    (2, 3000, 3, 128, 5, 128, True),    # ragged segments, [B, H, T, d] storage viewed as [B, T, H, d]
+    (4, 1030, 8, 128, 64, 7, False),
+    (2, 17, 2, 64, 16, 0, False),       # tiny ragged, no window
+    (131, 40, 8, 64, 3, 16, False),     # more than 1024 (b, h): page bases from the separate base pass
+])
+def test_compact_masked_kvzap_bit_exact(kvp, B, T, H, d, reserve, window, strided):
+    """Mask fused into the compaction == the oracle's mask followed by its
+    compaction, and == the two GPU calls in sequence."""
+    k, v = syn.kv_inputs(7, B, T, H, d)
+    s = syn.normal_f32(7, 21, (B, T, H))
+    s[0, min(5, T - 1), 0] = np.nan
+    tau = syn.normal_f32(7, 22, (B, H), std=0.7)
+    tau[0, 0] = -np.inf                 # keeps every entry of that head
+    tau[-1, -1] = np.inf                # keeps only the window of that head
+    now = T - 1
+    exp_r = orc.mask_kvzap(s, tau, now, window=window)[0]
+    max_pages = (T + reserve + 15) // 16
+    cap = B * H * max_pages
+    ref = orc.compact_dense(k, v, exp_r, now, reserve, cap, max_pages)
+    if strided:
+        kd = dev_bf16(np.ascontiguousarray(k.transpose(0, 2, 1, 3))).permute(0, 2, 1, 3)
+        vd = dev_bf16(np.ascontiguousarray(v.transpose(0, 2, 1, 3))).permute(0, 2, 1, 3)
+    else:
+        kd, vd = dev_bf16(k), dev_bf16(v)
+    sd, td = dev_f32(s), dev_f32(tau)
+    st = status_word()
+    dst = kvp.PagedKV.allocate(B, H, d, cap, max_pages)
+    kvp.kvp_compact_masked(kd, vd, now, reserve, dst, mode=kvp.KVP_MASK_KVZAP, scores=sd, tau=td, window=window,
+                           status=st)
+    two = kvp.PagedKV.allocate(B, H, d, cap, max_pages)
+    exp, _, _ = kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=now, scores=sd, tau=td,
+                             window=window)
+    kvp.kvp_compact(kd, vd, exp, now, reserve, two, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_cache(dst, ref)
+    for name in ("k_pool", "v_pool", "expire_pool", "page_table", "remap", "count"):
+        assert torch.equal(getattr(dst, name), getattr(two, name)), name
+
+
+@pytest.mark.parametrize("delay,window,now_back", [(256, 128, 0), (40, 32, 0), (0, 128, 300)])
+def test_compact_masked_dms_bit_exact(kvp, delay, window, now_back):
+    B, T, H, d = 3, 2100, 4, 128
+    k, v, f, _ = _dms_stream(B, T, H, d, delay, window, seed=12)
+    now = T - 1 - now_back              # entries past `now` are in the source too: expire decides
+    exp_r = orc.mask_dms(f, now, delay, window=window)[0]
+    max_pages = (T + 15) // 16
+    cap = B * H * max_pages
+    ref = orc.compact_dense(k, v, exp_r, now, 0, cap, max_pages)
+    st = status_word()
+    dst = kvp.PagedKV.allocate(B, H, d, cap, max_pages)
+    kvp.kvp_compact_masked(dev_bf16(k), dev_bf16(v), now, 0, dst, mode=kvp.KVP_MASK_DMS, flag_step=dev_i32(f),
+                           delay=delay, window=window, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_cache(dst, ref)
+
+
+def test_compact_masked_capacity_status(kvp):
+    B, T, H, d = 1, 256, 2, 64
+    k, v = syn.kv_inputs(6, B, T, H, d)
+    s = dev_f32(np.zeros((B, T, H), np.float32))
+    tau = dev_f32(np.full((B, H), -np.inf, np.float32))   # keeps all 512 entries: 32 pages
+    st = status_word()
+    dst = kvp.PagedKV.allocate(B, H, d, 20, 32)
+    kvp.kvp_compact_masked(dev_bf16(k), dev_bf16(v), T - 1, 0, dst, mode=kvp.KVP_MASK_KVZAP, scores=s, tau=tau,
+                           status=st)
     torch.cuda.synchronize()
     assert st.item() == kvp.KVP_ERR_CAPACITY
 

@@ -199,6 +199,40 @@ def test_threshold_quantile_prunes_expected_share():
         assert (above == T - math.floor(q * (T - 1))).all()
 
 
+def test_threshold_quantile_rank_by_brute_force():
+    """The threshold is the rank-k element, k = floor(q (T - 1)), with ties and
+    special values: brute force over a tiny column counts the scores strictly
+    below it (at most k) and at or below it (more than k); NaN ranks last."""
+    rng = np.random.default_rng(8)
+    B, T, H = 2, 23, 3
+    s = rng.integers(-3, 4, size=(B, T, H)).astype(np.float32) * 0.5   # many ties
+    s[0, :4, 0] = [np.inf, -np.inf, -0.0, 0.0]
+    s[1, :6, 1] = np.nan                                                 # 6 NaN of 23
+    for q in [0.0, 0.1, 0.5, 0.77, 0.9, 1.0]:
+        k = math.floor(q * (T - 1))
+        tau = orc.threshold_at_quantile(s, q)
+        for b in range(B):
+            for h in range(H):
+                col = [float(x) for x in s[b, :, h]]
+                num = [x for x in col if x == x]
+                t = float(tau[b, h])
+                if k >= len(num):
+                    assert t != t                    # rank among the NaN: the answer is NaN
+                    continue
+                assert t in num
+                assert sum(1 for x in num if x < t) <= k < sum(1 for x in num if x <= t)
+
+
+def test_threshold_quantile_special_cases():
+    """q = 0 and q = 1 give the column's minimum and maximum, q = 0.5 at odd T
+    the median (library routines), with no NaN present."""
+    rng = np.random.default_rng(9)
+    s = rng.standard_normal((3, 101, 4)).astype(np.float32)
+    np.testing.assert_array_equal(orc.threshold_at_quantile(s, 0.0), s.min(axis=1))
+    np.testing.assert_array_equal(orc.threshold_at_quantile(s, 1.0), s.max(axis=1))
+    np.testing.assert_array_equal(orc.threshold_at_quantile(s, 0.5), np.median(s, axis=1))
+
+
 def test_dms_bernoulli_keep_rate():
     # 8x compression: evict bit ~ Bernoulli(7/8) -> outside the delay band ~1/8 kept
     B, H, T = 4, 8, 4096
