@@ -351,8 +351,45 @@ def prune_sweep(kvp, dev, peaks, seed=0, calls=10, reps=5):
             "points": points}
 
 
+def threshold(kvp, dev, peaks, seed=0, calls=10, reps=5):
+    """Per-(b, h) threshold selection on the device (kvp_threshold, four radix
+    passes) at the score shapes of three layers: the tiny case, the Llama-3-8B
+    layer (batch 16, 8,192 tokens, 8 kv heads, 75th percentile) and one
+    Llama-65B MHA layer (1 x 131,072 tokens, 64 heads). Each result is checked
+    against torch.kthvalue; torch's time is printed beside ours for context."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    points = []
+    for name, B, T, H, q in (("tiny", 1, 512, 2, 0.5), ("llama3_8b_layer", 16, 8192, 8, 0.75),
+                             ("llama65b_mha_layer", 1, 131072, 64, 0.6)):
+        s = torch.randn((B, T, H), generator=g, device=dev)
+        tau = torch.empty(B, H, dtype=torch.float32, device=dev)
+        ws = torch.empty(kvp.kvp_threshold_workspace_bytes(B, H), dtype=torch.uint8, device=dev)
+        kvp.kvp_threshold(s, q, out=tau, workspace=ws)
+        kth = int(math.floor(q * (T - 1))) + 1
+        ref = torch.kthvalue(s, kth, dim=1).values
+        torch.cuda.synchronize()
+        assert torch.equal(tau, ref), name
+
+        def calls_fn():
+            for _ in range(calls):
+                kvp.kvp_threshold(s, q, out=tau, workspace=ws)
+
+        replay = _graph(calls_fn)
+        ms = _time(replay, reps=reps) / calls
+        ms_torch = _time(lambda: torch.kthvalue(s, kth, dim=1), reps=reps)
+        nbytes = B * T * H * 4
+        points.append({"shape": name, "batch": B, "n_pos": T, "n_kv_heads": H, "q": q, "threshold_us": ms * 1e3,
+                       "torch_kthvalue_us_eager": ms_torch * 1e3, "score_bytes": nbytes,
+                       "GB_s_one_read": nbytes / (ms * 1e-3) / 1e9,
+                       "frac_of_hbm_one_read": nbytes / (ms * 1e-3) / 1e9 / peaks[0]})
+    return {"workload": "threshold: per-(b, h) rank-floor(q(T-1)) score chosen on the device; "
+                        "each point = a CUDA graph of 10 calls (memset + 4 radix passes each)",
+            "points": points}
+
+
 RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha,
-           "prune_sweep": prune_sweep}
+           "prune_sweep": prune_sweep, "threshold": threshold}
 
 
 def run(name, kvp, dev, peaks):
