@@ -269,7 +269,7 @@ def run_gpu(args, rank: int, world: int):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ws_s = torch.empty(kvp.kvp_score_workspace_bytes(0, n_tok, D, H), dtype=torch.uint8, device=dev)
     ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
-    ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
 
     # ---- the layer's scorer weight in tensor-core form, made once per layer
     # like the weight itself (set-up, untimed)

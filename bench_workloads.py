@@ -110,7 +110,7 @@ def mlp_prefill(kvp, dev, peaks, seed=0):
     s_new = torch.empty(B, H, dtype=torch.float32, device=dev)
     ws_new = torch.empty(kvp.kvp_score_workspace_bytes(MLP, B, D, H, HID), dtype=torch.uint8, device=dev)
     out = torch.empty(steps, B, Hq, d, dtype=torch.float32, device=dev)
-    ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
 
     def restore():
         for dst, src in zip((cache.k_pool, cache.v_pool, cache.expire_pool, cache.page_table, cache.remap,
@@ -164,7 +164,7 @@ def dms_decode(kvp, dev, peaks, seed=0, steps=1024):
     cap = B * H * mp
     pools = [kvp.PagedKV.allocate(B, H, d, cap, mp, device=dev) for _ in range(2)]
     out = torch.empty(steps, B, Hq, d, dtype=torch.float32, device=dev)
-    ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
     ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T0), dtype=torch.uint8, device=dev)
     ws_p = torch.empty(kvp.kvp_compact_paged_workspace_bytes(B, H, mp), dtype=torch.uint8, device=dev)
     pages_read = torch.zeros((), dtype=torch.int64, device=dev)
@@ -257,7 +257,7 @@ def llama65b_mha(kvp, dev, peaks, seed=0, steps=32, n_layers=8):
     qs = _randn_bf16((steps, n_layers, B, H, d), g, dev)
     out = torch.empty(B, H, d, dtype=torch.float32, device=dev)
     s_new = torch.empty(B, H, dtype=torch.float32, device=dev)
-    ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, H, H, d), dtype=torch.uint8, device=dev)
+    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, H, H, d), dtype=torch.uint8, device=dev)
 
     def restore():
         for L in layers:
@@ -317,7 +317,7 @@ def prune_sweep(kvp, dev, peaks, seed=0, calls=10, reps=5):
     mp = (T + 15) // 16
     cache = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp, device=dev)
     out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
-    ws_a = torch.empty(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
     ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
     points = []
     for prune_q in (0.0, 0.5, 0.75, 0.875, 0.9375, 0.96875):

@@ -346,9 +346,12 @@ KVP_API kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_dim,
  * grid_limit 0 = the default grid (one CTA per SM); > 0 caps the number of
  *            CTAs (so the same inputs can be split differently)
  * workspace  device, >= kvp_decode_attn_workspace_bytes(...), 16-byte aligned;
- *            holds the partial states and per-(b, h) arrival counters (the
- *            call clears the counters itself). Calls that share a workspace
- *            must not overlap on the GPU.
+ *            holds the partial states and per-(b, h) arrival counters. It
+ *            must be zero-filled before its first use (cudaMemset of the whole
+ *            buffer); every call that records no error in `status` leaves it
+ *            ready for the next call (each merge resets its counter), so no
+ *            per-call clearing runs. After a call that recorded an error, zero
+ *            it again. Calls that share a workspace must not overlap on the GPU.
  */
 KVP_API size_t kvp_decode_attn_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim);
 KVP_API kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, int head_dim,

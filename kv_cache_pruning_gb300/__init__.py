@@ -383,13 +383,18 @@ def kvp_decode_attn_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim) -> i
 
 def kvp_decode_attn(q, cache: PagedKV, now, *, scale=0.0, out=None, grid_limit=0, workspace=None,
                     status=None, stream=None):
-    """out[B, Hq, d] fp32 = attention of q [B, Hq, d] (bf16) over the slots of `cache` present at `now`."""
+    """out[B, Hq, d] fp32 = attention of q [B, Hq, d] (bf16) over the slots of `cache` present at `now`.
+    A caller-provided workspace must be zero-filled before its first use (torch.zeros); calls that record
+    no error leave it that way."""
     B, Hq, d = q.shape
     H = cache.count.shape[1]
     if out is None:
         out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
     need = kvp_decode_attn_workspace_bytes(B, Hq, H, d)
-    ws = _ws(need, q.device, workspace)
+    if workspace is None:
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)  # zero-filled before first use
+    else:
+        ws = _ws(need, q.device, workspace)
     code = _lib.kvp_decode_attn(B, Hq, H, d, _ptr(q, torch.bfloat16, "q"), _ptr(cache.k_pool),
                                 _ptr(cache.v_pool), _ptr(cache.expire_pool, torch.int32), cache.n_pages_cap,
                                 _ptr(cache.page_table, torch.int32), cache.max_pages,

@@ -800,7 +800,8 @@ extern "C" kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, 
   int32_t* pieces = reinterpret_cast<int32_t*>(ws);
   float* part_ml = reinterpret_cast<float*>(ws + ws_counter_bytes(BH));
   float* part_acc = reinterpret_cast<float*>(ws + ws_counter_bytes(BH) + ws_ml_bytes(BH, G));
-  if (cudaMemsetAsync(pieces, 0, static_cast<size_t>(BH) * 4, st) != cudaSuccess) return KVP_ERR_CUDA;
+  // the counters are zero on entry: zero-filled by the caller before the
+  // workspace's first use, and reset by every merge of the previous call
   AttnParams p{static_cast<const uint16_t*>(q),
                static_cast<const uint16_t*>(k_pool),
                static_cast<const uint16_t*>(v_pool),

@@ -487,6 +487,30 @@ def test_decode_attn_split_independent(kvp):
         np.testing.assert_allclose(o, outs[0], rtol=0, atol=1e-5)
 
 
+def test_decode_attn_workspace_reused_across_calls(kvp):
+    """One zero-filled workspace serves consecutive calls on different caches
+    and grids: every result equals the one from a fresh zeroed workspace, and
+    the workspace's counters are zero again after each call."""
+    B, T, H, G, d = 3, 2100, 4, 4, 128
+    q = dev_bf16(syn.q_inputs(11, B, H * G, d))
+    st = status_word()
+    caches = []
+    for seed, tau_std in ((21, 0.7), (22, 0.2), (23, 1.5)):
+        k, v, exp, _ = _kvzap_case(B, T, H, d, seed=seed, tau_std=tau_std)
+        c = kvp.PagedKV.allocate(B, H, d, B * H * (T // 16 + 1), T // 16 + 1)
+        kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp), T - 1, 0, c, status=st)
+        caches.append(c)
+    ws = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, H * G, H, d), dtype=torch.uint8, device="cuda")
+    for c in caches:
+        for grid in (0, 3, 1):
+            o = kvp.kvp_decode_attn(q, c, T - 1, grid_limit=grid, workspace=ws, status=st)
+            fresh = kvp.kvp_decode_attn(q, c, T - 1, grid_limit=grid, status=st)
+            torch.cuda.synchronize()
+            assert st.item() == 0
+            assert torch.equal(o, fresh)
+            assert int(ws[: B * H * 4].view(torch.int32).abs().sum()) == 0   # counters back to zero
+
+
 def test_decode_attn_keep_all_is_dense_and_window(kvp):
     B, T, H, G, d = 1, 1100, 2, 4, 128
     k, v = syn.kv_inputs(8, B, T, H, d)
