@@ -147,6 +147,8 @@ template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnParams p) {
   using C = AttnCfg<D, G>;
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_launch_dependents();
+  pdl_wait();  // inputs (counts, pages, workspace counters) come from the kernels before this one
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BH = p.B * p.H;
   uint8_t* ring = smem + warp * kNst * C::STAGE_BYTES;
@@ -734,7 +736,8 @@ kvp_status launch_attn(const AttnParams& p, int grid_limit, cudaStream_t st) {
   int grid = attn_grid<D, G>();
   if (grid <= 0) return KVP_ERR_CUDA;
   if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
-  attn_decode_kernel<D, G><<<grid, kThreads, C::SMEM, st>>>(p);
+  if (launch_pdl(attn_decode_kernel<D, G>, dim3(grid), dim3(kThreads), C::SMEM, st, p) != cudaSuccess)
+    return KVP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 

@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) count_kernel(Src src, int n
                                                                    int32_t* __restrict__ seg_cnt,
                                                                    int32_t* __restrict__ count) {
   __shared__ int cta_kept[kWarpsPerCta];
+  pdl_launch_dependents();  // the copy pass may be scheduled now; it waits for this grid's end
   const int bh = blockIdx.y;
   const int warp = threadIdx.x >> 5;
   const int sg = blockIdx.x * kWarpsPerCta + warp;
@@ -373,6 +374,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
   constexpr int E16 = 2 * D * 2 / 16;   // 16-byte pieces per entry (K row then V row)
   constexpr int EPI = 32 / E16;         // entries per warp instruction (1 for D = 128, 2 for D = 64)
   extern __shared__ __align__(16) uint8_t sm_raw[];
+  pdl_launch_dependents();
+  pdl_wait();  // segment counts and (b, h) counts come from the passes before this one
   const int bh = blockIdx.x;  // pairs vary fastest: CTAs resident together read the same positions of all heads
   const int warp = threadIdx.x >> 5;
   const int sg = blockIdx.y * kWarpsPerCta + warp;
@@ -574,9 +577,11 @@ kvp_status run_compact(const Src& src, int BH, int NS, int head_dim, int now, in
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,            \
                                                      scatter_smem_bytes<DIM>()) == cudaSuccess;               \
     if (!attr_ok) return KVP_ERR_CUDA;                                                                        \
-    scatter_kernel<DIM, Src, FUSED><<<grid_t, kWarpsPerCta * 32, scatter_smem_bytes<DIM>(), st>>>(            \
-        src, now, NS, reserve, max_pages, n_pages_cap, BH, ws, count, status, kp, vp, expire_pool, page_table, \
-        remap);                                                                                               \
+    if (launch_pdl(scatter_kernel<DIM, Src, FUSED>, grid_t, dim3(kWarpsPerCta * 32), scatter_smem_bytes<DIM>(),  \
+                   st, src, now, NS, reserve, max_pages, n_pages_cap, BH, ws,                                 \
+                   static_cast<const int32_t*>(count), status, kp, vp, expire_pool, page_table,                \
+                   remap) != cudaSuccess)                                                                     \
+      return KVP_ERR_CUDA;                                                                                    \
   } while (0)
   if (head_dim == 128) {
     if (fused) KVP_SCATTER(128, true); else KVP_SCATTER(128, false);

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <utility>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -32,6 +33,33 @@ KVP_DEV void record_error(int32_t* status, int code) {
 // sees the final count orders its loads after it (no sequentially consistent
 // fence is needed for that).
 KVP_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream is still
+// running; it calls pdl_wait() before its first global memory access, which
+// returns once that kernel has completed and its writes are visible (a no-op
+// for a kernel launched without the attribute). pdl_launch_dependents() lets
+// the next such kernel be scheduled without waiting for this one to exit.
+KVP_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+KVP_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launches kern<<<grid, block, smem, st>>>(args...) with programmatic stream
+// serialization allowed (the kernel must call pdl_wait() first).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 KVP_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
