@@ -14,6 +14,8 @@ method is taken step by step from these pages:
           of a MarkTechPost article).
 [DeInfer] gist.science summary of arXiv 2604.17709 (DeInfer), section
           "2. 제안 방법 → 나. 페이지드 KV 캐시 및 CUDA Graph 통합".
+[BeaconKV] "LLM 추론 비용 혁신: '비콘KV'가 KV 캐시 메모리 4배 절감하며 성능까지
+          잡는 비결" (jiinsi.com paper briefing).
 
 Steps and where they come from:
 
@@ -29,6 +31,8 @@ Steps and where they come from:
            compact buffer with fixed addresses (16-token pages here).
 4. attend  [DMS, "DMS 작동 방식" step 5 and "메모리의 미래"]: standard
            attention over what is kept (single-query decode, GQA).
+5. quantize [BeaconKV]: instead of dropping the less important entries,
+           keep them in low precision (an fp8 tier, see section 5).
 
 Readings where the pages are silent (each is listed with its reason in the
 repository's design notes): scores are raw surrogate outputs compared to a
@@ -324,6 +328,168 @@ def window_attention(q_bits, k_bits, v_bits, now: int, window: int = WINDOW, sca
     """Sliding-window attention over the last `window` positions ending at now
     ([DMS, "문제 완화를 위한 이전 시도" table, first row])."""
     return dense_attention(q_bits, k_bits, v_bits, now, scale, lo=now - window + 1)
+
+
+# ---------------------------------------------------------------------------
+# 5. Quantize instead of drop  [BeaconKV: the important entries keep full
+#    precision, the others are compressed lossily by low-precision
+#    quantization or pruning ("비콘KV" article, core-idea paragraph and its
+#    first FAQ answer)]
+#
+# Reading (the article names no format): a second, fp8 tier. An entry whose
+# score s has tau_q <= s < tau (NaN never) is stored once more, its K and V
+# rows each as FP8 E4M3 codes with one float32 scale per row; it is visible
+# in that tier from step pos + window on, i.e. from the step its full
+# precision copy leaves the window. Entries with s >= tau stay bf16 for good
+# (section 2); entries below tau_q are dropped after the window as before.
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_positive_values() -> np.ndarray:
+    """Value of codes 0..127 of FP8 E4M3 (sign bit clear): exponent bias 7,
+    three mantissa bits, subnormals at exponent field 0, no infinities, code
+    127 (all ones) is NaN. Codes 128..255 are the negatives."""
+    vals = np.empty(128)
+    for code in range(128):
+        e, m = code >> 3, code & 7
+        if e == 15 and m == 7:
+            vals[code] = np.nan
+        elif e == 0:
+            vals[code] = (m / 8.0) * 2.0 ** -6
+        else:
+            vals[code] = (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    codes = np.asarray(codes, dtype=np.int64)
+    v = e4m3_positive_values()[codes & 0x7F]
+    return np.where(codes & 0x80, -v, v)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Round to the nearest E4M3 value, ties to the even code (the one whose
+    mantissa's last bit is 0); magnitudes above 448 saturate to 448; NaN gives
+    code 0x7F. The sign is kept, also for a result of zero (-0 -> 0x80)."""
+    v = np.asarray(v, dtype=np.float64)
+    grid = e4m3_positive_values()[:127]          # finite magnitudes, ascending
+    a = np.abs(v)
+    hi = np.clip(np.searchsorted(grid, a), 0, 126)
+    lo = np.clip(hi - 1, 0, 126)
+    dlo, dhi = a - grid[lo], grid[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(a >= E4M3_MAX, 126, np.where(a <= grid[lo], lo, np.where(pick_hi, hi, lo)))
+    code = np.where(np.isnan(v), 0x7F, code)
+    return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
+def quantize_rows(bits: np.ndarray):
+    """bf16 rows [..., d] -> (codes uint8 [..., d], scale float32 [...]).
+    scale = amax(|row|) / 448 in float32 (round to nearest); each element is
+    divided by the scale in float32 and rounded to E4M3. An all-zero row has
+    scale 0 and codes 0."""
+    x = widen_bf16(bits).astype(np.float32)
+    amax = np.abs(x).max(axis=-1)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    y = (x / safe[..., None]).astype(np.float32)
+    codes = np.where((scale > 0)[..., None], e4m3_encode(y), 0).astype(np.uint8)
+    return codes, scale
+
+
+def dequantize_rows(codes, scale) -> np.ndarray:
+    return e4m3_decode(codes) * np.asarray(scale, dtype=np.float64)[..., None]
+
+
+def quant_tier_select(scores_bth, tau_bh, tau_q_bh):
+    """Entries that go to the fp8 tier: tau_q <= s < tau. [B, H, T] bool."""
+    s = np.asarray(scores_bth).transpose(0, 2, 1)
+    t = np.asarray(tau_bh)[:, :, None]
+    tq = np.asarray(tau_q_bh)[:, :, None]
+    return (s >= tq) & (s < t)
+
+
+class QuantPagedCache:
+    """The fp8 tier: code pools [n_pages, 16, d] uint8 for K and V, per-slot
+    scales [n_pages, 16] float32, per-slot start step [n_pages, 16], page
+    table [B, H, max_pages] (-1 = unused), remap [B, H, max_pages*16], count."""
+
+    def __init__(self, batch, n_kv_heads, head_dim, n_pages_cap, max_pages):
+        self.kq_pool = np.zeros((n_pages_cap, PAGE, head_dim), dtype=np.uint8)
+        self.vq_pool = np.zeros((n_pages_cap, PAGE, head_dim), dtype=np.uint8)
+        self.kscale = np.zeros((n_pages_cap, PAGE), dtype=np.float32)
+        self.vscale = np.zeros((n_pages_cap, PAGE), dtype=np.float32)
+        self.start_pool = np.zeros((n_pages_cap, PAGE), dtype=np.int64)
+        self.page_table = np.full((batch, n_kv_heads, max_pages), -1, dtype=np.int64)
+        self.remap = np.full((batch, n_kv_heads, max_pages * PAGE), -1, dtype=np.int64)
+        self.count = np.zeros((batch, n_kv_heads), dtype=np.int64)
+        self.pages_used = 0
+
+    def slot_rows(self, b, h, slots):
+        slots = np.asarray(slots, dtype=np.int64)
+        return self.page_table[b, h, slots // PAGE], slots % PAGE
+
+
+def compact_quant_dense(k_bits, v_bits, scores_bth, tau_bh, tau_q_bh, reserve, n_pages_cap, max_pages,
+                        window: int = WINDOW) -> QuantPagedCache:
+    """Dense K/V [B, T, H, d] -> the fp8 tier of the entries with
+    tau_q <= s < tau, in ascending position, pages handed out in (b-major,
+    h-minor) order exactly as in section 3; start = position + window."""
+    B, T, H, d = k_bits.shape
+    out = QuantPagedCache(B, H, d, n_pages_cap, max_pages)
+    sel = quant_tier_select(scores_bth, tau_bh, tau_q_bh)
+    for b in range(B):
+        for h in range(H):
+            pos = np.nonzero(sel[b, h])[0]
+            n = len(pos)
+            npg = _pages_for(n, reserve)
+            if npg > max_pages or out.pages_used + npg > n_pages_cap:
+                raise CapacityError(f"(b={b}, h={h}) needs {npg} fp8 pages")
+            base = out.pages_used
+            out.page_table[b, h, :npg] = base + np.arange(npg)
+            j = np.arange(n)
+            kc, ks = quantize_rows(k_bits[b, pos, h])
+            vc, vs = quantize_rows(v_bits[b, pos, h])
+            out.kq_pool[base + j // PAGE, j % PAGE] = kc
+            out.vq_pool[base + j // PAGE, j % PAGE] = vc
+            out.kscale[base + j // PAGE, j % PAGE] = ks
+            out.vscale[base + j // PAGE, j % PAGE] = vs
+            out.start_pool[base + j // PAGE, j % PAGE] = pos + window
+            out.remap[b, h, :n] = pos
+            out.count[b, h] = n
+            out.pages_used += npg
+    return out
+
+
+def decode_attention_two_tier(q_bits, cache: PagedCache, qcache: QuantPagedCache, now: int,
+                              scale: float | None = None) -> np.ndarray:
+    """Attention over the union of the bf16 tier's slots present at `now`
+    (now < expire) and the fp8 tier's slots visible at `now` (now >= start),
+    the latter dequantized exactly (code value x row scale, float64)."""
+    B, Hq, d = q_bits.shape
+    H = cache.count.shape[1]
+    g = Hq // H
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    q = widen_bf16(q_bits)
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        for h in range(H):
+            pg, row = cache.slot_rows(b, h, np.arange(cache.count[b, h]))
+            sel = present(cache.expire_pool[pg, row], now)
+            Ka = widen_bf16(cache.k_pool[pg[sel], row[sel]])
+            Va = widen_bf16(cache.v_pool[pg[sel], row[sel]])
+            pq, rq = qcache.slot_rows(b, h, np.arange(qcache.count[b, h]))
+            vis = now >= qcache.start_pool[pq, rq]
+            pq, rq = pq[vis], rq[vis]
+            Kb = dequantize_rows(qcache.kq_pool[pq, rq], qcache.kscale[pq, rq])
+            Vb = dequantize_rows(qcache.vq_pool[pq, rq], qcache.vscale[pq, rq])
+            K = np.concatenate([Ka, Kb.reshape(-1, d)])
+            V = np.concatenate([Va, Vb.reshape(-1, d)])
+            for j in range(h * g, (h + 1) * g):
+                out[b, j] = _softmax_attend(q[b, j], K, V, scale)
+    return out.astype(np.float32)
 
 
 # ---------------------------------------------------------------------------

@@ -449,3 +449,123 @@ def test_scorer_overhead_matches_page():
     mlp = 100.0 * orc.scorer_macs(m["d_model"], m["n_kv_heads"], g["mlp_hidden_reading"]) / proj
     assert round(lin, g["linear_printed_digits"]) == g["linear_percent"]
     assert round(mlp, g["mlp_printed_digits"]) == g["mlp_percent"]
+
+
+# --------------------------------------------------------------------------- fp8 tier
+
+def test_e4m3_table_matches_closed_form_and_torch():
+    """All 256 codes: the closed form (1 + m/8) 2^(e-7), subnormals (m/8) 2^-6,
+    NaN at 0x7F / 0xFF, against torch's float8_e4m3fn decoding (a library
+    routine) and a few textbook values."""
+    codes = np.arange(256, dtype=np.uint8)
+    mine = orc.e4m3_decode(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(mine, lib)   # NaN == NaN here
+    assert orc.e4m3_decode([0x38])[0] == 1.0 and orc.e4m3_decode([0x7E])[0] == 448.0
+    assert orc.e4m3_decode([0x01])[0] == 2.0 ** -9 and orc.e4m3_decode([0x08])[0] == 2.0 ** -6
+    assert orc.e4m3_decode([0xB8])[0] == -1.0
+
+
+def test_e4m3_encode_matches_torch_cast():
+    """Round to nearest, ties to even, against torch's float8 cast on values
+    up to 464 (above it torch gives NaN, the encoder saturates to 448)."""
+    rng = np.random.default_rng(3)
+    grid = orc.e4m3_positive_values()[:127]
+    mids = (grid[:-1] + grid[1:]) / 2                                   # exact ties
+    v = np.concatenate([rng.uniform(-464, 464, 4000), rng.standard_normal(4000) * 0.01,
+                        mids, -mids, grid, -grid, [464.0, -464.0, 2.0 ** -10, -2.0 ** -11]]).astype(np.float32)
+    mine = orc.e4m3_encode(v)
+    lib = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(mine, lib)
+    np.testing.assert_array_equal(orc.e4m3_encode([500.0, -1e6, np.nan]), [0x7E, 0xFE, 0x7F])
+
+
+def test_quantize_rows_bounds_and_exact_cases():
+    """Per-row scale = amax / 448: the largest element encodes to +-448 exactly;
+    every element of the normal range is within half an E4M3 step (2^-4
+    relative), the subnormal range within 2^-10 scale; zero rows stay zero;
+    rows on the E4M3 grid times a power of two come back exactly."""
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((64, 128)).astype(np.float32)
+    bits = syn.f32_to_bf16_bits(x)
+    codes, scale = orc.quantize_rows(bits)
+    xb = orc.widen_bf16(bits)
+    back = orc.dequantize_rows(codes, scale)
+    amax_idx = np.abs(xb).argmax(axis=1)
+    assert np.all((codes[np.arange(64), amax_idx] & 0x7F) == 0x7E)
+    y = np.abs(xb) / scale[:, None]
+    normal = y >= 2.0 ** -6
+    err = np.abs(back - xb)
+    assert np.all(err[normal] <= 2.0 ** -4 * np.abs(xb[normal]) * (1 + 1e-6))
+    assert np.all(err[~normal] <= 2.0 ** -10 * np.broadcast_to(scale[:, None], err.shape)[~normal] * (1 + 1e-6))
+    zc, zs = orc.quantize_rows(np.zeros((2, 64), np.uint16))
+    assert (zc == 0).all() and (zs == 0).all()
+    grid = orc.e4m3_positive_values()[:127]
+    ex = rng.choice(np.concatenate([grid, -grid]), size=(8, 64)) * 2.0 ** 3
+    ex[:, 0] = 448.0 * 2.0 ** 3
+    eb = syn.f32_to_bf16_bits(ex.astype(np.float32))
+    c2, s2 = orc.quantize_rows(eb)
+    np.testing.assert_array_equal(s2, np.full(8, 8.0, np.float32))
+    np.testing.assert_array_equal(orc.dequantize_rows(c2, s2), ex)
+
+
+def test_quant_tier_partitions_the_entries():
+    """With tau_q <= tau every entry is in exactly one class: kept bf16
+    (s >= tau), fp8 tier (tau_q <= s < tau), dropped (s < tau_q or NaN)."""
+    rng = np.random.default_rng(6)
+    B, T, H = 2, 300, 3
+    s = rng.standard_normal((B, T, H))
+    s[0, :5, 0] = np.nan
+    tau = np.full((B, H), 0.5)
+    tq = np.full((B, H), -0.5)
+    fp8 = orc.quant_tier_select(s, tau, tq)
+    st = s.transpose(0, 2, 1)
+    keep = st >= 0.5
+    drop = ~(st >= -0.5)
+    assert ((keep.astype(int) + fp8.astype(int) + drop.astype(int)) == 1).all()
+    assert not fp8[0, 0, :5].any()
+    assert not orc.quant_tier_select(s, tau, tau).any()     # tau_q = tau: no fp8 tier
+
+
+def test_two_tier_attention_reduces_to_known_cases():
+    """(1) An empty fp8 tier gives the one-tier attention. (2) tau = +inf and
+    tau_q = -inf put every entry in the window (bf16) or, once out of it, in
+    the fp8 tier; with rows exactly representable in E4M3 (one element at
+    448 x 2^k, the rest on the grid x 2^k) that is dense attention over every
+    position, brute force. (3) A step before the window has passed shows no
+    fp8 slot at all: the last-128 window attention."""
+    rng = np.random.default_rng(7)
+    B, T, H, G, d = 1, 300, 2, 2, 64
+    grid = orc.e4m3_positive_values()[:127]
+    grid = grid[(grid >= 2.0 ** -3) & (grid <= 4.0)]
+    def rows():
+        r = rng.choice(np.concatenate([grid, -grid]), size=(B, T, H, d)) * 0.25
+        r[..., 0] = 448.0 * 0.25 * np.where(rng.random((B, T, H)) < 0.5, 1, -1)
+        return syn.f32_to_bf16_bits(r.astype(np.float32))
+    k, v = rows(), rows()
+    q = syn.f32_to_bf16_bits((rng.standard_normal((B, H * G, d)) * 0.05).astype(np.float32))
+    s = rng.standard_normal((B, T, H))
+    mp = T // 16 + 2
+    now = T - 1
+    # (1)
+    tau = np.zeros((B, H))
+    exp = orc.mask_kvzap(s, tau, now)[0]
+    ca = orc.compact_dense(k, v, exp, now, 0, B * H * mp, mp)
+    cq = orc.compact_quant_dense(k, v, s, tau, tau, 0, B * H * mp, mp)
+    assert cq.count.sum() == 0
+    np.testing.assert_array_equal(orc.decode_attention_two_tier(q, ca, cq, now), orc.decode_attention(q, ca, now))
+    # (2)
+    inf = np.full((B, H), np.inf)
+    exp = orc.mask_kvzap(s, inf, now)[0]
+    ca = orc.compact_dense(k, v, exp, now, 0, B * H * mp, mp)
+    cq = orc.compact_quant_dense(k, v, s, inf, -inf, 0, B * H * mp, mp)
+    assert (cq.count == T).all()
+    two = orc.decode_attention_two_tier(q, ca, cq, now)
+    np.testing.assert_allclose(two, orc.dense_attention(q, k, v, now), rtol=0, atol=1e-6)
+    # (3) at a step before any fp8 entry is visible (now < 0 + window)
+    early = 100
+    exp_e = orc.mask_kvzap(s[:, :early + 1], inf[:, :], early)[0]
+    ca_e = orc.compact_dense(k[:, :early + 1], v[:, :early + 1], exp_e, early, 0, B * H * mp, mp)
+    cq_e = orc.compact_quant_dense(k[:, :early + 1], v[:, :early + 1], s[:, :early + 1], inf, -inf, 0, B * H * mp, mp)
+    np.testing.assert_allclose(orc.decode_attention_two_tier(q, ca_e, cq_e, early),
+                               orc.window_attention(q, k, v, early), rtol=0, atol=1e-6)
