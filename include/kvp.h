@@ -248,6 +248,45 @@ KVP_API kvp_status kvp_compact_masked(int mode, int batch, int n_kv_heads, int h
                        int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
+/* kvp_compact_quant - the fp8 tier of "quantize instead of drop" (BeaconKV
+ * article "LLM 추론 비용 혁신: '비콘KV'가 ...", core idea and first FAQ answer:
+ * important entries keep full precision, the others are compressed lossily,
+ * for instance by low-precision quantization). The article fixes no format;
+ * this library's reading is:
+ *
+ *   - entry t of the dense source goes to the fp8 tier iff
+ *     tau_q[b,h] <= scores[b,t,h] < tau[b,h] (a NaN score never does); with
+ *     tau_q <= tau this is the band that the bf16 tier (kvp_mask with tau)
+ *     keeps only while it is in the window;
+ *   - its K row and its V row are each stored as FP8 E4M3 codes with one fp32
+ *     scale per row: scale = amax(|row|) / 448 (IEEE division), code =
+ *     E4M3(x / scale) rounded to nearest even with saturation to +-448; an
+ *     all-zero row has scale 0 and zero codes; value = code * scale;
+ *   - it is visible to kvp_decode_attn_two_tier from step t + window on, the
+ *     step its bf16 copy leaves the window, so at any step an entry is in one
+ *     tier at most.
+ *
+ * Selected entries are laid out like kvp_compact's survivors: ascending
+ * position, (b, h) in b-major / h-minor order, ceil((count + reserve) / 16)
+ * consecutive pages each.
+ * Source, strides, reserve, workspace (kvp_compact_workspace_bytes) and
+ * errors: as kvp_compact. scores device fp32 [B, n_pos, H]; tau, tau_q device
+ * fp32 [B, H].
+ * Outputs (all device):
+ *   kq_pool, vq_pool  uint8 [n_pages_cap, 16, head_dim] E4M3 codes, 16-byte
+ *                     aligned; rows past count in a (b, h)'s last page zero
+ *   meta_pool         int32 [n_pages_cap, 3, 16]: per slot the start step, the
+ *                     K scale and the V scale (fp32 bit patterns); 0 in unused rows
+ *   page_table, remap, count: as kvp_compact (remap = source position)
+ */
+KVP_API kvp_status kvp_compact_quant(int batch, int n_kv_heads, int head_dim, int n_pos,
+                       const void* k_src, const void* v_src,
+                       int64_t stride_b, int64_t stride_t, int64_t stride_h,
+                       const float* scores, const float* tau, const float* tau_q, int window, int reserve,
+                       void* kq_pool, void* vq_pool, int32_t* meta_pool, int n_pages_cap,
+                       int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                       void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
 /* kvp_compact_noalloc - kvp_compact for callers that cannot allocate device
  * memory. No page describes this entry point; it is a convenience of this
  * library. Some hosts hand a library only the tensors of the operation and no
@@ -359,6 +398,33 @@ KVP_API kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, int
                                    const int32_t* expire_pool, int n_pages_cap,
                                    const int32_t* page_table, int max_pages,
                                    const int32_t* count, int now, float scale, float* out,
+                                   int grid_limit, void* workspace, size_t workspace_bytes,
+                                   int32_t* status, void* stream);
+
+/* kvp_decode_attn_two_tier - kvp_decode_attn over both tiers of "quantize
+ * instead of drop" (BeaconKV article; the fp8 tier as kvp_compact_quant
+ * writes it):
+ *
+ *   out[b, j] = sum_i softmax_i(scale * q[b, j] . k_i) v_i
+ *
+ * over the bf16 slots i < count[b, h] with expire > now, and the fp8 slots
+ * i < count_q[b, h] with start <= now, whose k and v are their E4M3 codes
+ * times the row's scale. Both tiers' pages of a (b, h) form one list, split
+ * over the persistent grid like kvp_decode_attn's.
+ *
+ * Arguments up to `count` and from `now` on: as kvp_decode_attn (same
+ * workspace size and rules). kq_pool, vq_pool, meta_pool (16-byte aligned),
+ * n_pages_cap_q, page_table_q (width max_pages_q), count_q: the fp8 tier as
+ * kvp_compact_quant writes it. A fp8 page id outside [0, n_pages_cap_q)
+ * records KVP_ERR_BOUNDS and the page counts as empty.
+ */
+KVP_API kvp_status kvp_decode_attn_two_tier(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                   const void* q, const void* k_pool, const void* v_pool,
+                                   const int32_t* expire_pool, int n_pages_cap,
+                                   const int32_t* page_table, int max_pages, const int32_t* count,
+                                   const void* kq_pool, const void* vq_pool, const int32_t* meta_pool,
+                                   int n_pages_cap_q, const int32_t* page_table_q, int max_pages_q,
+                                   const int32_t* count_q, int now, float scale, float* out,
                                    int grid_limit, void* workspace, size_t workspace_bytes,
                                    int32_t* status, void* stream);
 

@@ -76,6 +76,8 @@ _SIGS = {
                          _P, _S, _P, _P]),
     "kvp_compact_masked": (_I, [_I, _I, _I, _I, _I, _P, _P, _L, _L, _L, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P,
                                 _I, _P, _I, _P, _P, _P, _S, _P, _P]),
+    "kvp_compact_quant": (_I, [_I, _I, _I, _I, _P, _P, _L, _L, _L, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I,
+                               _P, _P, _P, _S, _P, _P]),
     "kvp_compact_paged_workspace_bytes": (_S, [_I, _I, _I]),
     "kvp_compact_paged": (_I, [_I, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I,
                                _P, _P, _P, _S, _P, _P]),
@@ -83,6 +85,8 @@ _SIGS = {
                         _P, _P]),
     "kvp_decode_attn_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "kvp_decode_attn": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _I, _P, _S, _P, _P]),
+    "kvp_decode_attn_two_tier": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _P, _I, _P,
+                                      _I, _F, _P, _I, _P, _S, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -260,6 +264,52 @@ class PagedKV:
         return self.k_pool.shape[2]
 
 
+@dataclass
+class QuantPagedKV:
+    """Device buffers of the fp8 tier (quantize instead of drop)."""
+    kq_pool: torch.Tensor       # uint8 [n_pages_cap, 16, d] E4M3 codes of K rows
+    vq_pool: torch.Tensor       # uint8 [n_pages_cap, 16, d] E4M3 codes of V rows
+    meta_pool: torch.Tensor     # int32 [n_pages_cap, 3, 16]: start step, K scale, V scale (fp32 bits)
+    page_table: torch.Tensor    # int32 [B, H, max_pages]
+    remap: torch.Tensor         # int32 [B, H, max_pages * 16]
+    count: torch.Tensor         # int32 [B, H]
+
+    @staticmethod
+    def allocate(batch, n_kv_heads, head_dim, n_pages_cap, max_pages, device="cuda"):
+        return QuantPagedKV(
+            torch.zeros((n_pages_cap, PAGE, head_dim), dtype=torch.uint8, device=device),
+            torch.zeros((n_pages_cap, PAGE, head_dim), dtype=torch.uint8, device=device),
+            torch.zeros((n_pages_cap, 3, PAGE), dtype=torch.int32, device=device),
+            torch.full((batch, n_kv_heads, max_pages), -1, dtype=torch.int32, device=device),
+            torch.full((batch, n_kv_heads, max_pages * PAGE), -1, dtype=torch.int32, device=device),
+            torch.zeros((batch, n_kv_heads), dtype=torch.int32, device=device),
+        )
+
+    @property
+    def n_pages_cap(self):
+        return self.kq_pool.shape[0]
+
+    @property
+    def max_pages(self):
+        return self.page_table.shape[2]
+
+    @property
+    def head_dim(self):
+        return self.kq_pool.shape[2]
+
+    @property
+    def start_pool(self):
+        return self.meta_pool[:, 0, :]
+
+    @property
+    def kscale(self):
+        return self.meta_pool[:, 1, :].view(torch.float32)
+
+    @property
+    def vscale(self):
+        return self.meta_pool[:, 2, :].view(torch.float32)
+
+
 def kvp_threshold_workspace_bytes(batch, n_kv_heads) -> int:
     return _lib.kvp_threshold_workspace_bytes(batch, n_kv_heads)
 
@@ -339,6 +389,32 @@ def kvp_compact_masked(k, v, now, reserve, dst: PagedKV, *, mode, scores=None, t
     return dst
 
 
+def kvp_compact_quant(k, v, scores, tau, tau_q, dst: QuantPagedKV, *, reserve=0, window=WINDOW, status,
+                      workspace=None, stream=None):
+    """Dense K, V [B, T, H, d] -> the fp8 tier: entries with tau_q <= score < tau (scores [B*T, H] or
+    [B, T, H]; tau, tau_q [B, H]) as E4M3 codes with a per-row scale, visible from position + window on."""
+    B, T, H, d = k.shape
+    if k.stride() != v.stride() or k.stride(3) != 1:
+        raise ValueError("k and v need identical strides with the head_dim axis contiguous")
+    for t, nm in ((k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{nm} must be a CUDA bf16 tensor")
+    if scores.numel() != B * T * H or tau.numel() != B * H or tau_q.numel() != B * H:
+        raise ValueError("scores must hold B*T*H values, tau and tau_q B*H")
+    need = kvp_compact_workspace_bytes(B, H, T)
+    ws = _ws(need, k.device, workspace)
+    code = _lib.kvp_compact_quant(B, H, d, T, k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), k.stride(2),
+                                  _ptr(scores, torch.float32, "scores"), _ptr(tau, torch.float32, "tau"),
+                                  _ptr(tau_q, torch.float32, "tau_q"), window, reserve,
+                                  _ptr(dst.kq_pool, torch.uint8), _ptr(dst.vq_pool, torch.uint8),
+                                  _ptr(dst.meta_pool, torch.int32), dst.n_pages_cap,
+                                  _ptr(dst.page_table, torch.int32), dst.max_pages, _ptr(dst.remap, torch.int32),
+                                  _ptr(dst.count, torch.int32), ws.data_ptr(), ws.numel() * ws.element_size(),
+                                  _ptr(status, torch.int32, "status"), _stream(stream))
+    _check("kvp_compact_quant", code)
+    return dst
+
+
 def kvp_compact_paged_workspace_bytes(batch, n_kv_heads, src_max_pages) -> int:
     return _lib.kvp_compact_paged_workspace_bytes(batch, n_kv_heads, src_max_pages)
 
@@ -405,5 +481,30 @@ def kvp_decode_attn(q, cache: PagedKV, now, *, scale=0.0, out=None, grid_limit=0
     return out
 
 
-__all__ = [n for n in dir() if n.startswith(("kvp_", "KVP_", "PagedKV", "KvpError"))] + [
+def kvp_decode_attn_two_tier(q, cache: PagedKV, qcache: QuantPagedKV, now, *, scale=0.0, out=None, grid_limit=0,
+                             workspace=None, status=None, stream=None):
+    """Attention of q [B, Hq, d] over the bf16 tier `cache` (slots with now < expire) and the fp8 tier
+    `qcache` (slots with now >= start, dequantized) -> out [B, Hq, d] fp32."""
+    B, Hq, d = q.shape
+    H = cache.count.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    need = kvp_decode_attn_workspace_bytes(B, Hq, H, d)
+    if workspace is None:
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)  # zero-filled before first use
+    else:
+        ws = _ws(need, q.device, workspace)
+    code = _lib.kvp_decode_attn_two_tier(
+        B, Hq, H, d, _ptr(q, torch.bfloat16, "q"), _ptr(cache.k_pool), _ptr(cache.v_pool),
+        _ptr(cache.expire_pool, torch.int32), cache.n_pages_cap, _ptr(cache.page_table, torch.int32),
+        cache.max_pages, _ptr(cache.count, torch.int32), _ptr(qcache.kq_pool, torch.uint8),
+        _ptr(qcache.vq_pool, torch.uint8), _ptr(qcache.meta_pool, torch.int32), qcache.n_pages_cap,
+        _ptr(qcache.page_table, torch.int32), qcache.max_pages, _ptr(qcache.count, torch.int32), now, float(scale),
+        _ptr(out, torch.float32, "out"), grid_limit, ws.data_ptr(), ws.numel() * ws.element_size(),
+        _ptr(status, torch.int32, "status", True), _stream(stream))
+    _check("kvp_decode_attn_two_tier", code)
+    return out
+
+
+__all__ = [n for n in dir() if n.startswith(("kvp_", "KVP_", "PagedKV", "QuantPagedKV", "KvpError"))] + [
     "status_string", "version", "library", "PAGE", "WINDOW", "EXPIRE_NEVER"]

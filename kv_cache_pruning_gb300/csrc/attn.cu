@@ -19,6 +19,8 @@
 // bumps the (b, h)'s counter; the warp that brings the counter to the number
 // of pieces merges them (log-sum-exp in fp32) and resets the counter. Nothing
 // ever waits on another warp.
+#include <cuda_fp8.h>
+
 #include "kvp_common.cuh"
 
 namespace kvp {
@@ -47,6 +49,8 @@ struct AttnCfg {
   static constexpr int GL = LPR / G;
   static constexpr int PAGE_BYTES = kPage * D * 2;
   static constexpr int STAGE_BYTES = 2 * PAGE_BYTES + kPage * 4;
+  static constexpr int QPAGE_BYTES = kPage * D;         // fp8 tier: E4M3 codes of one page's K (or V) rows
+  static constexpr int QMETA_BYTES = 3 * kPage * 4;     // fp8 tier: start, K scale, V scale per slot
   static constexpr int RING_BYTES = kWarps * kNst * STAGE_BYTES;
   static constexpr int PS_FLOATS = RPS * G * RS;  // per warp
   static constexpr int PS_BYTES = kWarps * PS_FLOATS * 4;
@@ -56,6 +60,7 @@ struct AttnCfg {
   static_assert(G <= LPR, "group larger than lanes per row");
   static_assert(STAGE_BYTES % 16 == 0 && PS_BYTES % 16 == 0, "16-byte layout");
   static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(2 * QPAGE_BYTES + QMETA_BYTES <= STAGE_BYTES, "an fp8 page fits a stage");
 };
 
 struct AttnParams {
@@ -72,7 +77,31 @@ struct AttnParams {
   float* part_ml;    // [slots, G, 2]
   int32_t* pieces;   // [B*H] arrival counters, zero at entry and exit
   int32_t* status;
+  // fp8 tier (two-tier kernels only)
+  const uint8_t* kq_pool;      // [n_pages_cap_q, 16, D] E4M3 codes
+  const uint8_t* vq_pool;
+  const int32_t* meta_pool;    // [n_pages_cap_q, 3, 16]: start, K scale, V scale
+  const int32_t* page_table_q;
+  const int32_t* count_q;
+  int max_pages_q, n_pages_cap_q;
 };
+
+// Eight E4M3 codes (bytes of x then y, element 0 in the lowest byte) to fp32,
+// exactly (every E4M3 value is an fp16 value).
+KVP_DEV void unpack_e4m3_8(uint32_t x, uint32_t y, float (&f)[8]) {
+  const uint32_t w[2] = {x, y};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const __nv_fp8x2_storage_t pr = static_cast<__nv_fp8x2_storage_t>((w[h] >> (16 * q)) & 0xFFFFu);
+      const __half2 hh = __half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3));
+      const float2 ff = __half22float2(hh);
+      f[4 * h + 2 * q] = ff.x;
+      f[4 * h + 2 * q + 1] = ff.y;
+    }
+  }
+}
 
 // Transposing butterfly: N values per lane, exchange partner lane ^ O. After
 // each exchange a lane keeps the half of the index range selected by bit O of
@@ -143,7 +172,13 @@ KVP_DEV int slice_of(int g, int bh, int nw, int64_t c_end) {
   return static_cast<int>((2 * static_cast<int64_t>(g) + static_cast<int64_t>(kBoundaryCost) * bh) * nw / c_end);
 }
 
-template <int D, int G>
+// kQ: the two-tier kernel. Each (b, h) then lists its bf16 pages and after
+// them its fp8-tier pages (quantize instead of drop): a fp8 page stages its K
+// and V codes and its per-slot record; a lane reads the 8 codes of the same 8
+// columns it covers in a bf16 row, the K row scale multiplies the lane's
+// partial dot product and the V row scale multiplies p in the P.V update (the
+// softmax sum takes p itself); a slot of that tier counts once now >= start.
+template <int D, int G, bool kQ>
 __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnParams p) {
   using C = AttnCfg<D, G>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -164,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
     __syncthreads();
     for (int base = 0; base < BH; base += kThreads) {
       const int bh = base + tid;
-      const int np = bh < BH ? (clamp_count(p.count, bh, p.max_pages) + kPage - 1) / kPage : 0;
+      int np = bh < BH ? (clamp_count(p.count, bh, p.max_pages) + kPage - 1) / kPage : 0;
+      if constexpr (kQ) np += bh < BH ? (clamp_count(p.count_q, bh, p.max_pages_q) + kPage - 1) / kPage : 0;
       int incl = np;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -246,35 +282,62 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   // Page ids of the slice, 32 per register: lane j of block b holds the id of
   // slice page 32*b + j. Block b+1 is loaded when issuing enters block b, so
   // every id is in a register about 32 pages before lane 0 needs it.
-  auto load_ids = [&](int blk) {
+  // bit j of qb0 / qb1: slice page 32 * blk + j (blk even / odd) is a fp8-tier page
+  uint32_t qb0 = 0, qb1 = 0;
+  auto load_ids = [&](int blk, uint32_t& qbits) {  // all lanes call this
     const int kk = blk * 32 + lane;
-    if (kk >= n_my) return -1;
-    const int g = r0 + kk;
-    int a = 0, b = BH - 1;
-    while (a < b) {
-      const int mid = (a + b + 1) >> 1;
-      if (pref[mid] <= g) a = mid; else b = mid - 1;
+    int id = -1;
+    bool isq = false;
+    if (kk < n_my) {
+      const int g = r0 + kk;
+      int a = 0, b = BH - 1;
+      while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (pref[mid] <= g) a = mid; else b = mid - 1;
+      }
+      const int li = g - pref[a];
+      if constexpr (kQ) {
+        const int na = (clamp_count(p.count, a, p.max_pages) + kPage - 1) / kPage;
+        isq = li >= na;
+        id = isq ? static_cast<int>(p.page_table_q[static_cast<int64_t>(a) * p.max_pages_q + (li - na)])
+                 : static_cast<int>(p.page_table[static_cast<int64_t>(a) * p.max_pages + li]);
+      } else {
+        id = static_cast<int>(p.page_table[static_cast<int64_t>(a) * p.max_pages + li]);
+      }
     }
-    return static_cast<int>(p.page_table[static_cast<int64_t>(a) * p.max_pages + (g - pref[a])]);
+    if constexpr (kQ) qbits = __ballot_sync(0xffffffffu, isq);
+    return id;
   };
-  int ids0 = load_ids(0), ids1 = load_ids(1);
-  auto page_id = [&](int k) {  // all lanes call this
+  int ids0 = load_ids(0, qb0), ids1 = load_ids(1, qb1);
+  auto page_id = [&](int k, bool& isq) {  // all lanes call this
     const int blk = k >> 5;
     const int v = __shfl_sync(0xffffffffu, (blk & 1) ? ids1 : ids0, k & 31);
+    isq = kQ && ((((blk & 1) ? qb1 : qb0) >> (k & 31)) & 1u);
     if ((k & 31) == 0 && k > 0) {  // block blk - 1 is done: its register takes block blk + 1
-      if (blk & 1) ids0 = load_ids(blk + 1); else ids1 = load_ids(blk + 1);
+      if (blk & 1) ids0 = load_ids(blk + 1, qb0); else ids1 = load_ids(blk + 1, qb1);
     }
     return v;
   };
-  auto issue = [&](int k, int64_t phys) {  // lane 0
+  auto issue = [&](int k, int64_t phys, bool isq) {  // lane 0
     const int st = k % kNst;
     uint8_t* dst = ring + st * C::STAGE_BYTES;
-    if (phys < 0 || phys >= p.n_pages_cap) {
+    if (phys < 0 || phys >= (isq ? p.n_pages_cap_q : p.n_pages_cap)) {
       // inconsistent page table: no copy; the stage reads as an empty page
       record_error(p.status, KVP_ERR_BOUNDS);
       uint4* z = reinterpret_cast<uint4*>(dst);
       for (int i = 0; i < C::STAGE_BYTES / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+      if (isq) {  // a fp8 slot counts once now >= start: make every start unreachable
+        int32_t* starts = reinterpret_cast<int32_t*>(dst + 2 * C::QPAGE_BYTES);
+        for (int i = 0; i < kPage; ++i) starts[i] = kNever;
+      }
       mbar_arrive(&bars[st]);
+      return;
+    }
+    if (kQ && isq) {
+      mbar_arrive_expect_tx(&bars[st], 2 * C::QPAGE_BYTES + C::QMETA_BYTES);
+      bulk_g2s(dst, p.kq_pool + phys * C::QPAGE_BYTES, C::QPAGE_BYTES, &bars[st]);
+      bulk_g2s(dst + C::QPAGE_BYTES, p.vq_pool + phys * C::QPAGE_BYTES, C::QPAGE_BYTES, &bars[st]);
+      bulk_g2s(dst + 2 * C::QPAGE_BYTES, p.meta_pool + phys * 3 * kPage, C::QMETA_BYTES, &bars[st]);
       return;
     }
     mbar_arrive_expect_tx(&bars[st], C::STAGE_BYTES);
@@ -288,8 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   }
   __syncwarp();
   for (int k = 0; k < n_my && k < kNst; ++k) {
-    const int pid = page_id(k);
-    if (lane == 0) issue(k, pid);
+    bool isq;
+    const int pid = page_id(k, isq);
+    if (lane == 0) issue(k, pid, isq);
   }
   __syncwarp();
 
@@ -324,9 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   int seg_end = min(pref[cbh + 1], r1);
   int cnt = clamp_count(p.count, cbh, p.max_pages);
   int cnt_next = 0;
+  int cnt_q = kQ ? clamp_count(p.count_q, cbh, p.max_pages_q) : 0;  // fp8-tier slots of this (b, h)
+  int cnt_q_next = 0;
   if (seg_end < r1) {
     load_q(next_bh(cbh), qn);
     cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
+    if constexpr (kQ) cnt_q_next = clamp_count(p.count_q, next_bh(cbh), p.max_pages_q);
   }
 
   float m_run[G], l_run[G], acc[G][8];
@@ -351,26 +418,47 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
     const uint16_t* Ks = reinterpret_cast<const uint16_t*>(stage);
     const uint16_t* Vs = reinterpret_cast<const uint16_t*>(stage + C::PAGE_BYTES);
     const int32_t* Es = reinterpret_cast<const int32_t*>(stage + 2 * C::PAGE_BYTES);
-    const int slot0 = (g - pref[cbh]) * kPage;
+    const int li = g - pref[cbh];
+    const int na_cur = (cnt + kPage - 1) / kPage;  // bf16 pages of this (b, h)
+    const bool isq = kQ && li >= na_cur;           // a fp8-tier page (uniform in the warp)
+    const int slot0 = (isq ? li - na_cur : li) * kPage;
 
     // this lane's share of the page goes to registers and the stage is handed
     // straight back to the copy engine: every stage of the ring stays in
     // flight while the warp computes
     uint4 kr[C::RS], vr[C::RS];
     int32_t er[C::VL];
+    if (isq) {
+      // codes of the lane's 8 columns in .x/.y, the row's scale in .z
+      const uint8_t* Kq = stage;
+      const uint8_t* Vq = stage + C::QPAGE_BYTES;
+      const int32_t* Mq = reinterpret_cast<const int32_t*>(stage + 2 * C::QPAGE_BYTES);
 #pragma unroll
-    for (int t = 0; t < C::RS; ++t) {
-      kr[t] = reinterpret_cast<const uint4*>(Ks + (t * C::RPS + rowsel) * D)[s];
-      vr[t] = reinterpret_cast<const uint4*>(Vs + (t * C::RPS + rowsel) * D)[s];
+      for (int t = 0; t < C::RS; ++t) {
+        const int row = t * C::RPS + rowsel;
+        const uint2 kc = reinterpret_cast<const uint2*>(Kq + row * D)[s];
+        const uint2 vc = reinterpret_cast<const uint2*>(Vq + row * D)[s];
+        kr[t] = make_uint4(kc.x, kc.y, static_cast<uint32_t>(Mq[kPage + row]), 0u);
+        vr[t] = make_uint4(vc.x, vc.y, static_cast<uint32_t>(Mq[2 * kPage + row]), 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < C::VL; ++u) er[u] = Mq[((idx_base + u) % C::RS) * C::RPS + rowsel];
+    } else {
+#pragma unroll
+      for (int t = 0; t < C::RS; ++t) {
+        kr[t] = reinterpret_cast<const uint4*>(Ks + (t * C::RPS + rowsel) * D)[s];
+        vr[t] = reinterpret_cast<const uint4*>(Vs + (t * C::RPS + rowsel) * D)[s];
+      }
+#pragma unroll
+      for (int u = 0; u < C::VL; ++u) er[u] = Es[((idx_base + u) % C::RS) * C::RPS + rowsel];
     }
-#pragma unroll
-    for (int u = 0; u < C::VL; ++u) er[u] = Es[((idx_base + u) % C::RS) * C::RPS + rowsel];
     __syncwarp();
     if (k + kNst < n_my) {
-      const int pid = page_id(k + kNst);
+      bool isq_n;
+      const int pid = page_id(k + kNst, isq_n);
       if (lane == 0) {
         fence_proxy_async();
-        issue(k + kNst, pid);
+        issue(k + kNst, pid, isq_n);
       }
     }
 
@@ -379,13 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
 #pragma unroll
     for (int t = 0; t < C::RS; ++t) {
       float kf[8];
-      unpack8(kr[t], kf);
+      if (isq) unpack_e4m3_8(kr[t].x, kr[t].y, kf); else unpack8(kr[t], kf);
 #pragma unroll
       for (int i = 0; i < G; ++i) {
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; e += 2) fma2(a0, a1, qf[i][e], qf[i][e + 1], kf[e], kf[e + 1]);
-        part[i * C::RS + t] = a0 + a1;
+        part[i * C::RS + t] = isq ? (a0 + a1) * __uint_as_float(kr[t].z) : a0 + a1;
       }
     }
     TransposeReduce<C::V, C::LPR / 2>::run(part, lane);
@@ -399,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
 #pragma unroll
     for (int u = 0; u < C::VL; ++u) {
       const int r = ((idx_base + u) % C::RS) * C::RPS + rowsel;
-      const bool valid = (slot0 + r < cnt) && (p.now < er[u]);
+      const bool valid = isq ? (slot0 + r < cnt_q) && (p.now >= er[u]) : (slot0 + r < cnt) && (p.now < er[u]);
       x[u] = valid ? part[u] : -INFINITY;
       grow |= x[u] > mh + kLazyRescale;
     }
@@ -438,13 +526,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
 #pragma unroll
     for (int t = 0; t < C::RS; ++t) {
       float vf[8];
-      unpack8(vr[t], vf);
+      if (isq) unpack_e4m3_8(vr[t].x, vr[t].y, vf); else unpack8(vr[t], vf);
 #pragma unroll
       for (int i = 0; i < G; ++i) {
         const float pr = p_s[rowsel * G * C::RS + i * C::RS + t];
         l_run[i] += pr;
+        const float pw = isq ? pr * __uint_as_float(vr[t].z) : pr;
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) fma2(acc[i][e], acc[i][e + 1], pr, pr, vf[e], vf[e + 1]);
+        for (int e = 0; e < 8; e += 2) fma2(acc[i][e], acc[i][e + 1], pw, pw, vf[e], vf[e + 1]);
       }
     }
 
@@ -690,6 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
         cbh = next_bh(cbh);
         seg_end = min(pref[cbh + 1], r1);
         cnt = cnt_next;
+        cnt_q = cnt_q_next;
 #pragma unroll
         for (int i = 0; i < G; ++i) {
           unpack8(qn[i], qf[i]);
@@ -699,6 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
         if (seg_end < r1) {
           load_q(next_bh(cbh), qn);
           cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
+          if constexpr (kQ) cnt_q_next = clamp_count(p.count_q, next_bh(cbh), p.max_pages_q);
         }
 #pragma unroll
         for (int i = 0; i < G; ++i) {
@@ -714,11 +805,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
 
 // Grid of the persistent kernel on this process's device: one CTA per SM
 // times the CTAs an SM holds, computed once (with the shared-memory opt-in).
-template <int D, int G>
+template <int D, int G, bool kQ>
 int attn_grid() {
   static const int grid = [] {
     using C = AttnCfg<D, G>;
-    auto kern = attn_decode_kernel<D, G>;
+    auto kern = attn_decode_kernel<D, G, kQ>;
     int dev = 0, nsm = 0, occ = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess ||
         cudaGetDevice(&dev) != cudaSuccess ||
@@ -730,24 +821,24 @@ int attn_grid() {
   return grid;
 }
 
-template <int D, int G>
+template <int D, int G, bool kQ>
 kvp_status launch_attn(const AttnParams& p, int grid_limit, cudaStream_t st) {
   using C = AttnCfg<D, G>;
-  int grid = attn_grid<D, G>();
+  int grid = attn_grid<D, G, kQ>();
   if (grid <= 0) return KVP_ERR_CUDA;
   if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
-  if (launch_pdl(attn_decode_kernel<D, G>, dim3(grid), dim3(kThreads), C::SMEM, st, p) != cudaSuccess)
+  if (launch_pdl(attn_decode_kernel<D, G, kQ>, dim3(grid), dim3(kThreads), C::SMEM, st, p) != cudaSuccess)
     return KVP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
-template <int D>
+template <int D, bool kQ>
 kvp_status dispatch_g(const AttnParams& p, int G, int grid_limit, cudaStream_t st) {
   switch (G) {
-    case 1: return launch_attn<D, 1>(p, grid_limit, st);
-    case 2: return launch_attn<D, 2>(p, grid_limit, st);
-    case 4: return launch_attn<D, 4>(p, grid_limit, st);
-    case 8: return launch_attn<D, 8>(p, grid_limit, st);
+    case 1: return launch_attn<D, 1, kQ>(p, grid_limit, st);
+    case 2: return launch_attn<D, 2, kQ>(p, grid_limit, st);
+    case 4: return launch_attn<D, 4, kQ>(p, grid_limit, st);
+    case 8: return launch_attn<D, 8, kQ>(p, grid_limit, st);
     default: return KVP_ERR_UNSUPPORTED;
   }
 }
@@ -774,11 +865,22 @@ extern "C" size_t kvp_decode_attn_workspace_bytes(int batch, int n_q_heads, int 
   return ws_counter_bytes(BH) + ws_ml_bytes(BH, G) + ws_slots(BH) * G * head_dim * sizeof(float);
 }
 
-extern "C" kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q,
-                                      const void* k_pool, const void* v_pool, const int32_t* expire_pool,
-                                      int n_pages_cap, const int32_t* page_table, int max_pages,
-                                      const int32_t* count, int now, float scale, float* out, int grid_limit,
-                                      void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+namespace {
+struct QuantTier {
+  const void* kq_pool;
+  const void* vq_pool;
+  const int32_t* meta_pool;
+  int n_pages_cap;
+  const int32_t* page_table;
+  int max_pages;
+  const int32_t* count;
+};
+
+kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q, const void* k_pool,
+                            const void* v_pool, const int32_t* expire_pool, int n_pages_cap,
+                            const int32_t* page_table, int max_pages, const int32_t* count, const QuantTier* qt,
+                            int now, float scale, float* out, int grid_limit, void* workspace,
+                            size_t workspace_bytes, int32_t* status, void* stream) {
   if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_pages < 0 || grid_limit < 0 || n_pages_cap < 0)
     return KVP_ERR_INVALID;
   if (n_q_heads % n_kv_heads != 0) return KVP_ERR_INVALID;
@@ -793,6 +895,14 @@ extern "C" kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, 
     return KVP_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(expire_pool) || !aligned16(out))
     return KVP_ERR_ALIGN;
+  if (qt != nullptr) {
+    if (qt->max_pages < 0 || qt->n_pages_cap < 0) return KVP_ERR_INVALID;
+    if (static_cast<int64_t>(qt->max_pages) * kPage > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
+    if (qt->kq_pool == nullptr || qt->vq_pool == nullptr || qt->meta_pool == nullptr || qt->page_table == nullptr ||
+        qt->count == nullptr)
+      return KVP_ERR_INVALID;
+    if (!aligned16(qt->kq_pool) || !aligned16(qt->vq_pool) || !aligned16(qt->meta_pool)) return KVP_ERR_ALIGN;
+  }
   const size_t need = kvp_decode_attn_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim);
   if (workspace == nullptr || workspace_bytes < need) return KVP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return KVP_ERR_ALIGN;
@@ -822,6 +932,40 @@ extern "C" kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, 
                part_acc,
                part_ml,
                pieces,
-               status};
-  return head_dim == 128 ? dispatch_g<128>(p, G, grid_limit, st) : dispatch_g<64>(p, G, grid_limit, st);
+               status,
+               qt ? static_cast<const uint8_t*>(qt->kq_pool) : nullptr,
+               qt ? static_cast<const uint8_t*>(qt->vq_pool) : nullptr,
+               qt ? qt->meta_pool : nullptr,
+               qt ? qt->page_table : nullptr,
+               qt ? qt->count : nullptr,
+               qt ? qt->max_pages : 0,
+               qt ? qt->n_pages_cap : 0};
+  if (qt != nullptr)
+    return head_dim == 128 ? dispatch_g<128, true>(p, G, grid_limit, st) : dispatch_g<64, true>(p, G, grid_limit, st);
+  return head_dim == 128 ? dispatch_g<128, false>(p, G, grid_limit, st) : dispatch_g<64, false>(p, G, grid_limit, st);
+}
+}  // namespace
+
+extern "C" kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q,
+                                      const void* k_pool, const void* v_pool, const int32_t* expire_pool,
+                                      int n_pages_cap, const int32_t* page_table, int max_pages,
+                                      const int32_t* count, int now, float scale, float* out, int grid_limit,
+                                      void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+  return decode_attn_impl(batch, n_q_heads, n_kv_heads, head_dim, q, k_pool, v_pool, expire_pool, n_pages_cap,
+                          page_table, max_pages, count, nullptr, now, scale, out, grid_limit, workspace,
+                          workspace_bytes, status, stream);
+}
+
+extern "C" kvp_status kvp_decode_attn_two_tier(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q,
+                                               const void* k_pool, const void* v_pool, const int32_t* expire_pool,
+                                               int n_pages_cap, const int32_t* page_table, int max_pages,
+                                               const int32_t* count, const void* kq_pool, const void* vq_pool,
+                                               const int32_t* meta_pool, int n_pages_cap_q,
+                                               const int32_t* page_table_q, int max_pages_q, const int32_t* count_q,
+                                               int now, float scale, float* out, int grid_limit, void* workspace,
+                                               size_t workspace_bytes, int32_t* status, void* stream) {
+  const QuantTier qt{kq_pool, vq_pool, meta_pool, n_pages_cap_q, page_table_q, max_pages_q, count_q};
+  return decode_attn_impl(batch, n_q_heads, n_kv_heads, head_dim, q, k_pool, v_pool, expire_pool, n_pages_cap,
+                          page_table, max_pages, count, &qt, now, scale, out, grid_limit, workspace,
+                          workspace_bytes, status, stream);
 }

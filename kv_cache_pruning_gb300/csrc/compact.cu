@@ -1,4 +1,4 @@
-// kvp_mask, kvp_compact, kvp_compact_masked, kvp_compact_paged, kvp_append.
+// kvp_mask, kvp_compact, kvp_compact_masked, kvp_compact_quant, kvp_compact_paged, kvp_append.
 //
 // Rules (KVzap summary "실제 적용"; DMS article "지연 삭제 (Delayed Eviction)"):
 // an entry gets the first step at which it is gone,
@@ -15,6 +15,9 @@
 // and moves its K and V rows with 16-byte vector loads and stores, 8 rows'
 // loads in flight per lane before their stores.
 #include <mutex>
+#include <type_traits>
+
+#include <cuda_fp8.h>
 
 #include "kvp_common.cuh"
 
@@ -22,6 +25,7 @@ namespace kvp {
 namespace {
 
 constexpr int kSeg = 128;           // entries per warp segment
+constexpr int kQuantMetaWords = 3 * KVP_PAGE_TOKENS;  // fp8 tier page record: start, K scale, V scale
 constexpr int kWarpsPerCta = 4;     // segments per CTA in the count and copy passes
 
 KVP_DEV int32_t expire_kvzap(float s, float tau, int pos, int window) {
@@ -119,6 +123,7 @@ struct DenseSrc {
       return exp[t];
     }
     KVP_DEV int position_of(int t) const { return t; }
+    KVP_DEV bool keep(int32_t e, int now) const { return now < e; }
   };
   KVP_DEV View view(int bh) const {
     const int b = bh / H, h = bh - b * H;
@@ -158,6 +163,7 @@ struct MaskedSrc {
                                     : expire_dms(fl[t], t, delay, window);
     }
     KVP_DEV int position_of(int t) const { return t; }
+    KVP_DEV bool keep(int32_t e, int now) const { return now < e; }
   };
   KVP_DEV View view(int bh) const {
     const int b = bh / H, h = bh - b * H;
@@ -174,6 +180,47 @@ struct MaskedSrc {
                 window,
                 delay,
                 n};
+  }
+};
+
+// Selection for the fp8 tier (quantize instead of drop; BeaconKV article):
+// entry t of the dense source goes to the tier iff tau_q <= score < tau (NaN
+// never), and its value is the step from which it is visible there, the
+// step its full-precision copy leaves the window (t + window). `now` plays
+// no part in the choice.
+constexpr int32_t kNotSelected = INT32_MIN;
+
+struct QuantSrc {
+  const uint16_t* k;
+  const uint16_t* v;
+  int64_t sb, st, sh;
+  const float* scores;     // [B, n, H]
+  const float* tau;        // [B, H]
+  const float* tau_q;      // [B, H]
+  int window;
+  int H;
+  int n;
+  struct View {
+    const uint16_t* kb;
+    const uint16_t* vb;
+    int64_t stride;
+    const float* sc;
+    float th, tq;
+    int H, window, n;
+    KVP_DEV int length() const { return n; }
+    KVP_DEV int32_t expire_row(int t, int64_t& row) const {
+      row = t;
+      const float x = sc[static_cast<int64_t>(t) * H];
+      return (x >= tq && x < th) ? t + window : kNotSelected;
+    }
+    KVP_DEV int position_of(int t) const { return t; }
+    KVP_DEV bool keep(int32_t e, int) const { return e != kNotSelected; }
+  };
+  KVP_DEV View view(int bh) const {
+    const int b = bh / H, h = bh - b * H;
+    const int64_t off = b * sb + h * sh;
+    return View{k + off, v + off, st, scores + static_cast<int64_t>(b) * n * H + h, tau[bh], tau_q[bh],
+                H, window, n};
   }
 };
 
@@ -212,6 +259,7 @@ struct PagedSrc {
       return expire_pool[row];
     }
     KVP_DEV int position_of(int j) const { return remap[j]; }
+    KVP_DEV bool keep(int32_t e, int now) const { return now < e; }
   };
   KVP_DEV View view(int bh) const {
     const int n = min(max(count[bh], 0), max_pages * kPage);
@@ -260,7 +308,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) count_kernel(Src src, int n
       if (t < hi) {
         int64_t row;
         const int32_t e = sv.expire_row(t, row);
-        kept += (row >= 0 && now < e);
+        kept += (row >= 0 && sv.keep(e, now));
       }
     }
     kept = __reduce_add_sync(0xffffffffu, kept);
@@ -373,6 +421,10 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
                                                                      int32_t* __restrict__ remap) {
   constexpr int E16 = 2 * D * 2 / 16;   // 16-byte pieces per entry (K row then V row)
   constexpr int EPI = 32 / E16;         // entries per warp instruction (1 for D = 128, 2 for D = 64)
+  // fp8 tier: k_pool / v_pool hold E4M3 codes (D bytes a row) and expire_pool
+  // is the per-page record [start x 16, K scale x 16, V scale x 16]
+  constexpr bool kQuant = std::is_same<Src, QuantSrc>::value;
+  constexpr int kMetaStride = kQuant ? kQuantMetaWords : kPage;
   extern __shared__ __align__(16) uint8_t sm_raw[];
   pdl_launch_dependents();
   pdl_wait();  // segment counts and (b, h) counts come from the passes before this one
@@ -460,11 +512,19 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
     const int zseg = (pages * kPage - cnt + NS - 1) / NS;
     for (int j = cnt + sg * zseg; j < min(pages * kPage, cnt + (sg + 1) * zseg); ++j) {
       const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
-      if (lane < VPR) {
-        reinterpret_cast<uint4*>(k_pool + row * D)[lane] = make_uint4(0, 0, 0, 0);
-        reinterpret_cast<uint4*>(v_pool + row * D)[lane] = make_uint4(0, 0, 0, 0);
+      if constexpr (kQuant) {
+        if (lane < D / 16) {
+          reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(k_pool) + row * D)[lane] = make_uint4(0, 0, 0, 0);
+          reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(v_pool) + row * D)[lane] = make_uint4(0, 0, 0, 0);
+        }
+        if (lane < 3) expire_pool[static_cast<int64_t>(base + (j >> 4)) * kMetaStride + lane * kPage + (j & 15)] = 0;
+      } else {
+        if (lane < VPR) {
+          reinterpret_cast<uint4*>(k_pool + row * D)[lane] = make_uint4(0, 0, 0, 0);
+          reinterpret_cast<uint4*>(v_pool + row * D)[lane] = make_uint4(0, 0, 0, 0);
+        }
+        if (lane == 0) expire_pool[row] = 0;
       }
-      if (lane == 0) expire_pool[row] = 0;
     }
   }
 
@@ -475,13 +535,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
     const int t = lo + u * 32 + lane;
     const int64_t row = rows[u];
     const int32_t e = exps[u];
-    const bool keep = (t < hi) && (row >= 0) && (now < e);
+    const bool keep = (t < hi) && (row >= 0) && sv.keep(e, now);
     const unsigned bal = __ballot_sync(0xffffffffu, keep);
     if (keep) {
       const int i = nk + __popc(bal & ((1u << lane) - 1u));
       const int j = slot0 + i;
       lst[i] = row;
-      expire_pool[static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15)] = e;
+      expire_pool[static_cast<int64_t>(base + (j >> 4)) * kMetaStride + (j & 15)] = e;
       remap_bh[j] = sv.position_of(t);
     }
     nk += __popc(bal);
@@ -501,10 +561,52 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
       cp_async16(stage + i * E16 + piece, reinterpret_cast<const uint4*>(sbase + lst[i0 + i] * sv.stride) + vi);
     cp_async_wait_all();
     __syncwarp();
-    for (int i = sub; i < nb; i += EPI) {
-      const int j = slot0 + i0 + i;
-      const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
-      reinterpret_cast<uint4*>(dbase + row * D)[vi] = stage[i * E16 + piece];
+    if constexpr (kQuant) {
+      // each row's E16 / 2 lanes: amax over the row, scale = amax / 448, then
+      // every element divided by the scale and rounded to E4M3 (saturating);
+      // the lanes of a row store 8 codes each, its first lane the scale
+      uint8_t* qbase = reinterpret_cast<uint8_t*>(dbase);
+      for (int ib = 0; ib < nb; ib += EPI) {
+        const int i = ib + sub;
+        const bool act = i < nb;  // the warp's lanes all take part in the reduction
+        const uint4 w = act ? stage[i * E16 + piece] : make_uint4(0, 0, 0, 0);
+        float f[8];
+        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x);
+        f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+        f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z);
+        f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+        for (int o = 1; o < E16 / 2; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float scale = __fdiv_rn(amax, 448.f);
+        uint32_t packed[2] = {0u, 0u};
+        if (scale > 0.f) {
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            float2 pr;
+            pr.x = __fdiv_rn(f[e], scale);
+            pr.y = __fdiv_rn(f[e + 1], scale);
+            const uint32_t c2 = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3));
+            packed[e >> 2] |= c2 << (16 * ((e >> 1) & 1));
+          }
+        }
+        if (act) {
+          const int j = slot0 + i0 + i;
+          const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
+          reinterpret_cast<uint2*>(qbase + row * D)[vi] = make_uint2(packed[0], packed[1]);
+          if (vi == 0)
+            reinterpret_cast<float*>(expire_pool)[static_cast<int64_t>(base + (j >> 4)) * kMetaStride +
+                                                  (is_v ? 2 : 1) * kPage + (j & 15)] = scale;
+        }
+      }
+    } else {
+      for (int i = sub; i < nb; i += EPI) {
+        const int j = slot0 + i0 + i;
+        const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
+        reinterpret_cast<uint4*>(dbase + row * D)[vi] = stage[i * E16 + piece];
+      }
     }
     __syncwarp();
   }
@@ -709,6 +811,40 @@ extern "C" kvp_status kvp_compact_masked(int mode, int batch, int n_kv_heads, in
                 n_kv_heads,
                 n_pos};
   return run_compact(src, batch * n_kv_heads, NS, head_dim, now, reserve, k_pool, v_pool, expire_pool, n_pages_cap,
+                     page_table, max_pages, remap, count, workspace, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvp_status kvp_compact_quant(int batch, int n_kv_heads, int head_dim, int n_pos, const void* k_src,
+                                        const void* v_src, int64_t stride_b, int64_t stride_t, int64_t stride_h,
+                                        const float* scores, const float* tau, const float* tau_q, int window,
+                                        int reserve, void* kq_pool, void* vq_pool, int32_t* meta_pool,
+                                        int n_pages_cap, int32_t* page_table, int max_pages, int32_t* remap,
+                                        int32_t* count, void* workspace, size_t workspace_bytes, int32_t* status,
+                                        void* stream) {
+  if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0 || window < 0) return KVP_ERR_INVALID;
+  if (scores == nullptr || tau == nullptr || tau_q == nullptr) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(n_pos) + window >= kNever) return KVP_ERR_INVALID;
+  kvp_status s = check_dst(head_dim, reserve, kq_pool, vq_pool, meta_pool, n_pages_cap, page_table, max_pages,
+                           remap, count, status);
+  if (s != KVP_OK) return s;
+  if (n_pos > 0 && (k_src == nullptr || v_src == nullptr)) return KVP_ERR_INVALID;
+  if (!aligned16(k_src) || !aligned16(v_src) || stride_b % 8 || stride_t % 8 || stride_h % 8) return KVP_ERR_ALIGN;
+  if (stride_b < 0 || stride_t < 0 || stride_h < 0) return KVP_ERR_INVALID;
+  if (workspace == nullptr || workspace_bytes < kvp_compact_workspace_bytes(batch, n_kv_heads, n_pos))
+    return KVP_ERR_WORKSPACE;
+  const int NS = n_segments(n_pos);
+  QuantSrc src{static_cast<const uint16_t*>(k_src),
+               static_cast<const uint16_t*>(v_src),
+               stride_b,
+               stride_t,
+               stride_h,
+               scores,
+               tau,
+               tau_q,
+               window,
+               n_kv_heads,
+               n_pos};
+  return run_compact(src, batch * n_kv_heads, NS, head_dim, 0, reserve, kq_pool, vq_pool, meta_pool, n_pages_cap,
                      page_table, max_pages, remap, count, workspace, status, static_cast<cudaStream_t>(stream));
 }
 

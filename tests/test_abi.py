@@ -25,7 +25,7 @@ def lib():
 
 def test_header_declares_the_path():
     names = set(_declared())
-    for n in ["kvp_score", "kvp_mask", "kvp_compact", "kvp_compact_masked", "kvp_compact_paged", "kvp_threshold", "kvp_append", "kvp_decode_attn",
+    for n in ["kvp_score", "kvp_mask", "kvp_compact", "kvp_compact_masked", "kvp_compact_quant", "kvp_compact_paged", "kvp_threshold", "kvp_append", "kvp_decode_attn",
               "kvp_score_workspace_bytes", "kvp_compact_workspace_bytes", "kvp_decode_attn_workspace_bytes",
               "kvp_status_string", "kvp_version"]:
         assert n in names, n
@@ -111,6 +111,23 @@ def test_compact_masked_host_checks():
     assert call(hd=96) == k.KVP_ERR_UNSUPPORTED
     assert call(status=None) == k.KVP_ERR_INVALID
     assert call(kp=8) == k.KVP_ERR_ALIGN
+
+
+def test_compact_quant_host_checks():
+    import kv_cache_pruning_gb300 as k
+    L = k.library()
+
+    def call(hd=128, scores=16, tau=16, tau_q=16, window=128, kq=16, meta=16, status=16):
+        return L.kvp_compact_quant(1, 1, hd, 16, 16, 16, 0, 0, 0, scores, tau, tau_q, window, 0, kq, 16, meta, 1,
+                                   16, 1, 16, 16, 16, 1 << 20, status, None)
+
+    assert call(tau_q=None) == k.KVP_ERR_INVALID
+    assert call(scores=None) == k.KVP_ERR_INVALID
+    assert call(window=-1) == k.KVP_ERR_INVALID
+    assert call(meta=None) == k.KVP_ERR_INVALID
+    assert call(status=None) == k.KVP_ERR_INVALID
+    assert call(hd=96) == k.KVP_ERR_UNSUPPORTED
+    assert call(kq=8) == k.KVP_ERR_ALIGN
 
 
 def test_threshold_host_checks():

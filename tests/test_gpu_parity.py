@@ -362,6 +362,90 @@ def test_compact_masked_capacity_status(kvp):
     assert st.item() == kvp.KVP_ERR_CAPACITY
 
 
+# --------------------------------------------------------------------------- fp8 tier
+
+def _compare_qcache(gpu, ref: orc.QuantPagedCache):
+    np.testing.assert_array_equal(gpu.count.cpu().numpy(), ref.count, err_msg="count")
+    np.testing.assert_array_equal(gpu.page_table.cpu().numpy(), ref.page_table, err_msg="page_table")
+    np.testing.assert_array_equal(gpu.remap.cpu().numpy(), ref.remap, err_msg="remap")
+    used = ref.pages_used
+    np.testing.assert_array_equal(gpu.kq_pool.cpu().numpy()[:used], ref.kq_pool[:used], err_msg="K codes")
+    np.testing.assert_array_equal(gpu.vq_pool.cpu().numpy()[:used], ref.vq_pool[:used], err_msg="V codes")
+    np.testing.assert_array_equal(gpu.kscale.cpu().numpy()[:used].view(np.uint32),
+                                  ref.kscale[:used].view(np.uint32), err_msg="K scales")
+    np.testing.assert_array_equal(gpu.vscale.cpu().numpy()[:used].view(np.uint32),
+                                  ref.vscale[:used].view(np.uint32), err_msg="V scales")
+    np.testing.assert_array_equal(gpu.start_pool.cpu().numpy()[:used], ref.start_pool[:used], err_msg="start")
+
+
+def _quant_case(B, T, H, d, seed, kv_std=1.0):
+    k, v = syn.kv_inputs(seed, B, T, H, d)
+    if kv_std != 1.0:
+        k = syn.f32_to_bf16_bits((orc.widen_bf16(k) * kv_std).astype(np.float32))
+    s = syn.normal_f32(seed, 31, (B, T, H))
+    s[0, min(3, T - 1), 0] = np.nan
+    tau = syn.normal_f32(seed, 32, (B, H), std=0.3) + np.float32(0.7)
+    tau_q = syn.normal_f32(seed, 33, (B, H), std=0.3) - np.float32(0.7)
+    tau_q[-1, -1] = -np.inf                # every entry below tau goes to the fp8 tier
+    tau_q[0, -1] = tau[0, -1]              # empty fp8 tier for this head
+    return k, v, s, tau.astype(np.float32), tau_q.astype(np.float32)
+
+
+@pytest.mark.parametrize("B,T,H,d,reserve,window,strided", [
+    (1, 512, 2, 64, 0, 128, False),
+    (2, 3000, 3, 128, 5, 128, True),
+    (4, 1030, 8, 128, 64, 7, False),
+    (2, 17, 2, 64, 16, 0, False),
+    (131, 40, 8, 64, 3, 16, False),     # more than 1024 (b, h): page bases from the separate base pass
+])
+def test_compact_quant_bit_exact(kvp, B, T, H, d, reserve, window, strided):
+    """fp8-tier compaction: codes, scales, start steps, page tables and remap
+    lists bit-identical to the oracle."""
+    k, v, s, tau, tau_q = _quant_case(B, T, H, d, seed=13, kv_std=3.0)
+    max_pages = (T + reserve + 15) // 16
+    cap = B * H * max_pages
+    ref = orc.compact_quant_dense(k, v, s, tau, tau_q, reserve, cap, max_pages, window=window)
+    if strided:
+        kd = dev_bf16(np.ascontiguousarray(k.transpose(0, 2, 1, 3))).permute(0, 2, 1, 3)
+        vd = dev_bf16(np.ascontiguousarray(v.transpose(0, 2, 1, 3))).permute(0, 2, 1, 3)
+    else:
+        kd, vd = dev_bf16(k), dev_bf16(v)
+    st = status_word()
+    dst = kvp.QuantPagedKV.allocate(B, H, d, cap, max_pages)
+    kvp.kvp_compact_quant(kd, vd, dev_f32(s), dev_f32(tau), dev_f32(tau_q), dst, reserve=reserve, window=window,
+                          status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_qcache(dst, ref)
+
+
+def test_compact_quant_special_rows(kvp):
+    """All-zero rows (scale 0, codes 0), rows with one huge element (everything
+    else in the subnormal range) and exact ties on the E4M3 grid."""
+    B, T, H, d = 1, 64, 2, 128
+    rng = np.random.default_rng(5)
+    kf = rng.standard_normal((B, T, H, d)).astype(np.float32)
+    kf[0, 0] = 0.0                                    # zero rows
+    kf[0, 1, :, :] *= 1e-3
+    kf[0, 1, :, 0] = 300.0                            # one large element, the rest tiny
+    grid = orc.e4m3_positive_values()[:127]
+    mids = np.resize(((grid[:-1] + grid[1:]) / 2)[20:], d - 1)
+    kf[0, 2, :, 0] = 448.0                            # scale exactly 1: the others are exact ties
+    kf[0, 2, :, 1:] = mids
+    k = syn.f32_to_bf16_bits(kf)
+    v = syn.f32_to_bf16_bits(kf[:, ::-1].copy())
+    s = np.zeros((B, T, H), np.float32)
+    tau = np.ones((B, H), np.float32)
+    tau_q = np.full((B, H), -1.0, np.float32)
+    ref = orc.compact_quant_dense(k, v, s, tau, tau_q, 0, 16, 8)
+    st = status_word()
+    dst = kvp.QuantPagedKV.allocate(B, H, d, 16, 8)
+    kvp.kvp_compact_quant(dev_bf16(k), dev_bf16(v), dev_f32(s), dev_f32(tau), dev_f32(tau_q), dst, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_qcache(dst, ref)
+
+
 def _dms_stream(B, T, H, d, delay, window, seed):
     k, v = syn.kv_inputs(seed, B, T, H, d)
     pos = np.arange(T)[None, None, :]
@@ -509,6 +593,63 @@ def test_decode_attn_workspace_reused_across_calls(kvp):
             assert st.item() == 0
             assert torch.equal(o, fresh)
             assert int(ws[: B * H * 4].view(torch.int32).abs().sum()) == 0   # counters back to zero
+
+
+def _two_tier_case(kvp, B, T, H, G, d, pps=0, now=None, seed=17, empty_q=False):
+    k, v = syn.kv_inputs(seed, B, T, H, d)
+    q = syn.q_inputs(seed, B, H * G, d)
+    s = syn.normal_f32(seed, 41, (B, T, H))
+    tau = (syn.normal_f32(seed, 42, (B, H), std=0.3) + np.float32(0.7)).astype(np.float32)
+    tau_q = tau.copy() if empty_q else (syn.normal_f32(seed, 43, (B, H), std=0.3) - np.float32(0.5)).astype(np.float32)
+    if not empty_q:
+        tau_q[-1, -1] = -np.inf
+    now = T - 1 if now is None else now
+    exp = orc.mask_kvzap(s, tau, now)[0].astype(np.int32)
+    mp = (T + 15) // 16
+    cap = B * H * mp
+    ref_a = orc.compact_dense(k, v, exp, now, 0, cap, mp)
+    ref_q = orc.compact_quant_dense(k, v, s, tau, tau_q, 0, cap, mp)
+    ref = orc.decode_attention_two_tier(q, ref_a, ref_q, now)
+    st = status_word()
+    kd, vd = dev_bf16(k), dev_bf16(v)
+    ca = kvp.PagedKV.allocate(B, H, d, cap, mp)
+    kvp.kvp_compact(kd, vd, dev_i32(exp), now, 0, ca, status=st)
+    cq = kvp.QuantPagedKV.allocate(B, H, d, cap, mp)
+    kvp.kvp_compact_quant(kd, vd, dev_f32(s), dev_f32(tau), dev_f32(tau_q), cq, status=st)
+    qd = dev_bf16(q)
+    out = kvp.kvp_decode_attn_two_tier(qd, ca, cq, now, grid_limit=pps, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return out, ref, (qd, ca, cq, now, st)
+
+
+@pytest.mark.parametrize("B,T,H,G,d,pps", [
+    (1, 512, 2, 2, 64, 0),
+    (2, 2000, 8, 4, 128, 0),     # Llama-3-8B GQA 4
+    (2, 2000, 8, 4, 128, 3),     # 3 CTAs: slices cross tiers and (b, h)
+    (1, 3000, 4, 1, 128, 5),
+    (2, 1500, 2, 8, 128, 0),
+    (3, 777, 3, 2, 64, 1),
+    (7, 3333, 5, 4, 128, 2),
+])
+def test_decode_attn_two_tier(kvp, B, T, H, G, d, pps):
+    out, ref, _ = _two_tier_case(kvp, B, T, H, G, d, pps=pps)
+    check_attention(out.cpu().numpy(), ref)
+
+
+def test_decode_attn_two_tier_visibility_and_empty_tier(kvp):
+    """Before any fp8 entry's start step the result is the bf16 tier's alone;
+    with an empty fp8 tier the two-tier kernel equals kvp_decode_attn bit for
+    bit (the same page list and partition)."""
+    B, T, H, G, d = 2, 1200, 4, 4, 128
+    out, ref, _ = _two_tier_case(kvp, B, T, H, G, d, now=100)   # now < 0 + window: no fp8 slot visible
+    check_attention(out.cpu().numpy(), ref)
+    out, ref, (qd, ca, cq, now, st) = _two_tier_case(kvp, B, T, H, G, d, empty_q=True)
+    assert int(cq.count.sum()) == 0
+    one = kvp.kvp_decode_attn(qd, ca, now, status=st)
+    torch.cuda.synchronize()
+    assert torch.equal(out, one)
+    check_attention(out.cpu().numpy(), ref)
 
 
 def test_decode_attn_keep_all_is_dense_and_window(kvp):
