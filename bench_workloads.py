@@ -388,8 +388,79 @@ def threshold(kvp, dev, peaks, seed=0, calls=10, reps=5):
             "points": points}
 
 
+def quant_tier(kvp, dev, peaks, seed=0, calls=10, reps=5):
+    """Quantize instead of drop on the Llama-3-8B-shaped layer (batch 16,
+    8,192 cached tokens, 32 q / 8 kv heads, head_dim 128): tau at each head's
+    75th-percentile score (bf16 tier: those entries plus the 128-token window),
+    and the entries below tau but at or above tau_q in the fp8 tier, for
+    tau_q at the 50th and 25th percentiles and at -inf (every entry kept in
+    some form). Times the fp8-tier compaction and the two-tier attention (CUDA
+    graphs of 10 calls) next to the one-tier attention over the bf16 tier
+    alone; bytes are the pages each call reads."""
+    B, T, H, Hq, d, W = 16, 8192, 8, 32, 128, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    K = _randn_bf16((B, T, H, d), g, dev)
+    V = _randn_bf16((B, T, H, d), g, dev)
+    q = _randn_bf16((B, Hq, d), g, dev)
+    s = torch.randn((B, T, H), generator=g, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    mp = (T + 15) // 16
+    ca = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp, device=dev)
+    cq = kvp.QuantPagedKV.allocate(B, H, d, B * H * mp, mp, device=dev)
+    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
+    tau = _tau_quantile(kvp, s, 0.75)
+    kvp.kvp_compact_masked(K, V, T - 1, 0, ca, mode=kvp.KVP_MASK_KVZAP, scores=s.view(B * T, H), tau=tau, window=W,
+                           status=st, workspace=ws_c)
+    torch.cuda.synchronize()
+    pages_a = int(((ca.count + 15) // 16).sum().item())
+    bytes_a = pages_a * 16 * (2 * d * 2 + 4) + B * Hq * d * (2 + 4)
+
+    def one_tier():
+        for _ in range(calls):
+            kvp.kvp_decode_attn(q, ca, T - 1, out=out, workspace=ws_a, status=st)
+
+    ms_one = _time(_graph(one_tier), reps=reps) / calls
+    points = [{"tau_q": "tau (no fp8 tier)", "bf16_kept_fraction": int(ca.count.sum()) / (B * H * T),
+               "fp8_fraction": 0.0, "attention_us": ms_one * 1e3, "attention_bytes": bytes_a,
+               "frac_of_hbm": bytes_a / (ms_one * 1e-3) / 1e9 / peaks[0]}]
+    for name, tq in (("50th percentile", _tau_quantile(kvp, s, 0.5)), ("25th percentile", _tau_quantile(kvp, s, 0.25)),
+                     ("-inf", torch.full((B, H), -math.inf, device=dev))):
+        def comp():
+            kvp.kvp_compact_quant(K, V, s, tau, tq, cq, window=W, status=st, workspace=ws_c)
+
+        ms_comp = _time(_graph(comp), reps=reps)
+        torch.cuda.synchronize()
+        assert st.item() == 0, kvp.status_string(st.item())
+        nq = int(cq.count.sum().item())
+        pages_q = int(((cq.count + 15) // 16).sum().item())
+        bytes_q = pages_q * (2 * 16 * d + 3 * 16 * 4)
+
+        def two_tier():
+            for _ in range(calls):
+                kvp.kvp_decode_attn_two_tier(q, ca, cq, T - 1, out=out, workspace=ws_a, status=st)
+
+        ms_two = _time(_graph(two_tier), reps=reps) / calls
+        assert st.item() == 0, kvp.status_string(st.item())
+        nbytes = bytes_a + bytes_q
+        comp_bytes = nq * 2 * d * 2 + nq * 2 * d + pages_q * 3 * 16 * 4 + B * T * H * 4
+        points.append({"tau_q": name, "bf16_kept_fraction": int(ca.count.sum()) / (B * H * T),
+                       "fp8_fraction": nq / (B * H * T), "fp8_pages": pages_q,
+                       "compact_quant_us": ms_comp * 1e3,
+                       "compact_quant_frac_of_hbm": comp_bytes / (ms_comp * 1e-3) / 1e9 / peaks[0],
+                       "attention_us": ms_two * 1e3, "attention_bytes": nbytes,
+                       "frac_of_hbm": nbytes / (ms_two * 1e-3) / 1e9 / peaks[0],
+                       "decode_tokens_per_s": B / (ms_two * 1e-3)})
+    return {"workload": "quant_tier: Llama-3-8B layer (batch 16 x 8192 tokens, 32 q / 8 kv heads, head_dim 128), "
+                        "tau at the 75th percentile, fp8 tier for tau_q <= s < tau; CUDA graphs of 10 calls",
+            "points": points}
+
+
 RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha,
-           "prune_sweep": prune_sweep, "threshold": threshold}
+           "prune_sweep": prune_sweep, "threshold": threshold,
+           "quant_tier": quant_tier}
 
 
 def run(name, kvp, dev, peaks):

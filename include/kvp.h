@@ -259,9 +259,10 @@ KVP_API kvp_status kvp_compact_masked(int mode, int batch, int n_kv_heads, int h
  *     tau_q <= tau this is the band that the bf16 tier (kvp_mask with tau)
  *     keeps only while it is in the window;
  *   - its K row and its V row are each stored as FP8 E4M3 codes with one fp32
- *     scale per row: scale = amax(|row|) / 448 (IEEE division), code =
- *     E4M3(x / scale) rounded to nearest even with saturation to +-448; an
- *     all-zero row has scale 0 and zero codes; value = code * scale;
+ *     scale per row: scale = amax(|row|) / 448 and inv = 448 / amax(|row|)
+ *     (IEEE divisions), code = E4M3(x * inv) (fp32 product, rounded to
+ *     nearest even, saturating to +-448); an all-zero row has scale 0 and
+ *     zero codes; value = code * scale;
  *   - it is visible to kvp_decode_attn_two_tier from step t + window on, the
  *     step its bf16 copy leaves the window, so at any step an entry is in one
  *     tier at most.

@@ -428,8 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
     // flight while the warp computes
     uint4 kr[C::RS], vr[C::RS];
     int32_t er[C::VL];
+    float ksu[C::VL];  // fp8 page: K scale of the row of each logit this lane holds after the reduction
     if (isq) {
-      // codes of the lane's 8 columns in .x/.y, the row's scale in .z
+      // codes of the lane's 8 columns in .x/.y, the V row's scale in vr[t].z
       const uint8_t* Kq = stage;
       const uint8_t* Vq = stage + C::QPAGE_BYTES;
       const int32_t* Mq = reinterpret_cast<const int32_t*>(stage + 2 * C::QPAGE_BYTES);
@@ -438,11 +439,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
         const int row = t * C::RPS + rowsel;
         const uint2 kc = reinterpret_cast<const uint2*>(Kq + row * D)[s];
         const uint2 vc = reinterpret_cast<const uint2*>(Vq + row * D)[s];
-        kr[t] = make_uint4(kc.x, kc.y, static_cast<uint32_t>(Mq[kPage + row]), 0u);
+        kr[t] = make_uint4(kc.x, kc.y, 0u, 0u);
         vr[t] = make_uint4(vc.x, vc.y, static_cast<uint32_t>(Mq[2 * kPage + row]), 0u);
       }
 #pragma unroll
-      for (int u = 0; u < C::VL; ++u) er[u] = Mq[((idx_base + u) % C::RS) * C::RPS + rowsel];
+      for (int u = 0; u < C::VL; ++u) {
+        const int r = ((idx_base + u) % C::RS) * C::RPS + rowsel;
+        er[u] = Mq[r];
+        ksu[u] = __int_as_float(Mq[kPage + r]);
+      }
     } else {
 #pragma unroll
       for (int t = 0; t < C::RS; ++t) {
@@ -473,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; e += 2) fma2(a0, a1, qf[i][e], qf[i][e + 1], kf[e], kf[e + 1]);
-        part[i * C::RS + t] = isq ? (a0 + a1) * __uint_as_float(kr[t].z) : a0 + a1;
+        part[i * C::RS + t] = a0 + a1;
       }
     }
     TransposeReduce<C::V, C::LPR / 2>::run(part, lane);
@@ -488,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
     for (int u = 0; u < C::VL; ++u) {
       const int r = ((idx_base + u) % C::RS) * C::RPS + rowsel;
       const bool valid = isq ? (slot0 + r < cnt_q) && (p.now >= er[u]) : (slot0 + r < cnt) && (p.now < er[u]);
-      x[u] = valid ? part[u] : -INFINITY;
+      x[u] = valid ? (isq ? part[u] * ksu[u] : part[u]) : -INFINITY;
       grow |= x[u] > mh + kLazyRescale;
     }
     if (__any_sync(0xffffffffu, grow)) {

@@ -562,9 +562,10 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
     cp_async_wait_all();
     __syncwarp();
     if constexpr (kQuant) {
-      // each row's E16 / 2 lanes: amax over the row, scale = amax / 448, then
-      // every element divided by the scale and rounded to E4M3 (saturating);
-      // the lanes of a row store 8 codes each, its first lane the scale
+      // each row's E16 / 2 lanes: amax over the row, scale = amax / 448 and
+      // inv = 448 / amax (IEEE divisions), every element times inv rounded to
+      // E4M3 (saturating); the lanes of a row store 8 codes each, its first
+      // lane the scale
       uint8_t* qbase = reinterpret_cast<uint8_t*>(dbase);
       for (int ib = 0; ib < nb; ib += EPI) {
         const int i = ib + sub;
@@ -582,12 +583,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
         for (int o = 1; o < E16 / 2; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float scale = __fdiv_rn(amax, 448.f);
         uint32_t packed[2] = {0u, 0u};
-        if (scale > 0.f) {
+        if (amax > 0.f) {
+          const float inv = __fdiv_rn(448.f, amax);
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             float2 pr;
-            pr.x = __fdiv_rn(f[e], scale);
-            pr.y = __fdiv_rn(f[e + 1], scale);
+            pr.x = __fmul_rn(f[e], inv);
+            pr.y = __fmul_rn(f[e + 1], inv);
             const uint32_t c2 = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3));
             packed[e >> 2] |= c2 << (16 * ((e >> 1) & 1));
           }

@@ -387,15 +387,17 @@ def e4m3_encode(v) -> np.ndarray:
 
 def quantize_rows(bits: np.ndarray):
     """bf16 rows [..., d] -> (codes uint8 [..., d], scale float32 [...]).
-    scale = amax(|row|) / 448 in float32 (round to nearest); each element is
-    divided by the scale in float32 and rounded to E4M3. An all-zero row has
-    scale 0 and codes 0."""
+    In float32 with round to nearest: scale = amax(|row|) / 448 (the
+    dequantization factor) and inv = 448 / amax(|row|); each element is
+    multiplied by inv and rounded to E4M3. An all-zero row has scale 0 and
+    codes 0."""
     x = widen_bf16(bits).astype(np.float32)
     amax = np.abs(x).max(axis=-1)
     scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
-    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
-    y = (x / safe[..., None]).astype(np.float32)
-    codes = np.where((scale > 0)[..., None], e4m3_encode(y), 0).astype(np.uint8)
+    nz = amax > 0
+    inv = (np.float32(E4M3_MAX) / np.where(nz, amax, np.float32(1.0))).astype(np.float32)
+    y = (x * inv[..., None]).astype(np.float32)
+    codes = np.where(nz[..., None], e4m3_encode(y), 0).astype(np.uint8)
     return codes, scale
 
 
