@@ -465,6 +465,34 @@ def compact_quant_dense(k_bits, v_bits, scores_bth, tau_bh, tau_q_bh, reserve, n
     return out
 
 
+def append_quant(qcache: QuantPagedCache, k_new_bits, v_new_bits, pos: int, score_bh, tau_bh, tau_q_bh,
+                 window: int = WINDOW):
+    """Decode step for the fp8 tier: the token at `pos` (k/v [B, H, d]) goes
+    into slot count[b, h] of its (b, h)'s fp8 pages iff tau_q <= score < tau,
+    quantized like the compaction's rows, with start = pos + window; raises if
+    the reserved slots are used up."""
+    B, H = qcache.count.shape
+    sel = (np.asarray(score_bh) >= np.asarray(tau_q_bh)) & (np.asarray(score_bh) < np.asarray(tau_bh))
+    for b in range(B):
+        for h in range(H):
+            if not sel[b, h]:
+                continue
+            j = int(qcache.count[b, h])
+            p = j // PAGE
+            if p >= qcache.page_table.shape[2] or qcache.page_table[b, h, p] < 0:
+                raise CapacityError(f"(b={b}, h={h}) has no free fp8 slot")
+            page = qcache.page_table[b, h, p]
+            kc, ks = quantize_rows(k_new_bits[b, h][None])
+            vc, vs = quantize_rows(v_new_bits[b, h][None])
+            qcache.kq_pool[page, j % PAGE] = kc[0]
+            qcache.vq_pool[page, j % PAGE] = vc[0]
+            qcache.kscale[page, j % PAGE] = ks[0]
+            qcache.vscale[page, j % PAGE] = vs[0]
+            qcache.start_pool[page, j % PAGE] = pos + window
+            qcache.remap[b, h, j] = pos
+            qcache.count[b, h] = j + 1
+
+
 def decode_attention_two_tier(q_bits, cache: PagedCache, qcache: QuantPagedCache, now: int,
                               scale: float | None = None) -> np.ndarray:
     """Attention over the union of the bf16 tier's slots present at `now`

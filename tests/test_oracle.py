@@ -569,3 +569,39 @@ def test_two_tier_attention_reduces_to_known_cases():
     cq_e = orc.compact_quant_dense(k[:, :early + 1], v[:, :early + 1], s[:, :early + 1], inf, -inf, 0, B * H * mp, mp)
     np.testing.assert_allclose(orc.decode_attention_two_tier(q, ca_e, cq_e, early),
                                orc.window_attention(q, k, v, early), rtol=0, atol=1e-6)
+
+
+def test_quant_append_equals_one_compaction():
+    """Compacting positions [0, T0) into the fp8 tier and appending T0..T-1
+    one at a time gives the same tier (codes, scales, starts, remap, count)
+    as one compaction of [0, T) with the same reserve budget."""
+    rng = np.random.default_rng(12)
+    B, T0, T, H, d = 2, 90, 140, 3, 64
+    k = syn.f32_to_bf16_bits(rng.standard_normal((B, T, H, d)).astype(np.float32))
+    v = syn.f32_to_bf16_bits(rng.standard_normal((B, T, H, d)).astype(np.float32))
+    s = rng.standard_normal((B, T, H))
+    tau = np.full((B, H), 0.6)
+    tq = np.full((B, H), -0.4)
+    mp = 16
+    step = orc.compact_quant_dense(k[:, :T0], v[:, :T0], s[:, :T0], tau, tq, 64, B * H * mp, mp)
+    for t in range(T0, T):
+        orc.append_quant(step, k[:, t], v[:, t], t, s[:, t], tau, tq)
+    once = orc.compact_quant_dense(k, v, s, tau, tq, 64, B * H * mp, mp)
+    np.testing.assert_array_equal(step.count, once.count)
+    for b in range(B):
+        for h in range(H):
+            n = int(once.count[b, h])
+            np.testing.assert_array_equal(step.remap[b, h, :n], once.remap[b, h, :n])
+            p1, r1 = step.slot_rows(b, h, np.arange(n))
+            p2, r2 = once.slot_rows(b, h, np.arange(n))
+            np.testing.assert_array_equal(step.kq_pool[p1, r1], once.kq_pool[p2, r2])
+            np.testing.assert_array_equal(step.vq_pool[p1, r1], once.vq_pool[p2, r2])
+            np.testing.assert_array_equal(step.kscale[p1, r1], once.kscale[p2, r2])
+            np.testing.assert_array_equal(step.start_pool[p1, r1], once.start_pool[p2, r2])
+    # the reserve runs out: an error, nothing written
+    tight = orc.compact_quant_dense(k[:, :T0], v[:, :T0], s[:, :T0], tau, np.full((B, H), -np.inf), 0, B * H * mp, mp)
+    full = tight.count.copy()
+    with pytest.raises(orc.CapacityError):
+        for t in range(T0, T):
+            orc.append_quant(tight, k[:, t], v[:, t], t, s[:, t], tau, np.full((B, H), -np.inf))
+    assert (tight.count >= full).all()
