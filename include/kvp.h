@@ -288,6 +288,23 @@ KVP_API kvp_status kvp_compact_quant(int batch, int n_kv_heads, int head_dim, in
                        int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
+/* kvp_append_quant - the decode-time side of the fp8 tier: the token at
+ * position `pos` (k_new, v_new device bf16 [B, H, head_dim], 16-byte aligned)
+ * goes into slot count[b, h] of its (b, h)'s fp8 pages iff
+ * tau_q[b, h] <= score[b, h] < tau[b, h] (device fp32 [B, H]; the score the
+ * token got for the bf16 tier's kvp_append), quantized exactly as
+ * kvp_compact_quant does, with start = pos + window; remap and count grow by
+ * one. The slot must be one of the pages the compaction reserved, else
+ * KVP_ERR_CAPACITY is recorded in `status` and that (b, h) is left as it is.
+ * Pools and tables: as kvp_compact_quant writes them.
+ */
+KVP_API kvp_status kvp_append_quant(int batch, int n_kv_heads, int head_dim, int pos,
+                       const void* k_new, const void* v_new,
+                       const float* score, const float* tau, const float* tau_q, int window,
+                       void* kq_pool, void* vq_pool, int32_t* meta_pool, int n_pages_cap,
+                       const int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                       int32_t* status, void* stream);
+
 /* kvp_compact_noalloc - kvp_compact for callers that cannot allocate device
  * memory. No page describes this entry point; it is a convenience of this
  * library. Some hosts hand a library only the tensors of the operation and no

@@ -83,6 +83,7 @@ _SIGS = {
                                _P, _P, _P, _S, _P, _P]),
     "kvp_append": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
                         _P, _P]),
+    "kvp_append_quant": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P]),
     "kvp_decode_attn_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "kvp_decode_attn": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _I, _P, _S, _P, _P]),
     "kvp_decode_attn_two_tier": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _P, _I, _P,
@@ -449,6 +450,21 @@ def kvp_append(cache: PagedKV, k_new, v_new, pos, *, mode, score=None, tau=None,
                            _ptr(cache.page_table, torch.int32), cache.max_pages, _ptr(cache.remap, torch.int32),
                            _ptr(cache.count, torch.int32), _ptr(status, torch.int32, "status"), _stream(stream))
     _check("kvp_append", code)
+
+
+def kvp_append_quant(qcache: QuantPagedKV, k_new, v_new, pos, *, score, tau, tau_q, window=WINDOW, status,
+                     stream=None):
+    """Writes the token at position `pos` (k_new, v_new [B, H, d]) into the fp8 tier of every (b, h) whose
+    score falls in [tau_q, tau)."""
+    B, H, d = k_new.shape
+    code = _lib.kvp_append_quant(B, H, d, pos, _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
+                                 _ptr(score, torch.float32, "score"), _ptr(tau, torch.float32, "tau"),
+                                 _ptr(tau_q, torch.float32, "tau_q"), window, _ptr(qcache.kq_pool, torch.uint8),
+                                 _ptr(qcache.vq_pool, torch.uint8), _ptr(qcache.meta_pool, torch.int32),
+                                 qcache.n_pages_cap, _ptr(qcache.page_table, torch.int32), qcache.max_pages,
+                                 _ptr(qcache.remap, torch.int32), _ptr(qcache.count, torch.int32),
+                                 _ptr(status, torch.int32, "status"), _stream(stream))
+    _check("kvp_append_quant", code)
 
 
 # --------------------------------------------------------------------------- attention

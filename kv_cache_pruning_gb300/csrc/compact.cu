@@ -1,4 +1,5 @@
-// kvp_mask, kvp_compact, kvp_compact_masked, kvp_compact_quant, kvp_compact_paged, kvp_append.
+// kvp_mask, kvp_compact, kvp_compact_masked, kvp_compact_quant, kvp_compact_paged, kvp_append,
+// kvp_append_quant.
 //
 // Rules (KVzap summary "실제 적용"; DMS article "지연 삭제 (Delayed Eviction)"):
 // an entry gets the first step at which it is gone,
@@ -660,6 +661,84 @@ __global__ void __launch_bounds__(256) append_kernel(int mode, int BH, int pos, 
   }
 }
 
+// Decode-time append into the fp8 tier: one warp per (b, h); the token goes
+// in iff tau_q <= score < tau, its K and V rows quantized like the copy
+// pass's (each lane takes D / 32 elements, the row's amax is reduced over the
+// warp), start = pos + window.
+template <int D>
+__global__ void __launch_bounds__(256) append_quant_kernel(int BH, int pos, const uint16_t* __restrict__ k_new,
+                                                           const uint16_t* __restrict__ v_new,
+                                                           const float* __restrict__ score,
+                                                           const float* __restrict__ tau,
+                                                           const float* __restrict__ tau_q, int window,
+                                                           uint8_t* __restrict__ kq_pool, uint8_t* __restrict__ vq_pool,
+                                                           int32_t* __restrict__ meta_pool, int n_pages_cap,
+                                                           const int32_t* __restrict__ page_table, int max_pages,
+                                                           int32_t* __restrict__ remap, int32_t* __restrict__ count,
+                                                           int32_t* __restrict__ status) {
+  constexpr int EPL = D / 32;  // elements a lane quantizes (4 or 2)
+  const int bh = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (bh >= BH) return;
+  const float sc = score[bh];
+  if (!(sc >= tau_q[bh] && sc < tau[bh])) return;  // not in the fp8 tier (the same for the whole warp)
+  const int j = count[bh];
+  if (j < 0) {
+    if (lane == 0) record_error(status, KVP_ERR_BOUNDS);
+    return;
+  }
+  const int p = j >> 4;
+  const int page = (p < max_pages) ? page_table[static_cast<int64_t>(bh) * max_pages + p] : -1;
+  if (page < 0) {
+    if (lane == 0) record_error(status, KVP_ERR_CAPACITY);
+    return;
+  }
+  if (page >= n_pages_cap) {
+    if (lane == 0) record_error(status, KVP_ERR_BOUNDS);
+    return;
+  }
+  const int64_t row = static_cast<int64_t>(page) * kPage + (j & 15);
+  int32_t* meta = meta_pool + static_cast<int64_t>(page) * kQuantMetaWords;
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const uint16_t* src = (w ? v_new : k_new) + static_cast<int64_t>(bh) * D + lane * EPL;
+    float f[EPL];
+    if constexpr (EPL == 4) {
+      const uint2 x = *reinterpret_cast<const uint2*>(src);
+      f[0] = bf16_lo(x.x); f[1] = bf16_hi(x.x); f[2] = bf16_lo(x.y); f[3] = bf16_hi(x.y);
+    } else {
+      const uint32_t x = *reinterpret_cast<const uint32_t*>(src);
+      f[0] = bf16_lo(x); f[1] = bf16_hi(x);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = __fdiv_rn(amax, 448.f);
+    uint32_t packed = 0u;
+    if (amax > 0.f) {
+      const float inv = __fdiv_rn(448.f, amax);
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        float2 pr;
+        pr.x = __fmul_rn(f[e], inv);
+        pr.y = __fmul_rn(f[e + 1], inv);
+        packed |= static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3)) << (8 * e);
+      }
+    }
+    uint8_t* dst = (w ? vq_pool : kq_pool) + row * D + lane * EPL;
+    if constexpr (EPL == 4) *reinterpret_cast<uint32_t*>(dst) = packed;
+    else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
+    if (lane == 0) reinterpret_cast<float*>(meta)[(1 + w) * kPage + (j & 15)] = scale;
+  }
+  if (lane == 0) {
+    meta[j & 15] = pos + window;
+    remap[static_cast<int64_t>(bh) * max_pages * kPage + j] = pos;
+    count[bh] = j + 1;
+  }
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 template <class Src>
@@ -922,6 +1001,37 @@ extern "C" kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_d
     append_kernel<64><<<blocks, 256, 0, st>>>(mode, BH, pos, kn, vn, score, tau, flag_step, window, delay, kp, vp,
                                               expire_pool, n_pages_cap, page_table, max_pages, remap, count,
                                               status);
+  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+extern "C" kvp_status kvp_append_quant(int batch, int n_kv_heads, int head_dim, int pos, const void* k_new,
+                                       const void* v_new, const float* score, const float* tau, const float* tau_q,
+                                       int window, void* kq_pool, void* vq_pool, int32_t* meta_pool, int n_pages_cap,
+                                       const int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                                       int32_t* status, void* stream) {
+  if (batch <= 0 || n_kv_heads <= 0 || pos < 0 || window < 0 || max_pages < 0 || n_pages_cap < 0)
+    return KVP_ERR_INVALID;
+  if (head_dim != 64 && head_dim != 128) return KVP_ERR_UNSUPPORTED;
+  if (k_new == nullptr || v_new == nullptr || score == nullptr || tau == nullptr || tau_q == nullptr ||
+      kq_pool == nullptr || vq_pool == nullptr || meta_pool == nullptr || page_table == nullptr || remap == nullptr ||
+      count == nullptr || status == nullptr)
+    return KVP_ERR_INVALID;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kq_pool) || !aligned16(vq_pool) || !aligned16(meta_pool))
+    return KVP_ERR_ALIGN;
+  if (static_cast<int64_t>(pos) + window >= kNever) return KVP_ERR_INVALID;
+  const int BH = batch * n_kv_heads;
+  const int blocks = (BH + 7) / 8;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto* kn = static_cast<const uint16_t*>(k_new);
+  auto* vn = static_cast<const uint16_t*>(v_new);
+  auto* kq = static_cast<uint8_t*>(kq_pool);
+  auto* vq = static_cast<uint8_t*>(vq_pool);
+  if (head_dim == 128)
+    append_quant_kernel<128><<<blocks, 256, 0, st>>>(BH, pos, kn, vn, score, tau, tau_q, window, kq, vq, meta_pool,
+                                                     n_pages_cap, page_table, max_pages, remap, count, status);
+  else
+    append_quant_kernel<64><<<blocks, 256, 0, st>>>(BH, pos, kn, vn, score, tau, tau_q, window, kq, vq, meta_pool,
+                                                    n_pages_cap, page_table, max_pages, remap, count, status);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 

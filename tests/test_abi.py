@@ -25,7 +25,8 @@ def lib():
 
 def test_header_declares_the_path():
     names = set(_declared())
-    for n in ["kvp_score", "kvp_mask", "kvp_compact", "kvp_compact_masked", "kvp_compact_quant", "kvp_compact_paged", "kvp_threshold", "kvp_append", "kvp_decode_attn",
+    for n in ["kvp_score", "kvp_mask", "kvp_compact", "kvp_compact_masked", "kvp_compact_quant", "kvp_append_quant", "kvp_compact_paged",
+              "kvp_threshold", "kvp_append", "kvp_decode_attn",
               "kvp_score_workspace_bytes", "kvp_compact_workspace_bytes", "kvp_decode_attn_workspace_bytes",
               "kvp_status_string", "kvp_version"]:
         assert n in names, n
@@ -128,6 +129,23 @@ def test_compact_quant_host_checks():
     assert call(status=None) == k.KVP_ERR_INVALID
     assert call(hd=96) == k.KVP_ERR_UNSUPPORTED
     assert call(kq=8) == k.KVP_ERR_ALIGN
+
+
+def test_append_quant_host_checks():
+    import kv_cache_pruning_gb300 as k
+    L = k.library()
+
+    def call(hd=128, pos=5, kn=16, tau_q=16, window=128, status=16):
+        return L.kvp_append_quant(1, 1, hd, pos, kn, 16, 16, 16, tau_q, window, 16, 16, 16, 1, 16, 1, 16, 16,
+                                  status, None)
+
+    assert call(tau_q=None) == k.KVP_ERR_INVALID
+    assert call(pos=-1) == k.KVP_ERR_INVALID
+    assert call(window=-2) == k.KVP_ERR_INVALID
+    assert call(status=None) == k.KVP_ERR_INVALID
+    assert call(hd=32) == k.KVP_ERR_UNSUPPORTED
+    assert call(kn=8) == k.KVP_ERR_ALIGN
+    assert call(pos=2**31 - 100) == k.KVP_ERR_INVALID       # start would overflow
 
 
 def test_threshold_host_checks():

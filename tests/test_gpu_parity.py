@@ -446,6 +446,94 @@ def test_compact_quant_special_rows(kvp):
     _compare_qcache(dst, ref)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_append_quant_bit_exact(kvp, d):
+    """fp8-tier compaction of [0, T0), then appends of T0..T-1: bit-identical
+    to the oracle at every slot; an exhausted reserve records
+    KVP_ERR_CAPACITY and leaves that (b, h) unchanged."""
+    B, T0, T, H = 3, 700, 780, 4
+    k, v = syn.kv_inputs(19, B, T, H, d)
+    s = syn.normal_f32(19, 51, (B, T, H))
+    tau = np.full((B, H), 0.6, np.float32)
+    tau_q = np.full((B, H), -0.4, np.float32)
+    tau_q[0, 0] = -np.inf                 # every token below tau: this (b, h)'s reserve runs out first
+    reserve, mp = 48, (T + 48 + 15) // 16
+    cap = B * H * mp
+    ref = orc.compact_quant_dense(k[:, :T0], v[:, :T0], s[:, :T0], tau, tau_q, reserve, cap, mp)
+    st = status_word()
+    cq = kvp.QuantPagedKV.allocate(B, H, d, cap, mp)
+    kvp.kvp_compact_quant(dev_bf16(k[:, :T0].copy()), dev_bf16(v[:, :T0].copy()), dev_f32(s[:, :T0].copy()),
+                          dev_f32(tau), dev_f32(tau_q), cq, reserve=reserve, status=st)
+    kd, vd, sd = dev_bf16(k), dev_bf16(v), dev_f32(s)
+    tq_d, tau_d = dev_f32(tau_q), dev_f32(tau)
+    t_fail = None
+    for t in range(T0, T):
+        try:
+            orc.append_quant(ref, k[:, t], v[:, t], t, s[:, t], tau, tau_q)
+        except orc.CapacityError:
+            t_fail = t
+            break
+        kvp.kvp_append_quant(cq, kd[:, t].contiguous(), vd[:, t].contiguous(), t, score=sd[:, t].contiguous(),
+                             tau=tau_d, tau_q=tq_d, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_qcache(cq, ref)
+    assert t_fail is not None, "the test expects the reserve of (0, 0) to run out"
+    before = cq.count.clone()
+    kvp.kvp_append_quant(cq, kd[:, t_fail].contiguous(), vd[:, t_fail].contiguous(), t_fail,
+                         score=sd[:, t_fail].contiguous(), tau=tau_d, tau_q=tq_d, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == kvp.KVP_ERR_CAPACITY
+    assert int(cq.count[0, 0]) == int(before[0, 0])
+
+
+def test_step_in_cuda_graph_matches_eager(kvp):
+    """Score, fused mask + compaction and attention captured as one CUDA graph
+    (the copy pass and the attention launched as programmatic dependents)
+    replay to the same bits as the eager calls."""
+    B, T, H, G, d, D = 2, 3000, 4, 4, 128, 256
+    x, w = syn.linear_inputs(23, B * T, D, H)
+    k, v = syn.kv_inputs(23, B, T, H, d)
+    q = syn.q_inputs(23, B, H * G, d)
+    xd, wd, kd, vd, qd = dev_bf16(x), torch.from_numpy(w).cuda(), dev_bf16(k), dev_bf16(v), dev_bf16(q)
+    ws_split = kvp.kvp_score_split_weight(wd)
+    scores = torch.empty(B * T, H, dtype=torch.float32, device="cuda")
+    st = status_word()
+    kvp.kvp_score(xd, ws_split, scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H, out=scores, status=st)
+    tau = kvp.kvp_threshold(scores.view(B, T, H), 0.75)
+    mp = (T + 15) // 16
+    outs = []
+    for use_graph in (False, True):
+        cache = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp)
+        out = torch.empty(B, H * G, d, dtype=torch.float32, device="cuda")
+        ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device="cuda")
+        ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, H * G, H, d), dtype=torch.uint8, device="cuda")
+
+        def step():
+            kvp.kvp_score(xd, ws_split, scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H, out=scores, status=st)
+            kvp.kvp_compact_masked(kd, vd, T - 1, 0, cache, mode=kvp.KVP_MASK_KVZAP, scores=scores, tau=tau,
+                                   status=st, workspace=ws_c)
+            kvp.kvp_decode_attn(qd, cache, T - 1, out=out, workspace=ws_a, status=st)
+
+        if use_graph:
+            step()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step()
+            cache.count.zero_()
+            out.zero_()
+            for _ in range(3):
+                g.replay()
+        else:
+            step()
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        outs.append((out.clone(), cache.count.clone(), cache.page_table.clone()))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+
+
 def _dms_stream(B, T, H, d, delay, window, seed):
     k, v = syn.kv_inputs(seed, B, T, H, d)
     pos = np.arange(T)[None, None, :]
