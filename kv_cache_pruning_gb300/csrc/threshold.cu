@@ -64,7 +64,10 @@ ThrWs thr_carve(void* ws, int B, int H) {
 
 // VEC = 4 reads four adjacent heads of a row as one 16-byte load (H a
 // multiple of 4, scores 16-byte aligned); VEC = 1 reads one score at a time.
-template <int VEC>
+// kFixed (VEC = 4, and the loads of a row divide the block): every thread
+// keeps the same four heads for the whole chunk, with their prefixes in
+// registers, and steps down the rows.
+template <int VEC, bool kFixed>
 __global__ void __launch_bounds__(kThrThreads, 4) select_pass(int pass, int H, int n, int rows, uint32_t k0,
                                                            const float* __restrict__ scores, ThrWs ws,
                                                            float* __restrict__ tau) {
@@ -86,6 +89,35 @@ __global__ void __launch_bounds__(kThrThreads, 4) select_pass(int pass, int H, i
   const int hv = hn / VEC;          // loads per row
   const int nv = (t1 - t0) * hv;    // loads in the chunk
   const float* base = scores + (static_cast<int64_t>(b) * n + t0) * H + h0;
+  if constexpr (kFixed) {
+    const int jc = threadIdx.x % hv;  // this thread's heads: 4 jc .. 4 jc + 3
+    const int dr = kThrThreads / hv;  // rows between two of its loads
+    const int nrows = t1 - t0;
+    uint32_t pre[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) pre[c] = pre_s[4 * jc + c];
+    uint32_t* hj = hist + 4 * jc * kBins;
+    for (int r0 = threadIdx.x / hv; r0 < nrows; r0 += dr * kThrUnroll) {
+      float4 x[kThrUnroll];
+#pragma unroll
+      for (int u = 0; u < kThrUnroll; ++u) {  // all loads first
+        const int r = r0 + u * dr;
+        x[u] = r < nrows ? __ldg(reinterpret_cast<const float4*>(base + static_cast<int64_t>(r) * H + 4 * jc))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kThrUnroll; ++u) {
+        if (r0 + u * dr < nrows) {
+          const float f[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t key = order_key(f[c]);
+            if (pass == 0 || (key >> (shift + 8)) == pre[c]) atomicAdd(&hj[c * kBins + ((key >> shift) & 0xffu)], 1u);
+          }
+        }
+      }
+    }
+  } else {
   // load e = r * hv + j (row t0 + r, heads h0 + VEC j ..); (r, j) of this
   // thread's next load is advanced by kThrThreads loads without a division
   const int dr = kThrThreads / hv, dj = kThrThreads - dr * hv;
@@ -126,6 +158,7 @@ __global__ void __launch_bounds__(kThrThreads, 4) select_pass(int pass, int H, i
         }
       }
     }
+  }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < hn * kBins; i += kThrThreads) {
@@ -233,11 +266,17 @@ extern "C" kvp_status kvp_threshold(int batch, int n_kv_heads, int n_pos, const 
     return KVP_ERR_CUDA;
   const dim3 grid(chunks, batch, G);
   const bool vec4 = n_kv_heads % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15u) == 0;
+  // fixed heads per thread when every head group's row of float4 loads (8
+  // for a full group, (H mod 32) / 4 for the last) divides the block
+  const int hv_last = (n_kv_heads - (G - 1) * kHeadsPerCta) / 4;
+  const bool fixed = vec4 && kThrThreads % (kHeadsPerCta / 4) == 0 && hv_last > 0 && kThrThreads % hv_last == 0;
   for (int p = 0; p < kPasses; ++p) {
-    if (vec4)
-      select_pass<4><<<grid, kThrThreads, 0, st>>>(p, n_kv_heads, n_pos, rows, k0, scores, ws, tau);
+    if (fixed)
+      select_pass<4, true><<<grid, kThrThreads, 0, st>>>(p, n_kv_heads, n_pos, rows, k0, scores, ws, tau);
+    else if (vec4)
+      select_pass<4, false><<<grid, kThrThreads, 0, st>>>(p, n_kv_heads, n_pos, rows, k0, scores, ws, tau);
     else
-      select_pass<1><<<grid, kThrThreads, 0, st>>>(p, n_kv_heads, n_pos, rows, k0, scores, ws, tau);
+      select_pass<1, false><<<grid, kThrThreads, 0, st>>>(p, n_kv_heads, n_pos, rows, k0, scores, ws, tau);
   }
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }

@@ -150,6 +150,8 @@ def _check_tau(t_gpu, t_ref):
     (4, 777, 3, 0.0),
     (4, 777, 3, 1.0),
     (1, 131072, 64, 0.6),      # the 65B-MHA layer: one b, 64 heads, long rows
+    (2, 700, 12, 0.4),         # 16-byte loads whose row of 3 does not divide the block
+    (2, 900, 44, 0.7),         # second head group of 12
 ])
 def test_threshold_matches_oracle(kvp, B, T, H, q):
     s = syn.normal_f32(4, 40, (B, T, H))
