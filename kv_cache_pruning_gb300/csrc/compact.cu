@@ -861,10 +861,11 @@ extern "C" kvp_status kvp_compact_masked(int mode, int batch, int n_kv_heads, in
                                          int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
                                          void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
   if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0 || window < 0 || delay < 0) return KVP_ERR_INVALID;
+  // the per-position inputs may be NULL when there are no positions; tau is read per (b, h)
   if (mode == KVP_MASK_KVZAP) {
-    if (flag_step != nullptr || scores == nullptr || tau == nullptr) return KVP_ERR_INVALID;
+    if (flag_step != nullptr || tau == nullptr || (n_pos > 0 && scores == nullptr)) return KVP_ERR_INVALID;
   } else if (mode == KVP_MASK_DMS) {
-    if (scores != nullptr || tau != nullptr || flag_step == nullptr) return KVP_ERR_INVALID;
+    if (scores != nullptr || tau != nullptr || (n_pos > 0 && flag_step == nullptr)) return KVP_ERR_INVALID;
   } else {
     return KVP_ERR_INVALID;
   }
@@ -903,7 +904,7 @@ extern "C" kvp_status kvp_compact_quant(int batch, int n_kv_heads, int head_dim,
                                         int32_t* count, void* workspace, size_t workspace_bytes, int32_t* status,
                                         void* stream) {
   if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0 || window < 0) return KVP_ERR_INVALID;
-  if (scores == nullptr || tau == nullptr || tau_q == nullptr) return KVP_ERR_INVALID;
+  if (tau == nullptr || tau_q == nullptr || (n_pos > 0 && scores == nullptr)) return KVP_ERR_INVALID;
   if (static_cast<int64_t>(n_pos) + window >= kNever) return KVP_ERR_INVALID;
   kvp_status s = check_dst(head_dim, reserve, kq_pool, vq_pool, meta_pool, n_pages_cap, page_table, max_pages,
                            remap, count, status);

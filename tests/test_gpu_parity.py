@@ -351,6 +351,32 @@ def test_compact_masked_dms_bit_exact(kvp, delay, window, now_back):
     _compare_cache(dst, ref)
 
 
+def test_compact_masked_and_quant_empty_source(kvp):
+    """No positions at all: every (b, h) gets its reserve's pages (zeroed),
+    count 0, remap -1; the fp8 tier likewise."""
+    B, T, H, d, reserve = 2, 0, 3, 64, 20
+    k = np.zeros((B, T, H, d), np.uint16)
+    s = np.zeros((B, T, H), np.float32)
+    tau = np.zeros((B, H), np.float32)
+    mp = 4
+    ref = orc.compact_dense(k, k, np.zeros((B, H, T), np.int32), 0, reserve, B * H * mp, mp)
+    refq = orc.compact_quant_dense(k, k, s, tau, tau - 1, reserve, B * H * mp, mp)
+    st = status_word()
+    kd = torch.zeros((B, T, H, d), dtype=torch.bfloat16, device="cuda")
+    sd = torch.zeros((B * T, H), dtype=torch.float32, device="cuda")
+    c = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp)
+    c.k_pool.fill_(1.0)      # the reserved rows must come back zeroed
+    kvp.kvp_compact_masked(kd, kd, 0, reserve, c, mode=kvp.KVP_MASK_KVZAP, scores=sd, tau=dev_f32(tau), status=st)
+    cq = kvp.QuantPagedKV.allocate(B, H, d, B * H * mp, mp)
+    cq.kq_pool.fill_(7)
+    kvp.kvp_compact_quant(kd, kd, sd, dev_f32(tau), dev_f32(tau - 1), cq, reserve=reserve, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_cache(c, ref)
+    _compare_qcache(cq, refq)
+    assert ref.pages_used == B * H * 2
+
+
 def test_compact_masked_capacity_status(kvp):
     B, T, H, d = 1, 256, 2, 64
     k, v = syn.kv_inputs(6, B, T, H, d)
