@@ -458,9 +458,80 @@ def quant_tier(kvp, dev, peaks, seed=0, calls=10, reps=5):
             "points": points}
 
 
+def quant_decode(kvp, dev, peaks, seed=0, steps=64, reps=3):
+    """A decode loop over both tiers on the Llama-3-8B-shaped layer (batch
+    16, 8,192-token prompt, 32 q / 8 kv heads, head_dim 128): tau at each
+    head's 75th-percentile prompt score, tau_q at the 25th, 128-token window.
+    Each step appends the new token to the bf16 tier (kvp_append) and, when
+    its score is in [tau_q, tau), to the fp8 tier (kvp_append_quant), then runs
+    the two-tier attention; the 64 steps are one CUDA graph. The one-tier loop
+    (the same steps without the fp8 tier) is timed beside it."""
+    B, T, H, Hq, d, W = 16, 8192, 8, 32, 128, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    K = _randn_bf16((B, T + steps, H, d), g, dev)
+    V = _randn_bf16((B, T + steps, H, d), g, dev)
+    q = _randn_bf16((steps, B, Hq, d), g, dev)
+    s = torch.randn((B, T + steps, H), generator=g, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    reserve = steps
+    mp = (T + reserve + 15) // 16
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
+    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+    sp = s[:, :T].contiguous()
+    tau = _tau_quantile(kvp, sp, 0.75)
+    tau_q = _tau_quantile(kvp, sp, 0.25)
+    Kp, Vp = K[:, :T], V[:, :T]
+    k_new = [K[:, T + i].contiguous() for i in range(steps)]
+    v_new = [V[:, T + i].contiguous() for i in range(steps)]
+    s_new = [s[:, T + i].contiguous() for i in range(steps)]
+    res = {}
+    for tiers in (1, 2):
+        ca = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp, device=dev)
+        cq = kvp.QuantPagedKV.allocate(B, H, d, B * H * mp, mp, device=dev)
+
+        def prefill():
+            kvp.kvp_compact_masked(Kp, Vp, T - 1, reserve, ca, mode=kvp.KVP_MASK_KVZAP, scores=sp, tau=tau, window=W,
+                                   status=st, workspace=ws_c)
+            if tiers == 2:
+                kvp.kvp_compact_quant(Kp, Vp, sp, tau, tau_q, cq, reserve=reserve, window=W, status=st,
+                                      workspace=ws_c)
+
+        def loop():
+            for i in range(steps):
+                t = T + i
+                kvp.kvp_append(ca, k_new[i], v_new[i], t, mode=kvp.KVP_MASK_KVZAP, score=s_new[i], tau=tau,
+                               window=W, status=st)
+                if tiers == 2:
+                    kvp.kvp_append_quant(cq, k_new[i], v_new[i], t, score=s_new[i], tau=tau, tau_q=tau_q, window=W,
+                                         status=st)
+                    kvp.kvp_decode_attn_two_tier(q[i], ca, cq, t, out=out, workspace=ws_a, status=st)
+                else:
+                    kvp.kvp_decode_attn(q[i], ca, t, out=out, workspace=ws_a, status=st)
+
+        prefill()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            loop()
+        best = 1e30
+        for _ in range(reps):
+            prefill()               # the loop appends: start every replay from the prompt's caches
+            torch.cuda.synchronize()
+            best = min(best, _time(gr.replay))
+        assert st.item() == 0, kvp.status_string(st.item())
+        res[tiers] = {"ms_per_step": best / steps, "decode_tokens_per_s": B / (best / steps * 1e-3),
+                      "bf16_slots": int(ca.count.sum().item()), "fp8_slots": int(cq.count.sum().item())}
+    return {"workload": "quant_decode: Llama-3-8B layer, batch 16, 8192-token prompt + 64 decode steps, "
+                        "tau 75th / tau_q 25th percentile, window 128; each step = append (both tiers) + attention; "
+                        "the 64 steps are one CUDA graph",
+            "one_tier": res[1], "two_tier": res[2]}
+
+
 RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha,
            "prune_sweep": prune_sweep, "threshold": threshold,
-           "quant_tier": quant_tier}
+           "quant_tier": quant_tier, "quant_decode": quant_decode}
 
 
 def run(name, kvp, dev, peaks):

@@ -768,6 +768,50 @@ def test_decode_attn_two_tier_visibility_and_empty_tier(kvp):
     check_attention(out.cpu().numpy(), ref)
 
 
+def test_two_tier_decode_loop(kvp):
+    """Prefill both tiers at step T0 - 1, then decode steps T0..T-1: each new
+    token is appended to the bf16 tier (kvp_append, KVzap rule) and, when its
+    score falls in [tau_q, tau), to the fp8 tier (kvp_append_quant); every
+    step's two-tier attention is checked against the oracle's. Window 32, so
+    that entries cross from the bf16 tier to the fp8 tier during the loop."""
+    B, T0, T, H, G, d, W = 2, 600, 680, 4, 4, 128, 32
+    k, v = syn.kv_inputs(29, B, T, H, d)
+    q_all = syn.normal_f32(29, 71, (T - T0, B, H * G, d))
+    s = syn.normal_f32(29, 72, (B, T, H))
+    tau = np.full((B, H), 0.5, np.float32)
+    tau_q = np.full((B, H), -0.5, np.float32)
+    now0 = T0 - 1
+    reserve, mp = 96, (T + 96 + 15) // 16
+    cap = B * H * mp
+    exp0 = orc.mask_kvzap(s[:, :T0], tau, now0, window=W)[0].astype(np.int32)
+    ref_a = orc.compact_dense(k[:, :T0], v[:, :T0], exp0, now0, reserve, cap, mp)
+    ref_q = orc.compact_quant_dense(k[:, :T0], v[:, :T0], s[:, :T0], tau, tau_q, reserve, cap, mp, window=W)
+    st = status_word()
+    ca = kvp.PagedKV.allocate(B, H, d, cap, mp)
+    cq = kvp.QuantPagedKV.allocate(B, H, d, cap, mp)
+    kvp.kvp_compact(dev_bf16(k[:, :T0].copy()), dev_bf16(v[:, :T0].copy()), dev_i32(exp0), now0, reserve, ca,
+                    status=st)
+    kvp.kvp_compact_quant(dev_bf16(k[:, :T0].copy()), dev_bf16(v[:, :T0].copy()), dev_f32(s[:, :T0].copy()),
+                          dev_f32(tau), dev_f32(tau_q), cq, reserve=reserve, window=W, status=st)
+    kd, vd, sd, tau_d, tq_d = dev_bf16(k), dev_bf16(v), dev_f32(s), dev_f32(tau), dev_f32(tau_q)
+    ws = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, H * G, H, d), dtype=torch.uint8, device="cuda")
+    for i, t in enumerate(range(T0, T)):
+        orc.append(ref_a, k[:, t], v[:, t], t, orc.expire_kvzap(s[:, t], tau, t, W))
+        orc.append_quant(ref_q, k[:, t], v[:, t], t, s[:, t], tau, tau_q, window=W)
+        kvp.kvp_append(ca, kd[:, t].contiguous(), vd[:, t].contiguous(), t, mode=kvp.KVP_MASK_KVZAP,
+                       score=sd[:, t].contiguous(), tau=tau_d, window=W, status=st)
+        kvp.kvp_append_quant(cq, kd[:, t].contiguous(), vd[:, t].contiguous(), t, score=sd[:, t].contiguous(),
+                             tau=tau_d, tau_q=tq_d, window=W, status=st)
+        qb = syn.f32_to_bf16_bits(q_all[i])
+        o = kvp.kvp_decode_attn_two_tier(dev_bf16(qb), ca, cq, t, workspace=ws, status=st)
+        if i % 8 == 0 or t == T - 1:
+            torch.cuda.synchronize()
+            assert st.item() == 0
+            check_attention(o.cpu().numpy(), orc.decode_attention_two_tier(qb, ref_a, ref_q, t))
+    _compare_cache(ca, ref_a)
+    _compare_qcache(cq, ref_q)
+
+
 def test_decode_attn_keep_all_is_dense_and_window(kvp):
     B, T, H, G, d = 1, 1100, 2, 4, 128
     k, v = syn.kv_inputs(8, B, T, H, d)
