@@ -90,6 +90,7 @@ class OracleSample:
         self.k, self.v = syn.kv_inputs(seed, 1, T, H, d)
         self.q = syn.q_inputs(seed, 1, H * G, d)
         self.tau = np.zeros((1, H), np.float32)  # the oracle's work does not depend on tau's value
+        self.phases = {"score": 0.0, "mask": 0.0, "compact": 0.0, "attention": 0.0}
 
     def run(self, rows: int):
         import oracle as orc
@@ -98,11 +99,17 @@ class OracleSample:
         now, pos0 = T - 1, T - rows
         t0 = time.perf_counter()
         s = orc.score_linear(self.x[pos0:], self.W).reshape(1, rows, H)
+        t1 = time.perf_counter()
         exp = orc.mask_kvzap(s, self.tau, now, window=w["window"], pos0=pos0)[0]
+        t2 = time.perf_counter()
         mp = (rows + 15) // 16
         c = orc.compact_dense(self.k[:, pos0:], self.v[:, pos0:], exp, now, 0, H * mp, mp)
+        t3 = time.perf_counter()
         orc.decode_attention(self.q, c, now)
-        return time.perf_counter() - t0, rows / T
+        t4 = time.perf_counter()
+        for k, dt in zip(("score", "mask", "compact", "attention"), (t1 - t0, t2 - t1, t3 - t2, t4 - t3)):
+            self.phases[k] += dt
+        return t4 - t0, rows / T
 
 
 def run_cpu_baseline(budget_s: float):
@@ -119,7 +126,7 @@ def run_cpu_baseline(budget_s: float):
     return {"value": total_seq / total_t, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{runs} full sequences of the workload (one sequence's 8192 cached positions, drawn once "
                       f"and re-run): float64 score, mask, compaction and attention of its query heads, one thread",
-            "seconds": total_t}
+            "seconds": total_t, "phase_seconds": {k: round(v, 3) for k, v in sample.phases.items()}}
 
 
 def run_reference(args, rank: int, world: int):
