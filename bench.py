@@ -59,6 +59,18 @@ SCORE_DRAM_BYTES_PER_ROW = 272.084e6 / 32768
 KERNELS_PER_STEP = {"fused": 4, "separate": 5}
 
 
+def scorer_overhead(w=WORKLOAD, ffn_hidden=14336, mlp_hidden=1024):
+    """The KVzap summary's overhead figures ("메모리 및 계산 효율": about 0.02 % of the linear-projection FLOPs
+    for KVzap-Linear, about 1.1 % for KVzap-MLP) as closed forms for this layer's shape: scorer multiply-adds
+    per token over the layer's Q, K, V, O and gated feed-forward projections."""
+    D, Hq, H, d = w["d_model"], w["n_q_heads"], w["n_kv_heads"], w["head_dim"]
+    proj = 2 * D * Hq * d + 2 * D * H * d + 3 * D * ffn_hidden
+    lin = D * H
+    mlp = D * mlp_hidden + mlp_hidden * H
+    return {"projection_macs_per_token": proj, "linear_macs_per_token": lin, "linear_fraction": lin / proj,
+            "mlp_macs_per_token": mlp, "mlp_fraction": mlp / proj, "ffn_hidden": ffn_hidden, "mlp_hidden": mlp_hidden}
+
+
 def config_desc(w=WORKLOAD, mask_mode=None):
     return {
         "workload": (f"{w['name']}: one layer, d_model {w['d_model']}, {w['n_q_heads']} q / {w['n_kv_heads']} kv "
@@ -443,6 +455,7 @@ def run_gpu(args, rank: int, world: int):
         "gpu_launches": KERNELS_PER_STEP[args.mask] * args.steps, "roofline": roofline,
         "kernels": kernels, "effective_step_GB_s": step_b / (ms_step * 1e-3) / 1e9,
         "scored_tokens_per_s": n_tok / (k_ms[0] * 1e-3),
+        "scorer_overhead": scorer_overhead(w),
         "kept_fraction": kept / (B * H * T), "clocks": clocks, "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
