@@ -342,6 +342,9 @@ def window_attention(q_bits, k_bits, v_bits, now: int, window: int = WINDOW, sca
 # in that tier from step pos + window on, i.e. from the step its full
 # precision copy leaves the window. Entries with s >= tau stay bf16 for good
 # (section 2); entries below tau_q are dropped after the window as before.
+# With DMS flags instead of scores, every flagged entry (flag_step >= 0) is
+# the one quantized instead of evicted: it enters the fp8 tier at the step
+# its bf16 copy is gone, max(flag + delay, pos + window).
 # ---------------------------------------------------------------------------
 
 E4M3_MAX = 448.0
@@ -434,14 +437,22 @@ class QuantPagedCache:
         return self.page_table[b, h, slots // PAGE], slots % PAGE
 
 
+def quant_tier_select_dms(flag_step_bht):
+    """DMS: the entries flagged for eviction go to the fp8 tier. [B, H, T] bool."""
+    return np.asarray(flag_step_bht) >= 0
+
+
 def compact_quant_dense(k_bits, v_bits, scores_bth, tau_bh, tau_q_bh, reserve, n_pages_cap, max_pages,
-                        window: int = WINDOW) -> QuantPagedCache:
+                        window: int = WINDOW, flag_step_bht=None, delay: int = 0) -> QuantPagedCache:
     """Dense K/V [B, T, H, d] -> the fp8 tier of the entries with
-    tau_q <= s < tau, in ascending position, pages handed out in (b-major,
-    h-minor) order exactly as in section 3; start = position + window."""
+    tau_q <= s < tau (or, given DMS flag steps instead of scores, the flagged
+    ones), in ascending position, pages handed out in (b-major, h-minor)
+    order exactly as in section 3; start = position + window (DMS:
+    max(flag + delay, position + window))."""
     B, T, H, d = k_bits.shape
     out = QuantPagedCache(B, H, d, n_pages_cap, max_pages)
-    sel = quant_tier_select(scores_bth, tau_bh, tau_q_bh)
+    dms = flag_step_bht is not None
+    sel = quant_tier_select_dms(flag_step_bht) if dms else quant_tier_select(scores_bth, tau_bh, tau_q_bh)
     for b in range(B):
         for h in range(H):
             pos = np.nonzero(sel[b, h])[0]
@@ -458,7 +469,8 @@ def compact_quant_dense(k_bits, v_bits, scores_bth, tau_bh, tau_q_bh, reserve, n
             out.vq_pool[base + j // PAGE, j % PAGE] = vc
             out.kscale[base + j // PAGE, j % PAGE] = ks
             out.vscale[base + j // PAGE, j % PAGE] = vs
-            out.start_pool[base + j // PAGE, j % PAGE] = pos + window
+            out.start_pool[base + j // PAGE, j % PAGE] = (
+                expire_dms(np.asarray(flag_step_bht)[b, h, pos], pos, delay, window) if dms else pos + window)
             out.remap[b, h, :n] = pos
             out.count[b, h] = n
             out.pages_used += npg
@@ -466,13 +478,17 @@ def compact_quant_dense(k_bits, v_bits, scores_bth, tau_bh, tau_q_bh, reserve, n
 
 
 def append_quant(qcache: QuantPagedCache, k_new_bits, v_new_bits, pos: int, score_bh, tau_bh, tau_q_bh,
-                 window: int = WINDOW):
+                 window: int = WINDOW, flag_bh=None, delay: int = 0):
     """Decode step for the fp8 tier: the token at `pos` (k/v [B, H, d]) goes
-    into slot count[b, h] of its (b, h)'s fp8 pages iff tau_q <= score < tau,
-    quantized like the compaction's rows, with start = pos + window; raises if
-    the reserved slots are used up."""
+    into slot count[b, h] of its (b, h)'s fp8 pages iff tau_q <= score < tau
+    (DMS: iff flagged, flag_bh >= 0), quantized like the compaction's rows,
+    with start = pos + window (DMS: max(flag + delay, pos + window)); raises
+    if the reserved slots are used up."""
     B, H = qcache.count.shape
-    sel = (np.asarray(score_bh) >= np.asarray(tau_q_bh)) & (np.asarray(score_bh) < np.asarray(tau_bh))
+    if flag_bh is not None:
+        sel = np.asarray(flag_bh) >= 0
+    else:
+        sel = (np.asarray(score_bh) >= np.asarray(tau_q_bh)) & (np.asarray(score_bh) < np.asarray(tau_bh))
     for b in range(B):
         for h in range(H):
             if not sel[b, h]:
@@ -488,7 +504,8 @@ def append_quant(qcache: QuantPagedCache, k_new_bits, v_new_bits, pos: int, scor
             qcache.vq_pool[page, j % PAGE] = vc[0]
             qcache.kscale[page, j % PAGE] = ks[0]
             qcache.vscale[page, j % PAGE] = vs[0]
-            qcache.start_pool[page, j % PAGE] = pos + window
+            qcache.start_pool[page, j % PAGE] = (
+                expire_dms(np.asarray(flag_bh)[b, h], pos, delay, window) if flag_bh is not None else pos + window)
             qcache.remap[b, h, j] = pos
             qcache.count[b, h] = j + 1
 

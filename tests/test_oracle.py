@@ -605,3 +605,35 @@ def test_quant_append_equals_one_compaction():
         for t in range(T0, T):
             orc.append_quant(tight, k[:, t], v[:, t], t, s[:, t], tau, np.full((B, H), -np.inf))
     assert (tight.count >= full).all()
+
+
+def test_dms_fp8_tier_takes_over_where_eviction_was():
+    """DMS flags: the fp8 tier holds exactly the flagged entries, each from the
+    step its bf16 copy is gone; at every step an entry is in exactly one tier,
+    and on rows exactly representable in E4M3 the two-tier attention equals
+    dense attention over every position (nothing is dropped any more)."""
+    rng = np.random.default_rng(14)
+    B, T, H, G, d, delay, W = 1, 260, 2, 2, 64, 40, 16
+    grid = orc.e4m3_positive_values()[:127]
+    grid = grid[(grid >= 2.0 ** -3) & (grid <= 4.0)]
+
+    def rows():
+        r = rng.choice(np.concatenate([grid, -grid]), size=(B, T, H, d)) * 0.25
+        r[..., 0] = 448.0 * 0.25
+        return syn.f32_to_bf16_bits(r.astype(np.float32))
+    k, v = rows(), rows()
+    q = syn.f32_to_bf16_bits((rng.standard_normal((B, H * G, d)) * 0.05).astype(np.float32))
+    pos = np.arange(T)[None, None, :]
+    f = np.where(rng.random((B, H, T)) < 0.875, pos, -1)
+    mp = T // 16 + 2
+    for now in (120, T - 1):
+        exp = orc.mask_dms(f[:, :, :now + 1], now, delay, window=W)[0]
+        ca = orc.compact_dense(k[:, :now + 1], v[:, :now + 1], exp, now, 0, B * H * mp, mp)
+        cq = orc.compact_quant_dense(k[:, :now + 1], v[:, :now + 1], None, None, None, 0, B * H * mp, mp,
+                                     window=W, flag_step_bht=f[:, :, :now + 1], delay=delay)
+        assert (cq.count == (f[:, :, :now + 1] >= 0).sum(axis=2)).all()
+        in_a = orc.present(exp, now).sum()
+        vis_b = sum(int((now >= cq.start_pool[cq.slot_rows(0, h, np.arange(cq.count[0, h]))]).sum()) for h in range(H))
+        assert in_a + vis_b == H * (now + 1)
+        np.testing.assert_allclose(orc.decode_attention_two_tier(q, ca, cq, now),
+                                   orc.dense_attention(q, k, v, now), rtol=0, atol=1e-6)
