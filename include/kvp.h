@@ -267,12 +267,18 @@ KVP_API kvp_status kvp_compact_masked(int mode, int batch, int n_kv_heads, int h
  *     step its bf16 copy leaves the window, so at any step an entry is in one
  *     tier at most.
  *
+ * With DMS flags (mode KVP_MASK_DMS) the entries quantized are the flagged
+ * ones (flag_step >= 0: quantize instead of evict), visible from
+ * max(flag + delay, t + window) on, the step their bf16 copy is gone.
+ *
  * Selected entries are laid out like kvp_compact's survivors: ascending
  * position, (b, h) in b-major / h-minor order, ceil((count + reserve) / 16)
  * consecutive pages each.
  * Source, strides, reserve, workspace (kvp_compact_workspace_bytes) and
- * errors: as kvp_compact. scores device fp32 [B, n_pos, H]; tau, tau_q device
- * fp32 [B, H].
+ * errors: as kvp_compact. KVP_MASK_KVZAP: scores device fp32 [B, n_pos, H]
+ * (may be NULL when n_pos is 0), tau and tau_q device fp32 [B, H], flag_step
+ * NULL. KVP_MASK_DMS: flag_step device int32 [B, H, n_pos] and delay as in
+ * kvp_mask, scores / tau / tau_q NULL.
  * Outputs (all device):
  *   kq_pool, vq_pool  uint8 [n_pages_cap, 16, head_dim] E4M3 codes, 16-byte
  *                     aligned; rows past count in a (b, h)'s last page zero
@@ -280,10 +286,11 @@ KVP_API kvp_status kvp_compact_masked(int mode, int batch, int n_kv_heads, int h
  *                     K scale and the V scale (fp32 bit patterns); 0 in unused rows
  *   page_table, remap, count: as kvp_compact (remap = source position)
  */
-KVP_API kvp_status kvp_compact_quant(int batch, int n_kv_heads, int head_dim, int n_pos,
+KVP_API kvp_status kvp_compact_quant(int mode, int batch, int n_kv_heads, int head_dim, int n_pos,
                        const void* k_src, const void* v_src,
                        int64_t stride_b, int64_t stride_t, int64_t stride_h,
-                       const float* scores, const float* tau, const float* tau_q, int window, int reserve,
+                       const float* scores, const float* tau, const float* tau_q, const int32_t* flag_step,
+                       int window, int delay, int reserve,
                        void* kq_pool, void* vq_pool, int32_t* meta_pool, int n_pages_cap,
                        int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
@@ -291,16 +298,18 @@ KVP_API kvp_status kvp_compact_quant(int batch, int n_kv_heads, int head_dim, in
 /* kvp_append_quant - the decode-time side of the fp8 tier: the token at
  * position `pos` (k_new, v_new device bf16 [B, H, head_dim], 16-byte aligned)
  * goes into slot count[b, h] of its (b, h)'s fp8 pages iff
- * tau_q[b, h] <= score[b, h] < tau[b, h] (device fp32 [B, H]; the score the
- * token got for the bf16 tier's kvp_append), quantized exactly as
- * kvp_compact_quant does, with start = pos + window; remap and count grow by
- * one. The slot must be one of the pages the compaction reserved, else
+ * tau_q[b, h] <= score[b, h] < tau[b, h] (KVP_MASK_KVZAP; device fp32 [B, H],
+ * the score the token got for the bf16 tier's kvp_append), start = pos +
+ * window; or iff flag_step[b, h] >= 0 (KVP_MASK_DMS; device int32 [B, H]),
+ * start = max(flag + delay, pos + window). It is quantized exactly as
+ * kvp_compact_quant does; remap and count grow by one. The slot must be one of the pages the compaction reserved, else
  * KVP_ERR_CAPACITY is recorded in `status` and that (b, h) is left as it is.
  * Pools and tables: as kvp_compact_quant writes them.
  */
-KVP_API kvp_status kvp_append_quant(int batch, int n_kv_heads, int head_dim, int pos,
+KVP_API kvp_status kvp_append_quant(int mode, int batch, int n_kv_heads, int head_dim, int pos,
                        const void* k_new, const void* v_new,
-                       const float* score, const float* tau, const float* tau_q, int window,
+                       const float* score, const float* tau, const float* tau_q, const int32_t* flag_step,
+                       int window, int delay,
                        void* kq_pool, void* vq_pool, int32_t* meta_pool, int n_pages_cap,
                        const int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
                        int32_t* status, void* stream);

@@ -76,14 +76,15 @@ _SIGS = {
                          _P, _S, _P, _P]),
     "kvp_compact_masked": (_I, [_I, _I, _I, _I, _I, _P, _P, _L, _L, _L, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P,
                                 _I, _P, _I, _P, _P, _P, _S, _P, _P]),
-    "kvp_compact_quant": (_I, [_I, _I, _I, _I, _P, _P, _L, _L, _L, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I,
-                               _P, _P, _P, _S, _P, _P]),
+    "kvp_compact_quant": (_I, [_I, _I, _I, _I, _I, _P, _P, _L, _L, _L, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
+                               _I, _P, _I, _P, _P, _P, _S, _P, _P]),
     "kvp_compact_paged_workspace_bytes": (_S, [_I, _I, _I]),
     "kvp_compact_paged": (_I, [_I, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I,
                                _P, _P, _P, _S, _P, _P]),
     "kvp_append": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
                         _P, _P]),
-    "kvp_append_quant": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P]),
+    "kvp_append_quant": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
+                              _P, _P]),
     "kvp_decode_attn_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "kvp_decode_attn": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _I, _P, _S, _P, _P]),
     "kvp_decode_attn_two_tier": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _P, _I, _P,
@@ -390,23 +391,28 @@ def kvp_compact_masked(k, v, now, reserve, dst: PagedKV, *, mode, scores=None, t
     return dst
 
 
-def kvp_compact_quant(k, v, scores, tau, tau_q, dst: QuantPagedKV, *, reserve=0, window=WINDOW, status,
-                      workspace=None, stream=None):
+def kvp_compact_quant(k, v, scores, tau, tau_q, dst: QuantPagedKV, *, mode=KVP_MASK_KVZAP, flag_step=None, delay=0,
+                      reserve=0, window=WINDOW, status, workspace=None, stream=None):
     """Dense K, V [B, T, H, d] -> the fp8 tier: entries with tau_q <= score < tau (scores [B*T, H] or
-    [B, T, H]; tau, tau_q [B, H]) as E4M3 codes with a per-row scale, visible from position + window on."""
+    [B, T, H]; tau, tau_q [B, H]), or with mode KVP_MASK_DMS the flagged entries (flag_step [B, H, T];
+    scores, tau, tau_q None), as E4M3 codes with a per-row scale, visible from the step their bf16 copy
+    is gone."""
     B, T, H, d = k.shape
     if k.stride() != v.stride() or k.stride(3) != 1:
         raise ValueError("k and v need identical strides with the head_dim axis contiguous")
     for t, nm in ((k, "k"), (v, "v")):
         if t.dtype != torch.bfloat16 or not t.is_cuda:
             raise TypeError(f"{nm} must be a CUDA bf16 tensor")
-    if scores.numel() != B * T * H or tau.numel() != B * H or tau_q.numel() != B * H:
+    if mode == KVP_MASK_KVZAP and (scores.numel() != B * T * H or tau.numel() != B * H or tau_q.numel() != B * H):
         raise ValueError("scores must hold B*T*H values, tau and tau_q B*H")
+    if mode == KVP_MASK_DMS and flag_step.numel() != B * H * T:
+        raise ValueError("flag_step must hold B*H*T values")
     need = kvp_compact_workspace_bytes(B, H, T)
     ws = _ws(need, k.device, workspace)
-    code = _lib.kvp_compact_quant(B, H, d, T, k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), k.stride(2),
-                                  _ptr(scores, torch.float32, "scores"), _ptr(tau, torch.float32, "tau"),
-                                  _ptr(tau_q, torch.float32, "tau_q"), window, reserve,
+    code = _lib.kvp_compact_quant(mode, B, H, d, T, k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1),
+                                  k.stride(2), _ptr(scores, torch.float32, "scores", True),
+                                  _ptr(tau, torch.float32, "tau", True), _ptr(tau_q, torch.float32, "tau_q", True),
+                                  _ptr(flag_step, torch.int32, "flag_step", True), window, delay, reserve,
                                   _ptr(dst.kq_pool, torch.uint8), _ptr(dst.vq_pool, torch.uint8),
                                   _ptr(dst.meta_pool, torch.int32), dst.n_pages_cap,
                                   _ptr(dst.page_table, torch.int32), dst.max_pages, _ptr(dst.remap, torch.int32),
@@ -452,14 +458,16 @@ def kvp_append(cache: PagedKV, k_new, v_new, pos, *, mode, score=None, tau=None,
     _check("kvp_append", code)
 
 
-def kvp_append_quant(qcache: QuantPagedKV, k_new, v_new, pos, *, score, tau, tau_q, window=WINDOW, status,
-                     stream=None):
+def kvp_append_quant(qcache: QuantPagedKV, k_new, v_new, pos, *, score=None, tau=None, tau_q=None,
+                     mode=KVP_MASK_KVZAP, flag_step=None, delay=0, window=WINDOW, status, stream=None):
     """Writes the token at position `pos` (k_new, v_new [B, H, d]) into the fp8 tier of every (b, h) whose
-    score falls in [tau_q, tau)."""
+    score falls in [tau_q, tau) (or, mode KVP_MASK_DMS, whose flag_step [B, H] is >= 0)."""
     B, H, d = k_new.shape
-    code = _lib.kvp_append_quant(B, H, d, pos, _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
-                                 _ptr(score, torch.float32, "score"), _ptr(tau, torch.float32, "tau"),
-                                 _ptr(tau_q, torch.float32, "tau_q"), window, _ptr(qcache.kq_pool, torch.uint8),
+    code = _lib.kvp_append_quant(mode, B, H, d, pos, _ptr(k_new, torch.bfloat16, "k_new"),
+                                 _ptr(v_new, torch.bfloat16, "v_new"), _ptr(score, torch.float32, "score", True),
+                                 _ptr(tau, torch.float32, "tau", True), _ptr(tau_q, torch.float32, "tau_q", True),
+                                 _ptr(flag_step, torch.int32, "flag_step", True), window, delay,
+                                 _ptr(qcache.kq_pool, torch.uint8),
                                  _ptr(qcache.vq_pool, torch.uint8), _ptr(qcache.meta_pool, torch.int32),
                                  qcache.n_pages_cap, _ptr(qcache.page_table, torch.int32), qcache.max_pages,
                                  _ptr(qcache.remap, torch.int32), _ptr(qcache.count, torch.int32),

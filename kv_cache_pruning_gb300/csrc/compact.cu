@@ -185,9 +185,10 @@ struct MaskedSrc {
 };
 
 // Selection for the fp8 tier (quantize instead of drop; BeaconKV article):
-// entry t of the dense source goes to the tier iff tau_q <= score < tau (NaN
-// never), and its value is the step from which it is visible there, the
-// step its full-precision copy leaves the window (t + window). `now` plays
+// KVzap: entry t of the dense source goes to the tier iff tau_q <= score <
+// tau (NaN never); DMS: iff it is flagged (flag step >= 0). Its value is the
+// step from which it is visible there, the step its full-precision copy is
+// gone: t + window (KVzap), max(flag + delay, t + window) (DMS). `now` plays
 // no part in the choice.
 constexpr int32_t kNotSelected = INT32_MIN;
 
@@ -195,22 +196,30 @@ struct QuantSrc {
   const uint16_t* k;
   const uint16_t* v;
   int64_t sb, st, sh;
-  const float* scores;     // [B, n, H]
-  const float* tau;        // [B, H]
-  const float* tau_q;      // [B, H]
-  int window;
+  int mode;
+  const float* scores;     // KVzap: [B, n, H]
+  const float* tau;        // KVzap: [B, H]
+  const float* tau_q;      // KVzap: [B, H]
+  const int32_t* flag;     // DMS: [B, H, n]
+  int window, delay;
   int H;
   int n;
   struct View {
     const uint16_t* kb;
     const uint16_t* vb;
     int64_t stride;
+    int mode;
     const float* sc;
+    const int32_t* fl;
     float th, tq;
-    int H, window, n;
+    int H, window, delay, n;
     KVP_DEV int length() const { return n; }
     KVP_DEV int32_t expire_row(int t, int64_t& row) const {
       row = t;
+      if (mode == KVP_MASK_DMS) {
+        const int32_t f = fl[t];
+        return f >= 0 ? expire_dms(f, t, delay, window) : kNotSelected;
+      }
       const float x = sc[static_cast<int64_t>(t) * H];
       return (x >= tq && x < th) ? t + window : kNotSelected;
     }
@@ -220,8 +229,19 @@ struct QuantSrc {
   KVP_DEV View view(int bh) const {
     const int b = bh / H, h = bh - b * H;
     const int64_t off = b * sb + h * sh;
-    return View{k + off, v + off, st, scores + static_cast<int64_t>(b) * n * H + h, tau[bh], tau_q[bh],
-                H, window, n};
+    const bool kvz = mode == KVP_MASK_KVZAP;
+    return View{k + off,
+                v + off,
+                st,
+                mode,
+                kvz ? scores + static_cast<int64_t>(b) * n * H + h : nullptr,
+                kvz ? nullptr : flag + static_cast<int64_t>(bh) * n,
+                kvz ? tau[bh] : 0.f,
+                kvz ? tau_q[bh] : 0.f,
+                H,
+                window,
+                delay,
+                n};
   }
 };
 
@@ -666,11 +686,13 @@ __global__ void __launch_bounds__(256) append_kernel(int mode, int BH, int pos, 
 // pass's (each lane takes D / 32 elements, the row's amax is reduced over the
 // warp), start = pos + window.
 template <int D>
-__global__ void __launch_bounds__(256) append_quant_kernel(int BH, int pos, const uint16_t* __restrict__ k_new,
+__global__ void __launch_bounds__(256) append_quant_kernel(int mode, int BH, int pos,
+                                                           const uint16_t* __restrict__ k_new,
                                                            const uint16_t* __restrict__ v_new,
                                                            const float* __restrict__ score,
                                                            const float* __restrict__ tau,
-                                                           const float* __restrict__ tau_q, int window,
+                                                           const float* __restrict__ tau_q,
+                                                           const int32_t* __restrict__ flag, int window, int delay,
                                                            uint8_t* __restrict__ kq_pool, uint8_t* __restrict__ vq_pool,
                                                            int32_t* __restrict__ meta_pool, int n_pages_cap,
                                                            const int32_t* __restrict__ page_table, int max_pages,
@@ -680,8 +702,16 @@ __global__ void __launch_bounds__(256) append_quant_kernel(int BH, int pos, cons
   const int bh = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (bh >= BH) return;
-  const float sc = score[bh];
-  if (!(sc >= tau_q[bh] && sc < tau[bh])) return;  // not in the fp8 tier (the same for the whole warp)
+  int32_t start;
+  if (mode == KVP_MASK_DMS) {
+    const int32_t f = flag[bh];
+    if (f < 0) return;  // not flagged: stays bf16 (the same for the whole warp)
+    start = expire_dms(f, pos, delay, window);
+  } else {
+    const float sc = score[bh];
+    if (!(sc >= tau_q[bh] && sc < tau[bh])) return;  // not in the fp8 tier (the same for the whole warp)
+    start = pos + window;
+  }
   const int j = count[bh];
   if (j < 0) {
     if (lane == 0) record_error(status, KVP_ERR_BOUNDS);
@@ -733,7 +763,7 @@ __global__ void __launch_bounds__(256) append_quant_kernel(int BH, int pos, cons
     if (lane == 0) reinterpret_cast<float*>(meta)[(1 + w) * kPage + (j & 15)] = scale;
   }
   if (lane == 0) {
-    meta[j & 15] = pos + window;
+    meta[j & 15] = start;
     remap[static_cast<int64_t>(bh) * max_pages * kPage + j] = pos;
     count[bh] = j + 1;
   }
@@ -896,16 +926,24 @@ extern "C" kvp_status kvp_compact_masked(int mode, int batch, int n_kv_heads, in
                      page_table, max_pages, remap, count, workspace, status, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" kvp_status kvp_compact_quant(int batch, int n_kv_heads, int head_dim, int n_pos, const void* k_src,
-                                        const void* v_src, int64_t stride_b, int64_t stride_t, int64_t stride_h,
-                                        const float* scores, const float* tau, const float* tau_q, int window,
-                                        int reserve, void* kq_pool, void* vq_pool, int32_t* meta_pool,
-                                        int n_pages_cap, int32_t* page_table, int max_pages, int32_t* remap,
-                                        int32_t* count, void* workspace, size_t workspace_bytes, int32_t* status,
-                                        void* stream) {
-  if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0 || window < 0) return KVP_ERR_INVALID;
-  if (tau == nullptr || tau_q == nullptr || (n_pos > 0 && scores == nullptr)) return KVP_ERR_INVALID;
-  if (static_cast<int64_t>(n_pos) + window >= kNever) return KVP_ERR_INVALID;
+extern "C" kvp_status kvp_compact_quant(int mode, int batch, int n_kv_heads, int head_dim, int n_pos,
+                                        const void* k_src, const void* v_src, int64_t stride_b, int64_t stride_t,
+                                        int64_t stride_h, const float* scores, const float* tau, const float* tau_q,
+                                        const int32_t* flag_step, int window, int delay, int reserve, void* kq_pool,
+                                        void* vq_pool, int32_t* meta_pool, int n_pages_cap, int32_t* page_table,
+                                        int max_pages, int32_t* remap, int32_t* count, void* workspace,
+                                        size_t workspace_bytes, int32_t* status, void* stream) {
+  if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0 || window < 0 || delay < 0) return KVP_ERR_INVALID;
+  if (mode == KVP_MASK_KVZAP) {
+    if (flag_step != nullptr || tau == nullptr || tau_q == nullptr || (n_pos > 0 && scores == nullptr))
+      return KVP_ERR_INVALID;
+  } else if (mode == KVP_MASK_DMS) {
+    if (scores != nullptr || tau != nullptr || tau_q != nullptr || (n_pos > 0 && flag_step == nullptr))
+      return KVP_ERR_INVALID;
+  } else {
+    return KVP_ERR_INVALID;
+  }
+  if (static_cast<int64_t>(n_pos) + window + delay >= kNever) return KVP_ERR_INVALID;
   kvp_status s = check_dst(head_dim, reserve, kq_pool, vq_pool, meta_pool, n_pages_cap, page_table, max_pages,
                            remap, count, status);
   if (s != KVP_OK) return s;
@@ -920,10 +958,13 @@ extern "C" kvp_status kvp_compact_quant(int batch, int n_kv_heads, int head_dim,
                stride_b,
                stride_t,
                stride_h,
+               mode,
                scores,
                tau,
                tau_q,
+               flag_step,
                window,
+               delay,
                n_kv_heads,
                n_pos};
   return run_compact(src, batch * n_kv_heads, NS, head_dim, 0, reserve, kq_pool, vq_pool, meta_pool, n_pages_cap,
@@ -1005,21 +1046,27 @@ extern "C" kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_d
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
-extern "C" kvp_status kvp_append_quant(int batch, int n_kv_heads, int head_dim, int pos, const void* k_new,
+extern "C" kvp_status kvp_append_quant(int mode, int batch, int n_kv_heads, int head_dim, int pos, const void* k_new,
                                        const void* v_new, const float* score, const float* tau, const float* tau_q,
-                                       int window, void* kq_pool, void* vq_pool, int32_t* meta_pool, int n_pages_cap,
-                                       const int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
-                                       int32_t* status, void* stream) {
-  if (batch <= 0 || n_kv_heads <= 0 || pos < 0 || window < 0 || max_pages < 0 || n_pages_cap < 0)
+                                       const int32_t* flag_step, int window, int delay, void* kq_pool, void* vq_pool,
+                                       int32_t* meta_pool, int n_pages_cap, const int32_t* page_table, int max_pages,
+                                       int32_t* remap, int32_t* count, int32_t* status, void* stream) {
+  if (batch <= 0 || n_kv_heads <= 0 || pos < 0 || window < 0 || delay < 0 || max_pages < 0 || n_pages_cap < 0)
     return KVP_ERR_INVALID;
   if (head_dim != 64 && head_dim != 128) return KVP_ERR_UNSUPPORTED;
-  if (k_new == nullptr || v_new == nullptr || score == nullptr || tau == nullptr || tau_q == nullptr ||
-      kq_pool == nullptr || vq_pool == nullptr || meta_pool == nullptr || page_table == nullptr || remap == nullptr ||
-      count == nullptr || status == nullptr)
+  if (mode == KVP_MASK_KVZAP) {
+    if (score == nullptr || tau == nullptr || tau_q == nullptr || flag_step != nullptr) return KVP_ERR_INVALID;
+  } else if (mode == KVP_MASK_DMS) {
+    if (flag_step == nullptr || score != nullptr || tau != nullptr || tau_q != nullptr) return KVP_ERR_INVALID;
+  } else {
+    return KVP_ERR_INVALID;
+  }
+  if (k_new == nullptr || v_new == nullptr || kq_pool == nullptr || vq_pool == nullptr || meta_pool == nullptr ||
+      page_table == nullptr || remap == nullptr || count == nullptr || status == nullptr)
     return KVP_ERR_INVALID;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kq_pool) || !aligned16(vq_pool) || !aligned16(meta_pool))
     return KVP_ERR_ALIGN;
-  if (static_cast<int64_t>(pos) + window >= kNever) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(pos) + window + delay >= kNever) return KVP_ERR_INVALID;
   const int BH = batch * n_kv_heads;
   const int blocks = (BH + 7) / 8;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1028,11 +1075,13 @@ extern "C" kvp_status kvp_append_quant(int batch, int n_kv_heads, int head_dim, 
   auto* kq = static_cast<uint8_t*>(kq_pool);
   auto* vq = static_cast<uint8_t*>(vq_pool);
   if (head_dim == 128)
-    append_quant_kernel<128><<<blocks, 256, 0, st>>>(BH, pos, kn, vn, score, tau, tau_q, window, kq, vq, meta_pool,
-                                                     n_pages_cap, page_table, max_pages, remap, count, status);
+    append_quant_kernel<128><<<blocks, 256, 0, st>>>(mode, BH, pos, kn, vn, score, tau, tau_q, flag_step, window,
+                                                     delay, kq, vq, meta_pool, n_pages_cap, page_table, max_pages,
+                                                     remap, count, status);
   else
-    append_quant_kernel<64><<<blocks, 256, 0, st>>>(BH, pos, kn, vn, score, tau, tau_q, window, kq, vq, meta_pool,
-                                                    n_pages_cap, page_table, max_pages, remap, count, status);
+    append_quant_kernel<64><<<blocks, 256, 0, st>>>(mode, BH, pos, kn, vn, score, tau, tau_q, flag_step, window,
+                                                    delay, kq, vq, meta_pool, n_pages_cap, page_table, max_pages,
+                                                    remap, count, status);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 

@@ -118,11 +118,16 @@ def test_compact_quant_host_checks():
     import kv_cache_pruning_gb300 as k
     L = k.library()
 
-    def call(hd=128, scores=16, tau=16, tau_q=16, window=128, kq=16, meta=16, status=16):
-        return L.kvp_compact_quant(1, 1, hd, 16, 16, 16, 0, 0, 0, scores, tau, tau_q, window, 0, kq, 16, meta, 1,
-                                   16, 1, 16, 16, 16, 1 << 20, status, None)
+    def call(mode=0, hd=128, scores=16, tau=16, tau_q=16, flag=None, window=128, delay=0, kq=16, meta=16, status=16):
+        return L.kvp_compact_quant(mode, 1, 1, hd, 16, 16, 16, 0, 0, 0, scores, tau, tau_q, flag, window, delay, 0,
+                                   kq, 16, meta, 1, 16, 1, 16, 16, 16, 1 << 20, status, None)
 
     assert call(tau_q=None) == k.KVP_ERR_INVALID
+    assert call(flag=16) == k.KVP_ERR_INVALID                                   # KVzap with flags too
+    assert call(mode=1, flag=16) == k.KVP_ERR_INVALID                           # DMS with scores too
+    assert call(mode=1, scores=None, tau=None, tau_q=None) == k.KVP_ERR_INVALID  # DMS without flags
+    assert call(mode=1, scores=None, tau=None, tau_q=None, flag=16, delay=-1) == k.KVP_ERR_INVALID
+    assert call(mode=3) == k.KVP_ERR_INVALID
     assert call(scores=None) == k.KVP_ERR_INVALID
     assert call(window=-1) == k.KVP_ERR_INVALID
     assert call(meta=None) == k.KVP_ERR_INVALID
@@ -135,11 +140,13 @@ def test_append_quant_host_checks():
     import kv_cache_pruning_gb300 as k
     L = k.library()
 
-    def call(hd=128, pos=5, kn=16, tau_q=16, window=128, status=16):
-        return L.kvp_append_quant(1, 1, hd, pos, kn, 16, 16, 16, tau_q, window, 16, 16, 16, 1, 16, 1, 16, 16,
-                                  status, None)
+    def call(mode=0, hd=128, pos=5, kn=16, score=16, tau=16, tau_q=16, flag=None, window=128, delay=0, status=16):
+        return L.kvp_append_quant(mode, 1, 1, hd, pos, kn, 16, score, tau, tau_q, flag, window, delay, 16, 16, 16, 1,
+                                  16, 1, 16, 16, status, None)
 
     assert call(tau_q=None) == k.KVP_ERR_INVALID
+    assert call(mode=1, flag=16) == k.KVP_ERR_INVALID                          # DMS with scores too
+    assert call(mode=1, score=None, tau=None, tau_q=None) == k.KVP_ERR_INVALID  # DMS without flags
     assert call(pos=-1) == k.KVP_ERR_INVALID
     assert call(window=-2) == k.KVP_ERR_INVALID
     assert call(status=None) == k.KVP_ERR_INVALID

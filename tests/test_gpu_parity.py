@@ -812,6 +812,98 @@ def test_two_tier_decode_loop(kvp):
     _compare_qcache(cq, ref_q)
 
 
+def test_decode_attn_largest_pair_count(kvp):
+    """4096 (b, h) pairs, the most the kernel's shared page prefix holds, with
+    short and empty heads mixed in; one more pair is refused on the host."""
+    B, T, H, G, d = 512, 70, 8, 1, 64
+    k, v = syn.kv_inputs(31, B, T, H, d)
+    q = syn.q_inputs(31, B, H * G, d)
+    s = syn.normal_f32(31, 81, (B, T, H))
+    tau = syn.normal_f32(31, 82, (B, H), std=1.0)
+    tau[::7, :] = np.inf                  # window only
+    now = T - 1
+    exp = orc.mask_kvzap(s, tau, now, window=3)[0].astype(np.int32)
+    exp[::5, ::3, :] = 0                  # some heads keep nothing
+    mp = (T + 15) // 16
+    ref_c = orc.compact_dense(k, v, exp, now, 0, B * H * mp, mp)
+    st = status_word()
+    c = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp)
+    kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp), now, 0, c, status=st)
+    o = kvp.kvp_decode_attn(dev_bf16(q), c, now, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_cache(c, ref_c)
+    check_attention(o.cpu().numpy(), orc.decode_attention(q, ref_c, now))
+    big = kvp.PagedKV.allocate(B + 1, H, d, 8, 1)
+    with pytest.raises(kvp.KvpError):
+        kvp.kvp_decode_attn(dev_bf16(syn.q_inputs(31, B + 1, H * G, d)), big, now, status=st)
+
+
+@pytest.mark.parametrize("B,T,H,d,delay,window,reserve", [
+    (2, 1000, 4, 128, 256, 128, 0),
+    (3, 777, 3, 64, 40, 16, 20),
+    (131, 40, 8, 64, 8, 4, 3),          # more than 1024 (b, h)
+])
+def test_compact_quant_dms_bit_exact(kvp, B, T, H, d, delay, window, reserve):
+    """DMS flags: the fp8 tier holds the flagged entries with start =
+    max(flag + delay, pos + window), bit-exact against the oracle."""
+    k, v, f, _ = _dms_stream(B, T, H, d, delay, window, seed=33)
+    mp = (T + reserve + 15) // 16
+    cap = B * H * mp
+    ref = orc.compact_quant_dense(k, v, None, None, None, reserve, cap, mp, window=window, flag_step_bht=f,
+                                  delay=delay)
+    st = status_word()
+    cq = kvp.QuantPagedKV.allocate(B, H, d, cap, mp)
+    kvp.kvp_compact_quant(dev_bf16(k), dev_bf16(v), None, None, None, cq, mode=kvp.KVP_MASK_DMS,
+                          flag_step=dev_i32(f), delay=delay, reserve=reserve, window=window, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_qcache(cq, ref)
+
+
+def test_two_tier_dms_decode_loop(kvp):
+    """DMS decode with quantize-instead-of-evict: prefill both tiers, then
+    each step appends the token to the bf16 tier (kvp_append, DMS rule) and,
+    if flagged, to the fp8 tier (kvp_append_quant, DMS); the two-tier
+    attention at every step matches the oracle's, and the flagged entries
+    cross into the fp8 tier as their delay runs out."""
+    B, T0, T, H, G, d, delay, W = 2, 500, 580, 4, 4, 128, 24, 16
+    k, v, f, exp = _dms_stream(B, T, H, d, delay, W, seed=37)
+    q_all = syn.normal_f32(37, 91, (T - T0, B, H * G, d))
+    now0 = T0 - 1
+    reserve, mp = 96, (T + 96 + 15) // 16
+    cap = B * H * mp
+    ref_a = orc.compact_dense(k[:, :T0], v[:, :T0], exp[:, :, :T0], now0, reserve, cap, mp)
+    ref_q = orc.compact_quant_dense(k[:, :T0], v[:, :T0], None, None, None, reserve, cap, mp, window=W,
+                                    flag_step_bht=f[:, :, :T0], delay=delay)
+    st = status_word()
+    ca = kvp.PagedKV.allocate(B, H, d, cap, mp)
+    cq = kvp.QuantPagedKV.allocate(B, H, d, cap, mp)
+    kvp.kvp_compact(dev_bf16(k[:, :T0].copy()), dev_bf16(v[:, :T0].copy()), dev_i32(exp[:, :, :T0].copy()), now0,
+                    reserve, ca, status=st)
+    kvp.kvp_compact_quant(dev_bf16(k[:, :T0].copy()), dev_bf16(v[:, :T0].copy()), None, None, None, cq,
+                          mode=kvp.KVP_MASK_DMS, flag_step=dev_i32(f[:, :, :T0].copy()), delay=delay,
+                          reserve=reserve, window=W, status=st)
+    kd, vd, fd = dev_bf16(k), dev_bf16(v), dev_i32(f)
+    ws = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, H * G, H, d), dtype=torch.uint8, device="cuda")
+    for i, t in enumerate(range(T0, T)):
+        orc.append(ref_a, k[:, t], v[:, t], t, exp[:, :, t])
+        orc.append_quant(ref_q, k[:, t], v[:, t], t, None, None, None, window=W, flag_bh=f[:, :, t], delay=delay)
+        ft = fd[:, :, t].contiguous()
+        kvp.kvp_append(ca, kd[:, t].contiguous(), vd[:, t].contiguous(), t, mode=kvp.KVP_MASK_DMS, flag_step=ft,
+                       delay=delay, window=W, status=st)
+        kvp.kvp_append_quant(cq, kd[:, t].contiguous(), vd[:, t].contiguous(), t, mode=kvp.KVP_MASK_DMS,
+                             flag_step=ft, delay=delay, window=W, status=st)
+        qb = syn.f32_to_bf16_bits(q_all[i])
+        o = kvp.kvp_decode_attn_two_tier(dev_bf16(qb), ca, cq, t, workspace=ws, status=st)
+        if i % 10 == 0 or t == T - 1:
+            torch.cuda.synchronize()
+            assert st.item() == 0
+            check_attention(o.cpu().numpy(), orc.decode_attention_two_tier(qb, ref_a, ref_q, t))
+    _compare_cache(ca, ref_a)
+    _compare_qcache(cq, ref_q)
+
+
 def test_decode_attn_keep_all_is_dense_and_window(kvp):
     B, T, H, G, d = 1, 1100, 2, 4, 128
     k, v = syn.kv_inputs(8, B, T, H, d)
