@@ -9,12 +9,16 @@
 //
 // Compaction (DeInfer summary, "나. 페이지드 KV 캐시 및 CUDA Graph 통합"):
 // a preparation pass counts the present entries of each 128-entry segment of
-// every (b, h) (one warp per segment, ballots), a single-CTA scan turns the
-// counts into the remapping offsets and the page base of every (b, h), and a
-// copy pass (again one warp per segment, no block-level synchronisation)
-// re-derives each entry's slot from its segment offset plus a ballot prefix
-// and moves its K and V rows with 16-byte vector loads and stores, 8 rows'
-// loads in flight per lane before their stores.
+// every (b, h) (one warp per segment) and adds each CTA's total to the
+// (b, h)'s count with one atomic; a copy pass (again one warp per segment)
+// derives its segment's first slot from the counts of the segments before it
+// and, up to 1,024 (b, h), its page base and the budget check from all
+// counts (above that a one-CTA pass computes the bases), lists the segment's
+// present entries with ballots (the remapping index list) and moves their K
+// and V rows through a shared-memory stage with 16-byte asynchronous copies.
+// Where an entry's presence comes from is a "source" view: a precomputed
+// expire array, the mask rule applied to scores or flag steps on the fly, a
+// paged cache, or the fp8 tier's selection (whose copy pass quantizes).
 #include <mutex>
 #include <type_traits>
 
