@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   int cnt_q = kQ ? clamp_count(p.count_q, cbh, p.max_pages_q) : 0;  // fp8-tier slots of this (b, h)
   int cnt_q_next = 0;
   if (seg_end < r1) {
-    load_q(next_bh(cbh), qn);
+    if constexpr (G < 8) load_q(next_bh(cbh), qn);  // G = 8 loads the next query rows at the switch
     cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
     if constexpr (kQ) cnt_q_next = clamp_count(p.count_q, next_bh(cbh), p.max_pages_q);
   }
@@ -423,25 +423,55 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
     const bool isq = kQ && li >= na_cur;           // a fp8-tier page (uniform in the warp)
     const int slot0 = (isq ? li - na_cur : li) * kPage;
 
-    // this lane's share of the page goes to registers and the stage is handed
-    // straight back to the copy engine: every stage of the ring stays in
-    // flight while the warp computes
-    uint4 kr[C::RS], vr[C::RS];
+    // For G <= 4 this lane's share of the page goes to registers and the
+    // stage is handed straight back to the copy engine, so every stage of the
+    // ring stays in flight while the warp computes. For G = 8 the query rows
+    // and accumulators take those registers: K and V are read from the stage
+    // where they are used and the stage goes back after the page.
+    constexpr bool kRegStage = G < 8;
+    const uint8_t* Kq = stage;
+    const uint8_t* Vq = stage + C::QPAGE_BYTES;
+    const int32_t* Mq = reinterpret_cast<const int32_t*>(stage + 2 * C::QPAGE_BYTES);
+    // the lane's 16 bytes of K (or V) row t * RPS + rowsel; fp8 page: the 8
+    // codes in .x/.y and, for V, the row's scale in .z
+    auto k_word = [&](int t) {
+      const int row = t * C::RPS + rowsel;
+      if (isq) {
+        const uint2 kc = reinterpret_cast<const uint2*>(Kq + row * D)[s];
+        return make_uint4(kc.x, kc.y, 0u, 0u);
+      }
+      return reinterpret_cast<const uint4*>(Ks + row * D)[s];
+    };
+    auto v_word = [&](int t) {
+      const int row = t * C::RPS + rowsel;
+      if (isq) {
+        const uint2 vc = reinterpret_cast<const uint2*>(Vq + row * D)[s];
+        return make_uint4(vc.x, vc.y, static_cast<uint32_t>(Mq[2 * kPage + row]), 0u);
+      }
+      return reinterpret_cast<const uint4*>(Vs + row * D)[s];
+    };
+    auto issue_next = [&]() {
+      __syncwarp();
+      if (k + kNst < n_my) {
+        bool isq_n;
+        const int pid = page_id(k + kNst, isq_n);
+        if (lane == 0) {
+          fence_proxy_async();
+          issue(k + kNst, pid, isq_n);
+        }
+      }
+    };
+    uint4 kr[kRegStage ? C::RS : 1], vr[kRegStage ? C::RS : 1];
     int32_t er[C::VL];
     float ksu[C::VL];  // fp8 page: K scale of the row of each logit this lane holds after the reduction
-    if (isq) {
-      // codes of the lane's 8 columns in .x/.y, the V row's scale in vr[t].z
-      const uint8_t* Kq = stage;
-      const uint8_t* Vq = stage + C::QPAGE_BYTES;
-      const int32_t* Mq = reinterpret_cast<const int32_t*>(stage + 2 * C::QPAGE_BYTES);
+    if constexpr (kRegStage) {
 #pragma unroll
       for (int t = 0; t < C::RS; ++t) {
-        const int row = t * C::RPS + rowsel;
-        const uint2 kc = reinterpret_cast<const uint2*>(Kq + row * D)[s];
-        const uint2 vc = reinterpret_cast<const uint2*>(Vq + row * D)[s];
-        kr[t] = make_uint4(kc.x, kc.y, 0u, 0u);
-        vr[t] = make_uint4(vc.x, vc.y, static_cast<uint32_t>(Mq[2 * kPage + row]), 0u);
+        kr[t] = k_word(t);
+        vr[t] = v_word(t);
       }
+    }
+    if (isq) {
 #pragma unroll
       for (int u = 0; u < C::VL; ++u) {
         const int r = ((idx_base + u) % C::RS) * C::RPS + rowsel;
@@ -450,29 +480,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
       }
     } else {
 #pragma unroll
-      for (int t = 0; t < C::RS; ++t) {
-        kr[t] = reinterpret_cast<const uint4*>(Ks + (t * C::RPS + rowsel) * D)[s];
-        vr[t] = reinterpret_cast<const uint4*>(Vs + (t * C::RPS + rowsel) * D)[s];
-      }
-#pragma unroll
       for (int u = 0; u < C::VL; ++u) er[u] = Es[((idx_base + u) % C::RS) * C::RPS + rowsel];
     }
-    __syncwarp();
-    if (k + kNst < n_my) {
-      bool isq_n;
-      const int pid = page_id(k + kNst, isq_n);
-      if (lane == 0) {
-        fence_proxy_async();
-        issue(k + kNst, pid, isq_n);
-      }
-    }
+    if constexpr (kRegStage) issue_next();
 
     // ---- logits
     float part[C::V];
 #pragma unroll
     for (int t = 0; t < C::RS; ++t) {
       float kf[8];
-      if (isq) unpack_e4m3_8(kr[t].x, kr[t].y, kf); else unpack8(kr[t], kf);
+      uint4 kw;
+      if constexpr (kRegStage) kw = kr[t]; else kw = k_word(t);
+      if (isq) unpack_e4m3_8(kw.x, kw.y, kf); else unpack8(kw, kf);
 #pragma unroll
       for (int i = 0; i < G; ++i) {
         float a0 = 0.f, a1 = 0.f;
@@ -531,16 +550,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
 #pragma unroll
     for (int t = 0; t < C::RS; ++t) {
       float vf[8];
-      if (isq) unpack_e4m3_8(vr[t].x, vr[t].y, vf); else unpack8(vr[t], vf);
+      uint4 vw;
+      if constexpr (kRegStage) vw = vr[t]; else vw = v_word(t);
+      if (isq) unpack_e4m3_8(vw.x, vw.y, vf); else unpack8(vw, vf);
 #pragma unroll
       for (int i = 0; i < G; ++i) {
         const float pr = p_s[rowsel * G * C::RS + i * C::RS + t];
         l_run[i] += pr;
-        const float pw = isq ? pr * __uint_as_float(vr[t].z) : pr;
+        const float pw = isq ? pr * __uint_as_float(vw.z) : pr;
 #pragma unroll
         for (int e = 0; e < 8; e += 2) fma2(acc[i][e], acc[i][e + 1], pw, pw, vf[e], vf[e + 1]);
       }
     }
+    if constexpr (!kRegStage) issue_next();  // the stage is read for the last time above
 
     // ---- end of a (b, h) segment of this slice
     if (g + 1 == seg_end) {
@@ -785,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
         seg_end = min(pref[cbh + 1], r1);
         cnt = cnt_next;
         cnt_q = cnt_q_next;
+        if constexpr (G >= 8) load_q(cbh, qn);
 #pragma unroll
         for (int i = 0; i < G; ++i) {
           unpack8(qn[i], qf[i]);
@@ -792,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
           for (int e = 0; e < 8; ++e) qf[i][e] *= p.qscale;
         }
         if (seg_end < r1) {
-          load_q(next_bh(cbh), qn);
+          if constexpr (G < 8) load_q(next_bh(cbh), qn);
           cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
           if constexpr (kQ) cnt_q_next = clamp_count(p.count_q, next_bh(cbh), p.max_pages_q);
         }
