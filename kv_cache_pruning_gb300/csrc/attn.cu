@@ -172,6 +172,196 @@ KVP_DEV int slice_of(int g, int bh, int nw, int64_t c_end) {
   return static_cast<int>((2 * static_cast<int64_t>(g) + static_cast<int64_t>(kBoundaryCost) * bh) * nw / c_end);
 }
 
+// Merge of the npc partial states (acc, m, l) of (b, h) cbh, held in
+// consecutive workspace slots from s0, by the warp whose arrival completed
+// them: writes the output rows and resets the (b, h)'s counter. With `staged`
+// (the warp's page ring is idle, at the end of its slice) two bulk copies
+// bring every piece into the ring in one round trip; otherwise the lanes load
+// them from L2. Returns false if a bounded wait gave up.
+template <int D, int G>
+KVP_DEV bool merge_pieces(const AttnParams& p, int cbh, int npc, size_t s0, bool staged, uint8_t* ring,
+                          uint64_t* mbar, uint32_t& merge_par, int lane) {
+  // every piece of this (b, h) is written: merge them. Lanes take
+  // pieces for the maxima and weights (one round of loads for up to
+  // 32 pieces); then lanes take float4 columns of all G heads and the
+  // pieces go by in batches of 8 whose loads are all in flight at once.
+  fence_acq_rel_gpu();
+  constexpr int F4 = G * D / 4;           // float4 of one piece's acc
+  constexpr int FPL = (F4 + 31) / 32;     // ... per lane
+  constexpr int JB = 16 / FPL < 8 ? (16 / FPL > 0 ? 16 / FPL : 1) : 8;  // pieces per batch of loads
+  constexpr int kAccB = G * D * 4, kMlB = G * 2 * 4;  // bytes of a piece's acc and (m, l)
+  if (staged) {
+    // End of the slice: this warp's ring is idle. The pieces sit in
+    // consecutive slots, so two bulk copies bring every acc and every
+    // (m, l) into it in one round trip.
+    float* sacc = reinterpret_cast<float*>(ring);
+    uint8_t* sml_raw = ring + static_cast<size_t>(npc) * kAccB;
+    const size_t ml0 = s0 * kMlB, ml_a = ml0 & ~size_t(15);
+    const size_t ml_b = (ml0 + static_cast<size_t>(npc) * kMlB + 15) & ~size_t(15);
+    const float* sml = reinterpret_cast<const float*>(sml_raw + (ml0 - ml_a));
+    if (lane == 0) {
+      fence_proxy_async();
+      mbar_arrive_expect_tx(mbar, static_cast<uint32_t>(npc * kAccB + (ml_b - ml_a)));
+      bulk_g2s(sacc, p.part_acc + s0 * G * D, static_cast<uint32_t>(npc * kAccB), mbar);
+      bulk_g2s(sml_raw, reinterpret_cast<const uint8_t*>(p.part_ml) + ml_a, static_cast<uint32_t>(ml_b - ml_a),
+               mbar);
+    }
+    const bool okm = mbar_wait(mbar, merge_par, nullptr, p.status);
+    merge_par ^= 1u;
+    if (!__all_sync(0xffffffffu, okm)) {
+      if (lane == 0) record_error(p.status, KVP_ERR_TIMEOUT);
+      return false;
+    }
+    float M[G], wr[G], L[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const float m = lane < npc ? sml[lane * G * 2 + 2 * i] : -1e30f;
+      float mx = m;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      M[i] = mx;
+      wr[i] = lane < npc ? exp2f(m - mx) : 0.f;
+      float l = wr[i] * (lane < npc ? sml[lane * G * 2 + 2 * i + 1] : 0.f);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      L[i] = l;
+    }
+    float4 A[FPL];
+#pragma unroll
+    for (int k2 = 0; k2 < FPL; ++k2) A[k2] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < npc; ++j) {
+#pragma unroll
+      for (int k2 = 0; k2 < FPL; ++k2) {
+        constexpr int kHeadF4 = D / 4;
+        const int h0 = (32 * k2) / kHeadF4 < G ? (32 * k2) / kHeadF4 : G - 1;
+        float w = __shfl_sync(0xffffffffu, wr[h0], j);
+        if constexpr (kHeadF4 < 32) {
+          const int h1 = (32 * k2 + 16) / kHeadF4 < G ? (32 * k2 + 16) / kHeadF4 : G - 1;
+          const float w1 = __shfl_sync(0xffffffffu, wr[h1], j);
+          if (lane >= 16) w = w1;
+        }
+        const int f = lane + 32 * k2;
+        if (f < F4) {
+          const float4 v = reinterpret_cast<const float4*>(sacc + static_cast<size_t>(j) * G * D)[f];
+          A[k2].x = fmaf(w, v.x, A[k2].x);
+          A[k2].y = fmaf(w, v.y, A[k2].y);
+          A[k2].z = fmaf(w, v.z, A[k2].z);
+          A[k2].w = fmaf(w, v.w, A[k2].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int k2 = 0; k2 < FPL; ++k2) {
+      const int f = lane + 32 * k2;
+      if (f < F4) {
+        const int hd = f / (D / 4);
+        float Lh = L[0];
+#pragma unroll
+        for (int i = 1; i < G; ++i)
+          if (hd == i) Lh = L[i];
+        const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
+        reinterpret_cast<float4*>(p.out + static_cast<size_t>(cbh) * G * D)[f] =
+            make_float4(A[k2].x * inv, A[k2].y * inv, A[k2].z * inv, A[k2].w * inv);
+      }
+    }
+    if (lane == 0) p.pieces[cbh] = 0;
+    return true;
+  }
+  float M[G], mr[G], lr[G];
+#pragma unroll
+  for (int i = 0; i < G; ++i) M[i] = -1e30f;
+  for (int b0 = 0; b0 < npc; b0 += 32) {
+    const int pc = b0 + lane;
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      mr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2) : -1e30f;
+      lr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2 + 1) : 0.f;
+      M[i] = fmaxf(M[i], mr[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M[i] = fmaxf(M[i], __shfl_xor_sync(0xffffffffu, M[i], o));
+  }
+  float L[G];
+  float4 A[FPL];
+#pragma unroll
+  for (int i = 0; i < G; ++i) L[i] = 0.f;
+#pragma unroll
+  for (int k = 0; k < FPL; ++k) A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int b0 = 0; b0 < npc; b0 += 32) {
+    const int pc = b0 + lane;
+    if (npc > 32) {  // the registers hold the last chunk of the first pass
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        mr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2) : -1e30f;
+        lr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2 + 1) : 0.f;
+      }
+    }
+    float wr[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      wr[i] = pc < npc ? exp2f(mr[i] - M[i]) : 0.f;
+      L[i] = fmaf(wr[i], lr[i], L[i]);
+    }
+    const int nb = min(32, npc - b0);
+    for (int j0 = 0; j0 < nb; j0 += JB) {
+      float4 v[JB][FPL];
+#pragma unroll
+      for (int jj = 0; jj < JB; ++jj) {
+#pragma unroll
+        for (int k = 0; k < FPL; ++k) {
+          const int f = lane + 32 * k;
+          v[jj][k] = (j0 + jj < nb && f < F4)
+                         ? __ldcg(reinterpret_cast<const float4*>(p.part_acc + (s0 + b0 + j0 + jj) * G * D) + f)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < JB; ++jj) {
+        const int src = (j0 + jj) & 31;  // the lane that holds this piece's weights
+#pragma unroll
+        for (int k = 0; k < FPL; ++k) {
+          constexpr int kHeadF4 = D / 4;  // float4 per head row
+          const int h0 = (32 * k) / kHeadF4 < G ? (32 * k) / kHeadF4 : G - 1;
+          float w = __shfl_sync(0xffffffffu, wr[h0], src);
+          if constexpr (kHeadF4 < 32) {  // lanes 16-31 are on the next head
+            const int h1 = (32 * k + 16) / kHeadF4 < G ? (32 * k + 16) / kHeadF4 : G - 1;
+            const float w1 = __shfl_sync(0xffffffffu, wr[h1], src);
+            if (lane >= 16) w = w1;
+          }
+          A[k].x = fmaf(w, v[jj][k].x, A[k].x);
+          A[k].y = fmaf(w, v[jj][k].y, A[k].y);
+          A[k].z = fmaf(w, v[jj][k].z, A[k].z);
+          A[k].w = fmaf(w, v[jj][k].w, A[k].w);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L[i] += __shfl_xor_sync(0xffffffffu, L[i], o);
+  }
+#pragma unroll
+  for (int k = 0; k < FPL; ++k) {
+    const int f = lane + 32 * k;
+    if (f < F4) {
+      const int hd = f / (D / 4);
+      float Lh = L[0];
+#pragma unroll
+      for (int i = 1; i < G; ++i)
+        if (hd == i) Lh = L[i];
+      const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
+      reinterpret_cast<float4*>(p.out + static_cast<size_t>(cbh) * G * D)[f] =
+          make_float4(A[k].x * inv, A[k].y * inv, A[k].z * inv, A[k].w * inv);
+    }
+  }
+  if (lane == 0) p.pieces[cbh] = 0;
+  return true;
+}
+
 // kQ: the two-tier kernel. Each (b, h) then lists its bf16 pages and after
 // them its fp8-tier pages (quantize instead of drop): a fp8 page stages its K
 // and V codes and its per-slot record; a lane reads the 8 codes of the same 8
@@ -618,187 +808,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
         if (lane == 0) last = atomicAdd(&p.pieces[cbh], 1) == (w_last - w_first);
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
-          // every piece of this (b, h) is written: merge them. Lanes take
-          // pieces for the maxima and weights (one round of loads for up to
-          // 32 pieces); then lanes take float4 columns of all G heads and the
-          // pieces go by in batches of 8 whose loads are all in flight at once.
-          fence_acq_rel_gpu();
-          constexpr int F4 = G * D / 4;           // float4 of one piece's acc
-          constexpr int FPL = (F4 + 31) / 32;     // ... per lane
-          constexpr int JB = 16 / FPL < 8 ? (16 / FPL > 0 ? 16 / FPL : 1) : 8;  // pieces per batch of loads
           constexpr int kAccB = G * D * 4, kMlB = G * 2 * 4;  // bytes of a piece's acc and (m, l)
           constexpr int kStaged = (kNst * C::STAGE_BYTES - 32) / (kAccB + kMlB);  // pieces the idle ring holds
           const int npc = w_last - w_first + 1;
-          const size_t s0 = static_cast<size_t>(w_first) + cbh;
-          if (g + 1 == r1 && npc <= kStaged) {
-            // End of the slice: this warp's ring is idle. The pieces sit in
-            // consecutive slots, so two bulk copies bring every acc and every
-            // (m, l) into it in one round trip.
-            float* sacc = reinterpret_cast<float*>(ring);
-            uint8_t* sml_raw = ring + static_cast<size_t>(npc) * kAccB;
-            const size_t ml0 = s0 * kMlB, ml_a = ml0 & ~size_t(15);
-            const size_t ml_b = (ml0 + static_cast<size_t>(npc) * kMlB + 15) & ~size_t(15);
-            const float* sml = reinterpret_cast<const float*>(sml_raw + (ml0 - ml_a));
-            if (lane == 0) {
-              fence_proxy_async();
-              mbar_arrive_expect_tx(&bars[kNst], static_cast<uint32_t>(npc * kAccB + (ml_b - ml_a)));
-              bulk_g2s(sacc, p.part_acc + s0 * G * D, static_cast<uint32_t>(npc * kAccB), &bars[kNst]);
-              bulk_g2s(sml_raw, reinterpret_cast<const uint8_t*>(p.part_ml) + ml_a, static_cast<uint32_t>(ml_b - ml_a),
-                       &bars[kNst]);
-            }
-            const bool okm = mbar_wait(&bars[kNst], merge_par, nullptr, p.status);
-            merge_par ^= 1u;
-            if (!__all_sync(0xffffffffu, okm)) {
-              if (lane == 0) record_error(p.status, KVP_ERR_TIMEOUT);
-              return;
-            }
-            float M[G], wr[G], L[G];
-#pragma unroll
-            for (int i = 0; i < G; ++i) {
-              const float m = lane < npc ? sml[lane * G * 2 + 2 * i] : -1e30f;
-              float mx = m;
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-              M[i] = mx;
-              wr[i] = lane < npc ? exp2f(m - mx) : 0.f;
-              float l = wr[i] * (lane < npc ? sml[lane * G * 2 + 2 * i + 1] : 0.f);
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-              L[i] = l;
-            }
-            float4 A[FPL];
-#pragma unroll
-            for (int k2 = 0; k2 < FPL; ++k2) A[k2] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < npc; ++j) {
-#pragma unroll
-              for (int k2 = 0; k2 < FPL; ++k2) {
-                constexpr int kHeadF4 = D / 4;
-                const int h0 = (32 * k2) / kHeadF4 < G ? (32 * k2) / kHeadF4 : G - 1;
-                float w = __shfl_sync(0xffffffffu, wr[h0], j);
-                if constexpr (kHeadF4 < 32) {
-                  const int h1 = (32 * k2 + 16) / kHeadF4 < G ? (32 * k2 + 16) / kHeadF4 : G - 1;
-                  const float w1 = __shfl_sync(0xffffffffu, wr[h1], j);
-                  if (lane >= 16) w = w1;
-                }
-                const int f = lane + 32 * k2;
-                if (f < F4) {
-                  const float4 v = reinterpret_cast<const float4*>(sacc + static_cast<size_t>(j) * G * D)[f];
-                  A[k2].x = fmaf(w, v.x, A[k2].x);
-                  A[k2].y = fmaf(w, v.y, A[k2].y);
-                  A[k2].z = fmaf(w, v.z, A[k2].z);
-                  A[k2].w = fmaf(w, v.w, A[k2].w);
-                }
-              }
-            }
-#pragma unroll
-            for (int k2 = 0; k2 < FPL; ++k2) {
-              const int f = lane + 32 * k2;
-              if (f < F4) {
-                const int hd = f / (D / 4);
-                float Lh = L[0];
-#pragma unroll
-                for (int i = 1; i < G; ++i)
-                  if (hd == i) Lh = L[i];
-                const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
-                reinterpret_cast<float4*>(p.out + static_cast<size_t>(cbh) * G * D)[f] =
-                    make_float4(A[k2].x * inv, A[k2].y * inv, A[k2].z * inv, A[k2].w * inv);
-              }
-            }
-            if (lane == 0) p.pieces[cbh] = 0;
-            continue;  // the slice is done
-          }
-          float M[G], mr[G], lr[G];
-#pragma unroll
-          for (int i = 0; i < G; ++i) M[i] = -1e30f;
-          for (int b0 = 0; b0 < npc; b0 += 32) {
-            const int pc = b0 + lane;
-#pragma unroll
-            for (int i = 0; i < G; ++i) {
-              mr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2) : -1e30f;
-              lr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2 + 1) : 0.f;
-              M[i] = fmaxf(M[i], mr[i]);
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < G; ++i) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M[i] = fmaxf(M[i], __shfl_xor_sync(0xffffffffu, M[i], o));
-          }
-          float L[G];
-          float4 A[FPL];
-#pragma unroll
-          for (int i = 0; i < G; ++i) L[i] = 0.f;
-#pragma unroll
-          for (int k = 0; k < FPL; ++k) A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int b0 = 0; b0 < npc; b0 += 32) {
-            const int pc = b0 + lane;
-            if (npc > 32) {  // the registers hold the last chunk of the first pass
-#pragma unroll
-              for (int i = 0; i < G; ++i) {
-                mr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2) : -1e30f;
-                lr[i] = pc < npc ? __ldcg(p.part_ml + ((s0 + pc) * G + i) * 2 + 1) : 0.f;
-              }
-            }
-            float wr[G];
-#pragma unroll
-            for (int i = 0; i < G; ++i) {
-              wr[i] = pc < npc ? exp2f(mr[i] - M[i]) : 0.f;
-              L[i] = fmaf(wr[i], lr[i], L[i]);
-            }
-            const int nb = min(32, npc - b0);
-            for (int j0 = 0; j0 < nb; j0 += JB) {
-              float4 v[JB][FPL];
-#pragma unroll
-              for (int jj = 0; jj < JB; ++jj) {
-#pragma unroll
-                for (int k = 0; k < FPL; ++k) {
-                  const int f = lane + 32 * k;
-                  v[jj][k] = (j0 + jj < nb && f < F4)
-                                 ? __ldcg(reinterpret_cast<const float4*>(p.part_acc + (s0 + b0 + j0 + jj) * G * D) + f)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-              }
-#pragma unroll
-              for (int jj = 0; jj < JB; ++jj) {
-                const int src = (j0 + jj) & 31;  // the lane that holds this piece's weights
-#pragma unroll
-                for (int k = 0; k < FPL; ++k) {
-                  constexpr int kHeadF4 = D / 4;  // float4 per head row
-                  const int h0 = (32 * k) / kHeadF4 < G ? (32 * k) / kHeadF4 : G - 1;
-                  float w = __shfl_sync(0xffffffffu, wr[h0], src);
-                  if constexpr (kHeadF4 < 32) {  // lanes 16-31 are on the next head
-                    const int h1 = (32 * k + 16) / kHeadF4 < G ? (32 * k + 16) / kHeadF4 : G - 1;
-                    const float w1 = __shfl_sync(0xffffffffu, wr[h1], src);
-                    if (lane >= 16) w = w1;
-                  }
-                  A[k].x = fmaf(w, v[jj][k].x, A[k].x);
-                  A[k].y = fmaf(w, v[jj][k].y, A[k].y);
-                  A[k].z = fmaf(w, v[jj][k].z, A[k].z);
-                  A[k].w = fmaf(w, v[jj][k].w, A[k].w);
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < G; ++i) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) L[i] += __shfl_xor_sync(0xffffffffu, L[i], o);
-          }
-#pragma unroll
-          for (int k = 0; k < FPL; ++k) {
-            const int f = lane + 32 * k;
-            if (f < F4) {
-              const int hd = f / (D / 4);
-              float Lh = L[0];
-#pragma unroll
-              for (int i = 1; i < G; ++i)
-                if (hd == i) Lh = L[i];
-              const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
-              reinterpret_cast<float4*>(p.out + static_cast<size_t>(cbh) * G * D)[f] =
-                  make_float4(A[k].x * inv, A[k].y * inv, A[k].z * inv, A[k].w * inv);
-            }
-          }
-          if (lane == 0) p.pieces[cbh] = 0;
+          if (!merge_pieces<D, G>(p, cbh, npc, static_cast<size_t>(w_first) + cbh, g + 1 == r1 && npc <= kStaged,
+                                  ring, &bars[kNst], merge_par, lane))
+            return;
         }
       }
       // next segment
@@ -831,6 +846,481 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   }
 }
 
+// ---------------------------------------------------------------- tensor-core page math
+// The same persistent split-KV decode, with each page's two products on the
+// tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulate):
+//   S   = K Q^T    M = 16 tokens, N = 8 query heads of the kv head (G <= 8,
+//                  the rest zero), K = head_dim in steps of 16
+//   O^T = V^T P^T  M = 16 dims per step, N = 8 heads, K = the page's 16 tokens
+// K and V arrive as 16-row x 64-column boxes with the 128-byte swizzle, so the
+// ldmatrix reads (V transposed by the load itself) are free of bank
+// conflicts; P goes through 512 bytes of shared memory per warp, as a bf16
+// hi + lo pair (two products, about 16 bits of p), to become the second
+// product's B operand. A thread owns heads 2t and 2t+1 of both
+// results, so its softmax state and its output columns coincide.
+template <int D>
+struct MmaCfg {
+  static constexpr int NBOX = D / 64;                    // 64-column boxes per page of K (or V)
+  static constexpr int BOX_BYTES = kPage * 128;          // 16 rows x 128 bytes
+  static constexpr int PAGE_BYTES = NBOX * BOX_BYTES;
+  static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;     // K boxes, then V boxes
+  static constexpr int RING_BYTES = kWarps * kNst * STAGE_BYTES;
+  static constexpr int REC_WORDS = 3 * kPage;            // per stage: the page's 16 expire values
+  static constexpr int REC_BYTES = kWarps * kNst * REC_WORDS * 4;
+  static constexpr int PT_BYTES = kWarps * 2 * 8 * kPage * 2;  // per warp: P^T hi and lo, 8 heads x 16 tokens, bf16
+  static constexpr int BAR_BYTES = kWarps * (kNst + 1) * 8;
+  static constexpr int PREF_BYTES = (kMaxBH + 1) * 4;
+  static constexpr int SMEM = 1024 + RING_BYTES + REC_BYTES + PT_BYTES + BAR_BYTES + PREF_BYTES;
+  static_assert(PAGE_BYTES == kPage * D * 2, "a page is its boxes");
+  static_assert(STAGE_BYTES % 1024 == 0, "swizzled boxes start on 1024 bytes");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+KVP_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+KVP_DEV void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+// d += A B, A 16 x 16 (row), B 16 x 8 (col), bf16 in, fp32 accumulate
+KVP_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                            uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams p,
+                                                               const __grid_constant__ CUtensorMap tmK,
+                                                               const __grid_constant__ CUtensorMap tmV) {
+  using C = MmaCfg<D>;
+  constexpr bool kQ = false;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  pdl_launch_dependents();
+  pdl_wait();  // inputs (counts, pages, workspace counters) come from the kernels before this one
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = p.B * p.H;
+  uint8_t* ring = smem + warp * kNst * C::STAGE_BYTES;
+  int32_t* exp_s = reinterpret_cast<int32_t*>(smem + C::RING_BYTES) + warp * kNst * C::REC_WORDS;
+  uint16_t* pt_s = reinterpret_cast<uint16_t*>(smem + C::RING_BYTES + C::REC_BYTES) + warp * 2 * 8 * kPage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES + C::REC_BYTES + C::PT_BYTES) + warp * (kNst + 1);
+  int* pref = reinterpret_cast<int*>(smem + C::RING_BYTES + C::REC_BYTES + C::PT_BYTES + C::BAR_BYTES);
+  if (tid == 0) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+
+  // ---- page prefix over (b, h), identical in every CTA
+  {
+    __shared__ int wsum[kWarps];
+    __shared__ int carry;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < BH; base += kThreads) {
+      const int bh = base + tid;
+      int np = bh < BH ? (clamp_count(p.count, bh, p.max_pages) + kPage - 1) / kPage : 0;
+      if constexpr (kQ) np += bh < BH ? (clamp_count(p.count_q, bh, p.max_pages_q) + kPage - 1) / kPage : 0;
+      int incl = np;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      int before = carry;
+      for (int w = 0; w < warp; ++w) before += wsum[w];
+      if (bh < BH) pref[bh] = before + incl - np;
+      __syncthreads();
+      if (tid == 0) {
+        int t = 0;
+        for (int w = 0; w < kWarps; ++w) t += wsum[w];
+        carry += t;
+      }
+      __syncthreads();
+    }
+    if (tid == 0) pref[BH] = carry;
+    __syncthreads();
+  }
+  const int NP = pref[BH];
+
+  // ---- (b, h) without pages: zero output rows
+  for (int bh = blockIdx.x; bh < BH; bh += gridDim.x) {
+    if (pref[bh + 1] == pref[bh]) {
+      for (int i = tid; i < G * D; i += kThreads) p.out[static_cast<size_t>(bh) * G * D + i] = 0.f;
+    }
+  }
+  if (NP == 0) return;
+
+  // ---- this warp's slice of the global page list
+  // slices of at least min_pages pages (fewer pieces to merge on small
+  // problems); every one of the first NW slices is non-empty
+  const int nw_all = gridDim.x * kWarps;
+  const int min_pages = NP >= 64 * BH ? kMinPagesLong : kMinPagesShort;
+  const int NW = max(1, min(nw_all, NP / min_pages));
+  const int gw = warp * gridDim.x + blockIdx.x;  // slices go round-robin over the CTAs (all SMs busy)
+  if (gw >= NW) return;
+  int last_bh = 0;  // (b, h) of the last page
+  {
+    int a = 0, b = BH - 1;
+    while (a < b) {
+      const int mid = (a + b + 1) >> 1;
+      if (pref[mid] <= NP - 1) a = mid; else b = mid - 1;
+    }
+    last_bh = a;
+  }
+  const int64_t c_end = 2 * static_cast<int64_t>(NP - 1) + static_cast<int64_t>(kBoundaryCost) * last_bh + 1;
+  auto slice_start = [&](int w) {  // first page of slice w: the first page whose cost reaches ceil(w * c_end / NW)
+    const int64_t T = (static_cast<int64_t>(w) * c_end + NW - 1) / NW;
+    auto maxc = [&](int k) {
+      return 2 * static_cast<int64_t>(pref[k + 1] - 1) + static_cast<int64_t>(kBoundaryCost) * k;
+    };
+    if (maxc(BH - 1) < T) return NP;
+    int a = 0, b = BH - 1;
+    while (a < b) {
+      const int mid = (a + b) >> 1;
+      if (maxc(mid) >= T) b = mid; else a = mid + 1;
+    }
+    const int64_t g = (T - static_cast<int64_t>(kBoundaryCost) * a + 1) / 2;
+    return static_cast<int>(min(static_cast<int64_t>(NP), max(static_cast<int64_t>(pref[a]), g)));
+  };
+  const int r0 = slice_start(gw);
+  const int r1 = gw + 1 < NW ? slice_start(gw + 1) : NP;
+  if (r1 <= r0) return;  // an empty slice (between two (b, h) with empty ones in between)
+  const int n_my = r1 - r0;
+
+  // first (b, h) of the slice: the one whose page range holds page r0
+  int lo = 0, hi = BH - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= r0) lo = mid; else hi = mid - 1;
+  }
+  int cbh = lo;  // consumer cursor
+  while (pref[cbh + 1] <= r0) ++cbh;
+
+  // Page ids of the slice, 32 per register: lane j of block b holds the id of
+  // slice page 32*b + j. Block b+1 is loaded when issuing enters block b, so
+  // every id is in a register about 32 pages before lane 0 needs it.
+  // bit j of qb0 / qb1: slice page 32 * blk + j (blk even / odd) is a fp8-tier page
+  uint32_t qb0 = 0, qb1 = 0;
+  auto load_ids = [&](int blk, uint32_t& qbits) {  // all lanes call this
+    const int kk = blk * 32 + lane;
+    int id = -1;
+    bool isq = false;
+    if (kk < n_my) {
+      const int g = r0 + kk;
+      int a = 0, b = BH - 1;
+      while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (pref[mid] <= g) a = mid; else b = mid - 1;
+      }
+      const int li = g - pref[a];
+      if constexpr (kQ) {
+        const int na = (clamp_count(p.count, a, p.max_pages) + kPage - 1) / kPage;
+        isq = li >= na;
+        id = isq ? static_cast<int>(p.page_table_q[static_cast<int64_t>(a) * p.max_pages_q + (li - na)])
+                 : static_cast<int>(p.page_table[static_cast<int64_t>(a) * p.max_pages + li]);
+      } else {
+        id = static_cast<int>(p.page_table[static_cast<int64_t>(a) * p.max_pages + li]);
+      }
+    }
+    if constexpr (kQ) qbits = __ballot_sync(0xffffffffu, isq);
+    return id;
+  };
+  int ids0 = load_ids(0, qb0), ids1 = load_ids(1, qb1);
+  auto page_id = [&](int k, bool& isq) {  // all lanes call this
+    const int blk = k >> 5;
+    const int v = __shfl_sync(0xffffffffu, (blk & 1) ? ids1 : ids0, k & 31);
+    isq = kQ && ((((blk & 1) ? qb1 : qb0) >> (k & 31)) & 1u);
+    if ((k & 31) == 0 && k > 0) {  // block blk - 1 is done: its register takes block blk + 1
+      if (blk & 1) ids0 = load_ids(blk + 1, qb0); else ids1 = load_ids(blk + 1, qb1);
+    }
+    return v;
+  };
+  // A page's K and V rows arrive as 16-row x 64-column boxes with the
+  // 128-byte swizzle (tensor copies of the pools viewed as [pages x 16, D]);
+  // its 16 expire values go to the stage's record with a 1-D bulk copy.
+  auto issue = [&](int k, int64_t phys, bool) {  // lane 0
+    const int st = k % kNst;
+    uint8_t* dst = ring + st * C::STAGE_BYTES;
+    int32_t* rec = exp_s + st * C::REC_WORDS;
+    if (phys < 0 || phys >= p.n_pages_cap) {
+      // inconsistent page table: no copy; every slot of the page reads as gone
+      record_error(p.status, KVP_ERR_BOUNDS);
+      uint4* z = reinterpret_cast<uint4*>(dst);
+      for (int i = 0; i < C::STAGE_BYTES / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < kPage; ++i) rec[i] = 0;
+      mbar_arrive(&bars[st]);
+      return;
+    }
+    mbar_arrive_expect_tx(&bars[st], C::STAGE_BYTES + kPage * 4);
+    const int y = static_cast<int>(phys) * kPage;
+#pragma unroll
+    for (int j = 0; j < C::NBOX; ++j) {
+      tma_load_2d(dst + j * C::BOX_BYTES, &tmK, 64 * j, y, &bars[st]);
+      tma_load_2d(dst + C::PAGE_BYTES + j * C::BOX_BYTES, &tmV, 64 * j, y, &bars[st]);
+    }
+    bulk_g2s(rec, p.expire_pool + phys * kPage, kPage * 4, &bars[st]);
+  };
+  if (lane == 0) {
+    for (int st = 0; st <= kNst; ++st) mbar_init(&bars[st], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  for (int k = 0; k < n_my && k < kNst; ++k) {
+    bool isq;
+    const int pid = page_id(k, isq);
+    if (lane == 0) issue(k, pid, isq);
+  }
+  __syncwarp();
+
+  // ---- query rows of the kv head as mma B fragments (bf16, unscaled): thread
+  // (g, t) = (lane / 4, lane % 4) holds head g's dims 16 ks + 2t, +1 and
+  // 16 ks + 8 + 2t, +1; heads g >= G are zero
+  const int gq = lane >> 2, tq = lane & 3;
+  constexpr int KS = D / 16;  // k-steps of the logits, m-tiles of the output
+  auto load_qf = [&](int bh, uint32_t (&f)[KS][2]) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      f[ks][0] = 0u;
+      f[ks][1] = 0u;
+    }
+    if (gq < G) {
+      const uint16_t* qr = p.q + (static_cast<size_t>(bh) * G + gq) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        f[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qr + 16 * ks + 2 * tq));
+        f[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qr + 16 * ks + 8 + 2 * tq));
+      }
+    }
+  };
+  auto next_bh = [&](int bh) {  // next (b, h) that has pages
+    int n = bh + 1;
+    while (n < BH && pref[n + 1] == pref[n]) ++n;
+    return n;
+  };
+  uint32_t qf[KS][2], qn[KS][2];
+  load_qf(cbh, qf);
+  int seg_end = min(pref[cbh + 1], r1);
+  int cnt = clamp_count(p.count, cbh, p.max_pages);
+  int cnt_next = 0;
+  if (seg_end < r1) {
+    load_qf(next_bh(cbh), qn);
+    cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
+  }
+
+  // running state of heads 2t and 2t+1 (this thread's columns of both mma
+  // results): max, this thread's share of the sum (its tokens g and g+8),
+  // and O^T[dim 16 mt + g (+8)][head 2t (+1)]
+  float m2[2] = {-1e30f, -1e30f}, l2[2] = {0.f, 0.f};
+  float o[KS][4];
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+  const uint32_t ring_u32 = smem_u32(ring);
+  const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: the lane's matrix and row within it
+  uint32_t merge_par = 0;  // phase of this warp's merge barrier
+  for (int k = 0; k < n_my; ++k) {
+    const int g = r0 + k;
+    const int st = k % kNst;
+    const bool ok = mbar_wait(&bars[st], static_cast<uint32_t>((k / kNst) & 1), nullptr, p.status);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) record_error(p.status, KVP_ERR_TIMEOUT);
+      return;  // outputs of this call are unspecified after a timeout
+    }
+    const uint32_t kbase = ring_u32 + st * C::STAGE_BYTES;
+    const uint32_t vbase = kbase + C::PAGE_BYTES;
+    const int32_t* rec = exp_s + st * C::REC_WORDS;
+    const int slot0 = (g - pref[cbh]) * kPage;
+
+    // ---- S = K Q^T: 16 tokens x 8 heads; A = K from the swizzled boxes
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      // matrices: 0 rows 0-7 / 1 rows 8-15 of the k-step's first 8 dims, 2 / 3 of its second 8
+      const int r = (mi & 1) * 8 + ri;
+      const int chunk = (ks & 3) * 2 + (mi >> 1);
+      const uint32_t addr = kbase + (ks >> 2) * C::BOX_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(addr, a0, a1, a2, a3);
+      mma_bf16_16816(sacc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+    }
+
+    // ---- mask and online softmax (base 2, lazy rescaling) for tokens g, g+8
+    const int32_t e0 = rec[gq], e1 = rec[gq + 8];
+    const bool v0 = (slot0 + gq < cnt) && (p.now < e0);
+    const bool v1 = (slot0 + gq + 8 < cnt) && (p.now < e1);
+    float x[4];
+    x[0] = v0 ? sacc[0] * p.qscale : -INFINITY;
+    x[1] = v0 ? sacc[1] * p.qscale : -INFINITY;
+    x[2] = v1 ? sacc[2] * p.qscale : -INFINITY;
+    x[3] = v1 ? sacc[3] * p.qscale : -INFINITY;
+    const bool grow = x[0] > m2[0] + kLazyRescale || x[2] > m2[0] + kLazyRescale || x[1] > m2[1] + kLazyRescale ||
+                      x[3] > m2[1] + kLazyRescale;
+    if (__any_sync(0xffffffffu, grow)) {
+      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float n0 = fmaxf(m2[0], mx0), n1 = fmaxf(m2[1], mx1);
+      const float al0 = exp2f(m2[0] - n0), al1 = exp2f(m2[1] - n1);
+      m2[0] = n0;
+      m2[1] = n1;
+      l2[0] *= al0;
+      l2[1] *= al1;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
+    // p as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)): the P.V
+    // product keeps about 16 bits of p; the sum takes p itself
+    float pf[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pf[i] = exp2f(x[i] - m2[i & 1]);
+    l2[0] += pf[0] + pf[2];
+    l2[1] += pf[1] + pf[3];
+    // P^T through shared memory: pt_s[hi / lo][head][token]
+    const int tok[4] = {gq, gq, gq + 8, gq + 8};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(pf[i]);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(pf[i] - __bfloat162float(hi));
+      pt_s[(2 * tq + (i & 1)) * kPage + tok[i]] = __bfloat16_as_ushort(hi);
+      pt_s[8 * kPage + (2 * tq + (i & 1)) * kPage + tok[i]] = __bfloat16_as_ushort(lo);
+    }
+    __syncwarp();
+    const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPage + 2 * tq);
+    const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPage + 8 + 2 * tq);
+    const uint32_t pl0 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPage + gq * kPage + 2 * tq);
+    const uint32_t pl1 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPage + gq * kPage + 8 + 2 * tq);
+
+    // ---- O^T += V^T P^T: A = V^T from the swizzled boxes, transposed by ldmatrix
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      // matrices: 0 tokens 0-7 / dims +0, 1 tokens 0-7 / dims +8, 2 tokens 8-15 / +0, 3 tokens 8-15 / +8
+      const int r = (mi >> 1) * 8 + ri;
+      const int chunk = (mt & 3) * 2 + (mi & 1);
+      const uint32_t addr = vbase + (mt >> 2) * C::BOX_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_trans(addr, a0, a1, a2, a3);
+      mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+      mma_bf16_16816(o[mt], a0, a1, a2, a3, pl0, pl1);
+    }
+    __syncwarp();  // every lane is done with the stage and with pt_s
+    if (k + kNst < n_my) {
+      bool isq_n;
+      const int pid = page_id(k + kNst, isq_n);
+      if (lane == 0) {
+        fence_proxy_async();
+        issue(k + kNst, pid, isq_n);
+      }
+    }
+
+    // ---- end of a (b, h) segment of this slice
+    if (g + 1 == seg_end) {
+      float lt0 = l2[0], lt1 = l2[1];
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {  // the sum over this warp's tokens
+        lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
+        lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
+      }
+      const int h0 = 2 * tq, h1 = 2 * tq + 1;
+      const bool whole = pref[cbh] >= r0 && pref[cbh + 1] <= r1;
+      if (whole) {
+        const float i0 = lt0 > 0.f ? 1.f / lt0 : 0.f, i1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
+        float* ob = p.out + static_cast<size_t>(cbh) * G * D;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          const int d0 = 16 * mt + gq;
+          if (h0 < G) {
+            ob[h0 * D + d0] = o[mt][0] * i0;
+            ob[h0 * D + d0 + 8] = o[mt][2] * i0;
+          }
+          if (h1 < G) {
+            ob[h1 * D + d0] = o[mt][1] * i1;
+            ob[h1 * D + d0 + 8] = o[mt][3] * i1;
+          }
+        }
+      } else {
+        const int w_first = slice_of(pref[cbh], cbh, NW, c_end);
+        const int w_last = slice_of(pref[cbh + 1] - 1, cbh, NW, c_end);
+        const size_t slot = static_cast<size_t>(gw) + cbh;
+        float* pa = p.part_acc + slot * G * D;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          const int d0 = 16 * mt + gq;
+          if (h0 < G) {
+            pa[h0 * D + d0] = o[mt][0];
+            pa[h0 * D + d0 + 8] = o[mt][2];
+          }
+          if (h1 < G) {
+            pa[h1 * D + d0] = o[mt][1];
+            pa[h1 * D + d0 + 8] = o[mt][3];
+          }
+        }
+        if (gq == 0) {
+          if (h0 < G) {
+            p.part_ml[(slot * G + h0) * 2] = m2[0];
+            p.part_ml[(slot * G + h0) * 2 + 1] = lt0;
+          }
+          if (h1 < G) {
+            p.part_ml[(slot * G + h1) * 2] = m2[1];
+            p.part_ml[(slot * G + h1) * 2 + 1] = lt1;
+          }
+        }
+        fence_acq_rel_gpu();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&p.pieces[cbh], 1) == (w_last - w_first);
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          constexpr int kAccB = G * D * 4, kMlB = G * 2 * 4;  // bytes of a piece's acc and (m, l)
+          constexpr int kStaged = (kNst * C::STAGE_BYTES - 32) / (kAccB + kMlB);  // pieces the idle ring holds
+          const int npc = w_last - w_first + 1;
+          if (!merge_pieces<D, G>(p, cbh, npc, static_cast<size_t>(w_first) + cbh, g + 1 == r1 && npc <= kStaged,
+                                  ring, &bars[kNst], merge_par, lane))
+            return;
+        }
+      }
+      // next segment
+      if (g + 1 < r1) {
+        cbh = next_bh(cbh);
+        seg_end = min(pref[cbh + 1], r1);
+        cnt = cnt_next;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          qf[ks][0] = qn[ks][0];
+          qf[ks][1] = qn[ks][1];
+        }
+        if (seg_end < r1) {
+          load_qf(next_bh(cbh), qn);
+          cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
+        }
+        m2[0] = m2[1] = -1e30f;
+        l2[0] = l2[1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      }
+    }
+  }
+}
+
 // Grid of the persistent kernel on this process's device: one CTA per SM
 // times the CTAs an SM holds, computed once (with the shared-memory opt-in).
 template <int D, int G, bool kQ>
@@ -858,6 +1348,49 @@ kvp_status launch_attn(const AttnParams& p, int grid_limit, cudaStream_t st) {
   if (launch_pdl(attn_decode_kernel<D, G, kQ>, dim3(grid), dim3(kThreads), C::SMEM, st, p) != cudaSuccess)
     return KVP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+template <int D, int G>
+int attn_mma_grid() {
+  static const int grid = [] {
+    using C = MmaCfg<D>;
+    auto kern = attn_mma_kernel<D, G>;
+    int dev = 0, nsm = 0, occ = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess ||
+        cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, C::SMEM) != cudaSuccess || occ <= 0)
+      return 0;
+    return nsm * occ < kMaxCtas ? nsm * occ : kMaxCtas;
+  }();
+  return grid;
+}
+
+template <int D, int G>
+kvp_status launch_attn_mma(const AttnParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int grid_limit,
+                           cudaStream_t st) {
+  using C = MmaCfg<D>;
+  int grid = attn_mma_grid<D, G>();
+  if (grid <= 0) return KVP_ERR_CUDA;
+  if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
+  if (launch_pdl(attn_mma_kernel<D, G>, dim3(grid), dim3(kThreads), C::SMEM, st, p, tmK, tmV) != cudaSuccess)
+    return KVP_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+template <int D>
+kvp_status dispatch_mma(const AttnParams& p, int G, int grid_limit, cudaStream_t st) {
+  CUtensorMap tmK, tmV;
+  const int64_t rows = static_cast<int64_t>(p.n_pages_cap) * kPage;
+  if (!make_tmap_bf16(&tmK, p.k_pool, rows, D, D, kPage, 64) || !make_tmap_bf16(&tmV, p.v_pool, rows, D, D, kPage, 64))
+    return KVP_ERR_CUDA;
+  switch (G) {
+    case 1: return launch_attn_mma<D, 1>(p, tmK, tmV, grid_limit, st);
+    case 2: return launch_attn_mma<D, 2>(p, tmK, tmV, grid_limit, st);
+    case 4: return launch_attn_mma<D, 4>(p, tmK, tmV, grid_limit, st);
+    case 8: return launch_attn_mma<D, 8>(p, tmK, tmV, grid_limit, st);
+    default: return KVP_ERR_UNSUPPORTED;
+  }
 }
 
 template <int D, bool kQ>
@@ -970,6 +1503,8 @@ kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_d
                qt ? qt->n_pages_cap : 0};
   if (qt != nullptr)
     return head_dim == 128 ? dispatch_g<128, true>(p, G, grid_limit, st) : dispatch_g<64, true>(p, G, grid_limit, st);
+  if (n_pages_cap > 0 && static_cast<int64_t>(n_pages_cap) * kPage <= 0x7fffffff)
+    return head_dim == 128 ? dispatch_mma<128>(p, G, grid_limit, st) : dispatch_mma<64>(p, G, grid_limit, st);
   return head_dim == 128 ? dispatch_g<128, false>(p, G, grid_limit, st) : dispatch_g<64, false>(p, G, grid_limit, st);
 }
 }  // namespace

@@ -755,8 +755,8 @@ def test_decode_attn_two_tier(kvp, B, T, H, G, d, pps):
 
 def test_decode_attn_two_tier_visibility_and_empty_tier(kvp):
     """Before any fp8 entry's start step the result is the bf16 tier's alone;
-    with an empty fp8 tier the two-tier kernel equals kvp_decode_attn bit for
-    bit (the same page list and partition)."""
+    with an empty fp8 tier the two-tier kernel (CUDA-core page math) agrees
+    with kvp_decode_attn (tensor-core page math) to fp32 rounding."""
     B, T, H, G, d = 2, 1200, 4, 4, 128
     out, ref, _ = _two_tier_case(kvp, B, T, H, G, d, now=100)   # now < 0 + window: no fp8 slot visible
     check_attention(out.cpu().numpy(), ref)
@@ -764,7 +764,7 @@ def test_decode_attn_two_tier_visibility_and_empty_tier(kvp):
     assert int(cq.count.sum()) == 0
     one = kvp.kvp_decode_attn(qd, ca, now, status=st)
     torch.cuda.synchronize()
-    assert torch.equal(out, one)
+    np.testing.assert_allclose(out.cpu().numpy(), one.cpu().numpy(), rtol=0, atol=2e-5)
     check_attention(out.cpu().numpy(), ref)
 
 
