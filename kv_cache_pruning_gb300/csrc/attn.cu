@@ -871,6 +871,9 @@ struct MmaCfg {
   static constexpr int BAR_BYTES = kWarps * (kNst + 1) * 8;
   static constexpr int PREF_BYTES = (kMaxBH + 1) * 4;
   static constexpr int SMEM = 1024 + RING_BYTES + REC_BYTES + PT_BYTES + BAR_BYTES + PREF_BYTES;
+  static constexpr int QPAGE_BYTES = kPage * D;         // fp8 tier: E4M3 codes of a page's K (or V) rows
+  static constexpr int QK_OFF = STAGE_BYTES - 2 * QPAGE_BYTES;  // where the codes land (upper half)
+  static constexpr int QV_OFF = STAGE_BYTES - QPAGE_BYTES;
   static_assert(PAGE_BYTES == kPage * D * 2, "a page is its boxes");
   static_assert(STAGE_BYTES % 1024 == 0, "swizzled boxes start on 1024 bytes");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -888,6 +891,28 @@ KVP_DEV void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& 
                : "r"(addr)
                : "memory");
 }
+// d += A B, A 16 x 16 (row), B 16 x 8 (col), fp16 in, fp32 accumulate
+KVP_DEV void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                           uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// two E4M3 codes (low byte first) -> fp16x2, exactly
+KVP_DEV uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+KVP_DEV uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+KVP_DEV uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 // d += A B, A 16 x 16 (row), B 16 x 8 (col), bf16 in, fp32 accumulate
 KVP_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                             uint32_t b1) {
@@ -898,12 +923,17 @@ KVP_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int D, int G>
+// kQ: the two-tier kernel. A fp8-tier page arrives as its E4M3 codes (1-D
+// bulk copies into the upper half of the stage) and its record (start steps,
+// K and V row scales); the warp turns the codes into fp16 in the same
+// swizzled layout (exactly: every E4M3 value is an fp16 value) and the page
+// goes through fp16 products, the query rows converted to fp16, the K row
+// scale applied to S and the V row scale folded into p.
+template <int D, int G, bool kQ>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap tmK,
                                                                const __grid_constant__ CUtensorMap tmV) {
   using C = MmaCfg<D>;
-  constexpr bool kQ = false;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   pdl_launch_dependents();
@@ -1050,17 +1080,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   // A page's K and V rows arrive as 16-row x 64-column boxes with the
   // 128-byte swizzle (tensor copies of the pools viewed as [pages x 16, D]);
   // its 16 expire values go to the stage's record with a 1-D bulk copy.
-  auto issue = [&](int k, int64_t phys, bool) {  // lane 0
+  auto issue = [&](int k, int64_t phys, bool isq) {  // lane 0
     const int st = k % kNst;
     uint8_t* dst = ring + st * C::STAGE_BYTES;
     int32_t* rec = exp_s + st * C::REC_WORDS;
-    if (phys < 0 || phys >= p.n_pages_cap) {
+    if (phys < 0 || phys >= (isq ? p.n_pages_cap_q : p.n_pages_cap)) {
       // inconsistent page table: no copy; every slot of the page reads as gone
       record_error(p.status, KVP_ERR_BOUNDS);
       uint4* z = reinterpret_cast<uint4*>(dst);
       for (int i = 0; i < C::STAGE_BYTES / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
-      for (int i = 0; i < kPage; ++i) rec[i] = 0;
+      for (int i = 0; i < C::REC_WORDS; ++i) rec[i] = (isq && i < kPage) ? kNever : 0;
       mbar_arrive(&bars[st]);
+      return;
+    }
+    if (kQ && isq) {
+      mbar_arrive_expect_tx(&bars[st], 2 * C::QPAGE_BYTES + C::REC_WORDS * 4);
+      bulk_g2s(dst + C::QK_OFF, p.kq_pool + phys * C::QPAGE_BYTES, C::QPAGE_BYTES, &bars[st]);
+      bulk_g2s(dst + C::QV_OFF, p.vq_pool + phys * C::QPAGE_BYTES, C::QPAGE_BYTES, &bars[st]);
+      bulk_g2s(rec, p.meta_pool + phys * C::REC_WORDS, C::REC_WORDS * 4, &bars[st]);
       return;
     }
     mbar_arrive_expect_tx(&bars[st], C::STAGE_BYTES + kPage * 4);
@@ -1114,9 +1151,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   int seg_end = min(pref[cbh + 1], r1);
   int cnt = clamp_count(p.count, cbh, p.max_pages);
   int cnt_next = 0;
+  int cnt_q = kQ ? clamp_count(p.count_q, cbh, p.max_pages_q) : 0;  // fp8-tier slots of this (b, h)
+  int cnt_q_next = 0;
   if (seg_end < r1) {
     load_qf(next_bh(cbh), qn);
     cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
+    if constexpr (kQ) cnt_q_next = clamp_count(p.count_q, next_bh(cbh), p.max_pages_q);
   }
 
   // running state of heads 2t and 2t+1 (this thread's columns of both mma
@@ -1141,7 +1181,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     const uint32_t kbase = ring_u32 + st * C::STAGE_BYTES;
     const uint32_t vbase = kbase + C::PAGE_BYTES;
     const int32_t* rec = exp_s + st * C::REC_WORDS;
-    const int slot0 = (g - pref[cbh]) * kPage;
+    const int li = g - pref[cbh];
+    const int na_cur = (cnt + kPage - 1) / kPage;  // bf16 pages of this (b, h)
+    const bool isq = kQ && li >= na_cur;           // a fp8-tier page (uniform in the warp)
+    const int slot0 = (isq ? li - na_cur : li) * kPage;
+
+    if (isq) {
+      // codes -> fp16 in the swizzled box layout. K codes sit above the K
+      // boxes' bytes; V codes sit inside the V boxes' bytes, so every lane
+      // reads its V codes before any V box is written.
+      uint8_t* stg = ring + st * C::STAGE_BYTES;
+      constexpr int CPR = D / 8;                 // 16-byte fp16 chunks per row
+      constexpr int NCH = kPage * CPR / 32;      // chunks per lane (K, and again V)
+      uint2 vc[NCH];
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int ci = lane + 32 * i, r = ci / CPR, c = ci - r * CPR;
+        vc[i] = *reinterpret_cast<const uint2*>(stg + C::QV_OFF + r * D + c * 8);
+      }
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int ci = lane + 32 * i, r = ci / CPR, c = ci - r * CPR;
+        const uint2 kc = *reinterpret_cast<const uint2*>(stg + C::QK_OFF + r * D + c * 8);
+        const uint4 h = make_uint4(e4m3x2_to_f16x2(kc.x), e4m3x2_to_f16x2(kc.x >> 16), e4m3x2_to_f16x2(kc.y),
+                                   e4m3x2_to_f16x2(kc.y >> 16));
+        *reinterpret_cast<uint4*>(stg + (c >> 3) * C::BOX_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = h;
+      }
+      __syncwarp();  // every lane has read its K codes, which the V boxes overwrite
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int ci = lane + 32 * i, r = ci / CPR, c = ci - r * CPR;
+        const uint4 h = make_uint4(e4m3x2_to_f16x2(vc[i].x), e4m3x2_to_f16x2(vc[i].x >> 16),
+                                   e4m3x2_to_f16x2(vc[i].y), e4m3x2_to_f16x2(vc[i].y >> 16));
+        *reinterpret_cast<uint4*>(stg + C::PAGE_BYTES + (c >> 3) * C::BOX_BYTES + r * 128 +
+                                  (((c & 7) ^ (r & 7)) << 4)) = h;
+      }
+      __syncwarp();
+    }
 
     // ---- S = K Q^T: 16 tokens x 8 heads; A = K from the swizzled boxes
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1153,18 +1229,64 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
       const uint32_t addr = kbase + (ks >> 2) * C::BOX_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4);
       uint32_t a0, a1, a2, a3;
       ldsm_x4(addr, a0, a1, a2, a3);
-      mma_bf16_16816(sacc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      if (isq)
+        mma_f16_16816(sacc, a0, a1, a2, a3, bf16x2_to_f16x2(qf[ks][0]), bf16x2_to_f16x2(qf[ks][1]));
+      else
+        mma_bf16_16816(sacc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+    }
+
+    // ---- V^T fragments: A of the second product, read transposed by ldmatrix
+    // from the swizzled boxes. For G <= 4 all of them go to registers now and
+    // the stage is handed back before the softmax, so the ring keeps kNst pages
+    // in flight; G = 8 needs those registers and reads them after the softmax.
+    constexpr bool kEarly = G <= 4;
+    auto v_frag = [&](int mt, uint32_t (&a)[4]) {
+      // matrices: 0 tokens 0-7 / dims +0, 1 tokens 0-7 / dims +8, 2 tokens 8-15 / +0, 3 tokens 8-15 / +8
+      const int r = (mi >> 1) * 8 + ri;
+      const int chunk = (mt & 3) * 2 + (mi & 1);
+      const uint32_t addr = vbase + (mt >> 2) * C::BOX_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4);
+      ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
+    };
+    uint32_t va[kEarly ? KS : 1][4];
+    const int32_t e0 = rec[gq], e1 = rec[gq + 8];
+    const float ks0 = isq ? __int_as_float(rec[kPage + gq]) : 1.f;
+    const float ks1 = isq ? __int_as_float(rec[kPage + gq + 8]) : 1.f;
+    const float vs0 = isq ? __int_as_float(rec[2 * kPage + gq]) : 1.f;
+    const float vs1 = isq ? __int_as_float(rec[2 * kPage + gq + 8]) : 1.f;
+    auto issue_next = [&]() {
+      __syncwarp();  // every lane is done with the stage
+      if (k + kNst < n_my) {
+        bool isq_n;
+        const int pid = page_id(k + kNst, isq_n);
+        if (lane == 0) {
+          fence_proxy_async();
+          issue(k + kNst, pid, isq_n);
+        }
+      }
+    };
+    if constexpr (kEarly) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) v_frag(mt, va[mt]);
+      issue_next();
     }
 
     // ---- mask and online softmax (base 2, lazy rescaling) for tokens g, g+8
-    const int32_t e0 = rec[gq], e1 = rec[gq + 8];
-    const bool v0 = (slot0 + gq < cnt) && (p.now < e0);
-    const bool v1 = (slot0 + gq + 8 < cnt) && (p.now < e1);
+    bool v0, v1;
+    float sc0 = p.qscale, sc1 = p.qscale;
+    if (isq) {  // fp8 slots count once now >= start; the K row scales apply to S
+      v0 = (slot0 + gq < cnt_q) && (p.now >= e0);
+      v1 = (slot0 + gq + 8 < cnt_q) && (p.now >= e1);
+      sc0 *= ks0;
+      sc1 *= ks1;
+    } else {
+      v0 = (slot0 + gq < cnt) && (p.now < e0);
+      v1 = (slot0 + gq + 8 < cnt) && (p.now < e1);
+    }
     float x[4];
-    x[0] = v0 ? sacc[0] * p.qscale : -INFINITY;
-    x[1] = v0 ? sacc[1] * p.qscale : -INFINITY;
-    x[2] = v1 ? sacc[2] * p.qscale : -INFINITY;
-    x[3] = v1 ? sacc[3] * p.qscale : -INFINITY;
+    x[0] = v0 ? sacc[0] * sc0 : -INFINITY;
+    x[1] = v0 ? sacc[1] * sc0 : -INFINITY;
+    x[2] = v1 ? sacc[2] * sc1 : -INFINITY;
+    x[3] = v1 ? sacc[3] * sc1 : -INFINITY;
     const bool grow = x[0] > m2[0] + kLazyRescale || x[2] > m2[0] + kLazyRescale || x[1] > m2[1] + kLazyRescale ||
                       x[3] > m2[1] + kLazyRescale;
     if (__any_sync(0xffffffffu, grow)) {
@@ -1188,8 +1310,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
         o[mt][3] *= al1;
       }
     }
-    // p as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)): the P.V
-    // product keeps about 16 bits of p; the sum takes p itself
+    // p as a bf16 (fp16 on a fp8 page) pair hi + lo: the P.V product keeps
+    // about 16 bits of p; the sum takes p itself. On a fp8 page the V row
+    // scale multiplies p for the product.
     float pf[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) pf[i] = exp2f(x[i] - m2[i & 1]);
@@ -1199,10 +1322,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     const int tok[4] = {gq, gq, gq + 8, gq + 8};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat16 hi = __float2bfloat16_rn(pf[i]);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(pf[i] - __bfloat162float(hi));
-      pt_s[(2 * tq + (i & 1)) * kPage + tok[i]] = __bfloat16_as_ushort(hi);
-      pt_s[8 * kPage + (2 * tq + (i & 1)) * kPage + tok[i]] = __bfloat16_as_ushort(lo);
+      uint16_t hb, lb;
+      if (isq) {
+        const float pv = pf[i] * ((i < 2) ? vs0 : vs1);
+        const __half hi = __float2half_rn(pv);
+        const __half lo = __float2half_rn(pv - __half2float(hi));
+        hb = __half_as_ushort(hi);
+        lb = __half_as_ushort(lo);
+      } else {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(pf[i]);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(pf[i] - __bfloat162float(hi));
+        hb = __bfloat16_as_ushort(hi);
+        lb = __bfloat16_as_ushort(lo);
+      }
+      pt_s[(2 * tq + (i & 1)) * kPage + tok[i]] = hb;
+      pt_s[8 * kPage + (2 * tq + (i & 1)) * kPage + tok[i]] = lb;
     }
     __syncwarp();
     const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPage + 2 * tq);
@@ -1210,27 +1344,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     const uint32_t pl0 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPage + gq * kPage + 2 * tq);
     const uint32_t pl1 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPage + gq * kPage + 8 + 2 * tq);
 
-    // ---- O^T += V^T P^T: A = V^T from the swizzled boxes, transposed by ldmatrix
+    // ---- O^T += V^T P^T
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
-      // matrices: 0 tokens 0-7 / dims +0, 1 tokens 0-7 / dims +8, 2 tokens 8-15 / +0, 3 tokens 8-15 / +8
-      const int r = (mi >> 1) * 8 + ri;
-      const int chunk = (mt & 3) * 2 + (mi & 1);
-      const uint32_t addr = vbase + (mt >> 2) * C::BOX_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4);
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4_trans(addr, a0, a1, a2, a3);
-      mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
-      mma_bf16_16816(o[mt], a0, a1, a2, a3, pl0, pl1);
-    }
-    __syncwarp();  // every lane is done with the stage and with pt_s
-    if (k + kNst < n_my) {
-      bool isq_n;
-      const int pid = page_id(k + kNst, isq_n);
-      if (lane == 0) {
-        fence_proxy_async();
-        issue(k + kNst, pid, isq_n);
+      uint32_t a[4];
+      if constexpr (kEarly) {
+        a[0] = va[mt][0];
+        a[1] = va[mt][1];
+        a[2] = va[mt][2];
+        a[3] = va[mt][3];
+      } else {
+        v_frag(mt, a);
+      }
+      if (isq) {
+        mma_f16_16816(o[mt], a[0], a[1], a[2], a[3], pb0, pb1);
+        mma_f16_16816(o[mt], a[0], a[1], a[2], a[3], pl0, pl1);
+      } else {
+        mma_bf16_16816(o[mt], a[0], a[1], a[2], a[3], pb0, pb1);
+        mma_bf16_16816(o[mt], a[0], a[1], a[2], a[3], pl0, pl1);
       }
     }
+    if constexpr (!kEarly) issue_next();
+    __syncwarp();  // pt_s is rewritten by the next page
 
     // ---- end of a (b, h) segment of this slice
     if (g + 1 == seg_end) {
@@ -1303,6 +1438,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
         cbh = next_bh(cbh);
         seg_end = min(pref[cbh + 1], r1);
         cnt = cnt_next;
+        cnt_q = cnt_q_next;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           qf[ks][0] = qn[ks][0];
@@ -1311,6 +1447,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
         if (seg_end < r1) {
           load_qf(next_bh(cbh), qn);
           cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
+          if constexpr (kQ) cnt_q_next = clamp_count(p.count_q, next_bh(cbh), p.max_pages_q);
         }
         m2[0] = m2[1] = -1e30f;
         l2[0] = l2[1] = 0.f;
@@ -1350,11 +1487,11 @@ kvp_status launch_attn(const AttnParams& p, int grid_limit, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
-template <int D, int G>
+template <int D, int G, bool kQ>
 int attn_mma_grid() {
   static const int grid = [] {
     using C = MmaCfg<D>;
-    auto kern = attn_mma_kernel<D, G>;
+    auto kern = attn_mma_kernel<D, G, kQ>;
     int dev = 0, nsm = 0, occ = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess ||
         cudaGetDevice(&dev) != cudaSuccess ||
@@ -1366,31 +1503,26 @@ int attn_mma_grid() {
   return grid;
 }
 
-template <int D, int G>
+template <int D, int G, bool kQ>
 kvp_status launch_attn_mma(const AttnParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int grid_limit,
                            cudaStream_t st) {
   using C = MmaCfg<D>;
-  int grid = attn_mma_grid<D, G>();
+  int grid = attn_mma_grid<D, G, kQ>();
   if (grid <= 0) return KVP_ERR_CUDA;
   if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
-  if (launch_pdl(attn_mma_kernel<D, G>, dim3(grid), dim3(kThreads), C::SMEM, st, p, tmK, tmV) != cudaSuccess)
+  if (launch_pdl(attn_mma_kernel<D, G, kQ>, dim3(grid), dim3(kThreads), C::SMEM, st, p, tmK, tmV) != cudaSuccess)
     return KVP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
-template <int D>
+template <int D, bool kQ>
 kvp_status dispatch_mma(const AttnParams& p, int G, int grid_limit, cudaStream_t st) {
   CUtensorMap tmK, tmV;
   const int64_t rows = static_cast<int64_t>(p.n_pages_cap) * kPage;
   if (!make_tmap_bf16(&tmK, p.k_pool, rows, D, D, kPage, 64) || !make_tmap_bf16(&tmV, p.v_pool, rows, D, D, kPage, 64))
     return KVP_ERR_CUDA;
-  switch (G) {
-    case 1: return launch_attn_mma<D, 1>(p, tmK, tmV, grid_limit, st);
-    case 2: return launch_attn_mma<D, 2>(p, tmK, tmV, grid_limit, st);
-    case 4: return launch_attn_mma<D, 4>(p, tmK, tmV, grid_limit, st);
-    case 8: return launch_attn_mma<D, 8>(p, tmK, tmV, grid_limit, st);
-    default: return KVP_ERR_UNSUPPORTED;
-  }
+  if (G != 8) return KVP_ERR_UNSUPPORTED;
+  return launch_attn_mma<D, 8, kQ>(p, tmK, tmV, grid_limit, st);
 }
 
 template <int D, bool kQ>
@@ -1501,10 +1633,21 @@ kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_d
                qt ? qt->count : nullptr,
                qt ? qt->max_pages : 0,
                qt ? qt->n_pages_cap : 0};
-  if (qt != nullptr)
+  // Eight query heads per kv head go to the tensor-core kernel: with the
+  // CUDA-core page math a page takes twice the multiply-adds of G = 4 and the
+  // kernel is bound by instruction issue (measured on a GB300, Llama-3-8B
+  // cache, keep-all: 192 against 95 us). Up to four the CUDA-core kernel is as
+  // fast or faster (75 % pruned at G = 4: 34.1 against 34.5 us; the fp8 tier:
+  // 65 against 69 us at a quarter of the entries). The tensor-core kernel reads
+  // the pools through tensor maps, whose row coordinates stay below 2^31.
+  const bool mma = G == 8 && n_pages_cap > 0 && static_cast<int64_t>(n_pages_cap) * kPage <= 0x7fffffff;
+  if (qt != nullptr) {
+    if (mma)
+      return head_dim == 128 ? dispatch_mma<128, true>(p, G, grid_limit, st) : dispatch_mma<64, true>(p, G, grid_limit, st);
     return head_dim == 128 ? dispatch_g<128, true>(p, G, grid_limit, st) : dispatch_g<64, true>(p, G, grid_limit, st);
-  if (n_pages_cap > 0 && static_cast<int64_t>(n_pages_cap) * kPage <= 0x7fffffff)
-    return head_dim == 128 ? dispatch_mma<128>(p, G, grid_limit, st) : dispatch_mma<64>(p, G, grid_limit, st);
+  }
+  if (mma)
+    return head_dim == 128 ? dispatch_mma<128, false>(p, G, grid_limit, st) : dispatch_mma<64, false>(p, G, grid_limit, st);
   return head_dim == 128 ? dispatch_g<128, false>(p, G, grid_limit, st) : dispatch_g<64, false>(p, G, grid_limit, st);
 }
 }  // namespace
