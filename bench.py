@@ -281,9 +281,10 @@ def run_gpu(args, rank: int, world: int):
     n_pages_cap = B * H * max_pages
     cache = kvp.PagedKV.allocate(B, H, d, n_pages_cap, max_pages, device=dev)
     scores = torch.empty(n_tok, H, dtype=torch.float32, device=dev)
-    expire = torch.empty(B, H, T, dtype=torch.int32, device=dev)
-    bits = torch.empty(B, H, (T + 31) // 32, dtype=torch.int32, device=dev)
-    count = torch.empty(B, H, dtype=torch.int32, device=dev)
+    separate = args.mask == "separate"  # the mask's own outputs exist only when it runs as its own kernel
+    expire = torch.empty(B, H, T, dtype=torch.int32, device=dev) if separate else None
+    bits = torch.empty(B, H, (T + 31) // 32, dtype=torch.int32, device=dev) if separate else None
+    count = torch.empty(B, H, dtype=torch.int32, device=dev) if separate else None
     out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ws_s = torch.empty(kvp.kvp_score_workspace_bytes(0, n_tok, D, H), dtype=torch.uint8, device=dev)
@@ -471,7 +472,7 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs only)")
     ap.add_argument("--workload", default="llama3_8b_layer",
                     choices=["llama3_8b_layer", "mlp_prefill", "dms_decode", "llama65b_mha", "prune_sweep",
-                             "threshold", "quant_tier", "quant_decode"],
+                             "threshold", "quant_tier", "quant_decode", "gqa_sweep"],
                     help="llama3_8b_layer = the bench line; the others print measurement lines "
                          "(see bench_workloads.py)")
     ap.add_argument("--eager", action="store_true", help="launch every step from the host (no CUDA graph)")

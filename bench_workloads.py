@@ -562,9 +562,50 @@ def quant_decode(kvp, dev, peaks, seed=0, steps=64, reps=3):
             "one_tier": res[1], "two_tier": res[2]}
 
 
+def gqa_sweep(kvp, dev, peaks, seed=0, calls=10, reps=5):
+    """Decode attention on the Llama-3-8B-shaped cache (batch 16, 8,192 cached
+    tokens, 8 kv heads, head_dim 128) with 1, 2, 4 and 8 query heads per kv
+    head, kept whole and 75 % pruned: the call time of the kernel each group
+    size is dispatched to (CUDA graphs of 10 calls)."""
+    B, T, H, d = 16, 8192, 8, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    K = _randn_bf16((B, T, H, d), g, dev)
+    V = _randn_bf16((B, T, H, d), g, dev)
+    s = torch.randn((B, T, H), generator=g, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    mp = (T + 15) // 16
+    cache = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp, device=dev)
+    points = []
+    for prune_q in (0.0, 0.75):
+        tau = torch.full((B, H), -math.inf, device=dev) if prune_q == 0.0 else _tau_quantile(kvp, s, prune_q)
+        kvp.kvp_compact_masked(K, V, T - 1, 0, cache, mode=kvp.KVP_MASK_KVZAP, scores=s.view(B * T, H), tau=tau,
+                               status=st)
+        torch.cuda.synchronize()
+        pages = int(((cache.count + 15) // 16).sum().item())
+        for G in (1, 2, 4, 8):
+            Hq = H * G
+            q = _randn_bf16((B, Hq, d), g, dev)
+            out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+            ws = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+
+            def calls_fn():
+                for _ in range(calls):
+                    kvp.kvp_decode_attn(q, cache, T - 1, out=out, workspace=ws, status=st)
+
+            ms = _time(_graph(calls_fn), reps=reps) / calls
+            nbytes = pages * 16 * (2 * d * 2 + 4) + B * Hq * d * (2 + 4)
+            points.append({"prune_q": prune_q, "group": G, "surviving_pages": pages, "decode_attn_us": ms * 1e3,
+                           "GB_s": nbytes / (ms * 1e-3) / 1e9, "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks[0]})
+    assert st.item() == 0, kvp.status_string(st.item())
+    return {"workload": "gqa_sweep: decode attention, batch 16, 8192 cached tokens, 8 kv heads, head_dim 128, "
+                        "1/2/4/8 query heads per kv head, keep-all and 75 % pruned; CUDA graphs of 10 calls",
+            "points": points}
+
+
 RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha,
            "prune_sweep": prune_sweep, "threshold": threshold,
-           "quant_tier": quant_tier, "quant_decode": quant_decode}
+           "quant_tier": quant_tier, "quant_decode": quant_decode, "gqa_sweep": gqa_sweep}
 
 
 def run(name, kvp, dev, peaks):
