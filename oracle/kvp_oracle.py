@@ -33,6 +33,8 @@ Steps and where they come from:
            attention over what is kept (single-query decode, GQA).
 5. quantize [BeaconKV]: instead of dropping the less important entries,
            keep them in low precision (an fp8 tier, see section 5).
+6. latent  [DMS, "주요 요점" / "앞으로의 전망"]: the same pruning over MLA's
+           single latent cache (section 6).
 
 Readings where the pages are silent (each is listed with its reason in the
 repository's design notes): scores are raw surrogate outputs compared to a
@@ -536,6 +538,47 @@ def decode_attention_two_tier(q_bits, cache: PagedCache, qcache: QuantPagedCache
             V = np.concatenate([Va, Vb.reshape(-1, d)])
             for j in range(h * g, (h + 1) * g):
                 out[b, j] = _softmax_attend(q[b, j], K, V, scale)
+    return out.astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# 6. Latent-cache (MLA) pruning  [DMS, "주요 요점" (compatible with Multi-Head
+#    Latent Attention as used by DeepSeek models) and "앞으로의 전망" (DMS
+#    combined with MLA)]
+#
+# Reading: with MLA every token caches one latent row shared by all query
+# heads, c_t (the compressed KV, dc values) followed by the shared rotary key
+# (dr values). Pruning keeps or drops that row as a whole: one score (or DMS
+# flag) per token, the rules of section 2 with a single "kv head", and the
+# compaction of section 3 over rows of dc + dr values. Attention is MLA's
+# absorbed decode form: query head j brings q_j = [q_nope_j W_UK_j^T, q_rope_j]
+# (dc + dr values), its logit against slot t is scale * q_j . row_t, and its
+# output is the softmax-weighted sum of the rows' first dc values (the
+# compressed value, to which the caller applies W_UV_j).
+# ---------------------------------------------------------------------------
+
+def compact_latent_dense(lat_bits, expire_bt, now: int, reserve: int, n_pages_cap: int, max_pages: int) -> PagedCache:
+    """Latent rows [B, T, dc + dr] + expire [B, T] -> PagedCache with one
+    "kv head" (H = 1) whose K pool holds the latent rows (its V pool holds the
+    same rows: one pool is enough for MLA, the cache format is section 3's)."""
+    lat = np.asarray(lat_bits)[:, :, None, :]
+    return compact_dense(lat, lat, np.asarray(expire_bt)[:, None, :], now, reserve, n_pages_cap, max_pages)
+
+
+def decode_attention_mla(q_bits, cache: PagedCache, dc: int, now: int, scale: float | None = None) -> np.ndarray:
+    """o[b, j] = sum_t softmax_t(scale * q[b, j] . row_t) row_t[:dc] over the
+    latent slots present at `now`; q [B, Hq, dc + dr] bf16 bits, rows from the
+    K pool; scale defaults to 1 / sqrt(dc + dr). Returns float32 [B, Hq, dc]."""
+    B, Hq, Dl = q_bits.shape
+    scale = 1.0 / math.sqrt(Dl) if scale is None else scale
+    q = widen_bf16(q_bits)
+    out = np.zeros((B, Hq, dc))
+    for b in range(B):
+        pg, row = cache.slot_rows(b, 0, np.arange(cache.count[b, 0]))
+        sel = present(cache.expire_pool[pg, row], now)
+        C = widen_bf16(cache.k_pool[pg[sel], row[sel]])
+        for j in range(Hq):
+            out[b, j] = _softmax_attend(q[b, j], C, C[:, :dc], scale)
     return out.astype(np.float32)
 
 

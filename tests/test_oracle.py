@@ -637,3 +637,76 @@ def test_dms_fp8_tier_takes_over_where_eviction_was():
         assert in_a + vis_b == H * (now + 1)
         np.testing.assert_allclose(orc.decode_attention_two_tier(q, ca, cq, now),
                                    orc.dense_attention(q, k, v, now), rtol=0, atol=1e-6)
+
+
+# --------------------------------------------------------------------------- latent cache (MLA)
+
+def test_mla_absorbed_attention_equals_decompressed_heads():
+    """The absorbed form is MLA's decompressed attention. Per head j the keys
+    [c_t W_UK_j^T, k_rope_t] and values c_t W_UV_j^T with the query
+    [q_nope_j, q_rope_j], by torch's scaled_dot_product_attention in float64
+    (a library routine), give the oracle's latent attention of the absorbed
+    query [q_nope_j W_UK_j, q_rope_j] followed by W_UV_j, on a pruned latent
+    cache. W_UK_j is a random permutation times 1/2, so the absorbed query is
+    exactly a bf16 value (the path's input format) and the two sides differ
+    only by float64 rounding; W_UV_j is a general matrix."""
+    rng = np.random.default_rng(21)
+    B, T, Hq, dc, dr, dv = 2, 150, 3, 64, 16, 24
+    lat = syn.f32_to_bf16_bits(rng.standard_normal((B, T, dc + dr)).astype(np.float32))
+    s = rng.standard_normal((B, T, 1))
+    now = T - 1
+    exp = orc.mask_kvzap(s, np.full((B, 1), 0.3), now, window=16)[0][:, 0]      # [B, T]
+    mp = T // 16 + 2
+    cache = orc.compact_latent_dense(lat, exp, now, 0, B * mp, mp)
+    w_uk = np.stack([np.eye(dc)[rng.permutation(dc)] * 0.5 for _ in range(Hq)])  # [Hq, dn = dc, dc]
+    w_uv = rng.standard_normal((Hq, dv, dc)) / math.sqrt(dc)
+    q_nope = orc.widen_bf16(syn.f32_to_bf16_bits(rng.standard_normal((B, Hq, dc)).astype(np.float32)))
+    q_rope = orc.widen_bf16(syn.f32_to_bf16_bits(rng.standard_normal((B, Hq, dr)).astype(np.float32)))
+    q_abs = np.concatenate([np.einsum("bhn,hnc->bhc", q_nope, w_uk), q_rope], axis=2)
+    q_bits = syn.f32_to_bf16_bits(q_abs.astype(np.float32))
+    np.testing.assert_array_equal(orc.widen_bf16(q_bits), q_abs)                 # exact in bf16
+    scale = 1.0 / math.sqrt(dc + dr)
+    got = np.einsum("bhc,hvc->bhv", orc.decode_attention_mla(q_bits, cache, dc, now, scale).astype(np.float64), w_uv)
+    L = orc.widen_bf16(lat)
+    keep = orc.present(exp, now)
+    for b in range(B):
+        C = torch.from_numpy(L[b, keep[b]])
+        for j in range(Hq):
+            kj = torch.cat([C[:, :dc] @ torch.from_numpy(w_uk[j]).T, C[:, dc:]], dim=1)   # decompressed keys
+            vj = C[:, :dc] @ torch.from_numpy(w_uv[j]).T                               # decompressed values
+            qj = torch.from_numpy(np.concatenate([q_nope[b, j], q_rope[b, j]]))
+            ref = torch.nn.functional.scaled_dot_product_attention(qj[None, None, None], kj[None, None],
+                                                                   vj[None, None], scale=scale)[0, 0, 0].numpy()
+            np.testing.assert_allclose(got[b, j], ref, rtol=2e-6, atol=1e-7)
+
+
+def test_mla_latent_pruning_special_cases():
+    """Keep-all reduces to dense latent attention (brute force over every
+    position); a score of -inf keeps exactly the last-window rows; the page
+    layout is section 3's with one kv head."""
+    rng = np.random.default_rng(22)
+    B, T, Hq, dc, dr = 1, 200, 4, 32, 8
+    lat = syn.f32_to_bf16_bits(rng.standard_normal((B, T, dc + dr)).astype(np.float32))
+    q = syn.f32_to_bf16_bits((rng.standard_normal((B, Hq, dc + dr)) * 0.3).astype(np.float32))
+    now = T - 1
+    mp = T // 16 + 2
+    L = orc.widen_bf16(lat)
+    qf = orc.widen_bf16(q)
+    scale = 1.0 / math.sqrt(dc + dr)
+
+    def brute(lo):
+        out = np.zeros((B, Hq, dc))
+        for j in range(Hq):
+            C = L[0, lo:now + 1]
+            w = np.exp((C @ qf[0, j]) * scale - ((C @ qf[0, j]) * scale).max())
+            out[0, j] = (w @ C[:, :dc]) / w.sum()
+        return out
+    keep_all = np.full((B, T), orc.NEVER)
+    c = orc.compact_latent_dense(lat, keep_all, now, 0, B * mp, mp)
+    np.testing.assert_allclose(orc.decode_attention_mla(q, c, dc, now), brute(0), rtol=0, atol=1e-6)
+    s = np.full((B, T, 1), -np.inf)
+    exp = orc.mask_kvzap(s, np.zeros((B, 1)), now, window=40)[0][:, 0]
+    c = orc.compact_latent_dense(lat, exp, now, 0, B * mp, mp)
+    assert int(c.count[0, 0]) == 40
+    np.testing.assert_array_equal(c.remap[0, 0, :40], np.arange(T - 40, T))
+    np.testing.assert_allclose(orc.decode_attention_mla(q, c, dc, now), brute(T - 40), rtol=0, atol=1e-6)
