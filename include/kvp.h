@@ -399,7 +399,10 @@ KVP_API kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_dim,
  * The pages of all (b, h) are split evenly over the warps of a persistent
  * grid (split-KV along pages, whatever the per-head survivor counts); partial
  * softmax states of a (b, h) that spans several warps are merged in fp32 by
- * the last of them to finish.
+ * the last of them to finish. Up to 4 query heads per kv head the page math
+ * runs on the CUDA cores in fp32; at 8 it runs on the tensor cores (bf16
+ * products with fp32 accumulation, the softmax weights entering the P.V
+ * product as a bf16 hi + lo pair, about 16 bits each).
  *
  * q          device bf16 [B, Hq, head_dim];  Hq a multiple of H, Hq/H in {1,2,4,8},
  *            B*H <= 4096
@@ -440,7 +443,9 @@ KVP_API kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, int
  * over the persistent grid like kvp_decode_attn's.
  *
  * Arguments up to `count` and from `now` on: as kvp_decode_attn (same
- * workspace size and rules). kq_pool, vq_pool, meta_pool (16-byte aligned),
+ * workspace size and rules). At 8 query heads per kv head a fp8 page's codes
+ * are turned into fp16 (exactly) and multiplied by the query converted to
+ * fp16, which is exact for bf16 values of magnitude 2^-17 .. 65504. kq_pool, vq_pool, meta_pool (16-byte aligned),
  * n_pages_cap_q, page_table_q (width max_pages_q), count_q: the fp8 tier as
  * kvp_compact_quant writes it. A fp8 page id outside [0, n_pages_cap_q)
  * records KVP_ERR_BOUNDS and the page counts as empty.
