@@ -209,7 +209,11 @@ KVP_DEV bool merge_pieces(const AttnParams& p, int cbh, int npc, size_t s0, bool
     const bool okm = mbar_wait(mbar, merge_par, nullptr, p.status);
     merge_par ^= 1u;
     if (!__all_sync(0xffffffffu, okm)) {
-      if (lane == 0) record_error(p.status, KVP_ERR_TIMEOUT);
+      if (lane == 0) {
+        record_error(p.status, KVP_ERR_TIMEOUT);
+        (void)mbar_wait(mbar, merge_par ^ 1u);  // the two copies land before the ring is released (bounded)
+      }
+      __syncwarp();
       return false;
     }
     float M[G], wr[G], L[G];
@@ -601,7 +605,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
     const int st = k % kNst;
     const bool ok = mbar_wait(&bars[st], static_cast<uint32_t>((k / kNst) & 1), nullptr, p.status);
     if (!__all_sync(0xffffffffu, ok)) {
-      if (lane == 0) record_error(p.status, KVP_ERR_TIMEOUT);
+      if (lane == 0) {
+        record_error(p.status, KVP_ERR_TIMEOUT);
+        // let the copies this warp issued land before its shared memory can
+        // go to another CTA (each wait bounded again)
+        for (int kk = k; kk < n_my && kk < k + kNst; ++kk) (void)mbar_wait(&bars[kk % kNst], (kk / kNst) & 1u);
+      }
+      __syncwarp();
       return;  // outputs of this call are unspecified after a timeout
     }
     const uint8_t* stage = ring + st * C::STAGE_BYTES;
@@ -1175,7 +1185,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     const int st = k % kNst;
     const bool ok = mbar_wait(&bars[st], static_cast<uint32_t>((k / kNst) & 1), nullptr, p.status);
     if (!__all_sync(0xffffffffu, ok)) {
-      if (lane == 0) record_error(p.status, KVP_ERR_TIMEOUT);
+      if (lane == 0) {
+        record_error(p.status, KVP_ERR_TIMEOUT);
+        // let the copies this warp issued land before its shared memory can
+        // go to another CTA (each wait bounded again)
+        for (int kk = k; kk < n_my && kk < k + kNst; ++kk) (void)mbar_wait(&bars[kk % kNst], (kk / kNst) & 1u);
+      }
+      __syncwarp();
       return;  // outputs of this call are unspecified after a timeout
     }
     const uint32_t kbase = ring_u32 + st * C::STAGE_BYTES;

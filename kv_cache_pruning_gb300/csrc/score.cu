@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(score_threads<EPI>(), 1)
       const uint64_t pol_x = policy_evict_first();  // hidden states stream through once
       const uint64_t pol_w = policy_evict_last();   // weights are re-read by every tile
       uint32_t stage = 0, phase = 0;
+      uint32_t issued = 0, issued_par = 0;  // per stage: loaded at least once, parity of its last load
       for (int t = blockIdx.x; t < n_tiles_total && !*abort_flag; t += gridDim.x) {
         const int mt = t / p.n_tiles, nt = t - mt * p.n_tiles;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -142,6 +143,8 @@ __global__ void __launch_bounds__(score_threads<EPI>(), 1)
             break;
           }
           uint8_t* a = tiles + stage * C::kStageBytes;
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
           tma_load_2d_hint(a, &tmA, kb * kBK, mt * kBM, &full[stage], pol_x);
           tma_load_2d_hint(a + C::kABytes, &tmB, kb * kBK, nt * BN, &full[stage], pol_w);
@@ -151,6 +154,12 @@ __global__ void __launch_bounds__(score_threads<EPI>(), 1)
           }
         }
       }
+      if (*abort_flag) {
+        // a wait gave up: the loads already issued land before the shared
+        // memory is released (each wait bounded again)
+        for (int s = 0; s < C::kStages; ++s)
+          if ((issued >> s) & 1u) (void)mbar_wait(&full[s], (issued_par >> s) & 1u);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -158,6 +167,8 @@ __global__ void __launch_bounds__(score_threads<EPI>(), 1)
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      int last_stage = -1;     // stage and phase of the last commit, which tracks every MMA issued before it
+      uint32_t last_par = 0;
       for (int t = blockIdx.x; t < n_tiles_total && !*abort_flag; t += gridDim.x) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
           record_error(p.status, KVP_ERR_TIMEOUT);
@@ -181,6 +192,8 @@ __global__ void __launch_bounds__(score_threads<EPI>(), 1)
             umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);  // frees this smem stage once the MMAs have read it
+          last_stage = static_cast<int>(stage);
+          last_par = phase;
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
@@ -190,6 +203,9 @@ __global__ void __launch_bounds__(score_threads<EPI>(), 1)
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
+      // a wait gave up: the MMAs already issued finish before tensor memory is
+      // freed (bounded)
+      if (*abort_flag && last_stage >= 0) (void)mbar_wait(&empty[last_stage], last_par);
     }
     __syncwarp();
   } else {
