@@ -603,9 +603,66 @@ def gqa_sweep(kvp, dev, peaks, seed=0, calls=10, reps=5):
             "points": points}
 
 
+def mla_sweep(kvp, dev, peaks, seed=0, calls=10, reps=5):
+    """MLA latent cache (DeepSeek-V3-shaped attention: latent rows of 512 + 64
+    values, batch 16, 8,192 cached tokens): latent compaction with the mask
+    fused in, then absorbed decode attention with 16, 32, 64 and 128 query
+    heads, kept whole and 75 % pruned (CUDA graphs of 10 calls). Bytes count
+    the surviving pages (16 rows of 1,152 bytes + 64 bytes of expire values)
+    and the query and output rows; flops count 2 x 16 x (576 + 512) per page
+    and head."""
+    B, T, row, dc = 16, 8192, kvp.LATENT_ROW, kvp.KVP_MLA_LATENT_DIM
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    lat = _randn_bf16((B, T, row), g, dev)
+    s = torch.randn((B, T, 1), generator=g, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    mp = (T + 15) // 16
+    cache = kvp.LatentPagedKV.allocate(B, B * mp, mp, device=dev)
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, 1, T), dtype=torch.uint8, device=dev)
+    points = []
+    for prune_q in (0.0, 0.75):
+        tau = torch.full((B, 1), -math.inf, device=dev) if prune_q == 0.0 else _tau_quantile(kvp, s, prune_q)
+
+        def compact_fn():
+            for _ in range(calls):
+                kvp.kvp_compact_latent(lat, T - 1, 0, cache, mode=kvp.KVP_MASK_KVZAP, scores=s.view(B, T),
+                                       tau=tau.view(B), workspace=ws_c, status=st)
+
+        ms_c = _time(_graph(compact_fn), reps=reps) / calls
+        torch.cuda.synchronize()
+        pages = int(((cache.count + 15) // 16).sum().item())
+        kept = int(cache.count.sum().item())
+        c_bytes = B * T * 4 + 2 * kept * row * 2 + pages * 16 * 4
+        for Hq in (16, 32, 64, 128):
+            q = _randn_bf16((B, Hq, row), g, dev)
+            out = torch.empty(B, Hq, dc, dtype=torch.float32, device=dev)
+            ws = torch.zeros(kvp.kvp_decode_attn_mla_workspace_bytes(B, Hq, 0), dtype=torch.uint8, device=dev)
+
+            def calls_fn():
+                for _ in range(calls):
+                    kvp.kvp_decode_attn_mla(q, cache, T - 1, out=out, workspace=ws, status=st)
+
+            ms = _time(_graph(calls_fn), reps=reps) / calls
+            nbytes = pages * (16 * row * 2 + 64) + B * Hq * (row * 2 + dc * 4)
+            flops = 2.0 * 16 * pages * Hq * (row + dc)
+            points.append({"prune_q": prune_q, "q_heads": Hq, "surviving_pages": pages,
+                           "compact_latent_us": ms_c * 1e3,
+                           "compact_frac_of_hbm": c_bytes / (ms_c * 1e-3) / 1e9 / peaks[0],
+                           "decode_attn_mla_us": ms * 1e3, "GB_s": nbytes / (ms * 1e-3) / 1e9,
+                           "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks[0],
+                           "TFLOP_s": flops / (ms * 1e-3) / 1e12,
+                           "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / peaks[1]})
+    assert st.item() == 0, kvp.status_string(st.item())
+    return {"workload": "mla_sweep: MLA latent cache, batch 16, 8192 cached tokens, rows of 512 + 64, latent "
+                        "compaction and absorbed decode attention at 16/32/64/128 query heads, keep-all and 75 % "
+                        "pruned; CUDA graphs of 10 calls",
+            "points": points}
+
+
 RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha,
            "prune_sweep": prune_sweep, "threshold": threshold,
-           "quant_tier": quant_tier, "quant_decode": quant_decode, "gqa_sweep": gqa_sweep}
+           "quant_tier": quant_tier, "quant_decode": quant_decode, "gqa_sweep": gqa_sweep, "mla_sweep": mla_sweep}
 
 
 def run(name, kvp, dev, peaks):

@@ -21,6 +21,9 @@
  *                    scored once and written into a reserved slot.
  *   kvp_decode_attn  DMS article, "DMS 작동 방식" step 5: standard attention
  *                    over what is kept; here split-KV single-query GQA decode.
+ *   kvp_*_latent, kvp_decode_attn_mla
+ *                    DMS article, "주요 요점" and "앞으로의 전망": the same
+ *                    pruning over MLA's single latent cache.
  *
  * Conventions shared by every entry point:
  *   - Pointers named in a comment as "device" are CUDA device addresses
@@ -459,6 +462,114 @@ KVP_API kvp_status kvp_decode_attn_two_tier(int batch, int n_q_heads, int n_kv_h
                                    const int32_t* count_q, int now, float scale, float* out,
                                    int grid_limit, void* workspace, size_t workspace_bytes,
                                    int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* MLA latent cache. The DMS article ("주요 요점"; "앞으로의 전망") says the method
+ * applies to Multi-Head Latent Attention, whose cache holds one latent row per
+ * token, shared by every query head: c_t (KVP_MLA_LATENT_DIM values of
+ * compressed KV) followed by the shared rotary key (KVP_MLA_ROPE_DIM values).
+ * The article gives no further detail; this library's reading is that a
+ * token's latent row is kept or dropped as a whole, by one score (or DMS
+ * flag) per token, under the same rules as a kv head's entry (kvp_mask), and
+ * that the pruned cache is read by MLA's absorbed decode attention.
+ *
+ * A latent cache is a paged cache with one "kv head" and one pool: pool bf16
+ * [n_pages_cap, 16, row_dim], row_dim = KVP_MLA_LATENT_DIM + KVP_MLA_ROPE_DIM
+ * (the only supported width; anything else is KVP_ERR_UNSUPPORTED);
+ * expire_pool, page_table [B, max_pages], remap [B, max_pages*16] and count
+ * [B] as kvp_compact writes them with n_kv_heads = 1.
+ */
+#define KVP_MLA_LATENT_DIM 512
+#define KVP_MLA_ROPE_DIM 64
+
+/* kvp_compact_latent - kvp_compact_masked for a latent cache: the present
+ * latent rows of every batch element into 16-row pages.
+ *
+ * lat_src    device bf16, row (b, t) at b*stride_b + t*stride_t (elements,
+ *            multiples of 8), row_dim contiguous values, t in [0, n_pos)
+ * scores     KVZAP: device fp32 [B, n_pos] (kvp_score's output with one
+ *            head); tau device fp32 [B];  DMS: NULL, NULL
+ * flag_step  DMS: device int32 [B, n_pos];  KVZAP: NULL
+ * Outputs, reserve, window, delay, now, status: kvp_compact_masked's with
+ * n_kv_heads = 1 and the one pool; rows past count in a batch element's
+ * last page are zero. Workspace: kvp_compact_workspace_bytes(batch, 1, n_pos).
+ */
+KVP_API kvp_status kvp_compact_latent(int mode, int batch, int row_dim, int n_pos, const void* lat_src,
+                                      int64_t stride_b, int64_t stride_t,
+                                      const float* scores, const float* tau, const int32_t* flag_step,
+                                      int window, int delay, int now, int reserve,
+                                      void* pool, int32_t* expire_pool, int n_pages_cap,
+                                      int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                                      void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* kvp_compact_latent_paged - kvp_compact_paged for a latent cache (the
+ * source and destination are latent caches; they share no buffer).
+ * Workspace: kvp_compact_paged_workspace_bytes(batch, 1, src_max_pages).
+ */
+KVP_API kvp_status kvp_compact_latent_paged(int batch, int row_dim, const void* src_pool,
+                                            const int32_t* src_expire_pool, int src_n_pages_cap,
+                                            const int32_t* src_page_table, int src_max_pages,
+                                            const int32_t* src_remap, const int32_t* src_count,
+                                            int now, int reserve, void* pool, int32_t* expire_pool, int n_pages_cap,
+                                            int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                                            void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* kvp_append_latent - kvp_append for a latent cache: the new token's latent
+ * row of every batch element into slot count[b].
+ *
+ * lat_new       device bf16 [B, row_dim]
+ * score, tau    KVZAP: device fp32 [B] each;  DMS: NULL
+ * flag_step     DMS: device int32 [B];  KVZAP: NULL
+ * Everything else, and the errors, as kvp_append.
+ */
+KVP_API kvp_status kvp_append_latent(int mode, int batch, int row_dim, int pos, const void* lat_new,
+                                     const float* score, const float* tau, const int32_t* flag_step,
+                                     int window, int delay, void* pool, int32_t* expire_pool, int n_pages_cap,
+                                     const int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                                     int32_t* status, void* stream);
+
+/* kvp_decode_attn_mla - MLA's absorbed decode attention over a pruned latent
+ * cache:
+ *
+ *   out[b, j] = sum_t softmax_t(scale * q[b, j] . row_t) row_t[0 : latent_dim]
+ *
+ * over the slots t < count[b] whose expire is greater than `now`. q[b, j] is
+ * query head j's absorbed query: its no-position part multiplied by that
+ * head's key up-projection (latent_dim values), then its rotary part
+ * (rope_dim values). The result is the head's attention-weighted compressed
+ * value, to which the caller applies the head's value up-projection. An
+ * empty set gives a zero row.
+ *
+ * Work is cut into units of 16 query heads of one batch element, and each
+ * unit's pages into n_splits equal slices, one CTA each (a CTA of a later
+ * unit of the same slice reads the same pages, mostly from L2). Both
+ * products run on the tensor cores: bf16 operands, fp32 accumulation, the
+ * softmax weights entering the weighted sum as a bf16 hi + lo pair; slices
+ * are merged in fp32 by the last CTA of the unit to finish.
+ *
+ * latent_dim, rope_dim  KVP_MLA_LATENT_DIM and KVP_MLA_ROPE_DIM (else
+ *            KVP_ERR_UNSUPPORTED)
+ * q          device bf16 [B, n_q_heads, latent_dim + rope_dim], n_q_heads >= 1
+ * pool, expire_pool, page_table (width max_pages), count: a latent cache;
+ *            count is clamped to max_pages*16, a page id outside
+ *            [0, n_pages_cap) records KVP_ERR_BOUNDS in `status` (may be
+ *            NULL) and the page counts as empty. n_pages_cap*16 < 2^31.
+ * scale      > 0, or 0 for 1/sqrt(latent_dim + rope_dim)
+ * out        device fp32 [B, n_q_heads, latent_dim], 16-byte aligned
+ * n_splits   slices per unit, 1..64; 0 picks one from the current device's
+ *            SM count (about two CTAs per SM in all)
+ * workspace  device, >= kvp_decode_attn_mla_workspace_bytes(batch,
+ *            n_q_heads, n_splits) (asked on the device that runs the call
+ *            when n_splits = 0), 16-byte aligned; zero-filled before its
+ *            first use and left ready by every call that records no error,
+ *            as kvp_decode_attn's workspace.
+ */
+KVP_API size_t kvp_decode_attn_mla_workspace_bytes(int batch, int n_q_heads, int n_splits);
+KVP_API kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_dim, int rope_dim, const void* q,
+                                       const void* pool, const int32_t* expire_pool, int n_pages_cap,
+                                       const int32_t* page_table, int max_pages, const int32_t* count, int now,
+                                       float scale, float* out, int n_splits, void* workspace,
+                                       size_t workspace_bytes, int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -39,6 +39,9 @@ KVP_MASK_DMS = 1
 PAGE = 16
 WINDOW = 128
 EXPIRE_NEVER = 2**31 - 1
+KVP_MLA_LATENT_DIM = 512
+KVP_MLA_ROPE_DIM = 64
+LATENT_ROW = KVP_MLA_LATENT_DIM + KVP_MLA_ROPE_DIM
 
 
 class KvpError(RuntimeError):
@@ -89,6 +92,13 @@ _SIGS = {
     "kvp_decode_attn": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _I, _P, _S, _P, _P]),
     "kvp_decode_attn_two_tier": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _P, _I, _P,
                                       _I, _F, _P, _I, _P, _S, _P, _P]),
+    "kvp_compact_latent": (_I, [_I, _I, _I, _I, _P, _L, _L, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _I, _P, _P,
+                                _P, _S, _P, _P]),
+    "kvp_compact_latent_paged": (_I, [_I, _I, _P, _P, _I, _P, _I, _P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _P,
+                                      _S, _P, _P]),
+    "kvp_append_latent": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P]),
+    "kvp_decode_attn_mla_workspace_bytes": (_S, [_I, _I, _I]),
+    "kvp_decode_attn_mla": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _I, _P, _S, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -530,5 +540,128 @@ def kvp_decode_attn_two_tier(q, cache: PagedKV, qcache: QuantPagedKV, now, *, sc
     return out
 
 
-__all__ = [n for n in dir() if n.startswith(("kvp_", "KVP_", "PagedKV", "QuantPagedKV", "KvpError"))] + [
-    "status_string", "version", "library", "PAGE", "WINDOW", "EXPIRE_NEVER"]
+# --------------------------------------------------------------------------- MLA latent cache
+
+@dataclass
+class LatentPagedKV:
+    """Device buffers of one compacted MLA latent cache: one "kv head", one pool of latent rows."""
+    pool: torch.Tensor          # bf16 [n_pages_cap, 16, 576]
+    expire_pool: torch.Tensor   # int32 [n_pages_cap, 16]
+    page_table: torch.Tensor    # int32 [B, max_pages]
+    remap: torch.Tensor         # int32 [B, max_pages * 16]
+    count: torch.Tensor         # int32 [B]
+
+    @staticmethod
+    def allocate(batch, n_pages_cap, max_pages, device="cuda"):
+        return LatentPagedKV(
+            torch.zeros((n_pages_cap, PAGE, LATENT_ROW), dtype=torch.bfloat16, device=device),
+            torch.zeros((n_pages_cap, PAGE), dtype=torch.int32, device=device),
+            torch.full((batch, max_pages), -1, dtype=torch.int32, device=device),
+            torch.full((batch, max_pages * PAGE), -1, dtype=torch.int32, device=device),
+            torch.zeros((batch,), dtype=torch.int32, device=device),
+        )
+
+    @property
+    def n_pages_cap(self):
+        return self.pool.shape[0]
+
+    @property
+    def max_pages(self):
+        return self.page_table.shape[1]
+
+    @property
+    def batch(self):
+        return self.count.shape[0]
+
+
+def kvp_compact_latent(lat, now, reserve, dst: LatentPagedKV, *, mode, scores=None, tau=None, flag_step=None,
+                       window=WINDOW, delay=0, status, workspace=None, stream=None):
+    """Dense latent rows [B, T, 576] (row contiguous) with the mask applied on the fly: KVzap scores [B, T]
+    (or [B*T, 1]) + tau [B], or DMS flag_step [B, T] -> dst."""
+    B, T, R = lat.shape
+    if lat.dtype != torch.bfloat16 or not lat.is_cuda or lat.stride(2) != 1:
+        raise TypeError("lat must be a CUDA bf16 tensor with contiguous rows")
+    if scores is not None and scores.numel() != B * T:
+        raise ValueError("scores must hold B*T values")
+    if flag_step is not None and flag_step.numel() != B * T:
+        raise ValueError("flag_step must hold B*T values")
+    if tau is not None and tau.numel() != B:
+        raise ValueError("tau must hold B values")
+    ws = _ws(kvp_compact_workspace_bytes(B, 1, T), lat.device, workspace)
+    code = _lib.kvp_compact_latent(mode, B, R, T, lat.data_ptr(), lat.stride(0), lat.stride(1),
+                                   _ptr(scores, torch.float32, "scores", True), _ptr(tau, torch.float32, "tau", True),
+                                   _ptr(flag_step, torch.int32, "flag_step", True), window, delay, now, reserve,
+                                   _ptr(dst.pool, torch.bfloat16), _ptr(dst.expire_pool, torch.int32),
+                                   dst.n_pages_cap, _ptr(dst.page_table, torch.int32), dst.max_pages,
+                                   _ptr(dst.remap, torch.int32), _ptr(dst.count, torch.int32), ws.data_ptr(),
+                                   ws.numel() * ws.element_size(), _ptr(status, torch.int32, "status"),
+                                   _stream(stream))
+    _check("kvp_compact_latent", code)
+    return dst
+
+
+def kvp_compact_latent_paged(src: LatentPagedKV, now, reserve, dst: LatentPagedKV, *, status, workspace=None,
+                             stream=None):
+    """Re-compaction of a latent cache: its slots present at `now`, in slot order, into dst."""
+    B = src.batch
+    ws = _ws(kvp_compact_paged_workspace_bytes(B, 1, src.max_pages), src.pool.device, workspace)
+    code = _lib.kvp_compact_latent_paged(B, src.pool.shape[2], _ptr(src.pool, torch.bfloat16),
+                                         _ptr(src.expire_pool, torch.int32), src.n_pages_cap,
+                                         _ptr(src.page_table, torch.int32), src.max_pages,
+                                         _ptr(src.remap, torch.int32), _ptr(src.count, torch.int32), now, reserve,
+                                         _ptr(dst.pool, torch.bfloat16), _ptr(dst.expire_pool, torch.int32),
+                                         dst.n_pages_cap, _ptr(dst.page_table, torch.int32), dst.max_pages,
+                                         _ptr(dst.remap, torch.int32), _ptr(dst.count, torch.int32), ws.data_ptr(),
+                                         ws.numel() * ws.element_size(), _ptr(status, torch.int32, "status"),
+                                         _stream(stream))
+    _check("kvp_compact_latent_paged", code)
+    return dst
+
+
+def kvp_append_latent(cache: LatentPagedKV, lat_new, pos, *, mode, score=None, tau=None, flag_step=None,
+                      window=WINDOW, delay=0, status, stream=None):
+    """Writes the token at position `pos` (lat_new [B, 576]) into every batch element's next slot."""
+    B, R = lat_new.shape
+    code = _lib.kvp_append_latent(mode, B, R, pos, _ptr(lat_new, torch.bfloat16, "lat_new"),
+                                  _ptr(score, torch.float32, "score", True), _ptr(tau, torch.float32, "tau", True),
+                                  _ptr(flag_step, torch.int32, "flag_step", True), window, delay,
+                                  _ptr(cache.pool, torch.bfloat16), _ptr(cache.expire_pool, torch.int32),
+                                  cache.n_pages_cap, _ptr(cache.page_table, torch.int32), cache.max_pages,
+                                  _ptr(cache.remap, torch.int32), _ptr(cache.count, torch.int32),
+                                  _ptr(status, torch.int32, "status"), _stream(stream))
+    _check("kvp_append_latent", code)
+
+
+def kvp_decode_attn_mla_workspace_bytes(batch, n_q_heads, n_splits=0) -> int:
+    return _lib.kvp_decode_attn_mla_workspace_bytes(batch, n_q_heads, n_splits)
+
+
+def kvp_decode_attn_mla(q, cache: LatentPagedKV, now, *, scale=0.0, out=None, n_splits=0, workspace=None,
+                        status=None, stream=None):
+    """out[B, Hq, 512] fp32 = absorbed MLA attention of q [B, Hq, 576] (bf16) over the latent slots of `cache`
+    present at `now`. A caller-provided workspace must be zero-filled before its first use (torch.zeros); calls
+    that record no error leave it that way."""
+    B, Hq, R = q.shape
+    if R != LATENT_ROW:
+        raise ValueError(f"q rows must hold {LATENT_ROW} values")
+    if out is None:
+        out = torch.empty((B, Hq, KVP_MLA_LATENT_DIM), dtype=torch.float32, device=q.device)
+    need = kvp_decode_attn_mla_workspace_bytes(B, Hq, n_splits)
+    if workspace is None:
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)  # zero-filled before first use
+    else:
+        ws = _ws(need, q.device, workspace)
+    code = _lib.kvp_decode_attn_mla(B, Hq, KVP_MLA_LATENT_DIM, KVP_MLA_ROPE_DIM, _ptr(q, torch.bfloat16, "q"),
+                                    _ptr(cache.pool, torch.bfloat16), _ptr(cache.expire_pool, torch.int32),
+                                    cache.n_pages_cap, _ptr(cache.page_table, torch.int32), cache.max_pages,
+                                    _ptr(cache.count, torch.int32), now, float(scale),
+                                    _ptr(out, torch.float32, "out"), n_splits, ws.data_ptr(),
+                                    ws.numel() * ws.element_size(), _ptr(status, torch.int32, "status", True),
+                                    _stream(stream))
+    _check("kvp_decode_attn_mla", code)
+    return out
+
+
+__all__ = [n for n in dir() if n.startswith(("kvp_", "KVP_", "PagedKV", "QuantPagedKV", "LatentPagedKV",
+                                             "KvpError"))] + [
+    "status_string", "version", "library", "PAGE", "WINDOW", "EXPIRE_NEVER", "LATENT_ROW"]

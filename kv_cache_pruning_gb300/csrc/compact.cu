@@ -1,5 +1,6 @@
 // kvp_mask, kvp_compact, kvp_compact_masked, kvp_compact_quant, kvp_compact_paged, kvp_append,
-// kvp_append_quant.
+// kvp_append_quant, and the MLA latent cache's kvp_compact_latent, kvp_compact_latent_paged,
+// kvp_append_latent.
 //
 // Rules (KVzap summary "실제 적용"; DMS article "지연 삭제 (Delayed Eviction)"):
 // an entry gets the first step at which it is gone,
@@ -32,6 +33,7 @@ namespace {
 constexpr int kSeg = 128;           // entries per warp segment
 constexpr int kQuantMetaWords = 3 * KVP_PAGE_TOKENS;  // fp8 tier page record: start, K scale, V scale
 constexpr int kWarpsPerCta = 4;     // segments per CTA in the count and copy passes
+constexpr int kLatentRow = KVP_MLA_LATENT_DIM + KVP_MLA_ROPE_DIM;  // MLA latent row: compressed KV, rotary key
 
 KVP_DEV int32_t expire_kvzap(float s, float tau, int pos, int window) {
   return (s >= tau) ? kNever : pos + window;  // NaN compares false: treated as low
@@ -428,12 +430,25 @@ KVP_DEV void cp_async_wait_all() {
 // 53.6 / 54.7 / 54.9 us for 16 / 24 / 32.
 constexpr int kStage = 20;
 
-template <int D>
+// An entry is NPOOL rows of D bf16 values: a K and a V row (NPOOL = 2), or
+// one latent row of an MLA cache (NPOOL = 1, D = 576: 72 pieces of 16 bytes,
+// moved kStageWide at a time, about as many bytes per batch as 20 K/V pairs
+// of 128 values).
+constexpr int kStageWide = 8;
+template <int D, int NPOOL>
+constexpr int entry_pieces() {
+  return NPOOL * D * 2 / 16;
+}
+template <int D, int NPOOL>
+constexpr int stage_entries() {
+  return entry_pieces<D, NPOOL>() > 32 ? kStageWide : kStage;
+}
+template <int D, int NPOOL>
 constexpr int scatter_smem_bytes() {
-  return kWarpsPerCta * (kStage * 2 * D * 2 + kSeg * 8);
+  return kWarpsPerCta * (stage_entries<D, NPOOL>() * entry_pieces<D, NPOOL>() * 16 + kSeg * 8);
 }
 
-template <int D, class Src, bool kFused>
+template <int D, int NPOOL, class Src, bool kFused>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int now, int NS, int reserve,
                                                                      int max_pages, int n_pages_cap, int BH,
                                                                      CompactWs ws,
@@ -444,11 +459,14 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
                                                                      int32_t* __restrict__ expire_pool,
                                                                      int32_t* __restrict__ page_table,
                                                                      int32_t* __restrict__ remap) {
-  constexpr int E16 = 2 * D * 2 / 16;   // 16-byte pieces per entry (K row then V row)
-  constexpr int EPI = 32 / E16;         // entries per warp instruction (1 for D = 128, 2 for D = 64)
+  constexpr int E16 = entry_pieces<D, NPOOL>();  // 16-byte pieces per entry (K row then V row, or the latent row)
+  constexpr bool kNarrow = E16 <= 32 && 32 % E16 == 0;  // whole entries per warp instruction
+  constexpr int EPI = kNarrow ? 32 / E16 : 1;    // entries per warp instruction (1 for D = 128, 2 for D = 64)
+  constexpr int kSt = stage_entries<D, NPOOL>();
   // fp8 tier: k_pool / v_pool hold E4M3 codes (D bytes a row) and expire_pool
   // is the per-page record [start x 16, K scale x 16, V scale x 16]
   constexpr bool kQuant = std::is_same<Src, QuantSrc>::value;
+  static_assert(NPOOL == 2 || (!kQuant && !kNarrow), "one-pool entries are the wide latent rows");
   constexpr int kMetaStride = kQuant ? kQuantMetaWords : kPage;
   extern __shared__ __align__(16) uint8_t sm_raw[];
   pdl_launch_dependents();
@@ -457,8 +475,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
   const int warp = threadIdx.x >> 5;
   const int sg = blockIdx.y * kWarpsPerCta + warp;
   const int lane = threadIdx.x & 31;
-  uint4* stage = reinterpret_cast<uint4*>(sm_raw) + warp * kStage * E16;
-  int64_t* lst = reinterpret_cast<int64_t*>(sm_raw + kWarpsPerCta * kStage * E16 * 16) + warp * kSeg;
+  uint4* stage = reinterpret_cast<uint4*>(sm_raw) + warp * kSt * E16;
+  int64_t* lst = reinterpret_cast<int64_t*>(sm_raw + kWarpsPerCta * kSt * E16 * 16) + warp * kSeg;
   const bool live = sg < NS;
 
   // ---- loads that do not depend on one another, all issued first
@@ -544,9 +562,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
         }
         if (lane < 3) expire_pool[static_cast<int64_t>(base + (j >> 4)) * kMetaStride + lane * kPage + (j & 15)] = 0;
       } else {
-        if (lane < VPR) {
-          reinterpret_cast<uint4*>(k_pool + row * D)[lane] = make_uint4(0, 0, 0, 0);
-          reinterpret_cast<uint4*>(v_pool + row * D)[lane] = make_uint4(0, 0, 0, 0);
+        for (int x = lane; x < VPR; x += 32) {
+          reinterpret_cast<uint4*>(k_pool + row * D)[x] = make_uint4(0, 0, 0, 0);
+          if constexpr (NPOOL == 2) reinterpret_cast<uint4*>(v_pool + row * D)[x] = make_uint4(0, 0, 0, 0);
         }
         if (lane == 0) expire_pool[row] = 0;
       }
@@ -574,14 +592,34 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
   __syncwarp();
 
   // ---- move the rows through the stage
+  if constexpr (!kNarrow) {
+    // wide rows: the warp's lanes walk the batch's (entry, piece) pairs in order
+    for (int i0 = 0; i0 < nk; i0 += kSt) {
+      const int nb = min(kSt, nk - i0);
+      for (int x = lane; x < nb * E16; x += 32) {
+        const int i = x / E16, pc = x - i * E16;
+        cp_async16(stage + x, reinterpret_cast<const uint4*>(sv.kb + lst[i0 + i] * sv.stride) + pc);
+      }
+      cp_async_wait_all();
+      __syncwarp();
+      for (int x = lane; x < nb * E16; x += 32) {
+        const int i = x / E16, pc = x - i * E16;
+        const int j = slot0 + i0 + i;
+        const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
+        reinterpret_cast<uint4*>(k_pool + row * D)[pc] = stage[x];
+      }
+      __syncwarp();
+    }
+    return;
+  }
   const int piece = lane % E16;          // 16-byte piece of an entry this lane moves
   const int sub = lane / E16;            // entry of a warp instruction this lane serves
   const bool is_v = piece >= E16 / 2;
   const int vi = is_v ? piece - E16 / 2 : piece;
   const uint16_t* sbase = is_v ? sv.vb : sv.kb;
   uint16_t* dbase = is_v ? v_pool : k_pool;
-  for (int i0 = 0; i0 < nk; i0 += kStage) {
-    const int nb = min(kStage, nk - i0);
+  for (int i0 = 0; i0 < nk; i0 += kSt) {
+    const int nb = min(kSt, nk - i0);
     for (int i = sub; i < nb; i += EPI)
       cp_async16(stage + i * E16 + piece, reinterpret_cast<const uint4*>(sbase + lst[i0 + i] * sv.stride) + vi);
     cp_async_wait_all();
@@ -773,6 +811,51 @@ __global__ void __launch_bounds__(256) append_quant_kernel(int mode, int BH, int
   }
 }
 
+// Decode-time append of MLA latent rows: one warp per batch element (one
+// latent "head"), the row's 72 pieces of 16 bytes spread over the lanes; the
+// expire value follows the same rules as append_kernel's.
+__global__ void __launch_bounds__(256) append_latent_kernel(int mode, int B, int pos,
+                                                            const uint16_t* __restrict__ lat_new,
+                                                            const float* __restrict__ score,
+                                                            const float* __restrict__ tau,
+                                                            const int32_t* __restrict__ flag, int window, int delay,
+                                                            uint16_t* __restrict__ pool,
+                                                            int32_t* __restrict__ expire_pool, int n_pages_cap,
+                                                            const int32_t* __restrict__ page_table, int max_pages,
+                                                            int32_t* __restrict__ remap, int32_t* __restrict__ count,
+                                                            int32_t* __restrict__ status) {
+  constexpr int VPR = kLatentRow / 8;
+  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (b >= B) return;
+  const int j = count[b];
+  if (j < 0) {
+    if (lane == 0) record_error(status, KVP_ERR_BOUNDS);
+    return;
+  }
+  const int p = j >> 4;
+  const int page = (p < max_pages) ? page_table[static_cast<int64_t>(b) * max_pages + p] : -1;
+  if (page < 0) {
+    if (lane == 0) record_error(status, KVP_ERR_CAPACITY);
+    return;
+  }
+  if (page >= n_pages_cap) {
+    if (lane == 0) record_error(status, KVP_ERR_BOUNDS);
+    return;
+  }
+  const int64_t row = static_cast<int64_t>(page) * kPage + (j & 15);
+  const uint4* src = reinterpret_cast<const uint4*>(lat_new + static_cast<int64_t>(b) * kLatentRow);
+  uint4* dst = reinterpret_cast<uint4*>(pool + row * kLatentRow);
+  for (int x = lane; x < VPR; x += 32) dst[x] = src[x];
+  if (lane == 0) {
+    const int32_t e = (mode == KVP_MASK_KVZAP) ? expire_kvzap(score[b], tau[b], pos, window)
+                                               : expire_dms(flag[b], pos, delay, window);
+    expire_pool[row] = e;
+    remap[static_cast<int64_t>(b) * max_pages * kPage + j] = pos;
+    count[b] = j + 1;
+  }
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 template <class Src>
@@ -788,22 +871,28 @@ kvp_status run_compact(const Src& src, int BH, int NS, int head_dim, int now, in
   if (!fused) base_kernel<<<1, 1024, 0, st>>>(BH, reserve, max_pages, n_pages_cap, ws, count, status);
   auto* kp = static_cast<uint16_t*>(k_pool);
   auto* vp = static_cast<uint16_t*>(v_pool);
-#define KVP_SCATTER(DIM, FUSED)                                                                              \
+#define KVP_SCATTER(DIM, NP, FUSED)                                                                          \
   do {                                                                                                        \
-    static const bool attr_ok = cudaFuncSetAttribute(scatter_kernel<DIM, Src, FUSED>,                        \
+    static const bool attr_ok = cudaFuncSetAttribute(scatter_kernel<DIM, NP, Src, FUSED>,                    \
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,            \
-                                                     scatter_smem_bytes<DIM>()) == cudaSuccess;               \
+                                                     scatter_smem_bytes<DIM, NP>()) == cudaSuccess;           \
     if (!attr_ok) return KVP_ERR_CUDA;                                                                        \
-    if (launch_pdl(scatter_kernel<DIM, Src, FUSED>, grid_t, dim3(kWarpsPerCta * 32), scatter_smem_bytes<DIM>(),  \
-                   st, src, now, NS, reserve, max_pages, n_pages_cap, BH, ws,                                 \
+    if (launch_pdl(scatter_kernel<DIM, NP, Src, FUSED>, grid_t, dim3(kWarpsPerCta * 32),                     \
+                   scatter_smem_bytes<DIM, NP>(), st, src, now, NS, reserve, max_pages, n_pages_cap, BH, ws,  \
                    static_cast<const int32_t*>(count), status, kp, vp, expire_pool, page_table,                \
                    remap) != cudaSuccess)                                                                     \
       return KVP_ERR_CUDA;                                                                                    \
   } while (0)
-  if (head_dim == 128) {
-    if (fused) KVP_SCATTER(128, true); else KVP_SCATTER(128, false);
+  if (head_dim == kLatentRow) {  // one pool: the MLA latent rows
+    if constexpr (!std::is_same<Src, QuantSrc>::value) {
+      if (fused) KVP_SCATTER(kLatentRow, 1, true); else KVP_SCATTER(kLatentRow, 1, false);
+    } else {
+      return KVP_ERR_UNSUPPORTED;
+    }
+  } else if (head_dim == 128) {
+    if (fused) KVP_SCATTER(128, 2, true); else KVP_SCATTER(128, 2, false);
   } else {
-    if (fused) KVP_SCATTER(64, true); else KVP_SCATTER(64, false);
+    if (fused) KVP_SCATTER(64, 2, true); else KVP_SCATTER(64, 2, false);
   }
 #undef KVP_SCATTER
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
@@ -1086,6 +1175,108 @@ extern "C" kvp_status kvp_append_quant(int mode, int batch, int n_kv_heads, int 
     append_quant_kernel<64><<<blocks, 256, 0, st>>>(mode, BH, pos, kn, vn, score, tau, tau_q, flag_step, window,
                                                     delay, kq, vq, meta_pool, n_pages_cap, page_table, max_pages,
                                                     remap, count, status);
+  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ MLA latent cache
+// One "kv head" whose entries are latent rows of kLatentRow bf16 values in a
+// single pool; the count, base and copy passes are those of the K/V cache.
+
+static kvp_status check_dst_latent(int row_dim, int reserve, void* pool, int32_t* expire_pool, int n_pages_cap,
+                                   int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                                   int32_t* status) {
+  if (row_dim != kLatentRow) return KVP_ERR_UNSUPPORTED;
+  if (reserve < 0 || n_pages_cap < 0 || max_pages < 0) return KVP_ERR_INVALID;
+  if (pool == nullptr || expire_pool == nullptr || page_table == nullptr || remap == nullptr || count == nullptr ||
+      status == nullptr)
+    return KVP_ERR_INVALID;
+  if (!aligned16(pool)) return KVP_ERR_ALIGN;
+  if (static_cast<int64_t>(max_pages) * kPage > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
+  return KVP_OK;
+}
+
+extern "C" kvp_status kvp_compact_latent(int mode, int batch, int row_dim, int n_pos, const void* lat_src,
+                                         int64_t stride_b, int64_t stride_t, const float* scores, const float* tau,
+                                         const int32_t* flag_step, int window, int delay, int now, int reserve,
+                                         void* pool, int32_t* expire_pool, int n_pages_cap, int32_t* page_table,
+                                         int max_pages, int32_t* remap, int32_t* count, void* workspace,
+                                         size_t workspace_bytes, int32_t* status, void* stream) {
+  if (batch <= 0 || n_pos < 0 || window < 0 || delay < 0) return KVP_ERR_INVALID;
+  if (mode == KVP_MASK_KVZAP) {
+    if (flag_step != nullptr || tau == nullptr || (n_pos > 0 && scores == nullptr)) return KVP_ERR_INVALID;
+  } else if (mode == KVP_MASK_DMS) {
+    if (scores != nullptr || tau != nullptr || (n_pos > 0 && flag_step == nullptr)) return KVP_ERR_INVALID;
+  } else {
+    return KVP_ERR_INVALID;
+  }
+  if (static_cast<int64_t>(n_pos) + window + delay >= kNever) return KVP_ERR_INVALID;
+  kvp_status s = check_dst_latent(row_dim, reserve, pool, expire_pool, n_pages_cap, page_table, max_pages, remap,
+                                  count, status);
+  if (s != KVP_OK) return s;
+  if (n_pos > 0 && lat_src == nullptr) return KVP_ERR_INVALID;
+  if (!aligned16(lat_src) || stride_b % 8 || stride_t % 8) return KVP_ERR_ALIGN;
+  if (stride_b < 0 || stride_t < 0) return KVP_ERR_INVALID;
+  if (workspace == nullptr || workspace_bytes < kvp_compact_workspace_bytes(batch, 1, n_pos))
+    return KVP_ERR_WORKSPACE;
+  const int NS = n_segments(n_pos);
+  const auto* l = static_cast<const uint16_t*>(lat_src);
+  MaskedSrc src{l, l, stride_b, stride_t, 0, mode, scores, tau, flag_step, window, delay, 1, n_pos};
+  return run_compact(src, batch, NS, kLatentRow, now, reserve, pool, nullptr, expire_pool, n_pages_cap, page_table,
+                     max_pages, remap, count, workspace, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvp_status kvp_compact_latent_paged(int batch, int row_dim, const void* src_pool,
+                                               const int32_t* src_expire_pool, int src_n_pages_cap,
+                                               const int32_t* src_page_table, int src_max_pages,
+                                               const int32_t* src_remap, const int32_t* src_count, int now,
+                                               int reserve, void* pool, int32_t* expire_pool, int n_pages_cap,
+                                               int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                                               void* workspace, size_t workspace_bytes, int32_t* status,
+                                               void* stream) {
+  if (batch <= 0 || src_max_pages < 0 || src_n_pages_cap < 0) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(src_max_pages) * kPage > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
+  kvp_status s = check_dst_latent(row_dim, reserve, pool, expire_pool, n_pages_cap, page_table, max_pages, remap,
+                                  count, status);
+  if (s != KVP_OK) return s;
+  if (src_pool == nullptr || src_expire_pool == nullptr || src_page_table == nullptr || src_remap == nullptr ||
+      src_count == nullptr)
+    return KVP_ERR_INVALID;
+  if (!aligned16(src_pool)) return KVP_ERR_ALIGN;
+  if (src_pool == pool || src_count == count || src_page_table == page_table || src_remap == remap ||
+      src_expire_pool == expire_pool)
+    return KVP_ERR_INVALID;
+  if (workspace == nullptr || workspace_bytes < kvp_compact_paged_workspace_bytes(batch, 1, src_max_pages))
+    return KVP_ERR_WORKSPACE;
+  const int NS = n_segments(src_max_pages * kPage);
+  const auto* sp = static_cast<const uint16_t*>(src_pool);
+  PagedSrc src{sp, sp, src_expire_pool, src_page_table, src_remap, src_count, src_max_pages, src_n_pages_cap,
+               kLatentRow, status};
+  return run_compact(src, batch, NS, kLatentRow, now, reserve, pool, nullptr, expire_pool, n_pages_cap, page_table,
+                     max_pages, remap, count, workspace, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvp_status kvp_append_latent(int mode, int batch, int row_dim, int pos, const void* lat_new,
+                                        const float* score, const float* tau, const int32_t* flag_step, int window,
+                                        int delay, void* pool, int32_t* expire_pool, int n_pages_cap,
+                                        const int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                                        int32_t* status, void* stream) {
+  if (batch <= 0 || pos < 0 || window < 0 || delay < 0 || max_pages < 0 || n_pages_cap < 0) return KVP_ERR_INVALID;
+  if (row_dim != kLatentRow) return KVP_ERR_UNSUPPORTED;
+  if (mode == KVP_MASK_KVZAP) {
+    if (score == nullptr || tau == nullptr || flag_step != nullptr) return KVP_ERR_INVALID;
+  } else if (mode == KVP_MASK_DMS) {
+    if (flag_step == nullptr || score != nullptr || tau != nullptr) return KVP_ERR_INVALID;
+  } else {
+    return KVP_ERR_INVALID;
+  }
+  if (lat_new == nullptr || pool == nullptr || expire_pool == nullptr || page_table == nullptr || remap == nullptr ||
+      count == nullptr || status == nullptr)
+    return KVP_ERR_INVALID;
+  if (!aligned16(lat_new) || !aligned16(pool)) return KVP_ERR_ALIGN;
+  if (static_cast<int64_t>(pos) + window + delay >= kNever) return KVP_ERR_INVALID;
+  append_latent_kernel<<<(batch + 7) / 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      mode, batch, pos, static_cast<const uint16_t*>(lat_new), score, tau, flag_step, window, delay,
+      static_cast<uint16_t*>(pool), expire_pool, n_pages_cap, page_table, max_pages, remap, count, status);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 

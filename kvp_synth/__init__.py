@@ -127,7 +127,7 @@ def beta_2_5(seed: int, stream: int, shape) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # Stream ids: one per tensor role, shared by every workload.
 # ---------------------------------------------------------------------------
-S_X, S_W, S_W1, S_W2, S_K, S_V, S_Q, S_FLAG, S_KEEPRATE = 1, 2, 3, 4, 5, 6, 7, 8, 9
+S_X, S_W, S_W1, S_W2, S_K, S_V, S_Q, S_FLAG, S_KEEPRATE, S_LAT = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
 S_STEP = 1000  # + 16 * step + role, for per-decode-step tensors
 
 
@@ -151,6 +151,9 @@ WORKLOADS = {
     # DMS delayed-eviction decode loop, Qwen-3-8B-shaped attention
     "dms_decode": dict(n_q_heads=32, n_kv_heads=8, head_dim=128, batch=64, n_pos=4096,
                        steps=1024, evict_p=7.0 / 8.0, delay=256, recompact_every=64, reserve=64),
+    # MLA latent cache (DeepSeek-V3-shaped attention: 128 query heads, latent rows of 512 + 64),
+    # one decode step over a 8192-token cache
+    "mla_layer": dict(n_q_heads=128, latent_dim=512, rope_dim=64, batch=16, n_pos=8192, prune_q=0.75),
     # Llama-65B-shaped MHA stress, 8 layers, 131072 cached tokens
     "llama65b_mha": dict(n_layers=8, d_model=8192, n_q_heads=64, n_kv_heads=64, head_dim=128,
                          batch=1, n_pos=131072, scorer="linear", steps=32, reserve=32),
@@ -179,6 +182,11 @@ def kv_inputs(seed: int, batch: int, n_pos: int, n_kv_heads: int, head_dim: int,
     k = normal_bf16(seed, S_K + off, (batch, n_pos, n_kv_heads, head_dim))
     v = normal_bf16(seed, S_V + off, (batch, n_pos, n_kv_heads, head_dim))
     return k, v
+
+
+def latent_inputs(seed: int, batch: int, n_pos: int, row: int = 576):
+    """MLA latent rows (compressed KV then rotary key) ~ N(0,1) bf16 [B, T, row]."""
+    return normal_bf16(seed, S_LAT, (batch, n_pos, row))
 
 
 def q_inputs(seed: int, batch: int, n_q_heads: int, head_dim: int, stream: int = S_Q):

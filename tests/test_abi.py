@@ -28,7 +28,8 @@ def test_header_declares_the_path():
     for n in ["kvp_score", "kvp_mask", "kvp_compact", "kvp_compact_masked", "kvp_compact_quant", "kvp_append_quant", "kvp_compact_paged",
               "kvp_threshold", "kvp_append", "kvp_decode_attn",
               "kvp_score_workspace_bytes", "kvp_compact_workspace_bytes", "kvp_decode_attn_workspace_bytes",
-              "kvp_status_string", "kvp_version"]:
+              "kvp_compact_latent", "kvp_compact_latent_paged", "kvp_append_latent", "kvp_decode_attn_mla",
+              "kvp_decode_attn_mla_workspace_bytes", "kvp_status_string", "kvp_version"]:
         assert n in names, n
 
 
@@ -175,6 +176,82 @@ def test_threshold_host_checks():
     assert call(wsb=ws - 4) == k.KVP_ERR_WORKSPACE
     assert call(wsp=None) == k.KVP_ERR_WORKSPACE
     assert call(B=70000, wsb=1 << 40) == k.KVP_ERR_UNSUPPORTED
+
+
+def test_latent_host_checks():
+    """The latent-cache entry points reject bad arguments on the host before
+    any CUDA call: row width other than 512 + 64, mode/input mismatches,
+    missing status, unaligned pools, short workspace, aliased source and
+    destination."""
+    import kv_cache_pruning_gb300 as k
+    L = k.library()
+    ws = L.kvp_compact_workspace_bytes(1, 1, 16)
+
+    def compact(mode=0, row=576, scores=16, tau=16, flag=None, window=128, lat=16, pool=16, status=16, wsb=ws):
+        return L.kvp_compact_latent(mode, 1, row, 16, lat, 0, 576, scores, tau, flag, window, 0, 15, 0, pool, 16, 1,
+                                    16, 1, 16, 16, 16, wsb, status, None)
+
+    assert compact(row=512) == k.KVP_ERR_UNSUPPORTED
+    assert compact(flag=16) == k.KVP_ERR_INVALID                         # KVzap with flags too
+    assert compact(mode=1, flag=16) == k.KVP_ERR_INVALID                 # DMS with scores too
+    assert compact(mode=1, scores=None, tau=None) == k.KVP_ERR_INVALID   # DMS without flags
+    assert compact(tau=None) == k.KVP_ERR_INVALID
+    assert compact(window=-1) == k.KVP_ERR_INVALID
+    assert compact(status=None) == k.KVP_ERR_INVALID
+    assert compact(pool=8) == k.KVP_ERR_ALIGN
+    assert compact(lat=8) == k.KVP_ERR_ALIGN
+    assert compact(wsb=ws - 4) == k.KVP_ERR_WORKSPACE
+    pws = L.kvp_compact_paged_workspace_bytes(1, 1, 2)
+
+    def paged(row=576, src=16, pool=32, cnt_src=16, cnt=48, wsb=pws):
+        return L.kvp_compact_latent_paged(1, row, src, 16, 4, 16, 2, 16, cnt_src, 15, 0, pool, 64, 4, 80, 2, 96, cnt,
+                                          16, wsb, 16, None)
+
+    assert paged(row=640) == k.KVP_ERR_UNSUPPORTED
+    assert paged(pool=16) == k.KVP_ERR_INVALID        # source and destination share the pool
+    assert paged(cnt=16) == k.KVP_ERR_INVALID         # ... or the count
+    assert paged(src=8) == k.KVP_ERR_ALIGN
+    assert paged(wsb=pws - 1) == k.KVP_ERR_WORKSPACE
+
+    def append(mode=0, row=576, pos=5, lat=16, score=16, tau=16, flag=None, status=16):
+        return L.kvp_append_latent(mode, 1, row, pos, lat, score, tau, flag, 128, 0, 16, 16, 1, 16, 1, 16, 16, status,
+                                   None)
+
+    assert append(row=128) == k.KVP_ERR_UNSUPPORTED
+    assert append(pos=-1) == k.KVP_ERR_INVALID
+    assert append(mode=1, flag=16) == k.KVP_ERR_INVALID
+    assert append(mode=1, score=None, tau=None) == k.KVP_ERR_INVALID
+    assert append(status=None) == k.KVP_ERR_INVALID
+    assert append(lat=8) == k.KVP_ERR_ALIGN
+    assert append(pos=2**31 - 100) == k.KVP_ERR_INVALID    # expire would overflow
+
+
+def test_mla_attention_host_checks_and_workspace():
+    import kv_cache_pruning_gb300 as k
+    L = k.library()
+    # counters [units] (16-byte rounded), (m, l) and accumulators per unit, slice and head of the 16-head tile
+    units = 2 * 2      # batch 2, 20 heads -> two 16-head tiles
+    assert L.kvp_decode_attn_mla_workspace_bytes(2, 20, 3) == 16 + units * 3 * 16 * 2 * 4 + units * 3 * 16 * 512 * 4
+    assert L.kvp_decode_attn_mla_workspace_bytes(1, 1, 1) == 16 + 16 * 2 * 4 + 16 * 512 * 4
+    assert L.kvp_decode_attn_mla_workspace_bytes(2, 16, 65) == 0
+    assert L.kvp_decode_attn_mla_workspace_bytes(0, 16, 1) == 0
+    ws = L.kvp_decode_attn_mla_workspace_bytes(2, 20, 3)
+
+    def call(hq=20, dc=512, dr=64, q=16, out=16, ns=3, scale=0.0, wsp=16, wsb=ws, cap=4):
+        return L.kvp_decode_attn_mla(2, hq, dc, dr, q, 16, 16, cap, 16, 2, 16, 30, scale, out, ns, wsp, wsb, None,
+                                     None)
+
+    assert call(dc=256) == k.KVP_ERR_UNSUPPORTED
+    assert call(dr=32) == k.KVP_ERR_UNSUPPORTED
+    assert call(hq=0) == k.KVP_ERR_INVALID
+    assert call(ns=65) == k.KVP_ERR_INVALID
+    assert call(scale=-1.0) == k.KVP_ERR_INVALID
+    assert call(q=None) == k.KVP_ERR_INVALID
+    assert call(q=8) == k.KVP_ERR_ALIGN
+    assert call(out=24) == k.KVP_ERR_ALIGN
+    assert call(wsb=ws - 16) == k.KVP_ERR_WORKSPACE
+    assert call(wsp=None) == k.KVP_ERR_WORKSPACE
+    assert call(cap=2**27) == k.KVP_ERR_UNSUPPORTED   # page rows past 2^31
 
 
 def test_missing_library_fails_loudly(monkeypatch):

@@ -1,0 +1,304 @@
+"""GPU parity of the MLA latent-cache path (DMS article, "주요 요점" and "앞으로의
+전망": the method over Multi-Head Latent Attention's single latent cache)
+against the oracle's section 6: latent compaction, append and re-compaction
+bit-exact, absorbed decode attention within the attention tolerances.
+
+These kernels have not yet run on a GB300; until their first run the file
+is opt-in (KVP_MLA_GPU=1), so that a first failure cannot stop the rest of
+the GPU suite."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import kvp_synth as syn
+import oracle as orc
+from helpers import check_attention, dev_bf16, dev_f32, dev_i32, host_bits, status_word
+
+pytestmark = [
+    pytest.mark.gpu,
+    pytest.mark.skipif(os.environ.get("KVP_MLA_GPU") != "1",
+                       reason="MLA kernels before their first GB300 run: set KVP_MLA_GPU=1"),
+]
+
+DC, DR = 512, 64
+ROW = DC + DR
+
+
+def _compare_latent(gpu, ref: orc.PagedCache):
+    np.testing.assert_array_equal(gpu.count.cpu().numpy(), ref.count[:, 0], err_msg="count")
+    np.testing.assert_array_equal(gpu.page_table.cpu().numpy(), ref.page_table[:, 0], err_msg="page_table")
+    np.testing.assert_array_equal(gpu.remap.cpu().numpy(), ref.remap[:, 0], err_msg="remap")
+    used = ref.pages_used
+    np.testing.assert_array_equal(gpu.expire_pool.cpu().numpy()[:used], ref.expire_pool[:used], err_msg="expire")
+    np.testing.assert_array_equal(host_bits(gpu.pool)[:used], ref.k_pool[:used], err_msg="pool")
+
+
+def _kvzap_latent(B, T, seed, tau_std=0.7, window=128):
+    lat = syn.latent_inputs(seed, B, T, ROW)
+    s = syn.normal_f32(seed, 51, (B, T, 1))
+    tau = syn.normal_f32(seed, 52, (B, 1), std=tau_std)
+    exp = orc.mask_kvzap(s, tau, T - 1, window=window)[0][:, 0].astype(np.int32)   # [B, T]
+    return lat, s, tau, exp
+
+
+@pytest.mark.parametrize("B,T,reserve,window,strided", [
+    (1, 512, 0, 128, False),
+    (2, 3000, 5, 128, True),     # ragged, several segments, rows 640 values apart
+    (3, 17, 16, 8, False),       # tiny ragged, a reserved full page
+    (5, 1030, 64, 32, False),
+])
+def test_compact_latent_kvzap_bit_exact(kvp, B, T, reserve, window, strided):
+    lat, s, tau, exp = _kvzap_latent(B, T, seed=31, window=window)
+    mp = (T + reserve + 15) // 16
+    cap = B * mp
+    now = T - 1
+    ref = orc.compact_latent_dense(lat, exp, now, reserve, cap, mp)
+    src = dev_bf16(lat)
+    if strided:
+        wide = torch.zeros((B, T, ROW + 64), dtype=torch.bfloat16, device="cuda")
+        wide[:, :, :ROW] = src
+        src = wide[:, :, :ROW]
+    st = status_word()
+    dst = kvp.LatentPagedKV.allocate(B, cap, mp)
+    kvp.kvp_compact_latent(src, now, reserve, dst, mode=kvp.KVP_MASK_KVZAP, scores=dev_f32(s[:, :, 0]),
+                           tau=dev_f32(tau[:, 0]), window=window, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_latent(dst, ref)
+
+
+@pytest.mark.parametrize("delay,window", [(256, 128), (40, 100)])
+def test_compact_latent_dms_bit_exact(kvp, delay, window):
+    B, T = 3, 2100
+    lat = syn.latent_inputs(33, B, T, ROW)
+    pos = np.arange(T)[None, :]
+    f = np.where(syn.bernoulli(33, 8, (B, T), 0.875), pos, -1).astype(np.int32)
+    exp = orc.expire_dms(f, pos, delay, window).astype(np.int32)
+    now = T - 1
+    mp = (T + 15) // 16
+    ref = orc.compact_latent_dense(lat, exp, now, 0, B * mp, mp)
+    st = status_word()
+    dst = kvp.LatentPagedKV.allocate(B, B * mp, mp)
+    kvp.kvp_compact_latent(dev_bf16(lat), now, 0, dst, mode=kvp.KVP_MASK_DMS, flag_step=dev_i32(f), delay=delay,
+                           window=window, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_latent(dst, ref)
+
+
+def test_latent_append_then_paged_recompaction(kvp):
+    """Prefill compaction, appends of the next tokens (DMS flags), then a paged
+    re-compaction: bit-exact against the oracle at every stage."""
+    B, T0, steps = 3, 700, 90
+    delay, window, reserve = 60, 32, 96
+    T = T0 + steps
+    lat = syn.latent_inputs(35, B, T, ROW)
+    pos = np.arange(T)[None, :]
+    f = np.where(syn.bernoulli(35, 8, (B, T), 0.875), pos, -1).astype(np.int32)
+    exp = orc.expire_dms(f, pos, delay, window).astype(np.int32)
+    mp = (T + reserve + 15) // 16
+    cap = B * mp
+    now0 = T0 - 1
+    ref = orc.compact_latent_dense(lat[:, :T0], exp[:, :T0], now0, reserve, cap, mp)
+    st = status_word()
+    c = kvp.LatentPagedKV.allocate(B, cap, mp)
+    kvp.kvp_compact_latent(dev_bf16(lat[:, :T0].copy()), now0, reserve, c, mode=kvp.KVP_MASK_DMS,
+                           flag_step=dev_i32(f[:, :T0].copy()), delay=delay, window=window, status=st)
+    ld, fd = dev_bf16(lat), dev_i32(f)
+    for t in range(T0, T):
+        orc.append(ref, lat[:, t][:, None, :], lat[:, t][:, None, :], t, exp[:, t][:, None])
+        kvp.kvp_append_latent(c, ld[:, t].contiguous(), t, mode=kvp.KVP_MASK_DMS, flag_step=fd[:, t].contiguous(),
+                              delay=delay, window=window, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_latent(c, ref)
+    now = T - 1
+    ref2 = orc.compact_paged(ref, now, 16, cap, mp)
+    c2 = kvp.LatentPagedKV.allocate(B, cap, mp)
+    kvp.kvp_compact_latent_paged(c, now, 16, c2, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_latent(c2, ref2)
+
+
+def test_latent_append_kvzap_and_reserve_exhausted(kvp):
+    B, T = 2, 100
+    lat = syn.latent_inputs(36, B, T + 20, ROW)
+    exp = np.full((B, T), orc.NEVER, np.int32)
+    reserve, mp = 12, 8   # 100 + 12 = 112 slots = 7 pages exactly
+    ref = orc.compact_latent_dense(lat[:, :T], exp, T - 1, reserve, 64, mp)
+    st = status_word()
+    c = kvp.LatentPagedKV.allocate(B, 64, mp)
+    kvp.kvp_compact_latent(dev_bf16(lat[:, :T].copy()), T - 1, reserve, c, mode=kvp.KVP_MASK_KVZAP,
+                           scores=dev_f32(np.zeros((B, T), np.float32)), tau=dev_f32(np.zeros(B, np.float32)),
+                           status=st)
+    score = syn.normal_f32(36, 30, (12, B))
+    tau = np.zeros(B, np.float32)
+    for i in range(12):
+        t = T + i
+        orc.append(ref, lat[:, t][:, None, :], lat[:, t][:, None, :], t,
+                   orc.expire_kvzap(score[i], tau, t, 128)[:, None])
+        kvp.kvp_append_latent(c, dev_bf16(lat[:, t].copy()), t, mode=kvp.KVP_MASK_KVZAP, score=dev_f32(score[i]),
+                              tau=dev_f32(tau), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _compare_latent(c, ref)
+    kvp.kvp_append_latent(c, dev_bf16(lat[:, T].copy()), T + 12, mode=kvp.KVP_MASK_KVZAP, score=dev_f32(score[0]),
+                          tau=dev_f32(tau), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == kvp.KVP_ERR_CAPACITY
+    np.testing.assert_array_equal(c.count.cpu().numpy(), ref.count[:, 0])  # unchanged
+
+
+# --------------------------------------------------------------------------- attention
+
+def _mla_case(kvp, B, T, Hq, n_splits=0, seed=37, tau_std=0.7, peaked=False, q_zero=False, workspace=None):
+    lat, s, tau, exp = _kvzap_latent(B, T, seed, tau_std=tau_std)
+    q = syn.q_inputs(seed, B, Hq, ROW)
+    if q_zero:
+        q = np.zeros_like(q)
+    if peaked:  # query x 8 and 16 planted rows equal to head 0's query: a sharp softmax
+        qf = orc.widen_bf16(q) * 8.0
+        q = syn.f32_to_bf16_bits(qf.astype(np.float32))
+        lat, s = lat.copy(), s.copy()
+        for i in range(16):
+            t = (i * 97 + 11) % T
+            s[:, t, 0] = np.float32(1e30)   # kept for good, on both sides
+            lat[:, t, :] = syn.f32_to_bf16_bits((qf[:, 0, :] / 8.0).astype(np.float32))
+        exp = orc.mask_kvzap(s, tau, T - 1)[0][:, 0].astype(np.int32)
+    mp = (T + 15) // 16
+    now = T - 1
+    ref_c = orc.compact_latent_dense(lat, exp, now, 0, B * mp, mp)
+    ref = orc.decode_attention_mla(q, ref_c, DC, now)
+    st = status_word()
+    c = kvp.LatentPagedKV.allocate(B, B * mp, mp)
+    kvp.kvp_compact_latent(dev_bf16(lat), now, 0, c, mode=kvp.KVP_MASK_KVZAP, scores=dev_f32(s[:, :, 0]),
+                           tau=dev_f32(tau[:, 0]), status=st)
+    out = kvp.kvp_decode_attn_mla(dev_bf16(q), c, now, n_splits=n_splits, workspace=workspace, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return out.cpu().numpy(), ref, c, q, now
+
+
+@pytest.mark.parametrize("B,T,Hq,n_splits", [
+    (1, 512, 16, 0),
+    (2, 2000, 16, 3),
+    (3, 1500, 20, 0),      # a ragged head tile (heads 16..19 of a second tile)
+    (1, 3000, 128, 2),     # DeepSeek-V3's 128 heads: 8 tiles read the same pages
+    (2, 700, 1, 1),        # one head, one slice: the output is written without a merge
+    (4, 300, 16, 64),      # more slices than pages: empty slices are skipped by the merge
+    (2, 4100, 32, 0),
+])
+def test_decode_attn_mla(kvp, B, T, Hq, n_splits):
+    o, ref, *_ = _mla_case(kvp, B, T, Hq, n_splits)
+    check_attention(o, ref)
+    # bf16 products are exact in fp32 and p enters as a hi + lo pair (about
+    # 2^-16 relative): the outputs, weighted means of N(0,1) values, stay well
+    # inside 1e-4
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("Hq", [16, 48])
+def test_decode_attn_mla_peaked(kvp, Hq):
+    o, ref, *_ = _mla_case(kvp, 2, 1500, Hq, peaked=True)
+    check_attention(o, ref)
+
+
+def test_decode_attn_mla_zero_query_is_the_mean(kvp):
+    """q = 0: every present row weighs the same, so each head's output is the
+    mean of the kept rows' compressed values (closed form)."""
+    o, _, c, _, now = _mla_case(kvp, 2, 900, 16, q_zero=True)
+    pool = orc.widen_bf16(host_bits(c.pool))
+    ep = c.expire_pool.cpu().numpy()
+    pt = c.page_table.cpu().numpy()
+    cnt = c.count.cpu().numpy()
+    for b in range(2):
+        j = np.arange(cnt[b])
+        pg, r = pt[b, j // 16], j % 16
+        keep = ep[pg, r] > now
+        mean = pool[pg[keep], r[keep], :DC].mean(axis=0)
+        np.testing.assert_allclose(o[b], np.broadcast_to(mean, (16, DC)), rtol=0, atol=2e-5)
+
+
+def test_decode_attn_mla_split_independent(kvp):
+    outs = [_mla_case(kvp, 2, 2500, 16, n_splits=n)[0] for n in (1, 2, 7, 0)]
+    for o in outs[1:]:
+        np.testing.assert_allclose(o, outs[0], rtol=0, atol=1e-5)
+
+
+def test_decode_attn_mla_workspace_reused(kvp):
+    """One zero-filled workspace serves consecutive calls: each result equals a
+    fresh workspace's, and the arrival counters are zero after every call."""
+    B, T, Hq, ns = 2, 1800, 32, 5
+    ws = torch.zeros(kvp.kvp_decode_attn_mla_workspace_bytes(B, Hq, ns), dtype=torch.uint8, device="cuda")
+    for seed in (41, 42, 43):
+        o, _, c, q, now = _mla_case(kvp, B, T, Hq, n_splits=ns, seed=seed, workspace=ws)
+        fresh = kvp.kvp_decode_attn_mla(dev_bf16(q), c, now, n_splits=ns)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(o, fresh.cpu().numpy())
+        units = B * ((Hq + 15) // 16)
+        assert int(ws[: units * 4].view(torch.int32).abs().sum()) == 0
+
+
+def test_decode_attn_mla_empty_batch_element(kvp):
+    """A batch element with no slots gives zero rows; the others are unchanged."""
+    B, T, Hq = 3, 600, 16
+    lat, s, tau, exp = _kvzap_latent(B, T, seed=45, window=0)
+    exp[1, :] = 0          # nothing of batch element 1 is present (score -inf, no window)
+    q = syn.q_inputs(45, B, Hq, ROW)
+    mp = (T + 15) // 16
+    now = T - 1
+    ref = orc.decode_attention_mla(q, orc.compact_latent_dense(lat, exp, now, 0, B * mp, mp), DC, now)
+    st = status_word()
+    c = kvp.LatentPagedKV.allocate(B, B * mp, mp)
+    kvp.kvp_compact_latent(dev_bf16(lat), now, 0, c, mode=kvp.KVP_MASK_KVZAP,
+                           scores=dev_f32(np.where(np.arange(B)[:, None] == 1, -np.inf, s[:, :, 0])
+                                          .astype(np.float32)),
+                           tau=dev_f32(tau[:, 0]), window=0, status=st)
+    torch.cuda.synchronize()
+    assert int(c.count[1]) == 0
+    for ns in (1, 4):
+        out = kvp.kvp_decode_attn_mla(dev_bf16(q), c, now, n_splits=ns, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        o = out.cpu().numpy()
+        assert (o[1] == 0).all()
+        check_attention(o[[0, 2]], ref[[0, 2]])
+
+
+def test_mla_decode_loop(kvp):
+    """DMS decode loop on a latent cache: per step the new row is appended and
+    attention runs; every 24 steps the cache is re-compacted. Each step's
+    output matches the oracle's."""
+    B, T0, steps, Hq = 2, 400, 60, 16
+    delay, window, reserve = 48, 32, 64
+    T = T0 + steps
+    lat = syn.latent_inputs(47, B, T, ROW)
+    pos = np.arange(T)[None, :]
+    f = np.where(syn.bernoulli(47, 8, (B, T), 0.875), pos, -1).astype(np.int32)
+    exp = orc.expire_dms(f, pos, delay, window).astype(np.int32)
+    mp = (T + reserve + 15) // 16
+    cap = B * mp
+    ref = orc.compact_latent_dense(lat[:, :T0], exp[:, :T0], T0 - 1, reserve, cap, mp)
+    st = status_word()
+    c = kvp.LatentPagedKV.allocate(B, cap, mp)
+    kvp.kvp_compact_latent(dev_bf16(lat[:, :T0].copy()), T0 - 1, reserve, c, mode=kvp.KVP_MASK_DMS,
+                           flag_step=dev_i32(f[:, :T0].copy()), delay=delay, window=window, status=st)
+    ld, fd = dev_bf16(lat), dev_i32(f)
+    ws = torch.zeros(kvp.kvp_decode_attn_mla_workspace_bytes(B, Hq, 0), dtype=torch.uint8, device="cuda")
+    for i, t in enumerate(range(T0, T)):
+        if i and i % 24 == 0:
+            ref = orc.compact_paged(ref, t - 1, reserve, cap, mp)
+            c2 = kvp.LatentPagedKV.allocate(B, cap, mp)
+            kvp.kvp_compact_latent_paged(c, t - 1, reserve, c2, status=st)
+            c = c2
+        orc.append(ref, lat[:, t][:, None, :], lat[:, t][:, None, :], t, exp[:, t][:, None])
+        kvp.kvp_append_latent(c, ld[:, t].contiguous(), t, mode=kvp.KVP_MASK_DMS, flag_step=fd[:, t].contiguous(),
+                              delay=delay, window=window, status=st)
+        q = syn.q_inputs(47, B, Hq, ROW, stream=syn.step_stream(i, 3))
+        o = kvp.kvp_decode_attn_mla(dev_bf16(q), c, t, workspace=ws, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        check_attention(o.cpu().numpy(), orc.decode_attention_mla(q, ref, DC, t))
