@@ -472,7 +472,7 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs only)")
     ap.add_argument("--workload", default="llama3_8b_layer",
                     choices=["llama3_8b_layer", "mlp_prefill", "dms_decode", "llama65b_mha", "prune_sweep",
-                             "threshold", "quant_tier", "quant_decode", "gqa_sweep", "mla_sweep"],
+                             "threshold", "quant_tier", "quant_decode", "gqa_sweep", "mla_sweep", "mla_dms_decode"],
                     help="llama3_8b_layer = the bench line; the others print measurement lines "
                          "(see bench_workloads.py)")
     ap.add_argument("--eager", action="store_true", help="launch every step from the host (no CUDA graph)")

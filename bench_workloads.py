@@ -660,9 +660,79 @@ def mla_sweep(kvp, dev, peaks, seed=0, calls=10, reps=5):
             "points": points}
 
 
+def mla_dms_decode(kvp, dev, peaks, seed=0, steps=256):
+    """The DMS decode loop on an MLA latent cache (rows of 512 + 64 values):
+    batch 64, 4,096-token prompt, then per step the new latent row is
+    appended and absorbed attention runs over the present rows; every 64
+    steps the cache is re-compacted. Run with 16 and with 128 query heads.
+    Bytes count the surviving pages read by the attention steps."""
+    B, T0, delay, W, every, reserve = 64, 4096, 256, 128, 64, 64
+    row, dc = kvp.LATENT_ROW, kvp.KVP_MLA_LATENT_DIM
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    lat = _randn_bf16((B, T0, row), g, dev)
+    pos = torch.arange(T0, device=dev, dtype=torch.int32)
+    f0 = torch.where(torch.rand((B, T0), generator=g, device=dev) < 7 / 8, pos, -1).to(torch.int32)
+    ls = _randn_bf16((steps, B, row), g, dev)
+    tpos = (T0 + torch.arange(steps, device=dev, dtype=torch.int32)).view(steps, 1)
+    fs = torch.where(torch.rand((steps, B), generator=g, device=dev) < 7 / 8, tpos, -1).to(torch.int32)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    now0 = T0 - 1
+    mp = (T0 + steps + reserve + 15) // 16
+    pools = [kvp.LatentPagedKV.allocate(B, B * mp, mp, device=dev) for _ in range(2)]
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, 1, T0), dtype=torch.uint8, device=dev)
+    ws_p = torch.empty(kvp.kvp_compact_paged_workspace_bytes(B, 1, mp), dtype=torch.uint8, device=dev)
+    points = []
+    for Hq in (16, 128):
+        qs = _randn_bf16((steps, B, Hq, row), g, dev)
+        out = torch.empty(steps, B, Hq, dc, dtype=torch.float32, device=dev)
+        ws_a = torch.zeros(kvp.kvp_decode_attn_mla_workspace_bytes(B, Hq, 0), dtype=torch.uint8, device=dev)
+        pages_read = torch.zeros((), dtype=torch.int64, device=dev)
+
+        def prefill():
+            kvp.kvp_compact_latent(lat, now0, reserve, pools[0], mode=kvp.KVP_MASK_DMS, flag_step=f0, delay=delay,
+                                   window=W, workspace=ws_c, status=st)
+
+        def decode(count_pages=False):
+            cur = 0
+            for i in range(steps):
+                t = T0 + i
+                if i > 0 and i % every == 0:
+                    kvp.kvp_compact_latent_paged(pools[cur], t, reserve, pools[1 - cur], workspace=ws_p, status=st)
+                    cur = 1 - cur
+                c = pools[cur]
+                kvp.kvp_append_latent(c, ls[i], t, mode=kvp.KVP_MASK_DMS, flag_step=fs[i], delay=delay, window=W,
+                                      status=st)
+                kvp.kvp_decode_attn_mla(qs[i], c, t, out=out[i], workspace=ws_a, status=st)
+                if count_pages:
+                    pages_read.add_(((c.count + 15) // 16).sum())
+
+        prefill()
+        decode(count_pages=True)  # eager pass: algorithmic bytes of the attention steps
+        torch.cuda.synchronize()
+        assert st.item() == 0, kvp.status_string(st.item())
+        total_pages = int(pages_read.item())
+        prefill()
+        replay = _graph(decode)
+        ms_pref = _time(prefill, reps=3)
+        ms = _time(lambda: (prefill(), replay()), reps=3) - ms_pref
+        torch.cuda.synchronize()
+        assert st.item() == 0, kvp.status_string(st.item())
+        attn_bytes = total_pages * (16 * row * 2 + 64)
+        points.append({"q_heads": Hq, "decode_ms_per_step": ms / steps, "decode_tokens_per_s": B * steps / (ms * 1e-3),
+                       "attn_pages_read_total": total_pages, "attn_bytes_total": attn_bytes,
+                       "frac_of_hbm": attn_bytes / (ms * 1e-3) / 1e9 / peaks[0],
+                       "dense_latent_bytes_last_step": B * (T0 + steps) * row * 2})
+    return {"workload": f"mla_dms_decode: MLA latent cache, batch 64, 4096-token prompt + {steps} steps, rows of "
+                        "512 + 64, evict ~Bernoulli(7/8), delay 256, window 128, re-compaction every 64 steps; 16 and "
+                        "128 query heads",
+            "points": points}
+
+
 RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha,
            "prune_sweep": prune_sweep, "threshold": threshold,
-           "quant_tier": quant_tier, "quant_decode": quant_decode, "gqa_sweep": gqa_sweep, "mla_sweep": mla_sweep}
+           "quant_tier": quant_tier, "quant_decode": quant_decode, "gqa_sweep": gqa_sweep, "mla_sweep": mla_sweep,
+           "mla_dms_decode": mla_dms_decode}
 
 
 def run(name, kvp, dev, peaks):
