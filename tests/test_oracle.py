@@ -710,3 +710,35 @@ def test_mla_latent_pruning_special_cases():
     assert int(c.count[0, 0]) == 40
     np.testing.assert_array_equal(c.remap[0, 0, :40], np.arange(T - 40, T))
     np.testing.assert_allclose(orc.decode_attention_mla(q, c, dc, now), brute(T - 40), rtol=0, atol=1e-6)
+
+
+def test_mla_attention_closed_forms():
+    """Closed forms of the latent attention: q = 0 weighs every present row the
+    same (the mean of their compressed parts); a row whose logit is 60 above
+    every other one takes all the weight (its compressed part, to e^-60); a
+    row that has expired by `now` takes none."""
+    rng = np.random.default_rng(23)
+    B, T, dc, dr = 1, 120, 32, 8
+    lat = syn.f32_to_bf16_bits(rng.standard_normal((B, T, dc + dr)).astype(np.float32))
+    now = T - 1
+    mp = T // 16 + 2
+    exp = np.full((B, T), orc.NEVER)
+    exp[0, 10:30] = now          # gone at `now`: never present
+    cache = orc.compact_latent_dense(lat, exp, now, 0, B * mp, mp)
+    L = orc.widen_bf16(lat)[0]
+    keep = np.ones(T, bool)
+    keep[10:30] = False
+    q0 = np.zeros((B, 1, dc + dr), np.uint16)
+    np.testing.assert_allclose(orc.decode_attention_mla(q0, cache, dc, now)[0, 0], L[keep, :dc].mean(axis=0),
+                               rtol=0, atol=1e-6)
+    # a query along row 50's direction, scaled so its logit leads by more than 60
+    j = 50
+    u = L[j] / np.linalg.norm(L[j])
+    others = np.delete(L[keep], np.flatnonzero(np.flatnonzero(keep) == j), axis=0)
+    gap = np.linalg.norm(L[j]) - (others @ u).max()
+    assert gap > 0
+    q = syn.f32_to_bf16_bits((u * (64.0 / gap) * math.sqrt(dc + dr)).astype(np.float32))[None, None]
+    qf = orc.widen_bf16(q)[0, 0]
+    logits = (L[keep] @ qf) / math.sqrt(dc + dr)
+    assert np.sort(logits)[-1] - np.sort(logits)[-2] > 60
+    np.testing.assert_allclose(orc.decode_attention_mla(q, cache, dc, now)[0, 0], L[j, :dc], rtol=1e-6, atol=1e-20)
