@@ -81,6 +81,8 @@ _SIGS = {
                                 _I, _P, _I, _P, _P, _P, _S, _P, _P]),
     "kvp_compact_quant": (_I, [_I, _I, _I, _I, _I, _P, _P, _L, _L, _L, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
                                _I, _P, _I, _P, _P, _P, _S, _P, _P]),
+    "kvp_compact_noalloc": (_I, [_I, _I, _I, _I, _P, _P, _L, _L, _L, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
+                                 _P, _P]),
     "kvp_compact_paged_workspace_bytes": (_S, [_I, _I, _I]),
     "kvp_compact_paged": (_I, [_I, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I,
                                _P, _P, _P, _S, _P, _P]),
@@ -366,6 +368,27 @@ def kvp_compact(k, v, expire, now, reserve, dst: PagedKV, *, status, workspace=N
                             _ptr(dst.count, torch.int32), ws.data_ptr(), ws.numel() * ws.element_size(),
                             _ptr(status, torch.int32, "status"), _stream(stream))
     _check("kvp_compact", code)
+    return dst
+
+
+def kvp_compact_noalloc(k, v, expire, now, reserve, dst: PagedKV, *, status, stream=None):
+    """kvp_compact with its scratch in the library's fixed device array: allocates nothing (not even through
+    torch). The first call on a device looks the array's address up, so make it before any stream capture; calls
+    that overlap on the GPU race on the array."""
+    B, T, H, d = k.shape
+    if k.stride() != v.stride() or k.stride(3) != 1:
+        raise ValueError("k and v need identical strides with the head_dim axis contiguous")
+    for t, nm in ((k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{nm} must be a CUDA bf16 tensor")
+    code = _lib.kvp_compact_noalloc(B, H, d, T, k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), k.stride(2),
+                                    _ptr(expire, torch.int32, "expire"), now, reserve,
+                                    _ptr(dst.k_pool, torch.bfloat16), _ptr(dst.v_pool, torch.bfloat16),
+                                    _ptr(dst.expire_pool, torch.int32), dst.n_pages_cap,
+                                    _ptr(dst.page_table, torch.int32), dst.max_pages, _ptr(dst.remap, torch.int32),
+                                    _ptr(dst.count, torch.int32), _ptr(status, torch.int32, "status"),
+                                    _stream(stream))
+    _check("kvp_compact_noalloc", code)
     return dst
 
 

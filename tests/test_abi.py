@@ -259,3 +259,56 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(k, "LIB_PATH", os.path.join(ROOT, "no_such_libkvp.so"))
     with pytest.raises(ImportError):
         k._load()
+
+
+def _prototypes():
+    """name -> (return type text, [parameter type texts]) for every KVP_API prototype of kvp.h."""
+    with open(os.path.join(ROOT, "include", "kvp.h")) as f:
+        text = re.sub(r"/\*.*?\*/", " ", f.read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"KVP_API\s+([^;(]*?)\b(kvp_\w+)\s*\(([^;]*?)\)\s*;", text, flags=re.S):
+        ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+        plist = [] if params in ("", "void") else [" ".join(p.split()) for p in params.split(",")]
+        # drop the parameter name: the last identifier (a pointer star stays with the type)
+        types = [re.sub(r"\s*\b\w+$", "", p).strip() for p in plist]
+        out[name] = (ret, types)
+    return out
+
+
+def _ctype_of(c_type: str):
+    if "*" in c_type:
+        return ctypes.c_char_p if c_type.replace(" ", "") == "constchar*" else ctypes.c_void_p
+    base = c_type.replace("const ", "").strip()
+    return {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t, "float": ctypes.c_float,
+            "double": ctypes.c_double, "kvp_status": ctypes.c_int}[base]
+
+
+def test_binding_signatures_match_the_header():
+    """Every entry point of kvp.h is bound in the Python package with the
+    ctypes argument and return types its C prototype implies (a wrong width,
+    say int for int64_t, would pass silently through ctypes otherwise)."""
+    import kv_cache_pruning_gb300 as k
+    protos = _prototypes()
+    assert set(protos) == set(_declared())
+    for name, (ret, params) in protos.items():
+        assert name in k._SIGS, f"{name} has no binding"
+        res, args = k._SIGS[name]
+        assert res == _ctype_of(ret), f"{name}: return {ret} bound as {res}"
+        assert len(args) == len(params), f"{name}: {len(params)} parameters, {len(args)} bound"
+        for i, (c, a) in enumerate(zip(params, args)):
+            assert a == _ctype_of(c), f"{name} parameter {i} ({c}) bound as {a}"
+
+
+def test_header_constants_match_the_binding():
+    import kv_cache_pruning_gb300 as k
+    with open(os.path.join(ROOT, "include", "kvp.h")) as f:
+        text = f.read()
+    defines = {m.group(1): int(m.group(2)) for m in re.finditer(r"^#define\s+(KVP_\w+)\s+(\d+)", text, flags=re.M)}
+    assert defines["KVP_PAGE_TOKENS"] == k.PAGE
+    assert defines["KVP_WINDOW_DEFAULT"] == k.WINDOW
+    assert defines["KVP_EXPIRE_NEVER"] == k.EXPIRE_NEVER
+    assert defines["KVP_MLA_LATENT_DIM"] == k.KVP_MLA_LATENT_DIM
+    assert defines["KVP_MLA_ROPE_DIM"] == k.KVP_MLA_ROPE_DIM
+    enums = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(KVP_(?:ERR|OK|SCORER|MASK)\w*)\s*=\s*(\d+)", text)}
+    for name, value in enums.items():
+        assert getattr(k, name) == value, name
