@@ -278,9 +278,10 @@ def append(cache: PagedCache, k_new_bits, v_new_bits, pos: int, expire_new):
 # ---------------------------------------------------------------------------
 
 def _softmax_attend(q, K, V, scale):
-    """One query q [d] over rows K, V [n, d] (float64). Two-pass softmax."""
+    """One query q [dk] over rows K [n, dk], V [n, dv] (float64). Two-pass
+    softmax; an empty set gives a zero row of V's width."""
     if K.shape[0] == 0:
-        return np.zeros(q.shape[0])
+        return np.zeros(V.shape[1])
     logits = (K @ q) * scale
     m = logits.max()
     w = np.exp(logits - m)

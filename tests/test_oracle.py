@@ -742,3 +742,22 @@ def test_mla_attention_closed_forms():
     logits = (L[keep] @ qf) / math.sqrt(dc + dr)
     assert np.sort(logits)[-1] - np.sort(logits)[-2] > 60
     np.testing.assert_allclose(orc.decode_attention_mla(q, cache, dc, now)[0, 0], L[j, :dc], rtol=1e-6, atol=1e-20)
+
+
+def test_mla_attention_empty_batch_element():
+    """A batch element with no present latent row gives a zero row of the
+    compressed width (dc values, not the row's dc + dr); the others are
+    unaffected."""
+    rng = np.random.default_rng(24)
+    B, T, Hq, dc, dr = 2, 40, 3, 16, 8
+    lat = syn.f32_to_bf16_bits(rng.standard_normal((B, T, dc + dr)).astype(np.float32))
+    q = syn.f32_to_bf16_bits(rng.standard_normal((B, Hq, dc + dr)).astype(np.float32))
+    exp = np.full((B, T), orc.NEVER)
+    exp[1] = 0
+    now = T - 1
+    c = orc.compact_latent_dense(lat, exp, now, 0, B * 4, 4)
+    o = orc.decode_attention_mla(q, c, dc, now)
+    assert o.shape == (B, Hq, dc)
+    assert (o[1] == 0).all()
+    alone = orc.decode_attention_mla(q[:1], orc.compact_latent_dense(lat[:1], exp[:1], now, 0, 4, 4), dc, now)
+    np.testing.assert_array_equal(o[0], alone[0])
