@@ -557,7 +557,7 @@ KVP_API kvp_status kvp_append_latent(int mode, int batch, int row_dim, int pos, 
  * scale      > 0, or 0 for 1/sqrt(latent_dim + rope_dim)
  * out        device fp32 [B, n_q_heads, latent_dim], 16-byte aligned
  * n_splits   slices per unit, 1..64; 0 picks one from the current device's
- *            SM count (about two CTAs per SM in all)
+ *            SM count (as many as fill one wave of two CTAs per SM, at least 1)
  * workspace  device, >= kvp_decode_attn_mla_workspace_bytes(batch,
  *            n_q_heads, n_splits) (asked on the device that runs the call
  *            when n_splits = 0), 16-byte aligned; zero-filled before its

@@ -444,11 +444,13 @@ int sm_count() {
 
 int n_tiles(int n_q_heads) { return (n_q_heads + kHT - 1) / kHT; }
 
-// Slices per unit: about two CTAs per SM over the whole grid.
+// Slices per unit: as many as one wave of CTAs holds (two per SM), so no
+// CTA waits for a second wave (128 units on 152 SMs: 2 slices, 256 CTAs,
+// rather than 3 slices and 384 CTAs in 1.26 waves); at least one.
 int pick_splits(int batch, int n_q_heads) {
   const int nsm = sm_count();
   const int64_t units = static_cast<int64_t>(batch) * n_tiles(n_q_heads);
-  const int64_t want = (2 * static_cast<int64_t>(nsm > 0 ? nsm : 1) + units - 1) / units;
+  const int64_t want = 2 * static_cast<int64_t>(nsm > 0 ? nsm : 1) / units;
   return static_cast<int>(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
 }
 
