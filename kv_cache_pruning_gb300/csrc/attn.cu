@@ -898,10 +898,6 @@ KVP_DEV uint32_t bf16x2_to_f16x2(uint32_t w) {
   const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
   return *reinterpret_cast<const uint32_t*>(&h);
 }
-KVP_DEV uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
 
 // kQ: the two-tier kernel. A fp8-tier page arrives as its E4M3 codes (1-D
 // bulk copies into the upper half of the stage) and its record (start steps,
