@@ -85,6 +85,19 @@ KVP_API const char* kvp_status_string(int status);
 /* Library version, major*10000 + minor*100 + patch. */
 KVP_API int kvp_version(void);
 
+/* kvp_selftest_wait - exercises the bounded wait that every kernel of this
+ * library puts on its mbarriers (no page describes it; it is the library's
+ * failure handling). One warp waits on an mbarrier that nothing arrives on;
+ * after limit_ns of wall time (the %globaltimer clock, checked every 1024
+ * probes; 0 gives up at the second check) the wait gives up, KVP_ERR_TIMEOUT
+ * is recorded in `status` and the kernel returns, leaving the context usable.
+ *
+ * limit_ns   at most 10 s (else KVP_ERR_INVALID)
+ * status     device int32 (required), as in every other call
+ * waited_us  device uint32 (or NULL): microseconds the wait lasted
+ */
+KVP_API kvp_status kvp_selftest_wait(uint64_t limit_ns, int32_t* status, uint32_t* waited_us, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* kvp_score - KVzap surrogate scores (KVzap summary, "KVzap의 구조",
  * "실제 적용").

@@ -99,6 +99,7 @@ _SIGS = {
     "kvp_compact_latent_paged": (_I, [_I, _I, _P, _P, _I, _P, _I, _P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _P,
                                       _S, _P, _P]),
     "kvp_append_latent": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P]),
+    "kvp_selftest_wait": (_I, [ctypes.c_uint64, _P, _P, _P]),
     "kvp_decode_attn_mla_workspace_bytes": (_S, [_I, _I, _I]),
     "kvp_decode_attn_mla": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _I, _P, _S, _P, _P]),
 }
@@ -561,6 +562,15 @@ def kvp_decode_attn_two_tier(q, cache: PagedKV, qcache: QuantPagedKV, now, *, sc
         _ptr(status, torch.int32, "status", True), _stream(stream))
     _check("kvp_decode_attn_two_tier", code)
     return out
+
+
+def kvp_selftest_wait(limit_ns, *, status, waited_us=None, stream=None):
+    """One warp waits on an mbarrier that nothing arrives on, with the bounded wait every kernel uses: after
+    limit_ns it records KVP_ERR_TIMEOUT in status (device int32) and returns; waited_us (device uint32 [1], or
+    None) receives how long the wait lasted."""
+    code = _lib.kvp_selftest_wait(int(limit_ns), _ptr(status, torch.int32, "status"),
+                                  _ptr(waited_us, None, "waited_us", True), _stream(stream))
+    _check("kvp_selftest_wait", code)
 
 
 # --------------------------------------------------------------------------- MLA latent cache

@@ -97,12 +97,12 @@ KVP_DEV uint64_t globaltimer_ns() {
   return t;
 }
 // Waits for the phase of parity `parity` to complete. Gives up (returns
-// false) after about kWaitLimitNs, as soon as *local_abort becomes nonzero, or
+// false) after about limit_ns, as soon as *local_abort becomes nonzero, or
 // once *status holds KVP_ERR_TIMEOUT (another CTA already gave up). The clock
 // and the status word are only consulted every 1024 probes, so a short wait
 // costs nothing but the barrier probes themselves.
 KVP_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* local_abort = nullptr,
-                       const volatile int32_t* status = nullptr) {
+                       const volatile int32_t* status = nullptr, uint64_t limit_ns = kWaitLimitNs) {
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -112,7 +112,7 @@ KVP_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* local
       const uint64_t now = globaltimer_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
+      } else if (now - t0 > limit_ns) {
         return false;
       }
     }

@@ -279,8 +279,8 @@ def _ctype_of(c_type: str):
     if "*" in c_type:
         return ctypes.c_char_p if c_type.replace(" ", "") == "constchar*" else ctypes.c_void_p
     base = c_type.replace("const ", "").strip()
-    return {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t, "float": ctypes.c_float,
-            "double": ctypes.c_double, "kvp_status": ctypes.c_int}[base]
+    return {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "uint64_t": ctypes.c_uint64, "size_t": ctypes.c_size_t,
+            "float": ctypes.c_float, "double": ctypes.c_double, "kvp_status": ctypes.c_int}[base]
 
 
 def test_binding_signatures_match_the_header():
@@ -312,3 +312,10 @@ def test_header_constants_match_the_binding():
     enums = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(KVP_(?:ERR|OK|SCORER|MASK)\w*)\s*=\s*(\d+)", text)}
     for name, value in enums.items():
         assert getattr(k, name) == value, name
+
+
+def test_selftest_wait_host_checks():
+    import kv_cache_pruning_gb300 as k
+    L = k.library()
+    assert L.kvp_selftest_wait(1000, None, None, None) == k.KVP_ERR_INVALID            # status is required
+    assert L.kvp_selftest_wait(10**10 + 1, 16, None, None) == k.KVP_ERR_INVALID        # more than 10 s

@@ -6,7 +6,7 @@ bit-exact, absorbed decode attention within the attention tolerances.
 The attention tests have passed on a GB300. The tests marked not_yet_run
 (bit-exact latent compaction, append, re-compaction, the decode loop, an
 empty batch element) have not run there yet; until they have, they are
-opt-in (KVP_MLA_GPU=1), so that a first failure cannot stop the rest of the
+opt-in (KVP_GPU_NOT_YET_RUN=1), so that a first failure cannot stop the rest of the
 GPU suite."""
 import os
 
@@ -19,8 +19,8 @@ import oracle as orc
 from helpers import check_attention, dev_bf16, dev_f32, dev_i32, host_bits, status_word
 
 pytestmark = pytest.mark.gpu
-not_yet_run = pytest.mark.skipif(os.environ.get("KVP_MLA_GPU") != "1",
-                                 reason="not yet run on a GB300: set KVP_MLA_GPU=1")
+not_yet_run = pytest.mark.skipif(os.environ.get("KVP_GPU_NOT_YET_RUN") != "1",
+                                 reason="not yet run on a GB300: set KVP_GPU_NOT_YET_RUN=1")
 
 DC, DR = 512, 64
 ROW = DC + DR
