@@ -1,11 +1,8 @@
 """Guard bands around every output and workspace (a substitute for a memory
 checker): each buffer a call writes sits between two 4 KiB bands of a
 sentinel byte, workspaces are exactly the size the library asks for, and
-after the calls every band must be intact and every status word zero.
-
-Not yet run on a GB300: opt-in (KVP_GPU_NOT_YET_RUN=1) until then."""
+after the calls every band must be intact and every status word zero."""
 import math
-import os
 
 import numpy as np
 import pytest
@@ -15,11 +12,7 @@ import kvp_synth as syn
 import oracle as orc
 from helpers import dev_bf16, dev_f32, dev_i32, status_word
 
-pytestmark = [
-    pytest.mark.gpu,
-    pytest.mark.skipif(os.environ.get("KVP_GPU_NOT_YET_RUN") != "1",
-                       reason="not yet run on a GB300: set KVP_GPU_NOT_YET_RUN=1"),
-]
+pytestmark = pytest.mark.gpu
 
 GUARD = 4096
 SENTINEL = 0x5A
@@ -60,6 +53,16 @@ def check_bands():
     bad = [i for i, b in enumerate(Guarded.bands) if not b.intact()]
     Guarded.bands = []
     assert not bad, f"guard bands overwritten: buffers {bad}"
+
+
+@pytest.fixture(autouse=True)
+def _fresh_bands():
+    """Every test starts with no guarded buffers and drops its own at the end,
+    even when it fails before check_bands(): a failure is never blamed on the
+    next test, and no device memory is held across tests."""
+    Guarded.bands = []
+    yield
+    Guarded.bands = []
 
 
 def test_canaries_decode_path(kvp):

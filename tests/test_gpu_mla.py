@@ -3,12 +3,7 @@
 against the oracle's section 6: latent compaction, append and re-compaction
 bit-exact, absorbed decode attention within the attention tolerances.
 
-The attention tests have passed on a GB300. The tests marked not_yet_run
-(bit-exact latent compaction, append, re-compaction, the decode loop, an
-empty batch element) have not run there yet; until they have, they are
-opt-in (KVP_GPU_NOT_YET_RUN=1), so that a first failure cannot stop the rest of the
-GPU suite."""
-import os
+Every test here has passed on a GB300."""
 
 import numpy as np
 import pytest
@@ -19,8 +14,6 @@ import oracle as orc
 from helpers import check_attention, dev_bf16, dev_f32, dev_i32, host_bits, status_word
 
 pytestmark = pytest.mark.gpu
-not_yet_run = pytest.mark.skipif(os.environ.get("KVP_GPU_NOT_YET_RUN") != "1",
-                                 reason="not yet run on a GB300: set KVP_GPU_NOT_YET_RUN=1")
 
 DC, DR = 512, 64
 ROW = DC + DR
@@ -43,7 +36,6 @@ def _kvzap_latent(B, T, seed, tau_std=0.7, window=128):
     return lat, s, tau, exp
 
 
-@not_yet_run
 @pytest.mark.parametrize("B,T,reserve,window,strided", [
     (1, 512, 0, 128, False),
     (2, 3000, 5, 128, True),     # ragged, several segments, rows 640 values apart
@@ -70,7 +62,6 @@ def test_compact_latent_kvzap_bit_exact(kvp, B, T, reserve, window, strided):
     _compare_latent(dst, ref)
 
 
-@not_yet_run
 @pytest.mark.parametrize("delay,window", [(256, 128), (40, 100)])
 def test_compact_latent_dms_bit_exact(kvp, delay, window):
     B, T = 3, 2100
@@ -90,7 +81,6 @@ def test_compact_latent_dms_bit_exact(kvp, delay, window):
     _compare_latent(dst, ref)
 
 
-@not_yet_run
 def test_latent_append_then_paged_recompaction(kvp):
     """Prefill compaction, appends of the next tokens (DMS flags), then a paged
     re-compaction: bit-exact against the oracle at every stage."""
@@ -126,7 +116,6 @@ def test_latent_append_then_paged_recompaction(kvp):
     _compare_latent(c2, ref2)
 
 
-@not_yet_run
 def test_latent_append_kvzap_and_reserve_exhausted(kvp):
     B, T = 2, 100
     lat = syn.latent_inputs(36, B, T + 20, ROW)
@@ -246,7 +235,6 @@ def test_decode_attn_mla_workspace_reused(kvp):
         assert int(ws[: units * 4].view(torch.int32).abs().sum()) == 0
 
 
-@not_yet_run
 def test_decode_attn_mla_empty_batch_element(kvp):
     """A batch element with no slots gives zero rows; the others are unchanged."""
     B, T, Hq = 3, 600, 16
@@ -273,7 +261,6 @@ def test_decode_attn_mla_empty_batch_element(kvp):
         check_attention(o[[0, 2]], ref[[0, 2]])
 
 
-@not_yet_run
 def test_mla_decode_loop(kvp):
     """DMS decode loop on a latent cache: per step the new row is appended and
     attention runs; every 24 steps the cache is re-compacted. Each step's

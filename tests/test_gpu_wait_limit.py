@@ -4,8 +4,7 @@ caller's status word and returns, and the context stays usable.
 
 kvp_selftest_wait makes one warp wait on an mbarrier that nothing arrives on
 (a flag that nothing sets), so the wait must run out; nothing traps, faults or
-hangs. Not yet run on a GB300: opt-in (KVP_GPU_NOT_YET_RUN=1) until then."""
-import os
+hangs."""
 
 import numpy as np
 import pytest
@@ -15,11 +14,7 @@ import kvp_synth as syn
 import oracle as orc
 from helpers import check_attention, dev_bf16, dev_i32, status_word
 
-pytestmark = [
-    pytest.mark.gpu,
-    pytest.mark.skipif(os.environ.get("KVP_GPU_NOT_YET_RUN") != "1",
-                       reason="not yet run on a GB300: set KVP_GPU_NOT_YET_RUN=1"),
-]
+pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("limit_ns", [0, 1_000_000, 20_000_000])
