@@ -165,13 +165,19 @@ def mask_dms(flag_step_bht, now: int, delay: int, window: int = WINDOW, pos0: in
     return (exp,) + mask(exp, now)
 
 
-def threshold_at_quantile(scores_bth: np.ndarray, q: float) -> np.ndarray:
+def threshold_at_quantile(scores_bth: np.ndarray, q) -> np.ndarray:
     """Per-(b, h) threshold: the lower order statistic at index floor(q*(T-1))
     of that head's T scores, rounded to float32 (the threshold is a float32
-    input of the masking step). A harness choice, not part of the method."""
+    input of the masking step). A harness choice, not part of the method.
+    q is one quantile for every head, or one per kv head (shape [H]), as for
+    heads with their own keep rates."""
     s = np.sort(np.asarray(scores_bth, dtype=np.float64), axis=1)
-    T = s.shape[1]
-    return s[:, int(math.floor(q * (T - 1))), :].astype(np.float32)
+    B, T, H = s.shape
+    if np.ndim(q) == 0:
+        return s[:, int(math.floor(q * (T - 1))), :].astype(np.float32)
+    k = np.floor(np.asarray(q, dtype=np.float64) * (T - 1)).astype(np.int64)
+    assert k.shape == (H,)
+    return s[:, k, np.arange(H)].astype(np.float32)
 
 
 # ---------------------------------------------------------------------------

@@ -11,7 +11,15 @@ import torch
 from scipy.stats import norm
 
 import kvp_synth as syn
-import oracle as orc
+import oracle
+
+# every pin runs against both implementations of the oracle: the C++ one and the numpy one
+IMPLS = {"cpp": oracle.cpp_impl, "numpy": oracle.numpy_impl}
+
+
+@pytest.fixture(params=sorted(IMPLS))
+def orc(request):
+    return IMPLS[request.param]
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -22,7 +30,13 @@ def _gold(name):
 
 
 def _exp_list(v):
-    return [orc.NEVER if e == "never" else e for e in v]
+    return [oracle.NEVER if e == "never" else e for e in v]
+
+
+def _widen(bits):
+    """bf16 bits -> float64 through torch's own bfloat16 type (a library routine)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
 
 
 def _bits(a):
@@ -31,7 +45,7 @@ def _bits(a):
 
 # --------------------------------------------------------------------------- score
 
-def test_widen_bf16_exact():
+def test_widen_bf16_exact(orc):
     vals = np.array([0.0, 1.0, -2.5, 0.1015625, 3.0e38, -1.0e-38], dtype=np.float32)
     b = _bits(vals)
     back = orc.widen_bf16(b)
@@ -41,7 +55,7 @@ def test_widen_bf16_exact():
     assert orc.widen_bf16(np.array([0xC000], np.uint16))[0] == -2.0
 
 
-def test_score_linear_unit_columns_pick_inputs():
+def test_score_linear_unit_columns_pick_inputs(orc):
     # W[h] = e_{k_h}: head h must read exactly column k_h of x (catches a transposed W)
     rng = np.random.default_rng(1)
     n, D, H = 37, 48, 5
@@ -56,7 +70,7 @@ def test_score_linear_unit_columns_pick_inputs():
         np.testing.assert_array_equal(s[:, h], xf[:, k])
 
 
-def test_score_linear_bias_and_full_sum():
+def test_score_linear_bias_and_full_sum(orc):
     D, H = 64, 3
     x = _bits(np.ones((4, D)))
     W = np.tile(np.arange(D, dtype=np.float32), (H, 1)) * np.array([[1], [2], [-1]], np.float32)
@@ -67,7 +81,7 @@ def test_score_linear_bias_and_full_sum():
     np.testing.assert_array_equal(s0, np.tile([1.0, 2.0, 3.0], (4, 1)))
 
 
-def test_gelu_matches_textbook_phi():
+def test_gelu_matches_textbook_phi(orc):
     g = _gold("gelu_phi.json")
     for p in g["points"]:
         assert orc.gelu(np.array(p["u"])) == pytest.approx(p["u"] * p["phi"], abs=1e-15)
@@ -77,7 +91,7 @@ def test_gelu_matches_textbook_phi():
     np.testing.assert_allclose(orc.gelu(big), [30.0, 0.0], atol=1e-12)
 
 
-def test_score_mlp_selection_weights():
+def test_score_mlp_selection_weights(orc):
     # W1 row j reads x[:, k_j] scaled by c_j; W2 row h picks hidden unit j_h.
     # Then s[:, h] = GELU(c_{j_h} x[:, k_{j_h}] + b1) + b2 exactly, checked with Phi.
     rng = np.random.default_rng(2)
@@ -100,7 +114,7 @@ def test_score_mlp_selection_weights():
         np.testing.assert_allclose(s[:, h], u * norm.cdf(u) + b2[h], rtol=0, atol=1e-13)
 
 
-def test_score_mlp_sums_hidden_units():
+def test_score_mlp_sums_hidden_units(orc):
     # all hidden units equal: s = hidden * GELU(u) (catches a dropped hidden term)
     D, hid = 16, 40
     x = _bits(np.full((2, D), 0.25))
@@ -113,7 +127,7 @@ def test_score_mlp_sums_hidden_units():
 
 # --------------------------------------------------------------------------- mask
 
-def test_kvzap_rule_worked_example():
+def test_kvzap_rule_worked_example(orc):
     g = _gold("mask_rules.json")["kvzap"]
     s = np.array([np.nan if v == "nan" else v for v in g["scores"]], dtype=np.float32)
     T = len(s)
@@ -129,7 +143,7 @@ def test_kvzap_rule_worked_example():
     assert list(np.nonzero(keep[0, 0])[0]) == e["present"] and count[0, 0] == e["count"]
 
 
-def test_dms_rule_worked_timeline():
+def test_dms_rule_worked_timeline(orc):
     g = _gold("mask_rules.json")["dms"]
     f = np.array(g["flag_step"])[None, None, :]
     T = f.shape[2]
@@ -142,7 +156,7 @@ def test_dms_rule_worked_timeline():
 
 
 @pytest.mark.parametrize("delay", [1, 129, 256, 300])
-def test_dms_delay_present_until_f_plus_d_minus_1(delay):
+def test_dms_delay_present_until_f_plus_d_minus_1(orc, delay):
     # flagged at its own step f (= position): present at f+d-1, gone at f+d when the
     # delay outlasts the window; otherwise the window decides (gone at f+window)
     W = 128
@@ -155,7 +169,7 @@ def test_dms_delay_present_until_f_plus_d_minus_1(delay):
     assert orc.expire_dms(np.array([-1]), np.array([3]), delay, W)[0] == orc.NEVER
 
 
-def test_mask_keep_all_and_window_only():
+def test_mask_keep_all_and_window_only(orc):
     rng = np.random.default_rng(3)
     B, T, H = 2, 700, 3
     s = rng.standard_normal((B, T, H)).astype(np.float32)
@@ -171,7 +185,7 @@ def test_mask_keep_all_and_window_only():
     assert count[0, 0] == 50
 
 
-def test_mask_monotone_in_tau_and_popcount():
+def test_mask_monotone_in_tau_and_popcount(orc):
     rng = np.random.default_rng(4)
     B, T, H = 2, 333, 4
     s = rng.standard_normal((B, T, H)).astype(np.float32)
@@ -188,7 +202,7 @@ def test_mask_monotone_in_tau_and_popcount():
         prev = count
 
 
-def test_threshold_quantile_prunes_expected_share():
+def test_threshold_quantile_prunes_expected_share(orc):
     rng = np.random.default_rng(5)
     B, T, H = 1, 512, 2
     s = rng.standard_normal((B, T, H))
@@ -199,7 +213,7 @@ def test_threshold_quantile_prunes_expected_share():
         assert (above == T - math.floor(q * (T - 1))).all()
 
 
-def test_threshold_quantile_rank_by_brute_force():
+def test_threshold_quantile_rank_by_brute_force(orc):
     """The threshold is the rank-k element, k = floor(q (T - 1)), with ties and
     special values: brute force over a tiny column counts the scores strictly
     below it (at most k) and at or below it (more than k); NaN ranks last."""
@@ -223,7 +237,7 @@ def test_threshold_quantile_rank_by_brute_force():
                 assert sum(1 for x in num if x < t) <= k < sum(1 for x in num if x <= t)
 
 
-def test_threshold_quantile_special_cases():
+def test_threshold_quantile_special_cases(orc):
     """q = 0 and q = 1 give the column's minimum and maximum, q = 0.5 at odd T
     the median (library routines), with no NaN present."""
     rng = np.random.default_rng(9)
@@ -233,7 +247,26 @@ def test_threshold_quantile_special_cases():
     np.testing.assert_array_equal(orc.threshold_at_quantile(s, 0.5), np.median(s, axis=1))
 
 
-def test_dms_bernoulli_keep_rate():
+def test_threshold_per_head_quantiles_rank_by_brute_force(orc):
+    """One quantile per kv head (heads with their own keep rates): each head's
+    threshold is that head's rank-floor(q_h (T - 1)) element, counted by brute
+    force over the column; heads kept whole (q = 0) and pruned to their last
+    element (q = 1) included."""
+    rng = np.random.default_rng(10)
+    B, T, H = 2, 37, 5
+    s = rng.integers(-4, 5, size=(B, T, H)).astype(np.float32) * 0.25
+    q = np.array([0.0, 0.3, 0.55, 0.9, 1.0])
+    tau = orc.threshold_at_quantile(s, q)
+    assert tau.shape == (B, H)
+    for b in range(B):
+        for h in range(H):
+            k = math.floor(q[h] * (T - 1))
+            col = sorted(float(x) for x in s[b, :, h])
+            t = float(tau[b, h])
+            assert sum(1 for x in col if x < t) <= k < sum(1 for x in col if x <= t)
+
+
+def test_dms_bernoulli_keep_rate(orc):
     # 8x compression: evict bit ~ Bernoulli(7/8) -> outside the delay band ~1/8 kept
     B, H, T = 4, 8, 4096
     ev = syn.bernoulli(0, syn.S_FLAG, (B, H, T), 7 / 8)
@@ -255,7 +288,7 @@ def _toy(B=2, T=300, H=3, d=16, seed=0):
     return k, v
 
 
-def test_compact_rows_remap_pages():
+def test_compact_rows_remap_pages(orc):
     B, T, H, d = 2, 300, 3, 16
     k, v = _toy(B, T, H, d)
     rng = np.random.default_rng(6)
@@ -290,7 +323,7 @@ def test_compact_rows_remap_pages():
     assert c.pages_used == base
 
 
-def test_compact_keep_all_is_identity():
+def test_compact_keep_all_is_identity(orc):
     B, T, H, d = 1, 64, 2, 8
     k, v = _toy(B, T, H, d)
     exp = np.full((B, H, T), orc.NEVER)
@@ -301,7 +334,7 @@ def test_compact_keep_all_is_identity():
         np.testing.assert_array_equal(rows, k[0, :, h])
 
 
-def test_compact_capacity_error():
+def test_compact_capacity_error(orc):
     k, v = _toy(1, 64, 1, 8)
     exp = np.full((1, 1, 64), orc.NEVER)
     with pytest.raises(orc.CapacityError):
@@ -310,7 +343,7 @@ def test_compact_capacity_error():
         orc.compact_dense(k, v, exp, 63, 1, n_pages_cap=10, max_pages=4)
 
 
-def test_paged_recompaction_equals_dense_on_same_set():
+def test_paged_recompaction_equals_dense_on_same_set(orc):
     # prefill compaction at step 60, then appends of positions 61..120, then a
     # paged re-compaction at 120 == one dense compaction of positions 0..120 at 120
     B, T, H, d = 2, 121, 2, 16
@@ -327,7 +360,7 @@ def test_paged_recompaction_equals_dense_on_same_set():
         np.testing.assert_array_equal(getattr(c2, name), getattr(ref, name), err_msg=name)
 
 
-def test_append_fills_reserved_slots():
+def test_append_fills_reserved_slots(orc):
     B, T, H, d = 1, 40, 2, 8
     k, v = _toy(B, T, H, d)
     exp = np.full((B, H, T), orc.NEVER)
@@ -351,9 +384,9 @@ def test_append_fills_reserved_slots():
 def _sdpa_ref(q_bits, k_bits, v_bits, allowed, scale=None):
     """torch's scaled_dot_product_attention in float64 with a boolean mask over
     the dense cache [B, T, H, d]; an independent library routine."""
-    q = torch.from_numpy(orc.widen_bf16(q_bits))          # [B, Hq, d]
-    K = torch.from_numpy(orc.widen_bf16(k_bits))          # [B, T, H, d]
-    V = torch.from_numpy(orc.widen_bf16(v_bits))
+    q = torch.from_numpy(_widen(q_bits))          # [B, Hq, d]
+    K = torch.from_numpy(_widen(k_bits))          # [B, T, H, d]
+    V = torch.from_numpy(_widen(v_bits))
     B, Hq, d = q.shape
     H = K.shape[2]
     g = Hq // H
@@ -364,7 +397,7 @@ def _sdpa_ref(q_bits, k_bits, v_bits, allowed, scale=None):
     return o[:, :, 0, :].numpy()
 
 
-def test_dense_attention_matches_library_sdpa():
+def test_dense_attention_matches_library_sdpa(orc):
     B, T, H, Hq, d = 2, 90, 2, 6, 32
     k, v = _toy(B, T, H, d)
     q = syn.normal_bf16(0, 7, (B, Hq, d))
@@ -378,7 +411,7 @@ def test_dense_attention_matches_library_sdpa():
     np.testing.assert_allclose(ow, _sdpa_ref(q, k, v, allowed), rtol=1e-6, atol=1e-7)
 
 
-def test_decode_attention_equals_masked_sdpa():
+def test_decode_attention_equals_masked_sdpa(orc):
     # paged pruned attention == library attention over the dense cache with the
     # rule's presence mask (catches any page/slot/remap/GQA indexing slip)
     B, T, H, Hq, d = 2, 333, 2, 8, 64
@@ -393,7 +426,7 @@ def test_decode_attention_equals_masked_sdpa():
     np.testing.assert_allclose(o, _sdpa_ref(q, k, v, keep), rtol=1e-6, atol=1e-7)
 
 
-def test_decode_attention_special_cases():
+def test_decode_attention_special_cases(orc):
     B, T, H, Hq, d = 1, 400, 2, 4, 64
     k, v = _toy(B, T, H, d)
     q = syn.normal_bf16(0, 7, (B, Hq, d))
@@ -414,7 +447,7 @@ def test_decode_attention_special_cases():
     np.testing.assert_allclose(o[0], np.repeat(vm, Hq // H, axis=0), rtol=1e-6, atol=1e-7)
 
 
-def test_decode_attention_dominant_key_and_empty():
+def test_decode_attention_dominant_key_and_empty(orc):
     d = 16
     k = np.zeros((1, 8, 1, d), np.uint16)
     v = syn.normal_bf16(0, 6, (1, 8, 1, d))
@@ -434,14 +467,14 @@ def test_decode_attention_dominant_key_and_empty():
 
 # --------------------------------------------------------------------------- closed forms
 
-def test_kv_cache_size_matches_page():
+def test_kv_cache_size_matches_page(orc):
     g = _gold("kv_cache_size.json")
     nb = orc.kv_cache_bytes(g["n_layers"], g["d_model"], g["n_tokens"], g["elem_bytes"])
     # 335.54e9 bytes: the page prints the integer part of the decimal-GB figure
     assert 0 <= nb / 1e9 - g["printed_total_gb"] < g["printed_precision_gb"]
 
 
-def test_scorer_overhead_matches_page():
+def test_scorer_overhead_matches_page(orc):
     g = _gold("scorer_overhead.json")
     m = g["model"]
     proj = orc.linear_projection_macs(m["d_model"], m["n_q_heads"], m["n_kv_heads"], m["head_dim"], m["ffn_hidden"])
@@ -453,7 +486,7 @@ def test_scorer_overhead_matches_page():
 
 # --------------------------------------------------------------------------- fp8 tier
 
-def test_e4m3_table_matches_closed_form_and_torch():
+def test_e4m3_table_matches_closed_form_and_torch(orc):
     """All 256 codes: the closed form (1 + m/8) 2^(e-7), subnormals (m/8) 2^-6,
     NaN at 0x7F / 0xFF, against torch's float8_e4m3fn decoding (a library
     routine) and a few textbook values."""
@@ -466,7 +499,7 @@ def test_e4m3_table_matches_closed_form_and_torch():
     assert orc.e4m3_decode([0xB8])[0] == -1.0
 
 
-def test_e4m3_encode_matches_torch_cast():
+def test_e4m3_encode_matches_torch_cast(orc):
     """Round to nearest, ties to even, against torch's float8 cast on values
     up to 464 (above it torch gives NaN, the encoder saturates to 448)."""
     rng = np.random.default_rng(3)
@@ -480,7 +513,7 @@ def test_e4m3_encode_matches_torch_cast():
     np.testing.assert_array_equal(orc.e4m3_encode([500.0, -1e6, np.nan]), [0x7E, 0xFE, 0x7F])
 
 
-def test_quantize_rows_bounds_and_exact_cases():
+def test_quantize_rows_bounds_and_exact_cases(orc):
     """Per-row scale = amax / 448: the largest element encodes to +-448 exactly;
     every element of the normal range is within half an E4M3 step (2^-4
     relative), the subnormal range within 2^-10 scale; zero rows stay zero;
@@ -509,7 +542,7 @@ def test_quantize_rows_bounds_and_exact_cases():
     np.testing.assert_array_equal(orc.dequantize_rows(c2, s2), ex)
 
 
-def test_quant_tier_partitions_the_entries():
+def test_quant_tier_partitions_the_entries(orc):
     """With tau_q <= tau every entry is in exactly one class: kept bf16
     (s >= tau), fp8 tier (tau_q <= s < tau), dropped (s < tau_q or NaN)."""
     rng = np.random.default_rng(6)
@@ -527,7 +560,7 @@ def test_quant_tier_partitions_the_entries():
     assert not orc.quant_tier_select(s, tau, tau).any()     # tau_q = tau: no fp8 tier
 
 
-def test_two_tier_attention_reduces_to_known_cases():
+def test_two_tier_attention_reduces_to_known_cases(orc):
     """(1) An empty fp8 tier gives the one-tier attention. (2) tau = +inf and
     tau_q = -inf put every entry in the window (bf16) or, once out of it, in
     the fp8 tier; with rows exactly representable in E4M3 (one element at
@@ -571,7 +604,7 @@ def test_two_tier_attention_reduces_to_known_cases():
                                orc.window_attention(q, k, v, early), rtol=0, atol=1e-6)
 
 
-def test_quant_append_equals_one_compaction():
+def test_quant_append_equals_one_compaction(orc):
     """Compacting positions [0, T0) into the fp8 tier and appending T0..T-1
     one at a time gives the same tier (codes, scales, starts, remap, count)
     as one compaction of [0, T) with the same reserve budget."""
@@ -607,7 +640,7 @@ def test_quant_append_equals_one_compaction():
     assert (tight.count >= full).all()
 
 
-def test_dms_fp8_tier_takes_over_where_eviction_was():
+def test_dms_fp8_tier_takes_over_where_eviction_was(orc):
     """DMS flags: the fp8 tier holds exactly the flagged entries, each from the
     step its bf16 copy is gone; at every step an entry is in exactly one tier,
     and on rows exactly representable in E4M3 the two-tier attention equals
@@ -641,7 +674,7 @@ def test_dms_fp8_tier_takes_over_where_eviction_was():
 
 # --------------------------------------------------------------------------- latent cache (MLA)
 
-def test_mla_absorbed_attention_equals_decompressed_heads():
+def test_mla_absorbed_attention_equals_decompressed_heads(orc):
     """The absorbed form is MLA's decompressed attention. Per head j the keys
     [c_t W_UK_j^T, k_rope_t] and values c_t W_UV_j^T with the query
     [q_nope_j, q_rope_j], by torch's scaled_dot_product_attention in float64
@@ -680,7 +713,7 @@ def test_mla_absorbed_attention_equals_decompressed_heads():
             np.testing.assert_allclose(got[b, j], ref, rtol=2e-6, atol=1e-7)
 
 
-def test_mla_latent_pruning_special_cases():
+def test_mla_latent_pruning_special_cases(orc):
     """Keep-all reduces to dense latent attention (brute force over every
     position); a score of -inf keeps exactly the last-window rows; the page
     layout is section 3's with one kv head."""
@@ -712,7 +745,7 @@ def test_mla_latent_pruning_special_cases():
     np.testing.assert_allclose(orc.decode_attention_mla(q, c, dc, now), brute(T - 40), rtol=0, atol=1e-6)
 
 
-def test_mla_attention_closed_forms():
+def test_mla_attention_closed_forms(orc):
     """Closed forms of the latent attention: q = 0 weighs every present row the
     same (the mean of their compressed parts); a row whose logit is 60 above
     every other one takes all the weight (its compressed part, to e^-60); a
@@ -744,7 +777,7 @@ def test_mla_attention_closed_forms():
     np.testing.assert_allclose(orc.decode_attention_mla(q, cache, dc, now)[0, 0], L[j, :dc], rtol=1e-6, atol=1e-20)
 
 
-def test_mla_attention_empty_batch_element():
+def test_mla_attention_empty_batch_element(orc):
     """A batch element with no present latent row gives a zero row of the
     compressed width (dc values, not the row's dc + dr); the others are
     unaffected."""
