@@ -30,6 +30,8 @@
  *     (any allocator; torch tensors work). The library never allocates,
  *     frees or keeps a device buffer: the caller owns every buffer,
  *     including workspace (size from the matching *_workspace_bytes call).
+ *     The one exception is kvp_compact_noalloc, whose scratch is a fixed
+ *     array in the library's device memory (see its declaration).
  *   - Every call is asynchronous and ordered on `stream` (a cudaStream_t,
  *     NULL = legacy default stream). Nothing synchronises the host.
  *   - Host-side argument checks return a status at once and launch nothing.
@@ -402,6 +404,25 @@ KVP_API kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_dim,
                       const int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
                       int32_t* status, void* stream);
 
+/* kvp_append_devpos - kvp_append with the position read from device memory:
+ * pos_dev is a device int32 (4-byte aligned) holding the position of the
+ * token being appended when the call runs on the stream. Everything else is
+ * kvp_append's. A decode step built from this call and
+ * kvp_decode_attn_devpos takes no per-step host value, so it can be captured
+ * once in a CUDA graph and replayed for every step, the caller advancing the
+ * position in device memory between replays (the fixed-address replay of the
+ * DeInfer summary, "나. 페이지드 KV 캐시 및 CUDA Graph 통합"). A position below 0
+ * or with pos + window + delay >= KVP_EXPIRE_NEVER records KVP_ERR_INVALID in
+ * `status` and nothing is written.
+ */
+KVP_API kvp_status kvp_append_devpos(int mode, int batch, int n_kv_heads, int head_dim, const int32_t* pos_dev,
+                                     const void* k_new, const void* v_new,
+                                     const float* score, const float* tau, const int32_t* flag_step,
+                                     int window, int delay,
+                                     void* k_pool, void* v_pool, int32_t* expire_pool, int n_pages_cap,
+                                     const int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
+                                     int32_t* status, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* kvp_decode_attn - single-query attention over the kept entries (DMS
  * article, "DMS 작동 방식" step 5: standard attention kernels on the pruned
@@ -446,6 +467,19 @@ KVP_API kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, int
                                    const int32_t* count, int now, float scale, float* out,
                                    int grid_limit, void* workspace, size_t workspace_bytes,
                                    int32_t* status, void* stream);
+
+/* kvp_decode_attn_devpos - kvp_decode_attn with the decode position read
+ * from device memory: now_dev is a device int32 (4-byte aligned) read when
+ * the call runs on the stream (see kvp_append_devpos). Everything else,
+ * including the workspace, is kvp_decode_attn's.
+ */
+KVP_API kvp_status kvp_decode_attn_devpos(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                          const void* q, const void* k_pool, const void* v_pool,
+                                          const int32_t* expire_pool, int n_pages_cap,
+                                          const int32_t* page_table, int max_pages,
+                                          const int32_t* count, const int32_t* now_dev, float scale, float* out,
+                                          int grid_limit, void* workspace, size_t workspace_bytes,
+                                          int32_t* status, void* stream);
 
 /* kvp_decode_attn_two_tier - kvp_decode_attn over both tiers of "quantize
  * instead of drop" (BeaconKV article; the fp8 tier as kvp_compact_quant

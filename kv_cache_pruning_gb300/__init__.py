@@ -88,10 +88,14 @@ _SIGS = {
                                _P, _P, _P, _S, _P, _P]),
     "kvp_append": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
                         _P, _P]),
+    "kvp_append_devpos": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
+                               _P, _P]),
     "kvp_append_quant": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P,
                               _P, _P]),
     "kvp_decode_attn_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "kvp_decode_attn": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _I, _P, _S, _P, _P]),
+    "kvp_decode_attn_devpos": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _F, _P, _I, _P, _S, _P,
+                                    _P]),
     "kvp_decode_attn_two_tier": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _P, _I, _P,
                                       _I, _F, _P, _I, _P, _S, _P, _P]),
     "kvp_compact_latent": (_I, [_I, _I, _I, _I, _P, _L, _L, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _I, _P, _P,
@@ -492,6 +496,24 @@ def kvp_append(cache: PagedKV, k_new, v_new, pos, *, mode, score=None, tau=None,
     _check("kvp_append", code)
 
 
+def kvp_append_devpos(cache: PagedKV, k_new, v_new, pos_dev, *, mode, score=None, tau=None, flag_step=None,
+                      window=WINDOW, delay=0, status, stream=None):
+    """kvp_append with the position taken from pos_dev (a device int32 tensor of one element) when the call
+    runs on the stream, so that one captured CUDA graph serves every decode step."""
+    B, H, d = k_new.shape
+    code = _lib.kvp_append_devpos(mode, B, H, d, _ptr(pos_dev, torch.int32, "pos_dev"),
+                                  _ptr(k_new, torch.bfloat16, "k_new"),
+                                  _ptr(v_new, torch.bfloat16, "v_new"), _ptr(score, torch.float32, "score", True),
+                                  _ptr(tau, torch.float32, "tau", True),
+                                  _ptr(flag_step, torch.int32, "flag_step", True),
+                                  window, delay, _ptr(cache.k_pool), _ptr(cache.v_pool),
+                                  _ptr(cache.expire_pool, torch.int32), cache.n_pages_cap,
+                                  _ptr(cache.page_table, torch.int32), cache.max_pages,
+                                  _ptr(cache.remap, torch.int32), _ptr(cache.count, torch.int32),
+                                  _ptr(status, torch.int32, "status"), _stream(stream))
+    _check("kvp_append_devpos", code)
+
+
 def kvp_append_quant(qcache: QuantPagedKV, k_new, v_new, pos, *, score=None, tau=None, tau_q=None,
                      mode=KVP_MASK_KVZAP, flag_step=None, delay=0, window=WINDOW, status, stream=None):
     """Writes the token at position `pos` (k_new, v_new [B, H, d]) into the fp8 tier of every (b, h) whose
@@ -536,6 +558,30 @@ def kvp_decode_attn(q, cache: PagedKV, now, *, scale=0.0, out=None, grid_limit=0
                                 grid_limit, ws.data_ptr(), ws.numel() * ws.element_size(),
                                 _ptr(status, torch.int32, "status", True), _stream(stream))
     _check("kvp_decode_attn", code)
+    return out
+
+
+def kvp_decode_attn_devpos(q, cache: PagedKV, now_dev, *, scale=0.0, out=None, grid_limit=0, workspace=None,
+                           status=None, stream=None):
+    """kvp_decode_attn with the decode position taken from now_dev (a device int32 tensor of one element)
+    when the call runs on the stream. Workspace rules: kvp_decode_attn's."""
+    B, Hq, d = q.shape
+    H = cache.count.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    need = kvp_decode_attn_workspace_bytes(B, Hq, H, d)
+    if workspace is None:
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)  # zero-filled before first use
+    else:
+        ws = _ws(need, q.device, workspace)
+    code = _lib.kvp_decode_attn_devpos(B, Hq, H, d, _ptr(q, torch.bfloat16, "q"), _ptr(cache.k_pool),
+                                       _ptr(cache.v_pool), _ptr(cache.expire_pool, torch.int32), cache.n_pages_cap,
+                                       _ptr(cache.page_table, torch.int32), cache.max_pages,
+                                       _ptr(cache.count, torch.int32), _ptr(now_dev, torch.int32, "now_dev"),
+                                       float(scale), _ptr(out, torch.float32, "out"),
+                                       grid_limit, ws.data_ptr(), ws.numel() * ws.element_size(),
+                                       _ptr(status, torch.int32, "status", True), _stream(stream))
+    _check("kvp_decode_attn_devpos", code)
     return out
 
 

@@ -84,6 +84,7 @@ struct AttnParams {
   const int32_t* page_table_q;
   const int32_t* count_q;
   int max_pages_q, n_pages_cap_q;
+  const int32_t* now_dev;  // device int32 holding the decode position, or null: `now` is used
 };
 
 // Eight E4M3 codes (bytes of x then y, element 0 in the lowest byte) to fp32,
@@ -378,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_launch_dependents();
   pdl_wait();  // inputs (counts, pages, workspace counters) come from the kernels before this one
+  const int now = p.now_dev != nullptr ? *p.now_dev : p.now;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BH = p.B * p.H;
   uint8_t* ring = smem + warp * kNst * C::STAGE_BYTES;
@@ -711,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
 #pragma unroll
     for (int u = 0; u < C::VL; ++u) {
       const int r = ((idx_base + u) % C::RS) * C::RPS + rowsel;
-      const bool valid = isq ? (slot0 + r < cnt_q) && (p.now >= er[u]) : (slot0 + r < cnt) && (p.now < er[u]);
+      const bool valid = isq ? (slot0 + r < cnt_q) && (now >= er[u]) : (slot0 + r < cnt) && (now < er[u]);
       x[u] = valid ? (isq ? part[u] * ksu[u] : part[u]) : -INFINITY;
       grow |= x[u] > mh + kLazyRescale;
     }
@@ -914,6 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   pdl_launch_dependents();
   pdl_wait();  // inputs (counts, pages, workspace counters) come from the kernels before this one
+  const int now = p.now_dev != nullptr ? *p.now_dev : p.now;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BH = p.B * p.H;
   uint8_t* ring = smem + warp * kNst * C::STAGE_BYTES;
@@ -1256,13 +1259,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     bool v0, v1;
     float sc0 = p.qscale, sc1 = p.qscale;
     if (isq) {  // fp8 slots count once now >= start; the K row scales apply to S
-      v0 = (slot0 + gq < cnt_q) && (p.now >= e0);
-      v1 = (slot0 + gq + 8 < cnt_q) && (p.now >= e1);
+      v0 = (slot0 + gq < cnt_q) && (now >= e0);
+      v1 = (slot0 + gq + 8 < cnt_q) && (now >= e1);
       sc0 *= ks0;
       sc1 *= ks1;
     } else {
-      v0 = (slot0 + gq < cnt) && (p.now < e0);
-      v1 = (slot0 + gq + 8 < cnt) && (p.now < e1);
+      v0 = (slot0 + gq < cnt) && (now < e0);
+      v1 = (slot0 + gq + 8 < cnt) && (now < e1);
     }
     float x[4];
     x[0] = v0 ? sacc[0] * sc0 : -INFINITY;
@@ -1554,11 +1557,12 @@ struct QuantTier {
 kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q, const void* k_pool,
                             const void* v_pool, const int32_t* expire_pool, int n_pages_cap,
                             const int32_t* page_table, int max_pages, const int32_t* count, const QuantTier* qt,
-                            int now, float scale, float* out, int grid_limit, void* workspace,
+                            int now, const int32_t* now_dev, float scale, float* out, int grid_limit, void* workspace,
                             size_t workspace_bytes, int32_t* status, void* stream) {
   if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_pages < 0 || grid_limit < 0 || n_pages_cap < 0)
     return KVP_ERR_INVALID;
   if (n_q_heads % n_kv_heads != 0) return KVP_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(now_dev) & 3u) != 0) return KVP_ERR_ALIGN;
   if (static_cast<int64_t>(max_pages) * kPage > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
   const int G = n_q_heads / n_kv_heads;
   if (head_dim != 64 && head_dim != 128) return KVP_ERR_UNSUPPORTED;
@@ -1614,7 +1618,8 @@ kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_d
                qt ? qt->page_table : nullptr,
                qt ? qt->count : nullptr,
                qt ? qt->max_pages : 0,
-               qt ? qt->n_pages_cap : 0};
+               qt ? qt->n_pages_cap : 0,
+               now_dev};
   // Eight query heads per kv head go to the tensor-core kernel: with the
   // CUDA-core page math a page takes twice the multiply-adds of G = 4 and the
   // kernel is bound by instruction issue (measured on a GB300, Llama-3-8B
@@ -1640,7 +1645,19 @@ extern "C" kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, 
                                       const int32_t* count, int now, float scale, float* out, int grid_limit,
                                       void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
   return decode_attn_impl(batch, n_q_heads, n_kv_heads, head_dim, q, k_pool, v_pool, expire_pool, n_pages_cap,
-                          page_table, max_pages, count, nullptr, now, scale, out, grid_limit, workspace,
+                          page_table, max_pages, count, nullptr, now, nullptr, scale, out, grid_limit, workspace,
+                          workspace_bytes, status, stream);
+}
+
+extern "C" kvp_status kvp_decode_attn_devpos(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q,
+                                             const void* k_pool, const void* v_pool, const int32_t* expire_pool,
+                                             int n_pages_cap, const int32_t* page_table, int max_pages,
+                                             const int32_t* count, const int32_t* now_dev, float scale, float* out,
+                                             int grid_limit, void* workspace, size_t workspace_bytes,
+                                             int32_t* status, void* stream) {
+  if (now_dev == nullptr) return KVP_ERR_INVALID;
+  return decode_attn_impl(batch, n_q_heads, n_kv_heads, head_dim, q, k_pool, v_pool, expire_pool, n_pages_cap,
+                          page_table, max_pages, count, nullptr, 0, now_dev, scale, out, grid_limit, workspace,
                           workspace_bytes, status, stream);
 }
 
@@ -1654,6 +1671,6 @@ extern "C" kvp_status kvp_decode_attn_two_tier(int batch, int n_q_heads, int n_k
                                                size_t workspace_bytes, int32_t* status, void* stream) {
   const QuantTier qt{kq_pool, vq_pool, meta_pool, n_pages_cap_q, page_table_q, max_pages_q, count_q};
   return decode_attn_impl(batch, n_q_heads, n_kv_heads, head_dim, q, k_pool, v_pool, expire_pool, n_pages_cap,
-                          page_table, max_pages, count, &qt, now, scale, out, grid_limit, workspace,
+                          page_table, max_pages, count, &qt, now, nullptr, scale, out, grid_limit, workspace,
                           workspace_bytes, status, stream);
 }

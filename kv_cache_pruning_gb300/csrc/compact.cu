@@ -304,7 +304,10 @@ struct CompactWs {
   int32_t* base;
   int32_t* ok;
 };
-size_t compact_ws_bytes(int BH, int NS) { return (static_cast<size_t>(2) * BH * NS + BH + 1) * sizeof(int32_t); }
+size_t compact_ws_bytes(int64_t BH, int NS) { return (static_cast<size_t>(2) * BH * NS + BH + 1) * sizeof(int32_t); }
+// (b, h) pairs a compaction takes: the count pass puts them on the grid's y
+// dimension.
+constexpr int64_t kMaxCompactBH = 65535;
 CompactWs carve(void* ws, int BH, int NS) {
   int32_t* p = static_cast<int32_t*>(ws);
   const size_t n = static_cast<size_t>(BH) * NS;
@@ -679,7 +682,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
 
 // ------------------------------------------------------------------ append
 template <int D>
-__global__ void __launch_bounds__(256) append_kernel(int mode, int BH, int pos, const uint16_t* __restrict__ k_new,
+__global__ void __launch_bounds__(256) append_kernel(int mode, int BH, int pos_arg, const int32_t* __restrict__ pos_dev,
+                                                     const uint16_t* __restrict__ k_new,
                                                      const uint16_t* __restrict__ v_new,
                                                      const float* __restrict__ score, const float* __restrict__ tau,
                                                      const int32_t* __restrict__ flag, int window, int delay,
@@ -692,6 +696,13 @@ __global__ void __launch_bounds__(256) append_kernel(int mode, int BH, int pos, 
   const int bh = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (bh >= BH) return;
+  // the position from device memory (one captured step replayed for every
+  // position) or the argument
+  const int pos = pos_dev != nullptr ? *pos_dev : pos_arg;
+  if (pos < 0 || static_cast<int64_t>(pos) + window + delay >= kNever) {
+    if (lane == 0) record_error(status, KVP_ERR_INVALID);
+    return;
+  }
   const int j = count[bh];
   if (j < 0) {
     if (lane == 0) record_error(status, KVP_ERR_BOUNDS);
@@ -933,11 +944,12 @@ extern "C" kvp_status kvp_mask(int mode, int batch, int n_kv_heads, int n_pos, i
 
 extern "C" size_t kvp_compact_workspace_bytes(int batch, int n_kv_heads, int n_pos) {
   if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0) return 0;
-  return compact_ws_bytes(batch * n_kv_heads, n_segments(n_pos));
+  return compact_ws_bytes(static_cast<int64_t>(batch) * n_kv_heads, n_segments(n_pos));
 }
 
 extern "C" size_t kvp_compact_paged_workspace_bytes(int batch, int n_kv_heads, int src_max_pages) {
   if (batch <= 0 || n_kv_heads <= 0 || src_max_pages < 0) return 0;
+  if (static_cast<int64_t>(src_max_pages) * kPage > 0x7fffffff) return 0;
   return kvp_compact_workspace_bytes(batch, n_kv_heads, src_max_pages * kPage);
 }
 
@@ -961,6 +973,7 @@ extern "C" kvp_status kvp_compact(int batch, int n_kv_heads, int head_dim, int n
                                   int32_t* remap, int32_t* count, void* workspace, size_t workspace_bytes,
                                   int32_t* status, void* stream) {
   if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(batch) * n_kv_heads > kMaxCompactBH) return KVP_ERR_UNSUPPORTED;
   kvp_status s = check_dst(head_dim, reserve, k_pool, v_pool, expire_pool, n_pages_cap, page_table, max_pages,
                            remap, count, status);
   if (s != KVP_OK) return s;
@@ -984,6 +997,7 @@ extern "C" kvp_status kvp_compact_masked(int mode, int batch, int n_kv_heads, in
                                          int32_t* page_table, int max_pages, int32_t* remap, int32_t* count,
                                          void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
   if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0 || window < 0 || delay < 0) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(batch) * n_kv_heads > kMaxCompactBH) return KVP_ERR_UNSUPPORTED;
   // the per-position inputs may be NULL when there are no positions; tau is read per (b, h)
   if (mode == KVP_MASK_KVZAP) {
     if (flag_step != nullptr || tau == nullptr || (n_pos > 0 && scores == nullptr)) return KVP_ERR_INVALID;
@@ -1027,6 +1041,7 @@ extern "C" kvp_status kvp_compact_quant(int mode, int batch, int n_kv_heads, int
                                         int max_pages, int32_t* remap, int32_t* count, void* workspace,
                                         size_t workspace_bytes, int32_t* status, void* stream) {
   if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0 || window < 0 || delay < 0) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(batch) * n_kv_heads > kMaxCompactBH) return KVP_ERR_UNSUPPORTED;
   if (mode == KVP_MASK_KVZAP) {
     if (flag_step != nullptr || tau == nullptr || tau_q == nullptr || (n_pos > 0 && scores == nullptr))
       return KVP_ERR_INVALID;
@@ -1072,6 +1087,7 @@ extern "C" kvp_status kvp_compact_paged(int batch, int n_kv_heads, int head_dim,
                                         int32_t* remap, int32_t* count, void* workspace, size_t workspace_bytes,
                                         int32_t* status, void* stream) {
   if (batch <= 0 || n_kv_heads <= 0 || src_max_pages < 0 || src_n_pages_cap < 0) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(batch) * n_kv_heads > kMaxCompactBH) return KVP_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(src_max_pages) * kPage > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
   kvp_status s = check_dst(head_dim, reserve, k_pool, v_pool, expire_pool, n_pages_cap, page_table, max_pages,
                            remap, count, status);
@@ -1101,13 +1117,15 @@ extern "C" kvp_status kvp_compact_paged(int batch, int n_kv_heads, int head_dim,
                      page_table, max_pages, remap, count, workspace, status, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_dim, int pos, const void* k_new,
-                                 const void* v_new, const float* score, const float* tau, const int32_t* flag_step,
-                                 int window, int delay, void* k_pool, void* v_pool, int32_t* expire_pool,
-                                 int n_pages_cap, const int32_t* page_table, int max_pages, int32_t* remap,
-                                 int32_t* count, int32_t* status, void* stream) {
+namespace {
+kvp_status append_impl(int mode, int batch, int n_kv_heads, int head_dim, int pos, const int32_t* pos_dev,
+                       const void* k_new, const void* v_new, const float* score, const float* tau,
+                       const int32_t* flag_step, int window, int delay, void* k_pool, void* v_pool,
+                       int32_t* expire_pool, int n_pages_cap, const int32_t* page_table, int max_pages,
+                       int32_t* remap, int32_t* count, int32_t* status, void* stream) {
   if (batch <= 0 || n_kv_heads <= 0 || pos < 0 || window < 0 || delay < 0 || max_pages < 0 || n_pages_cap < 0)
     return KVP_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(pos_dev) & 3u) != 0) return KVP_ERR_ALIGN;
   if (head_dim != 64 && head_dim != 128) return KVP_ERR_UNSUPPORTED;
   if (mode == KVP_MASK_KVZAP) {
     if (score == nullptr || tau == nullptr || flag_step != nullptr) return KVP_ERR_INVALID;
@@ -1121,6 +1139,7 @@ extern "C" kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_d
     return KVP_ERR_INVALID;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool)) return KVP_ERR_ALIGN;
   if (static_cast<int64_t>(pos) + window + delay >= kNever) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(batch) * n_kv_heads > 0x7ffffff0) return KVP_ERR_UNSUPPORTED;
   const int BH = batch * n_kv_heads;
   const int blocks = (BH + 7) / 8;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1129,14 +1148,37 @@ extern "C" kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_d
   auto* kn = static_cast<const uint16_t*>(k_new);
   auto* vn = static_cast<const uint16_t*>(v_new);
   if (head_dim == 128)
-    append_kernel<128><<<blocks, 256, 0, st>>>(mode, BH, pos, kn, vn, score, tau, flag_step, window, delay, kp, vp,
-                                               expire_pool, n_pages_cap, page_table, max_pages, remap, count,
+    append_kernel<128><<<blocks, 256, 0, st>>>(mode, BH, pos, pos_dev, kn, vn, score, tau, flag_step, window, delay,
+                                               kp, vp, expire_pool, n_pages_cap, page_table, max_pages, remap, count,
                                                status);
   else
-    append_kernel<64><<<blocks, 256, 0, st>>>(mode, BH, pos, kn, vn, score, tau, flag_step, window, delay, kp, vp,
-                                              expire_pool, n_pages_cap, page_table, max_pages, remap, count,
+    append_kernel<64><<<blocks, 256, 0, st>>>(mode, BH, pos, pos_dev, kn, vn, score, tau, flag_step, window, delay,
+                                              kp, vp, expire_pool, n_pages_cap, page_table, max_pages, remap, count,
                                               status);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" kvp_status kvp_append(int mode, int batch, int n_kv_heads, int head_dim, int pos, const void* k_new,
+                                 const void* v_new, const float* score, const float* tau, const int32_t* flag_step,
+                                 int window, int delay, void* k_pool, void* v_pool, int32_t* expire_pool,
+                                 int n_pages_cap, const int32_t* page_table, int max_pages, int32_t* remap,
+                                 int32_t* count, int32_t* status, void* stream) {
+  return append_impl(mode, batch, n_kv_heads, head_dim, pos, nullptr, k_new, v_new, score, tau, flag_step, window,
+                     delay, k_pool, v_pool, expire_pool, n_pages_cap, page_table, max_pages, remap, count, status,
+                     stream);
+}
+
+extern "C" kvp_status kvp_append_devpos(int mode, int batch, int n_kv_heads, int head_dim, const int32_t* pos_dev,
+                                        const void* k_new, const void* v_new, const float* score, const float* tau,
+                                        const int32_t* flag_step, int window, int delay, void* k_pool, void* v_pool,
+                                        int32_t* expire_pool, int n_pages_cap, const int32_t* page_table,
+                                        int max_pages, int32_t* remap, int32_t* count, int32_t* status,
+                                        void* stream) {
+  if (pos_dev == nullptr) return KVP_ERR_INVALID;
+  return append_impl(mode, batch, n_kv_heads, head_dim, 0, pos_dev, k_new, v_new, score, tau, flag_step, window,
+                     delay, k_pool, v_pool, expire_pool, n_pages_cap, page_table, max_pages, remap, count, status,
+                     stream);
 }
 
 extern "C" kvp_status kvp_append_quant(int mode, int batch, int n_kv_heads, int head_dim, int pos, const void* k_new,
@@ -1160,6 +1202,7 @@ extern "C" kvp_status kvp_append_quant(int mode, int batch, int n_kv_heads, int 
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kq_pool) || !aligned16(vq_pool) || !aligned16(meta_pool))
     return KVP_ERR_ALIGN;
   if (static_cast<int64_t>(pos) + window + delay >= kNever) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(batch) * n_kv_heads > 0x7ffffff0) return KVP_ERR_UNSUPPORTED;
   const int BH = batch * n_kv_heads;
   const int blocks = (BH + 7) / 8;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1202,6 +1245,7 @@ extern "C" kvp_status kvp_compact_latent(int mode, int batch, int row_dim, int n
                                          int max_pages, int32_t* remap, int32_t* count, void* workspace,
                                          size_t workspace_bytes, int32_t* status, void* stream) {
   if (batch <= 0 || n_pos < 0 || window < 0 || delay < 0) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(batch) > kMaxCompactBH) return KVP_ERR_UNSUPPORTED;
   if (mode == KVP_MASK_KVZAP) {
     if (flag_step != nullptr || tau == nullptr || (n_pos > 0 && scores == nullptr)) return KVP_ERR_INVALID;
   } else if (mode == KVP_MASK_DMS) {
@@ -1234,6 +1278,7 @@ extern "C" kvp_status kvp_compact_latent_paged(int batch, int row_dim, const voi
                                                void* workspace, size_t workspace_bytes, int32_t* status,
                                                void* stream) {
   if (batch <= 0 || src_max_pages < 0 || src_n_pages_cap < 0) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(batch) > kMaxCompactBH) return KVP_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(src_max_pages) * kPage > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
   kvp_status s = check_dst_latent(row_dim, reserve, pool, expire_pool, n_pages_cap, page_table, max_pages, remap,
                                   count, status);
@@ -1299,6 +1344,7 @@ extern "C" kvp_status kvp_compact_noalloc(int batch, int n_kv_heads, int head_di
                                           int32_t* expire_pool, int n_pages_cap, int32_t* page_table, int max_pages,
                                           int32_t* remap, int32_t* count, int32_t* status, void* stream) {
   if (batch <= 0 || n_kv_heads <= 0 || n_pos < 0) return KVP_ERR_INVALID;
+  if (static_cast<int64_t>(batch) * n_kv_heads > kMaxCompactBH) return KVP_ERR_UNSUPPORTED;
   const size_t need = kvp_compact_workspace_bytes(batch, n_kv_heads, n_pos);
   if (need > KVP_COMPACT_NOALLOC_SCRATCH_BYTES) return KVP_ERR_WORKSPACE;
   int dev = -1;

@@ -17,6 +17,14 @@ Generator (counter based, so any element can be drawn without the others):
 
 Every tensor of a workload gets its own ``stream`` id, so the same seed gives
 the same bits regardless of which other tensors are drawn.
+
+Tensors of a billion elements (the full-size workloads) take minutes with the
+generator above in numpy, so ``fast_normal_bf16`` draws them with numpy's
+Philox4x64-10 bit generator (Salmon, Moraes, Dror & Shaw, "Parallel random
+numbers: as easy as 1, 2, 3", SC 2011), also counter based, keyed by
+``(seed, stream)`` and advanced to each chunk's start; its normals are
+numpy's float32 ziggurat. The two generators give different numbers: a
+workload uses one of them for all its draws.
 """
 from __future__ import annotations
 
@@ -104,6 +112,47 @@ def _normal_slice(seed: int, stream: int, start: int, n: int) -> np.ndarray:
     z[0::2] = r * np.cos(th)
     z[1::2] = r * np.sin(th)
     return z[:n]
+
+
+_FAST_CHUNK = 1 << 24
+
+
+def _philox(seed: int, stream: int, start: int) -> np.random.Generator:
+    key = np.array([seed & 0xFFFFFFFFFFFFFFFF, stream & 0xFFFFFFFFFFFFFFFF], dtype=np.uint64)
+    return np.random.Generator(np.random.Philox(key=key).advance(start * 4))
+
+
+def fast_normal_bf16(seed: int, stream: int, shape, std: float = 1.0) -> np.ndarray:
+    """N(0, std^2) rounded to bf16 (uint16 bits of the given shape). Chunk c
+    of 2^24 values comes from a Philox4x64-10 generator keyed by (seed,
+    stream) and advanced by c * 2^24 blocks (a normal uses at most a few
+    draws, so chunks never overlap in practice); chunks are drawn on all host
+    cores, so the result does not depend on the thread count. The float32 ->
+    bf16 rounding (nearest even) is torch's conversion, multithreaded; it
+    gives the same bits as f32_to_bf16_bits on finite values."""
+    import concurrent.futures as cf
+    import os
+
+    import torch
+
+    n = int(np.prod(shape))
+    z = np.empty(n, dtype=np.float32)
+
+    def chunk(c0):
+        c1 = min(n, c0 + _FAST_CHUNK)
+        _philox(seed, stream, c0).standard_normal(dtype=np.float32, out=z[c0:c1])
+        if std != 1.0:
+            z[c0:c1] *= np.float32(std)
+
+    with cf.ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as ex:
+        list(ex.map(chunk, range(0, n, _FAST_CHUNK)))
+    out = torch.from_numpy(z).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return out.reshape(shape)
+
+
+def fast_uniform(seed: int, stream: int, shape) -> np.ndarray:
+    """float64 uniforms in [0, 1) from the same Philox keying as fast_normal_bf16."""
+    return _philox(seed, stream, 0).random(int(np.prod(shape))).reshape(shape)
 
 
 def normal_f32(seed: int, stream: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:

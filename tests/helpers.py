@@ -3,6 +3,8 @@ bf16 bit patterns and torch tensors, and the tolerance checks."""
 import numpy as np
 import torch
 
+import oracle as orc
+
 
 def dev_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
@@ -46,3 +48,46 @@ def check_attention(o_gpu: np.ndarray, o_ref: np.ndarray, max_abs=2e-2, mean_abs
     rel = np.where(den > 0, num / np.maximum(den, 1e-30), num)
     assert rel.max() <= rel_head, f"per-head relative err {rel.max():.3g}"
     return float(d.max()), float(d.mean()), float(rel.max())
+
+
+def oracle_linear_scores(x, w, chunk=16384):
+    """The oracle's KVzap-Linear scores of every row of x, in row chunks (the
+    widened float64 rows of a whole full-size x would not fit in host memory),
+    and the error scale ||x_t * w_h||_2 of each score."""
+    out = np.empty((x.shape[0], w.shape[0]))
+    scale = np.empty_like(out)
+    w64 = np.asarray(w, np.float64)
+    for a in range(0, x.shape[0], chunk):
+        xs = orc.widen_bf16(x[a:a + chunk])
+        out[a:a + chunk] = orc.score_linear(x[a:a + chunk], w)
+        scale[a:a + chunk] = np.sqrt((xs * xs) @ (w64 ** 2).T)
+    return out, scale
+
+
+def oracle_mlp_scores(x, w1, w2, b1=None, b2=None, chunk=8192):
+    """The oracle's KVzap-MLP scores of every row of x, in row chunks, and the
+    error scale of each: the 2-norm of the hidden terms z_j * w2[h, j]."""
+    H = w2.shape[0]
+    out = np.empty((x.shape[0], H))
+    scale = np.empty_like(out)
+    w1f = orc.widen_bf16(w1)
+    w2f = orc.widen_bf16(w2)
+    for a in range(0, x.shape[0], chunk):
+        out[a:a + chunk] = orc.score_mlp(x[a:a + chunk], w1, w2, b1, b2)
+        u = orc.widen_bf16(x[a:a + chunk]) @ w1f.T + (0 if b1 is None else np.asarray(b1, np.float64)[None, :])
+        z = orc.gelu(u)
+        scale[a:a + chunk] = np.sqrt((z * z) @ (w2f ** 2).T)
+    return out, scale
+
+
+def compare_paged(gpu, ref, used=None, what=""):
+    """Bit-exact comparison of a compacted cache with the oracle's: counts,
+    page table, remap list, and the used pages of the pools and expire_pool."""
+    used = ref.pages_used if used is None else used
+    np.testing.assert_array_equal(gpu.count.cpu().numpy(), ref.count, err_msg=what + " count")
+    np.testing.assert_array_equal(gpu.page_table.cpu().numpy(), ref.page_table, err_msg=what + " page_table")
+    np.testing.assert_array_equal(gpu.remap.cpu().numpy(), ref.remap, err_msg=what + " remap")
+    np.testing.assert_array_equal(gpu.expire_pool.cpu().numpy()[:used], ref.expire_pool[:used],
+                                  err_msg=what + " expire_pool")
+    np.testing.assert_array_equal(host_bits(gpu.k_pool)[:used], ref.k_pool[:used], err_msg=what + " k_pool")
+    np.testing.assert_array_equal(host_bits(gpu.v_pool)[:used], ref.v_pool[:used], err_msg=what + " v_pool")

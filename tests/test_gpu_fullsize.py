@@ -14,20 +14,10 @@ import torch
 
 import kvp_synth as syn
 import oracle as orc
-from helpers import check_attention, check_scores, dev_bf16, dev_f32, dev_i32, host_bits, status_word
+from helpers import (check_attention, check_scores, dev_bf16, dev_f32, dev_i32, host_bits,
+                     oracle_linear_scores, status_word)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
-
-
-def _oracle_scores_chunked(x, w, chunk=16384):
-    out = np.empty((x.shape[0], w.shape[0]))
-    scale = np.empty_like(out)
-    w64 = np.asarray(w, np.float64)
-    for a in range(0, x.shape[0], chunk):
-        xs = orc.widen_bf16(x[a:a + chunk])
-        out[a:a + chunk] = orc.score_linear(x[a:a + chunk], w)
-        scale[a:a + chunk] = np.sqrt((xs * xs) @ (w64 ** 2).T)
-    return out, scale
 
 
 def test_llama3_8b_layer_full_size(kvp):
@@ -45,7 +35,7 @@ def test_llama3_8b_layer_full_size(kvp):
     torch.cuda.synchronize()
     del xd
     assert st.item() == 0
-    s_ref, scale = _oracle_scores_chunked(x, w)
+    s_ref, scale = oracle_linear_scores(x, w)
     check_scores(s_gpu.cpu().numpy(), s_ref, scale)
 
     # ---- mask with the GPU's scores vs the oracle's, near-threshold entries excluded

@@ -29,7 +29,11 @@ def _noalloc(lib):
 
 
 def _case(seed, B, T, H, d):
-    k, v = syn.kv_inputs(seed, B, T, H, d)
+    if B * T * H * d > (1 << 24):   # large: the fast generator
+        k = syn.fast_normal_bf16(seed, syn.S_K, (B, T, H, d))
+        v = syn.fast_normal_bf16(seed, syn.S_V, (B, T, H, d))
+    else:
+        k, v = syn.kv_inputs(seed, B, T, H, d)
     s = syn.normal_f32(seed, 21, (B, T, H))
     tau = syn.normal_f32(seed, 22, (B, H), std=0.7)
     exp = orc.mask_kvzap(s, tau, T - 1)[0].astype(np.int32)
@@ -46,7 +50,10 @@ def _same(a, b):
 def test_compact_noalloc_matches_compact_on_consecutive_calls(kvp):
     fn = _noalloc(kvp.library())
     stream = torch.cuda.current_stream().cuda_stream
-    shapes = [(2, 3000, 4, 128, 5, 1), (3, 1777, 2, 64, 0, 2)]  # the second call reuses the scratch
+    # each call reuses the scratch the one before it left behind; the third has 2,048 (b, h) pairs, above
+    # the 1,024 that the copy pass's CTAs handle alone, so it also goes through the separate page-base
+    # pass, whose results live in the scratch too, in words the two smaller calls never wrote
+    shapes = [(2, 3000, 4, 128, 5, 1), (3, 1777, 2, 64, 0, 2), (1024, 640, 2, 64, 3, 3)]
     for B, T, H, d, reserve, seed in shapes:
         k, v, exp = _case(seed, B, T, H, d)
         mp = (T + reserve + 15) // 16
