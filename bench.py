@@ -1,26 +1,37 @@
 #!/usr/bin/env python
 """Benchmark of the pruned-KV decode path on GB300.
 
-One step = the whole path over one batch: KVzap-Linear scores of every cached
-token (tcgen05), keep/evict mask, compaction of the survivors into 16-token
-pages, split-KV decode attention of the batch's query tokens. Workload: a
-Llama-3-8B-shaped layer (d_model 4096, 32 query / 8 KV heads, head_dim 128,
-batch 16, 8192 cached tokens, threshold at each head's 75th-percentile score,
-last 128 tokens always kept). Metric: decode tokens/s (batch / step time).
+Headline workload: the Llama-65B-shaped long-context MHA stack (8 layers, 64
+heads, head_dim 128, d_model 8192, batch 1, 131,072 cached tokens), KVzap-Linear
+scores with per-(layer, head) keep rates ~ Beta(2, 5), 128-token window. Set-up
+(timed separately, reported under `prefill`): each layer's prompt is scored
+(tcgen05 scorer), each head's threshold is its quantile 1 - r, and the prompt
+is masked and compacted into 16-token pages with 32 reserved slots. One
+benchmark step = one decode step over the 8 layers: the new token's hidden
+state is scored, its K/V appended under the layer's thresholds, and split-KV
+attention runs over the survivors. The step is captured once as a CUDA graph
+(the position lives in device memory) and replayed; every 32 steps the caches
+return to the prompt's state (the workload's 32 decode steps). Metric: decode
+tokens/s (batch / step time).
+
+The Llama-3-8B-shaped layer (batch 16 x 8,192 tokens, score + mask + compact +
+attention per step) is measured too and reported under `llama3_8b_layer`.
 
 Arms:
   default            the CUDA path through the C ABI (device-resident inputs),
-                     plus an end-to-end leg with pinned host inputs copied in
-                     and the output copied back inside the timed region, plus
-                     the oracle timed on a bounded sample (cpu_baseline)
-  --impl reference   the oracle (float64 CPU reference) on host cores, on a
-                     bounded sample per step
-Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no data-path
-collective); rank 0 prints the max-over-ranks time.
+                     an end-to-end leg (host inputs copied in and the output
+                     copied back inside the timed region, eager calls), and the
+                     C++ oracle on a bounded sample on every host core
+                     (cpu_baseline)
+  --impl reference   the C++ oracle on host cores, each step a bounded sample
+                     of the same decode step
+Multi-GPU (torchrun): every rank runs its own replica (weak scaling, no
+data-path collective); rank 0 prints the max-over-ranks time.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -29,11 +40,6 @@ import subprocess
 import sys
 import time
 
-if "--impl" in sys.argv and "reference" in sys.argv or "--cpu-baseline-only" in sys.argv:
-    # the oracle is timed single-threaded: every library below runs on one core
-    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[_v] = "1"
-
 import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -41,136 +47,180 @@ sys.path.insert(0, ROOT)
 
 METRIC = "pruned-KV decode tokens/s at 1 GB300; effective HBM GB/s vs ~8 TB/s peak"
 UNIT = "tokens/s"
-WORKLOAD = dict(name="llama3_8b_layer", d_model=4096, n_q_heads=32, n_kv_heads=8, head_dim=128, batch=16,
-                n_pos=8192, prune_q=0.75, window=128)
+C5 = dict(name="llama65b_mha", n_layers=8, d_model=8192, n_heads=64, head_dim=128, batch=1, n_pos=131072,
+          window=128, reserve=32, steps=32)
+C2 = dict(name="llama3_8b_layer", d_model=4096, n_q_heads=32, n_kv_heads=8, head_dim=128, batch=16, n_pos=8192,
+          prune_q=0.75, window=128)
+
+# DRAM read + write bytes per surviving page of the decode attention kernel at
+# this workload (attn_decode_kernel<128, 1>), from an ncu capture of one launch
+# of layer 0 (147,229 surviving pages): (1,216,809,728 + 2,732,544) B / 147,229,
+# against 8,256 B of K, V and expire values per page. The SHA-256 of attn.cu it
+# was taken on: the figure is reported only while the kernel source is unchanged.
+ATTN_DRAM_BYTES_PER_PAGE = (1216809728 + 2732544) / 147229
+ATTN_SRC_SHA = "240d9c50ab72b8c1e2b22ecf848ba7a89e06d2c5cd0929c5b492c2cc1552e578"
 
 
-# DRAM read + write bytes per row of hidden states of the tcgen05 scorer
-# (KVzap-Linear, d_model 4096, 8 heads), from an ncu capture of that kernel on
-# 32,768 rows: (268.592 + 3.492) MB / 32,768 rows. Valid while the scorer kernel
-# is unchanged.
-SCORE_DRAM_BYTES_PER_ROW = 272.084e6 / 32768
-
-# Kernels of this library launched per step at this workload's size (B*H <= 1024):
-# scorer (on the weight split once at set-up), segment count + copy pass of the
-# compaction with the mask fused in, decode attention; one more (the mask
-# kernel) with --mask separate. The compaction and attention calls also issue
-# one memset each.
-KERNELS_PER_STEP = {"fused": 4, "separate": 5}
-
-
-def scorer_overhead(w=WORKLOAD, ffn_hidden=14336, mlp_hidden=1024):
-    """The KVzap summary's overhead figures ("메모리 및 계산 효율": about 0.02 % of the linear-projection FLOPs
-    for KVzap-Linear, about 1.1 % for KVzap-MLP) as closed forms for this layer's shape: scorer multiply-adds
-    per token over the layer's Q, K, V, O and gated feed-forward projections."""
-    D, Hq, H, d = w["d_model"], w["n_q_heads"], w["n_kv_heads"], w["head_dim"]
-    proj = 2 * D * Hq * d + 2 * D * H * d + 3 * D * ffn_hidden
-    lin = D * H
-    mlp = D * mlp_hidden + mlp_hidden * H
-    return {"projection_macs_per_token": proj, "linear_macs_per_token": lin, "linear_fraction": lin / proj,
-            "mlp_macs_per_token": mlp, "mlp_fraction": mlp / proj, "ffn_hidden": ffn_hidden, "mlp_hidden": mlp_hidden}
-
-
-def config_desc(w=WORKLOAD, mask_mode=None):
+def c5_desc(w=C5):
     return {
-        "workload": (f"{w['name']}: one layer, d_model {w['d_model']}, {w['n_q_heads']} q / {w['n_kv_heads']} kv "
-                     f"heads, head_dim {w['head_dim']}, batch {w['batch']}, context {w['n_pos']}, KVzap-Linear "
-                     f"scorer, threshold at each head's {int(w['prune_q'] * 100)}th-percentile score, last "
-                     f"{w['window']} tokens kept; step = score + mask + compact + decode attention"
-                     f"{ {'fused': ' (mask fused into the compaction)', 'separate': ' (mask as its own kernel)'}.get(mask_mode, '')}"),
+        "workload": (f"{w['name']}: {w['n_layers']} layers x ({w['n_heads']} MHA heads, head_dim {w['head_dim']}, "
+                     f"d_model {w['d_model']}), batch {w['batch']}, {w['n_pos']} cached tokens, KVzap-Linear scores, "
+                     f"keep rate per (layer, head) ~ Beta(2,5), last {w['window']} tokens kept; step = one decode "
+                     f"step over the {w['n_layers']} layers (new token scored, appended, split-KV attention over "
+                     f"the survivors); the caches return to the prompt's every {w['steps']} steps"),
         "global_batch": w["batch"],
         "seq_len": w["n_pos"],
-        "parallelism": "replicas: each rank decodes its own batch",
-        "l2": "inputs larger than L2 (hidden states 1.07 GB, dense K/V 1.07 GB per step); no flush",
+        "parallelism": "replicas: each rank decodes its own sequence",
+        "l2": "inputs larger than L2 (each step reads about 10 GB of surviving K/V); no flush",
     }
+
+
+def c2_desc(w=C2):
+    return (f"{w['name']}: one layer, d_model {w['d_model']}, {w['n_q_heads']} q / {w['n_kv_heads']} kv heads, "
+            f"head_dim {w['head_dim']}, batch {w['batch']}, context {w['n_pos']}, KVzap-Linear scorer, threshold "
+            f"at each head's {int(w['prune_q'] * 100)}th-percentile score, last {w['window']} tokens kept; step = "
+            f"score + mask + compact + decode attention")
 
 
 # --------------------------------------------------------------------------- oracle sample (CPU)
 
 class OracleSample:
-    """One sequence of the workload drawn once on the host; run(rows) times the
-    oracle over the last `rows` cached positions of it (score, mask,
-    compaction, attention of the sequence's query heads) and returns (seconds,
-    sequences-equivalent = rows / n_pos)."""
+    """`heads` of the 64 heads of one layer of the headline workload, at its
+    full context, drawn once on the host (seeded): the C++ oracle scores the
+    prompt of those heads, sets each head's threshold at its quantile 1 - r
+    (r ~ Beta(2, 5)), compacts the kept entries with the reserve, then runs
+    decode steps (the new token scored, appended, attention). A decode step of
+    the sample is heads / 64 of one layer's step; the full step is 8 layers."""
 
-    def __init__(self, seed: int = 0, w=WORKLOAD):
+    def __init__(self, heads=8, seed=0, w=C5):
         import kvp_synth as syn
-        self.w = w
-        D, H, d, T = w["d_model"], w["n_kv_heads"], w["head_dim"], w["n_pos"]
-        G = w["n_q_heads"] // H
-        self.x, self.W = syn.linear_inputs(seed, T, D, H)
-        self.k, self.v = syn.kv_inputs(seed, 1, T, H, d)
-        self.q = syn.q_inputs(seed, 1, H * G, d)
-        self.tau = np.zeros((1, H), np.float32)  # the oracle's work does not depend on tau's value
-        self.phases = {"score": 0.0, "mask": 0.0, "compact": 0.0, "attention": 0.0}
-
-    def run(self, rows: int):
         import oracle as orc
-        w = self.w
-        H, T = w["n_kv_heads"], w["n_pos"]
-        now, pos0 = T - 1, T - rows
+        self.orc, self.w, self.heads = orc, w, heads
+        D, T, d = w["d_model"], w["n_pos"], w["head_dim"]
+        h = heads
         t0 = time.perf_counter()
-        s = orc.score_linear(self.x[pos0:], self.W).reshape(1, rows, H)
+        self.x = syn.fast_normal_bf16(seed, syn.S_X, (T, D))
+        self.W = syn.normal_f32(seed, syn.S_W, (h, D), std=1.0 / math.sqrt(D))
+        self.k = syn.fast_normal_bf16(seed, syn.S_K, (1, T, h, d))
+        self.v = syn.fast_normal_bf16(seed, syn.S_V, (1, T, h, d))
+        self.r = syn.beta_2_5(seed, syn.S_KEEPRATE, (h,))
+        self.steps = [(syn.normal_bf16(seed, syn.step_stream(i, 1), (1, D)),
+                       syn.normal_bf16(seed, syn.step_stream(i, 2), (1, h, d)),
+                       syn.normal_bf16(seed, syn.step_stream(i, 3), (1, h, d)),
+                       syn.normal_bf16(seed, syn.step_stream(i, 4), (1, h, d))) for i in range(w["steps"])]
+        self.gen_s = time.perf_counter() - t0
+        self.phase = {}
+
+    def prefill(self):
+        orc, w = self.orc, self.w
+        T, R = w["n_pos"], w["reserve"]
+        t0 = time.perf_counter()
+        s = orc.score_linear(self.x, self.W).reshape(1, T, self.heads)
         t1 = time.perf_counter()
-        exp = orc.mask_kvzap(s, self.tau, now, window=w["window"], pos0=pos0)[0]
+        self.tau = orc.threshold_at_quantile(s, 1.0 - self.r)
+        exp = orc.mask_kvzap(s, self.tau, T - 1, window=w["window"])[0]
         t2 = time.perf_counter()
-        mp = (rows + 15) // 16
-        c = orc.compact_dense(self.k[:, pos0:], self.v[:, pos0:], exp, now, 0, H * mp, mp)
+        mp = (T + w["steps"] + R + 15) // 16
+        cnt = orc.mask(exp, T - 1)[2]
+        self.cache0 = orc.compact_dense(self.k, self.v, exp, T - 1, R, int(((cnt + R + 15) // 16).sum()), mp)
         t3 = time.perf_counter()
-        orc.decode_attention(self.q, c, now)
-        t4 = time.perf_counter()
-        for k, dt in zip(("score", "mask", "compact", "attention"), (t1 - t0, t2 - t1, t3 - t2, t4 - t3)):
-            self.phases[k] += dt
-        return t4 - t0, rows / T
+        self.phase = {"score_s": t1 - t0, "threshold_mask_s": t2 - t1, "compact_s": t3 - t2}
+        self.cache = self.cache0
+        return t3 - t0
+
+    def reset(self):
+        c0 = self.cache0
+        self.cache = self.orc.PagedCache(1, self.heads, self.w["head_dim"], c0.k_pool.shape[0], c0.page_table.shape[2])
+        for name in ("k_pool", "v_pool", "expire_pool", "page_table", "remap", "count"):
+            getattr(self.cache, name)[...] = getattr(c0, name)
+        self.cache.pages_used = c0.pages_used
+
+    def decode_step(self, i, heads=None):
+        """Decode step i of the sample (i < 32) over its first `heads` heads."""
+        orc, w = self.orc, self.w
+        h = self.heads if heads is None else heads
+        T = w["n_pos"]
+        xn, kn, vn, qn = self.steps[i]
+        t0 = time.perf_counter()
+        sn = orc.score_linear(xn, self.W[:h])
+        if h == self.heads:
+            orc.append(self.cache, kn, vn, T + i, orc.expire_kvzap(sn, self.tau, T + i, w["window"]))
+            orc.decode_attention(qn, self.cache, T + i)
+        else:   # a cache of the first h heads only: the attention over them
+            sub = orc.PagedCache(1, h, w["head_dim"], 1, 1)
+            sub.k_pool, sub.v_pool, sub.expire_pool = self.cache.k_pool, self.cache.v_pool, self.cache.expire_pool
+            sub.page_table = np.ascontiguousarray(self.cache.page_table[:, :h])
+            sub.remap = np.ascontiguousarray(self.cache.remap[:, :h])
+            sub.count = np.ascontiguousarray(self.cache.count[:, :h])
+            orc.append(sub, np.ascontiguousarray(kn[:, :h]), np.ascontiguousarray(vn[:, :h]), T + i,
+                       orc.expire_kvzap(sn, self.tau[:, :h], T + i, w["window"]))
+            self.cache.count[:, :h] = sub.count
+            orc.decode_attention(np.ascontiguousarray(qn[:, :h]), sub, T + i)
+        return time.perf_counter() - t0
+
+    def tokens_per_step(self, heads=None):
+        """Decode tokens of the full workload that one sample step stands for."""
+        h = self.heads if heads is None else heads
+        return h / (self.w["n_heads"] * self.w["n_layers"])
 
 
 def run_cpu_baseline(budget_s: float):
-    """About `budget_s` seconds of oracle work, single-threaded."""
-    T = WORKLOAD["n_pos"]
-    sample = OracleSample()
-    t1, _ = sample.run(T)
-    total_t, total_seq, runs = t1, 1.0, 1
-    while total_t < budget_s and runs < 1000:
-        t, sq = sample.run(T)
-        total_t += t
-        total_seq += sq
-        runs += 1
-    return {"value": total_seq / total_t, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{runs} full sequences of the workload (one sequence's 8192 cached positions, drawn once "
-                      f"and re-run): float64 score, mask, compaction and attention of its query heads, one thread",
-            "seconds": total_t, "phase_seconds": {k: round(v, 3) for k, v in sample.phases.items()}}
+    import oracle as orc
+    s = OracleSample()
+    t_pref = s.prefill()
+    n, t = 0, 0.0
+    while t < budget_s and n < 10000:
+        if n % C5["steps"] == 0:
+            s.reset()
+        t += s.decode_step(n % C5["steps"])
+        n += 1
+    value = n * s.tokens_per_step() / t
+    return {"value": value, "unit": UNIT, "cores": orc.threads(), "kind": "oracle",
+            "sample": (f"C++ oracle (float64, std::thread over heads and rows, {orc.threads()} threads): {s.heads} of "
+                       f"the 64 heads of one layer at the full 131072-token context; prompt scored, thresholded at "
+                       f"quantile 1 - r per head and compacted once ({t_pref:.1f} s), then {n} decode steps (new token "
+                       f"scored, appended, attention) in {t:.1f} s; value = the equivalent full 8-layer decode steps "
+                       f"per second"),
+            "seconds": t, "prefill_seconds_sample": t_pref, "prefill_phase_seconds": s.phase,
+            "input_generation_seconds": s.gen_s}
 
 
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
-    T = WORKLOAD["n_pos"]
+    import oracle as orc
+    s = OracleSample()
+    s.prefill()
+    s.reset()
+    t1 = s.decode_step(0, heads=1)   # one head of the decode step
     budget = 120.0
-    sample = OracleSample()
-    t1, _ = sample.run(T)
-    rows = int(max(64, min(T, budget / max(1, args.steps + args.warmup) / (t1 / T))))
-    for _ in range(args.warmup):
-        sample.run(rows)
-    total_t, total_seq = 0.0, 0.0
-    for _ in range(args.steps):
-        t, sq = sample.run(rows)
-        total_t += t
-        total_seq += sq
-    value = total_seq / total_t
+    heads = int(max(1, min(s.heads, budget / max(1, args.steps + args.warmup) / max(t1, 1e-6))))
+    s.reset()
+    for i in range(args.warmup):
+        s.decode_step(i % C5["steps"], heads)
+    s.reset()
+    total_t, done = 0.0, 0
+    for i in range(args.steps):
+        if i > 0 and i % C5["steps"] == 0:
+            s.reset()
+        total_t += s.decode_step(i % C5["steps"], heads)
+        done += 1
+    value = done * s.tokens_per_step(heads) / total_t
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": config_desc(), "impl": "reference",
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"per step the last {rows} cached positions of one sequence ({rows / T:.4f} of "
-                                   f"a sequence's decode step): score, mask, compaction, attention in float64"},
+        "config": c5_desc(), "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.threads(), "kind": "oracle",
+                         "sample": f"per step {heads} of the 64 heads of one layer's decode step (new token scored, "
+                                   f"appended, attention over the pruned 131072-token cache) in float64 C++; value "
+                                   f"= the equivalent full 8-layer decode steps per second"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-# --------------------------------------------------------------------------- GPU arm
+# --------------------------------------------------------------------------- GPU helpers
 
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
@@ -252,192 +302,346 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def _events(torch, n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def _attn_src_sha():
+    with open(os.path.join(ROOT, "kv_cache_pruning_gb300", "csrc", "attn.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# --------------------------------------------------------------------------- headline: 65B-shaped decode step
+
+def run_c5(args, rank, world, kvp, torch, dev):
+    w = C5
+    B, T, D, H, d, L, R, S = (w["batch"], w["n_pos"], w["d_model"], w["n_heads"], w["head_dim"], w["n_layers"],
+                              w["reserve"], w["steps"])
+    now0 = T - 1
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 * args.seed + rank)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
+    pre = {"score_ms": 0.0, "mask_compact_ms": 0.0}
+    layers = []
+    kept = 0
+    for layer in range(L):
+        x = torch.randn(B * T, D, generator=g, device=dev).to(torch.bfloat16)
+        wt = torch.randn(H, D, generator=g, device=dev) / math.sqrt(D)
+        wsplit = kvp.kvp_score_split_weight(wt)
+        scores = torch.empty(B * T, H, dtype=torch.float32, device=dev)
+
+        def score():
+            kvp.kvp_score(x, wsplit, scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H, out=scores, status=st)
+
+        score()
+        e0, e1 = _events(torch, 2)
+        e0.record(stream)
+        score()
+        e1.record(stream)
+        # per-head keep rate r ~ Beta(2, 5) (the 2nd smallest of 6 uniforms); the threshold is the head's
+        # lower order statistic at index floor((1 - r) (T - 1)) (harness set-up on the device, untimed)
+        r = torch.rand((H, 6), generator=g, device=dev).sort(dim=1).values[:, 1]
+        idx = torch.floor((1 - r) * (T - 1)).long()
+        tau = scores.view(B, T, H).sort(dim=1).values.gather(1, idx.view(1, 1, H).expand(B, 1, H)).view(B, H)
+        tau = tau.contiguous()
+        _, _, cnt = kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=now0, scores=scores,
+                                 tau=tau, window=w["window"], want_bits=False)
+        torch.cuda.synchronize()
+        pages = int(((cnt + R + 15) // 16).sum().item())
+        mp = (T + S + R + 15) // 16
+        cache = kvp.PagedKV.allocate(B, H, d, pages, mp, device=dev)
+        K = torch.randn(B, T, H, d, generator=g, device=dev).to(torch.bfloat16)
+        V = torch.randn(B, T, H, d, generator=g, device=dev).to(torch.bfloat16)
+        e2, e3 = _events(torch, 2)
+        e2.record(stream)
+        kvp.kvp_compact_masked(K, V, now0, R, cache, mode=kvp.KVP_MASK_KVZAP, scores=scores, tau=tau,
+                               window=w["window"], status=st, workspace=ws_c)
+        e3.record(stream)
+        torch.cuda.synchronize()
+        assert st.item() == 0, kvp.status_string(st.item())
+        pre["score_ms"] += e0.elapsed_time(e1)
+        pre["mask_compact_ms"] += e2.elapsed_time(e3)
+        kept += int(cache.count.sum().item())
+        layers.append(dict(wsplit=wsplit, tau=tau, cache=cache, count0=cache.count.clone()))
+        del x, K, V, scores
+        torch.cuda.empty_cache()
+
+    # per-step inputs of the 32 decode steps, resident; staged into fixed buffers inside the graph
+    xs = torch.randn(S, L, B, D, generator=g, device=dev).to(torch.bfloat16)
+    ks = torch.randn(S, L, B, H, d, generator=g, device=dev).to(torch.bfloat16)
+    vs = torch.randn(S, L, B, H, d, generator=g, device=dev).to(torch.bfloat16)
+    qs = torch.randn(S, L, B, H, d, generator=g, device=dev).to(torch.bfloat16)
+    x_st = torch.empty(1, L, B, D, dtype=torch.bfloat16, device=dev)
+    k_st = torch.empty(1, L, B, H, d, dtype=torch.bfloat16, device=dev)
+    v_st = torch.empty_like(k_st)
+    q_st = torch.empty_like(k_st)
+    s_new = torch.empty(L, B, H, dtype=torch.float32, device=dev)
+    out = torch.empty(L, B, H, d, dtype=torch.float32, device=dev)
+    pos = torch.full((1,), T, dtype=torch.int32, device=dev)
+    sidx = torch.zeros(1, dtype=torch.int64, device=dev)
+    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, H, H, d), dtype=torch.uint8, device=dev)
+
+    def step():
+        torch.index_select(xs, 0, sidx, out=x_st)
+        torch.index_select(ks, 0, sidx, out=k_st)
+        torch.index_select(vs, 0, sidx, out=v_st)
+        torch.index_select(qs, 0, sidx, out=q_st)
+        for li, Ld in enumerate(layers):
+            kvp.kvp_score(x_st[0, li], Ld["wsplit"], scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H,
+                          out=s_new[li], status=st)
+            kvp.kvp_append_devpos(Ld["cache"], k_st[0, li], v_st[0, li], pos, mode=kvp.KVP_MASK_KVZAP,
+                                  score=s_new[li], tau=Ld["tau"], window=w["window"], status=st)
+            kvp.kvp_decode_attn_devpos(q_st[0, li], Ld["cache"], pos, out=out[li], workspace=ws_a, status=st)
+        pos.add_(1)
+        sidx.add_(1)
+
+    def reset():
+        for Ld in layers:
+            Ld["cache"].count.copy_(Ld["count0"])
+        pos.fill_(T)
+        sidx.zero_()
+
+    def attn_only():   # the dominant kernel alone: the 8 layers' attention at the current position
+        for li, Ld in enumerate(layers):
+            kvp.kvp_decode_attn_devpos(q_st[0, li], Ld["cache"], pos, out=out[li], workspace=ws_a, status=st)
+
+    reset()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    reset()
+    torch.cuda.synchronize()
+    assert st.item() == 0, kvp.status_string(st.item())
+    g_step, g_reset, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step()
+    with torch.cuda.graph(g_reset):
+        reset()
+    with torch.cuda.graph(g_attn):
+        attn_only()
+    g_reset.replay()
+    for _ in range(args.warmup):
+        g_step.replay()
+    g_reset.replay()
+    torch.cuda.synchronize()
+    assert st.item() == 0, kvp.status_string(st.item())
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+    t0, t1 = _events(torch, 2)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        if dist:
+            tdist.barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(args.steps):
+            if i > 0 and i % S == 0:
+                g_reset.replay()
+            g_step.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            tdist.barrier()
+    clocks = clk.summary()
+    assert st.item() == 0, kvp.status_string(st.item())
+    ms_step = max_over_ranks(t0.elapsed_time(t1), dev) / args.steps
+
+    # ---- the dominant kernel: the attention launches of one step, alone (8 launches per replay), at the
+    # prompt's cache; algorithmic bytes = surviving pages x (16 K rows + 16 V rows + 16 expire values) + q + out
+    g_reset.replay()
+    g_attn.replay()
+    torch.cuda.synchronize()
+    n_rep = 10
+    a0, a1 = _events(torch, 2)
+    a0.record(stream)
+    for _ in range(n_rep):
+        g_attn.replay()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    attn_ms = a0.elapsed_time(a1) / (n_rep * L)
+    pages = [int(((Ld["count0"] + 15) // 16).sum().item()) for Ld in layers]
+    page_b = 16 * (2 * d * 2 + 4)
+    attn_b = sum(pages) * page_b / L + B * H * d * (2 + 4)
+    hbm, _, peak_kind = measured_peaks()
+    traffic = None
+    if args.traffic is not None:
+        traffic = args.traffic
+    elif ATTN_DRAM_BYTES_PER_PAGE is not None and ATTN_SRC_SHA == _attn_src_sha():
+        traffic = ATTN_DRAM_BYTES_PER_PAGE * sum(pages) / L
+    roofline = {"bound": "hbm", "kernel": "attn_decode_kernel<128, 1> (split-KV decode attention)",
+                "achieved": attn_b / (attn_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                "frac": attn_b / (attn_ms * 1e-3) / 1e9 / hbm,
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                "traffic": traffic, "launch_us": attn_ms * 1e3, "algorithmic_bytes_per_launch": int(attn_b),
+                "timing": "CUDA events around 10 replays of a graph of the step's 8 attention launches"}
+    step_b = sum(pages) * page_b + L * (B * D * 2 + B * H * d * (2 * 3 + 4))
+    value = weak_scaling_value(B, world, ms_step)
+
+    # ---- end to end through the public API: pinned host inputs copied in and the output copied out every
+    # step, the calls launched eagerly from the host
+    e2e = None
+    if not args.no_e2e:
+        xh, kh, vh, qh = (t.cpu().pin_memory() for t in (xs, ks, vs, qs))
+        outh = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        xb, kb, vb, qb = (torch.empty(t.shape[1:], dtype=t.dtype, device=dev) for t in (xs, ks, vs, qs))
+        h2d = sum(t[0].numel() * t.element_size() for t in (xh, kh, vh, qh))
+        d2h = outh.numel() * outh.element_size()
+
+        def e2e_step(i):
+            j = i % S
+            if j == 0:
+                for Ld in layers:
+                    Ld["cache"].count.copy_(Ld["count0"])
+            for dst, src in ((xb, xh), (kb, kh), (vb, vh), (qb, qh)):
+                dst.copy_(src[j], non_blocking=True)
+            for li, Ld in enumerate(layers):
+                kvp.kvp_score(xb[li], Ld["wsplit"], scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H,
+                              out=s_new[li], status=st)
+                kvp.kvp_append(Ld["cache"], kb[li], vb[li], T + j, mode=kvp.KVP_MASK_KVZAP, score=s_new[li],
+                               tau=Ld["tau"], window=w["window"], status=st)
+                kvp.kvp_decode_attn(qb[li], Ld["cache"], T + j, out=out[li], workspace=ws_a, status=st)
+            outh.copy_(out, non_blocking=True)
+
+        for i in range(S):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        n_e2e = 2 * S
+        if dist:
+            tdist.barrier()
+        b0, b1 = _events(torch, 2)
+        b0.record(stream)
+        for i in range(n_e2e):
+            e2e_step(i)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        assert st.item() == 0, kvp.status_string(st.item())
+        e_ms = max_over_ranks(b0.elapsed_time(b1) / n_e2e, dev)
+        e2e = {"value": weak_scaling_value(B, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms, "steps": n_e2e,
+               "how": "per step: pinned host inputs of the 8 layers copied in, the 24 calls launched eagerly "
+                      "through the Python binding of the C ABI, the 8 layers' outputs copied back"}
+
+    res = {"value": value, "ms_per_step": ms_step, "clocks": clocks, "roofline": roofline, "e2e": e2e,
+           "gpu_launches": 3 * L * args.steps,
+           "effective_step_GB_s": step_b / (ms_step * 1e-3) / 1e9,
+           "effective_step_frac_of_hbm": step_b / (ms_step * 1e-3) / 1e9 / hbm,
+           "attention_share_of_step": L * attn_ms / ms_step,
+           "kept_fraction": kept / (L * H * T),
+           "surviving_kv_bytes_per_step": sum(pages) * page_b, "pages_per_layer": pages,
+           "prefill": {"score_ms_8_layers": pre["score_ms"],
+                       "score_GB_s": L * B * T * D * 2 / (pre["score_ms"] * 1e-3) / 1e9,
+                       "mask_compact_ms_8_layers": pre["mask_compact_ms"]}}
+    del layers, xs, ks, vs, qs
+    torch.cuda.empty_cache()
+    return res
+
+
+# --------------------------------------------------------------------------- Llama-3-8B-shaped layer
+
+def run_c2(args, rank, world, kvp, torch, dev, steps):
+    w = C2
+    B, T, H, Hq, d, D = w["batch"], w["n_pos"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"], w["d_model"]
+    n_tok = B * T
+    now = T - 1
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 * args.seed + rank + 7)
+    x = torch.randn(n_tok, D, generator=g, device=dev).to(torch.bfloat16)
+    W = torch.randn(H, D, generator=g, device=dev) / math.sqrt(D)
+    K = torch.randn(B, T, H, d, generator=g, device=dev).to(torch.bfloat16)
+    V = torch.randn(B, T, H, d, generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn(B, Hq, d, generator=g, device=dev).to(torch.bfloat16)
+    max_pages = (T + 15) // 16
+    cache = kvp.PagedKV.allocate(B, H, d, B * H * max_pages, max_pages, device=dev)
+    scores = torch.empty(n_tok, H, dtype=torch.float32, device=dev)
+    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
+    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
+    Ws = kvp.kvp_score_split_weight(W)
+    kvp.kvp_score(x, Ws, scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H, out=scores, status=st)
+    tau = kvp.kvp_threshold(scores.view(B, T, H), w["prune_q"])
+    stream = torch.cuda.current_stream(dev)
+
+    def p_score():
+        kvp.kvp_score(x, Ws, scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H, out=scores, status=st)
+
+    def p_compact():
+        kvp.kvp_compact_masked(K, V, now, 0, cache, mode=kvp.KVP_MASK_KVZAP, scores=scores, tau=tau,
+                               window=w["window"], status=st, workspace=ws_c)
+
+    def p_attn():
+        kvp.kvp_decode_attn(q, cache, now, out=out, workspace=ws_a, status=st)
+
+    def step():
+        p_score()
+        p_compact()
+        p_attn()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert st.item() == 0, kvp.status_string(st.item())
+    kept = int(cache.count.sum().item())
+    surv_pages = int(((cache.count + 15) // 16).sum().item())
+    graphs = {}
+    for name, fn in (("step", step), ("score", p_score), ("mask+compact", p_compact), ("decode_attn", p_attn)):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            fn()
+        graphs[name] = gr
+    for _ in range(3):
+        graphs["step"].replay()
+    torch.cuda.synchronize()
+    e0, e1 = _events(torch, 2)
+    e0.record(stream)
+    for _ in range(steps):
+        graphs["step"].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert st.item() == 0, kvp.status_string(st.item())
+    ms_step = e0.elapsed_time(e1) / steps
+    # each phase alone, as its own graph (launch overhead excluded, as in the step's graph)
+    phase_ms = {}
+    for name in ("score", "mask+compact", "decode_attn"):
+        graphs[name].replay()
+        torch.cuda.synchronize()
+        p0, p1 = _events(torch, 2)
+        p0.record(stream)
+        for _ in range(20):
+            graphs[name].replay()
+        p1.record(stream)
+        torch.cuda.synchronize()
+        phase_ms[name] = p0.elapsed_time(p1) / 20
+    row_b = d * 2
+    score_b = n_tok * D * 2 + Ws.numel() * 2 + n_tok * H * 4
+    compact_b = n_tok * H * 4 + B * H * 4 + 2 * kept * 2 * row_b + kept * 4 + B * H * max_pages * 16 * 4 \
+        + B * H * max_pages * 4
+    attn_b = surv_pages * 16 * (2 * row_b + 4) + B * Hq * d * 2 + B * Hq * d * 4
+    hbm, _, _ = measured_peaks()
+    kb = {"score": score_b, "mask+compact": compact_b, "decode_attn": attn_b}
+    kernels = {n: {"ms": phase_ms[n], "bytes": int(kb[n]), "GB_s": kb[n] / (phase_ms[n] * 1e-3) / 1e9,
+                   "frac_of_hbm": kb[n] / (phase_ms[n] * 1e-3) / 1e9 / hbm} for n in kb}
+    res = {"workload": c2_desc(), "value": weak_scaling_value(B, world, ms_step), "unit": UNIT,
+           "ms_per_step": ms_step, "steps": steps, "kernels": kernels, "kept_fraction": kept / (B * H * T),
+           "scored_tokens_per_s": n_tok / (phase_ms["score"] * 1e-3),
+           "timing": "the step replayed as one CUDA graph; each phase alone as its own graph of one call"}
+    del x, K, V, cache
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args, rank: int, world: int):
     import torch
     import __graft_entry__
     __graft_entry__.build()
     import kv_cache_pruning_gb300 as kvp
 
-    w = dict(WORKLOAD)
-    if args.batch:
-        w["batch"] = args.batch
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    B, T, H, Hq, d, D = w["batch"], w["n_pos"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"], w["d_model"]
-    n_tok = B * T
-    now = T - 1
-
-    # ---- seeded synthetic inputs, resident in HBM
-    g = torch.Generator(device=dev)
-    g.manual_seed(1000 * args.seed + rank)
-    x = torch.randn(n_tok, D, generator=g, device=dev).to(torch.bfloat16)
-    W = torch.randn(H, D, generator=g, device=dev) / math.sqrt(D)
-    K = torch.randn(B, T, H, d, generator=g, device=dev).to(torch.bfloat16)
-    V = torch.randn(B, T, H, d, generator=g, device=dev).to(torch.bfloat16)
-    q = torch.randn(B, Hq, d, generator=g, device=dev).to(torch.bfloat16)
-
-    # ---- buffers, sized once (keep-all capacity), reused by every step
-    max_pages = (T + 15) // 16
-    n_pages_cap = B * H * max_pages
-    cache = kvp.PagedKV.allocate(B, H, d, n_pages_cap, max_pages, device=dev)
-    scores = torch.empty(n_tok, H, dtype=torch.float32, device=dev)
-    separate = args.mask == "separate"  # the mask's own outputs exist only when it runs as its own kernel
-    expire = torch.empty(B, H, T, dtype=torch.int32, device=dev) if separate else None
-    bits = torch.empty(B, H, (T + 31) // 32, dtype=torch.int32, device=dev) if separate else None
-    count = torch.empty(B, H, dtype=torch.int32, device=dev) if separate else None
-    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws_s = torch.empty(kvp.kvp_score_workspace_bytes(0, n_tok, D, H), dtype=torch.uint8, device=dev)
-    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
-    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, Hq, H, d), dtype=torch.uint8, device=dev)
-
-    # ---- the layer's scorer weight in tensor-core form, made once per layer
-    # like the weight itself (set-up, untimed)
-    Ws = kvp.kvp_score_split_weight(W)
-
-    # ---- threshold per (b, h): the 75th-percentile score, chosen on the device
-    # (harness set-up, untimed)
-    kvp.kvp_score(x, W, out=scores, workspace=ws_s, status=status)
-    tau = kvp.kvp_threshold(scores.view(B, T, H), w["prune_q"])
-    fused = args.mask == "fused"
-
-    stream = torch.cuda.current_stream(dev)
-    # event slots per step: before score, [mask,] compact, attention, after
-    names = ["score", "mask+compact", "decode_attn"] if fused else ["score", "mask", "compact", "decode_attn"]
-    N_EV = len(names) + 1
-
-    def step(evs=None):
-        e = iter(evs) if evs is not None else None
-        if e is not None:
-            next(e).record(stream)
-        kvp.kvp_score(x, Ws, scorer=kvp.KVP_SCORER_LINEAR_SPLIT, n_kv_heads=H, out=scores, status=status)
-        if e is not None:
-            next(e).record(stream)
-        if fused:
-            kvp.kvp_compact_masked(K, V, now, 0, cache, mode=kvp.KVP_MASK_KVZAP, scores=scores, tau=tau,
-                                   window=w["window"], status=status, workspace=ws_c)
-        else:
-            kvp.kvp_mask(mode=kvp.KVP_MASK_KVZAP, batch=B, n_kv_heads=H, n_pos=T, now=now, scores=scores, tau=tau,
-                         window=w["window"], expire=expire, keep_bits=bits, count=count)
-            if e is not None:
-                next(e).record(stream)
-            kvp.kvp_compact(K, V, expire, now, 0, cache, status=status, workspace=ws_c)
-        if e is not None:
-            next(e).record(stream)
-        kvp.kvp_decode_attn(q, cache, now, out=out, workspace=ws_a, status=status)
-        if e is not None:
-            next(e).record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert status.item() == 0, kvp.status_string(status.item())
-    count = cache.count
-    kept = int(count.sum().item())
-    surv_pages = int(((count + 15) // 16).sum().item())
-
-    dist = world > 1
-    if dist:
-        import torch.distributed as tdist
-    # The step is captured once as a CUDA graph (its kernels and memsets as
-    # nodes) and replayed: no host launch work inside the timed region.
-    graph = None
-    if not args.eager:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
-        for _ in range(args.warmup):
-            graph.replay()
-        torch.cuda.synchronize()
-        assert status.item() == 0, kvp.status_string(status.item())
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        if dist:
-            tdist.barrier()
-        torch.cuda.synchronize()
-        t_start.record(stream)
-        for i in range(args.steps):
-            if graph is not None:
-                graph.replay()
-            else:
-                step()
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        if dist:
-            tdist.barrier()
-    clocks = clk.summary()
-    assert status.item() == 0, kvp.status_string(status.item())
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
-    ms_step = total_ms / args.steps
-
-    # ---- per-phase times: eager steps with an event between phases (a
-    # separate loop, so these events are not inside the timed region above)
-    n_break = max(3, min(args.steps, 50))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(N_EV)] for _ in range(n_break)]
-    for i in range(n_break):
-        step(evs[i])
-    torch.cuda.synchronize()
-    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(N_EV - 1)] for i in range(n_break)])
-    k_ms = per.mean(axis=0)  # per phase of `names` (per launch, ms)
-
-    # ---- algorithmic bytes (what the method must move)
-    x_b = n_tok * D * 2
-    score_b = x_b + Ws.numel() * 2 + n_tok * H * 4
-    mask_b = n_tok * H * 4 + B * H * 4 + B * H * T * 4 + B * H * ((T + 31) // 32) * 4 + B * H * 4
-    row_b = d * 2
-    compact_b = 2 * B * H * T * 4 + 2 * kept * 2 * row_b + kept * 4 + B * H * max_pages * 16 * 4 \
-        + B * H * max_pages * 4
-    attn_b = surv_pages * 16 * (2 * row_b + 4) + B * Hq * d * 2 + B * Hq * d * 4
-    # fused: the mask reads the scores and thresholds and writes nothing of its own
-    fused_b = n_tok * H * 4 + B * H * 4 + (compact_b - 2 * B * H * T * 4)
-    kb = [score_b, fused_b, attn_b] if fused else [score_b, mask_b, compact_b, attn_b]
-    step_b = sum(kb)
-    hbm, _, peak_kind = measured_peaks()
-    kernels = {n: {"ms": float(k_ms[i]), "bytes": int(kb[i]), "GB_s": kb[i] / (k_ms[i] * 1e-3) / 1e9,
-                   "frac_of_hbm": kb[i] / (k_ms[i] * 1e-3) / 1e9 / hbm} for i, n in enumerate(names)}
-    dom = int(np.argmax(k_ms))
-    traffic = args.traffic
-    if traffic is None and names[dom] == "score":
-        traffic = SCORE_DRAM_BYTES_PER_ROW * n_tok
-    roofline = {"bound": "hbm", "kernel": names[dom], "achieved": kb[dom] / (k_ms[dom] * 1e-3) / 1e9,
-                "peak": hbm, "unit": "GB/s", "frac": kb[dom] / (k_ms[dom] * 1e-3) / 1e9 / hbm,
-                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
-                "traffic": traffic}
-    value = weak_scaling_value(B, world, ms_step)
-
-    # ---- end to end: pinned host inputs in, result out, inside the timed region
-    e2e = None
-    if not args.no_e2e:
-        xh = x.cpu().pin_memory()
-        Kh, Vh, qh = K.cpu().pin_memory(), V.cpu().pin_memory(), q.cpu().pin_memory()
-        Wh, tauh = Ws.cpu().pin_memory(), tau.cpu().pin_memory()
-        outh = torch.empty_like(out, device="cpu").pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (xh, Kh, Vh, qh, Wh, tauh))
-        d2h = outh.numel() * outh.element_size()
-
-        def e2e_step():
-            for dst, src in ((x, xh), (K, Kh), (V, Vh), (q, qh), (Ws, Wh), (tau, tauh)):
-                dst.copy_(src, non_blocking=True)
-            step()
-            outh.copy_(out, non_blocking=True)
-
-        n_e2e = max(3, min(args.steps, args.e2e_steps))
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        if dist:
-            tdist.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
-        e2e = {"value": weak_scaling_value(B, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms, "steps": n_e2e,
-               "h2d_GB_s": h2d / (e_ms * 1e-3) / 1e9}
-
+    c5 = run_c5(args, rank, world, kvp, torch, dev)
+    c2 = None if args.no_c2 else run_c2(args, rank, world, kvp, torch, dev, steps=min(args.steps, 200))
     if rank != 0:
         return
     cpu = None
@@ -447,17 +651,21 @@ def run_gpu(args, rank: int, world: int):
         try:
             cpu = json.loads(r.stdout.strip().splitlines()[-1])
         except Exception:
-            cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+            cpu = {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": "failed: " + r.stderr[-300:]}
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch RNG, N(0,1) hidden states and K/V)",
-        "config": dict(config_desc(w, args.mask), cuda_graph=graph is not None), "e2e": e2e,
-        "gpu_launches": KERNELS_PER_STEP[args.mask] * args.steps, "roofline": roofline,
-        "kernels": kernels, "effective_step_GB_s": step_b / (ms_step * 1e-3) / 1e9,
-        "scored_tokens_per_s": n_tok / (k_ms[0] * 1e-3),
-        "scorer_overhead": scorer_overhead(w),
-        "kept_fraction": kept / (B * H * T), "clocks": clocks, "cpu_baseline": cpu,
+        "metric": METRIC, "value": c5["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": c5["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch RNG on the device: N(0,1) hidden "
+                                                      "states, K, V, q; weights N(0, 1/d_model); Beta(2,5) keep rates)",
+        "config": dict(c5_desc(), cuda_graph=True), "e2e": c5["e2e"], "gpu_launches": c5["gpu_launches"],
+        "roofline": c5["roofline"], "clocks": c5["clocks"], "cpu_baseline": cpu,
+        "effective_step_GB_s": c5["effective_step_GB_s"],
+        "effective_step_frac_of_hbm": c5["effective_step_frac_of_hbm"],
+        "attention_share_of_step": c5["attention_share_of_step"], "kept_fraction": c5["kept_fraction"],
+        "surviving_kv_bytes_per_step": c5["surviving_kv_bytes_per_step"], "pages_per_layer": c5["pages_per_layer"],
+        "prefill": c5["prefill"],
+        "llama3_8b_layer": c2,
     }
     print(json.dumps(line), flush=True)
 
@@ -465,28 +673,22 @@ def run_gpu(args, rank: int, world: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=640)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvp", choices=["kvp", "reference"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs only)")
-    ap.add_argument("--workload", default="llama3_8b_layer",
-                    choices=["llama3_8b_layer", "mlp_prefill", "dms_decode", "llama65b_mha", "prune_sweep",
+    ap.add_argument("--workload", default="llama65b_mha_decode",
+                    choices=["llama65b_mha_decode", "mlp_prefill", "dms_decode", "llama65b_mha", "prune_sweep",
                              "threshold", "quant_tier", "quant_decode", "gqa_sweep", "mla_sweep", "mla_dms_decode"],
-                    help="llama3_8b_layer = the bench line; the others print measurement lines "
+                    help="llama65b_mha_decode = the bench line; the others print measurement lines "
                          "(see bench_workloads.py)")
-    ap.add_argument("--eager", action="store_true", help="launch every step from the host (no CUDA graph)")
-    ap.add_argument("--mask", default="fused", choices=["fused", "separate"],
-                    help="fused: the mask is computed inside the compaction's passes (kvp_compact_masked); "
-                         "separate: kvp_mask writes expire, then kvp_compact reads it")
-    ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-c2", action="store_true", help="skip the Llama-3-8B-shaped layer's extra measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--cpu-baseline-only", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="DRAM bytes per launch of the dominant kernel from an ncu capture of this kernel "
-                         "(default: the scorer's measured bytes per row times the rows of one launch)")
+                    help="DRAM bytes per launch of the attention kernel from an ncu capture of this kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -495,15 +697,15 @@ def main():
         return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
-    if world > 1 and args.impl != "reference":
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
         import torch
         import torch.distributed as tdist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group("nccl")
-    if args.impl == "reference":
-        run_reference(args, rank, world)
-        return
-    if args.workload != "llama3_8b_layer":
+    if args.workload != "llama65b_mha_decode":
         import torch
         import __graft_entry__
         import bench_workloads

@@ -127,7 +127,11 @@ KVP_API kvp_status kvp_selftest_wait(uint64_t limit_ns, int32_t* status, uint32_
  *
  * The dense contraction runs on the tcgen05 tensor cores: LINEAR splits the
  * fp32 weight into two bf16 halves (hi + lo) so that the products keep ~16
- * mantissa bits of w; accumulation is fp32 throughout. LINEAR does that split
+ * mantissa bits of w; accumulation is fp32 throughout. Up to 64 rows (the
+ * new tokens of a decode step) LINEAR and LINEAR_SPLIT run the same
+ * products on the CUDA cores instead, spread over one CTA per head and
+ * group of 8 rows (a single 128-row tensor-core tile would leave the whole
+ * weight to one CTA). LINEAR does that split
  * on every call (one small kernel); a caller whose weight does not change
  * between calls (a decode loop: the weight is the layer's) splits it once with
  * kvp_score_split_weight and passes LINEAR_SPLIT; the scores are identical.
@@ -591,8 +595,9 @@ KVP_API kvp_status kvp_append_latent(int mode, int batch, int row_dim, int pos, 
  * unit's pages into n_splits equal slices, one CTA each (a CTA of a later
  * unit of the same slice reads the same pages, mostly from L2). Both
  * products run on the tensor cores: bf16 operands, fp32 accumulation, the
- * softmax weights entering the weighted sum as a bf16 hi + lo pair; slices
- * are merged in fp32 by the last CTA of the unit to finish.
+ * softmax weights entering the weighted sum as a bf16 hi + lo pair; with
+ * more than one slice, a second kernel launched by the same call merges the
+ * slices in fp32, one CTA per (unit, head).
  *
  * latent_dim, rope_dim  KVP_MLA_LATENT_DIM and KVP_MLA_ROPE_DIM (else
  *            KVP_ERR_UNSUPPORTED)
@@ -607,9 +612,9 @@ KVP_API kvp_status kvp_append_latent(int mode, int batch, int row_dim, int pos, 
  *            SM count (as many as fill one wave of two CTAs per SM, at least 1)
  * workspace  device, >= kvp_decode_attn_mla_workspace_bytes(batch,
  *            n_q_heads, n_splits) (asked on the device that runs the call
- *            when n_splits = 0), 16-byte aligned; zero-filled before its
- *            first use and left ready by every call that records no error,
- *            as kvp_decode_attn's workspace.
+ *            when n_splits = 0), 16-byte aligned; every call writes what it
+ *            reads, so it needs no clearing. Calls that share a workspace
+ *            must not overlap on the GPU.
  */
 KVP_API size_t kvp_decode_attn_mla_workspace_bytes(int batch, int n_q_heads, int n_splits);
 KVP_API kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_dim, int rope_dim, const void* q,

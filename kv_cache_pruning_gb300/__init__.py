@@ -718,18 +718,14 @@ def kvp_decode_attn_mla_workspace_bytes(batch, n_q_heads, n_splits=0) -> int:
 def kvp_decode_attn_mla(q, cache: LatentPagedKV, now, *, scale=0.0, out=None, n_splits=0, workspace=None,
                         status=None, stream=None):
     """out[B, Hq, 512] fp32 = absorbed MLA attention of q [B, Hq, 576] (bf16) over the latent slots of `cache`
-    present at `now`. A caller-provided workspace must be zero-filled before its first use (torch.zeros); calls
-    that record no error leave it that way."""
+    present at `now`. The workspace needs no clearing between calls."""
     B, Hq, R = q.shape
     if R != LATENT_ROW:
         raise ValueError(f"q rows must hold {LATENT_ROW} values")
     if out is None:
         out = torch.empty((B, Hq, KVP_MLA_LATENT_DIM), dtype=torch.float32, device=q.device)
     need = kvp_decode_attn_mla_workspace_bytes(B, Hq, n_splits)
-    if workspace is None:
-        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)  # zero-filled before first use
-    else:
-        ws = _ws(need, q.device, workspace)
+    ws = _ws(need, q.device, workspace)
     code = _lib.kvp_decode_attn_mla(B, Hq, KVP_MLA_LATENT_DIM, KVP_MLA_ROPE_DIM, _ptr(q, torch.bfloat16, "q"),
                                     _ptr(cache.pool, torch.bfloat16), _ptr(cache.expire_pool, torch.int32),
                                     cache.n_pages_cap, _ptr(cache.page_table, torch.int32), cache.max_pages,

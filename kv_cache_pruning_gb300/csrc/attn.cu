@@ -27,7 +27,10 @@ namespace kvp {
 namespace {
 
 constexpr int kWarps = 8;       // warps per CTA
-constexpr int kNst = 3;         // pages in flight per warp
+// Pages in flight per warp. Two beat three on a GB300 (Llama-3-8B-shaped cache,
+// G = 4: 88.1 / 32.4 / 16.4 us against 89.9 / 33.9 / 16.0 us at 0 / 75 /
+// 93.75 % pruned): 1,216 warps x 2 pages already keep about 20 MB in flight.
+constexpr int kNst = 2;
 constexpr int kMaxBH = 4096;    // (b, h) pairs whose page prefix fits in shared memory
 constexpr int kMaxCtas = 512;   // grid bound used to size the workspace
 // Fewest pages a warp's slice gets when there are not enough pages for every
@@ -178,7 +181,8 @@ KVP_DEV int slice_of(int g, int bh, int nw, int64_t c_end) {
 // them: writes the output rows and resets the (b, h)'s counter. With `staged`
 // (the warp's page ring is idle, at the end of its slice) two bulk copies
 // bring every piece into the ring in one round trip; otherwise the lanes load
-// them from L2. Returns false if a bounded wait gave up.
+// them from L2 (the staged path holds one piece per lane: npc <= 32). Returns
+// false if a bounded wait gave up.
 template <int D, int G>
 KVP_DEV bool merge_pieces(const AttnParams& p, int cbh, int npc, size_t s0, bool staged, uint8_t* ring,
                           uint64_t* mbar, uint32_t& merge_par, int lane) {
@@ -821,7 +825,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           constexpr int kAccB = G * D * 4, kMlB = G * 2 * 4;  // bytes of a piece's acc and (m, l)
-          constexpr int kStaged = (kNst * C::STAGE_BYTES - 32) / (kAccB + kMlB);  // pieces the idle ring holds
+          // pieces the staged merge takes: as many as the idle ring holds, and at
+          // most one per lane (its maxima and weights are held one piece per lane)
+          constexpr int kRingPieces = (kNst * C::STAGE_BYTES - 32) / (kAccB + kMlB);
+          constexpr int kStaged = kRingPieces < 32 ? kRingPieces : 32;
           const int npc = w_last - w_first + 1;
           if (!merge_pieces<D, G>(p, cbh, npc, static_cast<size_t>(w_first) + cbh, g + 1 == r1 && npc <= kStaged,
                                   ring, &bars[kNst], merge_par, lane))
@@ -1411,7 +1418,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           constexpr int kAccB = G * D * 4, kMlB = G * 2 * 4;  // bytes of a piece's acc and (m, l)
-          constexpr int kStaged = (kNst * C::STAGE_BYTES - 32) / (kAccB + kMlB);  // pieces the idle ring holds
+          // pieces the staged merge takes: as many as the idle ring holds, and at
+          // most one per lane (its maxima and weights are held one piece per lane)
+          constexpr int kRingPieces = (kNst * C::STAGE_BYTES - 32) / (kAccB + kMlB);
+          constexpr int kStaged = kRingPieces < 32 ? kRingPieces : 32;
           const int npc = w_last - w_first + 1;
           if (!merge_pieces<D, G>(p, cbh, npc, static_cast<size_t>(w_first) + cbh, g + 1 == r1 && npc <= kStaged,
                                   ring, &bars[kNst], merge_par, lane))

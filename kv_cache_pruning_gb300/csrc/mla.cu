@@ -23,8 +23,10 @@
 //   O^T += Cv^T P^T M = 16 of the 512 compressed values at a time, N = 16
 //                   heads, K = 16 tokens: warp w owns values 128w .. 128w+127
 //                   (8 m-tiles), its A operand read transposed by ldmatrix
-// Slices of a unit (batch element, 16 heads) are merged in fp32 by the last
-// CTA to finish, which resets the unit's arrival counter.
+// Slices of a unit (batch element, 16 heads) write their partial states; a
+// second kernel, launched right after as the first one's programmatic
+// dependent, merges them in fp32 with one CTA per (unit, head), so the
+// merge's reads of the partial accumulators are spread over the whole GPU.
 #include "kvp_common.cuh"
 
 namespace kvp {
@@ -74,7 +76,6 @@ struct MlaParams {
   float* out;                 // [B, Hq, kDc]
   float* part_acc;            // [units, NS, 16, kDc]
   float* part_ml;             // [units, NS, 16, 2]
-  int32_t* arrivals;          // [units]
   int32_t* status;
 };
 
@@ -82,9 +83,6 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
                                                                   const __grid_constant__ CUtensorMap tmL) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ float w_s[kHT][kMaxSplits];  // merge: weight of each slice per head
-  __shared__ float il_s[kHT];             // merge: 1 / total sum per head
-  __shared__ int last_s;
   pdl_launch_dependents();
   pdl_wait();  // counts, pages and the workspace counters come from the kernels before this one
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -381,54 +379,66 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
       }
     }
   }
-  fence_acq_rel_gpu();
-  __syncthreads();
-  if (tid == 0) last_s = atomicAdd(&p.arrivals[unit], 1) == p.NS - 1;
-  __syncthreads();
-  if (!last_s) return;
-  fence_acq_rel_gpu();
+}
 
-  // ---- merge of the unit's slices: weights per (head, slice), then the
-  // values as float4 columns
-  if (tid < kHT) {
-    const float* ml = p.part_ml + static_cast<int64_t>(unit) * p.NS * kHT * 2;
+// Merge of the slices of every unit: CTA (unit, hl) takes head h_base + hl,
+// thread c the float4 c of its 512 output values. The slices' (m, l) give
+// the weights exp2(m - M) (an empty slice, l = 0, has none and its
+// accumulator is not read), then the accumulators are summed with all of a
+// batch of slices' loads in flight.
+__global__ void __launch_bounds__(kDc / 4) mla_merge_kernel(const MlaParams p) {
+  __shared__ float w_s[kMaxSplits];
+  __shared__ float il_s;
+  pdl_launch_dependents();
+  pdl_wait();  // every slice's partial state is written
+  const int unit = static_cast<int>(blockIdx.x / kHT), hl = static_cast<int>(blockIdx.x % kHT);
+  const int b = unit / p.HT, h = (unit % p.HT) * kHT + hl;
+  if (h >= p.Hq) return;
+  const int c4 = threadIdx.x;
+  const float* ml = p.part_ml + static_cast<int64_t>(unit) * p.NS * kHT * 2;
+  if (c4 < 32) {
     float M = -INFINITY;
-    for (int sl = 0; sl < p.NS; ++sl) {
-      const float l = __ldcg(ml + (sl * kHT + tid) * 2 + 1);
-      if (l > 0.f) M = fmaxf(M, __ldcg(ml + (sl * kHT + tid) * 2));
+    for (int sl = c4; sl < p.NS; sl += 32) {
+      const float l = __ldcg(ml + (sl * kHT + hl) * 2 + 1);
+      if (l > 0.f) M = fmaxf(M, __ldcg(ml + (sl * kHT + hl) * 2));
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
-    for (int sl = 0; sl < p.NS; ++sl) {
-      const float l = __ldcg(ml + (sl * kHT + tid) * 2 + 1);
-      const float w = l > 0.f ? exp2f(__ldcg(ml + (sl * kHT + tid) * 2) - M) : 0.f;
-      w_s[tid][sl] = w;
+    for (int sl = c4; sl < p.NS; sl += 32) {
+      const float l = __ldcg(ml + (sl * kHT + hl) * 2 + 1);
+      const float w = l > 0.f ? exp2f(__ldcg(ml + (sl * kHT + hl) * 2) - M) : 0.f;
+      w_s[sl] = w;
       L += w * l;
     }
-    il_s[tid] = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (c4 == 0) il_s = L > 0.f ? 1.f / L : 0.f;
   }
   __syncthreads();
-  constexpr int kF4 = kDc / 4;
-  for (int idx = tid; idx < kHT * kF4; idx += kMThreads) {
-    const int hl = idx / kF4, c4 = idx - hl * kF4;
-    const int h = h_base + hl;
-    if (h >= p.Hq) continue;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sl = 0; sl < p.NS; ++sl) {
-      const float w = w_s[hl][sl];
-      if (w == 0.f) continue;  // empty slice: its accumulator was not written
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                                  p.part_acc + ((static_cast<int64_t>(unit) * p.NS + sl) * kHT + hl) * kDc) +
-                              c4);
-      a.x += w * v.x;
-      a.y += w * v.y;
-      a.z += w * v.z;
-      a.w += w * v.w;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* acc = reinterpret_cast<const float4*>(p.part_acc + static_cast<int64_t>(unit) * p.NS * kHT * kDc);
+  constexpr int kBatch = 8;
+  for (int s0 = 0; s0 < p.NS; s0 += kBatch) {
+    float4 v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int sl = s0 + j;
+      v[j] = (sl < p.NS && w_s[sl] != 0.f) ? __ldcg(acc + (static_cast<int64_t>(sl) * kHT + hl) * (kDc / 4) + c4)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float il = il_s[hl];
-    reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(b) * p.Hq + h) * kDc)[c4] =
-        make_float4(a.x * il, a.y * il, a.z * il, a.w * il);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const float w = s0 + j < p.NS ? w_s[s0 + j] : 0.f;
+      a.x = fmaf(w, v[j].x, a.x);
+      a.y = fmaf(w, v[j].y, a.y);
+      a.z = fmaf(w, v[j].z, a.z);
+      a.w = fmaf(w, v[j].w, a.w);
+    }
   }
-  if (tid == 0) p.arrivals[unit] = 0;  // ready for the next call
+  const float il = il_s;
+  reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(b) * p.Hq + h) * kDc)[c4] =
+      make_float4(a.x * il, a.y * il, a.z * il, a.w * il);
 }
 
 int sm_count() {
@@ -457,9 +467,10 @@ int pick_splits(int batch, int n_q_heads) {
 size_t round16(size_t n) { return (n + 15) / 16 * 16; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// workspace: arrival counters [units], then part_ml [units, NS, 16, 2], then
-// part_acc [units, NS, 16, kDc], each region starting on 16 bytes
-size_t ws_counter_bytes(int64_t units) { return round16(static_cast<size_t>(units) * 4); }
+// workspace: part_ml [units, NS, 16, 2], then part_acc [units, NS, 16, kDc],
+// each region starting on 16 bytes; every call writes the (m, l) of every
+// slice and the accumulator of every slice with pages before the merge reads
+// them, so nothing carries over from one call to the next
 size_t ws_ml_bytes(int64_t units, int ns) { return round16(static_cast<size_t>(units) * ns * kHT * 2 * 4); }
 
 }  // namespace
@@ -471,7 +482,7 @@ extern "C" size_t kvp_decode_attn_mla_workspace_bytes(int batch, int n_q_heads, 
   if (batch <= 0 || n_q_heads <= 0 || n_splits < 0 || n_splits > kMaxSplits) return 0;
   const int ns = n_splits > 0 ? n_splits : pick_splits(batch, n_q_heads);
   const int64_t units = static_cast<int64_t>(batch) * n_tiles(n_q_heads);
-  return ws_counter_bytes(units) + ws_ml_bytes(units, ns) + static_cast<size_t>(units) * ns * kHT * kDc * 4;
+  return ws_ml_bytes(units, ns) + static_cast<size_t>(units) * ns * kHT * kDc * 4;
 }
 
 extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_dim, int rope_dim, const void* q,
@@ -493,7 +504,7 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
   const int HT = n_tiles(n_q_heads);
   const int64_t units = static_cast<int64_t>(batch) * HT;
   const int64_t grid = units * ns;
-  if (grid > 0x7fffffff || units > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
+  if (grid > 0x7fffffff || units * kHT > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < kvp_decode_attn_mla_workspace_bytes(batch, n_q_heads, ns))
     return KVP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return KVP_ERR_ALIGN;
@@ -510,8 +521,6 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
                                                    kSmemBytes) == cudaSuccess;
   if (!attr_ok) return KVP_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // the counters are zero on entry: zero-filled by the caller before the
-  // workspace's first use, and reset by every merge of the previous call
   MlaParams p{static_cast<const uint16_t*>(q),
               expire_pool,
               page_table,
@@ -525,12 +534,14 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
               now,
               (scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(kRow))) * 1.4426950408889634f,
               out,
-              reinterpret_cast<float*>(ws + ws_counter_bytes(units) + ws_ml_bytes(units, ns)),
-              reinterpret_cast<float*>(ws + ws_counter_bytes(units)),
-              reinterpret_cast<int32_t*>(ws),
+              reinterpret_cast<float*>(ws + ws_ml_bytes(units, ns)),
+              reinterpret_cast<float*>(ws),
               status};
   if (launch_pdl(mla_decode_kernel, dim3(static_cast<unsigned>(grid)), dim3(kMThreads), kSmemBytes,
                  static_cast<cudaStream_t>(stream), p, tmL) != cudaSuccess)
+    return KVP_ERR_CUDA;
+  if (ns > 1 && launch_pdl(mla_merge_kernel, dim3(static_cast<unsigned>(units * kHT)), dim3(kDc / 4), 0,
+                           static_cast<cudaStream_t>(stream), p) != cudaSuccess)
     return KVP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }

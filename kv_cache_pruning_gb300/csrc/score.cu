@@ -19,6 +19,11 @@
 //                       upper half's partial scores are added to the lower
 //                       half's through shared memory -> per-chunk partials
 // A small reduction kernel then sums the MLP chunk partials in a fixed order.
+//
+// A decode step scores only the batch's new tokens (a few rows): one 128-row
+// tile would leave the whole weight to a single CTA. Up to kGemvMaxRows rows
+// the Linear scorer is instead a CUDA-core dot product over the same bf16
+// hi/lo weight rows, spread over one CTA per (head, group of 8 rows).
 #include "kvp_common.cuh"
 
 namespace kvp {
@@ -28,6 +33,9 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kMlpBN = 256;
 constexpr int kMlpMaxH = 16;
+constexpr int kGemvMaxRows = 64;  // Linear scorer: rows up to which the CUDA-core kernel runs
+constexpr int kGemvRows = 8;      // rows per CTA of that kernel
+constexpr int kGemvThreads = 256;
 
 enum { kEpiLinear = 0, kEpiMlp = 1 };
 // TMA warp, MMA warp, then 4 epilogue warps (LINEAR) or 8 (MLP: its GELU and
@@ -327,6 +335,69 @@ __global__ void split_weight_kernel(const float* __restrict__ w, int H, int D, i
   }
 }
 
+// Linear scores of a few rows: CTA (h, g) computes scores[t, h] for the rows t
+// of group g, sum_k x[t, k] * (hi[k] + lo[k]) with the two bf16 halves of
+// weight row h (rows 2h and 2h + 1 of the split operand): each thread takes
+// 8-value chunks k = 8c .. 8c + 7 (16-byte loads) in a strided loop, both
+// products accumulated in fp32, then the CTA's partial sums are added
+// through shared memory in a fixed order.
+__global__ void __launch_bounds__(kGemvThreads) score_gemv_kernel(const uint16_t* __restrict__ x, int64_t ld_x,
+                                                                  int n_tok, int D, const uint16_t* __restrict__ wt,
+                                                                  int H, const float* __restrict__ bias,
+                                                                  float* __restrict__ out) {
+  __shared__ float red[kGemvThreads / 32][kGemvRows];
+  const int h = blockIdx.x;
+  const int r0 = blockIdx.y * kGemvRows;
+  const int nr = min(kGemvRows, n_tok - r0);
+  const uint4* hi = reinterpret_cast<const uint4*>(wt + static_cast<int64_t>(2 * h) * D);
+  const uint4* lo = reinterpret_cast<const uint4*>(wt + static_cast<int64_t>(2 * h + 1) * D);
+  float acc[kGemvRows];
+#pragma unroll
+  for (int r = 0; r < kGemvRows; ++r) acc[r] = 0.f;
+  for (int c = threadIdx.x; c < D / 8; c += kGemvThreads) {
+    float wh[8], wl[8];
+    const uint4 a = __ldg(hi + c), b = __ldg(lo + c);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      wh[2 * i] = __uint_as_float(aw[i] << 16);
+      wh[2 * i + 1] = __uint_as_float(aw[i] & 0xFFFF0000u);
+      wl[2 * i] = __uint_as_float(bw[i] << 16);
+      wl[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int r = 0; r < kGemvRows; ++r) {
+      if (r < nr) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(r0 + r) * ld_x) + c);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float x0 = __uint_as_float(xw[i] << 16), x1 = __uint_as_float(xw[i] & 0xFFFF0000u);
+          acc[r] = fmaf(x0, wh[2 * i], acc[r]);
+          acc[r] = fmaf(x0, wl[2 * i], acc[r]);
+          acc[r] = fmaf(x1, wh[2 * i + 1], acc[r]);
+          acc[r] = fmaf(x1, wl[2 * i + 1], acc[r]);
+        }
+      }
+    }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < kGemvRows; ++r) {
+    float v = acc[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[warp][r] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < nr) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGemvThreads / 32; ++w) v += red[w][threadIdx.x];
+    out[static_cast<int64_t>(r0 + threadIdx.x) * H + h] = v + (bias ? __ldg(bias + h) : 0.f);
+  }
+}
+
 // scores[t, h] = sum_c part[c, t, h] + b2[h], chunks summed in order.
 __global__ void mlp_reduce_kernel(const float* __restrict__ part, int n_chunks, int64_t n, int H,
                                   const float* __restrict__ b2, float* __restrict__ scores) {
@@ -456,6 +527,13 @@ extern "C" kvp_status kvp_score(int scorer, int64_t n_tok, int d_model, int n_kv
                                                   workspace_bytes, stream);
       if (s != KVP_OK) return s;
       wt = workspace;
+    }
+    if (n_tok <= kGemvMaxRows) {  // a decode step's few new tokens
+      const dim3 grid(n_kv_heads, static_cast<unsigned>((n_tok + kGemvRows - 1) / kGemvRows));
+      score_gemv_kernel<<<grid, kGemvThreads, 0, st>>>(static_cast<const uint16_t*>(x), ld_x, static_cast<int>(n_tok),
+                                                       d_model, static_cast<const uint16_t*>(wt), n_kv_heads, b,
+                                                       scores);
+      return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
     }
     if (!make_tmap(&tb, wt, bn, d_model, d_model, bn)) return KVP_ERR_CUDA;
     p.n_tiles = 1;

@@ -222,17 +222,16 @@ def test_decode_attn_mla_split_independent(kvp):
 
 
 def test_decode_attn_mla_workspace_reused(kvp):
-    """One zero-filled workspace serves consecutive calls: each result equals a
-    fresh workspace's, and the arrival counters are zero after every call."""
+    """One workspace serves consecutive calls on different caches without any
+    clearing (it starts full of garbage here): each result equals a fresh
+    workspace's."""
     B, T, Hq, ns = 2, 1800, 32, 5
-    ws = torch.zeros(kvp.kvp_decode_attn_mla_workspace_bytes(B, Hq, ns), dtype=torch.uint8, device="cuda")
+    ws = torch.full((kvp.kvp_decode_attn_mla_workspace_bytes(B, Hq, ns),), 0x7F, dtype=torch.uint8, device="cuda")
     for seed in (41, 42, 43):
         o, _, c, q, now = _mla_case(kvp, B, T, Hq, n_splits=ns, seed=seed, workspace=ws)
         fresh = kvp.kvp_decode_attn_mla(dev_bf16(q), c, now, n_splits=ns)
         torch.cuda.synchronize()
         np.testing.assert_array_equal(o, fresh.cpu().numpy())
-        units = B * ((Hq + 15) // 16)
-        assert int(ws[: units * 4].view(torch.int32).abs().sum()) == 0
 
 
 def test_decode_attn_mla_empty_batch_element(kvp):

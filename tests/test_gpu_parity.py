@@ -30,6 +30,12 @@ def _linear_scale(x_bits, w):
     (300, 512, 64, False),    # 64 heads (widest weight tile), ragged
     (129, 1032, 5, True),     # d_model not a multiple of 64, odd head count
     (1, 64, 1, False),        # single token, single head
+    # decode-step sizes: up to 64 rows go to the CUDA-core dot products
+    (1, 8192, 64, True),      # one new token of the 65B-shaped MHA layer
+    (16, 4096, 8, True),      # the Llama-3-8B layer's batch of new tokens
+    (61, 1032, 5, False),     # ragged last group of 8 rows, d_model not a multiple of 64
+    (64, 4096, 8, False),     # the largest count on that path
+    (65, 4096, 8, True),      # the smallest on the tensor-core path
 ])
 def test_score_linear(kvp, n_tok, D, H, bias):
     x, w = syn.linear_inputs(0, n_tok, D, H)
@@ -49,6 +55,23 @@ def test_score_linear_strided_rows(kvp):
     s = kvp.kvp_score(xs, dev_f32(w[:, :D].copy()))
     torch.cuda.synchronize()
     check_scores(s.cpu().numpy(), orc.score_linear(x[:, :D], w[:, :D]), _linear_scale(x[:, :D], w[:, :D]))
+
+
+@pytest.mark.parametrize("n_tok", [1, 9, 64])
+def test_score_linear_split_weight_few_rows(kvp, n_tok):
+    """The few-row path on the pre-split weight gives the LINEAR call's scores
+    bit for bit, and both are within the oracle tolerance."""
+    D, H = 8192, 64
+    x, w = syn.linear_inputs(9, n_tok, D, H)
+    b = syn.normal_f32(9, 30, (H,))
+    wd = dev_f32(w)
+    xd = dev_bf16(x)
+    s_lin = kvp.kvp_score(xd, wd, dev_f32(b))
+    s_split = kvp.kvp_score(xd, kvp.kvp_score_split_weight(wd), dev_f32(b), scorer=kvp.KVP_SCORER_LINEAR_SPLIT,
+                            n_kv_heads=H)
+    torch.cuda.synchronize()
+    assert torch.equal(s_lin, s_split)
+    check_scores(s_split.cpu().numpy(), orc.score_linear(x, w, b), _linear_scale(x, w))
 
 
 def test_score_linear_split_weight(kvp):
@@ -685,6 +708,30 @@ def test_decode_attn_split_independent(kvp):
     outs = [_attn_case(kvp, 1, 2500, 2, 4, 128, pps=p)[0] for p in (1, 2, 5, 0)]
     for o in outs[1:]:
         np.testing.assert_allclose(o, outs[0], rtol=0, atol=1e-5)
+
+
+@pytest.mark.parametrize("d,grid", [(128, 4), (128, 5), (128, 6), (64, 5), (128, 0)])
+def test_decode_attn_one_head_per_kv_head_many_pieces(kvp, d, grid):
+    """One query head per kv head (MHA), one long head among short ones: with
+    a capped grid the long head's pages span about 32 to 48 slices, the range
+    where the merge at a slice end can stage every piece in the warp's idle
+    ring; every piece must count (a per-head relative check catches one that
+    is dropped)."""
+    B, T, H, G = 1, 12000, 3, 1
+    k, v = syn.kv_inputs(31, B, T, H, d)
+    s = syn.normal_f32(31, 21, (B, T, H))
+    tau = np.array([[-np.inf, 2.5, 1.5]], np.float32)   # head 0 keeps everything, the others few entries
+    exp = orc.mask_kvzap(s, tau, T - 1)[0].astype(np.int32)
+    q = syn.q_inputs(31, B, H * G, d)
+    mp = (T + 15) // 16
+    ref_c = orc.compact_dense(k, v, exp, T - 1, 0, B * H * mp, mp)
+    c = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp)
+    st = status_word()
+    kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp), T - 1, 0, c, status=st)
+    o = kvp.kvp_decode_attn(dev_bf16(q), c, T - 1, grid_limit=grid, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    check_attention(o.cpu().numpy(), orc.decode_attention(q, ref_c, T - 1))
 
 
 def test_decode_attn_workspace_reused_across_calls(kvp):
