@@ -118,3 +118,46 @@ def test_graph_replayed_decode_step_matches_oracle(kvp):
         check_attention(out.cpu().numpy(), orc.decode_attention(qs[i], ref, t))
     assert int(pos.item()) == T0 + steps
     compare_paged(pools[cur], ref, what="after the replays")
+
+
+def test_devpos_entry_points_read_the_position_and_reject_bad_ones(kvp):
+    """The device-position forms equal the host-position forms for the same
+    position; a negative position, or one whose expire value would reach
+    KVP_EXPIRE_NEVER, records KVP_ERR_INVALID and leaves the cache as it is."""
+    B, T, H, G, d = 2, 300, 2, 4, 128
+    k, v = syn.kv_inputs(8, B, T, H, d)
+    s = syn.normal_f32(8, 21, (B, T, H))
+    tau = orc.threshold_at_quantile(s, 0.6)
+    exp = orc.mask_kvzap(s, tau, T - 1)[0].astype(np.int32)
+    mp = (T + 8 + 15) // 16
+    kn, vn = dev_bf16(syn.normal_bf16(8, 30, (B, H, d))), dev_bf16(syn.normal_bf16(8, 31, (B, H, d)))
+    sn = dev_f32(syn.normal_f32(8, 32, (B, H)))
+    q = dev_bf16(syn.q_inputs(8, B, H * G, d))
+    caches = []
+    for _ in range(2):
+        c = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp)
+        st = status_word()
+        kvp.kvp_compact(dev_bf16(k), dev_bf16(v), torch.from_numpy(exp).cuda(), T - 1, 8, c, status=st)
+        caches.append(c)
+    st = status_word()
+    kvp.kvp_append(caches[0], kn, vn, T, mode=kvp.KVP_MASK_KVZAP, score=sn, tau=dev_f32(tau), status=st)
+    o_host = kvp.kvp_decode_attn(q, caches[0], T, status=st)
+    pos = torch.full((1,), T, dtype=torch.int32, device="cuda")
+    kvp.kvp_append_devpos(caches[1], kn, vn, pos, mode=kvp.KVP_MASK_KVZAP, score=sn, tau=dev_f32(tau), status=st)
+    o_dev = kvp.kvp_decode_attn_devpos(q, caches[1], pos, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(o_host, o_dev)
+    for name in ("k_pool", "v_pool", "expire_pool", "page_table", "remap", "count"):
+        assert torch.equal(getattr(caches[0], name), getattr(caches[1], name)), name
+    before = [getattr(caches[1], n).clone() for n in ("k_pool", "expire_pool", "remap", "count")]
+    for bad, delay in ((-1, 0), (2**31 - 1 - 128, 0), (2**31 - 300, 256)):
+        st = status_word()
+        pos.fill_(bad)
+        kvp.kvp_append_devpos(caches[1], kn, vn, pos, mode=kvp.KVP_MASK_DMS,
+                              flag_step=torch.zeros(B, H, dtype=torch.int32, device="cuda"), delay=delay, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == kvp.KVP_ERR_INVALID, (bad, st.item())
+    after = [getattr(caches[1], n) for n in ("k_pool", "expire_pool", "remap", "count")]
+    for a, b in zip(before, after):
+        assert torch.equal(a, b)
