@@ -1,7 +1,7 @@
 """Measurement runs of the other synthetic workloads (bench.py --workload NAME).
 
-The default bench line is the Llama-3-8B-shaped layer; these runs measure the
-rest of the path on the shapes it is quoted for:
+The default bench line is the 8-layer Llama-65B-shaped MHA decode step; these
+runs measure the rest of the path on the shapes it is quoted for:
 
   mlp_prefill    KVzap-MLP scoring of 4 x 32,768 prompt tokens (d_model 4096 ->
                  1024 GELU -> 8 heads; tensor-bound), 80% pruned, compaction into
@@ -17,6 +17,8 @@ rest of the path on the shapes it is quoted for:
   prune_sweep    decode attention on the Llama-3-8B-shaped cache at pruning
                  levels 0 / 50 / 75 / 87.5 / 93.75 / 96.9 %: tokens/s against the
                  inverse of the kept fraction
+  prune_sweep_long  the same sweep on one layer of the 65B-shaped MHA stack
+                 (64 heads, 131,072 cached tokens, batch 1)
 
 Decode loops are captured once in a CUDA graph (the C-ABI calls only enqueue
 work on the current stream) and replayed for timing, so host launch overhead
@@ -384,6 +386,56 @@ def prune_sweep(kvp, dev, peaks, seed=0, calls=10, reps=5):
             "points": points}
 
 
+def prune_sweep_long(kvp, dev, peaks, seed=0, calls=5, reps=3):
+    """Decode attention over one layer of the 65B-shaped MHA stack (batch 1,
+    131,072 cached tokens, 64 heads, head_dim 128: 4.3 GB of dense K/V) at
+    pruning levels from 0 to 96.9 %, the threshold at each head's q-quantile
+    score, 128-token window: with gigabytes of survivors the call's fixed
+    cost is small, so decode tokens/s follow the inverse of the kept
+    fraction much further than on the 16 x 8,192-token cache."""
+    B, T, H, d, W = 1, 131072, 64, 128, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    K = _randn_bf16((B, T, H, d), g, dev)
+    V = _randn_bf16((B, T, H, d), g, dev)
+    q = _randn_bf16((B, H, d), g, dev)
+    s = torch.randn((B, T, H), generator=g, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    mp = (T + 15) // 16
+    cache = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp, device=dev)
+    out = torch.empty(B, H, d, dtype=torch.float32, device=dev)
+    ws_a = torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, H, H, d), dtype=torch.uint8, device=dev)
+    ws_c = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
+    points = []
+    for prune_q in (0.0, 0.5, 0.75, 0.875, 0.9375, 0.96875):
+        tau = torch.full((B, H), -math.inf, device=dev) if prune_q == 0.0 else _tau_quantile(kvp, s, prune_q)
+        kvp.kvp_compact_masked(K, V, T - 1, 0, cache, mode=kvp.KVP_MASK_KVZAP, scores=s.view(B * T, H), tau=tau,
+                               window=W, status=st, workspace=ws_c)
+        torch.cuda.synchronize()
+        assert st.item() == 0, kvp.status_string(st.item())
+        kept = int(cache.count.sum().item())
+        pages = int(((cache.count + 15) // 16).sum().item())
+
+        def calls_fn():
+            for _ in range(calls):
+                kvp.kvp_decode_attn(q, cache, T - 1, out=out, workspace=ws_a, status=st)
+
+        ms = _time(_graph(calls_fn), reps=reps) / calls
+        nbytes = pages * 16 * (2 * d * 2 + 4) + B * H * d * (2 + 4)
+        points.append({"prune_q": prune_q, "kept_fraction": kept / (B * H * T), "surviving_pages": pages,
+                       "decode_attn_us": ms * 1e3, "decode_tokens_per_s": B / (ms * 1e-3),
+                       "GB_s": nbytes / (ms * 1e-3) / 1e9, "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks[0]})
+    assert st.item() == 0, kvp.status_string(st.item())
+    base = points[0]
+    for p in points:
+        p["speedup_vs_keep_all"] = p["decode_tokens_per_s"] / base["decode_tokens_per_s"]
+        p["inverse_kept_ratio"] = base["kept_fraction"] / p["kept_fraction"]
+    return {"workload": "prune_sweep_long: decode attention, one 65B-shaped MHA layer, batch 1, 131072 cached "
+                        "tokens, 64 heads, head_dim 128, threshold at each head's q-quantile score, 128-token window; "
+                        "each point = a CUDA graph of 5 calls",
+            "points": points}
+
+
 def threshold(kvp, dev, peaks, seed=0, calls=10, reps=5):
     """Per-(b, h) threshold selection on the device (kvp_threshold, four radix
     passes) at the score shapes of three layers: the tiny case, the Llama-3-8B
@@ -730,7 +782,7 @@ def mla_dms_decode(kvp, dev, peaks, seed=0, steps=256):
 
 
 RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha,
-           "prune_sweep": prune_sweep, "threshold": threshold,
+           "prune_sweep": prune_sweep, "prune_sweep_long": prune_sweep_long, "threshold": threshold,
            "quant_tier": quant_tier, "quant_decode": quant_decode, "gqa_sweep": gqa_sweep, "mla_sweep": mla_sweep,
            "mla_dms_decode": mla_dms_decode}
 

@@ -123,15 +123,18 @@ KVP_API kvp_status kvp_selftest_wait(uint64_t limit_ns, int32_t* status, uint32_
  * b2         MLP: device fp32 [H] or NULL;  LINEAR: must be NULL
  * scores     device fp32 [n_tok, H] (output, token-major)
  * workspace  device, >= kvp_score_workspace_bytes(...) bytes, 256-byte aligned
- *            (LINEAR_SPLIT needs none: NULL and 0 are accepted)
+ *            (LINEAR_SPLIT needs none: NULL and 0 are accepted; MLP holds
+ *            fp32 partial scores per chunk of the hidden layer: hidden / 256
+ *            chunks, or hidden / 8 up to 64 rows)
  *
  * The dense contraction runs on the tcgen05 tensor cores: LINEAR splits the
  * fp32 weight into two bf16 halves (hi + lo) so that the products keep ~16
  * mantissa bits of w; accumulation is fp32 throughout. Up to 64 rows (the
- * new tokens of a decode step) LINEAR and LINEAR_SPLIT run the same
- * products on the CUDA cores instead, spread over one CTA per head and
- * group of 8 rows (a single 128-row tensor-core tile would leave the whole
- * weight to one CTA). LINEAR does that split
+ * new tokens of a decode step) the scorers run the same products on the CUDA
+ * cores instead (a single 128-row tensor-core tile would leave the whole
+ * weight to one CTA): LINEAR and LINEAR_SPLIT over one CTA per head and group
+ * of 8 rows, MLP over one CTA per 8 hidden units and group of 8 rows, its
+ * partial scores summed in a fixed order. LINEAR does that split
  * on every call (one small kernel); a caller whose weight does not change
  * between calls (a decode loop: the weight is the layer's) splits it once with
  * kvp_score_split_weight and passes LINEAR_SPLIT; the scores are identical.

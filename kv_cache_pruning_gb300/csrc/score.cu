@@ -23,7 +23,11 @@
 // A decode step scores only the batch's new tokens (a few rows): one 128-row
 // tile would leave the whole weight to a single CTA. Up to kGemvMaxRows rows
 // the Linear scorer is instead a CUDA-core dot product over the same bf16
-// hi/lo weight rows, spread over one CTA per (head, group of 8 rows).
+// hi/lo weight rows, spread over one CTA per (head, group of 8 rows); the
+// MLP scorer likewise runs its few rows on the CUDA cores, one CTA per 8
+// hidden units and group of 8 rows. Both request kGemvBatch chunks of each
+// row per thread before the first product, so a thread keeps that many
+// weight and input loads in flight.
 #include "kvp_common.cuh"
 
 namespace kvp {
@@ -36,6 +40,8 @@ constexpr int kMlpMaxH = 16;
 constexpr int kGemvMaxRows = 64;  // Linear scorer: rows up to which the CUDA-core kernel runs
 constexpr int kGemvRows = 8;      // rows per CTA of that kernel
 constexpr int kGemvThreads = 256;
+constexpr int kMlpGemvUnits = 8;   // MLP scorer, few rows: hidden units per CTA (one per warp)
+constexpr int kGemvBatch = 4;      // 16-byte chunks of a row each thread requests before using any
 
 enum { kEpiLinear = 0, kEpiMlp = 1 };
 // TMA warp, MMA warp, then 4 epilogue warps (LINEAR) or 8 (MLP: its GELU and
@@ -354,29 +360,37 @@ __global__ void __launch_bounds__(kGemvThreads) score_gemv_kernel(const uint16_t
   float acc[kGemvRows];
 #pragma unroll
   for (int r = 0; r < kGemvRows; ++r) acc[r] = 0.f;
-  for (int c = threadIdx.x; c < D / 8; c += kGemvThreads) {
-    float wh[8], wl[8];
-    const uint4 a = __ldg(hi + c), b = __ldg(lo + c);
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  const int nch = D / 8;
+  for (int c0 = threadIdx.x; c0 < nch; c0 += kGemvThreads * kGemvBatch) {
+    uint4 a[kGemvBatch], bq[kGemvBatch];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      wh[2 * i] = __uint_as_float(aw[i] << 16);
-      wh[2 * i + 1] = __uint_as_float(aw[i] & 0xFFFF0000u);
-      wl[2 * i] = __uint_as_float(bw[i] << 16);
-      wl[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
+    for (int u = 0; u < kGemvBatch; ++u) {
+      const int c = c0 + u * kGemvThreads;
+      a[u] = c < nch ? __ldg(hi + c) : make_uint4(0, 0, 0, 0);
+      bq[u] = c < nch ? __ldg(lo + c) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int r = 0; r < kGemvRows; ++r) {
       if (r < nr) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(r0 + r) * ld_x) + c);
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        uint4 xv[kGemvBatch];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float x0 = __uint_as_float(xw[i] << 16), x1 = __uint_as_float(xw[i] & 0xFFFF0000u);
-          acc[r] = fmaf(x0, wh[2 * i], acc[r]);
-          acc[r] = fmaf(x0, wl[2 * i], acc[r]);
-          acc[r] = fmaf(x1, wh[2 * i + 1], acc[r]);
-          acc[r] = fmaf(x1, wl[2 * i + 1], acc[r]);
+        for (int u = 0; u < kGemvBatch; ++u) {
+          const int c = c0 + u * kGemvThreads;
+          xv[u] = c < nch ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(r0 + r) * ld_x) + c)
+                          : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kGemvBatch; ++u) {
+          const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, bw[4] = {bq[u].x, bq[u].y, bq[u].z, bq[u].w};
+          const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float x0 = __uint_as_float(xw[i] << 16), x1 = __uint_as_float(xw[i] & 0xFFFF0000u);
+            acc[r] = fmaf(x0, __uint_as_float(aw[i] << 16), acc[r]);
+            acc[r] = fmaf(x0, __uint_as_float(bw[i] << 16), acc[r]);
+            acc[r] = fmaf(x1, __uint_as_float(aw[i] & 0xFFFF0000u), acc[r]);
+            acc[r] = fmaf(x1, __uint_as_float(bw[i] & 0xFFFF0000u), acc[r]);
+          }
         }
       }
     }
@@ -396,6 +410,110 @@ __global__ void __launch_bounds__(kGemvThreads) score_gemv_kernel(const uint16_t
     for (int w = 0; w < kGemvThreads / 32; ++w) v += red[w][threadIdx.x];
     out[static_cast<int64_t>(r0 + threadIdx.x) * H + h] = v + (bias ? __ldg(bias + h) : 0.f);
   }
+}
+
+// KVzap-MLP scores of a few rows. CTA (g, r) takes hidden units 8g .. 8g + 7
+// and rows 8r .. 8r + 7; warp w computes unit 8g + w: its lanes take 8-value
+// chunks of k in a strided loop (u[t, j] = sum_k x[t, k] w1[j, k] in fp32),
+// the warp sums them, and lane t applies the bias and the exact GELU. The
+// CTA then writes part[g, t, h] = sum over its 8 units, in order, of
+// z[t, j] * w2[h, j]; mlp_reduce_kernel adds the groups' partials in order.
+__global__ void __launch_bounds__(kGemvThreads) score_mlp_gemv_kernel(const uint16_t* __restrict__ x, int64_t ld_x,
+                                                                      int n_tok, int D, const uint16_t* __restrict__ w1,
+                                                                      const float* __restrict__ b1,
+                                                                      const uint16_t* __restrict__ w2, int hidden, int H,
+                                                                      float* __restrict__ part) {
+  __shared__ float zs[kMlpGemvUnits][kGemvRows];
+  const int g = blockIdx.x;
+  const int r0 = blockIdx.y * kGemvRows;
+  const int nr = min(kGemvRows, n_tok - r0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = g * kMlpGemvUnits + warp;
+  const uint4* wr = reinterpret_cast<const uint4*>(w1 + static_cast<int64_t>(j) * D);
+  float acc[kGemvRows];
+#pragma unroll
+  for (int r = 0; r < kGemvRows; ++r) acc[r] = 0.f;
+  const int nch = D / 8;
+  for (int c0 = lane; c0 < nch; c0 += 32 * kGemvBatch) {
+    uint4 a[kGemvBatch];
+#pragma unroll
+    for (int u = 0; u < kGemvBatch; ++u) {
+      const int c = c0 + 32 * u;
+      a[u] = c < nch ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int r = 0; r < kGemvRows; ++r) {
+      if (r < nr) {
+        uint4 xv[kGemvBatch];
+#pragma unroll
+        for (int u = 0; u < kGemvBatch; ++u) {
+          const int c = c0 + 32 * u;
+          xv[u] = c < nch ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(r0 + r) * ld_x) + c)
+                          : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kGemvBatch; ++u) {
+          const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+          const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[r] = fmaf(__uint_as_float(xw[i] << 16), __uint_as_float(aw[i] << 16), acc[r]);
+            acc[r] = fmaf(__uint_as_float(xw[i] & 0xFFFF0000u), __uint_as_float(aw[i] & 0xFFFF0000u), acc[r]);
+          }
+        }
+      }
+    }
+  }
+  float mine = 0.f;
+#pragma unroll
+  for (int r = 0; r < kGemvRows; ++r) {
+    float v = acc[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == r) mine = v;
+  }
+  if (lane < nr) {
+    const float u = mine + (b1 ? __ldg(b1 + j) : 0.f);
+    zs[warp][lane] = 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kGemvRows * H; idx += kGemvThreads) {
+    const int t = idx / H, h = idx - t * H;
+    if (t < nr) {
+      float pv = 0.f;
+#pragma unroll
+      for (int jl = 0; jl < kMlpGemvUnits; ++jl) {
+        const uint32_t wb = w2[static_cast<int64_t>(h) * hidden + g * kMlpGemvUnits + jl];
+        pv = fmaf(zs[jl][t], __uint_as_float(wb << 16), pv);
+      }
+      part[(static_cast<int64_t>(g) * n_tok + r0 + t) * H + h] = pv;
+    }
+  }
+}
+
+// The few-row MLP path's partials: hidden / 8 groups per score. One warp per
+// score: lane l loads groups l, l + 32, .. (all in flight), adds them in
+// that order, then the warp adds its lanes' sums with a fixed butterfly.
+__global__ void __launch_bounds__(256) mlp_reduce_warp_kernel(const float* __restrict__ part, int n_chunks, int64_t n,
+                                                              int H, const float* __restrict__ b2,
+                                                              float* __restrict__ scores) {
+  const int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (i >= n) return;  // uniform in the warp
+  constexpr int kPer = 8;
+  float v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int c = lane + 32 * u;
+    v[u] = c < n_chunks ? __ldg(part + c * n + i) : 0.f;
+  }
+  float s = 0.f;
+  for (int c0 = 32 * kPer; c0 < n_chunks; c0 += 32) s += (c0 + lane < n_chunks) ? __ldg(part + (c0 + lane) * n + i) : 0.f;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) s += v[u];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) scores[i] = s + (b2 ? b2[i % H] : 0.f);
 }
 
 // scores[t, h] = sum_c part[c, t, h] + b2[h], chunks summed in order.
@@ -484,7 +602,8 @@ extern "C" size_t kvp_score_workspace_bytes(int scorer, int64_t n_tok, int d_mod
   if (scorer == KVP_SCORER_LINEAR_SPLIT) return 0;
   if (scorer == KVP_SCORER_MLP) {
     if (hidden <= 0) return 0;
-    return static_cast<size_t>(hidden / kMlpBN) * n_tok * n_kv_heads * sizeof(float);
+    const int chunks = n_tok <= kGemvMaxRows ? hidden / kMlpGemvUnits : hidden / kMlpBN;
+    return static_cast<size_t>(chunks) * n_tok * n_kv_heads * sizeof(float);
   }
   return 0;
 }
@@ -551,8 +670,22 @@ extern "C" kvp_status kvp_score(int scorer, int64_t n_tok, int d_model, int n_kv
   if (w2 == nullptr) return KVP_ERR_INVALID;
   if (hidden <= 0 || hidden % kMlpBN != 0 || n_kv_heads > kMlpMaxH) return KVP_ERR_UNSUPPORTED;
   if (!aligned16(w)) return KVP_ERR_ALIGN;
-  if (!make_tmap(&tb, w, hidden, d_model, d_model, kMlpBN)) return KVP_ERR_CUDA;
   float* part = static_cast<float*>(workspace);
+  const int64_t n = n_tok * n_kv_heads;
+  const int blocks = static_cast<int>((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
+  if (n_tok <= kGemvMaxRows) {  // a decode step's few new tokens
+    const dim3 grid(hidden / kMlpGemvUnits, static_cast<unsigned>((n_tok + kGemvRows - 1) / kGemvRows));
+    score_mlp_gemv_kernel<<<grid, kGemvThreads, 0, st>>>(static_cast<const uint16_t*>(x), ld_x,
+                                                         static_cast<int>(n_tok), d_model,
+                                                         static_cast<const uint16_t*>(w), b,
+                                                         static_cast<const uint16_t*>(w2), hidden, n_kv_heads, part);
+    if (cudaGetLastError() != cudaSuccess) return KVP_ERR_CUDA;
+    const int64_t wblocks = (n * 32 + 255) / 256;
+    mlp_reduce_warp_kernel<<<static_cast<unsigned>(wblocks), 256, 0, st>>>(part, hidden / kMlpGemvUnits, n,
+                                                                           n_kv_heads, b2, scores);
+    return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+  }
+  if (!make_tmap(&tb, w, hidden, d_model, d_model, kMlpBN)) return KVP_ERR_CUDA;
   p.n_tiles = hidden / kMlpBN;
   p.hidden = hidden;
   p.bias = b;
@@ -560,8 +693,6 @@ extern "C" kvp_status kvp_score(int scorer, int64_t n_tok, int d_model, int n_kv
   p.out = part;
   kvp_status s = launch_score<kMlpBN, kEpiMlp>(ta, tb, p, st);
   if (s != KVP_OK) return s;
-  const int64_t n = n_tok * n_kv_heads;
-  const int blocks = static_cast<int>((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
   mlp_reduce_kernel<<<blocks, 256, 0, st>>>(part, p.n_tiles, n, n_kv_heads, b2, scores);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }

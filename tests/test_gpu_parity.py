@@ -124,6 +124,25 @@ def test_score_mlp(kvp, n_tok, D, hidden, H, bias):
     check_scores(s.cpu().numpy(), ref, scale)
 
 
+@pytest.mark.parametrize("n_tok,bias", [(1, True), (4, False), (13, True), (64, False), (65, True)])
+def test_score_mlp_decode_rows(kvp, n_tok, bias):
+    """A decode step's few rows at the MLP prefill config's width (d_model
+    4096 -> 1024 -> 8): up to 64 rows on the CUDA-core path, 65 on the tensor
+    cores; both within the score tolerance."""
+    D, hidden, H = 4096, 1024, 8
+    x, w1, w2 = syn.mlp_inputs(6, n_tok, D, hidden, H)
+    b1 = syn.normal_f32(6, 78, (hidden,), std=0.1) if bias else None
+    b2 = syn.normal_f32(6, 79, (H,)) if bias else None
+    st = status_word()
+    s = kvp.kvp_score(dev_bf16(x), dev_bf16(w1), dev_f32(b1) if bias else None, dev_bf16(w2),
+                      dev_f32(b2) if bias else None, scorer=kvp.KVP_SCORER_MLP, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    u = orc.widen_bf16(x) @ orc.widen_bf16(w1).T + (0 if b1 is None else b1[None, :])
+    z = orc.gelu(u)
+    check_scores(s.cpu().numpy(), orc.score_mlp(x, w1, w2, b1, b2), np.sqrt((z * z) @ (orc.widen_bf16(w2) ** 2).T))
+
+
 # --------------------------------------------------------------------------- mask
 
 @pytest.mark.parametrize("B,T,H,window", [(1, 512, 2, 128), (3, 1000, 5, 128), (2, 33, 3, 7), (1, 4096, 8, 0),
