@@ -411,6 +411,8 @@ void kvpo_decode_attention(const uint16_t* q, int64_t B, int64_t Hq, int64_t H, 
   parallel_for(B * H, [&](int64_t u) {
     const int64_t b = u / H, h = u % H;
     std::vector<double> Kf, Vf;
+    Kf.reserve(static_cast<size_t>(count[u]) * d);
+    Vf.reserve(static_cast<size_t>(count[u]) * d);
     for (int64_t j = 0; j < count[u]; ++j) {
       const int64_t row = page_table[u * max_pages + j / kPage] * kPage + j % kPage;
       if (!(now < expire_pool[row])) continue;
@@ -442,6 +444,8 @@ void kvpo_dense_attention(const uint16_t* q, int64_t B, int64_t Hq, const uint16
   parallel_for(B * Hq, [&](int64_t u) {
     const int64_t b = u / Hq, jq = u % Hq, h = jq / g;
     std::vector<double> Kf, Vf;
+    Kf.reserve(static_cast<size_t>(std::max<int64_t>(0, std::min(now + 1, T) - std::max<int64_t>(lo, 0))) * d);
+    Vf.reserve(Kf.capacity());
     for (int64_t t = std::max<int64_t>(lo, 0); t <= now && t < T; ++t) {
       for (int64_t e = 0; e < d; ++e) {
         Kf.push_back(widen(k[((b * T + t) * H + h) * d + e]));
@@ -556,6 +560,8 @@ void kvpo_decode_attention_two_tier(const uint16_t* q, int64_t B, int64_t Hq, in
   parallel_for(B * H, [&](int64_t u) {
     const int64_t b = u / H, h = u % H;
     std::vector<double> Kf, Vf;
+    Kf.reserve(static_cast<size_t>(count[u]) * d);
+    Vf.reserve(static_cast<size_t>(count[u]) * d);
     for (int64_t j = 0; j < count[u]; ++j) {
       const int64_t row = page_table[u * max_pages + j / kPage] * kPage + j % kPage;
       if (!(now < expire_pool[row])) continue;
@@ -598,6 +604,7 @@ void kvpo_decode_attention_mla(const uint16_t* q, int64_t B, int64_t Hq, int64_t
                                int64_t max_pages, const int64_t* count, int64_t now, double scale, float* out) {
   parallel_for(B, [&](int64_t b) {
     std::vector<double> C;
+    C.reserve(static_cast<size_t>(count[b]) * R);
     for (int64_t j = 0; j < count[b]; ++j) {
       const int64_t row = page_table[b * max_pages + j / kPage] * kPage + j % kPage;
       if (!(now < expire_pool[row])) continue;
