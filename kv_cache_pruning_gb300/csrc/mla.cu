@@ -70,12 +70,13 @@ struct MlaParams {
   const int32_t* expire_pool; // [n_pages_cap, 16]
   const int32_t* page_table;  // [B, max_pages]
   const int32_t* count;       // [B]
-  int B, Hq, HT, NS;          // batch, query heads, 16-head tiles, slices per unit
+  int B, Hq, HT, NS;          // batch, query heads, head tiles, slices per unit
+  int TH;                     // query heads per tile: 16 (mla_decode_kernel) or 64 (mla_tile_kernel)
   int max_pages, n_pages_cap, now;
   float qscale;               // scale * log2(e)
   float* out;                 // [B, Hq, kDc]
-  float* part_acc;            // [units, NS, 16, kDc]
-  float* part_ml;             // [units, NS, 16, 2]
+  float* part_acc;            // [units, NS, TH, kDc]
+  float* part_ml;             // [units, NS, TH, 2]
   int32_t* status;
 };
 
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
   }
 }
 
-// Merge of the slices of every unit: CTA (unit, hl) takes head h_base + hl,
+// Merge of the slices of every unit: CTA (unit, hl) takes head TH * tile + hl,
 // thread c the float4 c of its 512 output values. The slices' (m, l) give
 // the weights exp2(m - M) (an empty slice, l = 0, has none and its
 // accumulator is not read), then the accumulators are summed with all of a
@@ -391,23 +392,23 @@ __global__ void __launch_bounds__(kDc / 4) mla_merge_kernel(const MlaParams p) {
   __shared__ float il_s;
   pdl_launch_dependents();
   pdl_wait();  // every slice's partial state is written
-  const int unit = static_cast<int>(blockIdx.x / kHT), hl = static_cast<int>(blockIdx.x % kHT);
-  const int b = unit / p.HT, h = (unit % p.HT) * kHT + hl;
+  const int unit = static_cast<int>(blockIdx.x / p.TH), hl = static_cast<int>(blockIdx.x % p.TH);
+  const int b = unit / p.HT, h = (unit % p.HT) * p.TH + hl;
   if (h >= p.Hq) return;
   const int c4 = threadIdx.x;
-  const float* ml = p.part_ml + static_cast<int64_t>(unit) * p.NS * kHT * 2;
+  const float* ml = p.part_ml + static_cast<int64_t>(unit) * p.NS * p.TH * 2;
   if (c4 < 32) {
     float M = -INFINITY;
     for (int sl = c4; sl < p.NS; sl += 32) {
-      const float l = __ldcg(ml + (sl * kHT + hl) * 2 + 1);
-      if (l > 0.f) M = fmaxf(M, __ldcg(ml + (sl * kHT + hl) * 2));
+      const float l = __ldcg(ml + (sl * p.TH + hl) * 2 + 1);
+      if (l > 0.f) M = fmaxf(M, __ldcg(ml + (sl * p.TH + hl) * 2));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
     for (int sl = c4; sl < p.NS; sl += 32) {
-      const float l = __ldcg(ml + (sl * kHT + hl) * 2 + 1);
-      const float w = l > 0.f ? exp2f(__ldcg(ml + (sl * kHT + hl) * 2) - M) : 0.f;
+      const float l = __ldcg(ml + (sl * p.TH + hl) * 2 + 1);
+      const float w = l > 0.f ? exp2f(__ldcg(ml + (sl * p.TH + hl) * 2) - M) : 0.f;
       w_s[sl] = w;
       L += w * l;
     }
@@ -417,14 +418,14 @@ __global__ void __launch_bounds__(kDc / 4) mla_merge_kernel(const MlaParams p) {
   }
   __syncthreads();
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* acc = reinterpret_cast<const float4*>(p.part_acc + static_cast<int64_t>(unit) * p.NS * kHT * kDc);
+  const float4* acc = reinterpret_cast<const float4*>(p.part_acc + static_cast<int64_t>(unit) * p.NS * p.TH * kDc);
   constexpr int kBatch = 8;
   for (int s0 = 0; s0 < p.NS; s0 += kBatch) {
     float4 v[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int sl = s0 + j;
-      v[j] = (sl < p.NS && w_s[sl] != 0.f) ? __ldcg(acc + (static_cast<int64_t>(sl) * kHT + hl) * (kDc / 4) + c4)
+      v[j] = (sl < p.NS && w_s[sl] != 0.f) ? __ldcg(acc + (static_cast<int64_t>(sl) * p.TH + hl) * (kDc / 4) + c4)
                                            : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
@@ -441,6 +442,304 @@ __global__ void __launch_bounds__(kDc / 4) mla_merge_kernel(const MlaParams p) {
       make_float4(a.x * il, a.y * il, a.z * il, a.w * il);
 }
 
+
+// ---------------------------------------------------------------- 64-head tiles
+// From 33 query heads on: a CTA takes 64 query heads of one batch element and
+// one slice of its pages with eight warps, warp w owning query heads
+// 8w .. 8w + 7 of the tile outright. The slice's pages stream through a ring
+// of kTRing stages (the nine swizzled boxes and the 16 expire values of a
+// page per stage); each stage has a full barrier (the copies' bytes) and an
+// empty barrier (one arrival per warp with heads). Lane 0 of warp 0 fills the
+// ring: the first kTRing pages up front, then, after its warp's page k, page
+// k - 1 + kTRing into the stage of page k - 1, which the other warps have
+// usually left by then. Warps meet only at the ring; the page loop has no CTA
+// barrier. Per page, warp w computes
+//   S   = C Q^T     M = 16 tokens, N = its 8 heads, K = all 576 values
+//                   (the query rows from shared memory, ldmatrix), four
+//                   independent partial sums over the k-steps
+//   softmax         online, base 2, lazy rescaling, for heads 2t and 2t + 1
+//                   of the thread (as in the one-tier tensor-core attention)
+//   O^T += Cv^T P^T M = 16 of the 512 values at a time (32 m-tiles), N = 8
+//                   heads, K = the page's 16 tokens; P as bf16 hi + lo
+// One page load serves 64 heads. The SM's registers sit in four files of 16K,
+// one per scheduler: eight warps (two per file) may use up to 255 registers
+// each, and the 128 output accumulators of a thread need most of them; a
+// ninth, copy-only warp would put three warps on one file and cap every
+// thread at 168.
+constexpr int kTHeads = 64;                          // query heads per CTA
+constexpr int kTWarps = kTHeads / 8;                 // 8 heads each
+constexpr int kTThreads = kTWarps * 32;
+constexpr int kTRing = 6;                            // ring stages: up to 5 pages ahead of warp 0
+constexpr int kQRowBytes = kRow * 2 + 16;            // a query row in shared memory, padded (conflict-free ldmatrix)
+constexpr int kTRingOff = 0;
+constexpr int kTRecOff = kTRingOff + kTRing * kStageBytes;
+constexpr int kTQOff = kTRecOff + kTRing * kPage * 4;
+constexpr int kTPtOff = kTQOff + kTHeads * kQRowBytes;
+constexpr int kTBarOff = kTPtOff + kTWarps * 2 * 8 * kPage * 2;
+constexpr int kTSmemUsed = kTBarOff + 2 * kTRing * 8 + 16;
+constexpr int kTSmemBytes = 1024 + kTSmemUsed;
+static_assert(kTRecOff % 16 == 0 && kTQOff % 16 == 0 && kTPtOff % 16 == 0 && kTBarOff % 8 == 0, "alignment");
+static_assert(kTSmemBytes <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(kTThreads, 1) mla_tile_kernel(const MlaParams p,
+                                                                const __grid_constant__ CUtensorMap tmL) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  pdl_launch_dependents();
+  pdl_wait();  // counts and pages come from the kernels before this one
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ht = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.HT));
+  const int rest = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.HT));
+  const int s = rest % p.NS;
+  const int b = rest / p.NS;
+  const int unit = b * p.HT + ht;
+  const int h_base = ht * kTHeads;
+  const int n_act = min(kTWarps, (p.Hq - h_base + 7) / 8);  // warps with heads (at least warp 0)
+
+  uint8_t* ring = smem + kTRingOff;
+  int32_t* rec_s = reinterpret_cast<int32_t*>(smem + kTRecOff);
+  uint8_t* q_s = smem + kTQOff;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTBarOff);
+  uint64_t* empty = full + kTRing;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kTRing);
+
+  const int cnt = min(max(p.count[b], 0), p.max_pages * kPage);
+  const int np = (cnt + kPage - 1) / kPage;
+  const int pg0 = static_cast<int>(static_cast<int64_t>(s) * np / p.NS);
+  const int pg1 = static_cast<int>(static_cast<int64_t>(s + 1) * np / p.NS);
+  const int n_my = pg1 - pg0;
+
+  // ---- the tile's query rows into shared memory (zero past Hq)
+  for (int i = tid; i < kTHeads * (kRow / 8); i += kTThreads) {
+    const int hl = i / (kRow / 8), c = i - hl * (kRow / 8);
+    const int h = h_base + hl;
+    const uint4 v = h < p.Hq ? __ldg(reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(b) * p.Hq + h) * kRow) + c)
+                             : make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(q_s + hl * kQRowBytes + c * 16) = v;
+  }
+  if (tid == 0) {
+    prefetch_tmap(&tmL);
+    for (int st = 0; st < kTRing; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], n_act);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp >= n_act) return;
+
+  // page k of the slice into stage k % kTRing (lane 0 of warp 0 only; the stage is free)
+  const bool filler = tid == 0;
+  auto issue = [&](int k) {
+    const int st = k % kTRing;
+    uint8_t* dst = ring + st * kStageBytes;
+    int32_t* rec = rec_s + st * kPage;
+    const int phys = p.page_table[static_cast<int64_t>(b) * p.max_pages + pg0 + k];
+    if (phys < 0 || phys >= p.n_pages_cap) {
+      // inconsistent page table: no copy; the page reads as zeros and every slot of it as gone
+      record_error(p.status, KVP_ERR_BOUNDS);
+      uint4* z = reinterpret_cast<uint4*>(dst);
+      for (int i = 0; i < kStageBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < kPage; ++i) rec[i] = 0;
+      mbar_arrive(&full[st]);
+      return;
+    }
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&full[st], kStageBytes + kPage * 4);
+    const int y = phys * kPage;
+#pragma unroll
+    for (int j = 0; j < kBoxes; ++j) tma_load_2d(dst + j * kBoxBytes, &tmL, 64 * j, y, &full[st]);
+    bulk_g2s(rec, p.expire_pool + static_cast<int64_t>(phys) * kPage, kPage * 4, &full[st]);
+  };
+  int n_issued = 0;
+  if (filler) {
+    for (; n_issued < min(kTRing, n_my); ++n_issued) issue(n_issued);
+  }
+
+  const int gq = lane >> 2, tq = lane & 3;
+  const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: the lane's matrix and row within it
+  // query B fragments of two k-steps per ldmatrix.x4: matrix m = (k-step ks + m / 2, values 8 (m & 1) ..),
+  // row = head 8 warp + ri
+  const uint32_t qaddr = smem_u32(q_s) + (8 * warp + ri) * kQRowBytes + (mi >> 1) * 32 + (mi & 1) * 16;
+  uint16_t* pt_s = reinterpret_cast<uint16_t*>(smem + kTPtOff) + warp * 2 * 8 * kPage;
+  const uint32_t ring_u32 = smem_u32(ring);
+
+  float m2[2] = {-1e30f, -1e30f}, l2[2] = {0.f, 0.f};
+  float o[kDc / 16][4];
+#pragma unroll
+  for (int mt = 0; mt < kDc / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+  for (int k = 0; k < n_my; ++k) {
+    const int st = k % kTRing;
+    const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((k / kTRing) & 1), abort_flag, p.status);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) {
+        record_error(p.status, KVP_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      if (filler) {
+        // the copies already issued land before the CTA's shared memory is released (each wait bounded again)
+        for (int kk = k; kk < n_issued; ++kk) (void)mbar_wait(&full[kk % kTRing], (kk / kTRing) & 1u);
+      }
+      return;  // outputs of this call are unspecified after a timeout
+    }
+    const uint32_t base = ring_u32 + st * kStageBytes;
+
+    // ---- S = C Q^T: 16 tokens x this warp's 8 heads, four partial sums
+    float sacc[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) sacc[u][0] = sacc[u][1] = sacc[u][2] = sacc[u][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kRow / 16; ks += 2) {
+      uint32_t b00, b01, b10, b11;
+      ldsm_x4(qaddr + ks * 32, b00, b01, b10, b11);
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int kk = ks + h2;
+        // matrices: 0 rows 0-7 / 1 rows 8-15 of the k-step's first 8 values, 2 / 3 of its second 8
+        const int r = (mi & 1) * 8 + ri;
+        const int chunk = (kk & 3) * 2 + (mi >> 1);
+        const uint32_t addr = base + (kk >> 2) * kBoxBytes + r * 128 + ((chunk ^ (r & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(addr, a0, a1, a2, a3);
+        if (h2 == 0)
+          mma_bf16_16816(sacc[kk & 3], a0, a1, a2, a3, b00, b01);
+        else
+          mma_bf16_16816(sacc[kk & 3], a0, a1, a2, a3, b10, b11);
+      }
+    }
+    float sv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sv[i] = (sacc[0][i] + sacc[1][i]) + (sacc[2][i] + sacc[3][i]);
+
+    // ---- mask and online softmax (base 2, lazy rescaling) for tokens gq, gq + 8, heads 2tq, 2tq + 1
+    const int32_t* rec = rec_s + st * kPage;
+    const int slot0 = (pg0 + k) * kPage;
+    const bool v0 = (slot0 + gq < cnt) && (p.now < rec[gq]);
+    const bool v1 = (slot0 + gq + 8 < cnt) && (p.now < rec[gq + 8]);
+    float x[4];
+    x[0] = v0 ? sv[0] * p.qscale : -INFINITY;
+    x[1] = v0 ? sv[1] * p.qscale : -INFINITY;
+    x[2] = v1 ? sv[2] * p.qscale : -INFINITY;
+    x[3] = v1 ? sv[3] * p.qscale : -INFINITY;
+    const bool grow = x[0] > m2[0] + kLazyRescale || x[2] > m2[0] + kLazyRescale || x[1] > m2[1] + kLazyRescale ||
+                      x[3] > m2[1] + kLazyRescale;
+    if (__any_sync(0xffffffffu, grow)) {
+      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float n0 = fmaxf(m2[0], mx0), n1 = fmaxf(m2[1], mx1);
+      const float al0 = exp2f(m2[0] - n0), al1 = exp2f(m2[1] - n1);
+      m2[0] = n0;
+      m2[1] = n1;
+      l2[0] *= al0;
+      l2[1] *= al1;
+#pragma unroll
+      for (int mt = 0; mt < kDc / 16; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
+    // p as a bf16 pair hi + lo (the product keeps about 16 bits of p; the sum takes p itself);
+    // P^T through this warp's shared memory: pt_s[hi / lo][head][token]
+    float pf[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pf[i] = exp2f(x[i] - m2[i & 1]);
+    l2[0] += pf[0] + pf[2];
+    l2[1] += pf[1] + pf[3];
+    const int tok[4] = {gq, gq, gq + 8, gq + 8};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(pf[i]);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(pf[i] - __bfloat162float(hi));
+      pt_s[(2 * tq + (i & 1)) * kPage + tok[i]] = __bfloat16_as_ushort(hi);
+      pt_s[8 * kPage + (2 * tq + (i & 1)) * kPage + tok[i]] = __bfloat16_as_ushort(lo);
+    }
+    __syncwarp();
+    const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPage + 2 * tq);
+    const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPage + 8 + 2 * tq);
+    const uint32_t pl0 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPage + gq * kPage + 2 * tq);
+    const uint32_t pl1 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPage + gq * kPage + 8 + 2 * tq);
+
+    // ---- O^T += Cv^T P^T over all 512 compressed values
+#pragma unroll
+    for (int mt = 0; mt < kDc / 16; ++mt) {
+      // matrices: 0 tokens 0-7 / values +0, 1 tokens 0-7 / +8, 2 tokens 8-15 / +0, 3 tokens 8-15 / +8
+      const int r = (mi >> 1) * 8 + ri;
+      const int chunk = (mt & 3) * 2 + (mi & 1);
+      const uint32_t addr = base + (mt >> 2) * kBoxBytes + r * 128 + ((chunk ^ (r & 7)) << 4);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_trans(addr, a0, a1, a2, a3);
+      mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+      mma_bf16_16816(o[mt], a0, a1, a2, a3, pl0, pl1);
+    }
+    __syncwarp();  // every lane is done with the stage and with pt_s
+    if (lane == 0) mbar_arrive(&empty[st]);
+    if (filler && n_issued < n_my && k >= 1) {
+      // refill the stage of page k - 1 once every warp has left it
+      const int kr = k - 1;
+      if (mbar_wait(&empty[kr % kTRing], static_cast<uint32_t>((kr / kTRing) & 1), abort_flag, p.status)) {
+        issue(n_issued);
+        ++n_issued;
+      } else {
+        record_error(p.status, KVP_ERR_TIMEOUT);
+        *abort_flag = 1;  // every warp leaves at its next wait; this one drains its copies there
+      }
+    }
+  }
+
+  // ---- this slice's state: the sums over the tokens of all lanes
+  float lt[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    float v = l2[c];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    lt[c] = v;
+  }
+  const int hl0 = 8 * warp + 2 * tq;  // this thread's heads hl0, hl0 + 1 of the tile
+  if (p.NS == 1) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int h = h_base + hl0 + c;
+      if (h >= p.Hq) continue;
+      const float inv = lt[c] > 0.f ? 1.f / lt[c] : 0.f;
+      float* orow = p.out + (static_cast<int64_t>(b) * p.Hq + h) * kDc;
+#pragma unroll
+      for (int mt = 0; mt < kDc / 16; ++mt) {
+        orow[16 * mt + gq] = o[mt][c] * inv;
+        orow[16 * mt + gq + 8] = o[mt][2 + c] * inv;
+      }
+    }
+    return;
+  }
+  const int64_t slot = static_cast<int64_t>(unit) * p.NS + s;
+  if (n_my > 0) {  // an empty slice leaves its accumulator unwritten: its sum is 0 and the merge skips it
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float* pa = p.part_acc + (slot * kTHeads + hl0 + c) * kDc;
+#pragma unroll
+      for (int mt = 0; mt < kDc / 16; ++mt) {
+        pa[16 * mt + gq] = o[mt][c];
+        pa[16 * mt + gq + 8] = o[mt][2 + c];
+      }
+    }
+  }
+  if (gq == 0) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      p.part_ml[(slot * kTHeads + hl0 + c) * 2] = m2[c];
+      p.part_ml[(slot * kTHeads + hl0 + c) * 2 + 1] = lt[c];
+    }
+  }
+}
+
 int sm_count() {
   static const int n = [] {
     int dev = 0, nsm = 0;
@@ -452,26 +751,34 @@ int sm_count() {
   return n;
 }
 
-int n_tiles(int n_q_heads) { return (n_q_heads + kHT - 1) / kHT; }
+// Up to 32 query heads, CTAs of mla_decode_kernel take 16-head tiles (at 32
+// heads two tiles of 16 ran 87 us where one 64-head tile with half its warps
+// idle ran 90 us, batch 16 x 8192 tokens); above, mla_tile_kernel takes
+// tiles of 64.
+constexpr int kTileFrom = 33;
+int tile_heads(int n_q_heads) { return n_q_heads >= kTileFrom ? kTHeads : kHT; }
+int n_tiles(int n_q_heads) { return (n_q_heads + tile_heads(n_q_heads) - 1) / tile_heads(n_q_heads); }
 
-// Slices per unit: as many as one wave of CTAs holds (two per SM), so no
-// CTA waits for a second wave (128 units on 152 SMs: 2 slices, 256 CTAs,
-// rather than 3 slices and 384 CTAs in 1.26 waves); at least one.
+// Slices per unit: as many as one wave of CTAs holds (two per SM for the
+// 16-head kernel, one for the 64-head one), so no CTA waits for a second
+// wave (128 units on 152 SMs: 2 slices, 256 CTAs, rather than 3 slices and
+// 384 CTAs in 1.26 waves); at least one.
 int pick_splits(int batch, int n_q_heads) {
   const int nsm = sm_count();
   const int64_t units = static_cast<int64_t>(batch) * n_tiles(n_q_heads);
-  const int64_t want = 2 * static_cast<int64_t>(nsm > 0 ? nsm : 1) / units;
+  const int per_sm = n_q_heads >= kTileFrom ? 1 : 2;
+  const int64_t want = per_sm * static_cast<int64_t>(nsm > 0 ? nsm : 1) / units;
   return static_cast<int>(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
 }
 
 size_t round16(size_t n) { return (n + 15) / 16 * 16; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// workspace: part_ml [units, NS, 16, 2], then part_acc [units, NS, 16, kDc],
+// workspace: part_ml [units, NS, TH, 2], then part_acc [units, NS, TH, kDc],
 // each region starting on 16 bytes; every call writes the (m, l) of every
 // slice and the accumulator of every slice with pages before the merge reads
 // them, so nothing carries over from one call to the next
-size_t ws_ml_bytes(int64_t units, int ns) { return round16(static_cast<size_t>(units) * ns * kHT * 2 * 4); }
+size_t ws_ml_bytes(int64_t units, int ns, int th) { return round16(static_cast<size_t>(units) * ns * th * 2 * 4); }
 
 }  // namespace
 }  // namespace kvp
@@ -482,7 +789,8 @@ extern "C" size_t kvp_decode_attn_mla_workspace_bytes(int batch, int n_q_heads, 
   if (batch <= 0 || n_q_heads <= 0 || n_splits < 0 || n_splits > kMaxSplits) return 0;
   const int ns = n_splits > 0 ? n_splits : pick_splits(batch, n_q_heads);
   const int64_t units = static_cast<int64_t>(batch) * n_tiles(n_q_heads);
-  return ws_ml_bytes(units, ns) + static_cast<size_t>(units) * ns * kHT * kDc * 4;
+  const int th = tile_heads(n_q_heads);
+  return ws_ml_bytes(units, ns, th) + static_cast<size_t>(units) * ns * th * kDc * 4;
 }
 
 extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_dim, int rope_dim, const void* q,
@@ -502,9 +810,10 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
   if (!aligned16(q) || !aligned16(pool) || !aligned16(expire_pool) || !aligned16(out)) return KVP_ERR_ALIGN;
   const int ns = n_splits > 0 ? n_splits : pick_splits(batch, n_q_heads);
   const int HT = n_tiles(n_q_heads);
+  const int th = tile_heads(n_q_heads);
   const int64_t units = static_cast<int64_t>(batch) * HT;
   const int64_t grid = units * ns;
-  if (grid > 0x7fffffff || units * kHT > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
+  if (grid > 0x7fffffff || units * th > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < kvp_decode_attn_mla_workspace_bytes(batch, n_q_heads, ns))
     return KVP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return KVP_ERR_ALIGN;
@@ -517,8 +826,10 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
   CUtensorMap tmL;
   if (!make_tmap_bf16(&tmL, pool, static_cast<int64_t>(n_pages_cap) * kPage, kRow, kRow, kPage, 64))
     return KVP_ERR_CUDA;
-  static const bool attr_ok = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   kSmemBytes) == cudaSuccess;
+  static const bool attr_ok =
+      cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ==
+          cudaSuccess &&
+      cudaFuncSetAttribute(mla_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmemBytes) == cudaSuccess;
   if (!attr_ok) return KVP_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   MlaParams p{static_cast<const uint16_t*>(q),
@@ -529,18 +840,22 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
               n_q_heads,
               HT,
               ns,
+              th,
               max_pages,
               n_pages_cap,
               now,
               (scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(kRow))) * 1.4426950408889634f,
               out,
-              reinterpret_cast<float*>(ws + ws_ml_bytes(units, ns)),
+              reinterpret_cast<float*>(ws + ws_ml_bytes(units, ns, th)),
               reinterpret_cast<float*>(ws),
               status};
-  if (launch_pdl(mla_decode_kernel, dim3(static_cast<unsigned>(grid)), dim3(kMThreads), kSmemBytes,
-                 static_cast<cudaStream_t>(stream), p, tmL) != cudaSuccess)
-    return KVP_ERR_CUDA;
-  if (ns > 1 && launch_pdl(mla_merge_kernel, dim3(static_cast<unsigned>(units * kHT)), dim3(kDc / 4), 0,
+  const cudaError_t le =
+      th == kTHeads ? launch_pdl(mla_tile_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTThreads), kTSmemBytes,
+                                 static_cast<cudaStream_t>(stream), p, tmL)
+                    : launch_pdl(mla_decode_kernel, dim3(static_cast<unsigned>(grid)), dim3(kMThreads), kSmemBytes,
+                                 static_cast<cudaStream_t>(stream), p, tmL);
+  if (le != cudaSuccess) return KVP_ERR_CUDA;
+  if (ns > 1 && launch_pdl(mla_merge_kernel, dim3(static_cast<unsigned>(units * th)), dim3(kDc / 4), 0,
                            static_cast<cudaStream_t>(stream), p) != cudaSuccess)
     return KVP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;

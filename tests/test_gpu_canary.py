@@ -156,10 +156,11 @@ def test_canaries_mla(kvp):
     for i in range(4):
         kvp.kvp_append_latent(c, ln[:, i].contiguous(), T + i, mode=kvp.KVP_MASK_KVZAP,
                               score=dev_f32(np.zeros(B, np.float32)), tau=dev_f32(tau), status=st)
-    for ns in (1, 3):
-        out = g((B, Hq, kvp.KVP_MLA_LATENT_DIM), torch.float32)
-        kvp.kvp_decode_attn_mla(dev_bf16(q), c, T + 3, out=out, n_splits=ns,
-                                workspace=ws(kvp.kvp_decode_attn_mla_workspace_bytes(B, Hq, ns), zero=True),
+    for hq, ns in ((Hq, 1), (Hq, 3), (40, 1), (40, 3)):   # 16-head tiles, then 64-head tiles
+        qh = q if hq == Hq else syn.q_inputs(7, B, hq, row)
+        out = g((B, hq, kvp.KVP_MLA_LATENT_DIM), torch.float32)
+        kvp.kvp_decode_attn_mla(dev_bf16(qh), c, T + 3, out=out, n_splits=ns,
+                                workspace=ws(kvp.kvp_decode_attn_mla_workspace_bytes(B, hq, ns), zero=True),
                                 status=st)
     c2 = latent()
     kvp.kvp_compact_latent_paged(c, T + 3, reserve, c2, status=st,

@@ -183,6 +183,8 @@ def _mla_case(kvp, B, T, Hq, n_splits=0, seed=37, tau_std=0.7, peaked=False, q_z
     (2, 700, 1, 1),        # one head, one slice: the output is written without a merge
     (4, 300, 16, 64),      # more slices than pages: empty slices are skipped by the merge
     (2, 4100, 32, 0),
+    (1, 2000, 40, 3),      # 64-head tiles from 33 heads: five of the eight warps have heads
+    (2, 1100, 72, 0),      # a second 64-head tile with one warp of heads
 ])
 def test_decode_attn_mla(kvp, B, T, Hq, n_splits):
     o, ref, *_ = _mla_case(kvp, B, T, Hq, n_splits)
@@ -221,11 +223,12 @@ def test_decode_attn_mla_split_independent(kvp):
         np.testing.assert_allclose(o, outs[0], rtol=0, atol=1e-5)
 
 
-def test_decode_attn_mla_workspace_reused(kvp):
+@pytest.mark.parametrize("Hq", [32, 72])
+def test_decode_attn_mla_workspace_reused(kvp, Hq):
     """One workspace serves consecutive calls on different caches without any
     clearing (it starts full of garbage here): each result equals a fresh
     workspace's."""
-    B, T, Hq, ns = 2, 1800, 32, 5
+    B, T, ns = 2, 1800, 5
     ws = torch.full((kvp.kvp_decode_attn_mla_workspace_bytes(B, Hq, ns),), 0x7F, dtype=torch.uint8, device="cuda")
     for seed in (41, 42, 43):
         o, _, c, q, now = _mla_case(kvp, B, T, Hq, n_splits=ns, seed=seed, workspace=ws)
