@@ -594,13 +594,23 @@ KVP_API kvp_status kvp_append_latent(int mode, int batch, int row_dim, int pos, 
  * value, to which the caller applies the head's value up-projection. An
  * empty set gives a zero row.
  *
- * Work is cut into units of 16 query heads of one batch element, and each
- * unit's pages into n_splits equal slices, one CTA each (a CTA of a later
- * unit of the same slice reads the same pages, mostly from L2). Both
- * products run on the tensor cores: bf16 operands, fp32 accumulation, the
- * softmax weights entering the weighted sum as a bf16 hi + lo pair; with
- * more than one slice, a second kernel launched by the same call merges the
- * slices in fp32, one CTA per (unit, head).
+ * Work is cut into units (a tile of query heads of one batch element), and
+ * each unit's pages into n_splits equal slices. Both products run on the
+ * tensor cores with bf16 operands and fp32 accumulation:
+ *   up to 32 query heads   tiles of 16 heads, one CTA per (unit, slice)
+ *                          (mma.sync); the softmax weights enter the
+ *                          weighted sum as a bf16 hi + lo pair
+ *   33 to 64 query heads   one tile of 64 heads, one CTA per (unit, slice)
+ *                          (mma.sync), weights as a hi + lo pair
+ *   from 65 query heads    tiles of 128 heads on tcgen05 (tensor memory):
+ *                          four CTAs per (unit, slice), one per quarter of
+ *                          the latent_dim output values; each weight is
+ *                          rounded to bf16 once (relative error <= 2^-9 per
+ *                          weight; the normaliser sums the unrounded
+ *                          weights, so an output value is off by at most
+ *                          about 2^-9 times the largest |row value|)
+ * With more than one slice, a second kernel launched by the same call merges
+ * the slices in fp32, one CTA per (unit, head).
  *
  * latent_dim, rope_dim  KVP_MLA_LATENT_DIM and KVP_MLA_ROPE_DIM (else
  *            KVP_ERR_UNSUPPORTED)
@@ -612,7 +622,8 @@ KVP_API kvp_status kvp_append_latent(int mode, int batch, int row_dim, int pos, 
  * scale      > 0, or 0 for 1/sqrt(latent_dim + rope_dim)
  * out        device fp32 [B, n_q_heads, latent_dim], 16-byte aligned
  * n_splits   slices per unit, 1..64; 0 picks one from the current device's
- *            SM count (as many as fill one wave of two CTAs per SM, at least 1)
+ *            SM count (as many as fill one wave of CTAs: two per SM for
+ *            16-head tiles, one for the others; at least 1)
  * workspace  device, >= kvp_decode_attn_mla_workspace_bytes(batch,
  *            n_q_heads, n_splits) (asked on the device that runs the call
  *            when n_splits = 0), 16-byte aligned; every call writes what it

@@ -59,7 +59,27 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  // a rejected launch (a configuration error, not a fault) is reported here and
+  // taken off the runtime's last-error slot, so that the next call does not see it
+  if (e != cudaSuccess) (void)cudaGetLastError();
+  return e;
+}
+
+// Named barrier `id` (1..15) over n threads (a multiple of 32).
+KVP_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// The same, returning the OR of v over the n threads (every one of them must reach it).
+KVP_DEV bool named_bar_or(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
 }
 
 KVP_DEV uint32_t smem_u32(const void* p) {
@@ -182,6 +202,17 @@ KVP_DEV void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]: the A operand read from tensor memory
+// (row m in lane m, two bf16 per 32-bit column, the lower k in the low half).
+KVP_DEV void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread completes.
 KVP_DEV void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -198,6 +229,9 @@ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// The same with the B operand MN-major (N contiguous in shared memory).
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
+
 // Shared-memory matrix descriptor for a K-major tile whose rows are 128 bytes
 // (64 bf16) stored with the 128-byte swizzle, 8-row groups 1024 bytes apart.
 // The tile base must be 1024-byte aligned. Advancing K by 16 elements inside
@@ -208,6 +242,18 @@ KVP_DEV uint64_t sw128_kmajor_desc(uint32_t saddr) {
          | (static_cast<uint64_t>(1024 >> 4) << 32)         // stride byte offset: 8 rows x 128 B
          | (static_cast<uint64_t>(1) << 46)                 // descriptor version
          | (static_cast<uint64_t>(2) << 61);                // 128-byte swizzle
+}
+
+// Shared-memory matrix descriptor for an MN-major operand with the 128-byte
+// swizzle: each 1024-byte atom holds 8 consecutive k (rows of 128 bytes) of
+// 64 consecutive m or n values; atoms along M/N lie mn_stride bytes apart,
+// atoms along K (the next 8 k) k_stride bytes apart. Atoms 1024-byte aligned.
+KVP_DEV uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t mn_stride, uint32_t k_stride) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)            // start address
+         | (static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16)  // leading byte offset
+         | (static_cast<uint64_t>((k_stride >> 4) & 0x3FFFu) << 32)   // stride byte offset
+         | (static_cast<uint64_t>(1) << 46)                           // descriptor version
+         | (static_cast<uint64_t>(2) << 61);                          // 128-byte swizzle
 }
 
 // Loads 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one row per
@@ -242,6 +288,48 @@ KVP_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Loads 24 consecutive fp32 columns (16 + 8) of this warp's 32 TMEM lanes and waits for them.
+KVP_DEV void tmem_ld24(uint32_t taddr, float (&v)[24]) {
+  uint32_t r[24];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%24];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%25];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23])
+      : "r"(taddr), "r"(taddr + 16)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 24; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Stores 12 consecutive 32-bit columns (8 + 4) of this warp's 32 TMEM lanes.
+KVP_DEV void tmem_st12(uint32_t taddr, const uint32_t (&r)[12]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%2,%3,%4,%5,%6,%7,%8,%9};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%1], {%10,%11,%12,%13};" ::"r"(taddr),
+      "r"(taddr + 8), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11])
+      : "memory");
+}
+
+// Stores 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (one row
+// per thread); tmem_st_wait() waits for the stores issued so far.
+KVP_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+KVP_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ---------------------------------------------------------------- warp-level tensor-core products
 // ldmatrix: four 8x8 b16 matrices from shared memory, the row addresses given
 // by lanes 8i..8i+7 for matrix i (.trans: each matrix transposed on the way).
@@ -274,6 +362,15 @@ KVP_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^x by the PTX instruction ex2.approx.ftz.f32 (the special-function unit's
+// base-2 exponential, within a few units in the last place; subnormal results
+// flush to zero and 2^-inf = 0).
+KVP_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ---------------------------------------------------------------- bf16 helpers

@@ -71,7 +71,7 @@ struct MlaParams {
   const int32_t* page_table;  // [B, max_pages]
   const int32_t* count;       // [B]
   int B, Hq, HT, NS;          // batch, query heads, head tiles, slices per unit
-  int TH;                     // query heads per tile: 16 (mla_decode_kernel) or 64 (mla_tile_kernel)
+  int TH;                     // query heads per tile: 16, 64 (mla_tile_kernel) or 128 (mla_tc_kernel)
   int max_pages, n_pages_cap, now;
   float qscale;               // scale * log2(e)
   float* out;                 // [B, Hq, kDc]
@@ -740,6 +740,419 @@ __global__ void __launch_bounds__(kTThreads, 1) mla_tile_kernel(const MlaParams 
   }
 }
 
+// ---------------------------------------------------------------- tcgen05 tiles
+// From kTcFrom query heads on, both products run on the tcgen05 tensor cores
+// with the query heads as M = 128 (rows past Hq are zero). Tensor memory has
+// 512 columns of 128 lanes and the fp32 output of 128 heads x 512 values
+// alone would fill it, so the output is split over four CTAs: CTA (unit,
+// slice, quarter v) owns output values 128v .. 128v + 127, and all four
+// compute the same logits and weights. Per lane = head, tensor memory holds
+//   columns   0..287  the query row, 576 bf16 (the A operand of S)
+//   columns 288..335  buffer 0: S of a block of 48 tokens (3 pages), fp32;
+//                     P of that block, 48 bf16, is written over columns
+//                     288..311 once both warps of the row pair have read S
+//   columns 336..383  buffer 1: the same for the next block
+//   columns 384..511  the output quarter, fp32
+// Per block of 3 pages:
+//   S  = Q C^T      M = 128 heads, N = 48 tokens, K = 576: 36 MMAs, A from
+//                   tensor memory, B the block's rows (K-major, 128-byte
+//                   swizzle; box j of the 3 pages lies in one 6 KB run)
+//   softmax         online, base 2, lazy rescaling of the output in tensor
+//                   memory; p rounded to bf16 for the product, the running
+//                   sum takes p itself
+//   O += P Cv       M = 128, N = 128 values, K = 16 tokens per page: B is the
+//                   page's rows read MN-major (values contiguous)
+// With two buffers, S of block i + 1 is computed while the softmax works on
+// block i. Eight softmax warps: warps w and w + 4 share tensor-memory lane
+// quadrant w (rows 32w ..), warp w taking tokens 0..23 of each block and
+// output columns 0..63, w + 4 tokens 24..47 and columns 64..127; the pair
+// exchanges its row maximum once per block through shared memory behind a
+// 64-thread named barrier. Lane 0 of warp 8 issues the MMAs and lane 0 of
+// warp 9 the copies, into a ring of four 3-page stages.
+// Measured limits (a tcgen05.mma with A from tensor memory and N <= 96 takes
+// as long as one with N = 96, about 48 cycles): the logits run their
+// products at half rate and are computed four times; the ring holds a block
+// from its copy to its output product, so little more than one block is in
+// flight per SM. Other splits measured and not kept: output halves (the
+// query's last four boxes in shared memory, a ring of two stages), separate
+// rings for the boxes only the logits read and for the output boxes, a
+// prefetch of later pages into L2.
+constexpr int kCHeads = 128;                          // M of both products
+constexpr int kCParts = 4;                            // CTAs per (unit, slice), one per output quarter
+constexpr int kCVals = kDc / kCParts;                 // output values per CTA
+constexpr int kCPages = 3;                            // pages per block
+constexpr int kCTok = kCPages * kPage;                // tokens per block: the N of S
+constexpr int kCHalf = kCTok / 2;                     // tokens per softmax thread
+constexpr int kCBoxRun = kCPages * kBoxBytes;         // box j of a block's pages
+constexpr int kCRing = 4;                             // ring stages (blocks)
+constexpr int kCStageBytes = kBoxes * kCBoxRun;
+constexpr int kCSoftWarps = 8;
+constexpr int kCMmaWarp = kCSoftWarps, kCCopyWarp = kCSoftWarps + 1;
+constexpr int kCThreads = (kCSoftWarps + 2) * 32;
+constexpr uint32_t kTcQCol = 0;
+constexpr uint32_t kTcBufCol = kTcQCol + kRow / 2;    // buffer b at kTcBufCol + b * kCTok
+constexpr uint32_t kTcPOff = 0;                       // P at the start of its block's buffer
+constexpr uint32_t kTcOCol = kTcBufCol + 2 * kCTok;
+constexpr uint32_t kTcCols = 512;
+static_assert(kTcOCol + kCVals == kTcCols, "tensor-memory plan");
+static_assert(kCHalf % 8 == 0 && kCTok % 16 == 0 && kCBoxRun % 1024 == 0 && kCVals % 64 == 0, "block tiling");
+constexpr int kCRecOff = kCRing * kCStageBytes;                 // expire values of each stage's pages
+constexpr int kCBiasOff = kCRecOff + kCRing * kCTok * 4;        // per softmax warp: its tokens' mask as 0 / -inf
+constexpr int kCXchOff = kCBiasOff + kCSoftWarps * kCHalf * 4;  // [2][softmax warp][32]: row maxima, then sums
+constexpr int kCBarOff = kCXchOff + 2 * kCSoftWarps * 32 * 4;
+constexpr int kCNBars = 2 * kCRing + 7;               // full, empty, s_full[2], p_full[2], o_done[2], fin
+constexpr int kCSmemUsed = kCBarOff + kCNBars * 8 + 16;
+constexpr int kCSmemBytes = 1024 + kCSmemUsed;
+static_assert(kCStageBytes % 1024 == 0 && kCRecOff % 16 == 0 && kCBiasOff % 16 == 0 &&
+                  kCXchOff % 16 == 0 && kCBarOff % 8 == 0,
+              "alignment");
+static_assert(kCSmemBytes <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
+                                                              const __grid_constant__ CUtensorMap tmL) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  pdl_launch_dependents();
+  pdl_wait();  // counts and pages come from the kernels before this one
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // quarter fastest, then head tile: the CTAs that read the same pages run side by side
+  const int vq = static_cast<int>(blockIdx.x % kCParts);
+  const int r1 = static_cast<int>(blockIdx.x / kCParts);
+  const int ht = r1 % p.HT;
+  const int r2 = r1 / p.HT;
+  const int s = r2 % p.NS;
+  const int b = r2 / p.NS;
+  const int unit = b * p.HT + ht;
+  const int h_base = ht * kCHeads;
+
+  uint8_t* ring = smem;
+  int32_t* rec_s = reinterpret_cast<int32_t*>(smem + kCRecOff);
+  float* bias_s = reinterpret_cast<float*>(smem + kCBiasOff);
+  float* xch_s = reinterpret_cast<float*>(smem + kCXchOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kCBarOff);
+  uint64_t* empty = full + kCRing;
+  uint64_t* s_full = empty + kCRing;  // [2]
+  uint64_t* p_full = s_full + 2;      // [2]
+  uint64_t* o_done = p_full + 2;      // [2]
+  uint64_t* fin = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int cnt = min(max(p.count[b], 0), p.max_pages * kPage);
+  const int np = (cnt + kPage - 1) / kPage;
+  const int pg0 = static_cast<int>(static_cast<int64_t>(s) * np / p.NS);
+  const int pg1 = static_cast<int>(static_cast<int64_t>(s + 1) * np / p.NS);
+  const int n_my = pg1 - pg0;
+  const int nb = (n_my + kCPages - 1) / kCPages;
+  const int slot_end = min(cnt, pg1 * kPage);  // this slice's slots end here
+
+  if (tid == 0) {
+    for (int st = 0; st < kCRing; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&s_full[j], 1);
+      mbar_init(&p_full[j], kCSoftWarps);
+      mbar_init(&o_done[j], 1);
+    }
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmL);
+  }
+  if (warp == kCMmaWarp) {
+    tmem_alloc(tmem_slot, kTcCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    // ---- the query rows into tensor memory (thread = head row; zero past Hq)
+    const int row = warp * 32 + lane;
+    const int h = h_base + row;
+    const uint4* src =
+        h < p.Hq ? reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(b) * p.Hq + h) * kRow) : nullptr;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+    for (int c = 0; c < kBoxes; ++c) {
+      uint32_t v[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 u = src != nullptr ? __ldg(src + c * 8 + i) : make_uint4(0, 0, 0, 0);
+        v[4 * i] = u.x;
+        v[4 * i + 1] = u.y;
+        v[4 * i + 2] = u.z;
+        v[4 * i + 3] = u.w;
+      }
+      tmem_st32(trow + kTcQCol + c * 32, v);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == kCCopyWarp) {
+    // ------------------------------------------------------------ copies
+    if (lane == 0) {
+      int i = 0;
+      for (; i < nb; ++i) {
+        const int st = i % kCRing;
+        if (i >= kCRing &&
+            !mbar_wait(&empty[st], static_cast<uint32_t>((i / kCRing - 1) & 1), abort_flag, p.status)) {
+          record_error(p.status, KVP_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* stage = ring + st * kCStageBytes;
+        int32_t* rec = rec_s + st * kCTok;
+        int phys[kCPages];
+        int valid = 0;
+#pragma unroll
+        for (int pp = 0; pp < kCPages; ++pp) {
+          const int k = i * kCPages + pp;
+          int ph = -1;
+          if (k < n_my) {
+            ph = p.page_table[static_cast<int64_t>(b) * p.max_pages + pg0 + k];
+            if (ph < 0 || ph >= p.n_pages_cap) {
+              record_error(p.status, KVP_ERR_BOUNDS);  // inconsistent page table: the page reads as gone
+              ph = -1;
+            }
+          }
+          phys[pp] = ph;
+          valid += ph >= 0;
+          if (ph < 0) {
+            for (int t = 0; t < kPage; ++t) rec[pp * kPage + t] = 0;
+          }
+        }
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&full[st], kCStageBytes + valid * kPage * 4);
+#pragma unroll
+        for (int pp = 0; pp < kCPages; ++pp) {
+          // a page past the slice (or a bad one) is read from past the pool's last row: zeros
+          const int y = (phys[pp] >= 0 ? phys[pp] : p.n_pages_cap) * kPage;
+#pragma unroll
+          for (int j = 0; j < kBoxes; ++j)
+            tma_load_2d(stage + j * kCBoxRun + pp * kBoxBytes, &tmL, 64 * j, y, &full[st]);
+          if (phys[pp] >= 0)
+            bulk_g2s(rec + pp * kPage, p.expire_pool + static_cast<int64_t>(phys[pp]) * kPage, kPage * 4, &full[st]);
+        }
+      }
+      if (*abort_flag) {
+        // the copies already issued land before the CTA's shared memory is released (each wait bounded again)
+        for (int kk = max(0, i - kCRing); kk < i; ++kk) (void)mbar_wait(&full[kk % kCRing], (kk / kCRing) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kCMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nb > 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kCHeads, kCTok);
+      constexpr uint32_t idO = idesc_bf16_f32(kCHeads, kCVals) | kIdescBMnMajor;
+      const uint32_t ring_u32 = smem_u32(ring);
+      // S of block i into buffer i & 1; the block's pages must have landed and,
+      // from block 2 on, the products of block i - 2 (which read P from that
+      // buffer) must be complete
+      auto issue_s = [&](int i) -> bool {
+        if (!mbar_wait(&full[i % kCRing], static_cast<uint32_t>((i / kCRing) & 1), abort_flag, p.status)) return false;
+        if (i >= 2 && !mbar_wait(&o_done[i & 1], static_cast<uint32_t>(((i - 2) >> 1) & 1), abort_flag, p.status))
+          return false;
+        tc_fence_after();
+        const uint32_t base = ring_u32 + (i % kCRing) * kCStageBytes;
+        const uint32_t d = tmem + kTcBufCol + (i & 1) * kCTok;
+#pragma unroll
+        for (int kk = 0; kk < kRow / 16; ++kk) {
+          const uint64_t bdesc = sw128_kmajor_desc(base + (kk >> 2) * kCBoxRun + (kk & 3) * 32);
+          umma_bf16_tmem_a(d, tmem + kTcQCol + kk * 8, bdesc, idS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[i & 1]);
+        return true;
+      };
+      bool ok = issue_s(0) && (nb < 2 || issue_s(1));
+      for (int i = 0; ok && i < nb; ++i) {
+        const int st = i % kCRing;
+        ok = mbar_wait(&p_full[i & 1], static_cast<uint32_t>((i >> 1) & 1), abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vbase = ring_u32 + st * kCStageBytes + (kCVals / 64) * vq * kCBoxRun;
+        const uint32_t pa = tmem + kTcBufCol + (i & 1) * kCTok + kTcPOff;
+#pragma unroll
+        for (int ks = 0; ks < kCPages; ++ks) {
+          const uint64_t bdesc = sw128_mnmajor_desc(vbase + ks * kBoxBytes, kCBoxRun, 1024);
+          umma_bf16_tmem_a(tmem + kTcOCol, pa + ks * 8, bdesc, idO, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(&o_done[i & 1]);
+        umma_commit(&empty[st]);
+        if (i + 2 < nb) ok = issue_s(i + 2);
+      }
+      if (!ok) {
+        record_error(p.status, KVP_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit(fin);
+      (void)mbar_wait(fin, 0u);  // every product issued has completed before tensor memory is freed
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    // warp w: rows 32 (w & 3) .., tokens kCHalf (w >> 2) .. of each block; output columns (kCVals / 2) (w >> 2) ..
+    const int quad = warp & 3, hs = warp >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const int bar_id = 1 + quad;  // named barrier of the pair (warps quad, quad + 4)
+    float* bias = bias_s + warp * kCHalf;
+    float m = -1e30f, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < nb; ++i) {
+      const int st = i % kCRing;
+      const uint32_t bcol = kTcBufCol + (i & 1) * kCTok;
+      ok = mbar_wait(&s_full[i & 1], static_cast<uint32_t>((i >> 1) & 1), abort_flag, p.status);
+      // the pair leaves together, so that neither waits at the barrier for a partner that has left
+      if (named_bar_or(bar_id, 64, !ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[kCHalf];
+      tmem_ld24(trow + bcol + hs * kCHalf, x);
+      // this warp's tokens' mask as an additive bias
+      {
+        const int32_t* rec = rec_s + st * kCTok + hs * kCHalf;
+        const int slot0 = (pg0 + i * kCPages) * kPage + hs * kCHalf;
+        if (lane < kCHalf) bias[lane] = (slot0 + lane < slot_end && p.now < rec[lane]) ? 0.f : -INFINITY;
+        __syncwarp();
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kCHalf; j += 4) {
+        const float4 bb = *reinterpret_cast<const float4*>(bias + j);
+        x[j] = fmaf(x[j], p.qscale, bb.x);
+        x[j + 1] = fmaf(x[j + 1], p.qscale, bb.y);
+        x[j + 2] = fmaf(x[j + 2], p.qscale, bb.z);
+        x[j + 3] = fmaf(x[j + 3], p.qscale, bb.w);
+        mx = fmaxf(mx, fmaxf(fmaxf(x[j], x[j + 1]), fmaxf(x[j + 2], x[j + 3])));
+      }
+      // the row maximum over both halves (double-buffered by block parity); past this barrier both
+      // warps of the pair have read their S, so either may write P over it
+      float* xb = xch_s + (i & 1) * kCSoftWarps * 32;
+      xb[warp * 32 + lane] = mx;
+      tc_fence_before();
+      named_bar_sync(bar_id, 64);
+      tc_fence_after();
+      mx = fmaxf(mx, xb[(warp ^ 4) * 32 + lane]);
+      const bool grow = mx > m + kLazyRescale;  // the same in both warps of the pair
+      if (i > 0 && __any_sync(0xffffffffu, grow)) {
+        ok = mbar_wait(&o_done[(i - 1) & 1], static_cast<uint32_t>(((i - 1) >> 1) & 1), abort_flag, p.status);
+        if (named_bar_or(bar_id, 64, !ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float al = grow ? exp2f(m - mx) : 1.f;
+#pragma unroll 1
+        for (int c = hs * (kCVals / 2); c < (hs + 1) * (kCVals / 2); c += 32) {
+          float v[32];
+          tmem_ld32(trow + kTcOCol + c, v);
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(v[j] * al);
+          tmem_st32(trow + kTcOCol + c, w);
+        }
+      }
+      if (grow) {
+        l *= exp2f(m - mx);
+        m = mx;
+      }
+      // p = 2^(x - m) rounded to bf16 for the product; the sum takes p itself
+      uint32_t pk[kCHalf / 2];
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < kCHalf / 2; ++j) {
+        const float p0 = ex2_approx(x[2 * j] - m);
+        const float p1 = ex2_approx(x[2 * j + 1] - m);
+        ls0 += p0;
+        ls1 += p1;
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);  // p0 in the low half
+        pk[j] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
+      l += ls0 + ls1;
+      // P of tokens kCHalf hs .. at columns bcol + kTcPOff + (kCHalf / 2) hs ..
+      tmem_st12(trow + bcol + kTcPOff + hs * (kCHalf / 2), pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[i & 1]);
+    }
+    if (ok && nb > 0) {
+      ok = mbar_wait(&o_done[(nb - 1) & 1], static_cast<uint32_t>(((nb - 1) >> 1) & 1), abort_flag, p.status);
+      ok = !named_bar_or(bar_id, 64, !ok);
+      tc_fence_after();
+    }
+    if (!ok) {
+      if (lane == 0) {
+        record_error(p.status, KVP_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    } else {
+      // the row's sum over both halves
+      float* xb = xch_s + (nb & 1) * kCSoftWarps * 32;
+      xb[warp * 32 + lane] = l;
+      named_bar_sync(bar_id, 64);
+      const float lt = l + xb[(warp ^ 4) * 32 + lane];
+      const int h = h_base + row;
+      const int c0 = hs * (kCVals / 2);
+      if (p.NS == 1) {
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        float* orow = p.out + (static_cast<int64_t>(b) * p.Hq + h) * kDc + vq * kCVals;
+#pragma unroll 1
+        for (int c = c0; c < c0 + kCVals / 2; c += 32) {
+          float v[32];
+          if (nb > 0) {
+            tmem_ld32(trow + kTcOCol + c, v);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+          }
+          if (h < p.Hq) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(orow + c + j) =
+                  make_float4(v[j] * inv, v[j + 1] * inv, v[j + 2] * inv, v[j + 3] * inv);
+          }
+        }
+      } else {
+        const int64_t slot = static_cast<int64_t>(unit) * p.NS + s;
+        if (nb > 0) {  // an empty slice leaves its accumulator unwritten: its sum is 0 and the merge skips it
+          float* pa = p.part_acc + (slot * kCHeads + row) * kDc + vq * kCVals;
+#pragma unroll 1
+          for (int c = c0; c < c0 + kCVals / 2; c += 32) {
+            float v[32];
+            tmem_ld32(trow + kTcOCol + c, v);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(pa + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          }
+        }
+        if (vq == 0 && hs == 0) {
+          p.part_ml[(slot * kCHeads + row) * 2] = m;
+          p.part_ml[(slot * kCHeads + row) * 2 + 1] = lt;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kCMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcCols);
+  }
+}
+
 int sm_count() {
   static const int n = [] {
     int dev = 0, nsm = 0;
@@ -751,22 +1164,37 @@ int sm_count() {
   return n;
 }
 
-// Up to 32 query heads, CTAs of mla_decode_kernel take 16-head tiles (at 32
+// Which kernel takes a call (batch 16 x 8192 tokens): CTAs of
+// mla_decode_kernel take 16-head tiles up to kTileFrom - 1 query heads (at 32
 // heads two tiles of 16 ran 87 us where one 64-head tile with half its warps
-// idle ran 90 us, batch 16 x 8192 tokens); above, mla_tile_kernel takes
-// tiles of 64.
+// idle ran 90 us), mla_tile_kernel 64-head tiles up to kTcFrom - 1 (106 us at
+// 40 heads, 124 us at 64, where mla_tc_kernel takes about 163 us at any head
+// count up to 128), mla_tc_kernel 128-head tiles from kTcFrom on (166 us at
+// 96 or 128 heads, where two 64-head tiles take 262 us).
+#ifndef KVP_MLA_TC_FROM
+#define KVP_MLA_TC_FROM 65
+#endif
 constexpr int kTileFrom = 33;
-int tile_heads(int n_q_heads) { return n_q_heads >= kTileFrom ? kTHeads : kHT; }
+constexpr int kTcFrom = KVP_MLA_TC_FROM;
+enum MlaPath { kPath16, kPath64, kPathTc };
+MlaPath mla_path(int n_q_heads) {
+  return n_q_heads >= kTcFrom ? kPathTc : (n_q_heads >= kTileFrom ? kPath64 : kPath16);
+}
+int tile_heads(int n_q_heads) {
+  const MlaPath k = mla_path(n_q_heads);
+  return k == kPathTc ? kCHeads : (k == kPath64 ? kTHeads : kHT);
+}
 int n_tiles(int n_q_heads) { return (n_q_heads + tile_heads(n_q_heads) - 1) / tile_heads(n_q_heads); }
+int ctas_per_slice(int n_q_heads) { return mla_path(n_q_heads) == kPathTc ? kCParts : 1; }
 
 // Slices per unit: as many as one wave of CTAs holds (two per SM for the
-// 16-head kernel, one for the 64-head one), so no CTA waits for a second
-// wave (128 units on 152 SMs: 2 slices, 256 CTAs, rather than 3 slices and
-// 384 CTAs in 1.26 waves); at least one.
+// 16-head kernel, one for the others), so no CTA waits for a second wave
+// (128 units on 152 SMs: 2 slices, 256 CTAs, rather than 3 slices and 384
+// CTAs in 1.26 waves); at least one.
 int pick_splits(int batch, int n_q_heads) {
   const int nsm = sm_count();
-  const int64_t units = static_cast<int64_t>(batch) * n_tiles(n_q_heads);
-  const int per_sm = n_q_heads >= kTileFrom ? 1 : 2;
+  const int64_t units = static_cast<int64_t>(batch) * n_tiles(n_q_heads) * ctas_per_slice(n_q_heads);
+  const int per_sm = mla_path(n_q_heads) == kPath16 ? 2 : 1;
   const int64_t want = per_sm * static_cast<int64_t>(nsm > 0 ? nsm : 1) / units;
   return static_cast<int>(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
 }
@@ -812,7 +1240,8 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
   const int HT = n_tiles(n_q_heads);
   const int th = tile_heads(n_q_heads);
   const int64_t units = static_cast<int64_t>(batch) * HT;
-  const int64_t grid = units * ns;
+  const MlaPath path = mla_path(n_q_heads);
+  const int64_t grid = units * ns * ctas_per_slice(n_q_heads);
   if (grid > 0x7fffffff || units * th > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < kvp_decode_attn_mla_workspace_bytes(batch, n_q_heads, ns))
     return KVP_ERR_WORKSPACE;
@@ -829,7 +1258,9 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
   static const bool attr_ok =
       cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ==
           cudaSuccess &&
-      cudaFuncSetAttribute(mla_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmemBytes) == cudaSuccess;
+      cudaFuncSetAttribute(mla_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmemBytes) ==
+          cudaSuccess &&
+      cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCSmemBytes) == cudaSuccess;
   if (!attr_ok) return KVP_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   MlaParams p{static_cast<const uint16_t*>(q),
@@ -849,11 +1280,12 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
               reinterpret_cast<float*>(ws + ws_ml_bytes(units, ns, th)),
               reinterpret_cast<float*>(ws),
               status};
+  const dim3 g(static_cast<unsigned>(grid));
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const cudaError_t le =
-      th == kTHeads ? launch_pdl(mla_tile_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTThreads), kTSmemBytes,
-                                 static_cast<cudaStream_t>(stream), p, tmL)
-                    : launch_pdl(mla_decode_kernel, dim3(static_cast<unsigned>(grid)), dim3(kMThreads), kSmemBytes,
-                                 static_cast<cudaStream_t>(stream), p, tmL);
+      path == kPathTc   ? launch_pdl(mla_tc_kernel, g, dim3(kCThreads), kCSmemBytes, cs, p, tmL)
+      : path == kPath64 ? launch_pdl(mla_tile_kernel, g, dim3(kTThreads), kTSmemBytes, cs, p, tmL)
+                        : launch_pdl(mla_decode_kernel, g, dim3(kMThreads), kSmemBytes, cs, p, tmL);
   if (le != cudaSuccess) return KVP_ERR_CUDA;
   if (ns > 1 && launch_pdl(mla_merge_kernel, dim3(static_cast<unsigned>(units * th)), dim3(kDc / 4), 0,
                            static_cast<cudaStream_t>(stream), p) != cudaSuccess)

@@ -80,21 +80,6 @@ struct ScoreParams {
   int32_t* status;
 };
 
-KVP_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-// Barrier over n threads that also ORs v across them (every one of the n must reach it).
-KVP_DEV bool named_bar_or(int id, int n, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
 template <int BN, int EPI>
 __global__ void __launch_bounds__(score_threads<EPI>(), 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,

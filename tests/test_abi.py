@@ -229,10 +229,12 @@ def test_latent_host_checks():
 def test_mla_attention_host_checks_and_workspace():
     import kv_cache_pruning_gb300 as k
     L = k.library()
-    # (m, l) and accumulators per unit, slice and head of the tile: 16-head tiles up to 32 heads, 64 above
+    # (m, l) and accumulators per unit, slice and head of the tile: 16-head tiles up to 32 heads, 64-head
+    # tiles up to 64, 128-head tiles above
     assert L.kvp_decode_attn_mla_workspace_bytes(2, 20, 3) == 4 * 3 * 16 * 2 * 4 + 4 * 3 * 16 * 512 * 4
     assert L.kvp_decode_attn_mla_workspace_bytes(2, 33, 3) == 2 * 3 * 64 * 2 * 4 + 2 * 3 * 64 * 512 * 4
-    assert L.kvp_decode_attn_mla_workspace_bytes(2, 130, 3) == 6 * 3 * 64 * 2 * 4 + 6 * 3 * 64 * 512 * 4
+    assert L.kvp_decode_attn_mla_workspace_bytes(2, 65, 3) == 2 * 3 * 128 * 2 * 4 + 2 * 3 * 128 * 512 * 4
+    assert L.kvp_decode_attn_mla_workspace_bytes(2, 130, 3) == 4 * 3 * 128 * 2 * 4 + 4 * 3 * 128 * 512 * 4
     assert L.kvp_decode_attn_mla_workspace_bytes(3, 16, 2) == 3 * 2 * 16 * 2 * 4 + 3 * 2 * 16 * 512 * 4
     assert L.kvp_decode_attn_mla_workspace_bytes(1, 1, 1) == 16 * 2 * 4 + 16 * 512 * 4
     assert L.kvp_decode_attn_mla_workspace_bytes(2, 16, 65) == 0

@@ -156,7 +156,8 @@ def test_canaries_mla(kvp):
     for i in range(4):
         kvp.kvp_append_latent(c, ln[:, i].contiguous(), T + i, mode=kvp.KVP_MASK_KVZAP,
                               score=dev_f32(np.zeros(B, np.float32)), tau=dev_f32(tau), status=st)
-    for hq, ns in ((Hq, 1), (Hq, 3), (40, 1), (40, 3)):   # 16-head tiles, then 64-head tiles
+    # 16-head tiles, 64-head tiles, then the tensor-core kernel's 128-head tiles
+    for hq, ns in ((Hq, 1), (Hq, 3), (40, 1), (40, 3), (72, 1), (72, 3)):
         qh = q if hq == Hq else syn.q_inputs(7, B, hq, row)
         out = g((B, hq, kvp.KVP_MLA_LATENT_DIM), torch.float32)
         kvp.kvp_decode_attn_mla(dev_bf16(qh), c, T + 3, out=out, n_splits=ns,
