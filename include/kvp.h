@@ -603,8 +603,9 @@ KVP_API kvp_status kvp_append_latent(int mode, int batch, int row_dim, int pos, 
  *   33 to 64 query heads   one tile of 64 heads, one CTA per (unit, slice)
  *                          (mma.sync), weights as a hi + lo pair
  *   from 65 query heads    tiles of 128 heads on tcgen05 (tensor memory):
- *                          four CTAs per (unit, slice), one per quarter of
- *                          the latent_dim output values; each weight is
+ *                          a cluster of four CTAs per (unit, slice), one
+ *                          per quarter of the latent_dim output values,
+ *                          sharing each page's copies; each weight is
  *                          rounded to bf16 once (relative error <= 2^-9 per
  *                          weight; the normaliser sums the unrounded
  *                          weights, so an output value is off by at most

@@ -66,6 +66,31 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return e;
 }
 
+// launch_pdl with thread-block clusters of cluster_x CTAs (grid.x a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                               unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  // a rejected launch (a configuration error, not a fault) is reported here and
+  // taken off the runtime's last-error slot, so that the next call does not see it
+  if (e != cudaSuccess) (void)cudaGetLastError();
+  return e;
+}
+
 // Named barrier `id` (1..15) over n threads (a multiple of 32).
 KVP_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 // The same, returning the OR of v over the n threads (every one of them must reach it).
@@ -158,6 +183,16 @@ KVP_DEV void tma_load_2d(void* dst, const void* tmap, int c0, int c1, uint64_t* 
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
+// The same box delivered to the same shared-memory offset in every CTA of the
+// cluster named in cta_mask, each arrival counted on the mbarrier at `bar`'s
+// offset in that CTA.
+KVP_DEV void tma_load_2d_multicast(void* dst, const void* tmap, int c0, int c1, uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
+      : "memory");
+}
 KVP_DEV void tma_load_2d_hint(void* dst, const void* tmap, int c0, int c1, uint64_t* bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
@@ -217,6 +252,26 @@ KVP_DEV void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, 
 KVP_DEV void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// The same, arriving on the mbarrier at `bar`'s offset in every CTA of the cluster named in cta_mask.
+KVP_DEV void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Thread-block clusters: this CTA's rank, and a barrier over every thread of
+// every CTA of the cluster (release / acquire).
+KVP_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+KVP_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
@@ -303,6 +358,54 @@ KVP_DEV void tmem_ld24(uint32_t taddr, float (&v)[24]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 24; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Stores 16, 8 or 4 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+KVP_DEV void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+KVP_DEV void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+KVP_DEV void tmem_st4(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+// Stores N (a multiple of 4) consecutive 32-bit columns of this warp's 32 TMEM lanes.
+template <int N>
+KVP_DEV void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N % 4 == 0, "columns in fours");
+  int c = 0;
+#pragma unroll
+  for (; c + 16 <= N; c += 16) tmem_st16(taddr + c, r + c);
+  if constexpr (N % 16 >= 8) {
+    tmem_st8(taddr + c, r + c);
+    c += 8;
+  }
+  if constexpr (N % 8 == 4) tmem_st4(taddr + c, r + c);
+}
+// Loads N (a multiple of 8) consecutive fp32 columns of this warp's 32 TMEM lanes and waits for them.
+template <int N>
+KVP_DEV void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
+  static_assert(N % 8 == 0, "columns in eights");
+  if constexpr (N == 24) {
+    tmem_ld24(taddr, v);
+  } else {
+    int c = 0;
+#pragma unroll
+    for (; c + 32 <= N; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<float(*)[32]>(&v[c]));
+#pragma unroll
+    for (; c + 16 <= N; c += 16) tmem_ld16(taddr + c, *reinterpret_cast<float(*)[16]>(&v[c]));
+    static_assert(N % 16 == 0 || N == 24, "a remainder of 8 columns only at N = 24");
+  }
 }
 
 // Stores 12 consecutive 32-bit columns (8 + 4) of this warp's 32 TMEM lanes.

@@ -744,57 +744,55 @@ __global__ void __launch_bounds__(kTThreads, 1) mla_tile_kernel(const MlaParams 
 // From kTcFrom query heads on, both products run on the tcgen05 tensor cores
 // with the query heads as M = 128 (rows past Hq are zero). Tensor memory has
 // 512 columns of 128 lanes and the fp32 output of 128 heads x 512 values
-// alone would fill it, so the output is split over four CTAs: CTA (unit,
-// slice, quarter v) owns output values 128v .. 128v + 127, and all four
-// compute the same logits and weights. Per lane = head, tensor memory holds
+// alone would fill it, so the output is split over a cluster of four CTAs:
+// CTA (unit, slice, quarter v) owns output values 128v .. 128v + 127, and all
+// four compute the same logits and weights. Per lane = head, tensor memory
+// holds
 //   columns   0..287  the query row, 576 bf16 (the A operand of S)
-//   columns 288..335  buffer 0: S of a block of 48 tokens (3 pages), fp32;
-//                     P of that block, 48 bf16, is written over columns
-//                     288..311 once both warps of the row pair have read S
-//   columns 336..383  buffer 1: the same for the next block
+//   columns 288..383  S of a block of 96 tokens (6 pages), fp32; P of that
+//                     block, 96 bf16, is written over columns 288..335 once
+//                     both warps of the row pair have read S
 //   columns 384..511  the output quarter, fp32
-// Per block of 3 pages:
-//   S  = Q C^T      M = 128 heads, N = 48 tokens, K = 576: 36 MMAs, A from
+// Per block of 6 pages:
+//   S  = Q C^T      M = 128 heads, N = 96 tokens, K = 576: 36 MMAs, A from
 //                   tensor memory, B the block's rows (K-major, 128-byte
-//                   swizzle; box j of the 3 pages lies in one 6 KB run)
+//                   swizzle; box j of the 6 pages lies in one 12 KB run)
 //   softmax         online, base 2, lazy rescaling of the output in tensor
 //                   memory; p rounded to bf16 for the product, the running
 //                   sum takes p itself
 //   O += P Cv       M = 128, N = 128 values, K = 16 tokens per page: B is the
 //                   page's rows read MN-major (values contiguous)
-// With two buffers, S of block i + 1 is computed while the softmax works on
-// block i. Eight softmax warps: warps w and w + 4 share tensor-memory lane
-// quadrant w (rows 32w ..), warp w taking tokens 0..23 of each block and
-// output columns 0..63, w + 4 tokens 24..47 and columns 64..127; the pair
-// exchanges its row maximum once per block through shared memory behind a
-// 64-thread named barrier. Lane 0 of warp 8 issues the MMAs and lane 0 of
-// warp 9 the copies, into a ring of four 3-page stages.
-// Measured limits (a tcgen05.mma with A from tensor memory and N <= 96 takes
-// as long as one with N = 96, about 48 cycles): the logits run their
-// products at half rate and are computed four times; the ring holds a block
-// from its copy to its output product, so little more than one block is in
-// flight per SM. Other splits measured and not kept: output halves (the
-// query's last four boxes in shared memory, a ring of two stages), separate
-// rings for the boxes only the logits read and for the output boxes, a
-// prefetch of later pages into L2.
+// A tcgen05.mma with N <= 96 takes as long as one with N = 96 (about 48
+// cycles, measured), so the logits take 96 tokens a block; that leaves room
+// for one S buffer, and S of block i + 1 waits for block i's output product.
+// Eight softmax warps: warps w and w + 4 share tensor-memory lane quadrant w
+// (rows 32w ..), warp w taking tokens 0..47 of each block and output columns
+// 0..63, w + 4 tokens 48..95 and columns 64..127; the pair exchanges its row
+// maximum once per block through shared memory behind a 64-thread named
+// barrier. Lane 0 of warp 8 issues the MMAs and lane 0 of warp 9 the copies,
+// into a ring of two 6-page stages: each CTA of the cluster copies a quarter
+// of every page's boxes into all four (TMA multicast), and a stage is reused
+// once all four have released it (each CTA's release is a multicast commit).
 constexpr int kCHeads = 128;                          // M of both products
 constexpr int kCParts = 4;                            // CTAs per (unit, slice), one per output quarter
 constexpr int kCVals = kDc / kCParts;                 // output values per CTA
-constexpr int kCPages = 3;                            // pages per block
+constexpr int kCPages = 6;                            // pages per block
 constexpr int kCTok = kCPages * kPage;                // tokens per block: the N of S
 constexpr int kCHalf = kCTok / 2;                     // tokens per softmax thread
+constexpr int kCBufs = 1;                             // S buffers in tensor memory
 constexpr int kCBoxRun = kCPages * kBoxBytes;         // box j of a block's pages
-constexpr int kCRing = 4;                             // ring stages (blocks)
+constexpr int kCRing = 2;                             // ring stages (blocks)
 constexpr int kCStageBytes = kBoxes * kCBoxRun;
+constexpr uint16_t kCAllCtas = (1u << kCParts) - 1;   // the cluster: the four quarter CTAs of a (unit, slice)
 constexpr int kCSoftWarps = 8;
 constexpr int kCMmaWarp = kCSoftWarps, kCCopyWarp = kCSoftWarps + 1;
 constexpr int kCThreads = (kCSoftWarps + 2) * 32;
 constexpr uint32_t kTcQCol = 0;
 constexpr uint32_t kTcBufCol = kTcQCol + kRow / 2;    // buffer b at kTcBufCol + b * kCTok
 constexpr uint32_t kTcPOff = 0;                       // P at the start of its block's buffer
-constexpr uint32_t kTcOCol = kTcBufCol + 2 * kCTok;
+constexpr uint32_t kTcOCol = kTcBufCol + kCBufs * kCTok;
 constexpr uint32_t kTcCols = 512;
-static_assert(kTcOCol + kCVals == kTcCols, "tensor-memory plan");
+static_assert(kTcOCol + kCVals <= kTcCols, "tensor-memory plan");
 static_assert(kCHalf % 8 == 0 && kCTok % 16 == 0 && kCBoxRun % 1024 == 0 && kCVals % 64 == 0, "block tiling");
 constexpr int kCRecOff = kCRing * kCStageBytes;                 // expire values of each stage's pages
 constexpr int kCBiasOff = kCRecOff + kCRing * kCTok * 4;        // per softmax warp: its tokens' mask as 0 / -inf
@@ -849,7 +847,7 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
   if (tid == 0) {
     for (int st = 0; st < kCRing; ++st) {
       mbar_init(&full[st], 1);
-      mbar_init(&empty[st], 1);
+      mbar_init(&empty[st], kCParts);  // every CTA of the cluster releases the stage in all four
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(&s_full[j], 1);
@@ -868,7 +866,9 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_sync();  // every CTA's barriers exist before any copy or release reaches them
   const uint32_t tmem = *tmem_slot;
+  const uint32_t crank = cluster_ctarank();
 
   if (warp < 4) {
     // ---- the query rows into tensor memory (thread = head row; zero past Hq)
@@ -935,9 +935,9 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
         for (int pp = 0; pp < kCPages; ++pp) {
           // a page past the slice (or a bad one) is read from past the pool's last row: zeros
           const int y = (phys[pp] >= 0 ? phys[pp] : p.n_pages_cap) * kPage;
-#pragma unroll
-          for (int j = 0; j < kBoxes; ++j)
-            tma_load_2d(stage + j * kCBoxRun + pp * kBoxBytes, &tmL, 64 * j, y, &full[st]);
+          // this CTA copies boxes crank, crank + 4, ... of the page into all four CTAs of the cluster
+          for (int j = static_cast<int>(crank); j < kBoxes; j += kCParts)
+            tma_load_2d_multicast(stage + j * kCBoxRun + pp * kBoxBytes, &tmL, 64 * j, y, &full[st], kCAllCtas);
           if (phys[pp] >= 0)
             bulk_g2s(rec + pp * kPage, p.expire_pool + static_cast<int64_t>(phys[pp]) * kPage, kPage * 4, &full[st]);
         }
@@ -954,40 +954,42 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
       constexpr uint32_t idS = idesc_bf16_f32(kCHeads, kCTok);
       constexpr uint32_t idO = idesc_bf16_f32(kCHeads, kCVals) | kIdescBMnMajor;
       const uint32_t ring_u32 = smem_u32(ring);
-      // S of block i into buffer i & 1; the block's pages must have landed and,
-      // from block 2 on, the products of block i - 2 (which read P from that
-      // buffer) must be complete
+      // S of block i into buffer i % kCBufs; the block's pages must have landed
+      // and, from block kCBufs on, the products of block i - kCBufs (which read
+      // P from that buffer) must be complete
       auto issue_s = [&](int i) -> bool {
         if (!mbar_wait(&full[i % kCRing], static_cast<uint32_t>((i / kCRing) & 1), abort_flag, p.status)) return false;
-        if (i >= 2 && !mbar_wait(&o_done[i & 1], static_cast<uint32_t>(((i - 2) >> 1) & 1), abort_flag, p.status))
+        if (i >= kCBufs && !mbar_wait(&o_done[i % kCBufs], static_cast<uint32_t>(((i - kCBufs) / kCBufs) & 1),
+                                      abort_flag, p.status))
           return false;
         tc_fence_after();
         const uint32_t base = ring_u32 + (i % kCRing) * kCStageBytes;
-        const uint32_t d = tmem + kTcBufCol + (i & 1) * kCTok;
+        const uint32_t d = tmem + kTcBufCol + (i % kCBufs) * kCTok;
 #pragma unroll
         for (int kk = 0; kk < kRow / 16; ++kk) {
           const uint64_t bdesc = sw128_kmajor_desc(base + (kk >> 2) * kCBoxRun + (kk & 3) * 32);
           umma_bf16_tmem_a(d, tmem + kTcQCol + kk * 8, bdesc, idS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[i & 1]);
+        umma_commit(&s_full[i % kCBufs]);
         return true;
       };
-      bool ok = issue_s(0) && (nb < 2 || issue_s(1));
+      bool ok = true;
+      for (int i = 0; ok && i < min(kCBufs, nb); ++i) ok = issue_s(i);
       for (int i = 0; ok && i < nb; ++i) {
         const int st = i % kCRing;
-        ok = mbar_wait(&p_full[i & 1], static_cast<uint32_t>((i >> 1) & 1), abort_flag, p.status);
+        ok = mbar_wait(&p_full[i % kCBufs], static_cast<uint32_t>((i / kCBufs) & 1), abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vbase = ring_u32 + st * kCStageBytes + (kCVals / 64) * vq * kCBoxRun;
-        const uint32_t pa = tmem + kTcBufCol + (i & 1) * kCTok + kTcPOff;
+        const uint32_t pa = tmem + kTcBufCol + (i % kCBufs) * kCTok + kTcPOff;
 #pragma unroll
         for (int ks = 0; ks < kCPages; ++ks) {
           const uint64_t bdesc = sw128_mnmajor_desc(vbase + ks * kBoxBytes, kCBoxRun, 1024);
           umma_bf16_tmem_a(tmem + kTcOCol, pa + ks * 8, bdesc, idO, (i > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(&o_done[i & 1]);
-        umma_commit(&empty[st]);
-        if (i + 2 < nb) ok = issue_s(i + 2);
+        umma_commit(&o_done[i % kCBufs]);
+        umma_commit_multicast(&empty[st], kCAllCtas);  // the stage is free in this CTA: tell all four
+        if (i + kCBufs < nb) ok = issue_s(i + kCBufs);
       }
       if (!ok) {
         record_error(p.status, KVP_ERR_TIMEOUT);
@@ -995,6 +997,9 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
       }
       umma_commit(fin);
       (void)mbar_wait(fin, 0u);  // every product issued has completed before tensor memory is freed
+      // the other CTAs' releases of the last stages have reached this CTA's barriers before it exits
+      for (int i = max(0, nb - kCRing); i < nb; ++i)
+        (void)mbar_wait(&empty[i % kCRing], static_cast<uint32_t>((i / kCRing) & 1), abort_flag, p.status);
     }
     __syncwarp();
   } else {
@@ -1009,8 +1014,8 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
     bool ok = true;
     for (int i = 0; i < nb; ++i) {
       const int st = i % kCRing;
-      const uint32_t bcol = kTcBufCol + (i & 1) * kCTok;
-      ok = mbar_wait(&s_full[i & 1], static_cast<uint32_t>((i >> 1) & 1), abort_flag, p.status);
+      const uint32_t bcol = kTcBufCol + (i % kCBufs) * kCTok;
+      ok = mbar_wait(&s_full[i % kCBufs], static_cast<uint32_t>((i / kCBufs) & 1), abort_flag, p.status);
       // the pair leaves together, so that neither waits at the barrier for a partner that has left
       if (named_bar_or(bar_id, 64, !ok)) {
         ok = false;
@@ -1018,12 +1023,13 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
       }
       tc_fence_after();
       float x[kCHalf];
-      tmem_ld24(trow + bcol + hs * kCHalf, x);
+      tmem_ld_cols(trow + bcol + hs * kCHalf, x);
       // this warp's tokens' mask as an additive bias
       {
         const int32_t* rec = rec_s + st * kCTok + hs * kCHalf;
         const int slot0 = (pg0 + i * kCPages) * kPage + hs * kCHalf;
-        if (lane < kCHalf) bias[lane] = (slot0 + lane < slot_end && p.now < rec[lane]) ? 0.f : -INFINITY;
+#pragma unroll
+        for (int j = lane; j < kCHalf; j += 32) bias[j] = (slot0 + j < slot_end && p.now < rec[j]) ? 0.f : -INFINITY;
         __syncwarp();
       }
       float mx = -INFINITY;
@@ -1046,7 +1052,8 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
       mx = fmaxf(mx, xb[(warp ^ 4) * 32 + lane]);
       const bool grow = mx > m + kLazyRescale;  // the same in both warps of the pair
       if (i > 0 && __any_sync(0xffffffffu, grow)) {
-        ok = mbar_wait(&o_done[(i - 1) & 1], static_cast<uint32_t>(((i - 1) >> 1) & 1), abort_flag, p.status);
+        ok = mbar_wait(&o_done[(i - 1) % kCBufs], static_cast<uint32_t>(((i - 1) / kCBufs) & 1), abort_flag,
+                       p.status);
         if (named_bar_or(bar_id, 64, !ok)) {
           ok = false;
           break;
@@ -1081,14 +1088,15 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
       }
       l += ls0 + ls1;
       // P of tokens kCHalf hs .. at columns bcol + kTcPOff + (kCHalf / 2) hs ..
-      tmem_st12(trow + bcol + kTcPOff + hs * (kCHalf / 2), pk);
+      tmem_st_cols(trow + bcol + kTcPOff + hs * (kCHalf / 2), pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[i & 1]);
+      if (lane == 0) mbar_arrive(&p_full[i % kCBufs]);
     }
     if (ok && nb > 0) {
-      ok = mbar_wait(&o_done[(nb - 1) & 1], static_cast<uint32_t>(((nb - 1) >> 1) & 1), abort_flag, p.status);
+      ok = mbar_wait(&o_done[(nb - 1) % kCBufs], static_cast<uint32_t>(((nb - 1) / kCBufs) & 1), abort_flag,
+                     p.status);
       ok = !named_bar_or(bar_id, 64, !ok);
       tc_fence_after();
     }
@@ -1151,6 +1159,7 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
     tc_fence_after();
     tmem_dealloc(tmem, kTcCols);
   }
+  cluster_sync();  // no CTA leaves while another may still signal it
 }
 
 int sm_count() {
@@ -1283,7 +1292,7 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
   const dim3 g(static_cast<unsigned>(grid));
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const cudaError_t le =
-      path == kPathTc   ? launch_pdl(mla_tc_kernel, g, dim3(kCThreads), kCSmemBytes, cs, p, tmL)
+      path == kPathTc   ? launch_pdl_cluster(mla_tc_kernel, g, dim3(kCThreads), kCSmemBytes, cs, kCParts, p, tmL)
       : path == kPath64 ? launch_pdl(mla_tile_kernel, g, dim3(kTThreads), kTSmemBytes, cs, p, tmL)
                         : launch_pdl(mla_decode_kernel, g, dim3(kMThreads), kSmemBytes, cs, p, tmL);
   if (le != cudaSuccess) return KVP_ERR_CUDA;
