@@ -1177,9 +1177,9 @@ int sm_count() {
 // mla_decode_kernel take 16-head tiles up to kTileFrom - 1 query heads (at 32
 // heads two tiles of 16 ran 87 us where one 64-head tile with half its warps
 // idle ran 90 us), mla_tile_kernel 64-head tiles up to kTcFrom - 1 (106 us at
-// 40 heads, 124 us at 64, where mla_tc_kernel takes about 163 us at any head
-// count up to 128), mla_tc_kernel 128-head tiles from kTcFrom on (166 us at
-// 96 or 128 heads, where two 64-head tiles take 262 us).
+// 40 heads, 121 us at 64, where mla_tc_kernel takes about 137 us at any head
+// count up to 128), mla_tc_kernel 128-head tiles from kTcFrom on (137 us at
+// 128 heads, where two 64-head tiles take 262 us).
 #ifndef KVP_MLA_TC_FROM
 #define KVP_MLA_TC_FROM 65
 #endif
