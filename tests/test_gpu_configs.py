@@ -19,6 +19,11 @@ hundreds of millions of values).
   with the caches bit-exact after every recompaction and at the end, and
   the attention compared at every step.
 
+* MLA latent cache, DeepSeek-V3-shaped attention (DMS article, "주요 요점"
+  and "앞으로의 전망"): batch 16 x 8,192 tokens of 512 + 64-value rows, 128
+  query heads (the tensor-core kernel), kept whole and at each element's
+  75th-percentile score; four batch elements compared with the oracle in full.
+
 Bars: scores within 1e-3 relative, masks / pools / tables bit-exact,
 attention within max-abs 2e-2, mean-abs 2e-3 and 1e-2 relative per head."""
 import math
@@ -212,3 +217,36 @@ def test_dms_decode_loop_qwen3_8b_shape(kvp):
     compare_paged(pools[cur], ref, what="end of the loop")
     # delayed eviction at work: entries flagged in the last `delay` steps of the prompt are still cached
     assert int(ref.count.sum()) > B * H * (T0 // 8)
+
+
+# --------------------------------------------------------------------------- MLA latent cache
+
+@pytest.mark.parametrize("prune_q", [0.0, 0.75])
+def test_mla_latent_cache_128_heads_full_size(kvp, prune_q):
+    B, T, Hq, row, dc = 16, 8192, 128, kvp.LATENT_ROW, kvp.KVP_MLA_LATENT_DIM
+    now = T - 1
+    lat = syn.fast_normal_bf16(5, syn.S_LAT, (B, T, row))
+    s = syn.normal_f32(5, 61, (B, T, 1))
+    tau = (np.full((B, 1), -np.inf, np.float32) if prune_q == 0.0 else orc.threshold_at_quantile(s, prune_q))
+    q = syn.fast_normal_bf16(5, syn.S_Q, (B, Hq, row))
+    mp = T // 16
+    st = status_word()
+    c = kvp.LatentPagedKV.allocate(B, B * mp, mp)
+    kvp.kvp_compact_latent(dev_bf16(lat), now, 0, c, mode=kvp.KVP_MASK_KVZAP, scores=dev_f32(s[:, :, 0].copy()),
+                           tau=dev_f32(tau[:, 0].copy()), status=st)
+    out = kvp.kvp_decode_attn_mla(dev_bf16(q), c, now, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    o = out.cpu().numpy()
+    sel = [0, 5, 10, 15]
+    exp = orc.mask_kvzap(s[sel], tau[sel], now)[0][:, 0]
+    ref_c = orc.compact_latent_dense(lat[sel], exp, now, 0, len(sel) * mp, mp)
+    np.testing.assert_array_equal(c.count.cpu().numpy()[sel], ref_c.count[:, 0])
+    ref = orc.decode_attention_mla(q[sel], ref_c, dc, now)
+    check_attention(o[sel], ref)
+    # each softmax weight rounded to bf16 once: |error| <= (2^-9 + margin) * max |row value| of the element
+    u = 2.0 ** -9 + 2.0 ** -20
+    vmax = np.abs(orc.widen_bf16(lat[sel])[:, :, :dc]).max(axis=1)
+    assert (np.abs(o[sel] - ref) <= u * vmax[:, None, :] + 1e-5).all()
+    kept = int(ref_c.count.sum())
+    print(f"MLA 128 heads, pruned at q = {prune_q}: {kept} of {len(sel) * T} slots kept in the compared elements")

@@ -285,11 +285,13 @@ def test_decode_attn_mla_empty_batch_element(kvp):
         check_attention(o[[0, 2]], ref[[0, 2]])
 
 
-def test_mla_decode_loop(kvp):
+@pytest.mark.parametrize("Hq", [16, 128])
+def test_mla_decode_loop(kvp, Hq):
     """DMS decode loop on a latent cache: per step the new row is appended and
     attention runs; every 24 steps the cache is re-compacted. Each step's
-    output matches the oracle's."""
-    B, T0, steps, Hq = 2, 400, 60, 16
+    output matches the oracle's (16 heads: the mma.sync kernel; 128: the
+    tensor-core kernel, also within its bf16-weight bound)."""
+    B, T0, steps = 2, 400, 60
     delay, window, reserve = 48, 32, 64
     T = T0 + steps
     lat = syn.latent_inputs(47, B, T, ROW)
@@ -318,4 +320,7 @@ def test_mla_decode_loop(kvp):
         o = kvp.kvp_decode_attn_mla(dev_bf16(q), c, t, workspace=ws, status=st)
         torch.cuda.synchronize()
         assert st.item() == 0
-        check_attention(o.cpu().numpy(), orc.decode_attention_mla(q, ref, DC, t))
+        ref_o = orc.decode_attention_mla(q, ref, DC, t)
+        check_attention(o.cpu().numpy(), ref_o)
+        if Hq >= TC_FROM:
+            check_bf16_p_bound(o.cpu().numpy(), ref_o, lat)
