@@ -417,6 +417,10 @@ KVP_DEV void cp_async16(void* smem_dst, const void* gmem_src) {
 KVP_DEV void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
+// Closes the group of this thread's copies issued so far; waits until at most
+// one group (the newest) is still in flight.
+KVP_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+KVP_DEV void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Copy pass: one warp per 128-entry segment of one (b, h); grid
 // (B*H, ceil(NS / 4)). The warp lists the segment's present entries (source
@@ -435,8 +439,8 @@ constexpr int kStage = 20;
 
 // An entry is NPOOL rows of D bf16 values: a K and a V row (NPOOL = 2), or
 // one latent row of an MLA cache (NPOOL = 1, D = 576: 72 pieces of 16 bytes,
-// moved kStageWide at a time, about as many bytes per batch as 20 K/V pairs
-// of 128 values).
+// moved kStageWide at a time through two stage buffers, so that one batch is
+// loading while the other is stored).
 constexpr int kStageWide = 8;
 template <int D, int NPOOL>
 constexpr int entry_pieces() {
@@ -447,8 +451,13 @@ constexpr int stage_entries() {
   return entry_pieces<D, NPOOL>() > 32 ? kStageWide : kStage;
 }
 template <int D, int NPOOL>
+constexpr int stage_buffers() {
+  return entry_pieces<D, NPOOL>() > 32 ? 2 : 1;
+}
+template <int D, int NPOOL>
 constexpr int scatter_smem_bytes() {
-  return kWarpsPerCta * (stage_entries<D, NPOOL>() * entry_pieces<D, NPOOL>() * 16 + kSeg * 8);
+  return kWarpsPerCta * (stage_buffers<D, NPOOL>() * stage_entries<D, NPOOL>() * entry_pieces<D, NPOOL>() * 16 +
+                         kSeg * 8);
 }
 
 template <int D, int NPOOL, class Src, bool kFused>
@@ -478,8 +487,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
   const int warp = threadIdx.x >> 5;
   const int sg = blockIdx.y * kWarpsPerCta + warp;
   const int lane = threadIdx.x & 31;
-  uint4* stage = reinterpret_cast<uint4*>(sm_raw) + warp * kSt * E16;
-  int64_t* lst = reinterpret_cast<int64_t*>(sm_raw + kWarpsPerCta * kSt * E16 * 16) + warp * kSeg;
+  constexpr int kBufs = stage_buffers<D, NPOOL>();
+  uint4* stage = reinterpret_cast<uint4*>(sm_raw) + warp * kBufs * kSt * E16;
+  int64_t* lst = reinterpret_cast<int64_t*>(sm_raw + kWarpsPerCta * kBufs * kSt * E16 * 16) + warp * kSeg;
   const bool live = sg < NS;
 
   // ---- loads that do not depend on one another, all issued first
@@ -596,22 +606,36 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
 
   // ---- move the rows through the stage
   if constexpr (!kNarrow) {
-    // wide rows: the warp's lanes walk the batch's (entry, piece) pairs in order
-    for (int i0 = 0; i0 < nk; i0 += kSt) {
+    // wide rows: the warp's lanes walk the batch's (entry, piece) pairs in
+    // order; batch b + 1 is requested into the other buffer before batch b
+    // is stored
+    static_assert(kBufs == 2, "wide rows use two stage buffers");
+    auto load = [&](int i0, uint4* buf) {
       const int nb = min(kSt, nk - i0);
       for (int x = lane; x < nb * E16; x += 32) {
         const int i = x / E16, pc = x - i * E16;
-        cp_async16(stage + x, reinterpret_cast<const uint4*>(sv.kb + lst[i0 + i] * sv.stride) + pc);
+        cp_async16(buf + x, reinterpret_cast<const uint4*>(sv.kb + lst[i0 + i] * sv.stride) + pc);
       }
-      cp_async_wait_all();
-      __syncwarp();
+      cp_async_commit();
+    };
+    if (nk > 0) load(0, stage);
+    for (int b = 0, i0 = 0; i0 < nk; ++b, i0 += kSt) {
+      uint4* cur = stage + (b & 1) * kSt * E16;
+      if (i0 + kSt < nk) {
+        load(i0 + kSt, stage + ((b + 1) & 1) * kSt * E16);
+        cp_async_wait_one();  // this lane's copies of batch b have landed
+      } else {
+        cp_async_wait_all();
+      }
+      __syncwarp();  // and every lane's
+      const int nb = min(kSt, nk - i0);
       for (int x = lane; x < nb * E16; x += 32) {
         const int i = x / E16, pc = x - i * E16;
         const int j = slot0 + i0 + i;
         const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
-        reinterpret_cast<uint4*>(k_pool + row * D)[pc] = stage[x];
+        reinterpret_cast<uint4*>(k_pool + row * D)[pc] = cur[x];
       }
-      __syncwarp();
+      __syncwarp();  // every lane is done with this buffer before it is refilled
     }
     return;
   }
