@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
       mbar_arrive(&bars[st]);
       return;
     }
+    fence_proxy_async();  // a zero fill of this stage by ordinary stores is ordered before the tensor copy
     mbar_arrive_expect_tx(&bars[st], kStageBytes + kPage * 4);
     const int y = phys * kPage;
 #pragma unroll

@@ -186,6 +186,7 @@ def _mla_case(kvp, B, T, Hq, n_splits=0, seed=37, tau_std=0.7, peaked=False, q_z
     (1, 2000, 40, 3),      # 64-head tiles from 33 heads: five of the eight warps have heads
     (2, 1100, 72, 0),      # tensor-core kernel with rows 72..127 of its tile empty; many slices of 1-2 pages
     (1, 5000, 100, 1),     # one slice: the output written without a merge, 105 blocks through the ring
+    (2, 900, 136, 0),      # two 128-head tiles, the second with 8 heads
 ])
 def test_decode_attn_mla(kvp, B, T, Hq, n_splits):
     o, ref, *_ = _mla_case(kvp, B, T, Hq, n_splits)
@@ -259,9 +260,10 @@ def test_decode_attn_mla_workspace_reused(kvp, Hq):
         np.testing.assert_array_equal(o, fresh.cpu().numpy())
 
 
-def test_decode_attn_mla_empty_batch_element(kvp):
+@pytest.mark.parametrize("Hq", [16, 128])
+def test_decode_attn_mla_empty_batch_element(kvp, Hq):
     """A batch element with no slots gives zero rows; the others are unchanged."""
-    B, T, Hq = 3, 600, 16
+    B, T = 3, 600
     lat, s, tau, exp = _kvzap_latent(B, T, seed=45, window=0)
     exp[1, :] = 0          # nothing of batch element 1 is present (score -inf, no window)
     q = syn.q_inputs(45, B, Hq, ROW)
@@ -324,3 +326,32 @@ def test_mla_decode_loop(kvp, Hq):
         check_attention(o.cpu().numpy(), ref_o)
         if Hq >= TC_FROM:
             check_bf16_p_bound(o.cpu().numpy(), ref_o, lat)
+
+@pytest.mark.parametrize("Hq,n_splits", [(16, 0), (16, 3), (40, 3), (128, 0), (128, 3)])
+def test_decode_attn_mla_bad_page_ids(kvp, Hq, n_splits):
+    """A page id outside [0, n_pages_cap) in the page table records
+    KVP_ERR_BOUNDS; that page is read as no slots, the rest as usual (the
+    oracle with the page's slots expired)."""
+    B, T = 2, 1500
+    _, _, c, q, now = _mla_case(kvp, B, T, Hq, n_splits)
+    lat, s, tau, exp = _kvzap_latent(B, T, 37)
+    mp = (T + 15) // 16
+    ref_c = orc.compact_latent_dense(lat, exp, now, 0, B * mp, mp)
+    pt = c.page_table.clone()
+    cap = c.pool.shape[0]
+    for b, j, val in [(0, 2, -7), (1, 0, cap + 100), (1, 40, cap)]:
+        assert j * 16 < int(c.count[b])
+        ref_c.expire_pool[ref_c.page_table[b, 0, j]] = 0  # the oracle: every slot of the page gone
+        pt[b, j] = val
+    c_bad = kvp.LatentPagedKV(c.pool, c.expire_pool, pt, c.remap, c.count)
+    st = status_word()
+    out = kvp.kvp_decode_attn_mla(dev_bf16(q), c_bad, now, n_splits=n_splits, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == kvp.KVP_ERR_BOUNDS
+    ref = orc.decode_attention_mla(q, ref_c, DC, now)
+    o = out.cpu().numpy()
+    check_attention(o, ref)
+    if Hq >= TC_FROM:
+        check_bf16_p_bound(o, ref, lat)
+    else:
+        np.testing.assert_allclose(o, ref, rtol=0, atol=1e-4)
