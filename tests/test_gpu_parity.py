@@ -1046,3 +1046,33 @@ def test_chain_score_mask_compact_attend_tiny(kvp):
     assert st.item() == 0
     _compare_cache(c, ref_c)
     check_attention(o.cpu().numpy(), orc.decode_attention(q, ref_c, T - 1))
+
+
+@pytest.mark.parametrize("G,grid", [(4, 0), (4, 3), (8, 0), (8, 3)])
+def test_decode_attn_bad_page_ids(kvp, G, grid):
+    """A page id outside [0, n_pages_cap) in the page table records
+    KVP_ERR_BOUNDS; that page is read as no slots and everything else as
+    usual: the output equals the oracle's with that page's slots expired
+    (G = 4: the CUDA-core kernel; G = 8: the tensor-core page math)."""
+    B, T, H, d = 2, 1500, 4, 128
+    k, v, exp, cnt = _kvzap_case(B, T, H, d, seed=5)
+    q = syn.q_inputs(5, B, H * G, d)
+    max_pages = (T + 15) // 16
+    cap = B * H * max_pages
+    now = T - 1
+    ref_c = orc.compact_dense(k, v, exp, now, 0, cap, max_pages)
+    st = status_word()
+    c = kvp.PagedKV.allocate(B, H, d, cap, max_pages)
+    kvp.kvp_compact(dev_bf16(k), dev_bf16(v), dev_i32(exp), now, 0, c, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    pt = c.page_table.clone()
+    for b, h, j, val in [(0, 1, 3, -9), (1, 0, 0, cap + 7), (1, 3, 5, cap)]:
+        assert j * 16 < int(c.count[b, h])
+        ref_c.expire_pool[ref_c.page_table[b, h, j]] = 0  # the oracle: every slot of the page gone
+        pt[b, h, j] = val
+    c_bad = kvp.PagedKV(c.k_pool, c.v_pool, c.expire_pool, pt, c.remap, c.count)
+    out = kvp.kvp_decode_attn(dev_bf16(q), c_bad, now, grid_limit=grid, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == kvp.KVP_ERR_BOUNDS
+    check_attention(out.cpu().numpy(), orc.decode_attention(q, ref_c, now))
