@@ -7,23 +7,30 @@
 // rotary key) and takes the softmax-weighted sum of the rows' first 512
 // values. Every query head reads the same rows, so a page is worth
 // 16 tokens x (576 + 512) x 2 flops per head: on CUDA cores that outruns HBM
-// from a few heads on; here both products run on the tensor cores
-// (mma.sync m16n8k16, bf16 operands, fp32 accumulate).
+// from a few heads on, so both products run on the tensor cores. Pages arrive
+// as nine 16-row x 64-column boxes each (tensor copies of the pool viewed as
+// [pages x 16, 576], with the 128-byte swizzle) plus the page's 16 expire
+// values. Three kernels, by the number of query heads:
 //
-// A CTA (4 warps) takes 16 query heads of one batch element and one slice of
-// its pages. Its pages arrive through a ring of kRingPages stages as nine
-// 16-row x 64-column boxes each (tensor copies of the pool viewed as
-// [pages x 16, 576], with the 128-byte swizzle, so ldmatrix reads are free of
-// bank conflicts), plus the page's 16 expire values. Per page:
-//   S   = C Q^T     M = 16 tokens, N = 16 heads, K = 576: warp w takes the
-//                   144 values 144w .. 144w + 143; the four partial products
-//                   are summed through shared memory (one CTA barrier)
-//   softmax         every warp computes the same weights from the same sums
-//                   (online, base 2, lazy rescaling)
-//   O^T += Cv^T P^T M = 16 of the 512 compressed values at a time, N = 16
-//                   heads, K = 16 tokens: warp w owns values 128w .. 128w+127
-//                   (8 m-tiles), its A operand read transposed by ldmatrix
-// Slices of a unit (batch element, 16 heads) write their partial states; a
+//   mla_decode_kernel (up to 32 heads): a CTA of 4 warps per (batch element,
+//     16-head tile, slice of its pages), mma.sync m16n8k16:
+//       S   = C Q^T     M = 16 tokens, N = 16 heads, K = 576: warp w takes
+//                       the 144 values 144w .. 144w + 143; the four partial
+//                       products are summed through shared memory (one CTA
+//                       barrier per page)
+//       softmax         every warp computes the same weights (online, base 2,
+//                       lazy rescaling)
+//       O^T += Cv^T P^T M = 16 of the 512 compressed values at a time, N = 16
+//                       heads, K = 16 tokens: warp w owns values 128w ..
+//                       128w + 127 (its A operand read transposed by
+//                       ldmatrix); P as a bf16 hi + lo pair
+//   mla_tile_kernel (33 to 64 heads): a CTA of 8 warps per (batch element,
+//     64-head tile, slice), warp w owning heads 8w .. 8w + 7 outright
+//   mla_tc_kernel (65 heads and more): tcgen05 with the query, the logits and
+//     an output quarter in tensor memory, four CTAs per (batch element,
+//     128-head tile, slice) as a cluster sharing each page's copies
+//
+// Slices of a unit (batch element, head tile) write their partial states; a
 // second kernel, launched right after as the first one's programmatic
 // dependent, merges them in fp32 with one CTA per (unit, head), so the
 // merge's reads of the partial accumulators are spread over the whole GPU.
