@@ -25,9 +25,10 @@
 // the Linear scorer is instead a CUDA-core dot product over the same bf16
 // hi/lo weight rows, spread over one CTA per (head, group of 8 rows); the
 // MLP scorer likewise runs its few rows on the CUDA cores, one CTA per 8
-// hidden units and group of 8 rows. Both request kGemvBatch chunks of each
-// row per thread before the first product, so a thread keeps that many
-// weight and input loads in flight.
+// hidden units and group of 8 rows. The Linear path requests kGemvBatch
+// chunks of each row per thread before the first product; the MLP path
+// stages the rows' inputs in shared memory and requests a warp's weights a
+// piece (kMlpXPiece values) ahead.
 #include "kvp_common.cuh"
 
 namespace kvp {
@@ -398,16 +399,23 @@ __global__ void __launch_bounds__(kGemvThreads) score_gemv_kernel(const uint16_t
 }
 
 // KVzap-MLP scores of a few rows. CTA (g, r) takes hidden units 8g .. 8g + 7
-// and rows 8r .. 8r + 7; warp w computes unit 8g + w: its lanes take 8-value
-// chunks of k in a strided loop (u[t, j] = sum_k x[t, k] w1[j, k] in fp32),
-// the warp sums them, and lane t applies the bias and the exact GELU. The
-// CTA then writes part[g, t, h] = sum over its 8 units, in order, of
-// z[t, j] * w2[h, j]; mlp_reduce_kernel adds the groups' partials in order.
+// and rows 8r .. 8r + 7; warp w computes unit 8g + w (u[t, j] = sum_k x[t, k]
+// w1[j, k] in fp32), the warp sums its lanes, and lane t applies the bias and
+// the exact GELU. The CTA then writes part[g, t, h] = sum over its 8 units, in
+// order, of z[t, j] * w2[h, j]; mlp_reduce_warp_kernel adds the groups'
+// partials in order. The rows' x values pass through shared memory
+// kMlpXPiece at a time (one cooperative load for the CTA's 8 warps), and a
+// warp requests its w1 values for a piece in one go, the next piece's before
+// it uses the current one: 16-byte chunk c of a piece goes to lane c % 32.
+constexpr int kMlpXPiece = 2048;  // x values per row staged at a time
 __global__ void __launch_bounds__(kGemvThreads) score_mlp_gemv_kernel(const uint16_t* __restrict__ x, int64_t ld_x,
                                                                       int n_tok, int D, const uint16_t* __restrict__ w1,
                                                                       const float* __restrict__ b1,
                                                                       const uint16_t* __restrict__ w2, int hidden, int H,
                                                                       float* __restrict__ part) {
+  constexpr int kCh = kMlpXPiece / 8;  // 16-byte chunks of a row per piece
+  constexpr int kPer = kCh / 32;       // a lane's chunks per piece
+  __shared__ __align__(16) uint4 xs[kGemvRows][kCh];
   __shared__ float zs[kMlpGemvUnits][kGemvRows];
   const int g = blockIdx.x;
   const int r0 = blockIdx.y * kGemvRows;
@@ -419,27 +427,34 @@ __global__ void __launch_bounds__(kGemvThreads) score_mlp_gemv_kernel(const uint
 #pragma unroll
   for (int r = 0; r < kGemvRows; ++r) acc[r] = 0.f;
   const int nch = D / 8;
-  for (int c0 = lane; c0 < nch; c0 += 32 * kGemvBatch) {
-    uint4 a[kGemvBatch];
+  uint4 wa[kPer];
 #pragma unroll
-    for (int u = 0; u < kGemvBatch; ++u) {
-      const int c = c0 + 32 * u;
-      a[u] = c < nch ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
+  for (int u = 0; u < kPer; ++u) {
+    const int c = lane + 32 * u;
+    wa[u] = c < nch ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
+  }
+  for (int c0 = 0; c0 < nch; c0 += kCh) {
+    __syncthreads();  // every warp is done with the previous piece
+    for (int i = threadIdx.x; i < nr * kCh; i += kGemvThreads) {
+      const int r = i / kCh, c = i - r * kCh;
+      xs[r][c] = c0 + c < nch ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(r0 + r) * ld_x) + c0 + c)
+                              : make_uint4(0, 0, 0, 0);
     }
+    uint4 wn[kPer];  // the next piece's weights, in flight while this piece is used
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int c = c0 + kCh + lane + 32 * u;
+      wn[u] = c < nch ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
 #pragma unroll
     for (int r = 0; r < kGemvRows; ++r) {
       if (r < nr) {
-        uint4 xv[kGemvBatch];
 #pragma unroll
-        for (int u = 0; u < kGemvBatch; ++u) {
-          const int c = c0 + 32 * u;
-          xv[u] = c < nch ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(r0 + r) * ld_x) + c)
-                          : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < kGemvBatch; ++u) {
-          const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
-          const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+        for (int u = 0; u < kPer; ++u) {
+          const uint4 xv = xs[r][lane + 32 * u];
+          const uint32_t aw[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             acc[r] = fmaf(__uint_as_float(xw[i] << 16), __uint_as_float(aw[i] << 16), acc[r]);
@@ -448,6 +463,8 @@ __global__ void __launch_bounds__(kGemvThreads) score_mlp_gemv_kernel(const uint
         }
       }
     }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) wa[u] = wn[u];
   }
   float mine = 0.f;
 #pragma unroll
