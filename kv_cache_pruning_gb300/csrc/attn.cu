@@ -391,11 +391,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES + C::PS_BYTES) + warp * (kNst + 1);
   int* pref = reinterpret_cast<int*>(smem + C::RING_BYTES + C::PS_BYTES + C::BAR_BYTES);
 
-  // ---- page prefix over (b, h), identical in every CTA
+  // ---- page prefix over (b, h), identical in every CTA, and the last (b, h) with pages
+  __shared__ int s_last_bh;
   {
     __shared__ int wsum[kWarps];
+    __shared__ int wlast[kWarps];
     __shared__ int carry;
-    if (tid == 0) carry = 0;
+    if (tid == 0) {
+      carry = 0;
+      s_last_bh = 0;
+    }
     __syncthreads();
     for (int base = 0; base < BH; base += kThreads) {
       const int bh = base + tid;
@@ -407,16 +412,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
+      const int wl = __reduce_max_sync(0xffffffffu, np > 0 ? bh : -1);
       if (lane == 31) wsum[warp] = incl;
+      if (lane == 0) wlast[warp] = wl;
       __syncthreads();
       int before = carry;
       for (int w = 0; w < warp; ++w) before += wsum[w];
       if (bh < BH) pref[bh] = before + incl - np;
       __syncthreads();
       if (tid == 0) {
-        int t = 0;
-        for (int w = 0; w < kWarps; ++w) t += wsum[w];
+        int t = 0, lb = s_last_bh;
+        for (int w = 0; w < kWarps; ++w) {
+          t += wsum[w];
+          lb = max(lb, wlast[w]);
+        }
         carry += t;
+        s_last_bh = lb;
       }
       __syncthreads();
     }
@@ -441,17 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   const int NW = max(1, min(nw_all, NP / min_pages));
   const int gw = warp * gridDim.x + blockIdx.x;  // slices go round-robin over the CTAs (all SMs busy)
   if (gw >= NW) return;
-  int last_bh = 0;  // (b, h) of the last page
-  {
-    int a = 0, b = BH - 1;
-    while (a < b) {
-      const int mid = (a + b + 1) >> 1;
-      if (pref[mid] <= NP - 1) a = mid; else b = mid - 1;
-    }
-    last_bh = a;
-  }
+  const int last_bh = s_last_bh;  // (b, h) of the last page
   const int64_t c_end = 2 * static_cast<int64_t>(NP - 1) + static_cast<int64_t>(kBoundaryCost) * last_bh + 1;
-  auto slice_start = [&](int w) {  // first page of slice w: the first page whose cost reaches ceil(w * c_end / NW)
+  // first page of slice w: the first page whose cost reaches ceil(w * c_end / NW); a_out: the (b, h) searched
+  // to (that page's, or one before it with no pages)
+  auto slice_start = [&](int w, int& a_out) {
     const int64_t T = (static_cast<int64_t>(w) * c_end + NW - 1) / NW;
     auto maxc = [&](int k) {
       return 2 * static_cast<int64_t>(pref[k + 1] - 1) + static_cast<int64_t>(kBoundaryCost) * k;
@@ -463,20 +468,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
       if (maxc(mid) >= T) b = mid; else a = mid + 1;
     }
     const int64_t g = (T - static_cast<int64_t>(kBoundaryCost) * a + 1) / 2;
+    a_out = a;
     return static_cast<int>(min(static_cast<int64_t>(NP), max(static_cast<int64_t>(pref[a]), g)));
   };
-  const int r0 = slice_start(gw);
-  const int r1 = gw + 1 < NW ? slice_start(gw + 1) : NP;
+  // the slice's two ends on two lanes at once (a serial chain of integer work each)
+  int a_s = 0, r_s = NP;
+  if (lane == 0) r_s = slice_start(gw, a_s);
+  if (lane == 1 && gw + 1 < NW) r_s = slice_start(gw + 1, a_s);
+  const int r0 = __shfl_sync(0xffffffffu, r_s, 0);
+  const int r1 = __shfl_sync(0xffffffffu, r_s, 1);
   if (r1 <= r0) return;  // an empty slice (between two (b, h) with empty ones in between)
   const int n_my = r1 - r0;
 
-  // first (b, h) of the slice: the one whose page range holds page r0
-  int lo = 0, hi = BH - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pref[mid] <= r0) lo = mid; else hi = mid - 1;
-  }
-  int cbh = lo;  // consumer cursor
+  // first (b, h) of the slice: the one whose page range holds page r0 (the start's search ended at it or at
+  // a (b, h) with no pages before it)
+  int cbh = __shfl_sync(0xffffffffu, a_s, 0);  // consumer cursor
   while (pref[cbh + 1] <= r0) ++cbh;
 
   // Page ids of the slice, 32 per register: lane j of block b holds the id of
@@ -936,11 +942,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     prefetch_tmap(&tmV);
   }
 
-  // ---- page prefix over (b, h), identical in every CTA
+  // ---- page prefix over (b, h), identical in every CTA, and the last (b, h) with pages
+  __shared__ int s_last_bh;
   {
     __shared__ int wsum[kWarps];
+    __shared__ int wlast[kWarps];
     __shared__ int carry;
-    if (tid == 0) carry = 0;
+    if (tid == 0) {
+      carry = 0;
+      s_last_bh = 0;
+    }
     __syncthreads();
     for (int base = 0; base < BH; base += kThreads) {
       const int bh = base + tid;
@@ -952,16 +963,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
+      const int wl = __reduce_max_sync(0xffffffffu, np > 0 ? bh : -1);
       if (lane == 31) wsum[warp] = incl;
+      if (lane == 0) wlast[warp] = wl;
       __syncthreads();
       int before = carry;
       for (int w = 0; w < warp; ++w) before += wsum[w];
       if (bh < BH) pref[bh] = before + incl - np;
       __syncthreads();
       if (tid == 0) {
-        int t = 0;
-        for (int w = 0; w < kWarps; ++w) t += wsum[w];
+        int t = 0, lb = s_last_bh;
+        for (int w = 0; w < kWarps; ++w) {
+          t += wsum[w];
+          lb = max(lb, wlast[w]);
+        }
         carry += t;
+        s_last_bh = lb;
       }
       __syncthreads();
     }
@@ -986,17 +1003,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   const int NW = max(1, min(nw_all, NP / min_pages));
   const int gw = warp * gridDim.x + blockIdx.x;  // slices go round-robin over the CTAs (all SMs busy)
   if (gw >= NW) return;
-  int last_bh = 0;  // (b, h) of the last page
-  {
-    int a = 0, b = BH - 1;
-    while (a < b) {
-      const int mid = (a + b + 1) >> 1;
-      if (pref[mid] <= NP - 1) a = mid; else b = mid - 1;
-    }
-    last_bh = a;
-  }
+  const int last_bh = s_last_bh;  // (b, h) of the last page
   const int64_t c_end = 2 * static_cast<int64_t>(NP - 1) + static_cast<int64_t>(kBoundaryCost) * last_bh + 1;
-  auto slice_start = [&](int w) {  // first page of slice w: the first page whose cost reaches ceil(w * c_end / NW)
+  // first page of slice w: the first page whose cost reaches ceil(w * c_end / NW); a_out: the (b, h) searched
+  // to (that page's, or one before it with no pages)
+  auto slice_start = [&](int w, int& a_out) {
     const int64_t T = (static_cast<int64_t>(w) * c_end + NW - 1) / NW;
     auto maxc = [&](int k) {
       return 2 * static_cast<int64_t>(pref[k + 1] - 1) + static_cast<int64_t>(kBoundaryCost) * k;
@@ -1008,20 +1019,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
       if (maxc(mid) >= T) b = mid; else a = mid + 1;
     }
     const int64_t g = (T - static_cast<int64_t>(kBoundaryCost) * a + 1) / 2;
+    a_out = a;
     return static_cast<int>(min(static_cast<int64_t>(NP), max(static_cast<int64_t>(pref[a]), g)));
   };
-  const int r0 = slice_start(gw);
-  const int r1 = gw + 1 < NW ? slice_start(gw + 1) : NP;
+  // the slice's two ends on two lanes at once (a serial chain of integer work each)
+  int a_s = 0, r_s = NP;
+  if (lane == 0) r_s = slice_start(gw, a_s);
+  if (lane == 1 && gw + 1 < NW) r_s = slice_start(gw + 1, a_s);
+  const int r0 = __shfl_sync(0xffffffffu, r_s, 0);
+  const int r1 = __shfl_sync(0xffffffffu, r_s, 1);
   if (r1 <= r0) return;  // an empty slice (between two (b, h) with empty ones in between)
   const int n_my = r1 - r0;
 
-  // first (b, h) of the slice: the one whose page range holds page r0
-  int lo = 0, hi = BH - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pref[mid] <= r0) lo = mid; else hi = mid - 1;
-  }
-  int cbh = lo;  // consumer cursor
+  // first (b, h) of the slice: the one whose page range holds page r0 (the start's search ended at it or at
+  // a (b, h) with no pages before it)
+  int cbh = __shfl_sync(0xffffffffu, a_s, 0);  // consumer cursor
   while (pref[cbh + 1] <= r0) ++cbh;
 
   // Page ids of the slice, 32 per register: lane j of block b holds the id of
