@@ -343,23 +343,6 @@ KVP_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Loads 24 consecutive fp32 columns (16 + 8) of this warp's 32 TMEM lanes and waits for them.
-KVP_DEV void tmem_ld24(uint32_t taddr, float (&v)[24]) {
-  uint32_t r[24];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%24];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%25];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23])
-      : "r"(taddr), "r"(taddr + 16)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 24; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // Stores 16, 8 or 4 consecutive 32-bit columns of this warp's 32 TMEM lanes.
 KVP_DEV void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
@@ -392,30 +375,15 @@ KVP_DEV void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
   }
   if constexpr (N % 8 == 4) tmem_st4(taddr + c, r + c);
 }
-// Loads N (a multiple of 8) consecutive fp32 columns of this warp's 32 TMEM lanes and waits for them.
+// Loads N (a multiple of 16) consecutive fp32 columns of this warp's 32 TMEM lanes, waiting for each part.
 template <int N>
 KVP_DEV void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
-  static_assert(N % 8 == 0, "columns in eights");
-  if constexpr (N == 24) {
-    tmem_ld24(taddr, v);
-  } else {
-    int c = 0;
+  static_assert(N % 16 == 0, "columns in sixteens");
+  int c = 0;
 #pragma unroll
-    for (; c + 32 <= N; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<float(*)[32]>(&v[c]));
+  for (; c + 32 <= N; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<float(*)[32]>(&v[c]));
 #pragma unroll
-    for (; c + 16 <= N; c += 16) tmem_ld16(taddr + c, *reinterpret_cast<float(*)[16]>(&v[c]));
-    static_assert(N % 16 == 0 || N == 24, "a remainder of 8 columns only at N = 24");
-  }
-}
-
-// Stores 12 consecutive 32-bit columns (8 + 4) of this warp's 32 TMEM lanes.
-KVP_DEV void tmem_st12(uint32_t taddr, const uint32_t (&r)[12]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%2,%3,%4,%5,%6,%7,%8,%9};\n\t"
-      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%1], {%10,%11,%12,%13};" ::"r"(taddr),
-      "r"(taddr + 8), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11])
-      : "memory");
+  for (; c + 16 <= N; c += 16) tmem_ld16(taddr + c, *reinterpret_cast<float(*)[16]>(&v[c]));
 }
 
 // Stores 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (one row

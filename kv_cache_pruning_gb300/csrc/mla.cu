@@ -801,7 +801,7 @@ constexpr uint32_t kTcPOff = 0;                       // P at the start of its b
 constexpr uint32_t kTcOCol = kTcBufCol + kCBufs * kCTok;
 constexpr uint32_t kTcCols = 512;
 static_assert(kTcOCol + kCVals <= kTcCols, "tensor-memory plan");
-static_assert(kCHalf % 8 == 0 && kCTok % 16 == 0 && kCBoxRun % 1024 == 0 && kCVals % 64 == 0, "block tiling");
+static_assert(kCHalf % 16 == 0 && kCTok % 16 == 0 && kCBoxRun % 1024 == 0 && kCVals % 64 == 0, "block tiling");
 constexpr int kCRecOff = kCRing * kCStageBytes;                 // expire values of each stage's pages
 constexpr int kCBiasOff = kCRecOff + kCRing * kCTok * 4;        // per softmax warp: its tokens' mask as 0 / -inf
 constexpr int kCXchOff = kCBiasOff + kCSoftWarps * kCHalf * 4;  // [2][softmax warp][32]: row maxima, then sums
