@@ -193,6 +193,14 @@ KVP_DEV void tma_load_2d_multicast(void* dst, const void* tmap, int c0, int c1, 
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
       : "memory");
 }
+// 3-D tensor-map (TMA) load of one box at coordinates (c0 = innermost, c1, c2).
+KVP_DEV void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
 KVP_DEV void tma_load_2d_hint(void* dst, const void* tmap, int c0, int c1, uint64_t* bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
@@ -474,6 +482,25 @@ inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A row-major bf16 matrix [rows, cols] (cols a multiple of 64, row stride ld
+// elements) seen as [rows][cols / 64][64]: one box is box_rows consecutive rows
+// x every 64-column group, landing in shared memory as cols / 64 boxes of
+// box_rows x 128 bytes one after another (group-major), each with the 128-byte
+// swizzle. Dimension 1 (rows) has the larger stride; dimension 2 (the 64-column
+// group) steps 128 bytes.
+inline bool make_tmap_bf16_groups(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                                  int box_rows) {
+  auto fn = tmap_encode_fn();
+  if (fn == nullptr || cols % 64 != 0 || cols / 64 > 256) return false;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(cols / 64)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -7,9 +7,10 @@
 // rotary key) and takes the softmax-weighted sum of the rows' first 512
 // values. Every query head reads the same rows, so a page is worth
 // 16 tokens x (576 + 512) x 2 flops per head: on CUDA cores that outruns HBM
-// from a few heads on, so both products run on the tensor cores. Pages arrive
-// as nine 16-row x 64-column boxes each (tensor copies of the pool viewed as
-// [pages x 16, 576], with the 128-byte swizzle) plus the page's 16 expire
+// from a few heads on, so both products run on the tensor cores. A page lands
+// in shared memory as nine 16-row x 64-column boxes with the 128-byte swizzle
+// (the mma.sync kernels copy it whole, the pool seen as [rows][9][64]; the
+// tcgen05 kernel copies box by box, shared by a cluster) plus its 16 expire
 // values. Three kernels, by the number of query heads:
 //
 //   mla_decode_kernel (up to 32 heads): a CTA of 4 warps per (batch element,
@@ -87,8 +88,61 @@ struct MlaParams {
   int32_t* status;
 };
 
+// One page into a ring stage, issued by a whole warp with the same arguments
+// in every lane: lane 0 copies the page's nine swizzled 16 x 64 boxes with
+// one tensor copy (tmap_page views the pool as [rows][9][64], so the page's
+// 16 rows land box after box), lane 1 its 16 expire values. A copy
+// instruction takes about 100 ns of the SM's copy engine whatever its size,
+// so one 18 KB copy per page rather than nine 2 KB ones. An id outside the
+// pool (an inconsistent page table) makes no copy: the warp fills the stage
+// with zeros and the page's expire values with 0 (every slot gone) and lane
+// 0 arrives on the barrier.
+__device__ __forceinline__ void issue_page_warp(const void* tmap_page, uint8_t* dst, int32_t* rec, uint64_t* bar,
+                                                int phys, const MlaParams& p, int lane) {
+  if (phys < 0 || phys >= p.n_pages_cap) {
+    if (lane == 0) record_error(p.status, KVP_ERR_BOUNDS);
+    uint4* z = reinterpret_cast<uint4*>(dst);
+    for (int i = lane; i < kStageBytes / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+    if (lane < kPage) rec[lane] = 0;
+    fence_proxy_async();  // ordered before a later tensor copy into the stage
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+    return;
+  }
+  if (lane == 0) mbar_arrive_expect_tx(bar, kStageBytes + kPage * 4);
+  __syncwarp();
+  if (lane == 0)
+    tma_load_3d(dst, tmap_page, 0, phys * kPage, 0, bar);
+  else if (lane == 1)
+    bulk_g2s(rec, p.expire_pool + static_cast<int64_t>(phys) * kPage, kPage * 4, bar);
+}
+
+// The page ids of a slice for a warp that issues its pages in order: lane l
+// holds page 32 c + l of the current chunk c and of the next one, so an id
+// is a shuffle away and its load was made a chunk earlier (-1 past the slice).
+struct SlicePageIds {
+  const int32_t* row;  // the batch element's page-table row from the slice's first page
+  int n, lane, cur, nxt;
+  __device__ int load(int c) const {
+    const int k = 32 * c + lane;
+    return k < n ? row[k] : -1;
+  }
+  __device__ void start() {
+    cur = load(0);
+    nxt = load(1);
+  }
+  // page k's id; every lane calls it, for k = 0, 1, 2, ... in turn
+  __device__ int get(int k) {
+    if (k > 0 && (k & 31) == 0) {
+      cur = nxt;
+      nxt = load((k >> 5) + 1);
+    }
+    return __shfl_sync(0xffffffffu, cur, k & 31);
+  }
+};
+
 __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParams p,
-                                                                  const __grid_constant__ CUtensorMap tmL) {
+                                                                  const __grid_constant__ CUtensorMap tmPage) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   pdl_launch_dependents();
@@ -116,38 +170,23 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
   const int n_my = pg1 - pg0;
 
   if (tid == 0) {
-    prefetch_tmap(&tmL);
+    prefetch_tmap(&tmPage);
     for (int st = 0; st < kRingPages; ++st) mbar_init(&bars[st], 1);
     fence_mbar_init();
   }
   __syncthreads();
 
-  // Page k of the slice into stage k % kRingPages (thread 0).
+  // Page k of the slice into stage k % kRingPages (warp 0, every lane).
+  SlicePageIds ids{p.page_table + static_cast<int64_t>(b) * p.max_pages + pg0, n_my, lane, -1, -1};
   auto issue = [&](int k) {
     const int st = k % kRingPages;
-    uint8_t* dst = ring + st * kStageBytes;
-    int32_t* rec = rec_s + st * kPage;
-    const int phys = p.page_table[static_cast<int64_t>(b) * p.max_pages + pg0 + k];
-    if (phys < 0 || phys >= p.n_pages_cap) {
-      // inconsistent page table: no copy; the page reads as zeros and every
-      // slot of it as gone
-      record_error(p.status, KVP_ERR_BOUNDS);
-      uint4* z = reinterpret_cast<uint4*>(dst);
-      for (int i = 0; i < kStageBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
-      for (int i = 0; i < kPage; ++i) rec[i] = 0;
-      mbar_arrive(&bars[st]);
-      return;
-    }
-    fence_proxy_async();  // a zero fill of this stage by ordinary stores is ordered before the tensor copy
-    mbar_arrive_expect_tx(&bars[st], kStageBytes + kPage * 4);
-    const int y = phys * kPage;
-#pragma unroll
-    for (int j = 0; j < kBoxes; ++j) tma_load_2d(dst + j * kBoxBytes, &tmL, 64 * j, y, &bars[st]);
-    bulk_g2s(rec, p.expire_pool + static_cast<int64_t>(phys) * kPage, kPage * 4, &bars[st]);
+    issue_page_warp(&tmPage, ring + st * kStageBytes, rec_s + st * kPage, &bars[st], ids.get(k), p, lane);
   };
-  int issued = 0;  // pages issued so far (thread 0's count)
-  if (tid == 0)
+  int issued = 0;  // pages issued so far (warp 0's count)
+  if (warp == 0) {
+    ids.start();
     for (; issued < n_my && issued < kRingPages; ++issued) issue(issued);
+  }
 
   // ---- query rows of the tile as mma B fragments: thread (g, t) = (lane / 4,
   // lane % 4) holds, for k-step ks of this warp and n-tile nt, head
@@ -215,8 +254,9 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
       }
       return;  // outputs of this call are unspecified after a timeout
     }
-    if (tid == 0 && k >= 1 && issued < n_my) {  // page k - 1's stage takes the next page
-      fence_proxy_async();
+    if (warp == 0 && k >= 1 && issued < n_my) {  // page k - 1's stage takes the next page
+      if (lane == 0) fence_proxy_async();
+      __syncwarp();
       issue(issued);
       ++issued;
     }
@@ -490,7 +530,7 @@ static_assert(kTRecOff % 16 == 0 && kTQOff % 16 == 0 && kTPtOff % 16 == 0 && kTB
 static_assert(kTSmemBytes <= 232448, "shared memory budget");
 
 __global__ void __launch_bounds__(kTThreads, 1) mla_tile_kernel(const MlaParams p,
-                                                                const __grid_constant__ CUtensorMap tmL) {
+                                                                const __grid_constant__ CUtensorMap tmPage) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   pdl_launch_dependents();
@@ -526,7 +566,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mla_tile_kernel(const MlaParams 
     *reinterpret_cast<uint4*>(q_s + hl * kQRowBytes + c * 16) = v;
   }
   if (tid == 0) {
-    prefetch_tmap(&tmL);
+    prefetch_tmap(&tmPage);
     for (int st = 0; st < kTRing; ++st) {
       mbar_init(&full[st], 1);
       mbar_init(&empty[st], n_act);
@@ -537,31 +577,16 @@ __global__ void __launch_bounds__(kTThreads, 1) mla_tile_kernel(const MlaParams 
   __syncthreads();
   if (warp >= n_act) return;
 
-  // page k of the slice into stage k % kTRing (lane 0 of warp 0 only; the stage is free)
-  const bool filler = tid == 0;
+  // page k of the slice into stage k % kTRing (warp 0, every lane; the stage is free)
+  const bool filler = warp == 0;
+  SlicePageIds ids{p.page_table + static_cast<int64_t>(b) * p.max_pages + pg0, n_my, lane, -1, -1};
   auto issue = [&](int k) {
     const int st = k % kTRing;
-    uint8_t* dst = ring + st * kStageBytes;
-    int32_t* rec = rec_s + st * kPage;
-    const int phys = p.page_table[static_cast<int64_t>(b) * p.max_pages + pg0 + k];
-    if (phys < 0 || phys >= p.n_pages_cap) {
-      // inconsistent page table: no copy; the page reads as zeros and every slot of it as gone
-      record_error(p.status, KVP_ERR_BOUNDS);
-      uint4* z = reinterpret_cast<uint4*>(dst);
-      for (int i = 0; i < kStageBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
-      for (int i = 0; i < kPage; ++i) rec[i] = 0;
-      mbar_arrive(&full[st]);
-      return;
-    }
-    fence_proxy_async();
-    mbar_arrive_expect_tx(&full[st], kStageBytes + kPage * 4);
-    const int y = phys * kPage;
-#pragma unroll
-    for (int j = 0; j < kBoxes; ++j) tma_load_2d(dst + j * kBoxBytes, &tmL, 64 * j, y, &full[st]);
-    bulk_g2s(rec, p.expire_pool + static_cast<int64_t>(phys) * kPage, kPage * 4, &full[st]);
+    issue_page_warp(&tmPage, ring + st * kStageBytes, rec_s + st * kPage, &full[st], ids.get(k), p, lane);
   };
   int n_issued = 0;
   if (filler) {
+    ids.start();
     for (; n_issued < min(kTRing, n_my); ++n_issued) issue(n_issued);
   }
 
@@ -586,7 +611,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mla_tile_kernel(const MlaParams 
         record_error(p.status, KVP_ERR_TIMEOUT);
         *abort_flag = 1;
       }
-      if (filler) {
+      if (filler && lane == 0) {
         // the copies already issued land before the CTA's shared memory is released (each wait bounded again)
         for (int kk = k; kk < n_issued; ++kk) (void)mbar_wait(&full[kk % kTRing], (kk / kTRing) & 1u);
       }
@@ -690,12 +715,15 @@ __global__ void __launch_bounds__(kTThreads, 1) mla_tile_kernel(const MlaParams 
     __syncwarp();  // every lane is done with the stage and with pt_s
     if (lane == 0) mbar_arrive(&empty[st]);
     if (filler && n_issued < n_my && k >= 1) {
-      // refill the stage of page k - 1 once every warp has left it
+      // refill the stage of page k - 1 once every warp has left it (lane 0 waits for the warp)
       const int kr = k - 1;
-      if (mbar_wait(&empty[kr % kTRing], static_cast<uint32_t>((kr / kTRing) & 1), abort_flag, p.status)) {
+      bool freed = true;
+      if (lane == 0)
+        freed = mbar_wait(&empty[kr % kTRing], static_cast<uint32_t>((kr / kTRing) & 1), abort_flag, p.status);
+      if (__shfl_sync(0xffffffffu, freed ? 1 : 0, 0)) {
         issue(n_issued);
         ++n_issued;
-      } else {
+      } else if (lane == 0) {
         record_error(p.status, KVP_ERR_TIMEOUT);
         *abort_flag = 1;  // every warp leaves at its next wait; this one drains its copies there
       }
@@ -906,54 +934,70 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
 
   if (warp == kCCopyWarp) {
     // ------------------------------------------------------------ copies
-    if (lane == 0) {
-      int i = 0;
-      for (; i < nb; ++i) {
-        const int st = i % kCRing;
-        if (i >= kCRing &&
-            !mbar_wait(&empty[st], static_cast<uint32_t>((i / kCRing - 1) & 1), abort_flag, p.status)) {
+    // The whole warp issues, one copy per lane (a copy instruction holds its
+    // thread for about 100 ns): lane 3 pp + jj (pp < 6, jj < 3) copies box
+    // crank + 4 jj of page pp into all four CTAs, lane 18 + pp page pp's
+    // expire values into this one. Lane pp < 6 holds page pp of the block
+    // (-1: past the slice or a bad id), read a block ahead.
+    auto page_id = [&](int i) {
+      int ph = -1;
+      const int k = i * kCPages + lane;
+      if (lane < kCPages && i < nb && k < n_my) {
+        ph = p.page_table[static_cast<int64_t>(b) * p.max_pages + pg0 + k];
+        if (ph < 0 || ph >= p.n_pages_cap) {
+          record_error(p.status, KVP_ERR_BOUNDS);  // inconsistent page table: the page reads as gone
+          ph = -1;
+        }
+      }
+      return ph;
+    };
+    int ph_cur = page_id(0);
+    int i = 0;
+    bool okp = true;
+    for (; i < nb; ++i) {
+      const int st = i % kCRing;
+      bool okw = true;
+      if (lane == 0 && i >= kCRing)
+        okw = mbar_wait(&empty[st], static_cast<uint32_t>((i / kCRing - 1) & 1), abort_flag, p.status);
+      if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) {
+        if (lane == 0) {
           record_error(p.status, KVP_ERR_TIMEOUT);
           *abort_flag = 1;
-          break;
         }
-        uint8_t* stage = ring + st * kCStageBytes;
-        int32_t* rec = rec_s + st * kCTok;
-        int phys[kCPages];
-        int valid = 0;
-#pragma unroll
-        for (int pp = 0; pp < kCPages; ++pp) {
-          const int k = i * kCPages + pp;
-          int ph = -1;
-          if (k < n_my) {
-            ph = p.page_table[static_cast<int64_t>(b) * p.max_pages + pg0 + k];
-            if (ph < 0 || ph >= p.n_pages_cap) {
-              record_error(p.status, KVP_ERR_BOUNDS);  // inconsistent page table: the page reads as gone
-              ph = -1;
-            }
-          }
-          phys[pp] = ph;
-          valid += ph >= 0;
-          if (ph < 0) {
-            for (int t = 0; t < kPage; ++t) rec[pp * kPage + t] = 0;
-          }
-        }
+        okp = false;
+        break;
+      }
+      const int ph_nxt = page_id(i + 1);
+      uint8_t* stage = ring + st * kCStageBytes;
+      int32_t* rec = rec_s + st * kCTok;
+      if (lane < kCPages && ph_cur < 0) {
+        for (int tt = 0; tt < kPage; ++tt) rec[lane * kPage + tt] = 0;
+        fence_proxy_async();  // ordered before a later copy into the same place
+      }
+      const int valid = __popc(__ballot_sync(0xffffffffu, lane < kCPages && ph_cur >= 0));
+      __syncwarp();
+      if (lane == 0) {
         fence_proxy_async();
         mbar_arrive_expect_tx(&full[st], kCStageBytes + valid * kPage * 4);
-#pragma unroll
-        for (int pp = 0; pp < kCPages; ++pp) {
-          // a page past the slice (or a bad one) is read from past the pool's last row: zeros
-          const int y = (phys[pp] >= 0 ? phys[pp] : p.n_pages_cap) * kPage;
-          // this CTA copies boxes crank, crank + 4, ... of the page into all four CTAs of the cluster
-          for (int j = static_cast<int>(crank); j < kBoxes; j += kCParts)
-            tma_load_2d_multicast(stage + j * kCBoxRun + pp * kBoxBytes, &tmL, 64 * j, y, &full[st], kCAllCtas);
-          if (phys[pp] >= 0)
-            bulk_g2s(rec + pp * kPage, p.expire_pool + static_cast<int64_t>(phys[pp]) * kPage, kPage * 4, &full[st]);
-        }
       }
-      if (*abort_flag) {
-        // the copies already issued land before the CTA's shared memory is released (each wait bounded again)
-        for (int kk = max(0, i - kCRing); kk < i; ++kk) (void)mbar_wait(&full[kk % kCRing], (kk / kCRing) & 1u);
+      __syncwarp();
+      const int src = lane < 3 * kCPages ? lane / 3 : (lane < 4 * kCPages ? lane - 3 * kCPages : 0);
+      const int ph = __shfl_sync(0xffffffffu, ph_cur, src);
+      // a page past the slice (or a bad one) is read from past the pool's last row: zeros
+      const int y = (ph >= 0 ? ph : p.n_pages_cap) * kPage;
+      if (lane < 3 * kCPages) {
+        const int pp = lane / 3, j = static_cast<int>(crank) + kCParts * (lane % 3);
+        if (j < kBoxes)
+          tma_load_2d_multicast(stage + j * kCBoxRun + pp * kBoxBytes, &tmL, 64 * j, y, &full[st], kCAllCtas);
+      } else if (lane < 4 * kCPages && ph >= 0) {
+        const int pp = lane - 3 * kCPages;
+        bulk_g2s(rec + pp * kPage, p.expire_pool + static_cast<int64_t>(ph) * kPage, kPage * 4, &full[st]);
       }
+      ph_cur = ph_nxt;
+    }
+    if (!okp && lane == 0) {
+      // the copies already issued land before the CTA's shared memory is released (each wait bounded again)
+      for (int kk = max(0, i - kCRing); kk < i; ++kk) (void)mbar_wait(&full[kk % kCRing], (kk / kCRing) & 1u);
     }
     __syncwarp();
   } else if (warp == kCMmaWarp) {
@@ -1269,9 +1313,13 @@ extern "C" kvp_status kvp_decode_attn_mla(int batch, int n_q_heads, int latent_d
                ? KVP_OK
                : KVP_ERR_CUDA;
   }
+  // the tensor-core kernel copies 16 x 64 boxes; the others a page (16 rows x nine 64-column groups) at a time
   CUtensorMap tmL;
-  if (!make_tmap_bf16(&tmL, pool, static_cast<int64_t>(n_pages_cap) * kPage, kRow, kRow, kPage, 64))
-    return KVP_ERR_CUDA;
+  const bool ok_map = path == kPathTc
+                          ? make_tmap_bf16(&tmL, pool, static_cast<int64_t>(n_pages_cap) * kPage, kRow, kRow, kPage, 64)
+                          : make_tmap_bf16_groups(&tmL, pool, static_cast<int64_t>(n_pages_cap) * kPage, kRow, kRow,
+                                                  kPage);
+  if (!ok_map) return KVP_ERR_CUDA;
   static const bool attr_ok =
       cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ==
           cudaSuccess &&
