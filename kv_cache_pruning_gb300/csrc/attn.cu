@@ -19,7 +19,7 @@
 // bumps the (b, h)'s counter; the warp that brings the counter to the number
 // of pieces merges them (log-sum-exp in fp32) and resets the counter. Nothing
 // ever waits on another warp.
-#include <cuda_fp8.h>
+#include <cuda_fp16.h>
 
 #include "kvp_common.cuh"
 
@@ -98,9 +98,8 @@ KVP_DEV void unpack_e4m3_8(uint32_t x, uint32_t y, float (&f)[8]) {
   for (int h = 0; h < 2; ++h) {
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const __nv_fp8x2_storage_t pr = static_cast<__nv_fp8x2_storage_t>((w[h] >> (16 * q)) & 0xFFFFu);
-      const __half2 hh = __half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3));
-      const float2 ff = __half22float2(hh);
+      const uint32_t h2 = cvt_e4m3x2_to_f16x2(w[h] >> (16 * q));
+      const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&h2));
       f[4 * h + 2 * q] = ff.x;
       f[4 * h + 2 * q + 1] = ff.y;
     }
@@ -904,11 +903,6 @@ struct MmaCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// two E4M3 codes (low byte first) -> fp16x2, exactly
-KVP_DEV uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
 KVP_DEV uint32_t bf16x2_to_f16x2(uint32_t w) {
   const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -1207,16 +1201,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
       for (int i = 0; i < NCH; ++i) {
         const int ci = lane + 32 * i, r = ci / CPR, c = ci - r * CPR;
         const uint2 kc = *reinterpret_cast<const uint2*>(stg + C::QK_OFF + r * D + c * 8);
-        const uint4 h = make_uint4(e4m3x2_to_f16x2(kc.x), e4m3x2_to_f16x2(kc.x >> 16), e4m3x2_to_f16x2(kc.y),
-                                   e4m3x2_to_f16x2(kc.y >> 16));
+        const uint4 h = make_uint4(cvt_e4m3x2_to_f16x2(kc.x), cvt_e4m3x2_to_f16x2(kc.x >> 16),
+                                   cvt_e4m3x2_to_f16x2(kc.y), cvt_e4m3x2_to_f16x2(kc.y >> 16));
         *reinterpret_cast<uint4*>(stg + (c >> 3) * C::BOX_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = h;
       }
       __syncwarp();  // every lane has read its K codes, which the V boxes overwrite
 #pragma unroll
       for (int i = 0; i < NCH; ++i) {
         const int ci = lane + 32 * i, r = ci / CPR, c = ci - r * CPR;
-        const uint4 h = make_uint4(e4m3x2_to_f16x2(vc[i].x), e4m3x2_to_f16x2(vc[i].x >> 16),
-                                   e4m3x2_to_f16x2(vc[i].y), e4m3x2_to_f16x2(vc[i].y >> 16));
+        const uint4 h = make_uint4(cvt_e4m3x2_to_f16x2(vc[i].x), cvt_e4m3x2_to_f16x2(vc[i].x >> 16),
+                                   cvt_e4m3x2_to_f16x2(vc[i].y), cvt_e4m3x2_to_f16x2(vc[i].y >> 16));
         *reinterpret_cast<uint4*>(stg + C::PAGE_BYTES + (c >> 3) * C::BOX_BYTES + r * 128 +
                                   (((c & 7) ^ (r & 7)) << 4)) = h;
       }
@@ -1528,6 +1522,7 @@ kvp_status dispatch_mma(const AttnParams& p, int G, int grid_limit, cudaStream_t
   const int64_t rows = static_cast<int64_t>(p.n_pages_cap) * kPage;
   if (!make_tmap_bf16(&tmK, p.k_pool, rows, D, D, kPage, 64) || !make_tmap_bf16(&tmV, p.v_pool, rows, D, D, kPage, 64))
     return KVP_ERR_CUDA;
+  if (G == 4) return launch_attn_mma<D, 4, kQ>(p, tmK, tmV, grid_limit, st);
   if (G != 8) return KVP_ERR_UNSUPPORTED;
   return launch_attn_mma<D, 8, kQ>(p, tmK, tmV, grid_limit, st);
 }
@@ -1645,11 +1640,14 @@ kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_d
   // Eight query heads per kv head go to the tensor-core kernel: with the
   // CUDA-core page math a page takes twice the multiply-adds of G = 4 and the
   // kernel is bound by instruction issue (measured on a GB300, Llama-3-8B
-  // cache, keep-all: 192 against 95 us). Up to four the CUDA-core kernel is as
-  // fast or faster (75 % pruned at G = 4: 34.1 against 34.5 us; the fp8 tier:
-  // 65 against 69 us at a quarter of the entries). The tensor-core kernel reads
-  // the pools through tensor maps, whose row coordinates stay below 2^31.
-  const bool mma = G == 8 && n_pages_cap > 0 && static_cast<int64_t>(n_pages_cap) * kPage <= 0x7fffffff;
+  // cache, keep-all: 192 against 95 us). So do four with an fp8 tier (the same
+  // cache, a quarter / half / three quarters of the entries in the fp8 tier:
+  // 61.1 / 85.1 / 108.5 against 64.6 / 91.0 / 116.8 us). Otherwise up to four
+  // the CUDA-core kernel is as fast or faster (75 % pruned at G = 4: 34.1
+  // against 34.5 us). The tensor-core kernel reads the pools through tensor
+  // maps, whose row coordinates stay below 2^31.
+  const bool mma = (G == 8 || (G == 4 && qt != nullptr)) && n_pages_cap > 0 &&
+                   static_cast<int64_t>(n_pages_cap) * kPage <= 0x7fffffff;
   if (qt != nullptr) {
     if (mma)
       return head_dim == 128 ? dispatch_mma<128, true>(p, G, grid_limit, st) : dispatch_mma<64, true>(p, G, grid_limit, st);

@@ -23,7 +23,6 @@
 #include <mutex>
 #include <type_traits>
 
-#include <cuda_fp8.h>
 
 #include "kvp_common.cuh"
 
@@ -677,10 +676,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
           const float inv = __fdiv_rn(448.f, amax);
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
-            float2 pr;
-            pr.x = __fmul_rn(f[e], inv);
-            pr.y = __fmul_rn(f[e + 1], inv);
-            const uint32_t c2 = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3));
+            const uint32_t c2 = cvt_f32x2_to_e4m3x2(__fmul_rn(f[e], inv), __fmul_rn(f[e + 1], inv));
             packed[e >> 2] |= c2 << (16 * ((e >> 1) & 1));
           }
         }
@@ -828,10 +824,7 @@ __global__ void __launch_bounds__(256) append_quant_kernel(int mode, int BH, int
       const float inv = __fdiv_rn(448.f, amax);
 #pragma unroll
       for (int e = 0; e < EPL; e += 2) {
-        float2 pr;
-        pr.x = __fmul_rn(f[e], inv);
-        pr.y = __fmul_rn(f[e + 1], inv);
-        packed |= static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3)) << (8 * e);
+        packed |= cvt_f32x2_to_e4m3x2(__fmul_rn(f[e], inv), __fmul_rn(f[e + 1], inv)) << (8 * e);
       }
     }
     uint8_t* dst = (w ? vq_pool : kq_pool) + row * D + lane * EPL;

@@ -452,6 +452,24 @@ KVP_DEV float ex2_approx(float x) {
   return y;
 }
 
+// ---------------------------------------------------------------- E4M3 conversions
+// Two E4M3 codes (the first in the low byte of `two`) to two fp16 values (the
+// first in the low half), exactly: every E4M3 value is an fp16 value. One PTX
+// conversion instruction (cvt.rn.f16x2.e4m3x2).
+KVP_DEV uint32_t cvt_e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(two & 0xFFFFu)));
+  return r;
+}
+// Two fp32 values to E4M3 codes, rounded to nearest (ties to even) and
+// saturated to +-448, `lo` in the low byte. One PTX conversion instruction
+// (cvt.rn.satfinite.e4m3x2.f32, whose first source fills the high byte).
+KVP_DEV uint32_t cvt_f32x2_to_e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // ---------------------------------------------------------------- bf16 helpers
 KVP_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 KVP_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -813,6 +813,7 @@ def _two_tier_case(kvp, B, T, H, G, d, pps=0, now=None, seed=17, empty_q=False):
     (2, 1500, 2, 8, 128, 0),
     (3, 777, 3, 2, 64, 1),
     (7, 3333, 5, 4, 128, 2),
+    (2, 1500, 4, 4, 64, 0),      # G = 4 at head_dim 64 (the tensor-core kernel with one 64-column box per row)
 ])
 def test_decode_attn_two_tier(kvp, B, T, H, G, d, pps):
     out, ref, _ = _two_tier_case(kvp, B, T, H, G, d, pps=pps)
