@@ -891,7 +891,10 @@ struct MmaCfg {
   static constexpr int RING_BYTES = kWarps * kNst * STAGE_BYTES;
   static constexpr int REC_WORDS = 3 * kPage;            // per stage: the page's 16 expire values
   static constexpr int REC_BYTES = kWarps * kNst * REC_WORDS * 4;
-  static constexpr int PT_BYTES = kWarps * 2 * 8 * kPage * 2;  // per warp: P^T hi and lo, 8 heads x 16 tokens, bf16
+  // per warp: P^T hi and lo, 8 heads x 16 tokens, bf16; a head's row padded to kPtRow halves so that the
+  // stores (lanes 4 apart in heads) and the 32-bit reads (8 heads x 4 token pairs) fall on distinct banks
+  static constexpr int kPtRow = 24;
+  static constexpr int PT_BYTES = kWarps * 2 * 8 * kPtRow * 2;
   static constexpr int BAR_BYTES = kWarps * (kNst + 1) * 8;
   static constexpr int PREF_BYTES = (kMaxBH + 1) * 4;
   static constexpr int SMEM = 1024 + RING_BYTES + REC_BYTES + PT_BYTES + BAR_BYTES + PREF_BYTES;
@@ -928,7 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   const int BH = p.B * p.H;
   uint8_t* ring = smem + warp * kNst * C::STAGE_BYTES;
   int32_t* exp_s = reinterpret_cast<int32_t*>(smem + C::RING_BYTES) + warp * kNst * C::REC_WORDS;
-  uint16_t* pt_s = reinterpret_cast<uint16_t*>(smem + C::RING_BYTES + C::REC_BYTES) + warp * 2 * 8 * kPage;
+  uint16_t* pt_s = reinterpret_cast<uint16_t*>(smem + C::RING_BYTES + C::REC_BYTES) + warp * 2 * 8 * C::kPtRow;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES + C::REC_BYTES + C::PT_BYTES) + warp * (kNst + 1);
   int* pref = reinterpret_cast<int*>(smem + C::RING_BYTES + C::REC_BYTES + C::PT_BYTES + C::BAR_BYTES);
   if (tid == 0) {
@@ -1333,14 +1336,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
         hb = __bfloat16_as_ushort(hi);
         lb = __bfloat16_as_ushort(lo);
       }
-      pt_s[(2 * tq + (i & 1)) * kPage + tok[i]] = hb;
-      pt_s[8 * kPage + (2 * tq + (i & 1)) * kPage + tok[i]] = lb;
+      pt_s[(2 * tq + (i & 1)) * C::kPtRow + tok[i]] = hb;
+      pt_s[8 * C::kPtRow + (2 * tq + (i & 1)) * C::kPtRow + tok[i]] = lb;
     }
     __syncwarp();
-    const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPage + 2 * tq);
-    const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPage + 8 + 2 * tq);
-    const uint32_t pl0 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPage + gq * kPage + 2 * tq);
-    const uint32_t pl1 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPage + gq * kPage + 8 + 2 * tq);
+    const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pt_s + gq * C::kPtRow + 2 * tq);
+    const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pt_s + gq * C::kPtRow + 8 + 2 * tq);
+    const uint32_t pl0 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * C::kPtRow + gq * C::kPtRow + 2 * tq);
+    const uint32_t pl1 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * C::kPtRow + gq * C::kPtRow + 8 + 2 * tq);
 
     // ---- O^T += V^T P^T
 #pragma unroll

@@ -53,8 +53,11 @@ constexpr int kBoxBytes = kPage * 128;        // 16 rows x 128 bytes
 constexpr int kStageBytes = kBoxes * kBoxBytes;
 constexpr int kKsW = kRow / 16 / kMW;         // k-steps of the logits per warp
 constexpr int kMtW = kDc / 16 / kMW;          // m-tiles of the output per warp
-constexpr int kSpartFloats = 32 * 8;          // one warp's partial logits (8 per lane)
-constexpr int kPtHalves = 2 * 2 * 8 * kPage;  // one warp's P^T: n-tile x (hi, lo) x 8 heads x 16 tokens
+constexpr int kSpartFloats = 32 * 8;          // one warp's partial logits (8 per lane, as two planes of float4)
+// A head's row of P^T in shared memory: 16 tokens and 8 halves of padding, so that the stores (lanes
+// 4 apart in heads) and the 32-bit reads (8 heads x 4 token pairs) fall on distinct banks
+constexpr int kPtRow = 24;
+constexpr int kPtHalves = 2 * 2 * 8 * kPtRow;  // one warp's P^T: n-tile x (hi, lo) x 8 heads x kPtRow
 // The running maximum is raised only when a logit exceeds it by more than
 // this (base 2), so p stays below 2^8 and most pages skip the reduction.
 constexpr float kLazyRescale = 8.0f;
@@ -240,9 +243,10 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
       mma_bf16_16816(sacc[1], a0, a1, a2, a3, qf[i][1][0], qf[i][1][1]);
     }
     float* sp = spart + (k & 1) * (kMW * kSpartFloats);  // two buffers: page k + 1 writes the other
-    *reinterpret_cast<float4*>(sp + warp * kSpartFloats + lane * 8) =
+    // plane nt holds every lane's float4 of n-tile nt side by side: a warp's access is 512 contiguous bytes
+    *reinterpret_cast<float4*>(sp + warp * kSpartFloats + lane * 4) =
         make_float4(sacc[0][0], sacc[0][1], sacc[0][2], sacc[0][3]);
-    *reinterpret_cast<float4*>(sp + warp * kSpartFloats + lane * 8 + 4) =
+    *reinterpret_cast<float4*>(sp + warp * kSpartFloats + 128 + lane * 4) =
         make_float4(sacc[1][0], sacc[1][1], sacc[1][2], sacc[1][3]);
     // every partial is written; every warp is done with page k - 1's stage
     if (__syncthreads_or(!ok)) {
@@ -266,8 +270,8 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
     float sv[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int w = 0; w < kMW; ++w) {
-      const float4 u0 = *reinterpret_cast<const float4*>(sp + w * kSpartFloats + lane * 8);
-      const float4 u1 = *reinterpret_cast<const float4*>(sp + w * kSpartFloats + lane * 8 + 4);
+      const float4 u0 = *reinterpret_cast<const float4*>(sp + w * kSpartFloats + lane * 4);
+      const float4 u1 = *reinterpret_cast<const float4*>(sp + w * kSpartFloats + 128 + lane * 4);
       sv[0][0] += u0.x;
       sv[0][1] += u0.y;
       sv[0][2] += u0.z;
@@ -332,8 +336,8 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
         const __nv_bfloat16 hi = __float2bfloat16_rn(pf[i]);
         const __nv_bfloat16 lo = __float2bfloat16_rn(pf[i] - __bfloat162float(hi));
         const int hrow = 2 * tq + (i & 1);
-        pt_s[((nt * 2 + 0) * 8 + hrow) * kPage + tok[i]] = __bfloat16_as_ushort(hi);
-        pt_s[((nt * 2 + 1) * 8 + hrow) * kPage + tok[i]] = __bfloat16_as_ushort(lo);
+        pt_s[((nt * 2 + 0) * 8 + hrow) * kPtRow + tok[i]] = __bfloat16_as_ushort(hi);
+        pt_s[((nt * 2 + 1) * 8 + hrow) * kPtRow + tok[i]] = __bfloat16_as_ushort(lo);
       }
     }
     __syncwarp();
@@ -341,8 +345,8 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
     uint32_t pb[2][2], pl[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const uint16_t* hi_row = pt_s + ((nt * 2 + 0) * 8 + gq) * kPage;
-      const uint16_t* lo_row = pt_s + ((nt * 2 + 1) * 8 + gq) * kPage;
+      const uint16_t* hi_row = pt_s + ((nt * 2 + 0) * 8 + gq) * kPtRow;
+      const uint16_t* lo_row = pt_s + ((nt * 2 + 1) * 8 + gq) * kPtRow;
       pb[nt][0] = *reinterpret_cast<const uint32_t*>(hi_row + 2 * tq);
       pb[nt][1] = *reinterpret_cast<const uint32_t*>(hi_row + 8 + 2 * tq);
       pl[nt][0] = *reinterpret_cast<const uint32_t*>(lo_row + 2 * tq);
@@ -523,7 +527,7 @@ constexpr int kTRingOff = 0;
 constexpr int kTRecOff = kTRingOff + kTRing * kStageBytes;
 constexpr int kTQOff = kTRecOff + kTRing * kPage * 4;
 constexpr int kTPtOff = kTQOff + kTHeads * kQRowBytes;
-constexpr int kTBarOff = kTPtOff + kTWarps * 2 * 8 * kPage * 2;
+constexpr int kTBarOff = kTPtOff + kTWarps * 2 * 8 * kPtRow * 2;
 constexpr int kTSmemUsed = kTBarOff + 2 * kTRing * 8 + 16;
 constexpr int kTSmemBytes = 1024 + kTSmemUsed;
 static_assert(kTRecOff % 16 == 0 && kTQOff % 16 == 0 && kTPtOff % 16 == 0 && kTBarOff % 8 == 0, "alignment");
@@ -595,7 +599,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mla_tile_kernel(const MlaParams 
   // query B fragments of two k-steps per ldmatrix.x4: matrix m = (k-step ks + m / 2, values 8 (m & 1) ..),
   // row = head 8 warp + ri
   const uint32_t qaddr = smem_u32(q_s) + (8 * warp + ri) * kQRowBytes + (mi >> 1) * 32 + (mi & 1) * 16;
-  uint16_t* pt_s = reinterpret_cast<uint16_t*>(smem + kTPtOff) + warp * 2 * 8 * kPage;
+  uint16_t* pt_s = reinterpret_cast<uint16_t*>(smem + kTPtOff) + warp * 2 * 8 * kPtRow;
   const uint32_t ring_u32 = smem_u32(ring);
 
   float m2[2] = {-1e30f, -1e30f}, l2[2] = {0.f, 0.f};
@@ -691,14 +695,14 @@ __global__ void __launch_bounds__(kTThreads, 1) mla_tile_kernel(const MlaParams 
     for (int i = 0; i < 4; ++i) {
       const __nv_bfloat16 hi = __float2bfloat16_rn(pf[i]);
       const __nv_bfloat16 lo = __float2bfloat16_rn(pf[i] - __bfloat162float(hi));
-      pt_s[(2 * tq + (i & 1)) * kPage + tok[i]] = __bfloat16_as_ushort(hi);
-      pt_s[8 * kPage + (2 * tq + (i & 1)) * kPage + tok[i]] = __bfloat16_as_ushort(lo);
+      pt_s[(2 * tq + (i & 1)) * kPtRow + tok[i]] = __bfloat16_as_ushort(hi);
+      pt_s[8 * kPtRow + (2 * tq + (i & 1)) * kPtRow + tok[i]] = __bfloat16_as_ushort(lo);
     }
     __syncwarp();
-    const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPage + 2 * tq);
-    const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPage + 8 + 2 * tq);
-    const uint32_t pl0 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPage + gq * kPage + 2 * tq);
-    const uint32_t pl1 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPage + gq * kPage + 8 + 2 * tq);
+    const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPtRow + 2 * tq);
+    const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pt_s + gq * kPtRow + 8 + 2 * tq);
+    const uint32_t pl0 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPtRow + gq * kPtRow + 2 * tq);
+    const uint32_t pl1 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * kPtRow + gq * kPtRow + 8 + 2 * tq);
 
     // ---- O^T += Cv^T P^T over all 512 compressed values
 #pragma unroll
