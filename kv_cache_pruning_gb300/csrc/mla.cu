@@ -229,7 +229,8 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
     const uint32_t base = ring_u32 + st * kStageBytes;
 
     // ---- partial logits over this warp's 144 values
-    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // two independent partial sums per n-tile (even and odd k-steps), so the products do not form one chain
+    float sacc2[2][2][4] = {};
 #pragma unroll
     for (int i = 0; i < kKsW; ++i) {
       const int ks = warp * kKsW + i;
@@ -239,9 +240,14 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const MlaParam
       const uint32_t addr = base + (ks >> 2) * kBoxBytes + r * 128 + ((chunk ^ (r & 7)) << 4);
       uint32_t a0, a1, a2, a3;
       ldsm_x4(addr, a0, a1, a2, a3);
-      mma_bf16_16816(sacc[0], a0, a1, a2, a3, qf[i][0][0], qf[i][0][1]);
-      mma_bf16_16816(sacc[1], a0, a1, a2, a3, qf[i][1][0], qf[i][1][1]);
+      mma_bf16_16816(sacc2[0][i & 1], a0, a1, a2, a3, qf[i][0][0], qf[i][0][1]);
+      mma_bf16_16816(sacc2[1][i & 1], a0, a1, a2, a3, qf[i][1][0], qf[i][1][1]);
     }
+    float sacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[nt][e] = sacc2[nt][0][e] + sacc2[nt][1][e];
     float* sp = spart + (k & 1) * (kMW * kSpartFloats);  // two buffers: page k + 1 writes the other
     // plane nt holds every lane's float4 of n-tile nt side by side: a warp's access is 512 contiguous bytes
     *reinterpret_cast<float4*>(sp + warp * kSpartFloats + lane * 4) =
