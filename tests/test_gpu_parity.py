@@ -491,7 +491,9 @@ def test_compact_quant_bit_exact(kvp, B, T, H, d, reserve, window, strided):
 
 def test_compact_quant_special_rows(kvp):
     """All-zero rows (scale 0, codes 0), rows with one huge element (everything
-    else in the subnormal range) and exact ties on the E4M3 grid."""
+    else in the subnormal range), exact ties on the E4M3 grid, and rows at
+    scale exactly 1 that hold every finite E4M3 value (codes 0..126 and
+    129..254), so that each code's encoding is compared once."""
     B, T, H, d = 1, 64, 2, 128
     rng = np.random.default_rng(5)
     kf = rng.standard_normal((B, T, H, d)).astype(np.float32)
@@ -502,6 +504,12 @@ def test_compact_quant_special_rows(kvp):
     mids = np.resize(((grid[:-1] + grid[1:]) / 2)[20:], d - 1)
     kf[0, 2, :, 0] = 448.0                            # scale exactly 1: the others are exact ties
     kf[0, 2, :, 1:] = mids
+    full = orc.e4m3_positive_values()[:127]           # codes 0..126 (0 .. 448)
+    kf[0, 3, :, :127] = full                          # scale 1 (amax 448): every code is its own value
+    kf[0, 3, :, 127] = 448.0
+    kf[0, 4, :, :126] = -full[1:]                     # codes 129..254
+    kf[0, 4, :, 126] = 448.0
+    kf[0, 4, :, 127] = 1.0
     k = syn.f32_to_bf16_bits(kf)
     v = syn.f32_to_bf16_bits(kf[:, ::-1].copy())
     s = np.zeros((B, T, H), np.float32)
