@@ -651,42 +651,69 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
     cp_async_wait_all();
     __syncwarp();
     if constexpr (kQuant) {
-      // each row's E16 / 2 lanes: amax over the row, scale = amax / 448 and
-      // inv = 448 / amax (IEEE divisions), every element times inv rounded to
-      // E4M3 (saturating); the lanes of a row store 8 codes each, its first
-      // lane the scale
+      // Three steps per batch. (1) Each row's amax, reduced over its E16 / 2
+      // lanes and gathered so that lane i holds entry i's K and V maxima.
+      // (2) Lane i takes entry i's scales amax / 448 and inverses 448 / amax
+      // (IEEE divisions) and stores the scales: the divisions run once per
+      // batch rather than once per warp instruction. (3) Every element times
+      // its row's inverse, rounded to E4M3 (saturating), 8 codes per lane; a
+      // row whose amax is 0 stores zero codes.
+      static_assert(kSt <= 32, "one entry per lane in the scale step");
+      constexpr int kRowLanes = E16 / 2;
       uint8_t* qbase = reinterpret_cast<uint8_t*>(dbase);
+      float amk = 0.f, amv = 0.f;  // lane i: entry i's K and V row maxima
+#pragma unroll 4
       for (int ib = 0; ib < nb; ib += EPI) {
         const int i = ib + sub;
-        const bool act = i < nb;  // the warp's lanes all take part in the reduction
-        const uint4 w = act ? stage[i * E16 + piece] : make_uint4(0, 0, 0, 0);
-        float f[8];
-        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x);
-        f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
-        f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z);
-        f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+        const uint4 w = i < nb ? stage[i * E16 + piece] : make_uint4(0, 0, 0, 0);
+        const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                            bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
         float amax = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
 #pragma unroll
-        for (int o = 1; o < E16 / 2; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float scale = __fdiv_rn(amax, 448.f);
-        uint32_t packed[2] = {0u, 0u};
-        if (amax > 0.f) {
-          const float inv = __fdiv_rn(448.f, amax);
+        for (int o = 1; o < kRowLanes; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const uint32_t c2 = cvt_f32x2_to_e4m3x2(__fmul_rn(f[e], inv), __fmul_rn(f[e + 1], inv));
-            packed[e >> 2] |= c2 << (16 * ((e >> 1) & 1));
+        for (int e = 0; e < EPI; ++e) {
+          const float ak = __shfl_sync(0xffffffffu, amax, e * E16);
+          const float av = __shfl_sync(0xffffffffu, amax, e * E16 + kRowLanes);
+          if (lane == ib + e) {
+            amk = ak;
+            amv = av;
           }
         }
-        if (act) {
+      }
+      float ik = -1.f, iv = -1.f;  // the inverses; -1: amax 0, zero codes
+      if (lane < nb) {
+        const int j = slot0 + i0 + lane;
+        float* meta = reinterpret_cast<float*>(expire_pool) + static_cast<int64_t>(base + (j >> 4)) * kMetaStride +
+                      (j & 15);
+        meta[kPage] = __fdiv_rn(amk, 448.f);
+        meta[2 * kPage] = __fdiv_rn(amv, 448.f);
+        if (amk > 0.f) ik = __fdiv_rn(448.f, amk);
+        if (amv > 0.f) iv = __fdiv_rn(448.f, amv);
+      }
+#pragma unroll 4
+      for (int ib = 0; ib < nb; ib += EPI) {
+        const int i = ib + sub;
+        const float ink = __shfl_sync(0xffffffffu, ik, i & 31);
+        const float inv_v = __shfl_sync(0xffffffffu, iv, i & 31);
+        if (i < nb) {
+          const float inv = is_v ? inv_v : ink;
+          const uint4 w = stage[i * E16 + piece];
+          const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                              bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+          uint32_t packed[2] = {0u, 0u};
+          if (inv >= 0.f) {
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const uint32_t c2 = cvt_f32x2_to_e4m3x2(__fmul_rn(f[e], inv), __fmul_rn(f[e + 1], inv));
+              packed[e >> 2] |= c2 << (16 * ((e >> 1) & 1));
+            }
+          }
           const int j = slot0 + i0 + i;
           const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
           reinterpret_cast<uint2*>(qbase + row * D)[vi] = make_uint2(packed[0], packed[1]);
-          if (vi == 0)
-            reinterpret_cast<float*>(expire_pool)[static_cast<int64_t>(base + (j >> 4)) * kMetaStride +
-                                                  (is_v ? 2 : 1) * kPage + (j & 15)] = scale;
         }
       }
     } else {
