@@ -503,7 +503,9 @@ KVP_API kvp_status kvp_decode_attn_devpos(int batch, int n_q_heads, int n_kv_hea
  * workspace size and rules). At 4 and 8 query heads per kv head a fp8
  * page's codes are turned into fp16 (exactly) and multiplied by the query
  * converted to fp16, which is exact for bf16 values of magnitude
- * 2^-17 .. 65504. kq_pool, vq_pool, meta_pool (16-byte aligned),
+ * 2^-17 .. 65504; its softmax weights, times the V row scale, enter the
+ * P.V product as one fp16 value each (relative error <= 2^-11, subnormal
+ * below 2^-14). kq_pool, vq_pool, meta_pool (16-byte aligned),
  * n_pages_cap_q, page_table_q (width max_pages_q), count_q: the fp8 tier as
  * kvp_compact_quant writes it. A fp8 page id outside [0, n_pages_cap_q)
  * records KVP_ERR_BOUNDS and the page counts as empty.

@@ -899,8 +899,11 @@ struct MmaCfg {
   static constexpr int PREF_BYTES = (kMaxBH + 1) * 4;
   static constexpr int SMEM = 1024 + RING_BYTES + REC_BYTES + PT_BYTES + BAR_BYTES + PREF_BYTES;
   static constexpr int QPAGE_BYTES = kPage * D;         // fp8 tier: E4M3 codes of a page's K (or V) rows
-  static constexpr int QK_OFF = STAGE_BYTES - 2 * QPAGE_BYTES;  // where the codes land (upper half)
+  // where the codes land: K's (a swizzled tensor copy, read in place) in the room of the K boxes, V's at the
+  // top of the V boxes' room, which their fp16 values then fill
+  static constexpr int QK_OFF = 0;
   static constexpr int QV_OFF = STAGE_BYTES - QPAGE_BYTES;
+  static_assert(D == 64 || D == 128, "a code row is one 64- or 128-byte swizzle span");
   static_assert(PAGE_BYTES == kPage * D * 2, "a page is its boxes");
   static_assert(STAGE_BYTES % 1024 == 0, "swizzled boxes start on 1024 bytes");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -911,16 +914,23 @@ KVP_DEV uint32_t bf16x2_to_f16x2(uint32_t w) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// kQ: the two-tier kernel. A fp8-tier page arrives as its E4M3 codes (1-D
-// bulk copies into the upper half of the stage) and its record (start steps,
-// K and V row scales); the warp turns the codes into fp16 in the same
-// swizzled layout (exactly: every E4M3 value is an fp16 value) and the page
-// goes through fp16 products, the query rows converted to fp16, the K row
-// scale applied to S and the V row scale folded into p.
+// kQ: the two-tier kernel. A fp8-tier page arrives as its E4M3 codes and its
+// record (start steps, K and V row scales). The K codes come by a tensor copy
+// with the swizzle of their row width and are read by ldmatrix as they are:
+// a thread then holds dims 4t .. 4t + 3 of its rows where the fp16 product
+// expects 2t, 2t + 1, 2t + 8, 2t + 9, so the query fragments take the same
+// order (a dot product does not depend on the order of its terms), converted
+// to fp16 once per (b, h), and each pair of codes becomes fp16 in registers
+// (exactly: every E4M3 value is an fp16 value). The V codes (a bulk copy) are
+// turned into fp16 in the swizzled box layout for the transposing ldmatrix.
+// The K row scale applies to S; the V row scale is folded into p, which
+// enters the product as one fp16 value (11 bits; the bf16 pages take p as a
+// bf16 hi + lo pair).
 template <int D, int G, bool kQ>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap tmK,
-                                                               const __grid_constant__ CUtensorMap tmV) {
+                                                               const __grid_constant__ CUtensorMap tmV,
+                                                               const __grid_constant__ CUtensorMap tmKq) {
   using C = MmaCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -937,6 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   if (tid == 0) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
+    if constexpr (kQ) prefetch_tmap(&tmKq);
   }
 
   // ---- page prefix over (b, h), identical in every CTA, and the last (b, h) with pages
@@ -1090,7 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     }
     if (kQ && isq) {
       mbar_arrive_expect_tx(&bars[st], 2 * C::QPAGE_BYTES + C::REC_WORDS * 4);
-      bulk_g2s(dst + C::QK_OFF, p.kq_pool + phys * C::QPAGE_BYTES, C::QPAGE_BYTES, &bars[st]);
+      tma_load_2d(dst + C::QK_OFF, &tmKq, 0, static_cast<int>(phys) * kPage, &bars[st]);
       bulk_g2s(dst + C::QV_OFF, p.vq_pool + phys * C::QPAGE_BYTES, C::QPAGE_BYTES, &bars[st]);
       bulk_g2s(rec, p.meta_pool + phys * C::REC_WORDS, C::REC_WORDS * 4, &bars[st]);
       return;
@@ -1165,6 +1176,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   const uint32_t ring_u32 = smem_u32(ring);
   const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: the lane's matrix and row within it
   uint32_t merge_par = 0;  // phase of this warp's merge barrier
+  bool q_perm = false;     // qf holds this (b, h)'s query in the fp8 pages' order and fp16
   for (int k = 0; k < n_my; ++k) {
     const int g = r0 + k;
     const int st = k % kNst;
@@ -1188,27 +1200,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     const int slot0 = (isq ? li - na_cur : li) * kPage;
 
     if (isq) {
-      // codes -> fp16 in the swizzled box layout. K codes sit above the K
-      // boxes' bytes; V codes sit inside the V boxes' bytes, so every lane
-      // reads its V codes before any V box is written.
+      // V codes -> fp16 in the swizzled box layout. The codes sit inside the
+      // V boxes' bytes, so every lane reads its codes before any box is written.
       uint8_t* stg = ring + st * C::STAGE_BYTES;
       constexpr int CPR = D / 8;                 // 16-byte fp16 chunks per row
-      constexpr int NCH = kPage * CPR / 32;      // chunks per lane (K, and again V)
+      constexpr int NCH = kPage * CPR / 32;      // chunks per lane
       uint2 vc[NCH];
 #pragma unroll
       for (int i = 0; i < NCH; ++i) {
         const int ci = lane + 32 * i, r = ci / CPR, c = ci - r * CPR;
         vc[i] = *reinterpret_cast<const uint2*>(stg + C::QV_OFF + r * D + c * 8);
       }
-#pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const int ci = lane + 32 * i, r = ci / CPR, c = ci - r * CPR;
-        const uint2 kc = *reinterpret_cast<const uint2*>(stg + C::QK_OFF + r * D + c * 8);
-        const uint4 h = make_uint4(cvt_e4m3x2_to_f16x2(kc.x), cvt_e4m3x2_to_f16x2(kc.x >> 16),
-                                   cvt_e4m3x2_to_f16x2(kc.y), cvt_e4m3x2_to_f16x2(kc.y >> 16));
-        *reinterpret_cast<uint4*>(stg + (c >> 3) * C::BOX_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = h;
-      }
-      __syncwarp();  // every lane has read its K codes, which the V boxes overwrite
+      __syncwarp();
 #pragma unroll
       for (int i = 0; i < NCH; ++i) {
         const int ci = lane + 32 * i, r = ci / CPR, c = ci - r * CPR;
@@ -1218,22 +1221,54 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
                                   (((c & 7) ^ (r & 7)) << 4)) = h;
       }
       __syncwarp();
+      if (!q_perm) {
+        // the first fp8 page of this (b, h): the query fragments in the
+        // codes' order, as fp16. Thread (g, t) takes dims 4t, 4t + 1 (from
+        // thread (g, 2t mod 4)) and 4t + 2, 4t + 3 (from (g, 2t + 1 mod 4)) of
+        // each k-step: the first of its registers for t < 2, the second after.
+        const int s0 = (lane & ~3) | ((2 * tq) & 3), s1 = (lane & ~3) | ((2 * tq + 1) & 3);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t x0 = __shfl_sync(0xffffffffu, qf[ks][0], s0), x1 = __shfl_sync(0xffffffffu, qf[ks][1], s0);
+          const uint32_t y0 = __shfl_sync(0xffffffffu, qf[ks][0], s1), y1 = __shfl_sync(0xffffffffu, qf[ks][1], s1);
+          qf[ks][0] = bf16x2_to_f16x2(tq < 2 ? x0 : x1);
+          qf[ks][1] = bf16x2_to_f16x2(tq < 2 ? y0 : y1);
+        }
+        q_perm = true;
+      }
     }
 
-    // ---- S = K Q^T: 16 tokens x 8 heads; A = K from the swizzled boxes
+    // ---- S = K Q^T: 16 tokens x 8 heads
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (isq) {
+      // A = the K codes in place: matrices 0 / 1 are rows 0-7 / 8-15 of
+      // k-step 2 kp's 16 bytes, 2 / 3 of k-step 2 kp + 1's; thread (g, t)
+      // receives 4 codes (dims 4t .. 4t + 3) of rows g and g + 8 of each
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      // matrices: 0 rows 0-7 / 1 rows 8-15 of the k-step's first 8 dims, 2 / 3 of its second 8
-      const int r = (mi & 1) * 8 + ri;
-      const int chunk = (ks & 3) * 2 + (mi >> 1);
-      const uint32_t addr = kbase + (ks >> 2) * C::BOX_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4);
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(addr, a0, a1, a2, a3);
-      if (isq)
-        mma_f16_16816(sacc, a0, a1, a2, a3, bf16x2_to_f16x2(qf[ks][0]), bf16x2_to_f16x2(qf[ks][1]));
-      else
+      for (int kp = 0; kp < KS / 2; ++kp) {
+        const int r = (mi & 1) * 8 + ri;
+        const int chunk = 2 * kp + (mi >> 1);
+        const int sw = D == 128 ? (r & 7) : ((r >> 1) & 3);
+        const uint32_t addr = kbase + C::QK_OFF + r * D + ((chunk ^ sw) << 4);
+        uint32_t c0, c1, c2, c3;
+        ldsm_x4(addr, c0, c1, c2, c3);
+        mma_f16_16816(sacc, cvt_e4m3x2_to_f16x2(c0), cvt_e4m3x2_to_f16x2(c1), cvt_e4m3x2_to_f16x2(c0 >> 16),
+                      cvt_e4m3x2_to_f16x2(c1 >> 16), qf[2 * kp][0], qf[2 * kp][1]);
+        mma_f16_16816(sacc, cvt_e4m3x2_to_f16x2(c2), cvt_e4m3x2_to_f16x2(c3), cvt_e4m3x2_to_f16x2(c2 >> 16),
+                      cvt_e4m3x2_to_f16x2(c3 >> 16), qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+      }
+    } else {
+      // A = K from the swizzled boxes
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        // matrices: 0 rows 0-7 / 1 rows 8-15 of the k-step's first 8 dims, 2 / 3 of its second 8
+        const int r = (mi & 1) * 8 + ri;
+        const int chunk = (ks & 3) * 2 + (mi >> 1);
+        const uint32_t addr = kbase + (ks >> 2) * C::BOX_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(addr, a0, a1, a2, a3);
         mma_bf16_16816(sacc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      }
     }
 
     // ---- V^T fragments: A of the second product, read transposed by ldmatrix
@@ -1311,9 +1346,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
         o[mt][3] *= al1;
       }
     }
-    // p as a bf16 (fp16 on a fp8 page) pair hi + lo: the P.V product keeps
-    // about 16 bits of p; the sum takes p itself. On a fp8 page the V row
-    // scale multiplies p for the product.
+    // p on a bf16 page as a bf16 pair hi + lo (the P.V product keeps about
+    // 16 bits of p), on a fp8 page as one fp16 value times the V row scale
+    // (11 bits); the sum takes p itself.
     float pf[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) pf[i] = exp2f(x[i] - m2[i & 1]);
@@ -1323,27 +1358,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     const int tok[4] = {gq, gq, gq + 8, gq + 8};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      uint16_t hb, lb;
       if (isq) {
         const float pv = pf[i] * ((i < 2) ? vs0 : vs1);
-        const __half hi = __float2half_rn(pv);
-        const __half lo = __float2half_rn(pv - __half2float(hi));
-        hb = __half_as_ushort(hi);
-        lb = __half_as_ushort(lo);
+        pt_s[(2 * tq + (i & 1)) * C::kPtRow + tok[i]] = __half_as_ushort(__float2half_rn(pv));
       } else {
         const __nv_bfloat16 hi = __float2bfloat16_rn(pf[i]);
         const __nv_bfloat16 lo = __float2bfloat16_rn(pf[i] - __bfloat162float(hi));
-        hb = __bfloat16_as_ushort(hi);
-        lb = __bfloat16_as_ushort(lo);
+        pt_s[(2 * tq + (i & 1)) * C::kPtRow + tok[i]] = __bfloat16_as_ushort(hi);
+        pt_s[8 * C::kPtRow + (2 * tq + (i & 1)) * C::kPtRow + tok[i]] = __bfloat16_as_ushort(lo);
       }
-      pt_s[(2 * tq + (i & 1)) * C::kPtRow + tok[i]] = hb;
-      pt_s[8 * C::kPtRow + (2 * tq + (i & 1)) * C::kPtRow + tok[i]] = lb;
     }
     __syncwarp();
     const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pt_s + gq * C::kPtRow + 2 * tq);
     const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pt_s + gq * C::kPtRow + 8 + 2 * tq);
-    const uint32_t pl0 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * C::kPtRow + gq * C::kPtRow + 2 * tq);
-    const uint32_t pl1 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * C::kPtRow + gq * C::kPtRow + 8 + 2 * tq);
+    uint32_t pl0 = 0u, pl1 = 0u;
+    if (!isq) {
+      pl0 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * C::kPtRow + gq * C::kPtRow + 2 * tq);
+      pl1 = *reinterpret_cast<const uint32_t*>(pt_s + 8 * C::kPtRow + gq * C::kPtRow + 8 + 2 * tq);
+    }
 
     // ---- O^T += V^T P^T
 #pragma unroll
@@ -1359,7 +1391,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
       }
       if (isq) {
         mma_f16_16816(o[mt], a[0], a[1], a[2], a[3], pb0, pb1);
-        mma_f16_16816(o[mt], a[0], a[1], a[2], a[3], pl0, pl1);
       } else {
         mma_bf16_16816(o[mt], a[0], a[1], a[2], a[3], pb0, pb1);
         mma_bf16_16816(o[mt], a[0], a[1], a[2], a[3], pl0, pl1);
@@ -1448,6 +1479,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
           qf[ks][0] = qn[ks][0];
           qf[ks][1] = qn[ks][1];
         }
+        q_perm = false;
         if (seg_end < r1) {
           load_qf(next_bh(cbh), qn);
           cnt_next = clamp_count(p.count, next_bh(cbh), p.max_pages);
@@ -1508,13 +1540,14 @@ int attn_mma_grid() {
 }
 
 template <int D, int G, bool kQ>
-kvp_status launch_attn_mma(const AttnParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int grid_limit,
-                           cudaStream_t st) {
+kvp_status launch_attn_mma(const AttnParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                           const CUtensorMap& tmKq, int grid_limit, cudaStream_t st) {
   using C = MmaCfg<D>;
   int grid = attn_mma_grid<D, G, kQ>();
   if (grid <= 0) return KVP_ERR_CUDA;
   if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
-  if (launch_pdl(attn_mma_kernel<D, G, kQ>, dim3(grid), dim3(kThreads), C::SMEM, st, p, tmK, tmV) != cudaSuccess)
+  if (launch_pdl(attn_mma_kernel<D, G, kQ>, dim3(grid), dim3(kThreads), C::SMEM, st, p, tmK, tmV, tmKq) !=
+      cudaSuccess)
     return KVP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
@@ -1525,9 +1558,14 @@ kvp_status dispatch_mma(const AttnParams& p, int G, int grid_limit, cudaStream_t
   const int64_t rows = static_cast<int64_t>(p.n_pages_cap) * kPage;
   if (!make_tmap_bf16(&tmK, p.k_pool, rows, D, D, kPage, 64) || !make_tmap_bf16(&tmV, p.v_pool, rows, D, D, kPage, 64))
     return KVP_ERR_CUDA;
-  if (G == 4) return launch_attn_mma<D, 4, kQ>(p, tmK, tmV, grid_limit, st);
+  // the fp8 tier's K codes, 16 rows a box (a pool with no pages takes no copy: the K map stands in)
+  CUtensorMap tmKq = tmK;
+  if (kQ && p.n_pages_cap_q > 0 &&
+      !make_tmap_u8_rows(&tmKq, p.kq_pool, static_cast<int64_t>(p.n_pages_cap_q) * kPage, D, kPage))
+    return KVP_ERR_CUDA;
+  if (G == 4) return launch_attn_mma<D, 4, kQ>(p, tmK, tmV, tmKq, grid_limit, st);
   if (G != 8) return KVP_ERR_UNSUPPORTED;
-  return launch_attn_mma<D, 8, kQ>(p, tmK, tmV, grid_limit, st);
+  return launch_attn_mma<D, 8, kQ>(p, tmK, tmV, tmKq, grid_limit, st);
 }
 
 template <int D, bool kQ>

@@ -504,6 +504,23 @@ inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A byte matrix [rows, row_bytes] (row_bytes 64 or 128, rows packed) whose
+// box is box_rows whole rows, landing in shared memory with the swizzle of its
+// row width: 16-byte chunk c of box row r at chunk c ^ (r & 7) of a 128-byte
+// row, or c ^ ((r >> 1) & 3) of a 64-byte row (the destination aligned to
+// 1024 or 512 bytes).
+inline bool make_tmap_u8_rows(CUtensorMap* m, const void* base, int64_t rows, int row_bytes, int box_rows) {
+  auto fn = tmap_encode_fn();
+  if (fn == nullptr || (row_bytes != 64 && row_bytes != 128) || rows <= 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A row-major bf16 matrix [rows, cols] (cols a multiple of 64, row stride ld
 // elements) seen as [rows][cols / 64][64]: one box is box_rows consecutive rows
 // x every 64-column group, landing in shared memory as cols / 64 boxes of
