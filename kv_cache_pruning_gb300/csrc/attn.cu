@@ -899,11 +899,12 @@ struct MmaCfg {
   static constexpr int PREF_BYTES = (kMaxBH + 1) * 4;
   static constexpr int SMEM = 1024 + RING_BYTES + REC_BYTES + PT_BYTES + BAR_BYTES + PREF_BYTES;
   static constexpr int QPAGE_BYTES = kPage * D;         // fp8 tier: E4M3 codes of a page's K (or V) rows
-  // where the codes land: K's (a swizzled tensor copy, read in place) in the room of the K boxes, V's at the
-  // top of the V boxes' room, which their fp16 values then fill
+  // where the codes land (swizzled tensor copies, read in place): K's in the room of the K boxes, V's in the
+  // room of the V boxes, each on a 1024-byte boundary
   static constexpr int QK_OFF = 0;
-  static constexpr int QV_OFF = STAGE_BYTES - QPAGE_BYTES;
+  static constexpr int QV_OFF = PAGE_BYTES;
   static_assert(D == 64 || D == 128, "a code row is one 64- or 128-byte swizzle span");
+  static_assert(QV_OFF % 1024 == 0 && QV_OFF + QPAGE_BYTES <= STAGE_BYTES, "code tiles");
   static_assert(PAGE_BYTES == kPage * D * 2, "a page is its boxes");
   static_assert(STAGE_BYTES % 1024 == 0, "swizzled boxes start on 1024 bytes");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -915,22 +916,25 @@ KVP_DEV uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 // kQ: the two-tier kernel. A fp8-tier page arrives as its E4M3 codes and its
-// record (start steps, K and V row scales). The K codes come by a tensor copy
-// with the swizzle of their row width and are read by ldmatrix as they are:
-// a thread then holds dims 4t .. 4t + 3 of its rows where the fp16 product
-// expects 2t, 2t + 1, 2t + 8, 2t + 9, so the query fragments take the same
-// order (a dot product does not depend on the order of its terms), converted
-// to fp16 once per (b, h), and each pair of codes becomes fp16 in registers
-// (exactly: every E4M3 value is an fp16 value). The V codes (a bulk copy) are
-// turned into fp16 in the swizzled box layout for the transposing ldmatrix.
-// The K row scale applies to S; the V row scale is folded into p, which
-// enters the product as one fp16 value (11 bits; the bf16 pages take p as a
-// bf16 hi + lo pair).
+// record (start steps, K and V row scales). The codes come by tensor copies
+// with the swizzle of their row width and are read by ldmatrix as they are;
+// each pair of codes becomes fp16 in registers (exactly: every E4M3 value is
+// an fp16 value). K: a thread holds dims 4t .. 4t + 3 of its rows where the
+// fp16 product expects 2t, 2t + 1, 2t + 8, 2t + 9, so the query fragments take
+// the same order (a dot product does not depend on the order of its terms),
+// converted to fp16 once per (b, h). V, read transposed as 16-bit words: a
+// thread holds dims 2g, 2g + 1 of tokens 2t, 2t + 1, so its output rows g and
+// g + 8 are dims 2g and 2g + 1 of each 16 (the accumulators are moved to that
+// order by shuffles at the (b, h)'s first fp8 page, and stored from it). The
+// K row scale applies to S; the V row scale is folded into p, which enters
+// the product as one fp16 value (11 bits; the bf16 pages take p as a bf16
+// hi + lo pair).
 template <int D, int G, bool kQ>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap tmK,
                                                                const __grid_constant__ CUtensorMap tmV,
-                                                               const __grid_constant__ CUtensorMap tmKq) {
+                                                               const __grid_constant__ CUtensorMap tmKq,
+                                                               const __grid_constant__ CUtensorMap tmVq) {
   using C = MmaCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -947,7 +951,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   if (tid == 0) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
-    if constexpr (kQ) prefetch_tmap(&tmKq);
+    if constexpr (kQ) {
+      prefetch_tmap(&tmKq);
+      prefetch_tmap(&tmVq);
+    }
   }
 
   // ---- page prefix over (b, h), identical in every CTA, and the last (b, h) with pages
@@ -1102,7 +1109,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     if (kQ && isq) {
       mbar_arrive_expect_tx(&bars[st], 2 * C::QPAGE_BYTES + C::REC_WORDS * 4);
       tma_load_2d(dst + C::QK_OFF, &tmKq, 0, static_cast<int>(phys) * kPage, &bars[st]);
-      bulk_g2s(dst + C::QV_OFF, p.vq_pool + phys * C::QPAGE_BYTES, C::QPAGE_BYTES, &bars[st]);
+      tma_load_2d(dst + C::QV_OFF, &tmVq, 0, static_cast<int>(phys) * kPage, &bars[st]);
       bulk_g2s(rec, p.meta_pool + phys * C::REC_WORDS, C::REC_WORDS * 4, &bars[st]);
       return;
     }
@@ -1199,43 +1206,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     const bool isq = kQ && li >= na_cur;           // a fp8-tier page (uniform in the warp)
     const int slot0 = (isq ? li - na_cur : li) * kPage;
 
-    if (isq) {
-      // V codes -> fp16 in the swizzled box layout. The codes sit inside the
-      // V boxes' bytes, so every lane reads its codes before any box is written.
-      uint8_t* stg = ring + st * C::STAGE_BYTES;
-      constexpr int CPR = D / 8;                 // 16-byte fp16 chunks per row
-      constexpr int NCH = kPage * CPR / 32;      // chunks per lane
-      uint2 vc[NCH];
+    if (isq && !q_perm) {
+      // the first fp8 page of this (b, h). The query fragments go to the K
+      // codes' order, as fp16: thread (g, t) takes dims 4t, 4t + 1 (from
+      // thread (g, 2t mod 4)) and 4t + 2, 4t + 3 (from (g, 2t + 1 mod 4)) of
+      // each k-step, the first of its registers for t < 2, the second after.
+      const int s0 = (lane & ~3) | ((2 * tq) & 3), s1 = (lane & ~3) | ((2 * tq + 1) & 3);
 #pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const int ci = lane + 32 * i, r = ci / CPR, c = ci - r * CPR;
-        vc[i] = *reinterpret_cast<const uint2*>(stg + C::QV_OFF + r * D + c * 8);
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint32_t x0 = __shfl_sync(0xffffffffu, qf[ks][0], s0), x1 = __shfl_sync(0xffffffffu, qf[ks][1], s0);
+        const uint32_t y0 = __shfl_sync(0xffffffffu, qf[ks][0], s1), y1 = __shfl_sync(0xffffffffu, qf[ks][1], s1);
+        qf[ks][0] = bf16x2_to_f16x2(tq < 2 ? x0 : x1);
+        qf[ks][1] = bf16x2_to_f16x2(tq < 2 ? y0 : y1);
       }
-      __syncwarp();
+      // The accumulators go to the V codes' order: rows g and g + 8 of each
+      // 16 output dims become dims 2g and 2g + 1, held before by thread
+      // (2g mod 8, t) and (2g + 1 mod 8, t), in their first pair for g < 4
+      // and their second after.
+      const int sa = (((2 * gq) & 7) << 2) | tq, sb = (((2 * gq + 1) & 7) << 2) | tq;
+      const bool upper = gq >= 4;
 #pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const int ci = lane + 32 * i, r = ci / CPR, c = ci - r * CPR;
-        const uint4 h = make_uint4(cvt_e4m3x2_to_f16x2(vc[i].x), cvt_e4m3x2_to_f16x2(vc[i].x >> 16),
-                                   cvt_e4m3x2_to_f16x2(vc[i].y), cvt_e4m3x2_to_f16x2(vc[i].y >> 16));
-        *reinterpret_cast<uint4*>(stg + C::PAGE_BYTES + (c >> 3) * C::BOX_BYTES + r * 128 +
-                                  (((c & 7) ^ (r & 7)) << 4)) = h;
-      }
-      __syncwarp();
-      if (!q_perm) {
-        // the first fp8 page of this (b, h): the query fragments in the
-        // codes' order, as fp16. Thread (g, t) takes dims 4t, 4t + 1 (from
-        // thread (g, 2t mod 4)) and 4t + 2, 4t + 3 (from (g, 2t + 1 mod 4)) of
-        // each k-step: the first of its registers for t < 2, the second after.
-        const int s0 = (lane & ~3) | ((2 * tq) & 3), s1 = (lane & ~3) | ((2 * tq + 1) & 3);
+      for (int mt = 0; mt < KS; ++mt) {
+        float x[4], y[4];
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const uint32_t x0 = __shfl_sync(0xffffffffu, qf[ks][0], s0), x1 = __shfl_sync(0xffffffffu, qf[ks][1], s0);
-          const uint32_t y0 = __shfl_sync(0xffffffffu, qf[ks][0], s1), y1 = __shfl_sync(0xffffffffu, qf[ks][1], s1);
-          qf[ks][0] = bf16x2_to_f16x2(tq < 2 ? x0 : x1);
-          qf[ks][1] = bf16x2_to_f16x2(tq < 2 ? y0 : y1);
+        for (int c = 0; c < 4; ++c) {
+          x[c] = __shfl_sync(0xffffffffu, o[mt][c], sa);
+          y[c] = __shfl_sync(0xffffffffu, o[mt][c], sb);
         }
-        q_perm = true;
+        o[mt][0] = upper ? x[2] : x[0];
+        o[mt][1] = upper ? x[3] : x[1];
+        o[mt][2] = upper ? y[2] : y[0];
+        o[mt][3] = upper ? y[3] : y[1];
       }
+      q_perm = true;
     }
 
     // ---- S = K Q^T: 16 tokens x 8 heads
@@ -1283,6 +1286,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
       const uint32_t addr = vbase + (mt >> 2) * C::BOX_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4);
       ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
     };
+    // a fp8 page: the V fragments of output dims 16 mt .. 16 mt + 15, for mt = 2 mp and 2 mp + 1, from the codes.
+    // Matrices: 0 / 1 tokens 0-7 / 8-15 of the 16 codes of dims 32 mp .., 2 / 3 of dims 32 mp + 16 ..; read
+    // transposed as 16-bit words, thread (g, t) gets codes (2t, 2g), (2t, 2g + 1), (2t + 1, 2g), (2t + 1, 2g + 1)
+    // (token, dim) of each, regrouped by dim into two fp16 pairs
+    auto vq_frag2 = [&](int mp, uint32_t (&a0)[4], uint32_t (&a1)[4]) {
+      const int r = (mi & 1) * 8 + ri;
+      const int chunk = 2 * mp + (mi >> 1);
+      const int sw = D == 128 ? (r & 7) : ((r >> 1) & 3);
+      const uint32_t addr = kbase + C::QV_OFF + r * D + ((chunk ^ sw) << 4);
+      uint32_t w[4];
+      ldsm_x4_trans(addr, w[0], w[1], w[2], w[3]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = __byte_perm(w[j], 0u, 0x3120);  // [dim 2g: t0, t1 | dim 2g + 1: t0, t1]
+      a0[0] = cvt_e4m3x2_to_f16x2(w[0]);
+      a0[1] = cvt_e4m3x2_to_f16x2(w[0] >> 16);
+      a0[2] = cvt_e4m3x2_to_f16x2(w[1]);
+      a0[3] = cvt_e4m3x2_to_f16x2(w[1] >> 16);
+      a1[0] = cvt_e4m3x2_to_f16x2(w[2]);
+      a1[1] = cvt_e4m3x2_to_f16x2(w[2] >> 16);
+      a1[2] = cvt_e4m3x2_to_f16x2(w[3]);
+      a1[3] = cvt_e4m3x2_to_f16x2(w[3] >> 16);
+    };
     uint32_t va[kEarly ? KS : 1][4];
     const int32_t e0 = rec[gq], e1 = rec[gq + 8];
     const float ks0 = isq ? __int_as_float(rec[kPage + gq]) : 1.f;
@@ -1301,8 +1326,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
       }
     };
     if constexpr (kEarly) {
+      if (isq) {
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) v_frag(mt, va[mt]);
+        for (int mp = 0; mp < KS / 2; ++mp) vq_frag2(mp, va[2 * mp], va[2 * mp + 1]);
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) v_frag(mt, va[mt]);
+      }
       issue_next();
     }
 
@@ -1378,20 +1408,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
     }
 
     // ---- O^T += V^T P^T
+    if (isq) {
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      uint32_t a[4];
-      if constexpr (kEarly) {
-        a[0] = va[mt][0];
-        a[1] = va[mt][1];
-        a[2] = va[mt][2];
-        a[3] = va[mt][3];
-      } else {
-        v_frag(mt, a);
+      for (int mp = 0; mp < KS / 2; ++mp) {
+        if constexpr (kEarly) {
+          mma_f16_16816(o[2 * mp], va[2 * mp][0], va[2 * mp][1], va[2 * mp][2], va[2 * mp][3], pb0, pb1);
+          mma_f16_16816(o[2 * mp + 1], va[2 * mp + 1][0], va[2 * mp + 1][1], va[2 * mp + 1][2], va[2 * mp + 1][3],
+                        pb0, pb1);
+        } else {
+          uint32_t a0[4], a1[4];
+          vq_frag2(mp, a0, a1);
+          mma_f16_16816(o[2 * mp], a0[0], a0[1], a0[2], a0[3], pb0, pb1);
+          mma_f16_16816(o[2 * mp + 1], a1[0], a1[1], a1[2], a1[3], pb0, pb1);
+        }
       }
-      if (isq) {
-        mma_f16_16816(o[mt], a[0], a[1], a[2], a[3], pb0, pb1);
-      } else {
+    } else {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        uint32_t a[4];
+        if constexpr (kEarly) {
+          a[0] = va[mt][0];
+          a[1] = va[mt][1];
+          a[2] = va[mt][2];
+          a[3] = va[mt][3];
+        } else {
+          v_frag(mt, a);
+        }
         mma_bf16_16816(o[mt], a[0], a[1], a[2], a[3], pb0, pb1);
         mma_bf16_16816(o[mt], a[0], a[1], a[2], a[3], pl0, pl1);
       }
@@ -1408,20 +1450,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
         lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
       }
       const int h0 = 2 * tq, h1 = 2 * tq + 1;
+      // output rows g and g + 8 of each 16 dims: dims g and g + 8, or 2g and 2g + 1 after a fp8 page
+      const int da = q_perm ? 2 * gq : gq, db = q_perm ? 2 * gq + 1 : gq + 8;
       const bool whole = pref[cbh] >= r0 && pref[cbh + 1] <= r1;
       if (whole) {
         const float i0 = lt0 > 0.f ? 1.f / lt0 : 0.f, i1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
         float* ob = p.out + static_cast<size_t>(cbh) * G * D;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          const int d0 = 16 * mt + gq;
           if (h0 < G) {
-            ob[h0 * D + d0] = o[mt][0] * i0;
-            ob[h0 * D + d0 + 8] = o[mt][2] * i0;
+            ob[h0 * D + 16 * mt + da] = o[mt][0] * i0;
+            ob[h0 * D + 16 * mt + db] = o[mt][2] * i0;
           }
           if (h1 < G) {
-            ob[h1 * D + d0] = o[mt][1] * i1;
-            ob[h1 * D + d0 + 8] = o[mt][3] * i1;
+            ob[h1 * D + 16 * mt + da] = o[mt][1] * i1;
+            ob[h1 * D + 16 * mt + db] = o[mt][3] * i1;
           }
         }
       } else {
@@ -1431,14 +1474,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
         float* pa = p.part_acc + slot * G * D;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          const int d0 = 16 * mt + gq;
           if (h0 < G) {
-            pa[h0 * D + d0] = o[mt][0];
-            pa[h0 * D + d0 + 8] = o[mt][2];
+            pa[h0 * D + 16 * mt + da] = o[mt][0];
+            pa[h0 * D + 16 * mt + db] = o[mt][2];
           }
           if (h1 < G) {
-            pa[h1 * D + d0] = o[mt][1];
-            pa[h1 * D + d0 + 8] = o[mt][3];
+            pa[h1 * D + 16 * mt + da] = o[mt][1];
+            pa[h1 * D + 16 * mt + db] = o[mt][3];
           }
         }
         if (gq == 0) {
@@ -1541,12 +1583,12 @@ int attn_mma_grid() {
 
 template <int D, int G, bool kQ>
 kvp_status launch_attn_mma(const AttnParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                           const CUtensorMap& tmKq, int grid_limit, cudaStream_t st) {
+                           const CUtensorMap& tmKq, const CUtensorMap& tmVq, int grid_limit, cudaStream_t st) {
   using C = MmaCfg<D>;
   int grid = attn_mma_grid<D, G, kQ>();
   if (grid <= 0) return KVP_ERR_CUDA;
   if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
-  if (launch_pdl(attn_mma_kernel<D, G, kQ>, dim3(grid), dim3(kThreads), C::SMEM, st, p, tmK, tmV, tmKq) !=
+  if (launch_pdl(attn_mma_kernel<D, G, kQ>, dim3(grid), dim3(kThreads), C::SMEM, st, p, tmK, tmV, tmKq, tmVq) !=
       cudaSuccess)
     return KVP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
@@ -1558,14 +1600,15 @@ kvp_status dispatch_mma(const AttnParams& p, int G, int grid_limit, cudaStream_t
   const int64_t rows = static_cast<int64_t>(p.n_pages_cap) * kPage;
   if (!make_tmap_bf16(&tmK, p.k_pool, rows, D, D, kPage, 64) || !make_tmap_bf16(&tmV, p.v_pool, rows, D, D, kPage, 64))
     return KVP_ERR_CUDA;
-  // the fp8 tier's K codes, 16 rows a box (a pool with no pages takes no copy: the K map stands in)
-  CUtensorMap tmKq = tmK;
-  if (kQ && p.n_pages_cap_q > 0 &&
-      !make_tmap_u8_rows(&tmKq, p.kq_pool, static_cast<int64_t>(p.n_pages_cap_q) * kPage, D, kPage))
+  // the fp8 tier's K and V codes, 16 rows a box (a pool with no pages takes no copy: the bf16 maps stand in)
+  CUtensorMap tmKq = tmK, tmVq = tmV;
+  const int64_t rows_q = static_cast<int64_t>(p.n_pages_cap_q) * kPage;
+  if (kQ && rows_q > 0 &&
+      (!make_tmap_u8_rows(&tmKq, p.kq_pool, rows_q, D, kPage) || !make_tmap_u8_rows(&tmVq, p.vq_pool, rows_q, D, kPage)))
     return KVP_ERR_CUDA;
-  if (G == 4) return launch_attn_mma<D, 4, kQ>(p, tmK, tmV, tmKq, grid_limit, st);
+  if (G == 4) return launch_attn_mma<D, 4, kQ>(p, tmK, tmV, tmKq, tmVq, grid_limit, st);
   if (G != 8) return KVP_ERR_UNSUPPORTED;
-  return launch_attn_mma<D, 8, kQ>(p, tmK, tmV, tmKq, grid_limit, st);
+  return launch_attn_mma<D, 8, kQ>(p, tmK, tmV, tmKq, tmVq, grid_limit, st);
 }
 
 template <int D, bool kQ>
