@@ -488,6 +488,48 @@ KVP_API kvp_status kvp_decode_attn_devpos(int batch, int n_q_heads, int n_kv_hea
                                           int grid_limit, void* workspace, size_t workspace_bytes,
                                           int32_t* status, void* stream);
 
+/* kvp_decode_attn_lse - kvp_decode_attn that also returns each output row's
+ * log-sum-exp (DMS article, "DMS 작동 방식": the standard attention over what is
+ * kept, whose softmax normaliser this is):
+ *
+ *   lse[b, j] = ln sum_i exp(scale * q[b, j] . k_i)
+ *
+ * over the same present slots (-inf when there are none, with a zero output
+ * row). Attention over a set of slots split into parts, each part's rows
+ * with its lse, is recovered exactly by kvp_attn_merge: a long sequence's
+ * pages can be attended in parts (separate caches, or separate devices whose
+ * (out, lse) rows the caller gathers) and merged.
+ *
+ * lse        device fp32 [B, Hq] (output, required, 4-byte aligned). Every
+ *            other argument, and the workspace rules: as kvp_decode_attn.
+ */
+KVP_API kvp_status kvp_decode_attn_lse(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                       const void* q, const void* k_pool, const void* v_pool,
+                                       const int32_t* expire_pool, int n_pages_cap,
+                                       const int32_t* page_table, int max_pages,
+                                       const int32_t* count, int now, float scale, float* out, float* lse,
+                                       int grid_limit, void* workspace, size_t workspace_bytes,
+                                       int32_t* status, void* stream);
+
+/* kvp_attn_merge - one attention output from n_parts partial ones over
+ * disjoint parts of the same slots, each normalised over its own part
+ * (kvp_decode_attn_lse's out and lse):
+ *
+ *   lse[r] = ln sum_p exp(lses[p, r]),   out[r] = sum_p exp(lses[p, r] - lse[r]) outs[p, r]
+ *
+ * A part with lse -inf (no slots) weighs nothing; a row with no slots in any
+ * part comes out zero with lse -inf. lses must be finite or -inf.
+ *
+ * outs       device fp32 [n_parts, rows, head_dim], 16-byte aligned
+ * lses       device fp32 [n_parts, rows]
+ * out        device fp32 [rows, head_dim] (output), 16-byte aligned; it may
+ *            not overlap outs
+ * lse_out    device fp32 [rows] (output) or NULL
+ * head_dim   a multiple of 4; rows >= 0 (0: nothing to do); n_parts >= 1
+ */
+KVP_API kvp_status kvp_attn_merge(int n_parts, int64_t rows, int head_dim, const float* outs, const float* lses,
+                                  float* out, float* lse_out, void* stream);
+
 /* kvp_decode_attn_two_tier - kvp_decode_attn over both tiers of "quantize
  * instead of drop" (BeaconKV article; the fp8 tier as kvp_compact_quant
  * writes it):

@@ -96,6 +96,9 @@ _SIGS = {
     "kvp_decode_attn": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _I, _P, _S, _P, _P]),
     "kvp_decode_attn_devpos": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _F, _P, _I, _P, _S, _P,
                                     _P]),
+    "kvp_decode_attn_lse": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _I, _F, _P, _P, _I, _P, _S, _P,
+                                 _P]),
+    "kvp_attn_merge": (_I, [_I, _L, _I, _P, _P, _P, _P, _P]),
     "kvp_decode_attn_two_tier": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _P, _I, _P,
                                       _I, _F, _P, _I, _P, _S, _P, _P]),
     "kvp_compact_latent": (_I, [_I, _I, _I, _I, _P, _L, _L, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _I, _P, _P,
@@ -559,6 +562,49 @@ def kvp_decode_attn(q, cache: PagedKV, now, *, scale=0.0, out=None, grid_limit=0
                                 _ptr(status, torch.int32, "status", True), _stream(stream))
     _check("kvp_decode_attn", code)
     return out
+
+
+def kvp_decode_attn_lse(q, cache: PagedKV, now, *, scale=0.0, out=None, lse=None, grid_limit=0, workspace=None,
+                        status=None, stream=None):
+    """(out, lse): kvp_decode_attn's out [B, Hq, d] fp32 and each row's log-sum-exp lse [B, Hq] fp32 (ln of the
+    sum of exp(scale q.k) over the present slots; -inf for an empty row). Workspace rules: kvp_decode_attn's."""
+    B, Hq, d = q.shape
+    H = cache.count.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = kvp_decode_attn_workspace_bytes(B, Hq, H, d)
+    if workspace is None:
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)  # zero-filled before first use
+    else:
+        ws = _ws(need, q.device, workspace)
+    code = _lib.kvp_decode_attn_lse(B, Hq, H, d, _ptr(q, torch.bfloat16, "q"), _ptr(cache.k_pool),
+                                    _ptr(cache.v_pool), _ptr(cache.expire_pool, torch.int32), cache.n_pages_cap,
+                                    _ptr(cache.page_table, torch.int32), cache.max_pages,
+                                    _ptr(cache.count, torch.int32), now, float(scale),
+                                    _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+                                    grid_limit, ws.data_ptr(), ws.numel() * ws.element_size(),
+                                    _ptr(status, torch.int32, "status", True), _stream(stream))
+    _check("kvp_decode_attn_lse", code)
+    return out, lse
+
+
+def kvp_attn_merge(outs, lses, *, out=None, lse=None, stream=None):
+    """(out, lse) of attention over the union of disjoint parts, from each part's rows: outs [P, ..., d] fp32 and
+    lses [P, ...] fp32 (kvp_decode_attn_lse's, stacked). out [..., d], lse [...]."""
+    n_parts, d = outs.shape[0], outs.shape[-1]
+    if lses.shape != outs.shape[:-1]:
+        raise ValueError("lses must have the shape of outs without its last dimension")
+    rows = lses[0].numel()
+    if out is None:
+        out = torch.empty(outs.shape[1:], dtype=torch.float32, device=outs.device)
+    if lse is None:
+        lse = torch.empty(lses.shape[1:], dtype=torch.float32, device=outs.device)
+    code = _lib.kvp_attn_merge(n_parts, rows, d, _ptr(outs, torch.float32, "outs"), _ptr(lses, torch.float32, "lses"),
+                               _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream))
+    _check("kvp_attn_merge", code)
+    return out, lse
 
 
 def kvp_decode_attn_devpos(q, cache: PagedKV, now_dev, *, scale=0.0, out=None, grid_limit=0, workspace=None,

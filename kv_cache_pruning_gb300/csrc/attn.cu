@@ -88,7 +88,12 @@ struct AttnParams {
   const int32_t* count_q;
   int max_pages_q, n_pages_cap_q;
   const int32_t* now_dev;  // device int32 holding the decode position, or null: `now` is used
+  float* lse;              // [B, Hq]: ln of the sum of exp(scaled logits) of each row, or null
 };
+
+// A row's natural log-sum-exp from its base-2 reference m2 and its sum
+// l = sum 2^(x - m2) of the base-2 logits x (-inf when the row is empty).
+KVP_DEV float row_lse(float m2, float l) { return l > 0.f ? (m2 + log2f(l)) * 0.69314718055994531f : -INFINITY; }
 
 // Eight E4M3 codes (bytes of x then y, element 0 in the lowest byte) to fp32,
 // exactly (every E4M3 value is an fp16 value).
@@ -234,6 +239,16 @@ KVP_DEV bool merge_pieces(const AttnParams& p, int cbh, int npc, size_t s0, bool
       for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
       L[i] = l;
     }
+    if (p.lse != nullptr && lane < G) {
+      float mm = M[0], ll = L[0];
+#pragma unroll
+      for (int i = 1; i < G; ++i)
+        if (lane == i) {
+          mm = M[i];
+          ll = L[i];
+        }
+      p.lse[static_cast<size_t>(cbh) * G + lane] = row_lse(mm, ll);
+    }
     float4 A[FPL];
 #pragma unroll
     for (int k2 = 0; k2 < FPL; ++k2) A[k2] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -352,6 +367,16 @@ KVP_DEV bool merge_pieces(const AttnParams& p, int cbh, int npc, size_t s0, bool
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L[i] += __shfl_xor_sync(0xffffffffu, L[i], o);
   }
+  if (p.lse != nullptr && lane < G) {
+    float mm = M[0], ll = L[0];
+#pragma unroll
+    for (int i = 1; i < G; ++i)
+      if (lane == i) {
+        mm = M[i];
+        ll = L[i];
+      }
+    p.lse[static_cast<size_t>(cbh) * G + lane] = row_lse(mm, ll);
+  }
 #pragma unroll
   for (int k = 0; k < FPL; ++k) {
     const int f = lane + 32 * k;
@@ -439,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
   for (int bh = blockIdx.x; bh < BH; bh += gridDim.x) {
     if (pref[bh + 1] == pref[bh]) {
       for (int i = tid; i < G * D; i += kThreads) p.out[static_cast<size_t>(bh) * G * D + i] = 0.f;
+      if (p.lse != nullptr && tid < G) p.lse[static_cast<size_t>(bh) * G + tid] = -INFINITY;
     }
   }
   if (NP == 0) return;
@@ -791,6 +817,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const AttnPara
       }
       const bool whole = pref[cbh] >= r0 && pref[cbh + 1] <= r1;
       if (whole) {
+        if (p.lse != nullptr && lane < G) {
+          float mm = m_run[0], ll = lt[0];
+#pragma unroll
+          for (int i = 1; i < G; ++i)
+            if (lane == i) {
+              mm = m_run[i];
+              ll = lt[i];
+            }
+          p.lse[static_cast<size_t>(cbh) * G + lane] = row_lse(mm, ll);
+        }
         if (rowsel == 0) {
 #pragma unroll
           for (int i = 0; i < G; ++i) {
@@ -1006,6 +1042,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   for (int bh = blockIdx.x; bh < BH; bh += gridDim.x) {
     if (pref[bh + 1] == pref[bh]) {
       for (int i = tid; i < G * D; i += kThreads) p.out[static_cast<size_t>(bh) * G * D + i] = 0.f;
+      if (p.lse != nullptr && tid < G) p.lse[static_cast<size_t>(bh) * G + tid] = -INFINITY;
     }
   }
   if (NP == 0) return;
@@ -1456,6 +1493,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
       if (whole) {
         const float i0 = lt0 > 0.f ? 1.f / lt0 : 0.f, i1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
         float* ob = p.out + static_cast<size_t>(cbh) * G * D;
+        if (p.lse != nullptr && gq == 0) {
+          if (h0 < G) p.lse[static_cast<size_t>(cbh) * G + h0] = row_lse(m2[0], lt0);
+          if (h1 < G) p.lse[static_cast<size_t>(cbh) * G + h1] = row_lse(m2[1], lt1);
+        }
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           if (h0 < G) {
@@ -1658,8 +1699,8 @@ struct QuantTier {
 kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q, const void* k_pool,
                             const void* v_pool, const int32_t* expire_pool, int n_pages_cap,
                             const int32_t* page_table, int max_pages, const int32_t* count, const QuantTier* qt,
-                            int now, const int32_t* now_dev, float scale, float* out, int grid_limit, void* workspace,
-                            size_t workspace_bytes, int32_t* status, void* stream) {
+                            int now, const int32_t* now_dev, float scale, float* out, float* lse, int grid_limit,
+                            void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
   if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_pages < 0 || grid_limit < 0 || n_pages_cap < 0)
     return KVP_ERR_INVALID;
   if (n_q_heads % n_kv_heads != 0) return KVP_ERR_INVALID;
@@ -1675,6 +1716,7 @@ kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_d
     return KVP_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(expire_pool) || !aligned16(out))
     return KVP_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return KVP_ERR_ALIGN;
   if (qt != nullptr) {
     if (qt->max_pages < 0 || qt->n_pages_cap < 0) return KVP_ERR_INVALID;
     if (static_cast<int64_t>(qt->max_pages) * kPage > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
@@ -1720,7 +1762,8 @@ kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_d
                qt ? qt->count : nullptr,
                qt ? qt->max_pages : 0,
                qt ? qt->n_pages_cap : 0,
-               now_dev};
+               now_dev,
+               lse};
   // Eight query heads per kv head go to the tensor-core kernel: with the
   // CUDA-core page math a page takes twice the multiply-adds of G = 4 and the
   // kernel is bound by instruction issue (measured on a GB300, Llama-3-8B
@@ -1749,8 +1792,20 @@ extern "C" kvp_status kvp_decode_attn(int batch, int n_q_heads, int n_kv_heads, 
                                       const int32_t* count, int now, float scale, float* out, int grid_limit,
                                       void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
   return decode_attn_impl(batch, n_q_heads, n_kv_heads, head_dim, q, k_pool, v_pool, expire_pool, n_pages_cap,
-                          page_table, max_pages, count, nullptr, now, nullptr, scale, out, grid_limit, workspace,
-                          workspace_bytes, status, stream);
+                          page_table, max_pages, count, nullptr, now, nullptr, scale, out, nullptr, grid_limit,
+                          workspace, workspace_bytes, status, stream);
+}
+
+extern "C" kvp_status kvp_decode_attn_lse(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q,
+                                          const void* k_pool, const void* v_pool, const int32_t* expire_pool,
+                                          int n_pages_cap, const int32_t* page_table, int max_pages,
+                                          const int32_t* count, int now, float scale, float* out, float* lse,
+                                          int grid_limit, void* workspace, size_t workspace_bytes, int32_t* status,
+                                          void* stream) {
+  if (lse == nullptr) return KVP_ERR_INVALID;
+  return decode_attn_impl(batch, n_q_heads, n_kv_heads, head_dim, q, k_pool, v_pool, expire_pool, n_pages_cap,
+                          page_table, max_pages, count, nullptr, now, nullptr, scale, out, lse, grid_limit,
+                          workspace, workspace_bytes, status, stream);
 }
 
 extern "C" kvp_status kvp_decode_attn_devpos(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q,
@@ -1761,8 +1816,8 @@ extern "C" kvp_status kvp_decode_attn_devpos(int batch, int n_q_heads, int n_kv_
                                              int32_t* status, void* stream) {
   if (now_dev == nullptr) return KVP_ERR_INVALID;
   return decode_attn_impl(batch, n_q_heads, n_kv_heads, head_dim, q, k_pool, v_pool, expire_pool, n_pages_cap,
-                          page_table, max_pages, count, nullptr, 0, now_dev, scale, out, grid_limit, workspace,
-                          workspace_bytes, status, stream);
+                          page_table, max_pages, count, nullptr, 0, now_dev, scale, out, nullptr, grid_limit,
+                          workspace, workspace_bytes, status, stream);
 }
 
 extern "C" kvp_status kvp_decode_attn_two_tier(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q,
@@ -1775,6 +1830,80 @@ extern "C" kvp_status kvp_decode_attn_two_tier(int batch, int n_q_heads, int n_k
                                                size_t workspace_bytes, int32_t* status, void* stream) {
   const QuantTier qt{kq_pool, vq_pool, meta_pool, n_pages_cap_q, page_table_q, max_pages_q, count_q};
   return decode_attn_impl(batch, n_q_heads, n_kv_heads, head_dim, q, k_pool, v_pool, expire_pool, n_pages_cap,
-                          page_table, max_pages, count, &qt, now, nullptr, scale, out, grid_limit, workspace,
-                          workspace_bytes, status, stream);
+                          page_table, max_pages, count, &qt, now, nullptr, scale, out, nullptr, grid_limit,
+                          workspace, workspace_bytes, status, stream);
+}
+
+// ---------------------------------------------------------------- merging partial attention
+// Attention over a set of slots split into parts (each part's output row o_r
+// normalised over its own slots, and its log-sum-exp lse_r) is the same
+// attention over the union:
+//   lse = ln sum_r exp(lse_r),   o = sum_r exp(lse_r - lse) o_r.
+// One warp per row, lanes over float4 columns; a part with lse_r = -inf (no
+// slots) weighs nothing, and a row with no slots in any part is zero with
+// lse -inf.
+namespace kvp {
+namespace {
+
+constexpr int kMergeWarps = 8;
+
+__global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(int n_parts, int64_t rows, int d,
+                                                                      const float* __restrict__ outs,
+                                                                      const float* __restrict__ lses,
+                                                                      float* __restrict__ out,
+                                                                      float* __restrict__ lse_out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int r = lane; r < n_parts; r += 32) m = fmaxf(m, lses[static_cast<int64_t>(r) * rows + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const int f4 = d / 4;
+  float4* orow = reinterpret_cast<float4*>(out + row * d);
+  if (m == -INFINITY) {
+    for (int c = lane; c < f4; c += 32) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lse_out != nullptr && lane == 0) lse_out[row] = -INFINITY;
+    return;
+  }
+  float w_sum = 0.f;
+  for (int r = lane; r < n_parts; r += 32) w_sum += expf(lses[static_cast<int64_t>(r) * rows + row] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) w_sum += __shfl_xor_sync(0xffffffffu, w_sum, o);
+  const float inv = 1.f / w_sum;
+  for (int c = lane; c < f4; c += 32) {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < n_parts; ++r) {
+      const float w = expf(lses[static_cast<int64_t>(r) * rows + row] - m) * inv;
+      if (w == 0.f) continue;  // an empty part's row is not read
+      const float4 v = reinterpret_cast<const float4*>(outs + (static_cast<int64_t>(r) * rows + row) * d)[c];
+      a.x = fmaf(w, v.x, a.x);
+      a.y = fmaf(w, v.y, a.y);
+      a.z = fmaf(w, v.z, a.z);
+      a.w = fmaf(w, v.w, a.w);
+    }
+    orow[c] = a;
+  }
+  if (lse_out != nullptr && lane == 0) lse_out[row] = m + logf(w_sum);
+}
+
+}  // namespace
+}  // namespace kvp
+
+extern "C" kvp_status kvp_attn_merge(int n_parts, int64_t rows, int head_dim, const float* outs, const float* lses,
+                                     float* out, float* lse_out, void* stream) {
+  if (n_parts <= 0 || rows < 0 || head_dim <= 0 || head_dim % 4 != 0) return KVP_ERR_INVALID;
+  if (rows == 0) return KVP_OK;
+  if (outs == nullptr || lses == nullptr || out == nullptr) return KVP_ERR_INVALID;
+  if (!aligned16(outs) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lses) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(lse_out) & 3u) != 0)
+    return KVP_ERR_ALIGN;
+  const int64_t blocks = (rows + kMergeWarps - 1) / kMergeWarps;
+  if (blocks > 0x7fffffff) return KVP_ERR_UNSUPPORTED;
+  if (launch_pdl(attn_merge_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kMergeWarps * 32), 0,
+                 static_cast<cudaStream_t>(stream), n_parts, rows, head_dim, outs, lses, out, lse_out) != cudaSuccess)
+    return KVP_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }

@@ -246,6 +246,31 @@ def decode_attention(q_bits, cache: PagedCache, now: int, scale: float | None = 
     return out
 
 
+def decode_attention_lse(q_bits, cache: PagedCache, now: int, scale: float | None = None):
+    q = _c(q_bits, np.uint16)
+    B, Hq, d = q.shape
+    H = cache.count.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = np.empty((B, Hq, d), np.float32)
+    lse = np.empty((B, Hq), np.float64)
+    _L().kvpo_decode_attention_lse(_p(q), _I64(B), _I64(Hq), _I64(H), _I64(d), _p(cache.k_pool),
+                                   _p(cache.v_pool), _p(cache.expire_pool), _p(cache.page_table),
+                                   _I64(cache.page_table.shape[2]), _p(cache.count), _I64(now), _D(scale), _p(out),
+                                   _p(lse))
+    return out, lse
+
+
+def merge_attention(outs, lses):
+    o = _c(outs, np.float64)
+    ls = _c(lses, np.float64)
+    P, d = o.shape[0], o.shape[-1]
+    rows = int(np.prod(ls.shape[1:], dtype=np.int64))
+    out = np.empty(o.shape[1:], np.float64)
+    lse = np.empty(ls.shape[1:], np.float64)
+    _L().kvpo_merge_attention(_p(o), _p(ls), _I64(P), _I64(rows), _I64(d), _p(out), _p(lse))
+    return out, lse
+
+
 def dense_attention(q_bits, k_bits, v_bits, now: int, scale=None, lo=None):
     q, k, v = _c(q_bits, np.uint16), _c(k_bits, np.uint16), _c(v_bits, np.uint16)
     B, Hq, d = q.shape

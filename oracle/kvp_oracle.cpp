@@ -436,6 +436,68 @@ void kvpo_decode_attention(const uint16_t* q, int64_t B, int64_t Hq, int64_t H, 
   });
 }
 
+// The same attention with each row's softmax normaliser on the log scale:
+// lse[b, j] = ln sum_i exp(scale q[b, j] . k_i) over the present slots
+// (-inf, with a zero row, when there are none). lse [B, Hq] double.
+void kvpo_decode_attention_lse(const uint16_t* q, int64_t B, int64_t Hq, int64_t H, int64_t d,
+                               const uint16_t* k_pool, const uint16_t* v_pool, const int64_t* expire_pool,
+                               const int64_t* page_table, int64_t max_pages, const int64_t* count, int64_t now,
+                               double scale, float* out, double* lse) {
+  const int64_t g = Hq / H;
+  parallel_for(B * H, [&](int64_t u) {
+    const int64_t b = u / H, h = u % H;
+    std::vector<int64_t> rows;
+    for (int64_t j = 0; j < count[u]; ++j) {
+      const int64_t row = page_table[u * max_pages + j / kPage] * kPage + j % kPage;
+      if (now < expire_pool[row]) rows.push_back(row);
+    }
+    std::vector<double> qf(d), logit(rows.size()), o(d);
+    for (int64_t jq = h * g; jq < (h + 1) * g; ++jq) {
+      for (int64_t e = 0; e < d; ++e) qf[e] = widen(q[(b * Hq + jq) * d + e]);
+      double m = -INFINITY;
+      for (size_t i = 0; i < rows.size(); ++i) {
+        double dot = 0.0;
+        for (int64_t e = 0; e < d; ++e) dot += widen(k_pool[rows[i] * d + e]) * qf[e];
+        logit[i] = dot * scale;
+        m = std::max(m, logit[i]);
+      }
+      double den = 0.0;
+      for (int64_t e = 0; e < d; ++e) o[e] = 0.0;
+      for (size_t i = 0; i < rows.size(); ++i) {
+        const double w = std::exp(logit[i] - m);
+        den += w;
+        for (int64_t e = 0; e < d; ++e) o[e] += w * widen(v_pool[rows[i] * d + e]);
+      }
+      for (int64_t e = 0; e < d; ++e) out[(b * Hq + jq) * d + e] = rows.empty() ? 0.f : static_cast<float>(o[e] / den);
+      lse[b * Hq + jq] = rows.empty() ? -INFINITY : m + std::log(den);
+    }
+  });
+}
+
+// Attention over the union of disjoint parts from each part's rows
+// (normalised over the part) and lse: lse = ln sum_p exp(lse_p), out = sum_p
+// exp(lse_p - lse) out_p; parts with lse -inf weigh nothing, a row with none
+// is zero with lse -inf. outs [P, rows, d], lses [P, rows] double.
+void kvpo_merge_attention(const double* outs, const double* lses, int64_t P, int64_t rows, int64_t d, double* out,
+                          double* lse) {
+  for (int64_t r = 0; r < rows; ++r) {
+    double m = -INFINITY;
+    for (int64_t p = 0; p < P; ++p) m = std::max(m, lses[p * rows + r]);
+    for (int64_t e = 0; e < d; ++e) out[r * d + e] = 0.0;
+    if (m == -INFINITY) {
+      lse[r] = -INFINITY;
+      continue;
+    }
+    double total = 0.0;
+    for (int64_t p = 0; p < P; ++p) total += std::exp(lses[p * rows + r] - m);
+    for (int64_t p = 0; p < P; ++p) {
+      const double w = std::exp(lses[p * rows + r] - m) / total;
+      for (int64_t e = 0; e < d; ++e) out[r * d + e] += w * outs[(p * rows + r) * d + e];
+    }
+    lse[r] = m + std::log(total);
+  }
+}
+
 // Brute force over the dense cache K/V [B, T, H, d]: every position in
 // [lo, now] (no pages, no masks).
 void kvpo_dense_attention(const uint16_t* q, int64_t B, int64_t Hq, const uint16_t* k, const uint16_t* v, int64_t T,

@@ -315,6 +315,56 @@ def decode_attention(q_bits, cache: PagedCache, now: int, scale: float | None = 
     return out.astype(np.float32)
 
 
+def decode_attention_lse(q_bits, cache: PagedCache, now: int, scale: float | None = None):
+    """decode_attention's rows and, for each, the natural log of the softmax's
+    normaliser: lse[b, j] = ln sum_i exp(q[b, j] . k_i * scale) over the same
+    present slots (-inf and a zero row for an empty set). Returns (float32
+    [B, Hq, d], float64 [B, Hq])."""
+    B, Hq, d = q_bits.shape
+    H = cache.count.shape[1]
+    g = Hq // H
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    q = widen_bf16(q_bits)
+    out = np.zeros((B, Hq, d))
+    lse = np.full((B, Hq), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            slots = np.arange(cache.count[b, h])
+            pg, row = cache.slot_rows(b, h, slots)
+            sel = present(cache.expire_pool[pg, row], now)
+            K = widen_bf16(cache.k_pool[pg[sel], row[sel]])
+            V = widen_bf16(cache.v_pool[pg[sel], row[sel]])
+            if K.shape[0] == 0:
+                continue
+            for j in range(h * g, (h + 1) * g):
+                logits = (K @ q[b, j]) * scale
+                m = logits.max()
+                w = np.exp(logits - m)
+                out[b, j] = (w @ V) / w.sum()
+                lse[b, j] = m + math.log(w.sum())
+    return out.astype(np.float32), lse
+
+
+def merge_attention(outs, lses):
+    """Attention over the union of disjoint parts of a row's slots, from each
+    part's attention row o_p (normalised over its own part) and its lse_p:
+    lse = ln sum_p exp(lse_p), o = sum_p exp(lse_p - lse) o_p. A part with
+    lse_p = -inf has no slots and weighs nothing; a row with no slots in any
+    part is zero with lse -inf. outs [P, ..., d], lses [P, ...]. Returns
+    (float64 [..., d], float64 [...])."""
+    outs = np.asarray(outs, np.float64)
+    lses = np.asarray(lses, np.float64)
+    m = lses.max(axis=0)
+    has = m > -np.inf
+    m_safe = np.where(has, m, 0.0)
+    w = np.where(has[None], np.exp(lses - m_safe[None]), 0.0)
+    total = w.sum(axis=0)
+    lse = np.where(has, m_safe + np.log(np.where(has, total, 1.0)), -np.inf)
+    wn = np.where(has[None], w / np.where(has, total, 1.0)[None], 0.0)
+    out = (wn[..., None] * outs).sum(axis=0)
+    return out, lse
+
+
 def dense_attention(q_bits, k_bits, v_bits, now: int, scale=None, lo=None):
     """Brute force over the dense cache [B, T, H, d]: every position in
     [lo, now] (lo = 0 by default). No pages, no masks."""
