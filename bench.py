@@ -682,7 +682,8 @@ def main():
     ap.add_argument("--workload", default="llama65b_mha_decode",
                     choices=["llama65b_mha_decode", "mlp_prefill", "dms_decode", "llama65b_mha", "prune_sweep",
                              "prune_sweep_long",
-                             "threshold", "quant_tier", "quant_decode", "gqa_sweep", "mla_sweep", "mla_dms_decode"],
+                             "threshold", "quant_tier", "quant_tier_mha", "quant_decode", "gqa_sweep", "mla_sweep",
+                             "mla_dms_decode"],
                     help="llama65b_mha_decode = the bench line; the others print measurement lines "
                          "(see bench_workloads.py)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -482,7 +482,24 @@ def quant_tier(kvp, dev, peaks, seed=0, calls=10, reps=5):
     some form). Times the fp8-tier compaction and the two-tier attention (CUDA
     graphs of 10 calls) next to the one-tier attention over the bf16 tier
     alone; bytes are the pages each call reads."""
-    B, T, H, Hq, d, W = 16, 8192, 8, 32, 128, 128
+    pts = _quant_tier(kvp, dev, peaks, 16, 8192, 8, 32, 128, seed, calls, reps)
+    return {"workload": "quant_tier: Llama-3-8B layer (batch 16 x 8192 tokens, 32 q / 8 kv heads, head_dim 128), "
+                        "tau at the 75th percentile, fp8 tier for tau_q <= s < tau; CUDA graphs of 10 calls",
+            "points": pts}
+
+
+def quant_tier_mha(kvp, dev, peaks, seed=0, calls=5, reps=3):
+    """The same tiers on one layer of the 65B-shaped MHA stack (batch 1,
+    131,072 cached tokens, 64 heads, one query head per kv head, head_dim
+    128): tau at the 75th percentile, tau_q at the 50th / 25th / -inf."""
+    pts = _quant_tier(kvp, dev, peaks, 1, 131072, 64, 64, 128, seed, calls, reps)
+    return {"workload": "quant_tier_mha: one 65B-shaped MHA layer (batch 1 x 131072 tokens, 64 heads, head_dim 128), "
+                        "tau at the 75th percentile, fp8 tier for tau_q <= s < tau; CUDA graphs of 5 calls",
+            "points": pts}
+
+
+def _quant_tier(kvp, dev, peaks, B, T, H, Hq, d, seed, calls, reps):
+    W = 128
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
     K = _randn_bf16((B, T, H, d), g, dev)
@@ -538,9 +555,7 @@ def quant_tier(kvp, dev, peaks, seed=0, calls=10, reps=5):
                        "attention_us": ms_two * 1e3, "attention_bytes": nbytes,
                        "frac_of_hbm": nbytes / (ms_two * 1e-3) / 1e9 / peaks[0],
                        "decode_tokens_per_s": B / (ms_two * 1e-3)})
-    return {"workload": "quant_tier: Llama-3-8B layer (batch 16 x 8192 tokens, 32 q / 8 kv heads, head_dim 128), "
-                        "tau at the 75th percentile, fp8 tier for tau_q <= s < tau; CUDA graphs of 10 calls",
-            "points": points}
+    return points
 
 
 def quant_decode(kvp, dev, peaks, seed=0, steps=64, reps=3):
@@ -783,7 +798,7 @@ def mla_dms_decode(kvp, dev, peaks, seed=0, steps=256):
 
 RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha,
            "prune_sweep": prune_sweep, "prune_sweep_long": prune_sweep_long, "threshold": threshold,
-           "quant_tier": quant_tier, "quant_decode": quant_decode, "gqa_sweep": gqa_sweep, "mla_sweep": mla_sweep,
+           "quant_tier": quant_tier, "quant_tier_mha": quant_tier_mha, "quant_decode": quant_decode, "gqa_sweep": gqa_sweep, "mla_sweep": mla_sweep,
            "mla_dms_decode": mla_dms_decode}
 
 

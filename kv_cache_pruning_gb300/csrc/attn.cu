@@ -1647,6 +1647,10 @@ kvp_status dispatch_mma(const AttnParams& p, int G, int grid_limit, cudaStream_t
   if (kQ && rows_q > 0 &&
       (!make_tmap_u8_rows(&tmKq, p.kq_pool, rows_q, D, kPage) || !make_tmap_u8_rows(&tmVq, p.vq_pool, rows_q, D, kPage)))
     return KVP_ERR_CUDA;
+  if constexpr (kQ) {
+    if (G == 1) return launch_attn_mma<D, 1, kQ>(p, tmK, tmV, tmKq, tmVq, grid_limit, st);
+    if (G == 2) return launch_attn_mma<D, 2, kQ>(p, tmK, tmV, tmKq, tmVq, grid_limit, st);
+  }
   if (G == 4) return launch_attn_mma<D, 4, kQ>(p, tmK, tmV, tmKq, tmVq, grid_limit, st);
   if (G != 8) return KVP_ERR_UNSUPPORTED;
   return launch_attn_mma<D, 8, kQ>(p, tmK, tmV, tmKq, tmVq, grid_limit, st);
@@ -1695,6 +1699,13 @@ struct QuantTier {
   int max_pages;
   const int32_t* count;
 };
+
+// Two-tier calls from this many query heads per kv head on go to the tensor-core kernel (the CUDA-core kernel
+// keeps any below it); 1: all of them.
+#ifndef KVP_TWO_TIER_MMA_FROM
+#define KVP_TWO_TIER_MMA_FROM 1
+#endif
+constexpr int kTwoTierMmaFrom = KVP_TWO_TIER_MMA_FROM;
 
 kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q, const void* k_pool,
                             const void* v_pool, const int32_t* expire_pool, int n_pages_cap,
@@ -1767,13 +1778,15 @@ kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_d
   // Eight query heads per kv head go to the tensor-core kernel: with the
   // CUDA-core page math a page takes twice the multiply-adds of G = 4 and the
   // kernel is bound by instruction issue (measured on a GB300, Llama-3-8B
-  // cache, keep-all: 192 against 95 us). So do four with an fp8 tier (the same
-  // cache, a quarter / half / three quarters of the entries in the fp8 tier:
-  // 61.1 / 85.1 / 108.5 against 64.6 / 91.0 / 116.8 us). Otherwise up to four
-  // the CUDA-core kernel is as fast or faster (75 % pruned at G = 4: 34.1
-  // against 34.5 us). The tensor-core kernel reads the pools through tensor
-  // maps, whose row coordinates stay below 2^31.
-  const bool mma = (G == 8 || (G == 4 && qt != nullptr)) && n_pages_cap > 0 &&
+  // cache, keep-all: 192 against 95 us). So do two-tier calls at every G,
+  // where the tensor-core kernel reads a fp8 page's codes in place (Llama-3-8B
+  // cache at G = 4, a quarter / half / three quarters of the entries in the
+  // fp8 tier: 43.0 / 55.3 / 68.5 against 64.6 / 91.0 / 116.8 us; a 65B-shaped
+  // MHA layer at G = 1: 249 / 347 / 458 against 301 / 446 / 588 us). One-tier
+  // calls up to four stay on the CUDA-core kernel, as fast or faster there
+  // (75 % pruned at G = 4: 34.1 against 34.5 us). The tensor-core kernel reads
+  // the pools through tensor maps, whose row coordinates stay below 2^31.
+  const bool mma = (G == 8 || (qt != nullptr && G >= kTwoTierMmaFrom)) && n_pages_cap > 0 &&
                    static_cast<int64_t>(n_pages_cap) * kPage <= 0x7fffffff;
   if (qt != nullptr) {
     if (mma)
