@@ -547,7 +547,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
     if (ws.ok[0] == 0) return;
     base = ws.base[bh];
   }
-  if (!live) return;
+  // a warp past the last segment has nothing to list; with wide rows it stays for the CTA's shared copy below
+  if (kNarrow && !live) return;
   slot0 = __reduce_add_sync(0xffffffffu, slot0);
   const int cnt = count[bh];
   const int pages = (cnt + reserve + kPage - 1) / kPage;
@@ -605,35 +606,55 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
 
   // ---- move the rows through the stage
   if constexpr (!kNarrow) {
-    // wide rows: the warp's lanes walk the batch's (entry, piece) pairs in
-    // order; batch b + 1 is requested into the other buffer before batch b
-    // is stored
+    // wide rows: the CTA's kept rows (its warps' lists one after another, all
+    // of the same (b, h)) are shared out evenly over its warps, so that a
+    // segment kept whole (the recent window) does not fall to one warp alone;
+    // each warp's share goes through its two stage buffers, batch b + 1
+    // requested into the other buffer before batch b is stored
     static_assert(kBufs == 2, "wide rows use two stage buffers");
-    auto load = [&](int i0, uint4* buf) {
-      const int nb = min(kSt, nk - i0);
-      for (int x = lane; x < nb * E16; x += 32) {
-        const int i = x / E16, pc = x - i * E16;
-        cp_async16(buf + x, reinterpret_cast<const uint4*>(sv.kb + lst[i0 + i] * sv.stride) + pc);
+    __shared__ int s_nk[kWarpsPerCta], s_slot0[kWarpsPerCta];
+    if (lane == 0) {
+      s_nk[warp] = nk;
+      s_slot0[warp] = slot0;
+    }
+    __syncthreads();
+    int pre[kWarpsPerCta + 1];
+    pre[0] = 0;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerCta; ++w) pre[w + 1] = pre[w] + s_nk[w];
+    const int tot = pre[kWarpsPerCta];
+    const int c_lo = warp * tot / kWarpsPerCta, c_hi = (warp + 1) * tot / kWarpsPerCta;
+    const int64_t* lst_cta = reinterpret_cast<const int64_t*>(sm_raw + kWarpsPerCta * kBufs * kSt * E16 * 16);
+    // the source row of entry c of the CTA's list (its warp's list holds it at c - pre[w]); the same in every lane
+    auto src_row_of = [&](int c) {
+      int w = 0;
+#pragma unroll
+      for (int u = 1; u < kWarpsPerCta; ++u) w += c >= pre[u] ? 1 : 0;
+      return lst_cta[w * kSeg + (c - pre[w])];
+    };
+    // the CTA's entries take consecutive slots from its first warp's on, so a batch lands in consecutive rows
+    const int64_t row_cta = static_cast<int64_t>(base) * kPage + s_slot0[0];
+    auto load = [&](int c0, uint4* buf) {
+      const int nb = min(kSt, c_hi - c0);
+      for (int i = 0; i < nb; ++i) {
+        const uint4* src = reinterpret_cast<const uint4*>(sv.kb + src_row_of(c0 + i) * sv.stride);
+        for (int pc = lane; pc < E16; pc += 32) cp_async16(buf + i * E16 + pc, src + pc);
       }
       cp_async_commit();
     };
-    if (nk > 0) load(0, stage);
-    for (int b = 0, i0 = 0; i0 < nk; ++b, i0 += kSt) {
+    if (c_lo < c_hi) load(c_lo, stage);
+    for (int b = 0, c0 = c_lo; c0 < c_hi; ++b, c0 += kSt) {
       uint4* cur = stage + (b & 1) * kSt * E16;
-      if (i0 + kSt < nk) {
-        load(i0 + kSt, stage + ((b + 1) & 1) * kSt * E16);
+      if (c0 + kSt < c_hi) {
+        load(c0 + kSt, stage + ((b + 1) & 1) * kSt * E16);
         cp_async_wait_one();  // this lane's copies of batch b have landed
       } else {
         cp_async_wait_all();
       }
       __syncwarp();  // and every lane's
-      const int nb = min(kSt, nk - i0);
-      for (int x = lane; x < nb * E16; x += 32) {
-        const int i = x / E16, pc = x - i * E16;
-        const int j = slot0 + i0 + i;
-        const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
-        reinterpret_cast<uint4*>(k_pool + row * D)[pc] = cur[x];
-      }
+      const int nb = min(kSt, c_hi - c0);
+      uint4* dst = reinterpret_cast<uint4*>(k_pool + (row_cta + c0) * D);
+      for (int x = lane; x < nb * E16; x += 32) dst[x] = cur[x];
       __syncwarp();  // every lane is done with this buffer before it is refilled
     }
     return;
