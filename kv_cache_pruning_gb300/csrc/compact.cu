@@ -439,24 +439,26 @@ constexpr int kStage = 20;
 // An entry is NPOOL rows of D bf16 values: a K and a V row (NPOOL = 2), or
 // one latent row of an MLA cache (NPOOL = 1, D = 576: 72 pieces of 16 bytes,
 // moved kStageWide at a time through two stage buffers, so that one batch is
-// loading while the other is stored).
+// loading while the other is stored). The quantizing copy (kQ) splits the
+// same bytes into two buffers of kStage / 2 entries, so that its arithmetic
+// on one batch overlaps the next batch's loads.
 constexpr int kStageWide = 8;
 template <int D, int NPOOL>
 constexpr int entry_pieces() {
   return NPOOL * D * 2 / 16;
 }
-template <int D, int NPOOL>
+template <int D, int NPOOL, bool kQ>
 constexpr int stage_entries() {
-  return entry_pieces<D, NPOOL>() > 32 ? kStageWide : kStage;
+  return entry_pieces<D, NPOOL>() > 32 ? kStageWide : (kQ ? kStage / 2 : kStage);
 }
-template <int D, int NPOOL>
+template <int D, int NPOOL, bool kQ>
 constexpr int stage_buffers() {
-  return entry_pieces<D, NPOOL>() > 32 ? 2 : 1;
+  return (entry_pieces<D, NPOOL>() > 32 || kQ) ? 2 : 1;
 }
-template <int D, int NPOOL>
+template <int D, int NPOOL, bool kQ>
 constexpr int scatter_smem_bytes() {
-  return kWarpsPerCta * (stage_buffers<D, NPOOL>() * stage_entries<D, NPOOL>() * entry_pieces<D, NPOOL>() * 16 +
-                         kSeg * 8);
+  return kWarpsPerCta *
+         (stage_buffers<D, NPOOL, kQ>() * stage_entries<D, NPOOL, kQ>() * entry_pieces<D, NPOOL>() * 16 + kSeg * 8);
 }
 
 template <int D, int NPOOL, class Src, bool kFused>
@@ -473,10 +475,10 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
   constexpr int E16 = entry_pieces<D, NPOOL>();  // 16-byte pieces per entry (K row then V row, or the latent row)
   constexpr bool kNarrow = E16 <= 32 && 32 % E16 == 0;  // whole entries per warp instruction
   constexpr int EPI = kNarrow ? 32 / E16 : 1;    // entries per warp instruction (1 for D = 128, 2 for D = 64)
-  constexpr int kSt = stage_entries<D, NPOOL>();
   // fp8 tier: k_pool / v_pool hold E4M3 codes (D bytes a row) and expire_pool
   // is the per-page record [start x 16, K scale x 16, V scale x 16]
   constexpr bool kQuant = std::is_same<Src, QuantSrc>::value;
+  constexpr int kSt = stage_entries<D, NPOOL, kQuant>();
   static_assert(NPOOL == 2 || (!kQuant && !kNarrow), "one-pool entries are the wide latent rows");
   constexpr int kMetaStride = kQuant ? kQuantMetaWords : kPage;
   extern __shared__ __align__(16) uint8_t sm_raw[];
@@ -486,7 +488,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
   const int warp = threadIdx.x >> 5;
   const int sg = blockIdx.y * kWarpsPerCta + warp;
   const int lane = threadIdx.x & 31;
-  constexpr int kBufs = stage_buffers<D, NPOOL>();
+  constexpr int kBufs = stage_buffers<D, NPOOL, kQuant>();
   uint4* stage = reinterpret_cast<uint4*>(sm_raw) + warp * kBufs * kSt * E16;
   int64_t* lst = reinterpret_cast<int64_t*>(sm_raw + kWarpsPerCta * kBufs * kSt * E16 * 16) + warp * kSeg;
   const bool live = sg < NS;
@@ -665,11 +667,28 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
   const int vi = is_v ? piece - E16 / 2 : piece;
   const uint16_t* sbase = is_v ? sv.vb : sv.kb;
   uint16_t* dbase = is_v ? v_pool : k_pool;
-  for (int i0 = 0; i0 < nk; i0 += kSt) {
+  // the entries of batch i0 .. into buf, as one group of async copies
+  auto load_batch = [&](int i0, uint4* buf) {
     const int nb = min(kSt, nk - i0);
     for (int i = sub; i < nb; i += EPI)
-      cp_async16(stage + i * E16 + piece, reinterpret_cast<const uint4*>(sbase + lst[i0 + i] * sv.stride) + vi);
-    cp_async_wait_all();
+      cp_async16(buf + i * E16 + piece, reinterpret_cast<const uint4*>(sbase + lst[i0 + i] * sv.stride) + vi);
+    cp_async_commit();
+  };
+  if (kBufs == 2 && nk > 0) load_batch(0, stage);
+  for (int i0 = 0, bt = 0; i0 < nk; i0 += kSt, ++bt) {
+    const int nb = min(kSt, nk - i0);
+    uint4* cur = stage + (bt & (kBufs - 1)) * kSt * E16;
+    if constexpr (kBufs == 2) {  // the next batch is requested into the other buffer before this one is used
+      if (i0 + kSt < nk) {
+        load_batch(i0 + kSt, stage + ((bt + 1) & 1) * kSt * E16);
+        cp_async_wait_one();
+      } else {
+        cp_async_wait_all();
+      }
+    } else {
+      load_batch(i0, cur);
+      cp_async_wait_all();
+    }
     __syncwarp();
     if constexpr (kQuant) {
       // Three steps per batch. (1) Each row's amax, reduced over its E16 / 2
@@ -686,7 +705,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
 #pragma unroll 4
       for (int ib = 0; ib < nb; ib += EPI) {
         const int i = ib + sub;
-        const uint4 w = i < nb ? stage[i * E16 + piece] : make_uint4(0, 0, 0, 0);
+        const uint4 w = i < nb ? cur[i * E16 + piece] : make_uint4(0, 0, 0, 0);
         const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                             bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
         float amax = 0.f;
@@ -721,7 +740,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
         const float inv_v = __shfl_sync(0xffffffffu, iv, i & 31);
         if (i < nb) {
           const float inv = is_v ? inv_v : ink;
-          const uint4 w = stage[i * E16 + piece];
+          const uint4 w = cur[i * E16 + piece];
           const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                               bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
           uint32_t packed[2] = {0u, 0u};
@@ -741,7 +760,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
       for (int i = sub; i < nb; i += EPI) {
         const int j = slot0 + i0 + i;
         const int64_t row = static_cast<int64_t>(base + (j >> 4)) * kPage + (j & 15);
-        reinterpret_cast<uint4*>(dbase + row * D)[vi] = stage[i * E16 + piece];
+        reinterpret_cast<uint4*>(dbase + row * D)[vi] = cur[i * E16 + piece];
       }
     }
     __syncwarp();
@@ -947,14 +966,15 @@ kvp_status run_compact(const Src& src, int BH, int NS, int head_dim, int now, in
   if (!fused) base_kernel<<<1, 1024, 0, st>>>(BH, reserve, max_pages, n_pages_cap, ws, count, status);
   auto* kp = static_cast<uint16_t*>(k_pool);
   auto* vp = static_cast<uint16_t*>(v_pool);
+  constexpr bool kQ = std::is_same<Src, QuantSrc>::value;
 #define KVP_SCATTER(DIM, NP, FUSED)                                                                          \
   do {                                                                                                        \
     static const bool attr_ok = cudaFuncSetAttribute(scatter_kernel<DIM, NP, Src, FUSED>,                    \
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,            \
-                                                     scatter_smem_bytes<DIM, NP>()) == cudaSuccess;           \
+                                                     scatter_smem_bytes<DIM, NP, kQ>()) == cudaSuccess;       \
     if (!attr_ok) return KVP_ERR_CUDA;                                                                        \
     if (launch_pdl(scatter_kernel<DIM, NP, Src, FUSED>, grid_t, dim3(kWarpsPerCta * 32),                     \
-                   scatter_smem_bytes<DIM, NP>(), st, src, now, NS, reserve, max_pages, n_pages_cap, BH, ws,  \
+                   scatter_smem_bytes<DIM, NP, kQ>(), st, src, now, NS, reserve, max_pages, n_pages_cap, BH, ws, \
                    static_cast<const int32_t*>(count), status, kp, vp, expire_pool, page_table,                \
                    remap) != cudaSuccess)                                                                     \
       return KVP_ERR_CUDA;                                                                                    \
