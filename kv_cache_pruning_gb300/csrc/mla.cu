@@ -1027,11 +1027,14 @@ __global__ void __launch_bounds__(kCThreads, 1) mla_tc_kernel(const MlaParams p,
         tc_fence_after();
         const uint32_t base = ring_u32 + (i % kCRing) * kCStageBytes;
         const uint32_t d = tmem + kTcBufCol + (i % kCBufs) * kCTok;
+        // the descriptor once per block; each product adds its box's offset to the start-address field (in
+        // 16-byte units; shared addresses stay below 256 KB, so the field cannot carry into the next)
+        const uint64_t bdesc0 = sw128_kmajor_desc(base);
+        umma_bf16_tmem_a(d, tmem + kTcQCol, bdesc0, idS, 0u);
 #pragma unroll
-        for (int kk = 0; kk < kRow / 16; ++kk) {
-          const uint64_t bdesc = sw128_kmajor_desc(base + (kk >> 2) * kCBoxRun + (kk & 3) * 32);
-          umma_bf16_tmem_a(d, tmem + kTcQCol + kk * 8, bdesc, idS, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 1; kk < kRow / 16; ++kk)
+          umma_bf16_tmem_a_acc(d, tmem + kTcQCol + kk * 8,
+                               bdesc0 + static_cast<uint64_t>(((kk >> 2) * kCBoxRun + (kk & 3) * 32) >> 4), idS);
         umma_commit(&s_full[i % kCBufs]);
         return true;
       };
