@@ -683,7 +683,7 @@ def main():
                     choices=["llama65b_mha_decode", "mlp_prefill", "dms_decode", "llama65b_mha", "prune_sweep",
                              "prune_sweep_long",
                              "threshold", "quant_tier", "quant_tier_mha", "quant_decode", "gqa_sweep", "mla_sweep",
-                             "mla_dms_decode"],
+                             "mla_dms_decode", "seq_split"],
                     help="llama65b_mha_decode = the bench line; the others print measurement lines "
                          "(see bench_workloads.py)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -796,10 +796,77 @@ def mla_dms_decode(kvp, dev, peaks, seed=0, steps=256):
             "points": points}
 
 
+def seq_split(kvp, dev, peaks, seed=0, calls=5, reps=3):
+    """A long sequence attended in two parts and merged on the device (the
+    building blocks of a sequence split): one 65B-shaped MHA layer (batch 1,
+    131,072 cached tokens, 64 heads, head_dim 128), tau at each head's 75th
+    percentile; the cache of the whole sequence against two caches of its
+    halves, each attended with its log-sum-exp (kvp_decode_attn_lse) and the
+    rows merged (kvp_attn_merge); CUDA graphs of 5 calls."""
+    B, T, H, d, W = 1, 131072, 64, 128, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    K = _randn_bf16((B, T, H, d), g, dev)
+    V = _randn_bf16((B, T, H, d), g, dev)
+    q = _randn_bf16((B, H, d), g, dev)
+    s = torch.randn((B, T, H), generator=g, device=dev)
+    tau = _tau_quantile(kvp, s, 0.75)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    # a part's positions count from its first token: the second half is compacted and attended at its own
+    # step T / 2 - 1, so that its last 128 tokens are the recent window the whole sequence keeps
+    def cache_of(lo, hi, now):
+        n = hi - lo
+        mp = (n + 15) // 16
+        c = kvp.PagedKV.allocate(B, H, d, B * H * mp, mp, device=dev)
+        ws = torch.empty(kvp.kvp_compact_workspace_bytes(B, H, n), dtype=torch.uint8, device=dev)
+        kvp.kvp_compact_masked(K[:, lo:hi], V[:, lo:hi], now, 0, c, mode=kvp.KVP_MASK_KVZAP,
+                               scores=s[:, lo:hi].contiguous().view(B * n, H), tau=tau, window=W, status=st,
+                               workspace=ws)
+        return c
+
+    nows = [T - 1, T // 2 - 1]
+    whole = cache_of(0, T, T - 1)
+    parts = [cache_of(0, T // 2, nows[0]), cache_of(T // 2, T, nows[1])]
+    torch.cuda.synchronize()
+    assert st.item() == 0, kvp.status_string(st.item())
+    ws_a = [torch.zeros(kvp.kvp_decode_attn_workspace_bytes(B, H, H, d), dtype=torch.uint8, device=dev)
+            for _ in range(3)]
+    out = torch.empty(B, H, d, dtype=torch.float32, device=dev)
+    outs = torch.empty(2, B, H, d, dtype=torch.float32, device=dev)
+    lses = torch.empty(2, B, H, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, H, dtype=torch.float32, device=dev)
+
+    def one():
+        for _ in range(calls):
+            kvp.kvp_decode_attn(q, whole, T - 1, out=out, workspace=ws_a[0], status=st)
+
+    def split():
+        for _ in range(calls):
+            for i in range(2):
+                kvp.kvp_decode_attn_lse(q, parts[i], nows[i], out=outs[i], lse=lses[i], workspace=ws_a[1 + i],
+                                        status=st)
+            kvp.kvp_attn_merge(outs, lses, out=out, lse=lse)
+
+    ms_one = _time(_graph(one), reps=reps) / calls
+    ms_split = _time(_graph(split), reps=reps) / calls
+    torch.cuda.synchronize()
+    assert st.item() == 0, kvp.status_string(st.item())
+    pages = [int(((c.count + 15) // 16).sum().item()) for c in (whole, *parts)]
+    page_bytes = 16 * (2 * d * 2 + 4)
+    return {"workload": "seq_split: one 65B-shaped MHA layer (batch 1 x 131072 tokens, 64 heads, head_dim 128), tau at "
+                        "the 75th percentile; whole cache against two half caches attended with their log-sum-exps "
+                        "and merged; CUDA graphs of 5 calls",
+            "points": [{"form": "whole", "pages": pages[0], "attention_us": ms_one * 1e3,
+                        "frac_of_hbm": pages[0] * page_bytes / (ms_one * 1e-3) / 1e9 / peaks[0]},
+                       {"form": "two halves + merge", "pages": pages[1] + pages[2], "attention_us": ms_split * 1e3,
+                        "frac_of_hbm": (pages[1] + pages[2]) * page_bytes / (ms_split * 1e-3) / 1e9 / peaks[0]}]}
+
+
 RUNNERS = {"mlp_prefill": mlp_prefill, "dms_decode": dms_decode, "llama65b_mha": llama65b_mha,
            "prune_sweep": prune_sweep, "prune_sweep_long": prune_sweep_long, "threshold": threshold,
            "quant_tier": quant_tier, "quant_tier_mha": quant_tier_mha, "quant_decode": quant_decode, "gqa_sweep": gqa_sweep, "mla_sweep": mla_sweep,
-           "mla_dms_decode": mla_dms_decode}
+           "mla_dms_decode": mla_dms_decode, "seq_split": seq_split}
 
 
 def run(name, kvp, dev, peaks):
