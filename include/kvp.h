@@ -542,10 +542,11 @@ KVP_API kvp_status kvp_attn_merge(int n_parts, int64_t rows, int head_dim, const
  * over the persistent grid like kvp_decode_attn's.
  *
  * Arguments up to `count` and from `now` on: as kvp_decode_attn (same
- * workspace size and rules). At 4 and 8 query heads per kv head a fp8
- * page's codes are turned into fp16 (exactly) and multiplied by the query
- * converted to fp16, which is exact for bf16 values of magnitude
- * 2^-17 .. 65504; its softmax weights, times the V row scale, enter the
+ * workspace size and rules). On the tensor cores (every G, unless the
+ * pools pass 2^31 rows) a fp8 page's codes are turned into fp16 (exactly)
+ * and multiplied by the query converted to fp16, which is exact for bf16
+ * values of magnitude 2^-17 .. 65504; its softmax weights, times the V row
+ * scale, enter the
  * P.V product as one fp16 value each (relative error <= 2^-11, subnormal
  * below 2^-14). kq_pool, vq_pool, meta_pool (16-byte aligned),
  * n_pages_cap_q, page_table_q (width max_pages_q), count_q: the fp8 tier as
