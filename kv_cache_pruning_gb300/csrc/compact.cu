@@ -420,6 +420,7 @@ KVP_DEV void cp_async_wait_all() {
 // one group (the newest) is still in flight.
 KVP_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 KVP_DEV void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+KVP_DEV void cp_async_wait_two() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
 
 // Copy pass: one warp per 128-entry segment of one (b, h); grid
 // (B*H, ceil(NS / 4)). The warp lists the segment's present entries (source
@@ -438,8 +439,8 @@ constexpr int kStage = 20;
 
 // An entry is NPOOL rows of D bf16 values: a K and a V row (NPOOL = 2), or
 // one latent row of an MLA cache (NPOOL = 1, D = 576: 72 pieces of 16 bytes,
-// moved kStageWide at a time through two stage buffers, so that one batch is
-// loading while the other is stored). The quantizing copy (kQ) splits the
+// moved kStageWide at a time through three stage buffers, so that two batches
+// are loading while a third is stored). The quantizing copy (kQ) splits the
 // same bytes into two buffers of kStage / 2 entries, so that its arithmetic
 // on one batch overlaps the next batch's loads.
 constexpr int kStageWide = 8;
@@ -453,7 +454,7 @@ constexpr int stage_entries() {
 }
 template <int D, int NPOOL, bool kQ>
 constexpr int stage_buffers() {
-  return (entry_pieces<D, NPOOL>() > 32 || kQ) ? 2 : 1;
+  return entry_pieces<D, NPOOL>() > 32 ? 3 : (kQ ? 2 : 1);
 }
 template <int D, int NPOOL, bool kQ>
 constexpr int scatter_smem_bytes() {
@@ -611,9 +612,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
     // wide rows: the CTA's kept rows (its warps' lists one after another, all
     // of the same (b, h)) are shared out evenly over its warps, so that a
     // segment kept whole (the recent window) does not fall to one warp alone;
-    // each warp's share goes through its two stage buffers, batch b + 1
-    // requested into the other buffer before batch b is stored
-    static_assert(kBufs == 2, "wide rows use two stage buffers");
+    // each warp's share goes through its three stage buffers, batches b + 1
+    // and b + 2 requested before batch b is stored
+    static_assert(kBufs == 3, "wide rows use three stage buffers");
     __shared__ int s_nk[kWarpsPerCta], s_slot0[kWarpsPerCta];
     if (lane == 0) {
       s_nk[warp] = nk;
@@ -645,11 +646,15 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) scatter_kernel(Src src, int
       cp_async_commit();
     };
     if (c_lo < c_hi) load(c_lo, stage);
+    if (c_lo + kSt < c_hi) load(c_lo + kSt, stage + kSt * E16);
     for (int b = 0, c0 = c_lo; c0 < c_hi; ++b, c0 += kSt) {
-      uint4* cur = stage + (b & 1) * kSt * E16;
-      if (c0 + kSt < c_hi) {
-        load(c0 + kSt, stage + ((b + 1) & 1) * kSt * E16);
-        cp_async_wait_one();  // this lane's copies of batch b have landed
+      uint4* cur = stage + (b % 3) * kSt * E16;
+      // batch b + 2 goes into the buffer batch b - 1 was stored from; then this lane's copies of batch b have landed
+      if (c0 + 2 * kSt < c_hi) {
+        load(c0 + 2 * kSt, stage + ((b + 2) % 3) * kSt * E16);
+        cp_async_wait_two();
+      } else if (c0 + kSt < c_hi) {
+        cp_async_wait_one();
       } else {
         cp_async_wait_all();
       }
