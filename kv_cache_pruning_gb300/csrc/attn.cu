@@ -1706,6 +1706,11 @@ struct QuantTier {
 #define KVP_TWO_TIER_MMA_FROM 1
 #endif
 constexpr int kTwoTierMmaFrom = KVP_TWO_TIER_MMA_FROM;
+// One-tier calls from this many query heads per kv head on go to the tensor-core kernel.
+#ifndef KVP_ONE_TIER_MMA_FROM
+#define KVP_ONE_TIER_MMA_FROM 4
+#endif
+constexpr int kOneTierMmaFrom = KVP_ONE_TIER_MMA_FROM;
 
 kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_dim, const void* q, const void* k_pool,
                             const void* v_pool, const int32_t* expire_pool, int n_pages_cap,
@@ -1782,11 +1787,13 @@ kvp_status decode_attn_impl(int batch, int n_q_heads, int n_kv_heads, int head_d
   // where the tensor-core kernel reads a fp8 page's codes in place (Llama-3-8B
   // cache at G = 4, a quarter / half / three quarters of the entries in the
   // fp8 tier: 43.0 / 55.3 / 68.5 against 64.6 / 91.0 / 116.8 us; a 65B-shaped
-  // MHA layer at G = 1: 249 / 347 / 458 against 301 / 446 / 588 us). One-tier
-  // calls up to four stay on the CUDA-core kernel, as fast or faster there
-  // (75 % pruned at G = 4: 34.1 against 34.5 us). The tensor-core kernel reads
-  // the pools through tensor maps, whose row coordinates stay below 2^31.
-  const bool mma = (G == 8 || (qt != nullptr && G >= kTwoTierMmaFrom)) && n_pages_cap > 0 &&
+  // MHA layer at G = 1: 249 / 347 / 458 against 301 / 446 / 588 us). And
+  // one-tier calls from four on (the same cache at G = 4, kept whole / 75 /
+  // 87.5 / 96.9 % pruned: 89.4 / 31.9 / 17.1 / 12.4 against 90.9 / 33.2 /
+  // 22.8 / 14.8 us); below four the CUDA-core kernel is at the HBM rate kept
+  // whole. The tensor-core kernel reads the pools through tensor maps, whose
+  // row coordinates stay below 2^31.
+  const bool mma = (G >= kOneTierMmaFrom || (qt != nullptr && G >= kTwoTierMmaFrom)) && n_pages_cap > 0 &&
                    static_cast<int64_t>(n_pages_cap) * kPage <= 0x7fffffff;
   if (qt != nullptr) {
     if (mma)
