@@ -443,10 +443,10 @@ KVP_API kvp_status kvp_append_devpos(int mode, int batch, int n_kv_heads, int he
  * The pages of all (b, h) are split evenly over the warps of a persistent
  * grid (split-KV along pages, whatever the per-head survivor counts); partial
  * softmax states of a (b, h) that spans several warps are merged in fp32 by
- * the last of them to finish. Up to 4 query heads per kv head the page math
- * runs on the CUDA cores in fp32; at 8 it runs on the tensor cores (bf16
- * products with fp32 accumulation, the softmax weights entering the P.V
- * product as a bf16 hi + lo pair, about 16 bits each).
+ * the last of them to finish. At 1 and 2 query heads per kv head the page
+ * math runs on the CUDA cores in fp32; at 4 and 8 it runs on the tensor
+ * cores (bf16 products with fp32 accumulation, the softmax weights entering
+ * the P.V product as a bf16 hi + lo pair, about 16 bits each).
  *
  * q          device bf16 [B, Hq, head_dim];  Hq a multiple of H, Hq/H in {1,2,4,8},
  *            B*H <= 4096
